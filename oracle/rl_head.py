@@ -1,0 +1,316 @@
+"""fp64 oracle of the fused LM head + unified RL loss (forward, backward, metrics).
+
+TEST INFRASTRUCTURE: see the package docstring.  Written from prime-rl pull request
+#4233 (the loss_t equation; the estimator rules for u; "What changes"), with the mask
+sense from "IPO (INTELLECT Policy Optimization)", "Masking by Probability, Not Ratio".
+
+Per RL token t (loss_mask = 1), with z_t = W h_t / T:
+
+  log p_t(v)    = z_tv - logsumexp_v' z_tv'                    (full-vocab trainer p)
+  log P_t(v)    = z_tv - logsumexp_{v' in S_t} z_tv'  if replayed, else log p_t(v)  (READING R1)
+  u_e           = q_e (= exp logq_e) on a replayed support, 1/K_t on K i.i.d. draws
+  r             = P / q,   w = ipo:     1(|P - q| <= eps) * min(r, max_importance_ratio)
+                               icepop:  1(low <= r <= high) * r
+                               reinforce: 1
+  loss_t        = -adv_tau * A_t * (w_a log P(a) - sum_e sg[u_e w_e] log P(v_e)) + beta_t KL_t
+  KL_t          = exact: sum_e u_e (log q_e - log P(v_e));  k1: log q(a) - log P(a)  (READING R5)
+  beta_t        = kl_coeff * (1 or 1/sqrt(1 + age_t))                               (READING R6)
+
+w and u are held constant in the gradient (the sg[] of the equation; READING R4).
+Nothing here is blocked, fused or reordered beyond "one token row at a time".
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+LOSS_IPO, LOSS_ICEPOP, LOSS_REINFORCE = 0, 1, 2
+KL_EXACT, KL_K1 = 0, 1
+STALE_NONE, STALE_INV_SQRT = 0, 1
+
+
+@dataclasses.dataclass
+class HeadParams:
+    """Knobs of the unified loss (pull request #4233, "What changes")."""
+    loss_type: int = LOSS_IPO
+    eps: float = 0.3                   # ipo band half-width in probability
+    max_importance_ratio: float = 10.0  # ipo ratio cap
+    icepop_low: float = 0.5
+    icepop_high: float = 2.0
+    adv_tau: float = 1.0
+    temperature: float = 1.0
+    kl_coeff: float = 0.0
+    kl_estimator: int = KL_EXACT
+    kl_staleness: int = STALE_NONE
+
+
+def _logsumexp(x: np.ndarray) -> float:
+    m = float(np.max(x))
+    return m + math.log(float(np.sum(np.exp(x - m))))
+
+
+def rl_weight(logP: np.ndarray, logq: np.ndarray, p: HeadParams):
+    """Per-token importance weight w and keep bit for each (P, q) pair.
+
+    ipo:       1(|P - q| <= eps) * min(P/q, max_importance_ratio)
+    icepop:    1(low <= P/q <= high) * P/q
+    reinforce: 1
+    (pull request #4233, "What changes", first item; the probability-difference mask is
+    the one of "Masking by Probability, Not Ratio").  Threshold equality keeps the
+    token (READING R15).  Returns (w, keep, low_side, high_side), where the sides say
+    on which side of the band a masked token fell (P below / above q's band).
+    """
+    logP = np.asarray(logP, dtype=np.float64)
+    logq = np.asarray(logq, dtype=np.float64)
+    ratio = np.exp(logP - logq)
+    if p.loss_type == LOSS_IPO:
+        diff = np.exp(logP) - np.exp(logq)
+        keep = np.abs(diff) <= p.eps
+        w = np.where(keep, np.minimum(ratio, p.max_importance_ratio), 0.0)
+        low = ~keep & (diff < 0)
+        high = ~keep & (diff > 0)
+    elif p.loss_type == LOSS_ICEPOP:
+        keep = (ratio >= p.icepop_low) & (ratio <= p.icepop_high)
+        w = np.where(keep, ratio, 0.0)
+        low = ratio < p.icepop_low
+        high = ratio > p.icepop_high
+    elif p.loss_type == LOSS_REINFORCE:
+        keep = np.ones_like(ratio, dtype=bool)
+        w = np.ones_like(ratio)
+        low = np.zeros_like(keep)
+        high = np.zeros_like(keep)
+    else:
+        raise ValueError(f"unknown loss type {p.loss_type}")
+    return w, keep, low, high
+
+
+def kl_beta(age: int, p: HeadParams) -> float:
+    """beta_t = kl_coeff * s(age_t): s = 1 (none) or 1/sqrt(1 + age) (inv_sqrt, READING R6)."""
+    if p.kl_staleness == STALE_NONE:
+        return float(p.kl_coeff)
+    if p.kl_staleness == STALE_INV_SQRT:
+        return float(p.kl_coeff) / math.sqrt(1.0 + float(age))
+    raise ValueError(f"unknown staleness {p.kl_staleness}")
+
+
+def token_forward(z: np.ndarray, label: int, label_logq: float, adv: float, age: int,
+                  ids: np.ndarray, logq: np.ndarray, replayed: bool, p: HeadParams,
+                  w_frozen=None) -> dict:
+    """Loss and diagnostics of one RL token from its fp64 logits row z (already / T).
+
+    ``w_frozen = (w_label, w_entries)`` overrides the weights (finite-difference checks
+    hold w constant, as the sg[] in the loss says).
+    """
+    z = np.asarray(z, dtype=np.float64)
+    ids = np.asarray(ids, dtype=np.int64)
+    logq = np.asarray(logq, dtype=np.float64)
+    lse = _logsumexp(z)
+    logp_full = z - lse
+    pf = np.exp(logp_full)
+    entropy = float(-np.sum(pf * logp_full))
+    K = ids.shape[0]
+    if replayed:
+        lse_s = _logsumexp(z[ids])            # READING R1: renormalised over S
+        logP_lab = float(z[label] - lse_s)
+        logP_ent = z[ids] - lse_s
+        u = np.exp(logq)                      # u_v = q_v on a replayed support
+    else:
+        lse_s = lse
+        logP_lab = float(logp_full[label])
+        logP_ent = logp_full[ids]
+        u = np.full(K, 1.0 / K) if K > 0 else np.zeros(0)   # u = 1/K for K i.i.d. draws
+    w_lab, keep_lab, low_lab, high_lab = rl_weight(np.array([logP_lab]), np.array([label_logq]), p)
+    w_lab, keep_lab = float(w_lab[0]), bool(keep_lab[0])
+    w_ent, keep_ent, _, _ = rl_weight(logP_ent, logq, p)
+    if w_frozen is not None:
+        w_lab = float(w_frozen[0])
+        w_ent = np.asarray(w_frozen[1], dtype=np.float64)
+    c = u * w_ent                              # sg[u_v * w_v]
+    center = float(np.sum(c * logP_ent))
+    if p.kl_estimator == KL_EXACT:
+        kl = float(np.sum(u * (logq - logP_ent)))
+    elif p.kl_estimator == KL_K1:
+        kl = float(label_logq - logP_lab)
+    else:
+        raise ValueError(f"unknown kl estimator {p.kl_estimator}")
+    beta = kl_beta(age, p)
+    loss = -p.adv_tau * adv * (w_lab * logP_lab - center) + beta * kl
+    ratio_ent = np.exp(logP_ent - logq)
+    return dict(
+        loss=loss, lse=lse, lse_s=lse_s, entropy=entropy, logp_label=logP_lab,
+        logp_support=logP_ent, w_label=w_lab, keep_label=keep_lab, low_label=bool(low_lab[0]),
+        high_label=bool(high_lab[0]), w_support=w_ent, keep_support=keep_ent, u=u, c=c,
+        center=center, kl=kl, beta=beta,
+        # metrics (pull request #4233 "What changes", metrics item; READINGS R7-R9)
+        mismatch_kl=float(label_logq - logP_lab),
+        support_mass=float(np.sum(u * np.exp(logp_full[ids] - logq))),
+        mask_tv=float(np.sum(u * (~keep_ent) * ratio_ent)),
+    )
+
+
+def token_grad_z(z: np.ndarray, label: int, adv: float, ids: np.ndarray, replayed: bool,
+                 fwd: dict, p: HeadParams) -> np.ndarray:
+    """d loss_t / d z_t over the whole vocabulary, with w, c, u held constant.
+
+    d log P(v) / d z_j = delta_vj - P_j, where P is the full softmax of z, or for a
+    replayed token the softmax restricted to S (zero off S).  The sum over entries uses
+    np.add.at so duplicate draw ids each contribute.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    ids = np.asarray(ids, dtype=np.int64)
+    V = z.shape[0]
+    if replayed:
+        P = np.zeros(V)
+        P[ids] = np.exp(z[ids] - fwd["lse_s"])
+    else:
+        P = np.exp(z - fwd["lse"])
+
+    def dlogP(v):
+        g = -P.copy()
+        g[v] += 1.0
+        return g
+
+    # sum_e c_e d log P(v_e) = sum_e c_e onehot(v_e) - (sum_e c_e) P
+    sum_c_onehot = np.zeros(V)
+    np.add.at(sum_c_onehot, ids, fwd["c"])
+    d_center = sum_c_onehot - float(np.sum(fwd["c"])) * P
+    grad = -p.adv_tau * adv * (fwd["w_label"] * dlogP(label) - d_center)
+    if fwd["beta"] != 0.0:
+        if p.kl_estimator == KL_EXACT:
+            sum_u_onehot = np.zeros(V)
+            np.add.at(sum_u_onehot, ids, fwd["u"])
+            d_kl = -(sum_u_onehot - float(np.sum(fwd["u"])) * P)
+        else:
+            d_kl = -dlogP(label)
+        grad = grad + fwd["beta"] * d_kl
+    return grad
+
+
+def _rows(inputs: dict):
+    off = np.asarray(inputs["offsets"], dtype=np.int64)
+    return off
+
+
+def head_token_logits(inputs: dict, rows, temperature: float) -> np.ndarray:
+    """z = hidden[rows] @ W^T / T in fp64 (a library matmul as one step)."""
+    X = np.asarray(inputs["hidden"], dtype=np.float64)[rows]
+    W = np.asarray(inputs["W"], dtype=np.float64)
+    return (X @ W.T) / temperature
+
+
+def head_forward(inputs: dict, p: HeadParams, rows=None, chunk: int = 64) -> dict:
+    """Forward over tokens ``rows`` (default: all).  ``inputs`` holds numpy arrays:
+    hidden [N,H], W [V,H] (fp64 copies of the bf16 values), labels, label_logq, adv,
+    loss_mask, age, replayed, offsets [N+1], ids, logq.
+
+    Returns per-token arrays (indexed like ``rows``), per-entry arrays (in the entries
+    of those rows, concatenated in row order) and metric sums over the RL tokens.
+    """
+    off = _rows(inputs)
+    N = off.shape[0] - 1
+    rows = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
+    n = rows.shape[0]
+    out = {k: np.zeros(n) for k in ("loss", "lse", "lse_s", "entropy", "logp_label", "w_label",
+                                    "kl", "beta", "center")}
+    out["mask_label"] = np.zeros(n, dtype=np.uint8)
+    ent_lp, ent_mask, ent_w, ent_c, ent_u = [], [], [], [], []
+    met = dict(n_rl=0, mismatch_kl=0.0, masked=0, masked_low=0, masked_high=0, support_mass=0.0,
+               mask_tv=0.0, kl=0.0, beta=0.0, kl_age0=0.0, n_age0=0, entropy=0.0)
+    for c0 in range(0, n, chunk):
+        rr = rows[c0:c0 + chunk]
+        Z = head_token_logits(inputs, rr, p.temperature)
+        for j, t in enumerate(rr):
+            i = c0 + j
+            s, e = int(off[t]), int(off[t + 1])
+            fw = token_forward(Z[j], int(inputs["labels"][t]), float(inputs["label_logq"][t]),
+                               float(inputs["adv"][t]), int(inputs["age"][t]),
+                               inputs["ids"][s:e], inputs["logq"][s:e],
+                               bool(inputs["replayed"][t]), p)
+            rl = bool(inputs["loss_mask"][t])
+            out["loss"][i] = fw["loss"] if rl else 0.0
+            for k in ("lse", "lse_s", "entropy", "logp_label", "w_label", "kl", "beta", "center"):
+                out[k][i] = fw[k]
+            out["mask_label"][i] = 1 if fw["keep_label"] else 0
+            ent_lp.append(fw["logp_support"])
+            ent_mask.append(fw["keep_support"].astype(np.uint8))
+            ent_w.append(fw["w_support"])
+            ent_c.append(fw["c"])
+            ent_u.append(fw["u"])
+            if rl:
+                met["n_rl"] += 1
+                met["mismatch_kl"] += fw["mismatch_kl"]
+                met["masked"] += 0 if fw["keep_label"] else 1
+                met["masked_low"] += int(fw["low_label"])
+                met["masked_high"] += int(fw["high_label"])
+                met["support_mass"] += fw["support_mass"]
+                met["mask_tv"] += fw["mask_tv"]
+                met["kl"] += fw["kl"]
+                met["beta"] += fw["beta"]
+                met["entropy"] += fw["entropy"]
+                if int(inputs["age"][t]) == 0:
+                    met["kl_age0"] += fw["kl"]
+                    met["n_age0"] += 1
+    cat = lambda xs, dt=np.float64: np.concatenate(xs).astype(dt) if xs else np.zeros(0, dt)
+    out["logp_support"] = cat(ent_lp)
+    out["mask_support"] = cat(ent_mask, np.uint8)
+    out["w_support"] = cat(ent_w)
+    out["c_support"] = cat(ent_c)
+    out["u_support"] = cat(ent_u)
+    out["metrics"] = met
+    return out
+
+
+def head_backward(inputs: dict, p: HeadParams, dloss: np.ndarray, chunk: int = 64,
+                  rows=None, want_dW: bool = True):
+    """dX [N,H] and dW [V,H] of sum_t dloss_t * loss_t, fp64, by the chain rule:
+    G_tj = dloss_t / T * d loss_t / d z_tj;  dX = G W;  dW = G^T X.
+
+    ``rows`` restricts dX to those tokens (dW then sums over those tokens only).
+    """
+    off = _rows(inputs)
+    N = off.shape[0] - 1
+    rows = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
+    W = np.asarray(inputs["W"], dtype=np.float64)
+    Xall = np.asarray(inputs["hidden"], dtype=np.float64)
+    V, H = W.shape
+    dX = np.zeros((rows.shape[0], H))
+    dW = np.zeros((V, H)) if want_dW else None
+    for c0 in range(0, rows.shape[0], chunk):
+        rr = rows[c0:c0 + chunk]
+        Z = head_token_logits(inputs, rr, p.temperature)
+        G = np.zeros_like(Z)
+        for j, t in enumerate(rr):
+            if not inputs["loss_mask"][t] or dloss[t] == 0.0:
+                continue
+            s, e = int(off[t]), int(off[t + 1])
+            ids = inputs["ids"][s:e]
+            fw = token_forward(Z[j], int(inputs["labels"][t]), float(inputs["label_logq"][t]),
+                               float(inputs["adv"][t]), int(inputs["age"][t]), ids,
+                               inputs["logq"][s:e], bool(inputs["replayed"][t]), p)
+            G[j] = (float(dloss[t]) / p.temperature) * token_grad_z(
+                Z[j], int(inputs["labels"][t]), float(inputs["adv"][t]), ids,
+                bool(inputs["replayed"][t]), fw, p)
+        dX[c0:c0 + rr.shape[0]] = G @ W
+        if want_dW:
+            dW += G.T @ Xall[rr]
+    return dX, dW
+
+
+def head_loss_total(inputs: dict, p: HeadParams, dloss: np.ndarray, frozen=None) -> float:
+    """sum_t dloss_t * loss_t over RL tokens; ``frozen`` maps t -> (w_label, w_entries)."""
+    off = _rows(inputs)
+    N = off.shape[0] - 1
+    Z = head_token_logits(inputs, np.arange(N), p.temperature)
+    tot = 0.0
+    for t in range(N):
+        if not inputs["loss_mask"][t]:
+            continue
+        s, e = int(off[t]), int(off[t + 1])
+        fw = token_forward(Z[t], int(inputs["labels"][t]), float(inputs["label_logq"][t]),
+                           float(inputs["adv"][t]), int(inputs["age"][t]), inputs["ids"][s:e],
+                           inputs["logq"][s:e], bool(inputs["replayed"][t]), p,
+                           w_frozen=None if frozen is None else frozen[t])
+        tot += float(dloss[t]) * fw["loss"]
+    return tot

@@ -1,0 +1,397 @@
+"""Pins of the fp64 head oracle against what the pages and the mathematics fix.
+
+Each test names the fact it pins.  None of them re-types the oracle's own formula:
+they use worked examples from the pages (tests/golden/), closed forms (softmax
+cross-entropy gradient, KL, entropy through scipy), brute-force enumeration on tiny
+vocabularies, CLT bounds for the K-draw estimator, and central finite differences.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import scipy.stats
+
+import oracle
+from oracle import HeadParams, LOSS_IPO, LOSS_ICEPOP, LOSS_REINFORCE, KL_EXACT, KL_K1
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    rows = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = line.split()
+            rows[parts[0]] = parts[1:]
+    return rows
+
+
+def identity_case(z_rows, labels, label_logq, supports, replayed, adv=None, age=None,
+                  loss_mask=None):
+    """Inputs with W = I (H = V) so hidden rows are the logits and dX is dloss/dz."""
+    z_rows = np.asarray(z_rows, dtype=np.float64)
+    N, V = z_rows.shape
+    offsets = np.zeros(N + 1, dtype=np.int64)
+    ids, logq = [], []
+    for t, (i, lq) in enumerate(supports):
+        ids.extend(i)
+        logq.extend(lq)
+        offsets[t + 1] = offsets[t] + len(i)
+    return dict(hidden=z_rows, W=np.eye(V), labels=np.asarray(labels, dtype=np.int64),
+                label_logq=np.asarray(label_logq, dtype=np.float64),
+                adv=np.ones(N) if adv is None else np.asarray(adv, dtype=np.float64),
+                loss_mask=np.ones(N, dtype=np.uint8) if loss_mask is None else np.asarray(loss_mask),
+                age=np.zeros(N, dtype=np.int64) if age is None else np.asarray(age),
+                replayed=np.asarray(replayed, dtype=np.uint8), offsets=offsets,
+                ids=np.asarray(ids, dtype=np.int64), logq=np.asarray(logq, dtype=np.float64))
+
+
+# --------------------------------------------------------------------------------------
+# "IPO (INTELLECT Policy Optimization)", "Masking by Probability, Not Ratio"
+# --------------------------------------------------------------------------------------
+def _two_outcome_mask(pi_infer, pi_train, p):
+    """Vocabulary of two outcomes {token, rest}; trainer logits give pi_train."""
+    z = np.log([[pi_train, 1.0 - pi_train]])
+    inp = identity_case(z, [0], [math.log(pi_infer)],
+                        [([1], [math.log(1.0 - pi_infer)])], [0])
+    out = oracle.head_forward(inp, p)
+    return int(out["mask_label"][0]), out
+
+
+def test_two_outcome_examples_from_page():
+    g = _golden("two_outcome_examples.txt")
+    rare = [float(x) for x in g["rare_token"]]
+    likely = [float(x) for x in g["likely_token"]]
+    eps = float(_golden("default_constants.txt")["ipo_eps"][0])
+    ipo = HeadParams(loss_type=LOSS_IPO, eps=eps)
+    # IPO eps=0.3 keeps the rare token (moved 0.05) and masks the likely one (moved 0.70)
+    assert _two_outcome_mask(rare[0], rare[1], ipo)[0] == 1
+    assert _two_outcome_mask(likely[0], likely[1], ipo)[0] == 0
+    # the printed ratios and moved masses
+    assert round(rare[1] / rare[0]) == rare[2]
+    assert round(likely[1] / likely[0], 2) == likely[2]
+    assert abs(abs(rare[1] - rare[0]) - rare[3]) < 1e-12
+    assert abs(abs(likely[1] - likely[0]) - likely[3]) < 1e-12
+    # a ratio band with beta < 6 masks the rare token, the configs' [0.5, 2] included
+    for beta in (2.0, 3.0, 5.9):
+        icepop = HeadParams(loss_type=LOSS_ICEPOP, icepop_low=0.5, icepop_high=beta)
+        m, out = _two_outcome_mask(rare[0], rare[1], icepop)
+        assert m == 0
+        assert out["metrics"]["masked_high"] == 1
+    # the page's "IcePop keeps it" for 0.90 -> 0.20 needs alpha <= 0.222 (reading R16)
+    wide = HeadParams(loss_type=LOSS_ICEPOP, icepop_low=0.2, icepop_high=5.0)
+    assert _two_outcome_mask(likely[0], likely[1], wide)[0] == 1
+    narrow = HeadParams(loss_type=LOSS_ICEPOP, icepop_low=0.5, icepop_high=2.0)
+    m, out = _two_outcome_mask(likely[0], likely[1], narrow)
+    assert m == 0 and out["metrics"]["masked_low"] == 1
+
+
+@pytest.mark.parametrize("pi_infer,pi_train", [(0.01, 0.06), (0.9, 0.2), (0.4, 0.7), (0.3, 0.3)])
+def test_ipo_mask_is_two_outcome_total_variation(pi_infer, pi_train):
+    """|pi_train - pi_infer| is the TV distance on the split {token, rest}."""
+    tv = 0.5 * (abs(pi_train - pi_infer) + abs((1 - pi_train) - (1 - pi_infer)))
+    for eps in (0.05, 0.2, 0.3, 0.5):
+        m, _ = _two_outcome_mask(pi_infer, pi_train, HeadParams(loss_type=LOSS_IPO, eps=eps))
+        assert m == (1 if tv <= eps + 1e-12 else 0)
+
+
+def test_default_constants():
+    d = _golden("default_constants.txt")
+    hp = HeadParams()
+    pp = oracle.PolicyParams()
+    assert hp.eps == float(d["ipo_eps"][0])
+    assert hp.kl_coeff == float(d["kl_coeff"][0])
+    assert pp.clip_ratio_low == float(d["clip_ratio_low"][0])
+    assert pp.clip_ratio_high == float(d["clip_ratio_high"][0])
+    assert pp.clip_ratio_c == float(d["clip_ratio_c"][0])
+
+
+# --------------------------------------------------------------------------------------
+# Textbook special cases
+# --------------------------------------------------------------------------------------
+def _softmax(z):
+    return scipy.special.softmax(np.asarray(z, dtype=np.float64))
+
+
+@pytest.mark.parametrize("loss_type", [LOSS_IPO, LOSS_ICEPOP, LOSS_REINFORCE])
+def test_q_equals_p_full_replay(loss_type):
+    """q = p, replay over the whole vocabulary: w = 1, nothing masked, no mismatch,
+    support mass 1, KL 0, and loss = -A (log p(a) + H(p))."""
+    rng = np.random.default_rng(1)
+    V = 16
+    z = rng.normal(0, 1.5, size=(3, V))
+    labels = [2, 7, 15]
+    adv = [0.7, -1.3, 2.0]
+    sup = []
+    lab_lq = []
+    for t in range(3):
+        p = _softmax(z[t])
+        sup.append((list(range(V)), list(np.log(p))))
+        lab_lq.append(math.log(p[labels[t]]))
+    inp = identity_case(z, labels, lab_lq, sup, [1, 1, 1], adv=adv)
+    hp = HeadParams(loss_type=loss_type, kl_coeff=0.3, kl_estimator=KL_EXACT)
+    out = oracle.head_forward(inp, hp)
+    met = out["metrics"]
+    assert met["masked"] == 0 and abs(met["mismatch_kl"]) < 1e-12
+    assert abs(met["support_mass"] - 3.0) < 1e-12
+    assert abs(met["kl"]) < 1e-12 and abs(met["mask_tv"]) < 1e-12
+    assert np.all(out["mask_support"] == 1)
+    for t in range(3):
+        p = _softmax(z[t])
+        expect = -adv[t] * (math.log(p[labels[t]]) + scipy.stats.entropy(p))
+        assert abs(out["loss"][t] - expect) < 1e-12
+        assert abs(out["entropy"][t] - scipy.stats.entropy(p)) < 1e-12
+
+
+def test_reinforce_full_replay_gradient_is_label_minus_q():
+    """reinforce, replay with S = V, u = q: d loss / d z = -adv_tau A (onehot(a) - q),
+    independent of the trainer's p."""
+    rng = np.random.default_rng(2)
+    V = 12
+    z = rng.normal(0, 1, size=(2, V))
+    qz = rng.normal(0, 1, size=(2, V))
+    labels = [3, 9]
+    adv = [1.5, -0.4]
+    sup, lab_lq = [], []
+    for t in range(2):
+        q = _softmax(qz[t])
+        sup.append((list(range(V)), list(np.log(q))))
+        lab_lq.append(math.log(q[labels[t]]))
+    inp = identity_case(z, labels, lab_lq, sup, [1, 1], adv=adv)
+    hp = HeadParams(loss_type=LOSS_REINFORCE, adv_tau=0.8)
+    dX, dW = oracle.head_backward(inp, hp, np.ones(2))
+    for t in range(2):
+        q = _softmax(qz[t])
+        onehot = np.eye(V)[labels[t]]
+        np.testing.assert_allclose(dX[t], -0.8 * adv[t] * (onehot - q), atol=1e-13)
+
+
+@pytest.mark.parametrize("estimator", [KL_EXACT, KL_K1])
+def test_kl_full_replay_matches_dense_kl_and_xent_gradient(estimator):
+    """Exact KL over S = V is KL(q||p) and its gradient is p - q (the softmax
+    cross-entropy gradient); k1 is log q(a) - log p(a) with gradient p - onehot(a)."""
+    rng = np.random.default_rng(3)
+    V = 10
+    z = rng.normal(0, 1, size=(2, V))
+    qz = rng.normal(0, 1, size=(2, V))
+    labels = [1, 6]
+    sup, lab_lq = [], []
+    for t in range(2):
+        q = _softmax(qz[t])
+        sup.append((list(range(V)), list(np.log(q))))
+        lab_lq.append(math.log(q[labels[t]]))
+    inp = identity_case(z, labels, lab_lq, sup, [1, 1], adv=[0.0, 0.0])
+    beta = 0.25
+    hp = HeadParams(loss_type=LOSS_IPO, kl_coeff=beta, kl_estimator=estimator)
+    out = oracle.head_forward(inp, hp)
+    dX, _ = oracle.head_backward(inp, hp, np.ones(2))
+    for t in range(2):
+        p, q = _softmax(z[t]), _softmax(qz[t])
+        if estimator == KL_EXACT:
+            assert abs(out["kl"][t] - scipy.stats.entropy(q, p)) < 1e-12
+            np.testing.assert_allclose(dX[t], beta * (p - q), atol=1e-13)
+        else:
+            assert abs(out["kl"][t] - (math.log(q[labels[t]]) - math.log(p[labels[t]]))) < 1e-12
+            np.testing.assert_allclose(dX[t], beta * (p - np.eye(V)[labels[t]]), atol=1e-13)
+        assert abs(out["loss"][t] - beta * out["kl"][t]) < 1e-14
+
+
+def test_gradient_lies_on_label_and_support_when_sparse_eligible():
+    """reinforce without KL on K draws, and any loss on a replayed support: the logit
+    gradient is zero off label + support (pull request #4233, sparse LM-head backward)."""
+    rng = np.random.default_rng(4)
+    V, K = 40, 6
+    z = rng.normal(0, 1, size=(2, V))
+    q0 = _softmax(z[0] + rng.normal(0, 0.3, V))
+    draws = sorted(rng.choice(V, size=K, replace=True, p=q0))
+    S = sorted(rng.choice(V, size=9, replace=False))
+    qS = _softmax(z[1, S] + rng.normal(0, 0.3, len(S)))
+    lab1 = S[4]
+    inp = identity_case(z, [5, lab1], [math.log(q0[5]), math.log(qS[4])],
+                        [(draws, list(np.log(q0[draws]))), (S, list(np.log(qS)))], [0, 1],
+                        adv=[1.2, -0.7])
+    for hp in (HeadParams(loss_type=LOSS_REINFORCE),):
+        dX, _ = oracle.head_backward(inp, hp, np.ones(2))
+        off0 = np.setdiff1d(np.arange(V), np.r_[draws, 5])
+        assert np.max(np.abs(dX[0, off0])) < 1e-15
+    for hp in (HeadParams(loss_type=LOSS_IPO, kl_coeff=0.1), HeadParams(loss_type=LOSS_ICEPOP)):
+        dX, _ = oracle.head_backward(inp, hp, np.ones(2))
+        off1 = np.setdiff1d(np.arange(V), S)
+        assert np.max(np.abs(dX[1, off1])) == 0.0
+        # not eligible on the untruncated row: the dense softmax term is there
+        assert np.min(np.abs(dX[0])) > 0.0 or hp.loss_type == LOSS_REINFORCE
+
+
+# --------------------------------------------------------------------------------------
+# Brute force on tiny vocabularies
+# --------------------------------------------------------------------------------------
+def _keep_w(P, q, hp):
+    """Independent restatement of the three weights for enumerated (P, q) pairs."""
+    if hp.loss_type == LOSS_REINFORCE:
+        return 1.0
+    r = P / q
+    if hp.loss_type == LOSS_IPO:
+        return min(r, hp.max_importance_ratio) if abs(P - q) <= hp.eps else 0.0
+    return r if hp.icepop_low <= r <= hp.icepop_high else 0.0
+
+
+@pytest.mark.parametrize("loss_type", [LOSS_IPO, LOSS_ICEPOP, LOSS_REINFORCE])
+def test_exact_centering_equals_dense_expectation(loss_type):
+    """Replayed support: sum_v u_v w_v log P_v equals E_q[w log P] enumerated over the
+    whole vocabulary with q = 0 off S (pull request #4233: truncated sampling, u = q,
+    centering is exact)."""
+    rng = np.random.default_rng(5)
+    V = 24
+    z = rng.normal(0, 2.0, size=V)
+    S = sorted(rng.choice(V, size=7, replace=False))
+    qS = _softmax(z[S] + rng.normal(0, 0.8, len(S)))
+    q_dense = np.zeros(V)
+    q_dense[S] = qS
+    P_dense = np.zeros(V)
+    P_dense[S] = _softmax(z[S])
+    hp = HeadParams(loss_type=loss_type, eps=0.1, max_importance_ratio=1.5, icepop_low=0.7,
+                    icepop_high=1.4)
+    expect = 0.0
+    for v in range(V):
+        if q_dense[v] > 0:
+            expect += q_dense[v] * _keep_w(P_dense[v], q_dense[v], hp) * math.log(P_dense[v])
+    inp = identity_case(z[None], [S[0]], [math.log(qS[0])], [(S, list(np.log(qS)))], [1])
+    out = oracle.head_forward(inp, hp)
+    assert abs(out["center"][0] - expect) < 1e-12
+    if loss_type == LOSS_REINFORCE:
+        # E_q[log P] = -(H(q) + KL(q||P)), through scipy
+        alt = -(scipy.stats.entropy(qS) + scipy.stats.entropy(qS, P_dense[S]))
+        assert abs(out["center"][0] - alt) < 1e-12
+
+
+@pytest.mark.parametrize("K", [16, 256, 4096, 16384])
+def test_k_draw_estimator_converges_to_exact_centre(K):
+    """u = 1/K over K i.i.d. draws from q estimates E_q[w log p] and KL(q||p) within a
+    4 sigma / sqrt(K) CLT bound (pull request #4233, untruncated sampling)."""
+    rng = np.random.default_rng(1000 + K)
+    V = 32
+    z = rng.normal(0, 1.0, size=V)
+    q = _softmax(z + rng.normal(0, 0.4, V))
+    p = _softmax(z)
+    hp = HeadParams(loss_type=LOSS_IPO, eps=0.02, max_importance_ratio=1.3,
+                    kl_coeff=0.0, kl_estimator=KL_EXACT)
+    f = np.array([_keep_w(p[v], q[v], hp) * math.log(p[v]) for v in range(V)])
+    g = np.log(q) - np.log(p)
+    Ef, Eg = float(q @ f), float(scipy.stats.entropy(q, p))
+    sf = math.sqrt(float(q @ (f - Ef) ** 2))
+    sg = math.sqrt(float(q @ (g - Eg) ** 2))
+    draws = np.sort(rng.choice(V, size=K, replace=True, p=q))
+    inp = identity_case(z[None], [0], [math.log(q[0])], [(draws, list(np.log(q[draws])))], [0])
+    out = oracle.head_forward(inp, hp)
+    assert abs(out["center"][0] - Ef) <= 4 * sf / math.sqrt(K)
+    assert abs(out["kl"][0] - Eg) <= 4 * sg / math.sqrt(K)
+
+
+def test_support_mass_and_mismatch_kl_against_enumeration():
+    """support_mass = E_q[p/q] over the support with the full-vocab p (reading R8)
+    equals the trainer mass on S for a replayed support; mismatch KL at the label is
+    log q(a) - log P(a)."""
+    rng = np.random.default_rng(6)
+    V = 30
+    z = rng.normal(0, 1.0, size=V)
+    S = sorted(rng.choice(V, size=11, replace=False))
+    qS = _softmax(z[S] + rng.normal(0, 0.5, len(S)))
+    inp = identity_case(z[None], [S[2]], [math.log(qS[2])], [(S, list(np.log(qS)))], [1])
+    out = oracle.head_forward(inp, HeadParams(loss_type=LOSS_REINFORCE))
+    p = _softmax(z)
+    assert abs(out["metrics"]["support_mass"] - p[S].sum()) < 1e-12
+    PS = _softmax(z[S])
+    assert abs(out["metrics"]["mismatch_kl"] - (math.log(qS[2]) - math.log(PS[2]))) < 1e-12
+
+
+# --------------------------------------------------------------------------------------
+# Finite differences with w held constant (the sg[] of the loss)
+# --------------------------------------------------------------------------------------
+def _random_case(rng, N=6, H=5, V=9, mixed=True):
+    X = rng.normal(0, 1, size=(N, H))
+    W = rng.normal(0, 0.6, size=(V, H))
+    T = 0.7
+    z = X @ W.T / T
+    labels, lab_lq, sup, rep = [], [], [], []
+    for t in range(N):
+        q = _softmax(z[t] + rng.normal(0, 0.4, V))
+        if mixed and t % 2 == 1:
+            S = sorted(rng.choice(V, size=4, replace=False))
+            qS = q[S] / q[S].sum()
+            a = S[int(rng.integers(0, 4))]
+            labels.append(a)
+            lab_lq.append(math.log(qS[S.index(a)]))
+            sup.append((S, list(np.log(qS))))
+            rep.append(1)
+        else:
+            d = sorted(rng.choice(V, size=5, replace=True, p=q))
+            a = int(rng.integers(0, V))
+            labels.append(a)
+            lab_lq.append(math.log(q[a]))
+            sup.append((d, list(np.log(q[d]))))
+            rep.append(0)
+    inp = identity_case(np.zeros((N, V)), labels, lab_lq, sup, rep,
+                        adv=rng.normal(0, 1, N), age=rng.integers(0, 5, N))
+    inp["hidden"], inp["W"] = X, W
+    return inp, T
+
+
+@pytest.mark.parametrize("loss_type,est,stale", [
+    (LOSS_IPO, KL_EXACT, oracle.STALE_INV_SQRT),
+    (LOSS_ICEPOP, KL_K1, oracle.STALE_NONE),
+    (LOSS_REINFORCE, KL_EXACT, oracle.STALE_NONE),
+])
+def test_finite_differences(loss_type, est, stale):
+    rng = np.random.default_rng(7 + loss_type)
+    inp, T = _random_case(rng)
+    hp = HeadParams(loss_type=loss_type, eps=0.15, max_importance_ratio=1.4, icepop_low=0.8,
+                    icepop_high=1.25, adv_tau=0.9, temperature=T, kl_coeff=0.07,
+                    kl_estimator=est, kl_staleness=stale)
+    N = inp["hidden"].shape[0]
+    dloss = rng.normal(0, 1, N)
+    base = oracle.head_forward(inp, hp)
+    off = inp["offsets"]
+    frozen = {t: (base["w_label"][t], base["w_support"][off[t]:off[t + 1]]) for t in range(N)}
+    dX, dW = oracle.head_backward(inp, hp, dloss)
+    h = 1e-6
+    for name, grad in (("hidden", dX), ("W", dW)):
+        A = inp[name]
+        for idx in [(0, 0), (1, 3), (2, 4), (min(A.shape[0] - 1, 5), 2)]:
+            old = A[idx]
+            A[idx] = old + h
+            lp = oracle.head_loss_total(inp, hp, dloss, frozen)
+            A[idx] = old - h
+            lm = oracle.head_loss_total(inp, hp, dloss, frozen)
+            A[idx] = old
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - grad[idx]) <= 1e-7 * max(1.0, abs(grad[idx])), (name, idx, fd, grad[idx])
+
+
+def test_loss_mask_zero_tokens_have_no_loss_or_gradient():
+    rng = np.random.default_rng(8)
+    inp, T = _random_case(rng)
+    inp["loss_mask"] = np.array([1, 0, 1, 0, 1, 1], dtype=np.uint8)
+    hp = HeadParams(temperature=T, kl_coeff=0.1)
+    out = oracle.head_forward(inp, hp)
+    dX, _ = oracle.head_backward(inp, hp, np.ones(6))
+    assert out["loss"][1] == 0.0 and out["loss"][3] == 0.0
+    assert np.all(dX[1] == 0) and np.all(dX[3] == 0)
+    assert out["metrics"]["n_rl"] == 4
+
+
+def test_temperature_is_a_logit_scale():
+    """z = W h / T: doubling W and T leaves every forward output unchanged."""
+    rng = np.random.default_rng(9)
+    inp, T = _random_case(rng)
+    hp = HeadParams(temperature=T, kl_coeff=0.05)
+    a = oracle.head_forward(inp, hp)
+    inp2 = dict(inp)
+    inp2["W"] = 2.0 * inp["W"]
+    b = oracle.head_forward(inp2, HeadParams(temperature=2 * T, kl_coeff=0.05))
+    np.testing.assert_allclose(a["loss"], b["loss"], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(a["logp_support"], b["logp_support"], rtol=1e-12)
