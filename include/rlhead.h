@@ -1,0 +1,247 @@
+/*
+ * rlhead.h -- C ABI of the GB300 (sm_103a) fused LM head + unified RL loss library.
+ *
+ * The operation (prime-rl pull request #4233, the loss_t equation and "What changes"):
+ * for every RL token t with hidden row h_t, logits z_t = W h_t / T over the whole
+ * vocabulary, and a ragged sampler support S_t (CSR row: int32 ids, sampler log q),
+ *
+ *   loss_t = -adv_tau * A_t * ( w(a_t) log P_t(a_t) - sum_{e in S_t} sg[u_e w_e] log P_t(v_e) )
+ *            + beta_t * KL_t(q || P_t)
+ *
+ *   w:  ipo       1(|P - q| <= eps) * min(P/q, max_importance_ratio)
+ *       icepop    1(low <= P/q <= high) * P/q
+ *       reinforce 1
+ *   u:  q_e on a replayed (truncated top-p / top-k) support; 1/K on K i.i.d. sampler draws
+ *   P:  the trainer softmax at temperature T; on a replayed support the softmax
+ *       renormalised over S_t (the trainer distribution under the replayed truncation)
+ *   KL: exact = sum_e u_e (log q_e - log P(v_e));  k1 = log q(a) - log P(a)
+ *   beta_t = kl_coeff * (1, or 1/sqrt(1 + age_t) for inv_sqrt staleness)
+ *
+ * The [N, V] logits are never materialised: the forward streams vocabulary tiles through
+ * tcgen05 tensor-core tiles with an online logsumexp.  The backward is dense
+ * (softmax-gradient GEMMs for dX and dW) or sparse (a deterministic CSR matmul) when every
+ * logit gradient lies on the label and the support ("Sparse LM-head backward").
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" point to GPU global memory of the current CUDA device;
+ *     "host" pointers to CPU memory.  The caller allocates and owns every buffer,
+ *     including workspaces and the forward->backward saved state; the library never
+ *     allocates and never synchronises the host (except rl_status_read).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is enqueued
+ *     on it in order.
+ *   - Return value: RL_OK, or an RL_ERR_* code for errors visible on the host (bad
+ *     argument, workspace too small, unsupported shape, CUDA launch failure).  When an
+ *     error is returned nothing was enqueued, except for RL_ERR_CUDA.
+ *   - Data errors found on the device (a corrupt CSR, an out-of-range id, a wait that
+ *     ran out) are OR-ed into *dev_status as RL_STATUS_* bits; kernels never trap.
+ *     Read them with rl_status_read after the stream is synchronised ("checked once per
+ *     step before the optimizer", pull request #4233, GPU sampler-evidence validation).
+ *     The library never clears *dev_status; the caller zeroes it.
+ *   - Same inputs, same device => bitwise-identical outputs (no float atomics; fixed
+ *     reduction orders).
+ *   - Layouts are dense row-major; bf16 is IEEE bfloat16 (2 bytes).
+ */
+#ifndef RLHEAD_H
+#define RLHEAD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- host return codes ---------------------------------------------------------- */
+#define RL_OK               0
+#define RL_ERR_ARG          1   /* null pointer, negative size, bad enum or knob        */
+#define RL_ERR_WORKSPACE    2   /* ws_bytes smaller than the matching *_workspace_bytes */
+#define RL_ERR_UNSUPPORTED  3   /* H % 64 != 0, V % 8 != 0, or no sm_100-family device  */
+#define RL_ERR_CUDA         4   /* a CUDA call or kernel launch failed                   */
+
+/* ---- device status bits (OR-ed into *dev_status) -------------------------------- */
+#define RL_STATUS_OFFSETS            0x0001  /* offsets[0]!=0, decreasing, or offsets[N]!=nnz */
+#define RL_STATUS_ID_RANGE           0x0002  /* a support id or label outside [0, V)          */
+#define RL_STATUS_LOGQ               0x0004  /* a log q not finite or > 1e-6                  */
+#define RL_STATUS_LABEL_MISSING      0x0008  /* replayed row does not contain its label      */
+#define RL_STATUS_SUPPORT_MASS       0x0010  /* replayed row: |sum exp(log q) - 1| > 1e-3     */
+#define RL_STATUS_EMPTY_ROW          0x0020  /* an RL token with an empty support row        */
+#define RL_STATUS_ROW_ORDER          0x0040  /* ids not ascending (strictly, when replayed)  */
+#define RL_STATUS_SPARSE_INELIGIBLE  0x0080  /* sparse backward asked for, but a token's
+                                                gradient has a dense softmax part            */
+#define RL_STATUS_NONFINITE          0x0100  /* a non-finite loss or logsumexp               */
+#define RL_STATUS_TIMEOUT            0x0200  /* a kernel's bounded wait ran out; outputs invalid */
+
+/* ---- knobs ---------------------------------------------------------------------- */
+typedef enum { RL_LOSS_IPO = 0, RL_LOSS_ICEPOP = 1, RL_LOSS_REINFORCE = 2 } rl_loss_type;
+typedef enum { RL_KL_EXACT = 0, RL_KL_K1 = 1 } rl_kl_estimator;
+typedef enum { RL_STALE_NONE = 0, RL_STALE_INV_SQRT = 1 } rl_kl_staleness;
+/* AUTO = SPARSE when the knobs alone make every gradient lie on label + support
+ * (reinforce with kl_coeff == 0) or the caller asserts all_replayed; DENSE otherwise. */
+typedef enum { RL_BWD_AUTO = 0, RL_BWD_DENSE = 1, RL_BWD_SPARSE = 2 } rl_bwd_mode;
+/* Precision of the softmax-gradient operand G fed to the dX / dW tensor-core GEMMs:
+ * BF16 rounds G once to bf16; SPLIT feeds G as bf16 hi + bf16 lo (two GEMM passes),
+ * which carries ~16 significant bits. */
+typedef enum { RL_GRAD_BF16 = 0, RL_GRAD_SPLIT = 1 } rl_grad_precision;
+
+typedef struct rl_params {
+    int32_t loss_type;            /* rl_loss_type */
+    int32_t kl_estimator;         /* rl_kl_estimator */
+    int32_t kl_staleness;         /* rl_kl_staleness */
+    int32_t bwd_mode;             /* rl_bwd_mode */
+    int32_t grad_precision;       /* rl_grad_precision */
+    int32_t all_replayed;         /* caller's assertion that every row is replayed (AUTO) */
+    float eps;                    /* ipo band half-width in probability (>= 0); default 0.3 */
+    float max_importance_ratio;   /* ipo ratio cap (> 0); default 10 */
+    float icepop_low;             /* icepop band, 0 <= low <= high */
+    float icepop_high;
+    float adv_tau;                /* advantage scale */
+    float temperature;            /* T > 0; logits are (W h) / T */
+    float kl_coeff;               /* >= 0; default 0 */
+    int32_t token_chunk;          /* backward token chunk (multiple of 128); 0 = library default */
+} rl_params;
+
+/* Ragged per-token sampler support, CSR over tokens ("TokenSupport", pull request #4233,
+ * "What changes": int32 ids, int64 offsets, replayed flag, sampler logprobs).
+ * Row t holds entries [offsets[t], offsets[t+1]); ids ascending within a row (strictly
+ * ascending when replayed; repeated draws adjacent otherwise). */
+typedef struct rl_support {
+    const int64_t* offsets;   /* device [N+1] */
+    const int32_t* ids;       /* device [nnz] */
+    const float*   logq;      /* device [nnz] sampler log q of each entry (renormalised over
+                                 S on a replayed row) */
+    const uint8_t* replayed;  /* device [N]; 1 = truncated support replayed with u = q */
+    int64_t nnz;
+} rl_support;
+
+typedef struct rl_head_batch {
+    const void* hidden;       /* device [N, H] bf16 */
+    const void* weight;       /* device [V, H] bf16 (LM-head rows) */
+    int64_t N, H, V;
+    const int32_t* labels;    /* device [N] sampled token a_t */
+    const float* label_logq;  /* device [N] sampler log q(a_t) */
+    const float* adv;         /* device [N] advantage A_t */
+    const uint8_t* loss_mask; /* device [N] 1 = RL token; NULL = every token is an RL token */
+    const int32_t* age;       /* device [N] policy age for kl_staleness; NULL = all 0 */
+    rl_support support;
+} rl_head_batch;
+
+/* Metric sums over RL tokens (pull request #4233, metrics item: support_mass = E_q[p/q],
+ * mask_tv, kl, kl/beta, kl/age0; "IPO ...": mismatch_kl).  Divide by the counts on the
+ * host; sums compose across micro-batches. */
+typedef struct rl_head_metrics {
+    double loss;          /* sum_t loss_t */
+    double mismatch_kl;   /* sum_t (log q(a) - log P(a)) */
+    double support_mass;  /* sum_t sum_e u_e exp(log p_full(v_e) - log q_e) */
+    double mask_tv;       /* sum_t sum_e u_e (1 - m_e) P(v_e)/q_e */
+    double kl;            /* sum_t KL_t */
+    double beta;          /* sum_t beta_t */
+    double kl_age0;       /* sum of KL_t over age_t == 0 */
+    double entropy;       /* sum_t H(p_t) (full-vocab trainer entropy) */
+    int64_t n_rl;         /* RL tokens */
+    int64_t masked;       /* RL tokens whose label weight was masked */
+    int64_t masked_low;   /* ... with P below the band (ipo: P < q - eps; icepop: r < low) */
+    int64_t masked_high;  /* ... with P above the band */
+    int64_t n_age0;       /* RL tokens with age 0 */
+    int64_t reserved;
+} rl_head_metrics;
+
+typedef struct rl_head_outputs {
+    float*   loss;          /* device [N] per-token loss (0 for non-RL tokens); required */
+    float*   logp_label;    /* device [N] log P(a_t); NULL to skip */
+    float*   logp_support;  /* device [nnz] log P(v_e); NULL to skip */
+    float*   entropy;       /* device [N] full-vocab entropy of p_t; NULL to skip */
+    float*   lse;           /* device [N] logsumexp_v z_tv; NULL to skip */
+    uint8_t* mask_label;    /* device [N] keep bit of the label weight; NULL to skip */
+    uint8_t* mask_support;  /* device [nnz] keep bit of each entry weight; NULL to skip */
+    rl_head_metrics* metrics; /* device, one struct, overwritten; NULL to skip */
+} rl_head_outputs;
+
+/* Bytes of the caller-owned state the forward saves for the backward. */
+size_t rl_head_saved_bytes(int64_t N, int64_t nnz);
+/* Workspace bytes of rl_head_loss_fwd / rl_head_loss_bwd for these sizes and knobs. */
+size_t rl_head_fwd_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz,
+                                   const rl_params* params);
+size_t rl_head_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz,
+                                   const rl_params* params);
+
+/* Validate the CSR sampler evidence on the device (pull request #4233, GPU validation of
+ * the sampler evidence): sets RL_STATUS_OFFSETS / ID_RANGE / LOGQ / LABEL_MISSING /
+ * SUPPORT_MASS / EMPTY_ROW / ROW_ORDER bits.  rl_head_loss_fwd runs it first. */
+int rl_validate_support(const rl_head_batch* batch, int32_t* dev_status, void* stream);
+
+/* Forward: per-token loss, label / support log-probs, entropy, masks, metrics, and the
+ * saved state (`saved`, device, rl_head_saved_bytes) for the backward. */
+int rl_head_loss_fwd(const rl_head_batch* batch, const rl_params* params,
+                     const rl_head_outputs* out, void* saved, void* ws, size_t ws_bytes,
+                     int32_t* dev_status, void* stream);
+
+/* Backward of sum_t dloss[t] * loss_t.  dloss: device [N] fp32 (the caller's aggregation,
+ * e.g. 1 / #RL tokens for a token mean).  dhidden: device [N, H] bf16, overwritten.
+ * dW: device [V, H] fp32; accumulate_dW != 0 adds into it, else it is overwritten. */
+int rl_head_loss_bwd(const rl_head_batch* batch, const rl_params* params, const void* saved,
+                     const float* dloss, void* dhidden, float* dW, int accumulate_dW,
+                     void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* Reduce the per-token metric terms in `saved` (written by rl_head_loss_fwd for the same
+ * batch) into *metrics (device).  rl_head_loss_fwd calls it when out->metrics != NULL. */
+int rl_mismatch_metrics(const rl_head_batch* batch, const void* saved,
+                        rl_head_metrics* metrics, void* ws, size_t ws_bytes, void* stream);
+
+/* ---- elementwise PPO / decoupled-TIS / mismatch path --------------------------------
+ * "Rollout Correction Methods", "Algorithms" (standard, bypass and decoupled 3-policy PPO)
+ * and "Mismatch Metrics"; "10-KL-clip-entropy", section 2 (clip, dual clip, metrics);
+ * "IPO (INTELLECT Policy Optimization)", "Choosing eps" (masked fraction vs eps).
+ * Per token i with r = exp(lp_theta - lp_old):
+ *   l1 = -A r, l2 = -A clip(r, 1 - clip_ratio_low, 1 + clip_ratio_high), lc = max(l1, l2)
+ *   loss_ppo = A < 0 ? min(lc, -A clip_ratio_c) : lc          (dual clip)
+ *   loss_dec = min(exp(lp_old - lp_samp), tis_upper) * lc      (decoupled, TIS truncate)
+ *   grad_*   = d loss_* / d lp_theta
+ * Bypass PPO is the same call with lp_old := lp_samp. */
+#define RL_PG_MAX_CURVE 16
+typedef struct rl_pg_params {
+    float clip_ratio_low, clip_ratio_high, clip_ratio_c;  /* defaults 0.2, 0.2, 3.0 */
+    float tis_upper;                                      /* TIS truncation bound */
+    float icepop_low, icepop_high;                        /* ratio band for the IcePop count */
+    int32_t n_curve;                                      /* 0..RL_PG_MAX_CURVE */
+    float curve_eps[RL_PG_MAX_CURVE];                     /* IPO eps values */
+} rl_pg_params;
+
+typedef struct rl_pg_metrics {
+    double loss_ppo, loss_dec;   /* sums over valid tokens */
+    double ppo_kl;               /* sum (lp_old - lp_theta) */
+    double mis_kl;               /* sum (lp_samp - lp_old) */
+    double k3;                   /* sum (e^d - d - 1), d = lp_old - lp_samp */
+    double tis_sum;              /* sum of truncated TIS weights */
+    int64_t n_valid, n_clip, n_clip_lower, icepop_low, icepop_high, n_tis_trunc;
+    int64_t ipo_curve[RL_PG_MAX_CURVE];   /* count of |e^lp_old - e^lp_samp| > curve_eps[k] */
+} rl_pg_metrics;
+
+size_t rl_policy_workspace_bytes(int64_t T);
+/* All arrays device [T] fp32 (mask uint8, 1 = valid response token).  Output arrays may
+ * be NULL to skip; masked tokens get 0.  metrics: device, overwritten; NULL to skip. */
+int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const float* lp_samp,
+                               const float* adv, const uint8_t* mask, int64_t T,
+                               const rl_pg_params* params, float* loss_ppo, float* loss_dec,
+                               float* grad_ppo, float* grad_dec, rl_pg_metrics* metrics,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/* ---- utilities ------------------------------------------------------------------ */
+/* The head contraction alone: D[M, N] fp32 = A[M, K] * B[N, K]^T, A and B bf16 row-major
+ * (K contiguous), device pointers, 16-byte aligned; K % 8 == 0, N % 4 == 0.  Same tcgen05
+ * tensor-core pipeline as rl_head_loss_fwd with a plain store epilogue; for unit tests and
+ * for timing the contraction in isolation.  Status bits: RL_STATUS_TIMEOUT only. */
+int rl_gemm_bf16_tn(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* D,
+                    int32_t* dev_status, void* stream);
+
+/* Synchronous device->host copy of the status word.  Call after the stream is done. */
+int rl_status_read(const int32_t* dev_status, int32_t* host_out);
+/* Kernels this library has launched in this process (for launch accounting). */
+int64_t rl_kernel_launch_count(void);
+/* Static text for an RL_ERR_* code; the last error's detail in rl_last_error(). */
+const char* rl_error_string(int code);
+const char* rl_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RLHEAD_H */

@@ -1,0 +1,195 @@
+// C ABI of librlhead (declared in include/rlhead.h): host-side argument checks,
+// workspace sizing and dispatch to the implementations.  Nothing here allocates device
+// memory or synchronises, except rl_status_read.
+#include <cmath>
+#include <cstring>
+
+#include "internal.h"
+
+using namespace rl;
+
+int64_t rl_launch_counter_value();
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int fail(int code, const char* msg) {
+    set_last_error(msg);
+    return code;
+}
+
+int check_params(const rl_params* p) {
+    if (!p) return fail(RL_ERR_ARG, "params is NULL");
+    if (p->loss_type < RL_LOSS_IPO || p->loss_type > RL_LOSS_REINFORCE) return fail(RL_ERR_ARG, "bad loss_type");
+    if (p->kl_estimator < RL_KL_EXACT || p->kl_estimator > RL_KL_K1) return fail(RL_ERR_ARG, "bad kl_estimator");
+    if (p->kl_staleness < RL_STALE_NONE || p->kl_staleness > RL_STALE_INV_SQRT) return fail(RL_ERR_ARG, "bad kl_staleness");
+    if (p->bwd_mode < RL_BWD_AUTO || p->bwd_mode > RL_BWD_SPARSE) return fail(RL_ERR_ARG, "bad bwd_mode");
+    if (p->grad_precision < RL_GRAD_BF16 || p->grad_precision > RL_GRAD_SPLIT) return fail(RL_ERR_ARG, "bad grad_precision");
+    if (!(p->eps >= 0.f) || !(p->max_importance_ratio > 0.f)) return fail(RL_ERR_ARG, "bad eps / max_importance_ratio");
+    if (!(p->icepop_low >= 0.f) || !(p->icepop_low <= p->icepop_high)) return fail(RL_ERR_ARG, "bad icepop band");
+    if (!(p->temperature > 0.f) || !std::isfinite(p->temperature)) return fail(RL_ERR_ARG, "bad temperature");
+    if (!(p->kl_coeff >= 0.f) || !std::isfinite(p->adv_tau)) return fail(RL_ERR_ARG, "bad kl_coeff / adv_tau");
+    if (p->token_chunk < 0 || p->token_chunk % 128 != 0) return fail(RL_ERR_ARG, "token_chunk must be a multiple of 128");
+    return RL_OK;
+}
+
+int check_shape(int64_t N, int64_t H, int64_t V, int64_t nnz) {
+    if (N < 0 || H <= 0 || V <= 0 || nnz < 0) return fail(RL_ERR_ARG, "negative or zero size");
+    if (H % 64 != 0) return fail(RL_ERR_UNSUPPORTED, "H must be a multiple of 64");
+    if (V % 8 != 0) return fail(RL_ERR_UNSUPPORTED, "V must be a multiple of 8");
+    if (V >= (int64_t(1) << 30) || N >= (int64_t(1) << 31)) return fail(RL_ERR_UNSUPPORTED, "N or V too large");
+    return RL_OK;
+}
+
+int check_batch(const rl_head_batch* b) {
+    if (!b) return fail(RL_ERR_ARG, "batch is NULL");
+    int rc = check_shape(b->N, b->H, b->V, b->support.nnz);
+    if (rc != RL_OK) return rc;
+    if (b->N == 0) return RL_OK;
+    if (!b->hidden || !b->weight || !b->labels || !b->label_logq || !b->adv || !b->support.offsets ||
+        !b->support.replayed)
+        return fail(RL_ERR_ARG, "required batch pointer is NULL");
+    if (b->support.nnz > 0 && (!b->support.ids || !b->support.logq))
+        return fail(RL_ERR_ARG, "support ids/logq NULL with nnz > 0");
+    if (!aligned16(b->hidden) || !aligned16(b->weight)) return fail(RL_ERR_ARG, "hidden/weight not 16-byte aligned");
+    return RL_OK;
+}
+
+int sm100_family() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    int major = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return 0;
+    return major == 10;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+size_t rl_head_saved_bytes(int64_t N, int64_t nnz) {
+    if (N < 0 || nnz < 0) return 0;
+    size_t bytes = 0;
+    saved_view(nullptr, N, nnz, &bytes);
+    return bytes;
+}
+
+size_t rl_head_fwd_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* params) {
+    (void)params;
+    if (N < 0 || H <= 0 || V <= 0 || nnz < 0) return 0;
+    size_t bytes = 0;
+    fwd_ws_view(nullptr, N, H, V, nnz, &bytes);
+    return bytes;
+}
+
+size_t rl_head_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* params) {
+    if (N < 0 || H <= 0 || V <= 0 || nnz < 0 || !params) return 0;
+    size_t bytes = 0;
+    bwd_ws_view(nullptr, N, H, V, nnz, params, &bytes);
+    return bytes;
+}
+
+int rl_validate_support(const rl_head_batch* batch, int32_t* dev_status, void* stream) {
+    int rc = check_batch(batch);
+    if (rc != RL_OK) return rc;
+    if (!dev_status) return fail(RL_ERR_ARG, "dev_status is NULL");
+    if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
+    return validate_impl(batch, dev_status, as_stream(stream));
+}
+
+int rl_head_loss_fwd(const rl_head_batch* batch, const rl_params* params, const rl_head_outputs* out,
+                     void* saved, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+    int rc = check_batch(batch);
+    if (rc != RL_OK) return rc;
+    if ((rc = check_params(params)) != RL_OK) return rc;
+    if (!out || !out->loss || !saved || !dev_status) return fail(RL_ERR_ARG, "out/loss/saved/dev_status NULL");
+    if (ws_bytes < rl_head_fwd_workspace_bytes(batch->N, batch->H, batch->V, batch->support.nnz, params))
+        return fail(RL_ERR_WORKSPACE, "forward workspace too small");
+    if (!ws) return fail(RL_ERR_ARG, "ws is NULL");
+    if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
+    return head_fwd_impl(batch, params, out, saved, ws, dev_status, as_stream(stream));
+}
+
+int rl_head_loss_bwd(const rl_head_batch* batch, const rl_params* params, const void* saved, const float* dloss,
+                     void* dhidden, float* dW, int accumulate_dW, void* ws, size_t ws_bytes, int32_t* dev_status,
+                     void* stream) {
+    int rc = check_batch(batch);
+    if (rc != RL_OK) return rc;
+    if ((rc = check_params(params)) != RL_OK) return rc;
+    if (!saved || !dloss || !dW || !dev_status || (batch->N > 0 && !dhidden))
+        return fail(RL_ERR_ARG, "saved/dloss/dhidden/dW/dev_status NULL");
+    if (!aligned16(dW) || !aligned16(dhidden)) return fail(RL_ERR_ARG, "dW/dhidden not 16-byte aligned");
+    if (ws_bytes < rl_head_bwd_workspace_bytes(batch->N, batch->H, batch->V, batch->support.nnz, params))
+        return fail(RL_ERR_WORKSPACE, "backward workspace too small");
+    if (!ws) return fail(RL_ERR_ARG, "ws is NULL");
+    if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
+    return head_bwd_impl(batch, params, saved, dloss, dhidden, dW, accumulate_dW, ws, dev_status,
+                         as_stream(stream));
+}
+
+int rl_mismatch_metrics(const rl_head_batch* batch, const void* saved, rl_head_metrics* metrics, void* ws,
+                        size_t ws_bytes, void* stream) {
+    int rc = check_batch(batch);
+    if (rc != RL_OK) return rc;
+    if (!saved || !metrics || !ws) return fail(RL_ERR_ARG, "saved/metrics/ws NULL");
+    if (ws_bytes < rl_head_fwd_workspace_bytes(batch->N, batch->H, batch->V, batch->support.nnz, nullptr))
+        return fail(RL_ERR_WORKSPACE, "workspace too small");
+    if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
+    return metrics_impl(batch, saved, metrics, ws, as_stream(stream));
+}
+
+size_t rl_policy_workspace_bytes(int64_t T) { return T < 0 ? 0 : policy_ws_bytes(T); }
+
+int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const float* lp_samp, const float* adv,
+                               const uint8_t* mask, int64_t T, const rl_pg_params* params, float* loss_ppo,
+                               float* loss_dec, float* grad_ppo, float* grad_dec, rl_pg_metrics* metrics, void* ws,
+                               size_t ws_bytes, void* stream) {
+    if (T < 0) return fail(RL_ERR_ARG, "T < 0");
+    if (!params) return fail(RL_ERR_ARG, "params NULL");
+    if (params->n_curve < 0 || params->n_curve > RL_PG_MAX_CURVE) return fail(RL_ERR_ARG, "bad n_curve");
+    if (!(params->clip_ratio_low >= 0.f) || !(params->clip_ratio_high >= 0.f) || !(params->clip_ratio_c > 1.f) ||
+        !(params->tis_upper > 0.f) || !(params->icepop_low <= params->icepop_high))
+        return fail(RL_ERR_ARG, "bad pg params");
+    if (T > 0 && (!lp_theta || !lp_old || !lp_samp || !adv || !mask)) return fail(RL_ERR_ARG, "input NULL");
+    if (ws_bytes < rl_policy_workspace_bytes(T) || !ws) return fail(RL_ERR_WORKSPACE, "policy workspace too small");
+    if (T == 0 && !metrics) return RL_OK;
+    if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
+    return policy_impl(lp_theta, lp_old, lp_samp, adv, mask, T, params, loss_ppo, loss_dec, grad_ppo, grad_dec,
+                       metrics, ws, as_stream(stream));
+}
+
+int rl_gemm_bf16_tn(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* D,
+                    int32_t* dev_status, void* stream) {
+    if (!A || !B || !D || !dev_status) return fail(RL_ERR_ARG, "NULL pointer");
+    if (M <= 0 || N <= 0 || K <= 0) return fail(RL_ERR_ARG, "non-positive size");
+    if (K % 8 != 0 || N % 4 != 0) return fail(RL_ERR_UNSUPPORTED, "K % 8 or N % 4 != 0");
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D)) return fail(RL_ERR_ARG, "not 16-byte aligned");
+    if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
+    return gemm_util_impl(A, B, M, N, K, D, dev_status, as_stream(stream));
+}
+
+int rl_status_read(const int32_t* dev_status, int32_t* host_out) {
+    if (!dev_status || !host_out) return fail(RL_ERR_ARG, "NULL pointer");
+    return cudaMemcpy(host_out, dev_status, sizeof(int32_t), cudaMemcpyDeviceToHost) == cudaSuccess ? RL_OK
+                                                                                                     : RL_ERR_CUDA;
+}
+
+int64_t rl_kernel_launch_count(void) {
+    return rl_launch_counter_value();
+}
+
+const char* rl_error_string(int code) {
+    switch (code) {
+        case RL_OK: return "ok";
+        case RL_ERR_ARG: return "invalid argument";
+        case RL_ERR_WORKSPACE: return "workspace too small";
+        case RL_ERR_UNSUPPORTED: return "unsupported shape or device";
+        case RL_ERR_CUDA: return "CUDA error";
+        default: return "unknown error";
+    }
+}
+
+}  // extern "C"

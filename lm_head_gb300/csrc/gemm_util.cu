@@ -1,0 +1,51 @@
+// rl_gemm_bf16_tn: the head contraction alone, D[M, N] (fp32) = A[M, K] B[N, K]^T with
+// bf16 K-major operands, through the same tcgen05 pipeline as the fused kernels and a
+// plain store epilogue.  Used to unit-test and time the tensor-core path in isolation.
+#include "gemm_tc.cuh"
+#include "internal.h"
+
+namespace rl {
+
+struct EpiStore {
+    struct Params {
+        int64_t M, N;
+        float* D;
+    };
+    int64_t t;
+    bool valid;
+    RL_DEVINL void begin_unit(const Params& p, int row, int m_blk, int, int) {
+        t = static_cast<int64_t>(m_blk) * kBM + row;
+        valid = t < p.M;
+    }
+    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0) {
+        if (!valid || col0 >= p.N) return;
+        float* d = p.D + t * p.N + col0;
+        if (col0 + 32 <= p.N) {
+            float4* d4 = reinterpret_cast<float4*>(d);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                d4[q] = make_float4(__uint_as_float(acc[4 * q]), __uint_as_float(acc[4 * q + 1]),
+                                    __uint_as_float(acc[4 * q + 2]), __uint_as_float(acc[4 * q + 3]));
+        } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                if (col0 + k < p.N) d[k] = __uint_as_float(acc[k]);
+        }
+    }
+    RL_DEVINL void end_unit(const Params&, int) {}
+};
+
+int gemm_util_impl(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* D,
+                   int32_t* status, cudaStream_t stream) {
+    CUtensorMap ta, tb;
+    int rc = make_tmap_bf16(&ta, A, M, K, K, kBM);
+    if (rc != RL_OK) return rc;
+    if ((rc = make_tmap_bf16(&tb, B, N, K, K, kBN)) != RL_OK) return rc;
+    const GemmPlan plan = make_plan(M, N, K, 1, 1 << 30, 1, status);
+    EpiStore::Params ep{M, N, D};
+    rc = launch_gemm<EpiStore>(ta, ta, tb, plan, ep, stream);
+    count_launch();
+    return rc;
+}
+
+}  // namespace rl

@@ -1,0 +1,574 @@
+// Backward of the fused LM head + unified RL loss (prime-rl pull request #4233, "Sparse
+// LM-head backward": dense softmax-gradient GEMMs, or a deterministic CSR matmul when
+// every logit gradient lies on the label and the support).
+//
+// With g_t = dloss_t the logit gradient of token t splits into
+//     G_tj = alpha_t * P_full,tj  +  sum over spikes (label, support entries)
+// where alpha_t = g_t * dcoef_t / T is non-zero only on untruncated rows whose gradient
+// has a dense softmax part (the forward folds a replayed row's renormalised-softmax term
+// into its support entries).  The spikes always go through the sparse path:
+//     dX_t += sum_e c_e W[v_e],    dW[v] += sum_{e: v_e = v} c_e x_t     (fixed order)
+// and the dense part, chunk by chunk over tokens, through three tcgen05 GEMMs:
+//     G_c  = alpha * exp(X_c W^T / T - lse)      (EpiGrad: writes G_c [n, V] and G_c^T)
+//     dX_c = G_c * W   (+ sparse dX, -> bf16)    (A = G_c, B = W^T copy, K = V)
+//     dW  += G_c^T X_c                           (A = G_c^T, B = X_c^T copy, K = n)
+#include <climits>
+#include <cmath>
+
+#include "gemm_tc.cuh"
+#include "internal.h"
+
+namespace rl {
+
+bool bwd_is_dense(const rl_params* prm) {
+    if (prm->bwd_mode == RL_BWD_DENSE) return true;
+    if (prm->bwd_mode == RL_BWD_SPARSE) return false;
+    const bool knobs_sparse = prm->loss_type == RL_LOSS_REINFORCE && prm->kl_coeff == 0.f;
+    return !(knobs_sparse || prm->all_replayed != 0);
+}
+
+static int64_t bwd_chunk(int64_t N, const rl_params* prm) {
+    int64_t c = prm->token_chunk > 0 ? prm->token_chunk : 16384;
+    c = (c + kBM - 1) / kBM * kBM;
+    const int64_t n128 = (N + kBM - 1) / kBM * kBM;
+    if (c > n128) c = n128;
+    return c < kBM ? kBM : c;
+}
+
+constexpr int kSortTile = 2048;
+constexpr int kDigitBits = 9;
+constexpr int kDigits = 1 << kDigitBits;
+
+BwdWs bwd_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* prm,
+                  size_t* bytes) {
+    Carve c(base);
+    BwdWs w{};
+    w.dense = bwd_is_dense(prm);
+    w.split = prm->grad_precision == RL_GRAD_SPLIT;
+    w.chunk = bwd_chunk(N, prm);
+    const int64_t items = nnz + N;
+    if (w.dense) {
+        w.Wt = c.take<uint16_t>(static_cast<size_t>(V) * H);
+        w.Xt = c.take<uint16_t>(static_cast<size_t>(H) * w.chunk);
+        w.G = c.take<uint16_t>(static_cast<size_t>(w.chunk) * V);
+        w.Gt = c.take<uint16_t>(static_cast<size_t>(V) * w.chunk);
+        if (w.split) {
+            w.G_lo = c.take<uint16_t>(static_cast<size_t>(w.chunk) * V);
+            w.Gt_lo = c.take<uint16_t>(static_cast<size_t>(V) * w.chunk);
+        }
+        w.dxs = c.take<float>(static_cast<size_t>(N) * H);
+    }
+    w.item_tok = c.take<int32_t>(items);
+    w.keys_a = c.take<int32_t>(items);
+    w.vals_a = c.take<int32_t>(items);
+    w.keys_b = c.take<int32_t>(items);
+    w.vals_b = c.take<int32_t>(items);
+    const int64_t tiles = (items + kSortTile - 1) / kSortTile;
+    w.hist = c.take<int32_t>(static_cast<size_t>(tiles > 0 ? tiles : 1) * kDigits);
+    w.bucket = c.take<int64_t>(V + 2);
+    if (bytes) *bytes = align_up(c.off, 256);
+    return w;
+}
+
+// ----------------------------------------------------------------------------------
+// GEMM epilogues
+// ----------------------------------------------------------------------------------
+RL_DEVINL uint32_t pack_bf16x2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// G = alpha_t * exp(z - lse_t) for the tile, written as G [n, V] (row-major, ld V) and
+// G^T [V, ldt]; with `split`, also the bf16 remainder G - bf16(G) into G_lo / Gt_lo.
+struct EpiGrad {
+    struct Params {
+        int64_t n;       // valid tokens of the chunk
+        int32_t V;
+        float inv_T;
+        const float* lse;     // chunk-relative
+        const float* dloss;   // chunk-relative
+        const float* dcoef;   // chunk-relative
+        uint16_t* G;
+        uint16_t* Gt;
+        uint16_t* G_lo;
+        uint16_t* Gt_lo;
+        int64_t ldt;
+    };
+    int64_t t;
+    bool valid;
+    float alpha, lse;
+
+    RL_DEVINL void begin_unit(const Params& p, int row, int m_blk, int, int) {
+        t = static_cast<int64_t>(m_blk) * kBM + row;
+        valid = t < p.n;
+        alpha = 0.f;
+        lse = 0.f;
+        if (valid) {
+            alpha = p.dloss[t] * p.dcoef[t] * p.inv_T;
+            lse = p.lse[t];
+        }
+    }
+    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0) {
+        if (!valid || col0 >= p.V) return;
+        const int nvalid = p.V - col0 < 32 ? p.V - col0 : 32;  // multiple of 8
+        float g[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const float z = __uint_as_float(acc[k]) * p.inv_T;
+            g[k] = alpha == 0.f ? 0.f : alpha * exp2_approx((z - lse) * kLog2e);
+        }
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            hi[k] = pack_bf16x2(g[2 * k], g[2 * k + 1]);
+            if (p.G_lo) {
+                const float h0 = bf16_bits_to_float(static_cast<uint16_t>(hi[k] & 0xFFFFu));
+                const float h1 = bf16_bits_to_float(static_cast<uint16_t>(hi[k] >> 16));
+                lo[k] = pack_bf16x2(g[2 * k] - h0, g[2 * k + 1] - h1);
+            }
+        }
+        uint4* grow = reinterpret_cast<uint4*>(p.G + t * p.V + col0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (q * 8 < nvalid) grow[q] = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+        if (p.G_lo) {
+            uint4* lrow = reinterpret_cast<uint4*>(p.G_lo + t * p.V + col0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (q * 8 < nvalid) lrow[q] = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+        }
+        // transposed copy: for each column, the 32 lanes (consecutive tokens) write 64 B
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            if (k < nvalid) {
+                const uint16_t hv = static_cast<uint16_t>((k & 1) ? (hi[k >> 1] >> 16) : (hi[k >> 1] & 0xFFFFu));
+                p.Gt[static_cast<int64_t>(col0 + k) * p.ldt + t] = hv;
+                if (p.Gt_lo) {
+                    const uint16_t lv = static_cast<uint16_t>((k & 1) ? (lo[k >> 1] >> 16) : (lo[k >> 1] & 0xFFFFu));
+                    p.Gt_lo[static_cast<int64_t>(col0 + k) * p.ldt + t] = lv;
+                }
+            }
+        }
+    }
+    RL_DEVINL void end_unit(const Params&, int) {}
+};
+
+// dX rows of the chunk: bf16(acc + dxs) for columns < H.
+struct EpiDx {
+    struct Params {
+        int64_t n;
+        int32_t H;
+        const float* dxs;   // chunk-relative [n, H]
+        uint16_t* out;      // chunk-relative [n, H] bf16
+    };
+    int64_t t;
+    bool valid;
+    RL_DEVINL void begin_unit(const Params& p, int row, int m_blk, int, int) {
+        t = static_cast<int64_t>(m_blk) * kBM + row;
+        valid = t < p.n;
+    }
+    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0) {
+        if (!valid || col0 >= p.H) return;
+        const float4* s = reinterpret_cast<const float4*>(p.dxs + t * p.H + col0);
+        uint4* o = reinterpret_cast<uint4*>(p.out + t * p.H + col0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const float4 a = s[2 * q], b = s[2 * q + 1];
+            o[q] = make_uint4(pack_bf16x2(__uint_as_float(acc[8 * q + 0]) + a.x, __uint_as_float(acc[8 * q + 1]) + a.y),
+                              pack_bf16x2(__uint_as_float(acc[8 * q + 2]) + a.z, __uint_as_float(acc[8 * q + 3]) + a.w),
+                              pack_bf16x2(__uint_as_float(acc[8 * q + 4]) + b.x, __uint_as_float(acc[8 * q + 5]) + b.y),
+                              pack_bf16x2(__uint_as_float(acc[8 * q + 6]) + b.z, __uint_as_float(acc[8 * q + 7]) + b.w));
+        }
+    }
+    RL_DEVINL void end_unit(const Params&, int) {}
+};
+
+// dW rows: dW = (accumulate ? dW : 0) + acc for columns < H, rows < V.
+struct EpiDw {
+    struct Params {
+        int64_t V;
+        int32_t H;
+        int32_t accumulate;
+        float* dW;
+    };
+    int64_t v;
+    bool valid;
+    RL_DEVINL void begin_unit(const Params& p, int row, int m_blk, int, int) {
+        v = static_cast<int64_t>(m_blk) * kBM + row;
+        valid = v < p.V;
+    }
+    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0) {
+        if (!valid || col0 >= p.H) return;
+        float4* d = reinterpret_cast<float4*>(p.dW + v * p.H + col0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float4 r = make_float4(__uint_as_float(acc[4 * q]), __uint_as_float(acc[4 * q + 1]),
+                                   __uint_as_float(acc[4 * q + 2]), __uint_as_float(acc[4 * q + 3]));
+            if (p.accumulate) {
+                const float4 o = d[q];
+                r.x += o.x;
+                r.y += o.y;
+                r.z += o.z;
+                r.w += o.w;
+            }
+            d[q] = r;
+        }
+    }
+    RL_DEVINL void end_unit(const Params&, int) {}
+};
+
+// ----------------------------------------------------------------------------------
+// Transpose (bf16): out[c, r] = in[r, c] for r < rows, c < cols
+// ----------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* in, int64_t rows,
+                                                             int64_t cols, int64_t ld_in,
+                                                             uint16_t* out, int64_t ld_out) {
+    __shared__ uint16_t tile[64][66];
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 64;
+    const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
+    for (int i = ty; i < 64; i += 4) {
+        const int64_t r = r0 + i, c = c0 + tx;
+        tile[i][tx] = (r < rows && c < cols) ? in[r * ld_in + c] : 0;
+    }
+    __syncthreads();
+    for (int i = ty; i < 64; i += 4) {
+        const int64_t c = c0 + i, r = r0 + tx;
+        if (c < cols && r < rows) out[c * ld_out + r] = tile[tx][i];
+    }
+}
+
+static int transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in, void* out,
+                          int64_t ld_out, cudaStream_t s) {
+    if (rows <= 0 || cols <= 0) return RL_OK;
+    dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
+    if (grid.y > 65535u) return RL_ERR_UNSUPPORTED;
+    transpose_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(in), rows, cols, ld_in,
+                                               static_cast<uint16_t*>(out), ld_out);
+    count_launch();
+    return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------------------------
+// Sparse dX: dX_t = (g_t / T) (labcoef_t W[a_t] + sum_e entcoef_e W[v_e])
+// One block per token; thread i owns hidden columns [8 i, 8 i + 8) (+ 2048 strides).
+// ----------------------------------------------------------------------------------
+struct SparseArgs {
+    int64_t N, H, V, nnz;
+    const uint16_t* W;
+    const uint16_t* X;
+    const int32_t* labels;
+    const int64_t* offsets;
+    const int32_t* ids;
+    const float* dloss;
+    const float* labcoef;
+    const float* entcoef;
+    float inv_T;
+};
+
+RL_DEVINL void fma_row8(float (&acc)[8], const uint16_t* row, float c) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        acc[2 * k] = fmaf(c, __uint_as_float(w[k] << 16), acc[2 * k]);
+        acc[2 * k + 1] = fmaf(c, __uint_as_float(w[k] & 0xFFFF0000u), acc[2 * k + 1]);
+    }
+}
+
+template <bool kToBf16>
+__global__ void __launch_bounds__(256) sparse_dx_kernel(SparseArgs a, float* dxs, uint16_t* dx_bf16) {
+    const int64_t t = blockIdx.x;
+    const float g = a.dloss[t] * a.inv_T;
+    int64_t b = a.offsets[t], e = a.offsets[t + 1];
+    b = b < 0 ? 0 : (b > a.nnz ? a.nnz : b);
+    e = e < b ? b : (e > a.nnz ? a.nnz : e);
+    const int32_t lab = a.labels[t];
+    const float cl = g * a.labcoef[t];
+    for (int64_t h0 = static_cast<int64_t>(threadIdx.x) * 8; h0 < a.H; h0 += 256 * 8) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (g != 0.f) {
+            if (lab >= 0 && lab < a.V && cl != 0.f) fma_row8(acc, a.W + lab * a.H + h0, cl);
+            for (int64_t j = b; j < e; ++j) {
+                const int32_t id = a.ids[j];
+                const float c = g * a.entcoef[j];
+                if (id >= 0 && id < a.V && c != 0.f) fma_row8(acc, a.W + id * a.H + h0, c);
+            }
+        }
+        if (kToBf16) {
+            uint4 o = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                 pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+            *reinterpret_cast<uint4*>(dx_bf16 + t * a.H + h0) = o;
+        } else {
+            float4* o = reinterpret_cast<float4*>(dxs + t * a.H + h0);
+            o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------------
+// Sparse dW: stable LSD radix sort of the gradient items by vocab id, then one block per
+// vocab id sums its items in item order (items: support entries 0..nnz-1, then labels).
+// ----------------------------------------------------------------------------------
+__global__ void items_init_kernel(SparseArgs a, int32_t* item_tok, int32_t* keys, int32_t* vals) {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= a.N) return;
+    int64_t b = a.offsets[t], e = a.offsets[t + 1];
+    b = b < 0 ? 0 : (b > a.nnz ? a.nnz : b);
+    e = e < b ? b : (e > a.nnz ? a.nnz : e);
+    for (int64_t j = b + lane; j < e; j += 32) {
+        const int32_t id = a.ids[j];
+        item_tok[j] = static_cast<int32_t>(t);
+        keys[j] = (id >= 0 && id < a.V) ? id : static_cast<int32_t>(a.V);
+        vals[j] = static_cast<int32_t>(j);
+    }
+    if (lane == 0) {
+        const int64_t i = a.nnz + t;
+        const int32_t lab = a.labels[t];
+        item_tok[i] = static_cast<int32_t>(t);
+        keys[i] = (lab >= 0 && lab < a.V) ? lab : static_cast<int32_t>(a.V);
+        vals[i] = static_cast<int32_t>(i);
+    }
+}
+
+// Entries with a corrupt row range never get a token; mark them out of range.
+__global__ void items_guard_kernel(const int64_t* offsets, int64_t N, int64_t nnz, int32_t V,
+                                   int32_t* item_tok, int32_t* keys) {
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (j >= nnz) return;
+    const int32_t t = item_tok[j];
+    bool ok = t >= 0 && t < N;
+    if (ok) {
+        const int64_t b = offsets[t], e = offsets[t + 1];
+        ok = j >= b && j < e;
+    }
+    if (!ok) {
+        item_tok[j] = 0;
+        keys[j] = V;
+    }
+}
+
+__global__ void __launch_bounds__(256) radix_hist_kernel(const int32_t* keys, int64_t n, int shift,
+                                                         int32_t* hist, int64_t tiles) {
+    __shared__ int cnt[kDigits];
+    for (int i = threadIdx.x; i < kDigits; i += blockDim.x) cnt[i] = 0;
+    __syncthreads();
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kSortTile;
+    for (int i = threadIdx.x; i < kSortTile; i += blockDim.x) {
+        const int64_t j = t0 + i;
+        if (j < n) atomicAdd(&cnt[(keys[j] >> shift) & (kDigits - 1)], 1);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < kDigits; i += blockDim.x) hist[static_cast<int64_t>(i) * tiles + blockIdx.x] = cnt[i];
+}
+
+// Exclusive scan over hist in digit-major order (single block).
+__global__ void __launch_bounds__(1024) radix_scan_kernel(int32_t* hist, int64_t len) {
+    __shared__ int64_t part[1024];
+    const int64_t per = (len + blockDim.x - 1) / blockDim.x;
+    const int64_t b = threadIdx.x * per;
+    const int64_t e = b + per < len ? b + per : len;
+    int64_t s = 0;
+    for (int64_t i = b; i < e; ++i) s += hist[i];
+    part[threadIdx.x] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int64_t run = 0;
+        for (int i = 0; i < static_cast<int>(blockDim.x); ++i) {
+            const int64_t v = part[i];
+            part[i] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    int64_t run = part[threadIdx.x];
+    for (int64_t i = b; i < e; ++i) {
+        const int32_t v = hist[i];
+        hist[i] = static_cast<int32_t>(run);
+        run += v;
+    }
+}
+
+// One warp per tile scatters its items in order: rank among equal digits inside each
+// group of 32 via match.any, plus running per-digit counters -> stable.
+__global__ void __launch_bounds__(32) radix_scatter_kernel(const int32_t* keys_in, const int32_t* vals_in,
+                                                           int64_t n, int shift, const int32_t* hist,
+                                                           int64_t tiles, int32_t* keys_out,
+                                                           int32_t* vals_out) {
+    __shared__ int base[kDigits];
+    const int lane = threadIdx.x;
+    for (int i = lane; i < kDigits; i += 32) base[i] = hist[static_cast<int64_t>(i) * tiles + blockIdx.x];
+    __syncwarp();
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kSortTile;
+    for (int i = 0; i < kSortTile; i += 32) {
+        const int64_t j = t0 + i + lane;
+        const bool act = j < n;
+        const int32_t k = act ? keys_in[j] : 0;
+        const int digit = act ? ((k >> shift) & (kDigits - 1)) : kDigits;  // inactive lanes: own group
+        const unsigned peers = __match_any_sync(0xffffffffu, digit);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        int pos = 0;
+        if (act) pos = base[digit] + rank;
+        __syncwarp();
+        const int leader_hi = 31 - __clz(peers);  // highest lane of the group updates the counter
+        if (act && lane == leader_hi) base[digit] += __popc(peers);
+        __syncwarp();
+        if (act) {
+            keys_out[pos] = k;
+            vals_out[pos] = vals_in[j];
+        }
+    }
+}
+
+// bucket[v] = first sorted position whose key >= v, for v in [0, V + 1].
+__global__ void bucket_kernel(const int32_t* keys, int64_t n, int32_t V, int64_t* bucket) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i > n) return;
+    const int64_t prev = i == 0 ? -1 : keys[i - 1];
+    const int64_t cur = i == n ? static_cast<int64_t>(V) + 1 : keys[i];
+    for (int64_t v = prev + 1; v <= cur && v <= V + 1; ++v) bucket[v] = i;
+}
+
+__global__ void __launch_bounds__(256) sparse_dw_kernel(SparseArgs a, const int32_t* vals,
+                                                        const int32_t* item_tok, const int64_t* bucket,
+                                                        float* dW) {
+    const int64_t v = blockIdx.x;
+    const int64_t b = bucket[v], e = bucket[v + 1];
+    if (e <= b) return;
+    for (int64_t h0 = static_cast<int64_t>(threadIdx.x) * 8; h0 < a.H; h0 += 256 * 8) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int64_t i = b; i < e; ++i) {
+            const int32_t item = vals[i];
+            const int32_t t = item_tok[item];
+            const float g = a.dloss[t] * a.inv_T;
+            const float c = g * (item < a.nnz ? a.entcoef[item] : a.labcoef[t]);
+            if (c != 0.f) fma_row8(acc, a.X + static_cast<int64_t>(t) * a.H + h0, c);
+        }
+        float4* d = reinterpret_cast<float4*>(dW + v * a.H + h0);
+        float4 o0 = d[0], o1 = d[1];
+        o0.x += acc[0];
+        o0.y += acc[1];
+        o0.z += acc[2];
+        o0.w += acc[3];
+        o1.x += acc[4];
+        o1.y += acc[5];
+        o1.z += acc[6];
+        o1.w += acc[7];
+        d[0] = o0;
+        d[1] = o1;
+    }
+}
+
+static int sparse_dw(const SparseArgs& a, const BwdWs& w, float* dW, cudaStream_t s) {
+    const int64_t n = a.nnz + a.N;
+    if (n >= (int64_t(1) << 31)) {
+        set_last_error("sparse gradient items exceed 2^31");
+        return RL_ERR_UNSUPPORTED;
+    }
+    items_init_kernel<<<static_cast<unsigned>((a.N + 7) / 8), 256, 0, s>>>(a, w.item_tok, w.keys_a, w.vals_a);
+    if (a.nnz > 0)
+        items_guard_kernel<<<static_cast<unsigned>((a.nnz + 255) / 256), 256, 0, s>>>(
+            a.offsets, a.N, a.nnz, static_cast<int32_t>(a.V), w.item_tok, w.keys_a);
+    count_launch(2);
+    const int64_t tiles = (n + kSortTile - 1) / kSortTile;
+    int bits = 1;
+    while ((int64_t(1) << bits) <= a.V) ++bits;  // keys in [0, V]
+    const int passes = (bits + kDigitBits - 1) / kDigitBits;
+    int32_t *kin = w.keys_a, *vin = w.vals_a, *kout = w.keys_b, *vout = w.vals_b;
+    for (int p = 0; p < passes; ++p) {
+        const int shift = p * kDigitBits;
+        radix_hist_kernel<<<static_cast<unsigned>(tiles), 256, 0, s>>>(kin, n, shift, w.hist, tiles);
+        radix_scan_kernel<<<1, 1024, 0, s>>>(w.hist, tiles * kDigits);
+        radix_scatter_kernel<<<static_cast<unsigned>(tiles), 32, 0, s>>>(kin, vin, n, shift, w.hist, tiles, kout, vout);
+        count_launch(3);
+        int32_t* tk = kin;
+        kin = kout;
+        kout = tk;
+        int32_t* tv = vin;
+        vin = vout;
+        vout = tv;
+    }
+    bucket_kernel<<<static_cast<unsigned>((n + 1 + 255) / 256), 256, 0, s>>>(kin, n, static_cast<int32_t>(a.V), w.bucket);
+    sparse_dw_kernel<<<static_cast<unsigned>(a.V), 256, 0, s>>>(a, vin, w.item_tok, w.bucket, dW);
+    count_launch(2);
+    return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------------------------
+// Entry
+// ----------------------------------------------------------------------------------
+int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* saved,
+                  const float* dloss, void* dhidden, float* dW, int accumulate, void* ws,
+                  int32_t* status, cudaStream_t stream) {
+    const int64_t N = b->N, H = b->H, V = b->V, nnz = b->support.nnz;
+    if (N == 0) {
+        if (!accumulate && V > 0)
+            if (cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * sizeof(float), stream) != cudaSuccess)
+                return RL_ERR_CUDA;
+        return RL_OK;
+    }
+    const SavedView sv = saved_view(const_cast<void*>(saved), N, nnz, nullptr);
+    const BwdWs w = bwd_ws_view(ws, N, H, V, nnz, prm, nullptr);
+    SparseArgs sa{N, H, V, nnz,
+                  static_cast<const uint16_t*>(b->weight), static_cast<const uint16_t*>(b->hidden),
+                  b->labels, b->support.offsets, b->support.ids, dloss, sv.labcoef, sv.entcoef,
+                  1.0f / prm->temperature};
+    int rc;
+    if (!w.dense) {
+        sparse_dx_kernel<true><<<static_cast<unsigned>(N), 256, 0, stream>>>(sa, nullptr, static_cast<uint16_t*>(dhidden));
+        count_launch();
+        if (!accumulate)
+            if (cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * sizeof(float), stream) != cudaSuccess)
+                return RL_ERR_CUDA;
+        return sparse_dw(sa, w, dW, stream);
+    }
+
+    sparse_dx_kernel<false><<<static_cast<unsigned>(N), 256, 0, stream>>>(sa, w.dxs, nullptr);
+    count_launch();
+    rc = transpose_bf16(b->weight, V, H, H, w.Wt, V, stream);
+    if (rc != RL_OK) return rc;
+
+    CUtensorMap tmW, tmWt;
+    rc = make_tmap_bf16(&tmW, b->weight, V, H, H, kBN);
+    if (rc != RL_OK) return rc;
+    rc = make_tmap_bf16(&tmWt, w.Wt, H, V, V, kBN);
+    if (rc != RL_OK) return rc;
+    const int passes = w.split ? 2 : 1;
+    for (int64_t c0 = 0; c0 < N; c0 += w.chunk) {
+        const int64_t n = N - c0 < w.chunk ? N - c0 : w.chunk;
+        const uint16_t* Xc = static_cast<const uint16_t*>(b->hidden) + c0 * H;
+        rc = transpose_bf16(Xc, n, H, H, w.Xt, w.chunk, stream);
+        if (rc != RL_OK) return rc;
+        CUtensorMap tmX, tmG, tmGlo, tmGt, tmGtlo, tmXt;
+        if ((rc = make_tmap_bf16(&tmX, Xc, n, H, H, kBM)) != RL_OK) return rc;
+        if ((rc = make_tmap_bf16(&tmG, w.G, n, V, V, kBM)) != RL_OK) return rc;
+        if ((rc = make_tmap_bf16(&tmGt, w.Gt, V, n, w.chunk, kBM)) != RL_OK) return rc;
+        if ((rc = make_tmap_bf16(&tmXt, w.Xt, H, n, w.chunk, kBN)) != RL_OK) return rc;
+        tmGlo = tmG;
+        tmGtlo = tmGt;
+        if (w.split) {
+            if ((rc = make_tmap_bf16(&tmGlo, w.G_lo, n, V, V, kBM)) != RL_OK) return rc;
+            if ((rc = make_tmap_bf16(&tmGtlo, w.Gt_lo, V, n, w.chunk, kBM)) != RL_OK) return rc;
+        }
+        // G chunk (recomputed logits -> softmax gradient), both layouts
+        EpiGrad::Params gp{n, static_cast<int32_t>(V), 1.0f / prm->temperature, sv.lse + c0, dloss + c0,
+                           sv.dcoef + c0, static_cast<uint16_t*>(w.G), static_cast<uint16_t*>(w.Gt),
+                           static_cast<uint16_t*>(w.G_lo), static_cast<uint16_t*>(w.Gt_lo), w.chunk};
+        const GemmPlan p1 = make_plan(n, V, H, 1, 1 << 30, 1, status);
+        if ((rc = launch_gemm<EpiGrad>(tmX, tmX, tmW, p1, gp, stream)) != RL_OK) return rc;
+        // dX chunk = G W + sparse part
+        EpiDx::Params dp{n, static_cast<int32_t>(H), w.dxs + c0 * H, static_cast<uint16_t*>(dhidden) + c0 * H};
+        const GemmPlan p2 = make_plan(n, H, V, passes, 1 << 30, 0, status);
+        if ((rc = launch_gemm<EpiDx>(tmG, tmGlo, tmWt, p2, dp, stream)) != RL_OK) return rc;
+        // dW += G^T X
+        EpiDw::Params wp{V, static_cast<int32_t>(H), (c0 > 0 || accumulate) ? 1 : 0, dW};
+        const GemmPlan p3 = make_plan(V, H, n, passes, 1 << 30, 0, status);
+        if ((rc = launch_gemm<EpiDw>(tmGt, tmGtlo, tmXt, p3, wp, stream)) != RL_OK) return rc;
+        count_launch(3);
+    }
+    return sparse_dw(sa, w, dW, stream);
+}
+
+}  // namespace rl

@@ -1,0 +1,663 @@
+// Forward of the fused LM head + unified RL loss (prime-rl pull request #4233: the loss_t
+// equation, the two estimator rules for u, "What changes").
+//
+//   1. validate_kernel     CSR sampler evidence -> status bits (GPU validation item)
+//   2. gemm_tc<EpiStats>   z = X W^T / T by 128 x 256 tensor-core tiles; per row an online
+//                          (max, sum e^{z-m}, sum e^{z-m}(z-m)) over the unit's vocab range,
+//                          and the label / support logits gathered out of the tile
+//   3. token_loss_kernel   one warp per token: combine the split statistics into
+//                          logsumexp and entropy, renormalise over a replayed support,
+//                          weights w and masks, centering, KL, loss_t, backward
+//                          coefficients and per-token metric terms
+//   4. metrics kernels     deterministic fp64 reduction of the metric terms
+#include <cmath>
+#include <climits>
+
+#include "gemm_tc.cuh"
+#include "internal.h"
+
+namespace rl {
+
+// ----------------------------------------------------------------------------------
+// Workspace / saved-state layouts
+// ----------------------------------------------------------------------------------
+SavedView saved_view(void* base, int64_t N, int64_t nnz, size_t* bytes) {
+    Carve c(base);
+    SavedView v;
+    v.lse = c.take<float>(N);
+    v.lse_s = c.take<float>(N);
+    v.dcoef = c.take<float>(N);
+    v.labcoef = c.take<float>(N);
+    v.entcoef = c.take<float>(nnz > 0 ? nnz : 1);
+    v.mterm = c.take<float>(N * 8);
+    if (bytes) *bytes = align_up(c.off, 256);
+    return v;
+}
+
+static int max_splits(int64_t V) {
+    const int nb = static_cast<int>((V + kBN - 1) / kBN);
+    return nb < 32 ? nb : 32;
+}
+
+FwdWs fwd_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz, size_t* bytes) {
+    (void)H;
+    Carve c(base);
+    FwdWs w;
+    w.splits = max_splits(V);
+    w.part_m = c.take<float>(static_cast<size_t>(w.splits) * N);
+    w.part_s = c.take<float>(static_cast<size_t>(w.splits) * N);
+    w.part_u = c.take<float>(static_cast<size_t>(w.splits) * N);
+    w.zlab = c.take<float>(N);
+    w.zsup = c.take<float>(nnz > 0 ? nnz : 1);
+    w.mpart = c.take<double>(kMetricBlocks * kMetricFields);
+    if (bytes) *bytes = align_up(c.off, 256);
+    return w;
+}
+
+// Split count for the forward GEMM: units = m_blocks * splits spread over the SMs; pick
+// the count that fills the last wave best (ties -> fewer splits).
+static int choose_splits(int64_t N, int64_t V) {
+    const int m_blocks = static_cast<int>((N + kBM - 1) / kBM);
+    const int P = num_sms();
+    const int smax = max_splits(V);
+    int best = 1;
+    double best_eff = 0.0;
+    for (int s = 1; s <= smax; ++s) {
+        const int64_t units = static_cast<int64_t>(m_blocks) * s;
+        const int64_t waves = (units + P - 1) / P;
+        const double eff = static_cast<double>(units) / static_cast<double>(waves * P);
+        if (eff > best_eff + 0.01) {
+            best_eff = eff;
+            best = s;
+        }
+    }
+    return best;
+}
+
+// ----------------------------------------------------------------------------------
+// 1. Validation of the CSR sampler evidence
+// ----------------------------------------------------------------------------------
+struct ValidateArgs {
+    int64_t N, V, nnz;
+    const int64_t* offsets;
+    const int32_t* ids;
+    const float* logq;
+    const uint8_t* replayed;
+    const int32_t* labels;
+    const float* label_logq;
+    const uint8_t* loss_mask;
+    int32_t* status;
+};
+
+__global__ void __launch_bounds__(256) validate_kernel(ValidateArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (t >= a.N) return;
+    int32_t bad = 0;
+    const int64_t b = a.offsets[t], e = a.offsets[t + 1];
+    if (lane == 0) {
+        if (t == 0 && b != 0) bad |= RL_STATUS_OFFSETS;
+        if (t == a.N - 1 && e != a.nnz) bad |= RL_STATUS_OFFSETS;
+    }
+    if (b < 0 || e < b || e > a.nnz) {
+        if (lane == 0) set_status(a.status, bad | RL_STATUS_OFFSETS);
+        return;
+    }
+    const int32_t label = a.labels[t];
+    const bool rl = a.loss_mask ? a.loss_mask[t] != 0 : true;
+    const bool rep = a.replayed[t] != 0;
+    if (lane == 0) {
+        if (label < 0 || label >= a.V) bad |= RL_STATUS_ID_RANGE;
+        const float llq = a.label_logq[t];
+        if (!isfinite(llq) || llq > 1e-6f) bad |= RL_STATUS_LOGQ;
+        if (rl && e == b) bad |= RL_STATUS_EMPTY_ROW;
+    }
+    float mass = 0.f;
+    int found = 0;
+    for (int64_t j = b + lane; j < e; j += 32) {
+        const int32_t id = a.ids[j];
+        const float lq = a.logq[j];
+        if (id < 0 || id >= a.V) bad |= RL_STATUS_ID_RANGE;
+        if (!isfinite(lq) || lq > 1e-6f) bad |= RL_STATUS_LOGQ;
+        if (j > b) {
+            const int32_t prev = a.ids[j - 1];
+            if (rep ? (id <= prev) : (id < prev)) bad |= RL_STATUS_ROW_ORDER;
+        }
+        if (rep) mass += expf(lq);
+        found |= (id == label);
+    }
+    mass = warp_sum(mass);
+    found = __any_sync(0xffffffffu, found);
+    bad = __reduce_or_sync(0xffffffffu, bad);
+    if (lane == 0) {
+        if (rep && rl) {
+            if (!found) bad |= RL_STATUS_LABEL_MISSING;
+            if (fabsf(mass - 1.f) > 1e-3f) bad |= RL_STATUS_SUPPORT_MASS;
+        }
+        set_status(a.status, bad);
+    }
+}
+
+int validate_impl(const rl_head_batch* b, int32_t* status, cudaStream_t stream) {
+    if (b->N == 0) return RL_OK;
+    ValidateArgs a{b->N, b->V, b->support.nnz, b->support.offsets, b->support.ids,
+                   b->support.logq, b->support.replayed, b->labels, b->label_logq,
+                   b->loss_mask, status};
+    const int64_t blocks = (b->N + 7) / 8;
+    validate_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+    count_launch();
+    return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------------------------
+// 2. GEMM epilogue: online logsumexp / entropy statistics + label & support gather
+// ----------------------------------------------------------------------------------
+RL_DEVINL float select32(const float (&v)[32], int idx) {
+    float r = v[0];
+#pragma unroll
+    for (int k = 1; k < 32; ++k) r = (idx == k) ? v[k] : r;
+    return r;
+}
+RL_DEVINL void kahan_add(float& s, float& c, float x) {
+    const float y = x - c;
+    const float t = s + y;
+    c = (t - s) - y;
+    s = t;
+}
+
+struct EpiStats {
+    struct Params {
+        int64_t N;
+        int32_t V;
+        float inv_T;
+        int64_t nnz;
+        const int32_t* labels;
+        const int64_t* offsets;
+        const int32_t* ids;
+        float* zlab;
+        float* zsup;
+        float* part_m;
+        float* part_s;
+        float* part_u;
+    };
+    int64_t t;
+    bool valid;
+    float m, s, sc, u, uc;
+    int64_t ptr, end;
+    int32_t next_id;
+    int32_t label;
+
+    RL_DEVINL void begin_unit(const Params& p, int row, int m_blk, int split, int col_begin) {
+        (void)split;
+        t = static_cast<int64_t>(m_blk) * kBM + row;
+        valid = t < p.N;
+        m = -INFINITY;
+        s = sc = u = uc = 0.f;
+        ptr = end = 0;
+        next_id = INT_MAX;
+        label = -1;
+        if (!valid) return;
+        label = p.labels[t];
+        int64_t b = p.offsets[t], e = p.offsets[t + 1];
+        b = b < 0 ? 0 : (b > p.nnz ? p.nnz : b);
+        e = e < b ? b : (e > p.nnz ? p.nnz : e);
+        int64_t lo = b, hi = e;  // first entry with id >= col_begin
+        while (lo < hi) {
+            const int64_t mid = (lo + hi) >> 1;
+            if (p.ids[mid] < col_begin)
+                lo = mid + 1;
+            else
+                hi = mid;
+        }
+        ptr = lo;
+        end = e;
+        next_id = ptr < end ? p.ids[ptr] : INT_MAX;
+    }
+
+    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0) {
+        if (!valid || col0 >= p.V) return;
+        const int nvalid = p.V - col0;  // > 0
+        float z[32];
+        float cm = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            z[k] = (k < nvalid) ? __uint_as_float(acc[k]) * p.inv_T : -INFINITY;
+            cm = fmaxf(cm, z[k]);
+        }
+        if (cm > m) {
+            if (m == -INFINITY) {
+                s = sc = u = uc = 0.f;
+            } else {
+                const float a = exp2_approx((m - cm) * kLog2e);
+                u = a * (u + (m - cm) * s);
+                uc *= a;
+                s *= a;
+                sc *= a;
+            }
+            m = cm;
+        }
+        float cs = 0.f, cu = 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            const float d = fmaxf(z[k] - m, -1e30f);
+            const float e = exp2_approx(d * kLog2e);
+            cs += e;
+            cu = fmaf(e, d, cu);
+        }
+        kahan_add(s, sc, cs);
+        kahan_add(u, uc, cu);
+        if (static_cast<unsigned>(label - col0) < 32u) p.zlab[t] = select32(z, label - col0);
+        while (next_id < col0 + 32) {
+            p.zsup[ptr] = select32(z, (next_id - col0) & 31);
+            ++ptr;
+            next_id = ptr < end ? p.ids[ptr] : INT_MAX;
+        }
+    }
+
+    RL_DEVINL void end_unit(const Params& p, int split) {
+        if (!valid) return;
+        const int64_t i = static_cast<int64_t>(split) * p.N + t;
+        p.part_m[i] = m;
+        p.part_s[i] = s - sc;
+        p.part_u[i] = u - uc;
+    }
+};
+
+// ----------------------------------------------------------------------------------
+// 3. Per-token loss assembly (one warp per token)
+// ----------------------------------------------------------------------------------
+struct TokenArgs {
+    int64_t N;
+    int32_t V;
+    int32_t S;
+    int64_t nnz;
+    const float* part_m;
+    const float* part_s;
+    const float* part_u;
+    const float* zlab;
+    const float* zsup;
+    const int32_t* labels;
+    const float* label_logq;
+    const float* adv;
+    const uint8_t* loss_mask;
+    const int32_t* age;
+    const int64_t* offsets;
+    const int32_t* ids;
+    const float* logq;
+    const uint8_t* replayed;
+    int32_t loss_type, kl_est, kl_stale, sparse;
+    float eps, cap, lo, hi, adv_tau, kl_coeff;
+    float* loss;
+    float* logp_label;
+    float* logp_support;
+    float* entropy;
+    float* lse_out;
+    uint8_t* mask_label;
+    uint8_t* mask_support;
+    SavedView sv;
+    int32_t* status;
+};
+
+struct WeightOut {
+    float w;
+    float r;
+    bool keep, low, high;
+};
+
+// w of pull request #4233 ("What changes": ipo / icepop / reinforce) with the probability
+// band of "Masking by Probability, Not Ratio".  Decisions are taken in fp32 and re-taken
+// in fp64 (from the same fp32 log-probs) when the fp32 value lies within 1e-5 of a
+// threshold, so the keep bit equals the fp64 predicate evaluated on these log-probs.
+RL_DEVINL WeightOut rl_weight(float logP, float logq, const TokenArgs& a) {
+    WeightOut o;
+    o.r = expf(logP - logq);
+    if (a.loss_type == RL_LOSS_IPO) {
+        float diff = expf(logP) - expf(logq);
+        bool keep;
+        if (fabsf(fabsf(diff) - a.eps) <= 1e-5f) {
+            const double dd = exp(static_cast<double>(logP)) - exp(static_cast<double>(logq));
+            keep = fabs(dd) <= static_cast<double>(a.eps);
+            diff = dd < 0 ? -1.f : (dd > 0 ? 1.f : 0.f);
+        } else {
+            keep = fabsf(diff) <= a.eps;
+        }
+        o.keep = keep;
+        o.w = keep ? fminf(o.r, a.cap) : 0.f;
+        o.low = !keep && diff < 0.f;
+        o.high = !keep && diff > 0.f;
+    } else if (a.loss_type == RL_LOSS_ICEPOP) {
+        bool ge_lo, le_hi;
+        if (fabsf(o.r - a.lo) <= 1e-5f * a.lo || fabsf(o.r - a.hi) <= 1e-5f * a.hi) {
+            const double rd = exp(static_cast<double>(logP) - static_cast<double>(logq));
+            ge_lo = rd >= static_cast<double>(a.lo);
+            le_hi = rd <= static_cast<double>(a.hi);
+        } else {
+            ge_lo = o.r >= a.lo;
+            le_hi = o.r <= a.hi;
+        }
+        o.keep = ge_lo && le_hi;
+        o.w = o.keep ? o.r : 0.f;
+        o.low = !ge_lo;
+        o.high = !le_hi;
+    } else {
+        o.keep = true;
+        o.w = 1.f;
+        o.low = o.high = false;
+    }
+    return o;
+}
+
+__global__ void __launch_bounds__(256) token_loss_kernel(TokenArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (t >= a.N) return;
+    // combine the per-split (m, s, u) statistics: logsumexp and entropy of the full row
+    float M = -INFINITY;
+    for (int i = lane; i < a.S; i += 32) M = fmaxf(M, a.part_m[static_cast<int64_t>(i) * a.N + t]);
+    M = warp_max(M);
+    float s = 0.f, u = 0.f;
+    for (int i = lane; i < a.S; i += 32) {
+        const int64_t k = static_cast<int64_t>(i) * a.N + t;
+        const float mi = a.part_m[k], si = a.part_s[k], ui = a.part_u[k];
+        const float f = expf(mi - M);
+        s += f * si;
+        u += f * (ui + (mi - M) * si);
+    }
+    s = warp_sum(s);
+    u = warp_sum(u);
+    const float logs = logf(s);
+    const float lse = M + logs;
+    const float ent = logs - u / s;
+
+    int64_t b = a.offsets[t], e = a.offsets[t + 1];
+    b = b < 0 ? 0 : (b > a.nnz ? a.nnz : b);
+    e = e < b ? b : (e > a.nnz ? a.nnz : e);
+    const int K = static_cast<int>(e - b);
+    const bool rep = a.replayed[t] != 0;
+    const bool rl = a.loss_mask ? a.loss_mask[t] != 0 : true;
+    const int32_t label = a.labels[t];
+    const bool label_ok = label >= 0 && label < a.V;
+
+    // READING: a replayed token's P is the trainer softmax renormalised over S
+    float lse_s = lse;
+    if (rep) {
+        float mx = -INFINITY;
+        for (int64_t j = b + lane; j < e; j += 32) {
+            const int32_t id = a.ids[j];
+            if (id >= 0 && id < a.V) mx = fmaxf(mx, a.zsup[j]);
+        }
+        mx = warp_max(mx);
+        float ss = 0.f;
+        for (int64_t j = b + lane; j < e; j += 32) {
+            const int32_t id = a.ids[j];
+            if (id >= 0 && id < a.V) ss += expf(a.zsup[j] - mx);
+        }
+        ss = warp_sum(ss);
+        if (ss > 0.f) lse_s = mx + logf(ss);
+    }
+
+    // pass 1 over the support: log P, u, w, sums
+    const float inv_K = K > 0 ? 1.f / static_cast<float>(K) : 0.f;
+    float C = 0.f, U = 0.f, cen = 0.f, klx = 0.f, smass = 0.f, mtv = 0.f;
+    for (int64_t j = b + lane; j < e; j += 32) {
+        const int32_t id = a.ids[j];
+        const float lq = a.logq[j];
+        const bool ok = id >= 0 && id < a.V && isfinite(lq);
+        const float zj = ok ? a.zsup[j] : 0.f;
+        const float logP = zj - lse_s;
+        float uj = rep ? expf(lq) : inv_K;
+        WeightOut wo = rl_weight(logP, lq, a);
+        if (!ok) {
+            uj = 0.f;
+            wo.w = 0.f;
+            wo.keep = false;
+            wo.r = 0.f;
+        }
+        const float c = uj * wo.w;
+        C += c;
+        U += uj;
+        cen = fmaf(c, logP, cen);
+        klx = fmaf(uj, lq - logP, klx);
+        if (ok) smass = fmaf(uj, expf((zj - lse) - lq), smass);
+        if (!wo.keep) mtv = fmaf(uj, wo.r, mtv);
+        if (a.logp_support) a.logp_support[j] = ok ? logP : 0.f;
+        if (a.mask_support) a.mask_support[j] = wo.keep ? 1 : 0;
+        a.sv.entcoef[j] = c;  // pass 2 turns this into the spike coefficient
+    }
+    C = warp_sum(C);
+    U = warp_sum(U);
+    cen = warp_sum(cen);
+    klx = warp_sum(klx);
+    smass = warp_sum(smass);
+    mtv = warp_sum(mtv);
+
+    const float llq = a.label_logq[t];
+    const float logP_lab = label_ok ? a.zlab[t] - lse_s : 0.f;
+    WeightOut wl = rl_weight(logP_lab, llq, a);
+    const int age = a.age ? a.age[t] : 0;
+    const float beta = a.kl_stale == RL_STALE_INV_SQRT
+                           ? a.kl_coeff / sqrtf(1.f + static_cast<float>(age))
+                           : a.kl_coeff;
+    const bool exact = a.kl_est == RL_KL_EXACT;
+    const float kl = exact ? klx : (llq - logP_lab);
+    const float A = a.adv[t];
+    const float at = a.adv_tau * A;
+    float loss = -at * (wl.w * logP_lab - cen) + beta * kl;
+    // d loss / d z_j = d * P_j + spikes; d multiplies the (full or renormalised) softmax
+    const float d = at * (wl.w - C) + beta * (exact ? U : 1.f);
+    float labc = -at * wl.w - (exact ? 0.f : beta);
+    float dco = rep ? 0.f : d;
+    const bool eligible = rep || (a.loss_type == RL_LOSS_REINFORCE && beta == 0.f);
+    if (a.sparse) {
+        if (eligible)
+            dco = 0.f;
+        else if (rl && lane == 0)
+            set_status(a.status, RL_STATUS_SPARSE_INELIGIBLE);
+    }
+    if (!rl) {
+        loss = 0.f;
+        dco = 0.f;
+        labc = 0.f;
+    }
+
+    // pass 2: spike coefficient per entry (same lane touches the same j as in pass 1)
+    for (int64_t j = b + lane; j < e; j += 32) {
+        float ec = 0.f;
+        if (rl) {
+            const int32_t id = a.ids[j];
+            const float lq = a.logq[j];
+            const bool ok = id >= 0 && id < a.V && isfinite(lq);
+            if (ok) {
+                const float c = a.sv.entcoef[j];
+                const float uj = rep ? expf(lq) : inv_K;
+                ec = at * c - (exact ? beta * uj : 0.f);
+                if (rep) ec = fmaf(d, expf(a.zsup[j] - lse_s), ec);
+            }
+        }
+        a.sv.entcoef[j] = ec;
+    }
+
+    if (lane == 0) {
+        a.loss[t] = loss;
+        if (a.logp_label) a.logp_label[t] = logP_lab;
+        if (a.entropy) a.entropy[t] = ent;
+        if (a.lse_out) a.lse_out[t] = lse;
+        if (a.mask_label) a.mask_label[t] = wl.keep ? 1 : 0;
+        a.sv.lse[t] = lse;
+        a.sv.lse_s[t] = lse_s;
+        a.sv.dcoef[t] = dco;
+        a.sv.labcoef[t] = labc;
+        float* mt = a.sv.mterm + t * 8;
+        int flags = 0;
+        if (rl) {
+            flags = 1 | (wl.keep ? 0 : 2) | (wl.low ? 4 : 0) | (wl.high ? 8 : 0) | (age == 0 ? 16 : 0);
+        }
+        mt[0] = loss;
+        mt[1] = llq - logP_lab;
+        mt[2] = smass;
+        mt[3] = mtv;
+        mt[4] = kl;
+        mt[5] = beta;
+        mt[6] = ent;
+        mt[7] = __int_as_float(flags);
+        if (!isfinite(lse) || !isfinite(loss)) set_status(a.status, RL_STATUS_NONFINITE);
+    }
+}
+
+// ----------------------------------------------------------------------------------
+// 4. Deterministic metric reduction
+// ----------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) metrics_partial_kernel(const float* mterm, int64_t N,
+                                                              double* part) {
+    __shared__ double sh[256];
+    const int64_t per = (N + gridDim.x - 1) / gridDim.x;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * per;
+    const int64_t t1 = t0 + per < N ? t0 + per : N;
+    double acc[kMetricFields];
+#pragma unroll
+    for (int k = 0; k < kMetricFields; ++k) acc[k] = 0.0;
+    for (int64_t t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
+        const float* mt = mterm + t * 8;
+        const int flags = __float_as_int(mt[7]);
+        if (!(flags & 1)) continue;
+        acc[0] += mt[0];
+        acc[1] += mt[1];
+        acc[2] += mt[2];
+        acc[3] += mt[3];
+        acc[4] += mt[4];
+        acc[5] += mt[5];
+        if (flags & 16) acc[6] += mt[4];
+        acc[7] += mt[6];
+        acc[8] += 1.0;
+        acc[9] += (flags & 2) ? 1.0 : 0.0;
+        acc[10] += (flags & 4) ? 1.0 : 0.0;
+        acc[11] += (flags & 8) ? 1.0 : 0.0;
+        acc[12] += (flags & 16) ? 1.0 : 0.0;
+    }
+    for (int k = 0; k < kMetricFields; ++k) {
+        sh[threadIdx.x] = acc[k];
+        __syncthreads();
+        for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+            if (threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
+            __syncthreads();
+        }
+        if (threadIdx.x == 0) part[blockIdx.x * kMetricFields + k] = sh[0];
+        __syncthreads();
+    }
+}
+
+__global__ void metrics_final_kernel(const double* part, int nblk, rl_head_metrics* out) {
+    const int k = threadIdx.x;
+    if (k >= kMetricFields) return;
+    double s = 0.0;
+    for (int b = 0; b < nblk; ++b) s += part[b * kMetricFields + k];
+    switch (k) {
+        case 0: out->loss = s; break;
+        case 1: out->mismatch_kl = s; break;
+        case 2: out->support_mass = s; break;
+        case 3: out->mask_tv = s; break;
+        case 4: out->kl = s; break;
+        case 5: out->beta = s; break;
+        case 6: out->kl_age0 = s; break;
+        case 7: out->entropy = s; break;
+        case 8: out->n_rl = static_cast<int64_t>(s); break;
+        case 9: out->masked = static_cast<int64_t>(s); break;
+        case 10: out->masked_low = static_cast<int64_t>(s); break;
+        case 11: out->masked_high = static_cast<int64_t>(s); break;
+        case 12: out->n_age0 = static_cast<int64_t>(s); break;
+        case 13: out->reserved = 0; break;
+        default: break;
+    }
+}
+
+int metrics_impl(const rl_head_batch* b, const void* saved, rl_head_metrics* metrics, void* ws,
+                 cudaStream_t stream) {
+    const SavedView sv = saved_view(const_cast<void*>(saved), b->N, b->support.nnz, nullptr);
+    const FwdWs w = fwd_ws_view(ws, b->N, b->H, b->V, b->support.nnz, nullptr);
+    metrics_partial_kernel<<<kMetricBlocks, 256, 0, stream>>>(sv.mterm, b->N, w.mpart);
+    metrics_final_kernel<<<1, 32, 0, stream>>>(w.mpart, kMetricBlocks, metrics);
+    count_launch(2);
+    return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------------------------
+// Entry
+// ----------------------------------------------------------------------------------
+int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out,
+                  void* saved, void* ws, int32_t* status, cudaStream_t stream) {
+    const int64_t N = b->N, H = b->H, V = b->V, nnz = b->support.nnz;
+    int rc = validate_impl(b, status, stream);
+    if (rc != RL_OK) return rc;
+    if (N == 0) return RL_OK;
+    const SavedView sv = saved_view(saved, N, nnz, nullptr);
+    const FwdWs w = fwd_ws_view(ws, N, H, V, nnz, nullptr);
+    const int S = choose_splits(N, V);
+
+    CUtensorMap tmX, tmW;
+    rc = make_tmap_bf16(&tmX, b->hidden, N, H, H, kBM);
+    if (rc != RL_OK) return rc;
+    rc = make_tmap_bf16(&tmW, b->weight, V, H, H, kBN);
+    if (rc != RL_OK) return rc;
+    const GemmPlan plan = make_plan(N, V, H, 1, S, 1, status);
+    EpiStats::Params ep{N,
+                        static_cast<int32_t>(V),
+                        1.0f / prm->temperature,
+                        nnz,
+                        b->labels,
+                        b->support.offsets,
+                        b->support.ids,
+                        w.zlab,
+                        w.zsup,
+                        w.part_m,
+                        w.part_s,
+                        w.part_u};
+    rc = launch_gemm<EpiStats>(tmX, tmX, tmW, plan, ep, stream);
+    count_launch();
+    if (rc != RL_OK) return rc;
+
+    TokenArgs ta;
+    ta.N = N;
+    ta.V = static_cast<int32_t>(V);
+    ta.S = plan.n_splits;
+    ta.nnz = nnz;
+    ta.part_m = w.part_m;
+    ta.part_s = w.part_s;
+    ta.part_u = w.part_u;
+    ta.zlab = w.zlab;
+    ta.zsup = w.zsup;
+    ta.labels = b->labels;
+    ta.label_logq = b->label_logq;
+    ta.adv = b->adv;
+    ta.loss_mask = b->loss_mask;
+    ta.age = b->age;
+    ta.offsets = b->support.offsets;
+    ta.ids = b->support.ids;
+    ta.logq = b->support.logq;
+    ta.replayed = b->support.replayed;
+    ta.loss_type = prm->loss_type;
+    ta.kl_est = prm->kl_estimator;
+    ta.kl_stale = prm->kl_staleness;
+    ta.sparse = !bwd_is_dense(prm);
+    ta.eps = prm->eps;
+    ta.cap = prm->max_importance_ratio;
+    ta.lo = prm->icepop_low;
+    ta.hi = prm->icepop_high;
+    ta.adv_tau = prm->adv_tau;
+    ta.kl_coeff = prm->kl_coeff;
+    ta.loss = out->loss;
+    ta.logp_label = out->logp_label;
+    ta.logp_support = out->logp_support;
+    ta.entropy = out->entropy;
+    ta.lse_out = out->lse;
+    ta.mask_label = out->mask_label;
+    ta.mask_support = out->mask_support;
+    ta.sv = sv;
+    ta.status = status;
+    token_loss_kernel<<<static_cast<unsigned>((N + 7) / 8), 256, 0, stream>>>(ta);
+    count_launch();
+    if (cudaPeekAtLastError() != cudaSuccess) return RL_ERR_CUDA;
+    if (out->metrics) return metrics_impl(b, saved, out->metrics, ws, stream);
+    return RL_OK;
+}
+
+}  // namespace rl

@@ -1,0 +1,95 @@
+// Host-side declarations shared by the translation units of librlhead.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/rlhead.h"
+
+namespace rl {
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Bump allocator over a caller-provided buffer (or a null base when only measuring).
+struct Carve {
+    uint8_t* base;
+    size_t off = 0;
+    explicit Carve(void* b) : base(static_cast<uint8_t*>(b)) {}
+    template <class T>
+    T* take(size_t count) {
+        off = align_up(off, 256);
+        T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+        off += count * sizeof(T);
+        return p;
+    }
+};
+
+// Forward -> backward saved state (caller-owned).
+struct SavedView {
+    float* lse;       // [N] full-vocab logsumexp of z
+    float* lse_s;     // [N] logsumexp over the support on replayed rows (= lse otherwise)
+    float* dcoef;     // [N] coefficient of the dense softmax term P_full (0 on replayed rows)
+    float* labcoef;   // [N] coefficient of the spike at the label
+    float* entcoef;   // [nnz] coefficient of the spike at each support entry
+    float* mterm;     // [N, 8] per-token metric terms
+};
+SavedView saved_view(void* base, int64_t N, int64_t nnz, size_t* bytes);
+
+struct FwdWs {
+    int splits;
+    float* part_m;    // [splits, N]
+    float* part_s;
+    float* part_u;
+    float* zlab;      // [N]
+    float* zsup;      // [nnz]
+    double* mpart;    // metric partials
+};
+FwdWs fwd_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz, size_t* bytes);
+constexpr int kMetricBlocks = 128;
+constexpr int kMetricFields = 16;
+
+struct BwdWs {
+    int64_t chunk;        // tokens per chunk (multiple of 128)
+    bool dense;
+    bool split;
+    void* Wt;             // [H, V] bf16 (dense)
+    void* Xt;             // [H, chunk] bf16 (dense)
+    void* G;              // [chunk, V] bf16 (dense)       (hi)
+    void* Gt;             // [V, chunk] bf16 (dense)       (hi)
+    void* G_lo;           // split only
+    void* Gt_lo;
+    float* dxs;           // [N, H] fp32 sparse part of dX
+    int32_t* item_tok;    // [nnz + N] token of each gradient item
+    int32_t* keys_a;      // radix-sort double buffers (vocab id keys, item payloads)
+    int32_t* vals_a;
+    int32_t* keys_b;
+    int32_t* vals_b;
+    int32_t* hist;        // [tiles, 512]
+    int64_t* bucket;      // [V + 1] start of each vocab id's items after the sort
+};
+BwdWs bwd_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz,
+                  const rl_params* prm, size_t* bytes);
+bool bwd_is_dense(const rl_params* prm);
+
+void count_launch(int n = 1);
+void set_last_error(const char* msg);
+int num_sms();
+
+int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out,
+                  void* saved, void* ws, int32_t* status, cudaStream_t stream);
+int metrics_impl(const rl_head_batch* b, const void* saved, rl_head_metrics* metrics, void* ws,
+                 cudaStream_t stream);
+int validate_impl(const rl_head_batch* b, int32_t* status, cudaStream_t stream);
+int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* saved,
+                  const float* dloss, void* dhidden, float* dW, int accumulate, void* ws,
+                  int32_t* status, cudaStream_t stream);
+int policy_impl(const float* lt, const float* lo, const float* ls, const float* adv,
+                const uint8_t* mask, int64_t T, const rl_pg_params* p, float* loss_ppo,
+                float* loss_dec, float* grad_ppo, float* grad_dec, rl_pg_metrics* metrics,
+                void* ws, cudaStream_t stream);
+size_t policy_ws_bytes(int64_t T);
+int gemm_util_impl(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* D,
+                   int32_t* status, cudaStream_t stream);
+
+}  // namespace rl

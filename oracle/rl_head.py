@@ -216,7 +216,7 @@ def head_forward(inputs: dict, p: HeadParams, rows=None, chunk: int = 64) -> dic
                                     "kl", "beta", "center")}
     out["mask_label"] = np.zeros(n, dtype=np.uint8)
     ent_lp, ent_mask, ent_w, ent_c, ent_u = [], [], [], [], []
-    met = dict(n_rl=0, mismatch_kl=0.0, masked=0, masked_low=0, masked_high=0, support_mass=0.0,
+    met = dict(n_rl=0, loss=0.0, mismatch_kl=0.0, masked=0, masked_low=0, masked_high=0, support_mass=0.0,
                mask_tv=0.0, kl=0.0, beta=0.0, kl_age0=0.0, n_age0=0, entropy=0.0)
     for c0 in range(0, n, chunk):
         rr = rows[c0:c0 + chunk]
@@ -240,6 +240,7 @@ def head_forward(inputs: dict, p: HeadParams, rows=None, chunk: int = 64) -> dic
             ent_u.append(fw["u"])
             if rl:
                 met["n_rl"] += 1
+                met["loss"] += fw["loss"]
                 met["mismatch_kl"] += fw["mismatch_kl"]
                 met["masked"] += 0 if fw["keep_label"] else 1
                 met["masked_low"] += int(fw["low_label"])

@@ -1,0 +1,109 @@
+"""Tolerances and comparison helpers for the GPU-vs-oracle parity tests.
+
+The bars (stated for this path): logprobs within 1e-5 absolute; loss within 1e-4
+relative; masks, gathers and masked counts bit-exact; gradients within 2 bf16 ulp of
+the oracle rounded to bf16.  Readings of the gradient bar:
+  element  |gpu - bf16(ref)| <= 2 ulp(max(|ref|, 2^-8 * rowmax|ref|))  (grad_precision SPLIT)
+  row      max_h |gpu - bf16(ref)| <= 2 ulp(rowmax|ref|)                 (grad_precision BF16)
+where a row is one token of dX or one vocabulary id of dW.
+"""
+import math
+
+import numpy as np
+import torch
+
+import lm_head_gb300 as rh
+import oracle
+
+LOGP_TOL = 1e-5
+LOSS_REL = 1e-4
+
+
+def f32(x):
+    return float(np.float32(x))
+
+
+def oracle_params(hp: rh.HeadParams) -> oracle.HeadParams:
+    """The oracle sees the knobs exactly as the GPU does (fp32-rounded)."""
+    return oracle.HeadParams(loss_type=hp.loss_type, eps=f32(hp.eps),
+                             max_importance_ratio=f32(hp.max_importance_ratio),
+                             icepop_low=f32(hp.icepop_low), icepop_high=f32(hp.icepop_high),
+                             adv_tau=f32(hp.adv_tau), temperature=f32(hp.temperature),
+                             kl_coeff=f32(hp.kl_coeff), kl_estimator=hp.kl_estimator,
+                             kl_staleness=hp.kl_staleness)
+
+
+def ulp_bf16(x):
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(x, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def to_bf16(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def grad_check(gpu, ref, reading: str, what: str):
+    """Assert the gradient bar; returns the worst ratio err / allowed."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rb = to_bf16(ref)
+    err = np.abs(gpu - rb)
+    rowmax = np.max(np.abs(ref), axis=1, keepdims=True)
+    if reading == "element":
+        allowed = 2 * ulp_bf16(np.maximum(np.abs(ref), 2.0 ** -8 * rowmax))
+        ratio = err / allowed
+    else:
+        allowed = 2 * ulp_bf16(rowmax)
+        ratio = np.max(err, axis=1, keepdims=True) / allowed
+    ratio = np.where(rowmax > 0, ratio, np.where(np.max(err, axis=1, keepdims=True) > 0, np.inf, 0.0))
+    worst = float(np.max(ratio)) if ratio.size else 0.0
+    assert worst <= 1.0, f"{what}: worst err/allowed = {worst:.3f} ({reading} reading)"
+    return worst
+
+
+def loss_prop_tol(ref: dict, inp: dict, op: oracle.HeadParams):
+    """Per-token loss bar: the 1e-5 log-prob bar carried through the loss to first order,
+    |d loss_t| <= |adv_tau A_t| (|w_a| + sum_e |c_e|) * 1e-5 + beta_t * (sum_e u_e or 1) * 1e-5,
+    doubled.  (A per-token loss is a difference of O(1) log-prob terms, so where it
+    cancels a relative bar alone cannot hold.)"""
+    off = np.asarray(inp["offsets"], np.int64)
+    abs_c = np.add.reduceat(np.abs(ref["c_support"]), off[:-1]) if ref["c_support"].size else np.zeros(len(off) - 1)
+    sum_u = np.add.reduceat(ref["u_support"], off[:-1]) if ref["u_support"].size else np.zeros(len(off) - 1)
+    empty = off[1:] == off[:-1]
+    abs_c = np.where(empty, 0.0, abs_c)
+    sum_u = np.where(empty, 0.0, sum_u)
+    kl_w = sum_u if op.kl_estimator == oracle.KL_EXACT else np.ones_like(sum_u)
+    A = np.abs(op.adv_tau * np.asarray(inp["adv"], np.float64))
+    return 2 * LOGP_TOL * (A * (np.abs(ref["w_label"]) + abs_c) + np.asarray(ref["beta"]) * kl_w)
+
+
+def loss_check(gpu, ref, prop_tol=None, what="loss"):
+    """Aggregate loss within 1e-4 relative; per token within 1e-4 relative plus the
+    propagated log-prob bar."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    tol = LOSS_REL * np.abs(ref) + (0.0 if prop_tol is None else np.asarray(prop_tol, np.float64))
+    worst = float(np.max(np.abs(gpu - ref) / np.maximum(tol, 1e-30))) if ref.size else 0.0
+    assert worst <= 1.0, f"{what}: worst err/allowed {worst:.3e}"
+    tot_g, tot_r = float(gpu.sum()), float(ref.sum())
+    assert abs(tot_g - tot_r) <= LOSS_REL * max(abs(tot_r), 1e-12) + 1e-6, (tot_g, tot_r)
+    return worst
+
+
+def weight_keep_fp64(logP, logq, op: oracle.HeadParams):
+    """fp64 keep predicate of the oracle, evaluated on given (fp32) log-probs."""
+    _, keep, _, _ = oracle.rl_head.rl_weight(np.asarray(logP, np.float64), np.asarray(logq, np.float64), op)
+    return keep.astype(np.uint8)
+
+
+def margin(logP, logq, op: oracle.HeadParams):
+    """Distance of each pair from its nearest mask threshold (in the predicate's units)."""
+    logP = np.asarray(logP, np.float64)
+    logq = np.asarray(logq, np.float64)
+    if op.loss_type == oracle.LOSS_IPO:
+        return np.abs(np.abs(np.exp(logP) - np.exp(logq)) - op.eps)
+    if op.loss_type == oracle.LOSS_ICEPOP:
+        r = np.exp(logP - logq)
+        return np.minimum(np.abs(r - op.icepop_low), np.abs(r - op.icepop_high)) / np.maximum(r, 1e-30)
+    return np.full(logP.shape, np.inf)

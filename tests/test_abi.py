@@ -1,0 +1,95 @@
+"""CPU checks of the C-ABI library: it loads, exports every function include/rlhead.h
+declares, sizes its workspaces, and rejects bad host-side arguments before touching a
+GPU (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import lm_head_gb300 as rh
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(rl_\w+)\s*\(", text, flags=re.M):
+            names.append(m.group(1))
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from lm_head_gb300 import build
+    build.build()
+    return rh.load()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for n in ("rl_head_loss_fwd", "rl_head_loss_bwd", "rl_mismatch_metrics", "rl_policy_loss_elementwise",
+              "rl_validate_support", "rl_status_read"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(rh.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_struct_sizes_match_the_header_layout():
+    assert ctypes.sizeof(rh.RlParams) == 14 * 4
+    assert ctypes.sizeof(rh.RlHeadMetrics) == 8 * 8 + 6 * 8
+    assert ctypes.sizeof(rh.RlPgMetrics) == 6 * 8 + 6 * 8 + 16 * 8
+
+
+def test_workspace_queries(lib):
+    p = rh.HeadParams()
+    assert rh.rl_head_saved_bytes(256, 4096) >= 256 * 4 * 4 + 4096 * 4 + 256 * 32
+    f = rh.rl_head_fwd_workspace_bytes(65536, 2048, 151936, 1 << 20, p)
+    assert f >= (65536 * 3 * 4) + (1 << 20) * 4
+    dense = rh.rl_head_bwd_workspace_bytes(65536, 2048, 151936, 1 << 20, rh.HeadParams(bwd_mode=rh.RL_BWD_DENSE))
+    sparse = rh.rl_head_bwd_workspace_bytes(65536, 2048, 151936, 1 << 20, rh.HeadParams(bwd_mode=rh.RL_BWD_SPARSE))
+    assert dense > 151936 * 2048 * 2 > sparse > 0
+    assert rh.rl_policy_workspace_bytes(3_600_000) > 0
+
+
+def _batch(N=256, H=128, V=1024, nnz=10):
+    fake = 1 << 20   # never dereferenced: the host checks fail first
+    sup = rh.RlSupport(fake, fake, fake, fake, nnz)
+    return rh.RlHeadBatch(fake, fake, N, H, V, fake, fake, fake, None, None, sup)
+
+
+def _fwd(lib, batch, params, ws_bytes=1 << 40):
+    outs = rh.RlHeadOutputs(1 << 20, None, None, None, None, None, None, None)
+    return lib.rl_head_loss_fwd(ctypes.byref(batch) if batch is not None else None,
+                                ctypes.byref(params) if params is not None else None, ctypes.byref(outs),
+                                ctypes.c_void_p(1 << 20), ctypes.c_void_p(1 << 20), ws_bytes,
+                                ctypes.c_void_p(1 << 20), None)
+
+
+def test_bad_arguments_are_rejected_on_the_host(lib):
+    good = rh.HeadParams().c()
+    assert _fwd(lib, None, good) == rh.RL_ERR_ARG
+    assert _fwd(lib, _batch(), None) == rh.RL_ERR_ARG
+    assert _fwd(lib, _batch(H=100), good) == rh.RL_ERR_UNSUPPORTED
+    assert _fwd(lib, _batch(V=1001), good) == rh.RL_ERR_UNSUPPORTED
+    assert _fwd(lib, _batch(N=-1), good) == rh.RL_ERR_ARG
+    for field, val in (("temperature", 0.0), ("eps", -0.1), ("loss_type", 7), ("icepop_low", 3.0),
+                       ("token_chunk", 100), ("kl_coeff", -1.0)):
+        bad = rh.HeadParams().c()
+        setattr(bad, field, val)
+        assert _fwd(lib, _batch(), bad) == rh.RL_ERR_ARG, field
+    assert _fwd(lib, _batch(), good, ws_bytes=16) == rh.RL_ERR_WORKSPACE
+    assert lib.rl_status_read(None, None) == rh.RL_ERR_ARG
+    assert lib.rl_error_string(rh.RL_ERR_WORKSPACE) == b"workspace too small"
+    pp = rh.PgParams(clip_ratio_c=0.5).c()
+    assert lib.rl_policy_loss_elementwise(None, None, None, None, None, 10, ctypes.byref(pp), None, None, None,
+                                          None, None, None, 0, None) == rh.RL_ERR_ARG

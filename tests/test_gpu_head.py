@@ -1,0 +1,215 @@
+"""GPU parity of the fused LM head + RL loss (through the C-ABI) against the fp64 oracle.
+
+Inputs come from the seeded generators in workloads/ (the same tensors feed both sides).
+Sizes here are ones the oracle finishes in seconds while still spanning several 128 x 256
+tensor-core tiles and a ragged tail.
+"""
+import numpy as np
+import pytest
+import torch
+
+import lm_head_gb300 as rh
+import oracle
+import workloads
+from parity_util import (LOGP_TOL, grad_check, loss_check, loss_prop_tol, margin, oracle_params,
+                         weight_keep_fp64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from lm_head_gb300 import build
+    build.build()
+    rh.load()
+
+
+def _forward(case, hp):
+    dev = case.to("cuda")
+    batch = rh.HeadBatch.from_case(dev)
+    fwd = rh.rl_head_loss_fwd(batch, hp)
+    torch.cuda.synchronize()
+    return dev, batch, fwd
+
+
+def check_forward(case, hp, fwd, ref):
+    """Compare every forward output; returns the oracle result for reuse."""
+    st = fwd.status_bits()
+    assert st == 0, rh.status_names(st)
+    op = oracle_params(hp)
+    g_lse = fwd.lse.cpu().double().numpy()
+    np.testing.assert_allclose(g_lse, ref["lse"], atol=LOGP_TOL, rtol=0)
+    np.testing.assert_allclose(fwd.entropy.cpu().double().numpy(), ref["entropy"], atol=LOGP_TOL, rtol=0)
+    g_lab = fwd.logp_label.cpu().double().numpy()
+    np.testing.assert_allclose(g_lab, ref["logp_label"], atol=LOGP_TOL, rtol=0)
+    g_sup = fwd.logp_support.cpu().double().numpy()
+    np.testing.assert_allclose(g_sup, ref["logp_support"], atol=LOGP_TOL, rtol=0)
+    inp = case.numpy()
+    # masks: bit-exact against the oracle's fp64 predicate on the GPU's log-probs ...
+    gm_lab = fwd.mask_label.cpu().numpy()
+    gm_sup = fwd.mask_support.cpu().numpy()
+    np.testing.assert_array_equal(gm_lab, weight_keep_fp64(fwd.logp_label.cpu().numpy(), inp["label_logq"], op))
+    np.testing.assert_array_equal(gm_sup, weight_keep_fp64(fwd.logp_support.cpu().numpy(), inp["logq"], op))
+    # ... and against the oracle's own masks except within the log-prob tolerance of a threshold
+    near_lab = margin(ref["logp_label"], inp["label_logq"], op) < 4 * LOGP_TOL
+    near_sup = margin(ref["logp_support"], inp["logq"], op) < 4 * LOGP_TOL
+    assert np.all((gm_lab == ref["mask_label"]) | near_lab)
+    assert np.all((gm_sup == ref["mask_support"]) | near_sup)
+    # loss
+    mask = inp["loss_mask"].astype(bool)
+    ptol = loss_prop_tol(ref, inp, op)
+    loss_check(fwd.loss.cpu().double().numpy()[mask], ref["loss"][mask], ptol[mask])
+    assert np.all(fwd.loss.cpu().numpy()[~mask] == 0)
+    # metrics: counts equal the counts of the GPU's own masks; sums within tolerance
+    gm = fwd.metrics()
+    rm = ref["metrics"]
+    assert gm["n_rl"] == rm["n_rl"] == int(mask.sum())
+    assert gm["masked"] == int(((gm_lab == 0) & mask).sum())
+    flips = int(((gm_lab != ref["mask_label"]) & mask).sum())
+    assert abs(gm["masked"] - rm["masked"]) <= flips
+    assert gm["n_age0"] == rm["n_age0"]
+    for k in ("loss", "mismatch_kl", "support_mass", "mask_tv", "kl", "beta", "kl_age0", "entropy"):
+        tol = 1e-4 * max(abs(rm[k]), 1e-3 * rm["n_rl"]) + 1e-5 * rm["n_rl"] * (1 if k in ("mismatch_kl", "kl") else 0)
+        if k == "mask_tv":
+            tol += 2.0 * flips
+        assert abs(gm[k] - rm[k]) <= tol, (k, gm[k], rm[k])
+    return ref
+
+
+def check_backward(case, hp, batch, fwd, reading, dloss=None, rows_only=None):
+    inp = case.numpy()
+    op = oracle_params(hp)
+    mask = inp["loss_mask"].astype(bool)
+    if dloss is None:
+        dloss = mask.astype(np.float32) / max(int(mask.sum()), 1)   # token mean over RL tokens
+    dl = torch.from_numpy(np.asarray(dloss, np.float32)).cuda()
+    dX, dW, st = rh.rl_head_loss_bwd(batch, hp, fwd.saved, dl)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, rh.status_names(int(st.item()))
+    rX, rW = oracle.head_backward(inp, op, np.asarray(dloss, np.float64))
+    wx = grad_check(dX.float().cpu().numpy(), rX, reading, "dX")
+    ww = grad_check(dW.cpu().numpy(), rW, reading, "dW")
+    return dX, dW, (wx, ww)
+
+
+C1_IPO = dict(loss_type=rh.RL_LOSS_IPO, eps=0.3, max_importance_ratio=10.0, kl_coeff=0.0)
+
+
+def test_c1_forward_and_dense_backward():
+    """The tiny config: N=256, H=128, V=1024, K=16 draws, ipo eps 0.3, dense backward."""
+    case = workloads.make_head_case("c1")
+    hp = rh.HeadParams(**C1_IPO, bwd_mode=rh.RL_BWD_DENSE)
+    dev, batch, fwd = _forward(case, hp)
+    ref = oracle.head_forward(case.numpy(), oracle_params(hp))
+    check_forward(case, hp, fwd, ref)
+    check_backward(case, hp, batch, fwd, "row")
+
+
+@pytest.mark.parametrize("loss_type", [rh.RL_LOSS_IPO, rh.RL_LOSS_ICEPOP, rh.RL_LOSS_REINFORCE])
+def test_c1_mask_stress(loss_type):
+    """c1 shapes with sharp logits and a noisy sampler, so masks and caps are exercised;
+    ragged token count, some non-RL tokens, exact KL with inv_sqrt staleness."""
+    case = workloads.make_head_case("c1", n_tokens=300, hidden_scale=10.0, noise=1.0, loss_mask_frac=0.1,
+                                    age_max=4, seed=11 + loss_type)
+    hp = rh.HeadParams(loss_type=loss_type, eps=0.2, max_importance_ratio=2.0, icepop_low=0.5, icepop_high=2.0,
+                       adv_tau=0.7, kl_coeff=0.05, kl_estimator=rh.RL_KL_EXACT,
+                       kl_staleness=rh.RL_STALE_INV_SQRT, bwd_mode=rh.RL_BWD_DENSE)
+    dev, batch, fwd = _forward(case, hp)
+    ref = oracle.head_forward(case.numpy(), oracle_params(hp))
+    check_forward(case, hp, fwd, ref)
+    assert 0 < int(fwd.mask_support.sum()) < case.nnz or loss_type == rh.RL_LOSS_REINFORCE
+    check_backward(case, hp, batch, fwd, "row")
+
+
+def test_c1_split_precision_meets_element_reading():
+    case = workloads.make_head_case("c1", n_tokens=200, hidden_scale=4.0, noise=0.5, seed=21)
+    hp = rh.HeadParams(**C1_IPO, bwd_mode=rh.RL_BWD_DENSE, grad_precision=rh.RL_GRAD_SPLIT)
+    dev, batch, fwd = _forward(case, hp)
+    ref = oracle.head_forward(case.numpy(), oracle_params(hp))
+    check_forward(case, hp, fwd, ref)
+    check_backward(case, hp, batch, fwd, "element")
+
+
+def test_k1_estimator_and_temperature():
+    case = workloads.make_head_case("c1", n_tokens=130, hidden_scale=3.0, noise=0.3, temperature=0.7, seed=31)
+    hp = rh.HeadParams(loss_type=rh.RL_LOSS_ICEPOP, kl_coeff=0.1, kl_estimator=rh.RL_KL_K1, temperature=0.7,
+                       bwd_mode=rh.RL_BWD_DENSE)
+    dev, batch, fwd = _forward(case, hp)
+    ref = oracle.head_forward(case.numpy(), oracle_params(hp))
+    check_forward(case, hp, fwd, ref)
+    check_backward(case, hp, batch, fwd, "row")
+
+
+@pytest.mark.parametrize("loss_type", [rh.RL_LOSS_IPO, rh.RL_LOSS_REINFORCE])
+def test_replayed_support_sparse_equals_dense_and_oracle(loss_type):
+    """Replayed top-p supports (u = q, renormalised P): the sparse CSR-matmul backward
+    matches the dense one to fp32 rounding and both match the oracle."""
+    case = workloads.make_head_case("c1", n_tokens=260, support="replay", top_p=0.9, hidden_scale=6.0,
+                                    noise=0.3, seed=41 + loss_type)
+    base = dict(loss_type=loss_type, eps=0.3, kl_coeff=0.02, all_replayed=1)
+    hp_d = rh.HeadParams(**base, bwd_mode=rh.RL_BWD_DENSE)
+    hp_s = rh.HeadParams(**base, bwd_mode=rh.RL_BWD_SPARSE)
+    dev, batch, fwd_d = _forward(case, hp_d)
+    ref = oracle.head_forward(case.numpy(), oracle_params(hp_d))
+    check_forward(case, hp_d, fwd_d, ref)
+    dXd, dWd, _ = check_backward(case, hp_d, batch, fwd_d, "row")
+    fwd_s = rh.rl_head_loss_fwd(batch, hp_s)
+    dXs, dWs, _ = check_backward(case, hp_s, batch, fwd_s, "row")
+    torch.testing.assert_close(dWs, dWd, rtol=1e-5, atol=1e-7)
+    torch.testing.assert_close(dXs.float(), dXd.float(), rtol=1e-2, atol=1e-6)
+
+
+def test_reinforce_draws_sparse_without_kl():
+    case = workloads.make_head_case("c1", n_tokens=256, K=8, seed=51)
+    hp = rh.HeadParams(loss_type=rh.RL_LOSS_REINFORCE, kl_coeff=0.0)   # AUTO -> sparse
+    dev, batch, fwd = _forward(case, hp)
+    ref = oracle.head_forward(case.numpy(), oracle_params(hp))
+    check_forward(case, hp, fwd, ref)
+    check_backward(case, hp, batch, fwd, "element")
+
+
+def test_determinism_bitwise():
+    case = workloads.make_head_case("c1", n_tokens=300, hidden_scale=5.0, noise=0.5, seed=61)
+    hp = rh.HeadParams(loss_type=rh.RL_LOSS_IPO, kl_coeff=0.01, bwd_mode=rh.RL_BWD_DENSE)
+    dev, batch, f1 = _forward(case, hp)
+    f2 = rh.rl_head_loss_fwd(batch, hp)
+    dl = torch.full((case.N,), 1.0 / case.N, device="cuda")
+    a = rh.rl_head_loss_bwd(batch, hp, f1.saved, dl)
+    b = rh.rl_head_loss_bwd(batch, hp, f2.saved, dl)
+    torch.cuda.synchronize()
+    assert torch.equal(f1.loss, f2.loss) and torch.equal(f1.logp_support, f2.logp_support)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_corrupt_support_sets_status_bits_without_trapping():
+    case = workloads.make_head_case("c1", n_tokens=128, support="replay", top_p=0.9, hidden_scale=6.0, seed=71)
+    hp = rh.HeadParams(loss_type=rh.RL_LOSS_IPO, all_replayed=1)
+    bad = case.to("cuda")
+    ids = bad.ids.clone()
+    ids[3] = case.V + 5                     # out-of-range id
+    offsets = bad.offsets.clone()
+    logq = bad.logq.clone()
+    logq[0] = float("nan")                  # non-finite log q
+    labels = bad.labels.clone()
+    r = 7                                   # a replayed row whose label is not in its support
+    row = ids[int(offsets[r]):int(offsets[r + 1])].cpu().tolist()
+    labels[r] = next(v for v in range(case.V) if v not in row)
+    batch = rh.HeadBatch(bad.hidden, bad.W, labels, bad.label_logq, bad.adv, offsets, ids, logq, bad.replayed)
+    fwd = rh.rl_head_loss_fwd(batch, hp)
+    torch.cuda.synchronize()
+    names = rh.status_names(fwd.status_bits())
+    for n in ("ID_RANGE", "LOGQ", "LABEL_MISSING"):
+        assert n in names, names
+    # offsets that run past nnz: flagged, and no out-of-bounds access brings the context down
+    off2 = offsets.clone()
+    off2[-1] = off2[-1] + 1000
+    b2 = rh.HeadBatch(bad.hidden, bad.W, bad.labels, bad.label_logq, bad.adv, off2, bad.ids, bad.logq, bad.replayed)
+    st = rh.rl_validate_support(b2)
+    torch.cuda.synchronize()
+    assert "OFFSETS" in rh.status_names(int(st.item()))
+    # the context still works
+    ok = rh.rl_head_loss_fwd(rh.HeadBatch.from_case(bad), hp)
+    torch.cuda.synchronize()
+    assert ok.status_bits() == 0

@@ -1,0 +1,90 @@
+"""GPU parity of the elementwise PPO / decoupled-TIS / mismatch path (through the C-ABI)
+against the fp64 oracle, on the 1.8M-token synthetic replay and on edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import lm_head_gb300 as rh
+import oracle
+import workloads
+from parity_util import f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from lm_head_gb300 import build
+    build.build()
+    rh.load()
+
+
+def _oracle_pp(pp: rh.PgParams):
+    return oracle.PolicyParams(clip_ratio_low=f32(pp.clip_ratio_low), clip_ratio_high=f32(pp.clip_ratio_high),
+                               clip_ratio_c=f32(pp.clip_ratio_c), tis_upper=f32(pp.tis_upper),
+                               icepop_low=f32(pp.icepop_low), icepop_high=f32(pp.icepop_high),
+                               curve_eps=tuple(f32(e) for e in pp.curve_eps))
+
+
+def _run(lt, lo, ls, A, m, pp):
+    d = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (lt, lo, ls, A, m)]
+    out = rh.rl_policy_loss_elementwise(*d, pp)
+    torch.cuda.synchronize()
+    return [o.cpu().double().numpy() for o in out[:4]], rh.pg_metrics(out[4], len(pp.curve_eps))
+
+
+def _compare(lt, lo, ls, A, m, pp):
+    (lp, ld, gp, gd), gm = _run(lt, lo, ls, A, m, pp)
+    ref = oracle.policy_loss_elementwise(lt, lo, ls, A, m, _oracle_pp(pp))
+    rm = ref["metrics"]
+    for g, k in ((lp, "loss_ppo"), (ld, "loss_dec"), (gp, "grad_ppo"), (gd, "grad_dec")):
+        r = ref[k]
+        scale = np.maximum(np.abs(r), 1e-3 * max(float(np.mean(np.abs(r))), 1e-30))
+        assert float(np.max(np.abs(g - r) / scale)) <= 1e-4, k
+    for k in ("n_valid", "n_clip", "n_clip_lower", "icepop_low", "icepop_high", "n_tis_trunc"):
+        assert gm[k] == rm[k], (k, gm[k], rm[k])
+    assert gm["ipo_curve"] == rm["ipo_curve"]
+    n = max(rm["n_valid"], 1)
+    for k in ("loss_ppo", "loss_dec", "tis_sum"):
+        assert abs(gm[k] - rm[k]) <= 1e-4 * max(abs(rm[k]), 1e-3 * n), (k, gm[k], rm[k])
+    for k in ("ppo_kl", "mis_kl", "k3"):
+        assert abs(gm[k] - rm[k]) <= 1e-4 * abs(rm[k]) + 2e-6 * n, (k, gm[k], rm[k])
+    return gm, rm
+
+
+def test_c5_full_size():
+    """1.8M valid tokens, sequences 64-4096 padded to 4096: curve, IcePop band, PPO
+    clip + dual clip, decoupled TIS, mismatch KL."""
+    c = workloads.make_policy_case()
+    gm, rm = _compare(c.lp_theta, c.lp_old, c.lp_samp, c.adv, c.mask, rh.PgParams())
+    assert gm["n_valid"] == 1_800_000
+
+
+@pytest.mark.parametrize("T", [1, 3, 5, 1001])
+def test_ragged_and_scalar_path(T):
+    rng = np.random.default_rng(T)
+    lt = rng.normal(-1, 0.5, T).astype(np.float32)
+    lo = (lt + rng.normal(0, 0.3, T)).astype(np.float32)
+    ls = (lo + rng.normal(0, 0.5, T)).astype(np.float32)
+    A = rng.normal(0, 1, T).astype(np.float32)
+    m = (rng.random(T) < 0.8).astype(np.uint8)
+    _compare(lt, lo, ls, A, m, rh.PgParams())
+
+
+def test_exact_threshold_ties_are_bit_exact():
+    """Ratios placed exactly on / one ulp around every threshold."""
+    vals = []
+    for r in (0.8, 1.2, 2.0, 0.5, 3.0):
+        for d in (-1, 0, 1):
+            x = np.float32(np.log(r))
+            x = np.nextafter(x, np.float32(np.inf) if d > 0 else np.float32(-np.inf)) if d else x
+            vals.append(x)
+    vals = np.array(vals, dtype=np.float32)
+    T = len(vals)
+    lo = np.full(T, -1.0, np.float32)
+    lt = (lo + vals).astype(np.float32)
+    ls = (lo - vals).astype(np.float32)
+    for A in (1.0, -1.0, 0.0):
+        _compare(lt, lo, ls, np.full(T, A, np.float32), np.ones(T, np.uint8), rh.PgParams())
