@@ -233,6 +233,20 @@ int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const
 int rl_gemm_bf16_tn(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* D,
                     int32_t* dev_status, void* stream);
 
+/* Per-kernel timing: when enabled, the library records a CUDA event pair on the caller's
+ * stream around each of its kernel launches, grouped by kind (RL_PROF_* below).
+ * rl_profile_enable(1) also clears the counters.  rl_profile_read waits for the recorded
+ * events, then fills ms[k] (summed device milliseconds) and launches[k] for every kind
+ * k < RL_PROF_KINDS; either pointer may be NULL.  Host arrays. */
+#define RL_PROF_KINDS 14
+enum { RL_PROF_VALIDATE = 0, RL_PROF_GEMM_FWD = 1, RL_PROF_TOKEN_LOSS = 2, RL_PROF_METRICS = 3,
+       RL_PROF_TRANSPOSE = 4, RL_PROF_GEMM_GRAD = 5, RL_PROF_GEMM_DX = 6, RL_PROF_GEMM_DW = 7,
+       RL_PROF_SPARSE_DX = 8, RL_PROF_SPARSE_DW = 9, RL_PROF_POLICY = 10, RL_PROF_GEMM_UTIL = 11,
+       RL_PROF_MEMSET = 12, RL_PROF_OTHER = 13 };
+int rl_profile_enable(int on);
+int rl_profile_read(double* ms, int64_t* launches);
+const char* rl_profile_kind_name(int kind);
+
 /* Synchronous device->host copy of the status word.  Call after the stream is done. */
 int rl_status_read(const int32_t* dev_status, int32_t* host_out);
 /* Kernels this library has launched in this process (for launch accounting). */

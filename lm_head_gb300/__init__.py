@@ -103,6 +103,9 @@ _SIGS = {
     "rl_gemm_bf16_tn": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int64] * 3
                         + [ctypes.c_void_p] * 3),
     "rl_kernel_launch_count": (ctypes.c_int64, []),
+    "rl_profile_enable": (ctypes.c_int, [ctypes.c_int]),
+    "rl_profile_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "rl_profile_kind_name": (ctypes.c_char_p, [ctypes.c_int]),
     "rl_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "rl_last_error": (ctypes.c_char_p, []),
 }
@@ -416,6 +419,23 @@ def rl_status_read(status: torch.Tensor) -> int:
 
 def rl_kernel_launch_count() -> int:
     return int(load().rl_kernel_launch_count())
+
+
+RL_PROF_KINDS = 14
+
+
+def rl_profile_enable(on: bool = True) -> None:
+    _check(load().rl_profile_enable(int(bool(on))))
+
+
+def rl_profile_read() -> dict:
+    """{kind name: (total device ms, launches)} for kinds with launches; syncs on the events."""
+    lib = load()
+    ms = (ctypes.c_double * RL_PROF_KINDS)()
+    n = (ctypes.c_int64 * RL_PROF_KINDS)()
+    _check(lib.rl_profile_read(ctypes.cast(ms, ctypes.c_void_p), ctypes.cast(n, ctypes.c_void_p)))
+    return {lib.rl_profile_kind_name(k).decode(): (float(ms[k]), int(n[k]))
+            for k in range(RL_PROF_KINDS) if n[k] > 0}
 
 
 def status_names(bits: int):

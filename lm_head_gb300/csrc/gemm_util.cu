@@ -43,7 +43,10 @@ int gemm_util_impl(const void* A, const void* B, int64_t M, int64_t N, int64_t K
     if ((rc = make_tmap_bf16(&tb, B, N, K, K, kBN)) != RL_OK) return rc;
     const GemmPlan plan = make_plan(M, N, K, 1, 1 << 30, 1, status);
     EpiStore::Params ep{M, N, D};
-    rc = launch_gemm<EpiStore>(ta, ta, tb, plan, ep, stream);
+    {
+        ProfScope ps(RL_PROF_GEMM_UTIL, stream);
+        rc = launch_gemm<EpiStore>(ta, ta, tb, plan, ep, stream);
+    }
     count_launch();
     return rc;
 }

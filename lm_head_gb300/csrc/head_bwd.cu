@@ -78,6 +78,24 @@ RL_DEVINL uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// The dense softmax-gradient value alpha * exp(z - lse), with every rounding explicit so
+// that the GEMM epilogue and the sparse path compute the same fp32 number.
+RL_DEVINL float dense_alpha(float dloss, float dcoef, float inv_T) {
+    return __fmul_rn(__fmul_rn(dloss, dcoef), inv_T);
+}
+RL_DEVINL float dense_grad(float alpha, float z, float lse) {
+    if (alpha == 0.f) return 0.f;
+    return __fmul_rn(alpha, exp2_approx(__fmul_rn(__fsub_rn(z, lse), kLog2e)));
+}
+// What the bf16 operand(s) of the dense GEMMs drop from g: g - bf16(g), or with the hi/lo
+// split g - hi - lo.  Both differences are exact in fp32.
+RL_DEVINL float dense_residual(float g, bool split) {
+    const float hi = __bfloat162float(__float2bfloat16_rn(g));
+    float r = __fsub_rn(g, hi);
+    if (split) r = __fsub_rn(r, __bfloat162float(__float2bfloat16_rn(r)));
+    return r;
+}
+
 // G = alpha_t * exp(z - lse_t) for the tile, written as G [n, V] (row-major, ld V) and
 // G^T [V, ldt]; with `split`, also the bf16 remainder G - bf16(G) into G_lo / Gt_lo.
 struct EpiGrad {
@@ -104,7 +122,7 @@ struct EpiGrad {
         alpha = 0.f;
         lse = 0.f;
         if (valid) {
-            alpha = p.dloss[t] * p.dcoef[t] * p.inv_T;
+            alpha = dense_alpha(p.dloss[t], p.dcoef[t], p.inv_T);
             lse = p.lse[t];
         }
     }
@@ -113,10 +131,7 @@ struct EpiGrad {
         const int nvalid = p.V - col0 < 32 ? p.V - col0 : 32;  // multiple of 8
         float g[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            const float z = __uint_as_float(acc[k]) * p.inv_T;
-            g[k] = alpha == 0.f ? 0.f : alpha * exp2_approx((z - lse) * kLog2e);
-        }
+        for (int k = 0; k < 32; ++k) g[k] = dense_grad(alpha, __fmul_rn(__uint_as_float(acc[k]), p.inv_T), lse);
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -243,6 +258,7 @@ static int transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld
     if (rows <= 0 || cols <= 0) return RL_OK;
     dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
     if (grid.y > 65535u) return RL_ERR_UNSUPPORTED;
+    ProfScope ps(RL_PROF_TRANSPOSE, s);
     transpose_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(in), rows, cols, ld_in,
                                                static_cast<uint16_t*>(out), ld_out);
     count_launch();
@@ -264,7 +280,32 @@ struct SparseArgs {
     const float* labcoef;
     const float* entcoef;
     float inv_T;
+    // dense mode only (dcoef == nullptr otherwise): what the bf16 GEMM operands dropped at
+    // each spike position is added back here, once per distinct (token, vocab id)
+    const float* dcoef;
+    const float* lse;
+    const float* zlab;
+    const float* zsup;
+    int split;
 };
+
+// True when `v` occurs among ids[b, e) (ascending).
+RL_DEVINL bool row_contains(const int32_t* ids, int64_t b, int64_t e, int32_t v) {
+    int64_t lo = b, hi = e;
+    while (lo < hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (ids[mid] < v)
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    return lo < e && ids[lo] == v;
+}
+
+RL_DEVINL float spike_residual(const SparseArgs& a, float alpha, float z, float lse) {
+    if (alpha == 0.f) return 0.f;
+    return dense_residual(dense_grad(alpha, z, lse), a.split != 0);
+}
 
 RL_DEVINL void fma_row8(float (&acc)[8], const uint16_t* row, float c) {
     const uint4 v = *reinterpret_cast<const uint4*>(row);
@@ -284,14 +325,19 @@ __global__ void __launch_bounds__(256) sparse_dx_kernel(SparseArgs a, float* dxs
     b = b < 0 ? 0 : (b > a.nnz ? a.nnz : b);
     e = e < b ? b : (e > a.nnz ? a.nnz : e);
     const int32_t lab = a.labels[t];
-    const float cl = g * a.labcoef[t];
+    const float alpha = a.dcoef ? dense_alpha(a.dloss[t], a.dcoef[t], a.inv_T) : 0.f;
+    const float lse = alpha != 0.f ? a.lse[t] : 0.f;
+    float cl = g * a.labcoef[t];
+    if (alpha != 0.f && lab >= 0 && lab < a.V && !row_contains(a.ids, b, e, lab))
+        cl += spike_residual(a, alpha, a.zlab[t], lse);
     for (int64_t h0 = static_cast<int64_t>(threadIdx.x) * 8; h0 < a.H; h0 += 256 * 8) {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (g != 0.f) {
             if (lab >= 0 && lab < a.V && cl != 0.f) fma_row8(acc, a.W + lab * a.H + h0, cl);
             for (int64_t j = b; j < e; ++j) {
                 const int32_t id = a.ids[j];
-                const float c = g * a.entcoef[j];
+                float c = g * a.entcoef[j];
+                if (alpha != 0.f && (j == b || a.ids[j - 1] != id)) c += spike_residual(a, alpha, a.zsup[j], lse);
                 if (id >= 0 && id < a.V && c != 0.f) fma_row8(acc, a.W + id * a.H + h0, c);
             }
         }
@@ -443,7 +489,19 @@ __global__ void __launch_bounds__(256) sparse_dw_kernel(SparseArgs a, const int3
             const int32_t item = vals[i];
             const int32_t t = item_tok[item];
             const float g = a.dloss[t] * a.inv_T;
-            const float c = g * (item < a.nnz ? a.entcoef[item] : a.labcoef[t]);
+            float c = g * (item < a.nnz ? a.entcoef[item] : a.labcoef[t]);
+            if (a.dcoef != nullptr && g != 0.f) {
+                const float alpha = dense_alpha(a.dloss[t], a.dcoef[t], a.inv_T);
+                if (alpha != 0.f) {
+                    const int64_t rb = a.offsets[t], re = a.offsets[t + 1];
+                    if (item < a.nnz) {
+                        if (item == rb || a.ids[item - 1] != a.ids[item])
+                            c += spike_residual(a, alpha, a.zsup[item], a.lse[t]);
+                    } else if (!row_contains(a.ids, rb, re, a.labels[t])) {
+                        c += spike_residual(a, alpha, a.zlab[t], a.lse[t]);
+                    }
+                }
+            }
             if (c != 0.f) fma_row8(acc, a.X + static_cast<int64_t>(t) * a.H + h0, c);
         }
         float4* d = reinterpret_cast<float4*>(dW + v * a.H + h0);
@@ -467,6 +525,7 @@ static int sparse_dw(const SparseArgs& a, const BwdWs& w, float* dW, cudaStream_
         set_last_error("sparse gradient items exceed 2^31");
         return RL_ERR_UNSUPPORTED;
     }
+    ProfScope ps(RL_PROF_SPARSE_DW, s);
     items_init_kernel<<<static_cast<unsigned>((a.N + 7) / 8), 256, 0, s>>>(a, w.item_tok, w.keys_a, w.vals_a);
     if (a.nnz > 0)
         items_guard_kernel<<<static_cast<unsigned>((a.nnz + 255) / 256), 256, 0, s>>>(
@@ -514,18 +573,27 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
     SparseArgs sa{N, H, V, nnz,
                   static_cast<const uint16_t*>(b->weight), static_cast<const uint16_t*>(b->hidden),
                   b->labels, b->support.offsets, b->support.ids, dloss, sv.labcoef, sv.entcoef,
-                  1.0f / prm->temperature};
+                  1.0f / prm->temperature,
+                  w.dense ? sv.dcoef : nullptr, sv.lse, sv.zlab, sv.zsup, w.split ? 1 : 0};
     int rc;
     if (!w.dense) {
-        sparse_dx_kernel<true><<<static_cast<unsigned>(N), 256, 0, stream>>>(sa, nullptr, static_cast<uint16_t*>(dhidden));
+        {
+            ProfScope ps(RL_PROF_SPARSE_DX, stream);
+            sparse_dx_kernel<true><<<static_cast<unsigned>(N), 256, 0, stream>>>(sa, nullptr, static_cast<uint16_t*>(dhidden));
+        }
         count_launch();
-        if (!accumulate)
+        if (!accumulate) {
+            ProfScope ps(RL_PROF_MEMSET, stream);
             if (cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * sizeof(float), stream) != cudaSuccess)
                 return RL_ERR_CUDA;
+        }
         return sparse_dw(sa, w, dW, stream);
     }
 
-    sparse_dx_kernel<false><<<static_cast<unsigned>(N), 256, 0, stream>>>(sa, w.dxs, nullptr);
+    {
+        ProfScope ps(RL_PROF_SPARSE_DX, stream);
+        sparse_dx_kernel<false><<<static_cast<unsigned>(N), 256, 0, stream>>>(sa, w.dxs, nullptr);
+    }
     count_launch();
     rc = transpose_bf16(b->weight, V, H, H, w.Wt, V, stream);
     if (rc != RL_OK) return rc;
@@ -557,15 +625,24 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
                            sv.dcoef + c0, static_cast<uint16_t*>(w.G), static_cast<uint16_t*>(w.Gt),
                            static_cast<uint16_t*>(w.G_lo), static_cast<uint16_t*>(w.Gt_lo), w.chunk};
         const GemmPlan p1 = make_plan(n, V, H, 1, 1 << 30, 1, status);
-        if ((rc = launch_gemm<EpiGrad>(tmX, tmX, tmW, p1, gp, stream)) != RL_OK) return rc;
+        {
+            ProfScope ps(RL_PROF_GEMM_GRAD, stream);
+            if ((rc = launch_gemm<EpiGrad>(tmX, tmX, tmW, p1, gp, stream)) != RL_OK) return rc;
+        }
         // dX chunk = G W + sparse part
         EpiDx::Params dp{n, static_cast<int32_t>(H), w.dxs + c0 * H, static_cast<uint16_t*>(dhidden) + c0 * H};
         const GemmPlan p2 = make_plan(n, H, V, passes, 1 << 30, 0, status);
-        if ((rc = launch_gemm<EpiDx>(tmG, tmGlo, tmWt, p2, dp, stream)) != RL_OK) return rc;
+        {
+            ProfScope ps(RL_PROF_GEMM_DX, stream);
+            if ((rc = launch_gemm<EpiDx>(tmG, tmGlo, tmWt, p2, dp, stream)) != RL_OK) return rc;
+        }
         // dW += G^T X
         EpiDw::Params wp{V, static_cast<int32_t>(H), (c0 > 0 || accumulate) ? 1 : 0, dW};
         const GemmPlan p3 = make_plan(V, H, n, passes, 1 << 30, 0, status);
-        if ((rc = launch_gemm<EpiDw>(tmGt, tmGtlo, tmXt, p3, wp, stream)) != RL_OK) return rc;
+        {
+            ProfScope ps(RL_PROF_GEMM_DW, stream);
+            if ((rc = launch_gemm<EpiDw>(tmGt, tmGtlo, tmXt, p3, wp, stream)) != RL_OK) return rc;
+        }
         count_launch(3);
     }
     return sparse_dw(sa, w, dW, stream);

@@ -30,6 +30,8 @@ SavedView saved_view(void* base, int64_t N, int64_t nnz, size_t* bytes) {
     v.labcoef = c.take<float>(N);
     v.entcoef = c.take<float>(nnz > 0 ? nnz : 1);
     v.mterm = c.take<float>(N * 8);
+    v.zlab = c.take<float>(N);
+    v.zsup = c.take<float>(nnz > 0 ? nnz : 1);
     if (bytes) *bytes = align_up(c.off, 256);
     return v;
 }
@@ -47,8 +49,6 @@ FwdWs fwd_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz, size
     w.part_m = c.take<float>(static_cast<size_t>(w.splits) * N);
     w.part_s = c.take<float>(static_cast<size_t>(w.splits) * N);
     w.part_u = c.take<float>(static_cast<size_t>(w.splits) * N);
-    w.zlab = c.take<float>(N);
-    w.zsup = c.take<float>(nnz > 0 ? nnz : 1);
     w.mpart = c.take<double>(kMetricBlocks * kMetricFields);
     if (bytes) *bytes = align_up(c.off, 256);
     return w;
@@ -144,6 +144,7 @@ int validate_impl(const rl_head_batch* b, int32_t* status, cudaStream_t stream) 
                    b->support.logq, b->support.replayed, b->labels, b->label_logq,
                    b->loss_mask, status};
     const int64_t blocks = (b->N + 7) / 8;
+    ProfScope ps(RL_PROF_VALIDATE, stream);
     validate_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
     count_launch();
     return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
@@ -221,7 +222,7 @@ struct EpiStats {
         float cm = -INFINITY;
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-            z[k] = (k < nvalid) ? __uint_as_float(acc[k]) * p.inv_T : -INFINITY;
+            z[k] = (k < nvalid) ? __fmul_rn(__uint_as_float(acc[k]), p.inv_T) : -INFINITY;
             cm = fmaxf(cm, z[k]);
         }
         if (cm > m) {
@@ -574,6 +575,7 @@ int metrics_impl(const rl_head_batch* b, const void* saved, rl_head_metrics* met
                  cudaStream_t stream) {
     const SavedView sv = saved_view(const_cast<void*>(saved), b->N, b->support.nnz, nullptr);
     const FwdWs w = fwd_ws_view(ws, b->N, b->H, b->V, b->support.nnz, nullptr);
+    ProfScope ps(RL_PROF_METRICS, stream);
     metrics_partial_kernel<<<kMetricBlocks, 256, 0, stream>>>(sv.mterm, b->N, w.mpart);
     metrics_final_kernel<<<1, 32, 0, stream>>>(w.mpart, kMetricBlocks, metrics);
     count_launch(2);
@@ -606,12 +608,15 @@ int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_ou
                         b->labels,
                         b->support.offsets,
                         b->support.ids,
-                        w.zlab,
-                        w.zsup,
+                        sv.zlab,
+                        sv.zsup,
                         w.part_m,
                         w.part_s,
                         w.part_u};
-    rc = launch_gemm<EpiStats>(tmX, tmX, tmW, plan, ep, stream);
+    {
+        ProfScope ps(RL_PROF_GEMM_FWD, stream);
+        rc = launch_gemm<EpiStats>(tmX, tmX, tmW, plan, ep, stream);
+    }
     count_launch();
     if (rc != RL_OK) return rc;
 
@@ -623,8 +628,8 @@ int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_ou
     ta.part_m = w.part_m;
     ta.part_s = w.part_s;
     ta.part_u = w.part_u;
-    ta.zlab = w.zlab;
-    ta.zsup = w.zsup;
+    ta.zlab = sv.zlab;
+    ta.zsup = sv.zsup;
     ta.labels = b->labels;
     ta.label_logq = b->label_logq;
     ta.adv = b->adv;
@@ -653,7 +658,10 @@ int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_ou
     ta.mask_support = out->mask_support;
     ta.sv = sv;
     ta.status = status;
-    token_loss_kernel<<<static_cast<unsigned>((N + 7) / 8), 256, 0, stream>>>(ta);
+    {
+        ProfScope ps(RL_PROF_TOKEN_LOSS, stream);
+        token_loss_kernel<<<static_cast<unsigned>((N + 7) / 8), 256, 0, stream>>>(ta);
+    }
     count_launch();
     if (cudaPeekAtLastError() != cudaSuccess) return RL_ERR_CUDA;
     if (out->metrics) return metrics_impl(b, saved, out->metrics, ws, stream);

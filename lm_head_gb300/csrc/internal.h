@@ -33,6 +33,8 @@ struct SavedView {
     float* labcoef;   // [N] coefficient of the spike at the label
     float* entcoef;   // [nnz] coefficient of the spike at each support entry
     float* mterm;     // [N, 8] per-token metric terms
+    float* zlab;      // [N] label logit z_t,a_t (already / T), as the forward GEMM produced it
+    float* zsup;      // [nnz] support logits, same
 };
 SavedView saved_view(void* base, int64_t N, int64_t nnz, size_t* bytes);
 
@@ -41,8 +43,6 @@ struct FwdWs {
     float* part_m;    // [splits, N]
     float* part_s;
     float* part_u;
-    float* zlab;      // [N]
-    float* zsup;      // [nnz]
     double* mpart;    // metric partials
 };
 FwdWs fwd_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz, size_t* bytes);
@@ -73,6 +73,15 @@ BwdWs bwd_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz,
 bool bwd_is_dense(const rl_params* prm);
 
 void count_launch(int n = 1);
+
+// Event pair around a launch group when profiling is on (see rl_profile_enable).
+struct ProfScope {
+    int kind;
+    cudaStream_t stream;
+    void* begin;
+    ProfScope(int kind, cudaStream_t s);
+    ~ProfScope();
+};
 void set_last_error(const char* msg);
 int num_sms();
 

@@ -230,6 +230,7 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
              static_cast<double*>(ws)};
     const int nb = pg_blocks(T);
     if (static_cast<size_t>(nb) * kPgFields * sizeof(double) > policy_ws_bytes(T)) return RL_ERR_UNSUPPORTED;
+    ProfScope ps(RL_PROF_POLICY, stream);
     policy_kernel<<<nb, kPgThreads, 0, stream>>>(a);
     count_launch();
     if (metrics) {

@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -15,6 +16,52 @@ static std::atomic<int64_t> g_launches{0};
 static thread_local char g_last_error[256] = "";
 
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// ---- per-kind launch timing with recycled CUDA events ------------------------------
+namespace {
+struct Prof {
+    std::mutex mu;
+    bool on = false;
+    std::vector<cudaEvent_t> pool;
+    struct Pending {
+        int kind;
+        cudaEvent_t a, b;
+    };
+    std::vector<Pending> pending;
+    double ms[RL_PROF_KINDS] = {0};
+    int64_t launches[RL_PROF_KINDS] = {0};
+    cudaEvent_t get() {
+        if (!pool.empty()) {
+            cudaEvent_t e = pool.back();
+            pool.pop_back();
+            return e;
+        }
+        cudaEvent_t e = nullptr;
+        cudaEventCreate(&e);
+        return e;
+    }
+};
+Prof& prof() {
+    static Prof p;
+    return p;
+}
+}  // namespace
+
+ProfScope::ProfScope(int k, cudaStream_t s) : kind(k), stream(s), begin(nullptr) {
+    Prof& p = prof();
+    std::lock_guard<std::mutex> g(p.mu);
+    if (!p.on) return;
+    cudaEvent_t e = p.get();
+    if (e && cudaEventRecord(e, s) == cudaSuccess) begin = e;
+}
+ProfScope::~ProfScope() {
+    if (!begin) return;
+    Prof& p = prof();
+    std::lock_guard<std::mutex> g(p.mu);
+    cudaEvent_t e = p.get();
+    if (e && cudaEventRecord(e, stream) == cudaSuccess)
+        p.pending.push_back({kind, static_cast<cudaEvent_t>(begin), e});
+}
 void set_last_error(const char* msg) {
     std::strncpy(g_last_error, msg, sizeof(g_last_error) - 1);
     g_last_error[sizeof(g_last_error) - 1] = 0;
@@ -96,3 +143,49 @@ GemmPlan make_plan(int64_t M, int64_t N, int64_t K, int passes, int n_splits, in
 int64_t rl_launch_counter_value() { return rl::g_launches.load(std::memory_order_relaxed); }
 
 extern "C" const char* rl_last_error(void) { return rl::g_last_error; }
+
+extern "C" int rl_profile_enable(int on) {
+    rl::Prof& p = rl::prof();
+    std::lock_guard<std::mutex> g(p.mu);
+    p.on = on != 0;
+    for (auto& q : p.pending) {
+        p.pool.push_back(q.a);
+        p.pool.push_back(q.b);
+    }
+    p.pending.clear();
+    for (int k = 0; k < RL_PROF_KINDS; ++k) {
+        p.ms[k] = 0.0;
+        p.launches[k] = 0;
+    }
+    return RL_OK;
+}
+
+extern "C" int rl_profile_read(double* ms, int64_t* launches) {
+    rl::Prof& p = rl::prof();
+    std::lock_guard<std::mutex> g(p.mu);
+    int rc = RL_OK;
+    for (auto& q : p.pending) {
+        float t = 0.f;
+        if (cudaEventSynchronize(q.b) != cudaSuccess || cudaEventElapsedTime(&t, q.a, q.b) != cudaSuccess)
+            rc = RL_ERR_CUDA;
+        if (q.kind >= 0 && q.kind < RL_PROF_KINDS) {
+            p.ms[q.kind] += t;
+            p.launches[q.kind] += 1;
+        }
+        p.pool.push_back(q.a);
+        p.pool.push_back(q.b);
+    }
+    p.pending.clear();
+    for (int k = 0; k < RL_PROF_KINDS; ++k) {
+        if (ms) ms[k] = p.ms[k];
+        if (launches) launches[k] = p.launches[k];
+    }
+    return rc;
+}
+
+extern "C" const char* rl_profile_kind_name(int kind) {
+    static const char* names[RL_PROF_KINDS] = {
+        "validate", "gemm_fwd_stats", "token_loss", "metrics", "transpose", "gemm_bwd_grad",
+        "gemm_bwd_dx", "gemm_bwd_dw", "sparse_dx", "sparse_dw", "policy", "gemm_util", "memset", "other"};
+    return (kind >= 0 && kind < RL_PROF_KINDS) ? names[kind] : "unknown";
+}

@@ -264,11 +264,13 @@ def head_forward(inputs: dict, p: HeadParams, rows=None, chunk: int = 64) -> dic
 
 
 def head_backward(inputs: dict, p: HeadParams, dloss: np.ndarray, chunk: int = 64,
-                  rows=None, want_dW: bool = True):
+                  rows=None, want_dW: bool = True, want_bounds: bool = False):
     """dX [N,H] and dW [V,H] of sum_t dloss_t * loss_t, fp64, by the chain rule:
     G_tj = dloss_t / T * d loss_t / d z_tj;  dX = G W;  dW = G^T X.
 
     ``rows`` restricts dX to those tokens (dW then sums over those tokens only).
+    ``want_bounds`` also returns |G| |W| and |G|^T |X| (the magnitudes a finite-precision
+    evaluation of the two products is measured against).
     """
     off = _rows(inputs)
     N = off.shape[0] - 1
@@ -278,6 +280,8 @@ def head_backward(inputs: dict, p: HeadParams, dloss: np.ndarray, chunk: int = 6
     V, H = W.shape
     dX = np.zeros((rows.shape[0], H))
     dW = np.zeros((V, H)) if want_dW else None
+    bX = np.zeros((rows.shape[0], H)) if want_bounds else None
+    bW = np.zeros((V, H)) if (want_bounds and want_dW) else None
     for c0 in range(0, rows.shape[0], chunk):
         rr = rows[c0:c0 + chunk]
         Z = head_token_logits(inputs, rr, p.temperature)
@@ -296,6 +300,12 @@ def head_backward(inputs: dict, p: HeadParams, dloss: np.ndarray, chunk: int = 6
         dX[c0:c0 + rr.shape[0]] = G @ W
         if want_dW:
             dW += G.T @ Xall[rr]
+        if want_bounds:
+            bX[c0:c0 + rr.shape[0]] = np.abs(G) @ np.abs(W)
+            if want_dW:
+                bW += np.abs(G).T @ np.abs(Xall[rr])
+    if want_bounds:
+        return dX, dW, bX, bW
     return dX, dW
 
 

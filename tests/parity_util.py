@@ -43,13 +43,23 @@ def to_bf16(x):
     return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
 
 
-def grad_check(gpu, ref, reading: str, what: str):
-    """Assert the gradient bar; returns the worst ratio err / allowed."""
+def grad_check(gpu, ref, reading: str, what: str, bound=None):
+    """Assert the gradient bar; returns the worst ratio err / allowed.
+
+    readings: "element" (2 ulp of max(|ref|, 2^-8 rowmax)), "row" (2 ulp of the row max),
+    "operand" (2 ulp of |ref| plus 2^-8 of the magnitude bound |G||W| / |G|^T|X|: the
+    result is exact to the precision of its bf16-rounded softmax-gradient operand)."""
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     rb = to_bf16(ref)
     err = np.abs(gpu - rb)
     rowmax = np.max(np.abs(ref), axis=1, keepdims=True)
+    if reading == "operand":
+        allowed = 2 * ulp_bf16(ref) * (ref != 0) + 2.0 ** -8 * np.asarray(bound, np.float64)
+        ratio = np.where(allowed > 0, err / np.maximum(allowed, 1e-300), np.where(err > 0, np.inf, 0.0))
+        worst = float(np.max(ratio)) if ratio.size else 0.0
+        assert worst <= 1.0, f"{what}: worst err/allowed = {worst:.3f} (operand reading)"
+        return worst
     if reading == "element":
         allowed = 2 * ulp_bf16(np.maximum(np.abs(ref), 2.0 ** -8 * rowmax))
         ratio = err / allowed

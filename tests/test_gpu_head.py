@@ -4,6 +4,8 @@ Inputs come from the seeded generators in workloads/ (the same tensors feed both
 Sizes here are ones the oracle finishes in seconds while still spanning several 128 x 256
 tensor-core tiles and a ragged tail.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -78,20 +80,32 @@ def check_forward(case, hp, fwd, ref):
     return ref
 
 
-def check_backward(case, hp, batch, fwd, reading, dloss=None, rows_only=None):
+def check_backward(case, hp, batch, fwd, reading=None, dloss=None, both=True):
+    """Backward in hp's gradient precision, against the oracle.  SPLIT is held to the
+    element reading, BF16 to the operand reading; with ``both`` the other precision is
+    run and checked too (the forward's saved state does not depend on it)."""
     inp = case.numpy()
     op = oracle_params(hp)
     mask = inp["loss_mask"].astype(bool)
     if dloss is None:
         dloss = mask.astype(np.float32) / max(int(mask.sum()), 1)   # token mean over RL tokens
     dl = torch.from_numpy(np.asarray(dloss, np.float32)).cuda()
-    dX, dW, st = rh.rl_head_loss_bwd(batch, hp, fwd.saved, dl)
-    torch.cuda.synchronize()
-    assert int(st.item()) == 0, rh.status_names(int(st.item()))
-    rX, rW = oracle.head_backward(inp, op, np.asarray(dloss, np.float64))
-    wx = grad_check(dX.float().cpu().numpy(), rX, reading, "dX")
-    ww = grad_check(dW.cpu().numpy(), rW, reading, "dW")
-    return dX, dW, (wx, ww)
+    rX, rW, bX, bW = oracle.head_backward(inp, op, np.asarray(dloss, np.float64), want_bounds=True)
+    precisions = [hp.grad_precision]
+    if both:
+        precisions.append(rh.RL_GRAD_SPLIT if hp.grad_precision == rh.RL_GRAD_BF16 else rh.RL_GRAD_BF16)
+    out = None
+    for prec in precisions:
+        hpp = dataclasses.replace(hp, grad_precision=prec)
+        dX, dW, st = rh.rl_head_loss_bwd(batch, hpp, fwd.saved, dl)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, rh.status_names(int(st.item()))
+        rd = reading or ("element" if prec == rh.RL_GRAD_SPLIT else "operand")
+        wx = grad_check(dX.float().cpu().numpy(), rX, rd, "dX", bX)
+        ww = grad_check(dW.cpu().numpy(), rW, rd, "dW", bW)
+        if out is None:
+            out = (dX, dW, (wx, ww))
+    return out
 
 
 C1_IPO = dict(loss_type=rh.RL_LOSS_IPO, eps=0.3, max_importance_ratio=10.0, kl_coeff=0.0)
@@ -104,7 +118,7 @@ def test_c1_forward_and_dense_backward():
     dev, batch, fwd = _forward(case, hp)
     ref = oracle.head_forward(case.numpy(), oracle_params(hp))
     check_forward(case, hp, fwd, ref)
-    check_backward(case, hp, batch, fwd, "row")
+    check_backward(case, hp, batch, fwd)
 
 
 @pytest.mark.parametrize("loss_type", [rh.RL_LOSS_IPO, rh.RL_LOSS_ICEPOP, rh.RL_LOSS_REINFORCE])
@@ -120,7 +134,7 @@ def test_c1_mask_stress(loss_type):
     ref = oracle.head_forward(case.numpy(), oracle_params(hp))
     check_forward(case, hp, fwd, ref)
     assert 0 < int(fwd.mask_support.sum()) < case.nnz or loss_type == rh.RL_LOSS_REINFORCE
-    check_backward(case, hp, batch, fwd, "row")
+    check_backward(case, hp, batch, fwd)
 
 
 def test_c1_split_precision_meets_element_reading():
@@ -129,7 +143,7 @@ def test_c1_split_precision_meets_element_reading():
     dev, batch, fwd = _forward(case, hp)
     ref = oracle.head_forward(case.numpy(), oracle_params(hp))
     check_forward(case, hp, fwd, ref)
-    check_backward(case, hp, batch, fwd, "element")
+    check_backward(case, hp, batch, fwd)
 
 
 def test_k1_estimator_and_temperature():
@@ -139,7 +153,7 @@ def test_k1_estimator_and_temperature():
     dev, batch, fwd = _forward(case, hp)
     ref = oracle.head_forward(case.numpy(), oracle_params(hp))
     check_forward(case, hp, fwd, ref)
-    check_backward(case, hp, batch, fwd, "row")
+    check_backward(case, hp, batch, fwd)
 
 
 @pytest.mark.parametrize("loss_type", [rh.RL_LOSS_IPO, rh.RL_LOSS_REINFORCE])
@@ -154,9 +168,9 @@ def test_replayed_support_sparse_equals_dense_and_oracle(loss_type):
     dev, batch, fwd_d = _forward(case, hp_d)
     ref = oracle.head_forward(case.numpy(), oracle_params(hp_d))
     check_forward(case, hp_d, fwd_d, ref)
-    dXd, dWd, _ = check_backward(case, hp_d, batch, fwd_d, "row")
+    dXd, dWd, _ = check_backward(case, hp_d, batch, fwd_d, both=False)
     fwd_s = rh.rl_head_loss_fwd(batch, hp_s)
-    dXs, dWs, _ = check_backward(case, hp_s, batch, fwd_s, "row")
+    dXs, dWs, _ = check_backward(case, hp_s, batch, fwd_s, both=False)
     torch.testing.assert_close(dWs, dWd, rtol=1e-5, atol=1e-7)
     torch.testing.assert_close(dXs.float(), dXd.float(), rtol=1e-2, atol=1e-6)
 
@@ -167,7 +181,7 @@ def test_reinforce_draws_sparse_without_kl():
     dev, batch, fwd = _forward(case, hp)
     ref = oracle.head_forward(case.numpy(), oracle_params(hp))
     check_forward(case, hp, fwd, ref)
-    check_backward(case, hp, batch, fwd, "element")
+    check_backward(case, hp, batch, fwd)
 
 
 def test_determinism_bitwise():
