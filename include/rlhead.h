@@ -225,6 +225,30 @@ int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const
                                float* grad_ppo, float* grad_dec, rl_pg_metrics* metrics,
                                void* ws, size_t ws_bytes, void* stream);
 
+/* The same computation as rl_policy_loss_elementwise, for callers that cannot allocate
+ * device memory.  The pages have no counterpart of this entry point.  Some callers hold
+ * only their input and output buffers: for example a metrics or loss hook inside a
+ * trainer or inference engine whose device memory is reserved up front by its own pool,
+ * where an extra cudaMalloc would fail or compete with that pool, or plain C code with
+ * no device allocator at hand.  This variant takes no workspace and allocates nothing:
+ * its scratch (the per-block partial sums of the metric reduction) is a file-scope
+ * device array of 229376 bytes, enough for 1024 blocks; a launch uses at most 4 blocks
+ * per SM, so a device with more than 256 SMs is rejected with RL_ERR_WORKSPACE.
+ *   - Every GPU that loads the library holds that array until the process exits.
+ *   - The first call on a device looks the array's device address up (once per
+ *     device); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents.  Each call
+ *     writes every partial it reads before reading it, so nothing has to start at zero.
+ *     Calls that overlap on the GPU (other streams, other threads) race on the array:
+ *     serialise them.
+ * Arguments, outputs and errors as rl_policy_loss_elementwise, without ws / ws_bytes. */
+int rl_policy_loss_elementwise_noalloc(const float* lp_theta, const float* lp_old,
+                                       const float* lp_samp, const float* adv,
+                                       const uint8_t* mask, int64_t T,
+                                       const rl_pg_params* params, float* loss_ppo,
+                                       float* loss_dec, float* grad_ppo, float* grad_dec,
+                                       rl_pg_metrics* metrics, void* stream);
+
 /* ---- utilities ------------------------------------------------------------------ */
 /* The head contraction alone: D[M, N] fp32 = A[M, K] * B[N, K]^T, A and B bf16 row-major
  * (K contiguous), device pointers, 16-byte aligned; K % 8 == 0, N % 4 == 0.  Same tcgen05

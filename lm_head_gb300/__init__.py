@@ -99,6 +99,8 @@ _SIGS = {
     "rl_policy_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64]),
     "rl_policy_loss_elementwise": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int64] + [ctypes.c_void_p] * 7
                                    + [ctypes.c_size_t, ctypes.c_void_p]),
+    "rl_policy_loss_elementwise_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int64]
+                                           + [ctypes.c_void_p] * 7),
     "rl_status_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "rl_gemm_bf16_tn": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int64] * 3
                         + [ctypes.c_void_p] * 3),
@@ -388,6 +390,21 @@ def rl_policy_loss_elementwise(lp_theta, lp_old, lp_samp, adv, mask, params: PgP
     _check(lib.rl_policy_loss_elementwise(_ptr(lp_theta), _ptr(lp_old), _ptr(lp_samp), _ptr(adv), _ptr(mask), T,
                                           ctypes.byref(p), *[_ptr(o) for o in outputs], _ptr(metrics_dev),
                                           _ptr(ws), ws.numel(), _stream(stream)))
+    return (*outputs, metrics_dev)
+
+
+def rl_policy_loss_elementwise_noalloc(lp_theta, lp_old, lp_samp, adv, mask, params: PgParams, *, outputs,
+                                       metrics_dev, stream=None):
+    """rl_policy_loss_elementwise without a workspace, for callers that cannot allocate
+    device memory: the library's scratch is a static device array (see include/rlhead.h).
+    The caller passes every buffer, outputs and the metrics struct included."""
+    lib = load()
+    _require_cuda(lp_theta, lp_old, lp_samp, adv, mask, metrics_dev, *[o for o in outputs if o is not None])
+    T = int(lp_theta.numel())
+    p = params.c()
+    _check(lib.rl_policy_loss_elementwise_noalloc(_ptr(lp_theta), _ptr(lp_old), _ptr(lp_samp), _ptr(adv),
+                                                  _ptr(mask), T, ctypes.byref(p), *[_ptr(o) for o in outputs],
+                                                  _ptr(metrics_dev), _stream(stream)))
     return (*outputs, metrics_dev)
 
 

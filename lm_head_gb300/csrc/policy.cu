@@ -216,6 +216,10 @@ static int pg_blocks(int64_t T) {
     return nb < 1 ? 1 : static_cast<int>(nb);
 }
 
+size_t policy_ws_need(int64_t T) {
+    return static_cast<size_t>(pg_blocks(T)) * kPgFields * sizeof(double);
+}
+
 size_t policy_ws_bytes(int64_t T) {
     (void)T;
     // enough block partials for 4 blocks per SM on any device up to 256 SMs
