@@ -256,6 +256,11 @@ int rl_policy_loss_elementwise_noalloc(const float* lp_theta, const float* lp_ol
  * for timing the contraction in isolation.  Status bits: RL_STATUS_TIMEOUT only. */
 int rl_gemm_bf16_tn(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* D,
                     int32_t* dev_status, void* stream);
+/* General layouts of the same contraction: A is [M, K] (a_mn_major = 0) or [K, M]
+ * (a_mn_major = 1), B is [N, K] or [K, N]; the contiguous extent of each operand must be a
+ * multiple of 8; N % 4 == 0.  D[M, N] fp32 = A * B^T in the K-major naming. */
+int rl_gemm_bf16(const void* A, int a_mn_major, const void* B, int b_mn_major, int64_t M, int64_t N,
+                 int64_t K, float* D, int32_t* dev_status, void* stream);
 
 /* Per-kernel timing: when enabled, the library records a CUDA event pair on the caller's
  * stream around each of its kernel launches, grouped by kind (RL_PROF_* below).

@@ -104,6 +104,8 @@ _SIGS = {
     "rl_status_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "rl_gemm_bf16_tn": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int64] * 3
                         + [ctypes.c_void_p] * 3),
+    "rl_gemm_bf16": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
+                     + [ctypes.c_int64] * 3 + [ctypes.c_void_p] * 3),
     "rl_kernel_launch_count": (ctypes.c_int64, []),
     "rl_profile_enable": (ctypes.c_int, [ctypes.c_int]),
     "rl_profile_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
@@ -425,6 +427,22 @@ def rl_gemm_bf16_tn(A: torch.Tensor, B: torch.Tensor, D: Optional[torch.Tensor] 
         D = torch.empty(M, N, dtype=torch.float32, device=A.device)
     st = torch.zeros(1, dtype=torch.int32, device=A.device) if status is None else status
     _check(load().rl_gemm_bf16_tn(_ptr(A), _ptr(B), M, N, K, _ptr(D), _ptr(st), _stream(stream)))
+    return D, st
+
+
+def rl_gemm_bf16(A: torch.Tensor, a_mn_major: bool, B: torch.Tensor, b_mn_major: bool,
+                 D: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None, stream=None):
+    """D[M, N] fp32 = A B^T with A given as [M, K] or ([K, M], a_mn_major) and B as [N, K]
+    or ([K, N], b_mn_major)."""
+    _require_cuda(A, B)
+    M = A.shape[1] if a_mn_major else A.shape[0]
+    K = A.shape[0] if a_mn_major else A.shape[1]
+    N = B.shape[1] if b_mn_major else B.shape[0]
+    if D is None:
+        D = torch.empty(M, N, dtype=torch.float32, device=A.device)
+    st = torch.zeros(1, dtype=torch.int32, device=A.device) if status is None else status
+    _check(load().rl_gemm_bf16(_ptr(A), int(bool(a_mn_major)), _ptr(B), int(bool(b_mn_major)), M, N, K, _ptr(D),
+                               _ptr(st), _stream(stream)))
     return D, st
 
 

@@ -161,14 +161,21 @@ int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const
                        metrics, ws, as_stream(stream));
 }
 
-int rl_gemm_bf16_tn(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* D,
-                    int32_t* dev_status, void* stream) {
+int rl_gemm_bf16(const void* A, int a_mn_major, const void* B, int b_mn_major, int64_t M, int64_t N,
+                 int64_t K, float* D, int32_t* dev_status, void* stream) {
     if (!A || !B || !D || !dev_status) return fail(RL_ERR_ARG, "NULL pointer");
     if (M <= 0 || N <= 0 || K <= 0) return fail(RL_ERR_ARG, "non-positive size");
-    if (K % 8 != 0 || N % 4 != 0) return fail(RL_ERR_UNSUPPORTED, "K % 8 or N % 4 != 0");
+    if (N % 4 != 0) return fail(RL_ERR_UNSUPPORTED, "N % 4 != 0");
+    if ((a_mn_major ? M : K) % 8 != 0 || (b_mn_major ? N : K) % 8 != 0)
+        return fail(RL_ERR_UNSUPPORTED, "contiguous extent of an operand not a multiple of 8");
     if (!aligned16(A) || !aligned16(B) || !aligned16(D)) return fail(RL_ERR_ARG, "not 16-byte aligned");
     if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
-    return gemm_util_impl(A, B, M, N, K, D, dev_status, as_stream(stream));
+    return gemm_util_impl(A, a_mn_major != 0, B, b_mn_major != 0, M, N, K, D, dev_status, as_stream(stream));
+}
+
+int rl_gemm_bf16_tn(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* D,
+                    int32_t* dev_status, void* stream) {
+    return rl_gemm_bf16(A, 0, B, 0, M, N, K, D, dev_status, stream);
 }
 
 int rl_status_read(const int32_t* dev_status, int32_t* host_out) {

@@ -190,6 +190,21 @@ RL_DEVINL uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
+// Descriptor for an MN-major operand tile (M or N contiguous in memory), as TMA writes it
+// with 64 x 64 boxes and the 128-byte swizzle: each 128-byte row holds 64 consecutive M/N
+// elements of one K index; 8 rows form a 1024-byte swizzle atom; 8-row K groups are
+// 1024 bytes apart (stride-byte-offset) and 64-element M/N blocks `lbo` bytes apart
+// (leading-byte-offset).  Stepping K by 16 adds 16 rows = 2048 bytes.
+RL_DEVINL uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
 // Instruction descriptor for tcgen05.mma kind::f16: fp32 accumulator (bits 4-5 = 1),
 // bf16 A and B (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in bits
 // 17-22, M >> 4 in bits 24-28.

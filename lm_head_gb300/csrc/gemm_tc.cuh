@@ -1,6 +1,11 @@
 // Persistent warp-specialised tcgen05 GEMM for sm_100-family GPUs:
 //
-//   D[M, N] = A[M, K] * B[N, K]^T        (bf16 x bf16 -> fp32, both operands K-major)
+//   D[M, N] = A[M, K] * B[N, K]^T        (bf16 x bf16 -> fp32)
+//
+// Each operand is K-major (stored [M, K] / [N, K], K contiguous) or MN-major (stored
+// [K, M] / [K, N], M or N contiguous): the transpose bits of the instruction descriptor
+// and the shared-memory descriptors follow the layout, so no operand is ever transposed
+// in memory.
 //
 // * warp 0, one lane: TMA producer.  Stages A (128 x 64) and B (256 x 64) tiles with the
 //   128-byte swizzle into a 4-deep shared-memory ring; completion on per-stage mbarriers.
@@ -8,9 +13,11 @@
 //   TMEM accumulator; tcgen05.commit frees the stage and, after the last K block of a
 //   tile, hands the accumulator to the epilogue.  Two 256-column accumulators (all 512
 //   TMEM columns) let the epilogue of tile i overlap the MMAs of tile i+1.
-// * warps 2-5: epilogue.  Warp w reads TMEM lanes 32*(w%4) .. +31, so thread r of the
-//   128 owns row r of the tile and sees its 256 columns in eight 32-column chunks.  The
-//   epilogue policy (template parameter) decides what a row does with them.
+// * warps 2-9: epilogue.  Warp w reads TMEM lanes 32*(w%4) .. +31 and one half of the
+//   tile's columns (warps 2-5 the first 128, warps 6-9 the last 128), so each row of the
+//   tile is owned by two threads that see 128 columns each, in four 32-column chunks.
+//   Two epilogue warps per scheduler keep the epilogue off the MMA's critical path.  The
+//   epilogue policy (template parameter) decides what a row does with its columns.
 //
 // Work is split into "units": one 128-row block of A times a contiguous range of 256-col
 // tiles of B.  CTAs take units round-robin (grid = min(units, SMs)).  A unit's tiles are
@@ -33,7 +40,8 @@ constexpr int kStages = 4;
 constexpr int kATileBytes = kBM * kBK * 2;   // 16 KB
 constexpr int kBTileBytes = kBN * kBK * 2;   // 32 KB
 constexpr int kStageBytes = kATileBytes + kBTileBytes;
-constexpr int kGemmThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 + 256;
 constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
@@ -47,6 +55,8 @@ struct GemmPlan {
     int m_fastest;       // 1: u -> (m = u % m_blocks, s = u / m_blocks); 0: (m = u / n_splits, s = u % n_splits)
     int kb_per_pass;     // ceil(K / 64)
     int passes;          // 1; 2 when A comes as a hi/lo pair (tmA then tmA2, same B)
+    int a_mn;            // A stored [K, M] (MN-major): tensor map over [K, M], 64 x 64 boxes
+    int b_mn;            // B stored [K, N]
     int32_t* status;
 };
 
@@ -83,12 +93,14 @@ RL_DEVINL void tmem_load_row32(uint32_t taddr, uint32_t (&r)[32]) {
                  : "memory");
 }
 
-// Epilogue policy interface (all device, per thread; `row` in [0, 128)):
+// Epilogue policy interface (all device, per thread; `row` in [0, 128), `half` 0/1 says
+// which 128 columns of every 256-column tile this thread sees; `col_begin` is the first
+// column it will see in the unit):
 //   struct Epi {
 //     struct Params { ... };
-//     __device__ void begin_unit(const Params&, int row, int m_blk, int split, int col_begin);
+//     __device__ void begin_unit(const Params&, int row, int half, int m_blk, int split, int col_begin);
 //     __device__ void chunk(const Params&, const uint32_t (&acc)[32], int col0);
-//     __device__ void end_unit(const Params&, int split);
+//     __device__ void end_unit(const Params&, int split, int half);
 //   };
 template <class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -116,7 +128,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf + b, 1);
-            mbar_init(acce + b, 4);
+            mbar_init(acce + b, kEpiWarps);
         }
         mbar_init(done_bar, 1);
         *abort_flag = 0;
@@ -165,8 +177,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         armed_parity[stage] = phase;
                         const int pass = kb / plan.kb_per_pass;
                         const int kx = (kb - pass * plan.kb_per_pass) * kBK;
-                        tma_load_2d(pass ? &tmA2 : &tmA, full + stage, sa, kx, c.m_blk * kBM);
-                        tma_load_2d(&tmB, full + stage, sb, kx, nb * kBN);
+                        const CUtensorMap* ma = pass ? &tmA2 : &tmA;
+                        if (plan.a_mn) {
+#pragma unroll
+                            for (int i = 0; i < kBM / 64; ++i)
+                                tma_load_2d(ma, full + stage, sa + i * 8192, c.m_blk * kBM + 64 * i, kx);
+                        } else {
+                            tma_load_2d(ma, full + stage, sa, kx, c.m_blk * kBM);
+                        }
+                        if (plan.b_mn) {
+#pragma unroll
+                            for (int i = 0; i < kBN / 64; ++i)
+                                tma_load_2d(&tmB, full + stage, sb + i * 8192, nb * kBN + 64 * i, kx);
+                        } else {
+                            tma_load_2d(&tmB, full + stage, sb, kx, nb * kBN);
+                        }
                         if (++stage == kStages) {
                             stage = 0;
                             phase ^= 1u;
@@ -186,6 +211,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
             bool ok = true;
             bool issued = false;
+            const uint32_t idesc = kIdesc | (plan.a_mn ? (1u << 15) : 0u) | (plan.b_mn ? (1u << 16) : 0u);
             for (int u = blockIdx.x; u < plan.num_units && ok; u += gridDim.x) {
                 const UnitCoords c = decode_unit(plan, u);
                 for (int nb = c.nb_begin; nb < c.nb_end && ok; ++nb) {
@@ -207,9 +233,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const uint32_t sb = sa + kATileBytes;
 #pragma unroll
                         for (int k = 0; k < kBK / 16; ++k) {
-                            umma_bf16(d_tmem, sdesc_kmajor_sw128(sa + k * 32),
-                                      sdesc_kmajor_sw128(sb + k * 32), kIdesc,
-                                      (kb | k) != 0 ? 1u : 0u);
+                            const uint64_t da = plan.a_mn ? sdesc_mnmajor_sw128(sa + k * 2048, 8192)
+                                                          : sdesc_kmajor_sw128(sa + k * 32);
+                            const uint64_t db = plan.b_mn ? sdesc_mnmajor_sw128(sb + k * 2048, 8192)
+                                                          : sdesc_kmajor_sw128(sb + k * 32);
+                            umma_bf16(d_tmem, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
                         }
                         issued = true;
                         umma_commit(empty + stage);
@@ -231,15 +259,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
         }
     } else {
-        // ---------------- epilogue (warps 2..5) ----------------
+        // ---------------- epilogue (warps 2..9) ----------------
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
         uint32_t abuf = 0, aphase = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < plan.num_units && ok; u += gridDim.x) {
             const UnitCoords c = decode_unit(plan, u);
             Epi epi;
-            epi.begin_unit(ep, row, c.m_blk, c.split, c.nb_begin * kBN);
+            epi.begin_unit(ep, row, half, c.m_blk, c.split, c.nb_begin * kBN + half * (kBN / 2));
             for (int nb = c.nb_begin; nb < c.nb_end; ++nb) {
                 if (!mbar_wait(accf + abuf, aphase, plan.status) || *abort_flag) {
                     *abort_flag = 1;
@@ -250,7 +279,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        abuf * kBN;
 #pragma unroll 1
-                for (int ch = 0; ch < kBN / 32; ++ch) {
+                for (int ch = half * (kBN / 64); ch < (half + 1) * (kBN / 64); ++ch) {
                     uint32_t acc[32];
                     __syncwarp();
                     tmem_load_row32(taddr + ch * 32, acc);
@@ -262,7 +291,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 abuf ^= 1u;
                 if (abuf == 0) aphase ^= 1u;
             }
-            if (ok) epi.end_unit(ep, c.split);
+            if (ok) epi.end_unit(ep, c.split, half);
         }
     }
 
@@ -285,7 +314,7 @@ int make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t col
 int num_sms();
 
 GemmPlan make_plan(int64_t M, int64_t N, int64_t K, int passes, int n_splits, int m_fastest,
-                   int32_t* status);
+                   int32_t* status, int a_mn = 0, int b_mn = 0);
 
 // Launch `gemm_tc_kernel<Epi>`; A2 may equal A when passes == 1.
 template <class Epi>

@@ -13,7 +13,7 @@ struct EpiStore {
     };
     int64_t t;
     bool valid;
-    RL_DEVINL void begin_unit(const Params& p, int row, int m_blk, int, int) {
+    RL_DEVINL void begin_unit(const Params& p, int row, int, int m_blk, int, int) {
         t = static_cast<int64_t>(m_blk) * kBM + row;
         valid = t < p.M;
     }
@@ -32,16 +32,17 @@ struct EpiStore {
                 if (col0 + k < p.N) d[k] = __uint_as_float(acc[k]);
         }
     }
-    RL_DEVINL void end_unit(const Params&, int) {}
+    RL_DEVINL void end_unit(const Params&, int, int) {}
 };
 
-int gemm_util_impl(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* D,
-                   int32_t* status, cudaStream_t stream) {
+int gemm_util_impl(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
+                   float* D, int32_t* status, cudaStream_t stream) {
     CUtensorMap ta, tb;
-    int rc = make_tmap_bf16(&ta, A, M, K, K, kBM);
+    int rc = a_mn ? make_tmap_bf16(&ta, A, K, M, M, 64) : make_tmap_bf16(&ta, A, M, K, K, kBM);
     if (rc != RL_OK) return rc;
-    if ((rc = make_tmap_bf16(&tb, B, N, K, K, kBN)) != RL_OK) return rc;
-    const GemmPlan plan = make_plan(M, N, K, 1, 1 << 30, 1, status);
+    rc = b_mn ? make_tmap_bf16(&tb, B, K, N, N, 64) : make_tmap_bf16(&tb, B, N, K, K, kBN);
+    if (rc != RL_OK) return rc;
+    const GemmPlan plan = make_plan(M, N, K, 1, 1 << 30, 1, status, a_mn, b_mn);
     EpiStore::Params ep{M, N, D};
     {
         ProfScope ps(RL_PROF_GEMM_UTIL, stream);

@@ -116,7 +116,7 @@ struct EpiGrad {
     bool valid;
     float alpha, lse;
 
-    RL_DEVINL void begin_unit(const Params& p, int row, int m_blk, int, int) {
+    RL_DEVINL void begin_unit(const Params& p, int row, int, int m_blk, int, int) {
         t = static_cast<int64_t>(m_blk) * kBM + row;
         valid = t < p.n;
         alpha = 0.f;
@@ -165,7 +165,7 @@ struct EpiGrad {
             }
         }
     }
-    RL_DEVINL void end_unit(const Params&, int) {}
+    RL_DEVINL void end_unit(const Params&, int, int) {}
 };
 
 // dX rows of the chunk: bf16(acc + dxs) for columns < H.
@@ -178,7 +178,7 @@ struct EpiDx {
     };
     int64_t t;
     bool valid;
-    RL_DEVINL void begin_unit(const Params& p, int row, int m_blk, int, int) {
+    RL_DEVINL void begin_unit(const Params& p, int row, int, int m_blk, int, int) {
         t = static_cast<int64_t>(m_blk) * kBM + row;
         valid = t < p.n;
     }
@@ -195,7 +195,7 @@ struct EpiDx {
                               pack_bf16x2(__uint_as_float(acc[8 * q + 6]) + b.z, __uint_as_float(acc[8 * q + 7]) + b.w));
         }
     }
-    RL_DEVINL void end_unit(const Params&, int) {}
+    RL_DEVINL void end_unit(const Params&, int, int) {}
 };
 
 // dW rows: dW = (accumulate ? dW : 0) + acc for columns < H, rows < V.
@@ -208,7 +208,7 @@ struct EpiDw {
     };
     int64_t v;
     bool valid;
-    RL_DEVINL void begin_unit(const Params& p, int row, int m_blk, int, int) {
+    RL_DEVINL void begin_unit(const Params& p, int row, int, int m_blk, int, int) {
         v = static_cast<int64_t>(m_blk) * kBM + row;
         valid = v < p.V;
     }
@@ -229,7 +229,7 @@ struct EpiDw {
             d[q] = r;
         }
     }
-    RL_DEVINL void end_unit(const Params&, int) {}
+    RL_DEVINL void end_unit(const Params&, int, int) {}
 };
 
 // ----------------------------------------------------------------------------------

@@ -45,10 +45,10 @@ FwdWs fwd_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz, size
     (void)H;
     Carve c(base);
     FwdWs w;
-    w.splits = max_splits(V);
-    w.part_m = c.take<float>(static_cast<size_t>(w.splits) * N);
-    w.part_s = c.take<float>(static_cast<size_t>(w.splits) * N);
-    w.part_u = c.take<float>(static_cast<size_t>(w.splits) * N);
+    w.splits = max_splits(V);   // each split holds one partial per column half
+    w.part_m = c.take<float>(static_cast<size_t>(2 * w.splits) * N);
+    w.part_s = c.take<float>(static_cast<size_t>(2 * w.splits) * N);
+    w.part_u = c.take<float>(static_cast<size_t>(2 * w.splits) * N);
     w.mpart = c.take<double>(kMetricBlocks * kMetricFields);
     if (bytes) *bytes = align_up(c.off, 256);
     return w;
@@ -166,11 +166,28 @@ RL_DEVINL void kahan_add(float& s, float& c, float x) {
     s = t;
 }
 
+RL_DEVINL float max32(const float (&v)[32]) {
+    float m[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) m[k] = fmaxf(v[k], v[k + 16]);
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+        for (int k = 0; k < w; ++k) m[k] = fmaxf(m[k], m[k + w]);
+    return m[0];
+}
+
+// Per row and column half, an online (max, sum e^{z-m}, sum e^{z-m}(z-m)) over the unit's
+// vocabulary tiles, kept in log2 units (m2 = m log2(e)): each logit costs one FFMA, one
+// EX2, one FADD and one FFMA.  The partial is written in natural units.  Label and support
+// logits are taken from the chunk that holds them: the row's CSR ids are ascending, so a
+// pointer moves forward with the columns.
 struct EpiStats {
     struct Params {
         int64_t N;
         int32_t V;
         float inv_T;
+        float c2;          // log2(e) / T
         int64_t nnz;
         const int32_t* labels;
         const int64_t* offsets;
@@ -183,17 +200,18 @@ struct EpiStats {
     };
     int64_t t;
     bool valid;
-    float m, s, sc, u, uc;
+    float m2, s, sc, u2, uc;
     int64_t ptr, end;
     int32_t next_id;
     int32_t label;
 
-    RL_DEVINL void begin_unit(const Params& p, int row, int m_blk, int split, int col_begin) {
+    RL_DEVINL void begin_unit(const Params& p, int row, int half, int m_blk, int split, int col_begin) {
         (void)split;
+        (void)half;
         t = static_cast<int64_t>(m_blk) * kBM + row;
         valid = t < p.N;
-        m = -INFINITY;
-        s = sc = u = uc = 0.f;
+        m2 = -INFINITY;
+        s = sc = u2 = uc = 0.f;
         ptr = end = 0;
         next_id = INT_MAX;
         label = -1;
@@ -217,50 +235,68 @@ struct EpiStats {
 
     RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0) {
         if (!valid || col0 >= p.V) return;
-        const int nvalid = p.V - col0;  // > 0
-        float z[32];
-        float cm = -INFINITY;
+        float a[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            z[k] = (k < nvalid) ? __fmul_rn(__uint_as_float(acc[k]), p.inv_T) : -INFINITY;
-            cm = fmaxf(cm, z[k]);
+        for (int k = 0; k < 32; ++k) a[k] = __uint_as_float(acc[k]);
+        const bool full = col0 + 32 <= p.V;
+        if (!full) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+                if (col0 + k >= p.V) a[k] = -INFINITY;
         }
-        if (cm > m) {
-            if (m == -INFINITY) {
-                s = sc = u = uc = 0.f;
+        const float cm2 = max32(a) * p.c2;   // T > 0: the max of the raw accumulators is the max of z
+        if (cm2 > m2) {
+            if (m2 == -INFINITY) {
+                s = sc = u2 = uc = 0.f;
             } else {
-                const float a = exp2_approx((m - cm) * kLog2e);
-                u = a * (u + (m - cm) * s);
-                uc *= a;
-                s *= a;
-                sc *= a;
+                const float f = exp2_approx(m2 - cm2);
+                u2 = f * (u2 + (m2 - cm2) * s);
+                uc *= f;
+                s *= f;
+                sc *= f;
             }
-            m = cm;
+            m2 = cm2;
         }
-        float cs = 0.f, cu = 0.f;
+        float cs0 = 0.f, cs1 = 0.f, cu0 = 0.f, cu1 = 0.f;
+        if (full) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            const float d = fmaxf(z[k] - m, -1e30f);
-            const float e = exp2_approx(d * kLog2e);
-            cs += e;
-            cu = fmaf(e, d, cu);
+            for (int k = 0; k < 32; k += 2) {
+                const float d0 = fmaf(a[k], p.c2, -m2);
+                const float d1 = fmaf(a[k + 1], p.c2, -m2);
+                const float e0 = exp2_approx(d0);
+                const float e1 = exp2_approx(d1);
+                cs0 += e0;
+                cs1 += e1;
+                cu0 = fmaf(e0, d0, cu0);
+                cu1 = fmaf(e1, d1, cu1);
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const float d = fmaxf(fmaf(a[k], p.c2, -m2), -1e30f);
+                const float e = exp2_approx(d);
+                cs0 += e;
+                cu0 = fmaf(e, d, cu0);
+            }
         }
-        kahan_add(s, sc, cs);
-        kahan_add(u, uc, cu);
-        if (static_cast<unsigned>(label - col0) < 32u) p.zlab[t] = select32(z, label - col0);
-        while (next_id < col0 + 32) {
-            p.zsup[ptr] = select32(z, (next_id - col0) & 31);
+        kahan_add(s, sc, cs0 + cs1);
+        kahan_add(u2, uc, cu0 + cu1);
+        // z exactly as the backward's recompute forms it: one rounded multiply by 1/T
+        if (static_cast<unsigned>(label - col0) < 32u)
+            p.zlab[t] = __fmul_rn(select32(a, label - col0), p.inv_T);
+        while (next_id < col0 + 32) {  // ids below col0 belong to the other column half
+            if (next_id >= col0) p.zsup[ptr] = __fmul_rn(select32(a, next_id - col0), p.inv_T);
             ++ptr;
             next_id = ptr < end ? p.ids[ptr] : INT_MAX;
         }
     }
 
-    RL_DEVINL void end_unit(const Params& p, int split) {
+    RL_DEVINL void end_unit(const Params& p, int split, int half) {
         if (!valid) return;
-        const int64_t i = static_cast<int64_t>(split) * p.N + t;
-        p.part_m[i] = m;
+        const int64_t i = static_cast<int64_t>(2 * split + half) * p.N + t;
+        p.part_m[i] = m2 * kLn2;
         p.part_s[i] = s - sc;
-        p.part_u[i] = u - uc;
+        p.part_u[i] = (u2 - uc) * kLn2;
     }
 };
 
@@ -604,6 +640,7 @@ int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_ou
     EpiStats::Params ep{N,
                         static_cast<int32_t>(V),
                         1.0f / prm->temperature,
+                        kLog2e / prm->temperature,
                         nnz,
                         b->labels,
                         b->support.offsets,
@@ -623,7 +660,7 @@ int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_ou
     TokenArgs ta;
     ta.N = N;
     ta.V = static_cast<int32_t>(V);
-    ta.S = plan.n_splits;
+    ta.S = 2 * plan.n_splits;
     ta.nnz = nnz;
     ta.part_m = w.part_m;
     ta.part_s = w.part_s;

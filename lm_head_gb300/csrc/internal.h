@@ -99,7 +99,7 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
                 void* ws, cudaStream_t stream);
 size_t policy_ws_bytes(int64_t T);
 size_t policy_ws_need(int64_t T);   // bytes of block partials one launch for T tokens writes
-int gemm_util_impl(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* D,
-                   int32_t* status, cudaStream_t stream);
+int gemm_util_impl(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
+                   float* D, int32_t* status, cudaStream_t stream);
 
 }  // namespace rl

@@ -122,7 +122,7 @@ int make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t col
 }
 
 GemmPlan make_plan(int64_t M, int64_t N, int64_t K, int passes, int n_splits, int m_fastest,
-                   int32_t* status) {
+                   int32_t* status, int a_mn, int b_mn) {
     GemmPlan p;
     p.m_blocks = static_cast<int>((M + kBM - 1) / kBM);
     p.n_blocks = static_cast<int>((N + kBN - 1) / kBN);
@@ -134,6 +134,8 @@ GemmPlan make_plan(int64_t M, int64_t N, int64_t K, int passes, int n_splits, in
     p.m_fastest = m_fastest;
     p.kb_per_pass = static_cast<int>((K + kBK - 1) / kBK);
     p.passes = passes;
+    p.a_mn = a_mn;
+    p.b_mn = b_mn;
     p.status = status;
     return p;
 }

@@ -29,3 +29,27 @@ def test_gemm_matches_fp32_reference(M, N, K):
     ref = A.double() @ B.double().T
     err = (D.double() - ref).abs().max().item()
     assert err <= 1e-5 * (K ** 0.5) * max(1.0, ref.abs().max().item()), err
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (296, 1000, 192), (1024, 2048, 2048), (136, 24, 40)])
+def test_gemm_mn_major_operands(M, N, K, a_mn, b_mn):
+    """Operands stored M/N-contiguous ([K, M], [K, N]) read without a transpose."""
+    g = torch.Generator(device="cuda").manual_seed(M + 11 * N + 7 * K + a_mn + 2 * b_mn)
+    A = torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16)
+    B = torch.randn(N, K, device="cuda", generator=g).to(torch.bfloat16)
+    Aop = A.T.contiguous() if a_mn else A
+    Bop = B.T.contiguous() if b_mn else B
+    D, st = rh.rl_gemm_bf16(Aop, bool(a_mn), Bop, bool(b_mn))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ref = A.double() @ B.double().T
+    err = (D.double() - ref).abs().max().item()
+    assert err <= 1e-5 * (K ** 0.5) * max(1.0, ref.abs().max().item()), err
+
+
+def test_gemm_rejects_unaligned_contiguous_extent():
+    A = torch.zeros(192, 300, device="cuda", dtype=torch.bfloat16)   # [K, M] with M % 8 != 0
+    B = torch.zeros(1000, 192, device="cuda", dtype=torch.bfloat16)
+    with pytest.raises(rh.RLHeadError):
+        rh.rl_gemm_bf16(A, True, B, False)
