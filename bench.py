@@ -234,8 +234,7 @@ def run_ours(args):
     batch = rh.HeadBatch.from_case(case)
     torch.cuda.reset_peak_memory_stats(dev)
     base_mem = torch.cuda.memory_allocated(dev)
-    ws_f = torch.empty(rh.rl_head_fwd_workspace_bytes(N, H, V, nnz, hp), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(rh.rl_head_bwd_workspace_bytes(N, H, V, nnz, hp), dtype=torch.uint8, device=dev)
+    ws_fb = torch.empty(rh.rl_head_fwd_bwd_workspace_bytes(N, H, V, nnz, hp), dtype=torch.uint8, device=dev)
     saved = torch.empty(rh.rl_head_saved_bytes(N, nnz), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     dloss = (case.loss_mask.float() / case.loss_mask.float().sum()).contiguous()   # token mean
@@ -244,8 +243,9 @@ def run_ours(args):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)     # > 2x L2
 
     def step(b=batch, st=status):
-        f = rh.rl_head_loss_fwd(b, hp, ws=ws_f, saved=saved, status=st)
-        rh.rl_head_loss_bwd(b, hp, saved, dloss, dhidden=dX, dW=dW, ws=ws_b, status=st)
+        # one forward + backward of the head over the batch: the fused entry point (the
+        # token-mean weights are known before the forward)
+        f, _, _ = rh.rl_head_loss_fwd_bwd(b, hp, dloss, dhidden=dX, dW=dW, ws=ws_fb, saved=saved, status=st)
         return f
 
     for _ in range(args.warmup):
@@ -280,6 +280,28 @@ def run_ours(args):
     peak_gib = (torch.cuda.max_memory_allocated(dev)) / 2 ** 30
     work_gib = (torch.cuda.max_memory_allocated(dev) - base_mem) / 2 ** 30
 
+    # ---- side figure: the two-call path (forward, then backward with logit recompute) ----
+    unfused_ms = None
+    if not args.no_unfused:
+        del ws_fb
+        torch.cuda.empty_cache()
+        ws_f = torch.empty(rh.rl_head_fwd_workspace_bytes(N, H, V, nnz, hp), dtype=torch.uint8, device=dev)
+        ws_b = torch.empty(rh.rl_head_bwd_workspace_bytes(N, H, V, nnz, hp), dtype=torch.uint8, device=dev)
+        for i in range(2 + min(args.steps, 3)):
+            if i == 2:
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+            rh.rl_head_loss_fwd(batch, hp, ws=ws_f, saved=saved, status=status)
+            rh.rl_head_loss_bwd(batch, hp, saved, dloss, dhidden=dX, dW=dW, ws=ws_b, status=status)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e1.record()
+        torch.cuda.synchronize()
+        unfused_ms = e0.elapsed_time(e1) / min(args.steps, 3)
+        del ws_f, ws_b
+        torch.cuda.empty_cache()
+        ws_fb = torch.empty(rh.rl_head_fwd_bwd_workspace_bytes(N, H, V, nnz, hp), dtype=torch.uint8, device=dev)
+
     # ---- e2e: same step through the public API from pinned host buffers ----
     pin = {k: getattr(case, k).cpu().pin_memory() for k in
            ("hidden", "labels", "label_logq", "adv", "loss_mask", "age", "replayed", "offsets", "ids", "logq")}
@@ -311,8 +333,8 @@ def run_ours(args):
     e_ms, _, e_value = aggregate(e_ms, N, world)
 
     # ---- roofline of the dominant kernel (live CUDA-event times from the timed region) ----
-    flops_per_launch = {"gemm_fwd_stats": 2.0 * N * H * V}
     chunk = min(16384, (N + 127) // 128 * 128)
+    flops_per_launch = {"gemm_fwd_stats": 2.0 * chunk * H * V}     # fused path: one launch per chunk
     for k in ("gemm_bwd_grad", "gemm_bwd_dx", "gemm_bwd_dw"):
         flops_per_launch[k] = 2.0 * chunk * H * V * (2 if (args.grad_precision == "split" and k != "gemm_bwd_grad") else 1)
     dom = max(prof.items(), key=lambda kv: kv[1][0])
@@ -344,6 +366,7 @@ def run_ours(args):
             "tc_peak_frac": step_tflops / peak_burst,
             "step_tflops_6NHV": step_tflops,
             "peak_gib": peak_gib, "workspace_peak_gib": work_gib,
+            "two_call_ms_per_step": unfused_ms,
             "roofline": roof, "kernels": kernels,
             "e2e": {"value": e_value, "unit": "tokens/s", "ms_per_step": e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
@@ -396,6 +419,7 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=32, help="oracle sample per step, --impl reference")
     ap.add_argument("--tokens", type=int, default=None, help="fewer tokens, same shapes (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-unfused", action="store_true", help="skip the two-call side figure")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

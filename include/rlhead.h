@@ -182,6 +182,22 @@ int rl_head_loss_bwd(const rl_head_batch* batch, const rl_params* params, const 
                      const float* dloss, void* dhidden, float* dW, int accumulate_dW,
                      void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* Forward and backward in one call, for callers whose loss aggregation is known before
+ * the forward (dloss_t = the weight of loss_t in the scalar objective, e.g. 1 / #RL tokens
+ * for a token mean; an autograd caller then scales dhidden and dW by the upstream
+ * gradient of that scalar).  Same outputs as rl_head_loss_fwd (incl. `saved`, usable by a
+ * later rl_head_loss_bwd) plus the gradients of rl_head_loss_bwd, without recomputing
+ * the logits: per token chunk the forward tiles keep the softmax numerators (fp16,
+ * relative to the running row max) and the dense backward consumes them.  Dense-mode
+ * tensor work is 6 N H V flops instead of 8.  Sparse-mode knobs run the forward and
+ * the sparse backward.  Workspace: rl_head_fwd_bwd_workspace_bytes. */
+size_t rl_head_fwd_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz,
+                                       const rl_params* params);
+int rl_head_loss_fwd_bwd(const rl_head_batch* batch, const rl_params* params,
+                         const rl_head_outputs* out, const float* dloss, void* dhidden, float* dW,
+                         int accumulate_dW, void* saved, void* ws, size_t ws_bytes,
+                         int32_t* dev_status, void* stream);
+
 /* Reduce the per-token metric terms in `saved` (written by rl_head_loss_fwd for the same
  * batch) into *metrics (device).  rl_head_loss_fwd calls it when out->metrics != NULL. */
 int rl_mismatch_metrics(const rl_head_batch* batch, const void* saved,
@@ -267,11 +283,11 @@ int rl_gemm_bf16(const void* A, int a_mn_major, const void* B, int b_mn_major, i
  * rl_profile_enable(1) also clears the counters.  rl_profile_read waits for the recorded
  * events, then fills ms[k] (summed device milliseconds) and launches[k] for every kind
  * k < RL_PROF_KINDS; either pointer may be NULL.  Host arrays. */
-#define RL_PROF_KINDS 14
+#define RL_PROF_KINDS 16
 enum { RL_PROF_VALIDATE = 0, RL_PROF_GEMM_FWD = 1, RL_PROF_TOKEN_LOSS = 2, RL_PROF_METRICS = 3,
        RL_PROF_TRANSPOSE = 4, RL_PROF_GEMM_GRAD = 5, RL_PROF_GEMM_DX = 6, RL_PROF_GEMM_DW = 7,
        RL_PROF_SPARSE_DX = 8, RL_PROF_SPARSE_DW = 9, RL_PROF_POLICY = 10, RL_PROF_GEMM_UTIL = 11,
-       RL_PROF_MEMSET = 12, RL_PROF_OTHER = 13 };
+       RL_PROF_MEMSET = 12, RL_PROF_OTHER = 13, RL_PROF_RESID = 14, RL_PROF_GRAD_E = 15 };
 int rl_profile_enable(int on);
 int rl_profile_read(double* ms, int64_t* launches);
 const char* rl_profile_kind_name(int kind);

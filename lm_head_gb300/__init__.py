@@ -96,6 +96,10 @@ _SIGS = {
     "rl_head_loss_bwd": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
                                                                 ctypes.c_void_p, ctypes.c_void_p]),
     "rl_mismatch_metrics": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_size_t, ctypes.c_void_p]),
+    "rl_head_fwd_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 4 + [ctypes.c_void_p]),
+    "rl_head_loss_fwd_bwd": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                                                    ctypes.c_size_t, ctypes.c_void_p,
+                                                                    ctypes.c_void_p]),
     "rl_policy_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64]),
     "rl_policy_loss_elementwise": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int64] + [ctypes.c_void_p] * 7
                                    + [ctypes.c_size_t, ctypes.c_void_p]),
@@ -340,6 +344,51 @@ def rl_head_loss_bwd(batch: HeadBatch, params: HeadParams, saved: torch.Tensor, 
     return dhidden, dW, st
 
 
+def rl_head_fwd_bwd_workspace_bytes(N, H, V, nnz, params: HeadParams) -> int:
+    p = params.c()
+    return int(load().rl_head_fwd_bwd_workspace_bytes(N, H, V, nnz, ctypes.byref(p)))
+
+
+def rl_head_loss_fwd_bwd(batch: HeadBatch, params: HeadParams, dloss: torch.Tensor, *,
+                         dhidden: Optional[torch.Tensor] = None, dW: Optional[torch.Tensor] = None,
+                         accumulate_dW: bool = False, ws: Optional[torch.Tensor] = None,
+                         saved: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                         want_metrics: bool = True, stream=None):
+    """Forward + backward in one call (dloss known up front).  Returns (HeadForward, dhidden, dW)."""
+    lib = load()
+    dev = batch.hidden.device
+    _require_cuda(dloss)
+    if dloss.dtype != torch.float32 or dloss.numel() != batch.N:
+        raise RLHeadError("dloss must be fp32 [N]")
+    N, nnz = batch.N, batch.nnz
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = HeadForward(
+        loss=torch.empty(N, **f32), logp_label=torch.empty(N, **f32),
+        logp_support=torch.empty(max(nnz, 1), **f32)[:nnz], entropy=torch.empty(N, **f32),
+        lse=torch.empty(N, **f32), mask_label=torch.empty(N, dtype=torch.uint8, device=dev),
+        mask_support=torch.empty(max(nnz, 1), dtype=torch.uint8, device=dev)[:nnz],
+        metrics_dev=torch.zeros(ctypes.sizeof(RlHeadMetrics), dtype=torch.uint8, device=dev),
+        saved=saved if saved is not None else _u8(rl_head_saved_bytes(N, nnz), dev),
+        status=torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status)
+    if dhidden is None:
+        dhidden = torch.empty(N, batch.H, dtype=torch.bfloat16, device=dev)
+    if dW is None:
+        dW = torch.empty(batch.V, batch.H, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = _u8(rl_head_fwd_bwd_workspace_bytes(N, batch.H, batch.V, nnz, params), dev)
+    p = params.c()
+    cb = batch.c()
+    co = RlHeadOutputs(out.loss.data_ptr(), out.logp_label.data_ptr(),
+                       out.logp_support.data_ptr() if nnz else None, out.entropy.data_ptr(),
+                       out.lse.data_ptr(), out.mask_label.data_ptr(),
+                       out.mask_support.data_ptr() if nnz else None,
+                       out.metrics_dev.data_ptr() if want_metrics else None)
+    _check(lib.rl_head_loss_fwd_bwd(ctypes.byref(cb), ctypes.byref(p), ctypes.byref(co), _ptr(dloss), _ptr(dhidden),
+                                    _ptr(dW), int(bool(accumulate_dW)), _ptr(out.saved), _ptr(ws), ws.numel(),
+                                    _ptr(out.status), _stream(stream)))
+    return out, dhidden, dW
+
+
 def rl_mismatch_metrics(batch: HeadBatch, saved: torch.Tensor, params: HeadParams, *,
                         ws: Optional[torch.Tensor] = None, stream=None) -> dict:
     lib = load()
@@ -456,7 +505,7 @@ def rl_kernel_launch_count() -> int:
     return int(load().rl_kernel_launch_count())
 
 
-RL_PROF_KINDS = 14
+RL_PROF_KINDS = 16
 
 
 def rl_profile_enable(on: bool = True) -> None:

@@ -130,6 +130,28 @@ int rl_head_loss_bwd(const rl_head_batch* batch, const rl_params* params, const 
                          as_stream(stream));
 }
 
+size_t rl_head_fwd_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* params) {
+    if (N < 0 || H <= 0 || V <= 0 || nnz < 0 || !params) return 0;
+    return fused_ws_bytes(N, H, V, nnz, params);
+}
+
+int rl_head_loss_fwd_bwd(const rl_head_batch* batch, const rl_params* params, const rl_head_outputs* out,
+                         const float* dloss, void* dhidden, float* dW, int accumulate_dW, void* saved, void* ws,
+                         size_t ws_bytes, int32_t* dev_status, void* stream) {
+    int rc = check_batch(batch);
+    if (rc != RL_OK) return rc;
+    if ((rc = check_params(params)) != RL_OK) return rc;
+    if (!out || !out->loss || !saved || !dev_status || !dloss || !dW || (batch->N > 0 && !dhidden))
+        return fail(RL_ERR_ARG, "out/loss/saved/dev_status/dloss/dhidden/dW NULL");
+    if (!aligned16(dW) || !aligned16(dhidden)) return fail(RL_ERR_ARG, "dW/dhidden not 16-byte aligned");
+    if (ws_bytes < rl_head_fwd_bwd_workspace_bytes(batch->N, batch->H, batch->V, batch->support.nnz, params))
+        return fail(RL_ERR_WORKSPACE, "forward+backward workspace too small");
+    if (!ws) return fail(RL_ERR_ARG, "ws is NULL");
+    if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
+    return head_fused_impl(batch, params, out, dloss, dhidden, dW, accumulate_dW, saved, ws, dev_status,
+                           as_stream(stream));
+}
+
 int rl_mismatch_metrics(const rl_head_batch* batch, const void* saved, rl_head_metrics* metrics, void* ws,
                         size_t ws_bytes, void* stream) {
     int rc = check_batch(batch);

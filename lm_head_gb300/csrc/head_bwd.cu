@@ -15,6 +15,8 @@
 #include <climits>
 #include <cmath>
 
+#include <cuda_fp16.h>
+
 #include "gemm_tc.cuh"
 #include "internal.h"
 
@@ -27,7 +29,7 @@ bool bwd_is_dense(const rl_params* prm) {
     return !(knobs_sparse || prm->all_replayed != 0);
 }
 
-static int64_t bwd_chunk(int64_t N, const rl_params* prm) {
+int64_t bwd_chunk(int64_t N, const rl_params* prm) {
     int64_t c = prm->token_chunk > 0 ? prm->token_chunk : 16384;
     c = (c + kBM - 1) / kBM * kBM;
     const int64_t n128 = (N + kBM - 1) / kBM * kBM;
@@ -57,6 +59,7 @@ BwdWs bwd_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz, cons
             w.Gt_lo = c.take<uint16_t>(static_cast<size_t>(V) * w.chunk);
         }
         w.dxs = c.take<float>(static_cast<size_t>(N) * H);
+        w.resid = c.take<float>(nnz + N);
     }
     w.item_tok = c.take<int32_t>(items);
     w.keys_a = c.take<int32_t>(items);
@@ -280,13 +283,9 @@ struct SparseArgs {
     const float* labcoef;
     const float* entcoef;
     float inv_T;
-    // dense mode only (dcoef == nullptr otherwise): what the bf16 GEMM operands dropped at
-    // each spike position is added back here, once per distinct (token, vocab id)
-    const float* dcoef;
-    const float* lse;
-    const float* zlab;
-    const float* zsup;
-    int split;
+    // dense mode only (nullptr otherwise): per gradient item, what the bf16 dense GEMM
+    // operand dropped at that (token, vocab id); non-zero once per distinct pair
+    const float* resid;
 };
 
 // True when `v` occurs among ids[b, e) (ascending).
@@ -302,9 +301,81 @@ RL_DEVINL bool row_contains(const int32_t* ids, int64_t b, int64_t e, int32_t v)
     return lo < e && ids[lo] == v;
 }
 
-RL_DEVINL float spike_residual(const SparseArgs& a, float alpha, float z, float lse) {
+// Residual at one spike: the exact fp32 dense value g_true = alpha exp(z - lse) minus what
+// the dense GEMMs consume there (bf16 hi, and lo with the split), where g_gemm is either
+// g_true itself (recompute path) or F * e from the stored fp16 e (fused path).
+RL_DEVINL float spike_residual(float g_true, float g_gemm, bool split) {
+    const float hi = __bfloat162float(__float2bfloat16_rn(g_gemm));
+    float r = __fsub_rn(g_true, hi);
+    if (split) r = __fsub_rn(r, __bfloat162float(__float2bfloat16_rn(__fsub_rn(g_gemm, hi))));
+    return r;
+}
+// Per-row factor of the fused path: G = F * e with F = alpha 2^(m2 - lse log2(e)).
+RL_DEVINL float fused_factor(float alpha, float m2, float lse) {
     if (alpha == 0.f) return 0.f;
-    return dense_residual(dense_grad(alpha, z, lse), a.split != 0);
+    return __fmul_rn(alpha, exp2_approx(__fsub_rn(m2, __fmul_rn(lse, kLog2e))));
+}
+
+struct ResidArgs {
+    int64_t t0, n, V, nnz;
+    const int32_t* labels;    // absolute
+    const int64_t* offsets;   // absolute
+    const int32_t* ids;
+    const float* dloss;       // absolute
+    const float* dcoef;       // absolute
+    const float* lse;         // absolute
+    const float* zlab;        // absolute
+    const float* zsup;
+    float inv_T;
+    int split;
+    // fused path: e [n, V] (fp16, or fp32 in E32) and m2 [n, ldm], chunk-relative;
+    // both nullptr = recompute path
+    const uint16_t* E;
+    const float* E32;
+    const float* M2;
+    int64_t ldm;
+    float* resid;             // [nnz + N]
+};
+
+// One warp per token of [t0, t0 + n): residual at the label and at the first entry of each
+// distinct support id; 0 elsewhere (duplicates, rows without a dense part).
+__global__ void __launch_bounds__(256) resid_kernel(ResidArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (r >= a.n) return;
+    const int64_t t = a.t0 + r;
+    int64_t b = a.offsets[t], e = a.offsets[t + 1];
+    b = b < 0 ? 0 : (b > a.nnz ? a.nnz : b);
+    e = e < b ? b : (e > a.nnz ? a.nnz : e);
+    const float alpha = dense_alpha(a.dloss[t], a.dcoef[t], a.inv_T);
+    const float lse = a.lse[t];
+    auto resid_at = [&](int32_t v, float z) -> float {
+        if (alpha == 0.f || v < 0 || v >= a.V) return 0.f;
+        const float g_true = dense_grad(alpha, z, lse);
+        float g_gemm = g_true;
+        if (a.E != nullptr || a.E32 != nullptr) {
+            const float ev = a.E32 ? a.E32[r * a.V + v] : __half2float(__ushort_as_half(a.E[r * a.V + v]));
+            g_gemm = __fmul_rn(fused_factor(alpha, a.M2[r * a.ldm + (v >> 5)], lse), ev);
+        }
+        return spike_residual(g_true, g_gemm, a.split != 0);
+    };
+    for (int64_t j = b + lane; j < e; j += 32) {
+        const int32_t id = a.ids[j];
+        const bool first = (j == b) || (a.ids[j - 1] != id);
+        a.resid[j] = first ? resid_at(id, a.zsup[j]) : 0.f;
+    }
+    if (lane == 0) {
+        const int32_t lab = a.labels[t];
+        a.resid[a.nnz + t] = row_contains(a.ids, b, e, lab) ? 0.f : resid_at(lab, a.zlab[t]);
+    }
+}
+
+static int launch_resid(const ResidArgs& a, cudaStream_t s) {
+    if (a.n <= 0) return RL_OK;
+    ProfScope ps(RL_PROF_RESID, s);
+    resid_kernel<<<static_cast<unsigned>((a.n + 7) / 8), 256, 0, s>>>(a);
+    count_launch();
+    return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }
 
 RL_DEVINL void fma_row8(float (&acc)[8], const uint16_t* row, float c) {
@@ -318,18 +389,15 @@ RL_DEVINL void fma_row8(float (&acc)[8], const uint16_t* row, float c) {
 }
 
 template <bool kToBf16>
-__global__ void __launch_bounds__(256) sparse_dx_kernel(SparseArgs a, float* dxs, uint16_t* dx_bf16) {
-    const int64_t t = blockIdx.x;
+__global__ void __launch_bounds__(256) sparse_dx_kernel(SparseArgs a, int64_t t0, float* dxs, uint16_t* dx_bf16) {
+    const int64_t t = t0 + blockIdx.x;   // output row blockIdx.x (chunk-relative)
     const float g = a.dloss[t] * a.inv_T;
     int64_t b = a.offsets[t], e = a.offsets[t + 1];
     b = b < 0 ? 0 : (b > a.nnz ? a.nnz : b);
     e = e < b ? b : (e > a.nnz ? a.nnz : e);
     const int32_t lab = a.labels[t];
-    const float alpha = a.dcoef ? dense_alpha(a.dloss[t], a.dcoef[t], a.inv_T) : 0.f;
-    const float lse = alpha != 0.f ? a.lse[t] : 0.f;
     float cl = g * a.labcoef[t];
-    if (alpha != 0.f && lab >= 0 && lab < a.V && !row_contains(a.ids, b, e, lab))
-        cl += spike_residual(a, alpha, a.zlab[t], lse);
+    if (a.resid) cl += a.resid[a.nnz + t];
     for (int64_t h0 = static_cast<int64_t>(threadIdx.x) * 8; h0 < a.H; h0 += 256 * 8) {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (g != 0.f) {
@@ -337,7 +405,7 @@ __global__ void __launch_bounds__(256) sparse_dx_kernel(SparseArgs a, float* dxs
             for (int64_t j = b; j < e; ++j) {
                 const int32_t id = a.ids[j];
                 float c = g * a.entcoef[j];
-                if (alpha != 0.f && (j == b || a.ids[j - 1] != id)) c += spike_residual(a, alpha, a.zsup[j], lse);
+                if (a.resid) c += a.resid[j];
                 if (id >= 0 && id < a.V && c != 0.f) fma_row8(acc, a.W + id * a.H + h0, c);
             }
         }
@@ -346,7 +414,7 @@ __global__ void __launch_bounds__(256) sparse_dx_kernel(SparseArgs a, float* dxs
                                  pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
             *reinterpret_cast<uint4*>(dx_bf16 + t * a.H + h0) = o;
         } else {
-            float4* o = reinterpret_cast<float4*>(dxs + t * a.H + h0);
+            float4* o = reinterpret_cast<float4*>(dxs + static_cast<int64_t>(blockIdx.x) * a.H + h0);
             o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
             o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
         }
@@ -490,18 +558,7 @@ __global__ void __launch_bounds__(256) sparse_dw_kernel(SparseArgs a, const int3
             const int32_t t = item_tok[item];
             const float g = a.dloss[t] * a.inv_T;
             float c = g * (item < a.nnz ? a.entcoef[item] : a.labcoef[t]);
-            if (a.dcoef != nullptr && g != 0.f) {
-                const float alpha = dense_alpha(a.dloss[t], a.dcoef[t], a.inv_T);
-                if (alpha != 0.f) {
-                    const int64_t rb = a.offsets[t], re = a.offsets[t + 1];
-                    if (item < a.nnz) {
-                        if (item == rb || a.ids[item - 1] != a.ids[item])
-                            c += spike_residual(a, alpha, a.zsup[item], a.lse[t]);
-                    } else if (!row_contains(a.ids, rb, re, a.labels[t])) {
-                        c += spike_residual(a, alpha, a.zlab[t], a.lse[t]);
-                    }
-                }
-            }
+            if (a.resid) c += a.resid[item];
             if (c != 0.f) fma_row8(acc, a.X + static_cast<int64_t>(t) * a.H + h0, c);
         }
         float4* d = reinterpret_cast<float4*>(dW + v * a.H + h0);
@@ -573,13 +630,12 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
     SparseArgs sa{N, H, V, nnz,
                   static_cast<const uint16_t*>(b->weight), static_cast<const uint16_t*>(b->hidden),
                   b->labels, b->support.offsets, b->support.ids, dloss, sv.labcoef, sv.entcoef,
-                  1.0f / prm->temperature,
-                  w.dense ? sv.dcoef : nullptr, sv.lse, sv.zlab, sv.zsup, w.split ? 1 : 0};
+                  1.0f / prm->temperature, w.dense ? w.resid : nullptr};
     int rc;
     if (!w.dense) {
         {
             ProfScope ps(RL_PROF_SPARSE_DX, stream);
-            sparse_dx_kernel<true><<<static_cast<unsigned>(N), 256, 0, stream>>>(sa, nullptr, static_cast<uint16_t*>(dhidden));
+            sparse_dx_kernel<true><<<static_cast<unsigned>(N), 256, 0, stream>>>(sa, 0, nullptr, static_cast<uint16_t*>(dhidden));
         }
         count_launch();
         if (!accumulate) {
@@ -590,9 +646,13 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
         return sparse_dw(sa, w, dW, stream);
     }
 
+    ResidArgs ra{0, N, V, nnz, b->labels, b->support.offsets, b->support.ids, dloss, sv.dcoef, sv.lse,
+                 sv.zlab, sv.zsup, 1.0f / prm->temperature, w.split ? 1 : 0, nullptr, nullptr, nullptr, 0,
+                 w.resid};
+    if ((rc = launch_resid(ra, stream)) != RL_OK) return rc;
     {
         ProfScope ps(RL_PROF_SPARSE_DX, stream);
-        sparse_dx_kernel<false><<<static_cast<unsigned>(N), 256, 0, stream>>>(sa, w.dxs, nullptr);
+        sparse_dx_kernel<false><<<static_cast<unsigned>(N), 256, 0, stream>>>(sa, 0, w.dxs, nullptr);
     }
     count_launch();
     rc = transpose_bf16(b->weight, V, H, H, w.Wt, V, stream);
@@ -646,6 +706,265 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
         count_launch(3);
     }
     return sparse_dw(sa, w, dW, stream);
+}
+
+// ----------------------------------------------------------------------------------
+// Fused forward + backward (dloss known before the forward): no logit recompute.
+// Per token chunk the forward GEMM also stores e = 2^(z log2(e) - m2) in fp16 with its
+// running-max reference m2 per 32-column chunk; once the chunk's logsumexp is known,
+// G = alpha 2^(m2 - lse log2(e)) e (one factor per row and 32-column chunk) is written in
+// both layouts, and the dX / dW GEMMs follow.  6 N H V tensor flops per step.
+// ----------------------------------------------------------------------------------
+struct GradEArgs {
+    int64_t n, V, ldm, ldt;
+    const uint16_t* E;    // fp16 e, or
+    const float* E32;     // fp32 e
+    const float* M2;
+    const float* dloss;   // chunk-relative
+    const float* dcoef;
+    const float* lse;
+    float inv_T;
+    uint16_t* G;
+    uint16_t* Gt;
+    uint16_t* G_lo;
+    uint16_t* Gt_lo;
+};
+
+constexpr int kGradTileT = 64;    // tokens per block
+constexpr int kGradTileV = 128;   // vocabulary ids per block
+constexpr int kGradPitch = 72;    // smem row pitch (halfwords): 144 B keeps 16-byte rows
+
+// G = F e with one factor F = alpha 2^(m2 - lse log2 e) per row and 32-column chunk, written
+// row-major (16-byte stores) and, through a transposed smem tile, as G^T (16-byte stores).
+// Thread (r = tid / 4, c = tid % 4) converts token r's columns [32 c, 32 c + 32).
+__global__ void __launch_bounds__(256) grad_from_e_kernel(GradEArgs a) {
+    __shared__ __align__(16) uint16_t th[kGradTileV][kGradPitch];
+    __shared__ __align__(16) uint16_t tl[kGradTileV][kGradPitch];
+    const int tid = threadIdx.x, r = tid >> 2, c = tid & 3;
+    const int64_t t = static_cast<int64_t>(blockIdx.y) * kGradTileT + r;
+    const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kGradTileV + c * 32;
+    const bool split = a.G_lo != nullptr;
+    uint32_t hi[16], lo[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) hi[k] = lo[k] = 0u;
+    int nv = 0;
+    if (t < a.n && v0 < a.V) {
+        nv = a.V - v0 < 32 ? static_cast<int>(a.V - v0) : 32;   // multiple of 8
+        const float alpha = dense_alpha(a.dloss[t], a.dcoef[t], a.inv_T);
+        const float F = fused_factor(alpha, a.M2[t * a.ldm + (v0 >> 5)], a.lse[t]);
+        float e[32];
+        if (a.E32) {
+            const float4* src = reinterpret_cast<const float4*>(a.E32 + t * a.V + v0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 x = q * 4 < nv ? src[q] : make_float4(0.f, 0.f, 0.f, 0.f);
+                e[4 * q] = x.x;
+                e[4 * q + 1] = x.y;
+                e[4 * q + 2] = x.z;
+                e[4 * q + 3] = x.w;
+            }
+        } else {
+            const uint4* src = reinterpret_cast<const uint4*>(a.E + t * a.V + v0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 x = q * 8 < nv ? src[q] : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    e[8 * q + 2 * k] = __half2float(__ushort_as_half(static_cast<uint16_t>(w[k] & 0xFFFFu)));
+                    e[8 * q + 2 * k + 1] = __half2float(__ushort_as_half(static_cast<uint16_t>(w[k] >> 16)));
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float g0 = __fmul_rn(F, e[2 * k]), g1 = __fmul_rn(F, e[2 * k + 1]);
+            hi[k] = pack_bf16x2(g0, g1);
+            if (split) {
+                const float h0 = bf16_bits_to_float(static_cast<uint16_t>(hi[k] & 0xFFFFu));
+                const float h1 = bf16_bits_to_float(static_cast<uint16_t>(hi[k] >> 16));
+                lo[k] = pack_bf16x2(g0 - h0, g1 - h1);
+            }
+        }
+        uint4* gd = reinterpret_cast<uint4*>(a.G + t * a.V + v0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (q * 8 < nv) gd[q] = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+        if (split) {
+            uint4* ld = reinterpret_cast<uint4*>(a.G_lo + t * a.V + v0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (q * 8 < nv) ld[q] = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        th[c * 32 + k][r] = static_cast<uint16_t>((k & 1) ? (hi[k >> 1] >> 16) : (hi[k >> 1] & 0xFFFFu));
+        if (split) tl[c * 32 + k][r] = static_cast<uint16_t>((k & 1) ? (lo[k >> 1] >> 16) : (lo[k >> 1] & 0xFFFFu));
+    }
+    __syncthreads();
+    // G^T rows: 8 threads per vocabulary id, 8 tokens (16 B) each
+    const int64_t tbase = static_cast<int64_t>(blockIdx.y) * kGradTileT;
+    for (int row = tid >> 3; row < kGradTileV; row += 32) {
+        const int64_t v = static_cast<int64_t>(blockIdx.x) * kGradTileV + row;
+        const int j = (tid & 7) * 8;
+        if (v >= a.V) continue;
+        const int64_t tt = tbase + j;
+        if (tt + 8 <= a.n) {
+            *reinterpret_cast<uint4*>(a.Gt + v * a.ldt + tt) = *reinterpret_cast<const uint4*>(&th[row][j]);
+            if (split) *reinterpret_cast<uint4*>(a.Gt_lo + v * a.ldt + tt) = *reinterpret_cast<const uint4*>(&tl[row][j]);
+        } else {
+            for (int k = 0; k < 8 && tt + k < a.n; ++k) {
+                a.Gt[v * a.ldt + tt + k] = th[row][j + k];
+                if (split) a.Gt_lo[v * a.ldt + tt + k] = tl[row][j + k];
+            }
+        }
+    }
+}
+
+struct FusedWs {
+    int64_t chunk;
+    FwdWs fw;
+    uint16_t* E;     // fp16 e (bf16 gradient precision)
+    float* E32;      // fp32 e (hi/lo gradient precision)
+    float* M2;
+    int64_t ldm;
+    BwdWs bw;   // G, Gt, G_lo, Gt_lo, Wt, Xt, dxs [chunk, H], resid, sort buffers
+};
+
+static FusedWs fused_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* prm,
+                             size_t* bytes) {
+    FusedWs f{};
+    f.chunk = bwd_chunk(N, prm);
+    size_t fb = 0;
+    f.fw = fwd_ws_view(base, f.chunk, H, V, nnz, &fb);
+    Carve c(base ? static_cast<uint8_t*>(base) + fb : nullptr);
+    c.off = 0;
+    f.ldm = (V + 31) / 32;
+    if (prm->grad_precision == RL_GRAD_SPLIT)
+        f.E32 = c.take<float>(static_cast<size_t>(f.chunk) * V);
+    else
+        f.E = c.take<uint16_t>(static_cast<size_t>(f.chunk) * V);
+    f.M2 = c.take<float>(static_cast<size_t>(f.chunk) * f.ldm);
+    BwdWs& w = f.bw;
+    w.dense = true;
+    w.split = prm->grad_precision == RL_GRAD_SPLIT;
+    w.chunk = f.chunk;
+    w.Wt = c.take<uint16_t>(static_cast<size_t>(V) * H);
+    w.Xt = c.take<uint16_t>(static_cast<size_t>(H) * f.chunk);
+    w.G = c.take<uint16_t>(static_cast<size_t>(f.chunk) * V);
+    w.Gt = c.take<uint16_t>(static_cast<size_t>(V) * f.chunk);
+    if (w.split) {
+        w.G_lo = c.take<uint16_t>(static_cast<size_t>(f.chunk) * V);
+        w.Gt_lo = c.take<uint16_t>(static_cast<size_t>(V) * f.chunk);
+    }
+    w.dxs = c.take<float>(static_cast<size_t>(f.chunk) * H);
+    w.resid = c.take<float>(nnz + N);
+    const int64_t items = nnz + N;
+    w.item_tok = c.take<int32_t>(items);
+    w.keys_a = c.take<int32_t>(items);
+    w.vals_a = c.take<int32_t>(items);
+    w.keys_b = c.take<int32_t>(items);
+    w.vals_b = c.take<int32_t>(items);
+    const int64_t tiles = (items + kSortTile - 1) / kSortTile;
+    w.hist = c.take<int32_t>(static_cast<size_t>(tiles > 0 ? tiles : 1) * kDigits);
+    w.bucket = c.take<int64_t>(V + 2);
+    if (bytes) *bytes = align_up(fb + c.off, 256);
+    return f;
+}
+
+size_t fused_ws_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* prm) {
+    if (!bwd_is_dense(prm)) {   // no dense GEMMs: the forward, then the sparse backward
+        size_t a = 0, b = 0;
+        fwd_ws_view(nullptr, N, H, V, nnz, &a);
+        bwd_ws_view(nullptr, N, H, V, nnz, prm, &b);
+        return a > b ? a : b;
+    }
+    size_t bytes = 0;
+    fused_ws_view(nullptr, N, H, V, nnz, prm, &bytes);
+    return bytes;
+}
+
+int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out,
+                    const float* dloss, void* dhidden, float* dW, int accumulate, void* saved, void* ws,
+                    int32_t* status, cudaStream_t stream) {
+    const int64_t N = b->N, H = b->H, V = b->V, nnz = b->support.nnz;
+    if (!bwd_is_dense(prm)) {
+        int rc = head_fwd_impl(b, prm, out, saved, ws, status, stream);
+        if (rc != RL_OK) return rc;
+        return head_bwd_impl(b, prm, saved, dloss, dhidden, dW, accumulate, ws, status, stream);
+    }
+    int rc = validate_impl(b, status, stream);
+    if (rc != RL_OK) return rc;
+    if (N == 0) {
+        if (!accumulate && cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * sizeof(float), stream) != cudaSuccess)
+            return RL_ERR_CUDA;
+        return RL_OK;
+    }
+    const SavedView sv = saved_view(saved, N, nnz, nullptr);
+    const FusedWs f = fused_ws_view(ws, N, H, V, nnz, prm, nullptr);
+    const BwdWs& w = f.bw;
+    const float inv_T = 1.0f / prm->temperature;
+    SparseArgs sa{N, H, V, nnz,
+                  static_cast<const uint16_t*>(b->weight), static_cast<const uint16_t*>(b->hidden),
+                  b->labels, b->support.offsets, b->support.ids, dloss, sv.labcoef, sv.entcoef, inv_T, w.resid};
+    rc = transpose_bf16(b->weight, V, H, H, w.Wt, V, stream);
+    if (rc != RL_OK) return rc;
+    CUtensorMap tmWt;
+    if ((rc = make_tmap_bf16(&tmWt, w.Wt, H, V, V, kBN)) != RL_OK) return rc;
+    const int passes = w.split ? 2 : 1;
+    for (int64_t c0 = 0; c0 < N; c0 += f.chunk) {
+        const int64_t n = N - c0 < f.chunk ? N - c0 : f.chunk;
+        // forward GEMM (+ e store) and per-token loss for the chunk
+        if ((rc = fwd_rows(b, prm, out, sv, f.fw, c0, n, f.E, f.E32, f.M2, 0, status, stream)) != RL_OK) return rc;
+        // spike residuals of the chunk's tokens, then G / G^T from e
+        ResidArgs ra{c0, n, V, nnz, b->labels, b->support.offsets, b->support.ids, dloss, sv.dcoef, sv.lse,
+                     sv.zlab, sv.zsup, inv_T, w.split ? 1 : 0, f.E, f.E32, f.M2, f.ldm, w.resid};
+        if ((rc = launch_resid(ra, stream)) != RL_OK) return rc;
+        {
+            GradEArgs ga{n, V, f.ldm, f.chunk, f.E, f.E32, f.M2, dloss + c0, sv.dcoef + c0, sv.lse + c0, inv_T,
+                         static_cast<uint16_t*>(w.G), static_cast<uint16_t*>(w.Gt),
+                         static_cast<uint16_t*>(w.G_lo), static_cast<uint16_t*>(w.Gt_lo)};
+            dim3 grid(static_cast<unsigned>((V + kGradTileV - 1) / kGradTileV),
+                      static_cast<unsigned>((n + kGradTileT - 1) / kGradTileT));
+            ProfScope ps(RL_PROF_GRAD_E, stream);
+            grad_from_e_kernel<<<grid, 256, 0, stream>>>(ga);
+            count_launch();
+        }
+        const uint16_t* Xc = static_cast<const uint16_t*>(b->hidden) + c0 * H;
+        if ((rc = transpose_bf16(Xc, n, H, H, w.Xt, f.chunk, stream)) != RL_OK) return rc;
+        {
+            ProfScope ps(RL_PROF_SPARSE_DX, stream);
+            sparse_dx_kernel<false><<<static_cast<unsigned>(n), 256, 0, stream>>>(sa, c0, w.dxs, nullptr);
+            count_launch();
+        }
+        CUtensorMap tmG, tmGlo, tmGt, tmGtlo, tmXt;
+        if ((rc = make_tmap_bf16(&tmG, w.G, n, V, V, kBM)) != RL_OK) return rc;
+        if ((rc = make_tmap_bf16(&tmGt, w.Gt, V, n, f.chunk, kBM)) != RL_OK) return rc;
+        if ((rc = make_tmap_bf16(&tmXt, w.Xt, H, n, f.chunk, kBN)) != RL_OK) return rc;
+        tmGlo = tmG;
+        tmGtlo = tmGt;
+        if (w.split) {
+            if ((rc = make_tmap_bf16(&tmGlo, w.G_lo, n, V, V, kBM)) != RL_OK) return rc;
+            if ((rc = make_tmap_bf16(&tmGtlo, w.Gt_lo, V, n, f.chunk, kBM)) != RL_OK) return rc;
+        }
+        EpiDx::Params dp{n, static_cast<int32_t>(H), w.dxs, static_cast<uint16_t*>(dhidden) + c0 * H};
+        const GemmPlan p2 = make_plan(n, H, V, passes, 1 << 30, 0, status);
+        {
+            ProfScope ps(RL_PROF_GEMM_DX, stream);
+            if ((rc = launch_gemm<EpiDx>(tmG, tmGlo, tmWt, p2, dp, stream)) != RL_OK) return rc;
+        }
+        EpiDw::Params wp{V, static_cast<int32_t>(H), (c0 > 0 || accumulate) ? 1 : 0, dW};
+        const GemmPlan p3 = make_plan(V, H, n, passes, 1 << 30, 0, status);
+        {
+            ProfScope ps(RL_PROF_GEMM_DW, stream);
+            if ((rc = launch_gemm<EpiDw>(tmGt, tmGtlo, tmXt, p3, wp, stream)) != RL_OK) return rc;
+        }
+        count_launch(2);
+    }
+    if ((rc = sparse_dw(sa, w, dW, stream)) != RL_OK) return rc;
+    if (out->metrics) return metrics_run(b, saved, out->metrics, f.fw.mpart, stream);
+    return RL_OK;
 }
 
 }  // namespace rl

@@ -13,6 +13,8 @@
 #include <cmath>
 #include <climits>
 
+#include <cuda_fp16.h>
+
 #include "gemm_tc.cuh"
 #include "internal.h"
 
@@ -197,6 +199,12 @@ struct EpiStats {
         float* part_m;
         float* part_s;
         float* part_u;
+        // optional (fused forward + backward): e = 2^(z log2(e) - m2) as fp16 [N, V] and
+        // the running max m2 it is relative to, per 32-column chunk [N, ldm]
+        uint16_t* E;
+        float* E32;      // fp32 instead of fp16 (hi/lo gradient precision)
+        float* M2;
+        int64_t ldm;
     };
     int64_t t;
     bool valid;
@@ -258,29 +266,51 @@ struct EpiStats {
             m2 = cm2;
         }
         float cs0 = 0.f, cs1 = 0.f, cu0 = 0.f, cu1 = 0.f;
+        float ev[32];
         if (full) {
 #pragma unroll
             for (int k = 0; k < 32; k += 2) {
                 const float d0 = fmaf(a[k], p.c2, -m2);
                 const float d1 = fmaf(a[k + 1], p.c2, -m2);
-                const float e0 = exp2_approx(d0);
-                const float e1 = exp2_approx(d1);
-                cs0 += e0;
-                cs1 += e1;
-                cu0 = fmaf(e0, d0, cu0);
-                cu1 = fmaf(e1, d1, cu1);
+                ev[k] = exp2_approx(d0);
+                ev[k + 1] = exp2_approx(d1);
+                cs0 += ev[k];
+                cs1 += ev[k + 1];
+                cu0 = fmaf(ev[k], d0, cu0);
+                cu1 = fmaf(ev[k + 1], d1, cu1);
             }
         } else {
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
                 const float d = fmaxf(fmaf(a[k], p.c2, -m2), -1e30f);
-                const float e = exp2_approx(d);
-                cs0 += e;
-                cu0 = fmaf(e, d, cu0);
+                ev[k] = exp2_approx(d);
+                cs0 += ev[k];
+                cu0 = fmaf(ev[k], d, cu0);
             }
         }
         kahan_add(s, sc, cs0 + cs1);
         kahan_add(u2, uc, cu0 + cu1);
+        if (p.E32 != nullptr) {
+            float4* dst = reinterpret_cast<float4*>(p.E32 + t * static_cast<int64_t>(p.V) + col0);
+            const int nv = p.V - col0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q * 4 < nv) dst[q] = make_float4(ev[4 * q], ev[4 * q + 1], ev[4 * q + 2], ev[4 * q + 3]);
+            p.M2[t * p.ldm + (col0 >> 5)] = m2;
+        } else if (p.E != nullptr) {
+            uint32_t h[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const __half2 v = __floats2half2_rn(ev[2 * k], ev[2 * k + 1]);
+                h[k] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(p.E + t * static_cast<int64_t>(p.V) + col0);
+            const int nv = p.V - col0;   // multiple of 8
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (q * 8 < nv) dst[q] = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+            p.M2[t * p.ldm + (col0 >> 5)] = m2;
+        }
         // z exactly as the backward's recompute forms it: one rounded multiply by 1/T
         if (static_cast<unsigned>(label - col0) < 32u)
             p.zlab[t] = __fmul_rn(select32(a, label - col0), p.inv_T);
@@ -609,11 +639,16 @@ __global__ void metrics_final_kernel(const double* part, int nblk, rl_head_metri
 
 int metrics_impl(const rl_head_batch* b, const void* saved, rl_head_metrics* metrics, void* ws,
                  cudaStream_t stream) {
-    const SavedView sv = saved_view(const_cast<void*>(saved), b->N, b->support.nnz, nullptr);
     const FwdWs w = fwd_ws_view(ws, b->N, b->H, b->V, b->support.nnz, nullptr);
+    return metrics_run(b, saved, metrics, w.mpart, stream);
+}
+
+int metrics_run(const rl_head_batch* b, const void* saved, rl_head_metrics* metrics, double* mpart,
+                cudaStream_t stream) {
+    const SavedView sv = saved_view(const_cast<void*>(saved), b->N, b->support.nnz, nullptr);
     ProfScope ps(RL_PROF_METRICS, stream);
-    metrics_partial_kernel<<<kMetricBlocks, 256, 0, stream>>>(sv.mterm, b->N, w.mpart);
-    metrics_final_kernel<<<1, 32, 0, stream>>>(w.mpart, kMetricBlocks, metrics);
+    metrics_partial_kernel<<<kMetricBlocks, 256, 0, stream>>>(sv.mterm, b->N, mpart);
+    metrics_final_kernel<<<1, 32, 0, stream>>>(mpart, kMetricBlocks, metrics);
     count_launch(2);
     return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }
@@ -621,6 +656,99 @@ int metrics_impl(const rl_head_batch* b, const void* saved, rl_head_metrics* met
 // ----------------------------------------------------------------------------------
 // Entry
 // ----------------------------------------------------------------------------------
+// GEMM + per-token loss for token rows [c0, c0 + n): per-token pointers are offset by c0,
+// CSR entry arrays stay absolute.  With E != nullptr the GEMM also stores the fp16 e
+// values and their per-chunk reference (fused forward + backward).
+int fwd_rows(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out, const SavedView& sv,
+             const FwdWs& w, int64_t c0, int64_t n, uint16_t* E, float* E32, float* M2, int sparse,
+             int32_t* status, cudaStream_t stream) {
+    const int64_t H = b->H, V = b->V, nnz = b->support.nnz;
+    if (n <= 0) return RL_OK;
+    const int S = choose_splits(n, V);
+    CUtensorMap tmX, tmW;
+    const uint16_t* Xc = static_cast<const uint16_t*>(b->hidden) + c0 * H;
+    int rc = make_tmap_bf16(&tmX, Xc, n, H, H, kBM);
+    if (rc != RL_OK) return rc;
+    rc = make_tmap_bf16(&tmW, b->weight, V, H, H, kBN);
+    if (rc != RL_OK) return rc;
+    const GemmPlan plan = make_plan(n, V, H, 1, S, 1, status);
+    EpiStats::Params ep{n,
+                        static_cast<int32_t>(V),
+                        1.0f / prm->temperature,
+                        kLog2e / prm->temperature,
+                        nnz,
+                        b->labels + c0,
+                        b->support.offsets + c0,
+                        b->support.ids,
+                        sv.zlab + c0,
+                        sv.zsup,
+                        w.part_m,
+                        w.part_s,
+                        w.part_u,
+                        E,
+                        E32,
+                        M2,
+                        (V + 31) / 32};
+    {
+        ProfScope ps(RL_PROF_GEMM_FWD, stream);
+        rc = launch_gemm<EpiStats>(tmX, tmX, tmW, plan, ep, stream);
+    }
+    count_launch();
+    if (rc != RL_OK) return rc;
+
+    auto off = [c0](auto* p) { return p ? p + c0 : p; };
+    TokenArgs ta;
+    ta.N = n;
+    ta.V = static_cast<int32_t>(V);
+    ta.S = 2 * plan.n_splits;
+    ta.nnz = nnz;
+    ta.part_m = w.part_m;
+    ta.part_s = w.part_s;
+    ta.part_u = w.part_u;
+    ta.zlab = sv.zlab + c0;
+    ta.zsup = sv.zsup;
+    ta.labels = b->labels + c0;
+    ta.label_logq = b->label_logq + c0;
+    ta.adv = b->adv + c0;
+    ta.loss_mask = off(b->loss_mask);
+    ta.age = off(b->age);
+    ta.offsets = b->support.offsets + c0;
+    ta.ids = b->support.ids;
+    ta.logq = b->support.logq;
+    ta.replayed = b->support.replayed + c0;
+    ta.loss_type = prm->loss_type;
+    ta.kl_est = prm->kl_estimator;
+    ta.kl_stale = prm->kl_staleness;
+    ta.sparse = sparse;
+    ta.eps = prm->eps;
+    ta.cap = prm->max_importance_ratio;
+    ta.lo = prm->icepop_low;
+    ta.hi = prm->icepop_high;
+    ta.adv_tau = prm->adv_tau;
+    ta.kl_coeff = prm->kl_coeff;
+    ta.loss = out->loss + c0;
+    ta.logp_label = off(out->logp_label);
+    ta.logp_support = out->logp_support;
+    ta.entropy = off(out->entropy);
+    ta.lse_out = off(out->lse);
+    ta.mask_label = off(out->mask_label);
+    ta.mask_support = out->mask_support;
+    ta.sv = sv;
+    ta.sv.lse = sv.lse + c0;
+    ta.sv.lse_s = sv.lse_s + c0;
+    ta.sv.dcoef = sv.dcoef + c0;
+    ta.sv.labcoef = sv.labcoef + c0;
+    ta.sv.mterm = sv.mterm + c0 * 8;
+    ta.sv.zlab = sv.zlab + c0;
+    ta.status = status;
+    {
+        ProfScope ps(RL_PROF_TOKEN_LOSS, stream);
+        token_loss_kernel<<<static_cast<unsigned>((n + 7) / 8), 256, 0, stream>>>(ta);
+    }
+    count_launch();
+    return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
 int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out,
                   void* saved, void* ws, int32_t* status, cudaStream_t stream) {
     const int64_t N = b->N, H = b->H, V = b->V, nnz = b->support.nnz;
@@ -629,78 +757,8 @@ int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_ou
     if (N == 0) return RL_OK;
     const SavedView sv = saved_view(saved, N, nnz, nullptr);
     const FwdWs w = fwd_ws_view(ws, N, H, V, nnz, nullptr);
-    const int S = choose_splits(N, V);
-
-    CUtensorMap tmX, tmW;
-    rc = make_tmap_bf16(&tmX, b->hidden, N, H, H, kBM);
+    rc = fwd_rows(b, prm, out, sv, w, 0, N, nullptr, nullptr, nullptr, !bwd_is_dense(prm), status, stream);
     if (rc != RL_OK) return rc;
-    rc = make_tmap_bf16(&tmW, b->weight, V, H, H, kBN);
-    if (rc != RL_OK) return rc;
-    const GemmPlan plan = make_plan(N, V, H, 1, S, 1, status);
-    EpiStats::Params ep{N,
-                        static_cast<int32_t>(V),
-                        1.0f / prm->temperature,
-                        kLog2e / prm->temperature,
-                        nnz,
-                        b->labels,
-                        b->support.offsets,
-                        b->support.ids,
-                        sv.zlab,
-                        sv.zsup,
-                        w.part_m,
-                        w.part_s,
-                        w.part_u};
-    {
-        ProfScope ps(RL_PROF_GEMM_FWD, stream);
-        rc = launch_gemm<EpiStats>(tmX, tmX, tmW, plan, ep, stream);
-    }
-    count_launch();
-    if (rc != RL_OK) return rc;
-
-    TokenArgs ta;
-    ta.N = N;
-    ta.V = static_cast<int32_t>(V);
-    ta.S = 2 * plan.n_splits;
-    ta.nnz = nnz;
-    ta.part_m = w.part_m;
-    ta.part_s = w.part_s;
-    ta.part_u = w.part_u;
-    ta.zlab = sv.zlab;
-    ta.zsup = sv.zsup;
-    ta.labels = b->labels;
-    ta.label_logq = b->label_logq;
-    ta.adv = b->adv;
-    ta.loss_mask = b->loss_mask;
-    ta.age = b->age;
-    ta.offsets = b->support.offsets;
-    ta.ids = b->support.ids;
-    ta.logq = b->support.logq;
-    ta.replayed = b->support.replayed;
-    ta.loss_type = prm->loss_type;
-    ta.kl_est = prm->kl_estimator;
-    ta.kl_stale = prm->kl_staleness;
-    ta.sparse = !bwd_is_dense(prm);
-    ta.eps = prm->eps;
-    ta.cap = prm->max_importance_ratio;
-    ta.lo = prm->icepop_low;
-    ta.hi = prm->icepop_high;
-    ta.adv_tau = prm->adv_tau;
-    ta.kl_coeff = prm->kl_coeff;
-    ta.loss = out->loss;
-    ta.logp_label = out->logp_label;
-    ta.logp_support = out->logp_support;
-    ta.entropy = out->entropy;
-    ta.lse_out = out->lse;
-    ta.mask_label = out->mask_label;
-    ta.mask_support = out->mask_support;
-    ta.sv = sv;
-    ta.status = status;
-    {
-        ProfScope ps(RL_PROF_TOKEN_LOSS, stream);
-        token_loss_kernel<<<static_cast<unsigned>((N + 7) / 8), 256, 0, stream>>>(ta);
-    }
-    count_launch();
-    if (cudaPeekAtLastError() != cudaSuccess) return RL_ERR_CUDA;
     if (out->metrics) return metrics_impl(b, saved, out->metrics, ws, stream);
     return RL_OK;
 }

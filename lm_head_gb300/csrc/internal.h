@@ -60,6 +60,7 @@ struct BwdWs {
     void* G_lo;           // split only
     void* Gt_lo;
     float* dxs;           // [N, H] fp32 sparse part of dX
+    float* resid;         // [nnz + N] what bf16 rounding of the dense G drops at each spike
     int32_t* item_tok;    // [nnz + N] token of each gradient item
     int32_t* keys_a;      // radix-sort double buffers (vocab id keys, item payloads)
     int32_t* vals_a;
@@ -89,7 +90,17 @@ int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_ou
                   void* saved, void* ws, int32_t* status, cudaStream_t stream);
 int metrics_impl(const rl_head_batch* b, const void* saved, rl_head_metrics* metrics, void* ws,
                  cudaStream_t stream);
+int metrics_run(const rl_head_batch* b, const void* saved, rl_head_metrics* metrics, double* mpart,
+                cudaStream_t stream);
+int fwd_rows(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out, const SavedView& sv,
+             const FwdWs& w, int64_t c0, int64_t n, uint16_t* E, float* E32, float* M2, int sparse,
+             int32_t* status, cudaStream_t stream);
+int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out,
+                    const float* dloss, void* dhidden, float* dW, int accumulate, void* saved, void* ws,
+                    int32_t* status, cudaStream_t stream);
+size_t fused_ws_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* prm);
 int validate_impl(const rl_head_batch* b, int32_t* status, cudaStream_t stream);
+int64_t bwd_chunk(int64_t N, const rl_params* prm);
 int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* saved,
                   const float* dloss, void* dhidden, float* dW, int accumulate, void* ws,
                   int32_t* status, cudaStream_t stream);

@@ -93,3 +93,24 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
     pp = rh.PgParams(clip_ratio_c=0.5).c()
     assert lib.rl_policy_loss_elementwise(None, None, None, None, None, 10, ctypes.byref(pp), None, None, None,
                                           None, None, None, 0, None) == rh.RL_ERR_ARG
+
+
+def _declared_arity():
+    """Number of parameters of each rl_* function declared in include/*.h."""
+    out = {}
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"\b(rl_\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
+            args = m.group(2).strip()
+            out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_header_arity():
+    declared = _declared_arity()
+    for name, (_, args) in rh._SIGS.items():
+        assert name in declared, name
+        assert len(args) == declared[name], (name, len(args), declared[name])

@@ -227,3 +227,71 @@ def test_corrupt_support_sets_status_bits_without_trapping():
     ok = rh.rl_head_loss_fwd(rh.HeadBatch.from_case(bad), hp)
     torch.cuda.synchronize()
     assert ok.status_bits() == 0
+
+
+def check_fused(case, hp, reading=None, dloss=None):
+    """rl_head_loss_fwd_bwd (dloss given up front) against the oracle: every forward
+    output and both gradients, in the gradient precision of hp."""
+    dev = case.to("cuda")
+    batch = rh.HeadBatch.from_case(dev)
+    inp = case.numpy()
+    op = oracle_params(hp)
+    mask = inp["loss_mask"].astype(bool)
+    if dloss is None:
+        dloss = mask.astype(np.float32) / np.float32(max(int(mask.sum()), 1))
+    dl = torch.from_numpy(np.asarray(dloss, np.float32)).cuda()
+    fwd, dX, dW = rh.rl_head_loss_fwd_bwd(batch, hp, dl)
+    torch.cuda.synchronize()
+    ref = oracle.head_forward(inp, op)
+    check_forward(case, hp, fwd, ref)
+    rX, rW, bX, bW = oracle.head_backward(inp, op, np.asarray(dloss, np.float64), want_bounds=True)
+    rd = reading or ("element" if hp.grad_precision == rh.RL_GRAD_SPLIT else "operand")
+    grad_check(dX.float().cpu().numpy(), rX, rd, "dX", bX)
+    grad_check(dW.cpu().numpy(), rW, rd, "dW", bW)
+    return fwd, dX, dW
+
+
+@pytest.mark.parametrize("prec", [rh.RL_GRAD_BF16, rh.RL_GRAD_SPLIT])
+@pytest.mark.parametrize("loss_type", [rh.RL_LOSS_IPO, rh.RL_LOSS_ICEPOP])
+def test_fused_forward_backward_multi_chunk(loss_type, prec):
+    """Fused path over 3 token chunks (128, 128, 44): forward outputs and gradients."""
+    case = workloads.make_head_case("c1", n_tokens=300, hidden_scale=8.0, noise=0.7, loss_mask_frac=0.1,
+                                    age_max=4, seed=81 + loss_type)
+    hp = rh.HeadParams(loss_type=loss_type, eps=0.2, max_importance_ratio=3.0, kl_coeff=0.03,
+                       kl_estimator=rh.RL_KL_EXACT, kl_staleness=rh.RL_STALE_INV_SQRT, bwd_mode=rh.RL_BWD_DENSE,
+                       grad_precision=prec, token_chunk=128)
+    check_fused(case, hp)
+
+
+def test_fused_c1_and_matches_unfused():
+    """The tiny config through the fused call; its gradients agree with the recompute
+    path to bf16 rounding of G."""
+    case = workloads.make_head_case("c1")
+    hp = rh.HeadParams(**C1_IPO, bwd_mode=rh.RL_BWD_DENSE)
+    fwd, dX, dW = check_fused(case, hp)
+    dev = case.to("cuda")
+    batch = rh.HeadBatch.from_case(dev)
+    f2 = rh.rl_head_loss_fwd(batch, hp)
+    dl = torch.full((case.N,), 1.0 / case.N, device="cuda")
+    dX2, dW2, _ = rh.rl_head_loss_bwd(batch, hp, f2.saved, dl)
+    torch.cuda.synchronize()
+    assert torch.equal(fwd.loss, f2.loss) and torch.equal(fwd.logp_support, f2.logp_support)
+    scale = dW2.abs().max().item()
+    assert (dW - dW2).abs().max().item() <= 2 ** -7 * scale
+
+
+def test_fused_sparse_mode_and_replay():
+    case = workloads.make_head_case("c1", n_tokens=200, support="replay", top_p=0.9, hidden_scale=6.0,
+                                    noise=0.3, seed=91)
+    hp = rh.HeadParams(loss_type=rh.RL_LOSS_IPO, kl_coeff=0.02, all_replayed=1)
+    check_fused(case, hp, reading="element")
+
+
+def test_recompute_path_multi_chunk():
+    case = workloads.make_head_case("c1", n_tokens=300, hidden_scale=8.0, noise=0.7, seed=101)
+    hp = rh.HeadParams(loss_type=rh.RL_LOSS_IPO, eps=0.2, kl_coeff=0.03, bwd_mode=rh.RL_BWD_DENSE,
+                       token_chunk=128)
+    dev, batch, fwd = _forward(case, hp)
+    ref = oracle.head_forward(case.numpy(), oracle_params(hp))
+    check_forward(case, hp, fwd, ref)
+    check_backward(case, hp, batch, fwd)
