@@ -115,6 +115,24 @@ RL_DEVINL void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst, int
         : "memory");
 }
 
+// 2-D tiled bulk tensor store shared -> global (bulk-group completion).  Elements of the
+// box outside the tensor are not written.
+RL_DEVINL void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(smem_addr(src))
+                 : "memory");
+}
+RL_DEVINL void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N committed bulk groups still read their shared-memory source.
+template <int N>
+RL_DEVINL void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+RL_DEVINL void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA).
+RL_DEVINL void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------------
 // tcgen05: TMEM allocation, UMMA (kind::f16, bf16 x bf16 -> fp32), commit, loads
 // ---------------------------------------------------------------------------------

@@ -43,7 +43,9 @@ constexpr int kStageBytes = kATileBytes + kBTileBytes;
 constexpr int kEpiWarps = 8;
 constexpr int kGemmThreads = 64 + 32 * kEpiWarps;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 + 256;
+// Per epilogue warp: 4 KB of shared memory to stage tiles for TMA stores.
+constexpr int kEpiStageBytes = 4096;
+constexpr int kGemmSmemBytes = kStages * kStageBytes + kEpiWarps * kEpiStageBytes + 1024 + 256;
 constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN);
 
 struct GemmPlan {
@@ -95,22 +97,24 @@ RL_DEVINL void tmem_load_row32(uint32_t taddr, uint32_t (&r)[32]) {
 
 // Epilogue policy interface (all device, per thread; `row` in [0, 128), `half` 0/1 says
 // which 128 columns of every 256-column tile this thread sees; `col_begin` is the first
-// column it will see in the unit):
+// column it will see in the unit; `stage` is the warp's kEpiStageBytes of shared memory
+// for TMA stores, `lane` the thread's lane; chunk() is entered by all 32 lanes together):
 //   struct Epi {
 //     struct Params { ... };
 //     __device__ void begin_unit(const Params&, int row, int half, int m_blk, int split, int col_begin);
-//     __device__ void chunk(const Params&, const uint32_t (&acc)[32], int col0);
+//     __device__ void chunk(const Params&, const uint32_t (&acc)[32], int col0, uint8_t* stage, int lane);
 //     __device__ void end_unit(const Params&, int split, int half);
 //   };
 template <class Epi>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const GemmPlan plan,
-                   const typename Epi::Params ep) {
+                   const __grid_constant__ typename Epi::Params ep) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint8_t* epi_stage = smem + kStages * kStageBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(epi_stage + kEpiWarps * kEpiStageBytes);
     uint64_t* empty = full + kStages;
     uint64_t* accf = empty + kStages;
     uint64_t* acce = accf + 2;
@@ -263,6 +267,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int quarter = warp & 3;
         const int half = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
+        uint8_t* my_stage = epi_stage + (warp - 2) * kEpiStageBytes;
         uint32_t abuf = 0, aphase = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < plan.num_units && ok; u += gridDim.x) {
@@ -283,7 +288,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     uint32_t acc[32];
                     __syncwarp();
                     tmem_load_row32(taddr + ch * 32, acc);
-                    epi.chunk(ep, acc, nb * kBN + ch * 32);
+                    epi.chunk(ep, acc, nb * kBN + ch * 32, my_stage, lane);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -293,6 +298,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             if (ok) epi.end_unit(ep, c.split, half);
         }
+        if (lane == 0) bulk_wait_all();   // every TMA store of this warp has landed
     }
 
     tc_fence_before();
@@ -310,6 +316,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // box = box_rows x 64 columns, 128-byte swizzle, zero fill out of bounds.
 int make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
                    int box_rows);
+
+// General 2-D tensor map: [rows, cols] with row stride `ld` elements, box box_rows x box_cols.
+int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, int64_t rows,
+                 int64_t cols, int64_t ld, int box_cols, int box_rows, int swizzle128);
 
 int num_sms();
 

@@ -17,7 +17,7 @@ struct EpiStore {
         t = static_cast<int64_t>(m_blk) * kBM + row;
         valid = t < p.M;
     }
-    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0) {
+    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0, uint8_t*, int) {
         if (!valid || col0 >= p.N) return;
         float* d = p.D + t * p.N + col0;
         if (col0 + 32 <= p.N) {

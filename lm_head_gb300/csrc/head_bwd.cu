@@ -129,7 +129,7 @@ struct EpiGrad {
             lse = p.lse[t];
         }
     }
-    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0) {
+    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0, uint8_t*, int) {
         if (!valid || col0 >= p.V) return;
         const int nvalid = p.V - col0 < 32 ? p.V - col0 : 32;  // multiple of 8
         float g[32];
@@ -185,7 +185,7 @@ struct EpiDx {
         t = static_cast<int64_t>(m_blk) * kBM + row;
         valid = t < p.n;
     }
-    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0) {
+    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0, uint8_t*, int) {
         if (!valid || col0 >= p.H) return;
         const float4* s = reinterpret_cast<const float4*>(p.dxs + t * p.H + col0);
         uint4* o = reinterpret_cast<uint4*>(p.out + t * p.H + col0);
@@ -215,7 +215,7 @@ struct EpiDw {
         v = static_cast<int64_t>(m_blk) * kBM + row;
         valid = v < p.V;
     }
-    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0) {
+    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0, uint8_t*, int) {
         if (!valid || col0 >= p.H) return;
         float4* d = reinterpret_cast<float4*>(p.dW + v * p.H + col0);
 #pragma unroll
@@ -734,89 +734,75 @@ constexpr int kGradTileT = 64;    // tokens per block
 constexpr int kGradTileV = 128;   // vocabulary ids per block
 constexpr int kGradPitch = 72;    // smem row pitch (halfwords): 144 B keeps 16-byte rows
 
-// G = F e with one factor F = alpha 2^(m2 - lse log2 e) per row and 32-column chunk, written
-// row-major (16-byte stores) and, through a transposed smem tile, as G^T (16-byte stores).
-// Thread (r = tid / 4, c = tid % 4) converts token r's columns [32 c, 32 c + 32).
+// G = F e with one factor F = alpha 2^(m2 - lse log2 e) per row and 32-column chunk.
+// Row-major pass: 16 threads cover one token's 128 columns (8 each), so loads of e and
+// stores of G are full 256-byte row segments.  The tile is kept transposed in shared
+// memory (token index XOR-swizzled by 8 per 8-column group against bank conflicts) and
+// written as G^T with 16-byte stores, 8 threads per vocabulary row.
 __global__ void __launch_bounds__(256) grad_from_e_kernel(GradEArgs a) {
     __shared__ __align__(16) uint16_t th[kGradTileV][kGradPitch];
     __shared__ __align__(16) uint16_t tl[kGradTileV][kGradPitch];
-    const int tid = threadIdx.x, r = tid >> 2, c = tid & 3;
-    const int64_t t = static_cast<int64_t>(blockIdx.y) * kGradTileT + r;
-    const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kGradTileV + c * 32;
+    const int tid = threadIdx.x;
+    const int g = tid & 15;
+    const int sw = (g & 7) << 3;
+    const int64_t v = static_cast<int64_t>(blockIdx.x) * kGradTileV + g * 8;
     const bool split = a.G_lo != nullptr;
-    uint32_t hi[16], lo[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) hi[k] = lo[k] = 0u;
-    int nv = 0;
-    if (t < a.n && v0 < a.V) {
-        nv = a.V - v0 < 32 ? static_cast<int>(a.V - v0) : 32;   // multiple of 8
-        const float alpha = dense_alpha(a.dloss[t], a.dcoef[t], a.inv_T);
-        const float F = fused_factor(alpha, a.M2[t * a.ldm + (v0 >> 5)], a.lse[t]);
-        float e[32];
-        if (a.E32) {
-            const float4* src = reinterpret_cast<const float4*>(a.E32 + t * a.V + v0);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 x = q * 4 < nv ? src[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-                e[4 * q] = x.x;
-                e[4 * q + 1] = x.y;
-                e[4 * q + 2] = x.z;
-                e[4 * q + 3] = x.w;
-            }
-        } else {
-            const uint4* src = reinterpret_cast<const uint4*>(a.E + t * a.V + v0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const uint4 x = q * 8 < nv ? src[q] : make_uint4(0u, 0u, 0u, 0u);
+    for (int pass = 0; pass < kGradTileT / 16; ++pass) {
+        const int r = pass * 16 + (tid >> 4);
+        const int64_t t = static_cast<int64_t>(blockIdx.y) * kGradTileT + r;
+        uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
+        if (t < a.n && v < a.V) {
+            const float alpha = dense_alpha(a.dloss[t], a.dcoef[t], a.inv_T);
+            const float F = fused_factor(alpha, a.M2[t * a.ldm + (v >> 5)], a.lse[t]);
+            float e[8];
+            if (a.E32) {
+                const float4* src = reinterpret_cast<const float4*>(a.E32 + t * a.V + v);
+                const float4 x0 = src[0], x1 = src[1];
+                e[0] = x0.x; e[1] = x0.y; e[2] = x0.z; e[3] = x0.w;
+                e[4] = x1.x; e[5] = x1.y; e[6] = x1.z; e[7] = x1.w;
+            } else {
+                const uint4 x = *reinterpret_cast<const uint4*>(a.E + t * a.V + v);
                 const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    e[8 * q + 2 * k] = __half2float(__ushort_as_half(static_cast<uint16_t>(w[k] & 0xFFFFu)));
-                    e[8 * q + 2 * k + 1] = __half2float(__ushort_as_half(static_cast<uint16_t>(w[k] >> 16)));
+                    e[2 * k] = __half2float(__ushort_as_half(static_cast<uint16_t>(w[k] & 0xFFFFu)));
+                    e[2 * k + 1] = __half2float(__ushort_as_half(static_cast<uint16_t>(w[k] >> 16)));
                 }
             }
-        }
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const float g0 = __fmul_rn(F, e[2 * k]), g1 = __fmul_rn(F, e[2 * k + 1]);
-            hi[k] = pack_bf16x2(g0, g1);
-            if (split) {
-                const float h0 = bf16_bits_to_float(static_cast<uint16_t>(hi[k] & 0xFFFFu));
-                const float h1 = bf16_bits_to_float(static_cast<uint16_t>(hi[k] >> 16));
-                lo[k] = pack_bf16x2(g0 - h0, g1 - h1);
+            for (int k = 0; k < 4; ++k) {
+                const float g0 = __fmul_rn(F, e[2 * k]), g1 = __fmul_rn(F, e[2 * k + 1]);
+                hi[k] = pack_bf16x2(g0, g1);
+                if (split) {
+                    const float h0 = bf16_bits_to_float(static_cast<uint16_t>(hi[k] & 0xFFFFu));
+                    const float h1 = bf16_bits_to_float(static_cast<uint16_t>(hi[k] >> 16));
+                    lo[k] = pack_bf16x2(g0 - h0, g1 - h1);
+                }
             }
+            *reinterpret_cast<uint4*>(a.G + t * a.V + v) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            if (split) *reinterpret_cast<uint4*>(a.G_lo + t * a.V + v) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        uint4* gd = reinterpret_cast<uint4*>(a.G + t * a.V + v0);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            if (q * 8 < nv) gd[q] = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
-        if (split) {
-            uint4* ld = reinterpret_cast<uint4*>(a.G_lo + t * a.V + v0);
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (q * 8 < nv) ld[q] = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
+        for (int k = 0; k < 8; ++k) {
+            th[g * 8 + k][r ^ sw] = static_cast<uint16_t>((k & 1) ? (hi[k >> 1] >> 16) : (hi[k >> 1] & 0xFFFFu));
+            if (split) tl[g * 8 + k][r ^ sw] = static_cast<uint16_t>((k & 1) ? (lo[k >> 1] >> 16) : (lo[k >> 1] & 0xFFFFu));
         }
-    }
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-        th[c * 32 + k][r] = static_cast<uint16_t>((k & 1) ? (hi[k >> 1] >> 16) : (hi[k >> 1] & 0xFFFFu));
-        if (split) tl[c * 32 + k][r] = static_cast<uint16_t>((k & 1) ? (lo[k >> 1] >> 16) : (lo[k >> 1] & 0xFFFFu));
     }
     __syncthreads();
-    // G^T rows: 8 threads per vocabulary id, 8 tokens (16 B) each
     const int64_t tbase = static_cast<int64_t>(blockIdx.y) * kGradTileT;
     for (int row = tid >> 3; row < kGradTileV; row += 32) {
-        const int64_t v = static_cast<int64_t>(blockIdx.x) * kGradTileV + row;
+        const int64_t vr = static_cast<int64_t>(blockIdx.x) * kGradTileV + row;
+        if (vr >= a.V) continue;
         const int j = (tid & 7) * 8;
-        if (v >= a.V) continue;
+        const int jp = j ^ (((row >> 3) & 7) << 3);
         const int64_t tt = tbase + j;
         if (tt + 8 <= a.n) {
-            *reinterpret_cast<uint4*>(a.Gt + v * a.ldt + tt) = *reinterpret_cast<const uint4*>(&th[row][j]);
-            if (split) *reinterpret_cast<uint4*>(a.Gt_lo + v * a.ldt + tt) = *reinterpret_cast<const uint4*>(&tl[row][j]);
+            *reinterpret_cast<uint4*>(a.Gt + vr * a.ldt + tt) = *reinterpret_cast<const uint4*>(&th[row][jp]);
+            if (split) *reinterpret_cast<uint4*>(a.Gt_lo + vr * a.ldt + tt) = *reinterpret_cast<const uint4*>(&tl[row][jp]);
         } else {
             for (int k = 0; k < 8 && tt + k < a.n; ++k) {
-                a.Gt[v * a.ldt + tt + k] = th[row][j + k];
-                if (split) a.Gt_lo[v * a.ldt + tt + k] = tl[row][j + k];
+                a.Gt[vr * a.ldt + tt + k] = th[row][jp + k];
+                if (split) a.Gt_lo[vr * a.ldt + tt + k] = tl[row][jp + k];
             }
         }
     }

@@ -12,6 +12,7 @@
 //   4. metrics kernels     deterministic fp64 reduction of the metric terms
 #include <cmath>
 #include <climits>
+#include <cstring>
 
 #include <cuda_fp16.h>
 
@@ -205,6 +206,7 @@ struct EpiStats {
         float* E32;      // fp32 instead of fp16 (hi/lo gradient precision)
         float* M2;
         int64_t ldm;
+        CUtensorMap tmE;  // over E (fp16) or E32 ([N, V], box 32 x 32, no swizzle)
     };
     int64_t t;
     bool valid;
@@ -241,8 +243,62 @@ struct EpiStats {
         next_id = ptr < end ? p.ids[ptr] : INT_MAX;
     }
 
-    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0) {
-        if (!valid || col0 >= p.V) return;
+    RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0, uint8_t* stage, int lane) {
+        if (col0 >= p.V) return;   // uniform over the warp
+        float ev[32];
+        if (valid) {
+            stats(p, acc, col0, ev);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) ev[k] = 0.f;
+        }
+        if (p.E != nullptr || p.E32 != nullptr) store_e(p, ev, col0, stage, lane);
+    }
+
+    // The warp's 32 rows of e go through shared memory and TMA stores (rows past N and
+    // columns past V are clipped by the tensor map).  The 4 KB staging tile uses the
+    // 128-byte swizzle (16-byte chunk c of row r at c ^ (r % 8)), so the 32 lanes write
+    // without bank conflicts.  fp32: one 32-column store per chunk; fp16: one 64-column
+    // store per pair of chunks.
+    RL_DEVINL void store_e(const Params& p, const float (&ev)[32], int col0, uint8_t* stage, int lane) {
+        const bool f32 = p.E32 != nullptr;
+        const int par = (col0 >> 5) & 1;
+        if (f32 || par == 0) {
+            if (lane == 0) bulk_wait_read<0>();   // the previous store has read the tile
+            __syncwarp();
+        }
+        uint8_t* row = stage + lane * 128;
+        const int sw = lane & 7;
+        if (f32) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4*>(row + ((q ^ sw) << 4)) =
+                    make_float4(ev[4 * q], ev[4 * q + 1], ev[4 * q + 2], ev[4 * q + 3]);
+        } else {
+            uint32_t h[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const __half2 v = __floats2half2_rn(ev[2 * k], ev[2 * k + 1]);
+                h[k] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(row + (((par * 4 + q) ^ sw) << 4)) =
+                    make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+        }
+        if (valid) p.M2[t * p.ldm + (col0 >> 5)] = m2;
+        const bool flush = f32 || par == 1 || col0 + 32 >= p.V;
+        if (flush) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {   // lane 0 holds the warp's first row
+                tma_store_2d(&p.tmE, stage, f32 ? col0 : (col0 & ~63), static_cast<int32_t>(t));
+                bulk_commit();
+            }
+        }
+    }
+
+    RL_DEVINL void stats(const Params& p, const uint32_t (&acc)[32], int col0, float (&ev)[32]) {
         float a[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) a[k] = __uint_as_float(acc[k]);
@@ -266,7 +322,6 @@ struct EpiStats {
             m2 = cm2;
         }
         float cs0 = 0.f, cs1 = 0.f, cu0 = 0.f, cu1 = 0.f;
-        float ev[32];
         if (full) {
 #pragma unroll
             for (int k = 0; k < 32; k += 2) {
@@ -290,27 +345,6 @@ struct EpiStats {
         }
         kahan_add(s, sc, cs0 + cs1);
         kahan_add(u2, uc, cu0 + cu1);
-        if (p.E32 != nullptr) {
-            float4* dst = reinterpret_cast<float4*>(p.E32 + t * static_cast<int64_t>(p.V) + col0);
-            const int nv = p.V - col0;
-#pragma unroll
-            for (int q = 0; q < 8; ++q)
-                if (q * 4 < nv) dst[q] = make_float4(ev[4 * q], ev[4 * q + 1], ev[4 * q + 2], ev[4 * q + 3]);
-            p.M2[t * p.ldm + (col0 >> 5)] = m2;
-        } else if (p.E != nullptr) {
-            uint32_t h[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const __half2 v = __floats2half2_rn(ev[2 * k], ev[2 * k + 1]);
-                h[k] = *reinterpret_cast<const uint32_t*>(&v);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(p.E + t * static_cast<int64_t>(p.V) + col0);
-            const int nv = p.V - col0;   // multiple of 8
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (q * 8 < nv) dst[q] = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-            p.M2[t * p.ldm + (col0 >> 5)] = m2;
-        }
         // z exactly as the backward's recompute forms it: one rounded multiply by 1/T
         if (static_cast<unsigned>(label - col0) < 32u)
             p.zlab[t] = __fmul_rn(select32(a, label - col0), p.inv_T);
@@ -672,6 +706,13 @@ int fwd_rows(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs
     rc = make_tmap_bf16(&tmW, b->weight, V, H, H, kBN);
     if (rc != RL_OK) return rc;
     const GemmPlan plan = make_plan(n, V, H, 1, S, 1, status);
+    CUtensorMap tmE;
+    std::memset(&tmE, 0, sizeof(tmE));
+    if (E32 != nullptr)
+        rc = make_tmap_2d(&tmE, E32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, n, V, V, 32, 32, 1);
+    else if (E != nullptr)
+        rc = make_tmap_2d(&tmE, E, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, n, V, V, 64, 32, 1);
+    if (rc != RL_OK) return rc;
     EpiStats::Params ep{n,
                         static_cast<int32_t>(V),
                         1.0f / prm->temperature,
@@ -688,7 +729,8 @@ int fwd_rows(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs
                         E,
                         E32,
                         M2,
-                        (V + 31) / 32};
+                        (V + 31) / 32,
+                        tmE};
     {
         ProfScope ps(RL_PROF_GEMM_FWD, stream);
         rc = launch_gemm<EpiStats>(tmX, tmX, tmW, plan, ep, stream);

@@ -121,6 +121,32 @@ int make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t col
     return RL_OK;
 }
 
+int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, int64_t rows,
+                 int64_t cols, int64_t ld, int box_cols, int box_rows, int swizzle128) {
+    auto fn = encode_fn();
+    if (!fn) {
+        set_last_error("cuTensorMapEncodeTiled unavailable");
+        return RL_ERR_CUDA;
+    }
+    if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (ld * elem_bytes) % 16 != 0 || rows <= 0 || cols <= 0) {
+        set_last_error("tensor map: misaligned base/stride or bad extent");
+        return RL_ERR_UNSUPPORTED;
+    }
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(ld * elem_bytes)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = fn(map, dtype, 2, const_cast<void*>(base), gdim, gstride, box, estride,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        set_last_error("cuTensorMapEncodeTiled failed");
+        return RL_ERR_CUDA;
+    }
+    return RL_OK;
+}
+
 GemmPlan make_plan(int64_t M, int64_t N, int64_t K, int passes, int n_splits, int m_fastest,
                    int32_t* status, int a_mn, int b_mn) {
     GemmPlan p;
