@@ -222,6 +222,8 @@ def run_ours(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     build.build()
     rh.load()
+    if args.gemm_pair is not None:
+        rh.rl_set_option(rh.RL_OPT_GEMM_PAIR, args.gemm_pair)
     peaks = load_peaks()
 
     t_gen = time.perf_counter()
@@ -362,6 +364,8 @@ def run_ours(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "N": N, "H": H, "V": V, "nnz": nnz,
                        "grad_precision": args.grad_precision, "parallelism": f"replicas x{world}",
+                       "gemm": "sm-pair (cta_group::2, 256x256)" if rh.rl_get_option(rh.RL_OPT_GEMM_PAIR) else
+                               "single-sm (128x256)",
                        "l2": "inputs larger than L2 (W 622 MB); 256 MB flush between timed steps"},
             "tc_peak_frac": step_tflops / peak_burst,
             "step_tflops_6NHV": step_tflops,
@@ -420,6 +424,8 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=None, help="fewer tokens, same shapes (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true", help="skip the two-call side figure")
+    ap.add_argument("--gemm-pair", type=int, choices=[0, 1], default=None,
+                    help="tensor-core GEMMs on SM pairs (1) or single SMs (0); default: library default")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

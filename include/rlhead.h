@@ -292,6 +292,14 @@ int rl_profile_enable(int on);
 int rl_profile_read(double* ms, int64_t* launches);
 const char* rl_profile_kind_name(int kind);
 
+/* Library options (process-wide, host side).  RL_OPT_GEMM_PAIR: 1 (the default) runs the
+ * tensor-core GEMMs on pairs of SMs (two-CTA clusters, tcgen05 cta_group::2, 256 x 256
+ * tiles); 0 on single SMs (128 x 256 tiles).  Results are the same to fp32 rounding.
+ * rl_set_option returns RL_ERR_ARG for an unknown key; rl_get_option returns -1. */
+#define RL_OPT_GEMM_PAIR 1
+int rl_set_option(int key, int value);
+int rl_get_option(int key);
+
 /* Synchronous device->host copy of the status word.  Call after the stream is done. */
 int rl_status_read(const int32_t* dev_status, int32_t* host_out);
 /* Kernels this library has launched in this process (for launch accounting). */

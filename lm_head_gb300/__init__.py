@@ -111,6 +111,8 @@ _SIGS = {
     "rl_gemm_bf16": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
                      + [ctypes.c_int64] * 3 + [ctypes.c_void_p] * 3),
     "rl_kernel_launch_count": (ctypes.c_int64, []),
+    "rl_set_option": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+    "rl_get_option": (ctypes.c_int, [ctypes.c_int]),
     "rl_profile_enable": (ctypes.c_int, [ctypes.c_int]),
     "rl_profile_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "rl_profile_kind_name": (ctypes.c_char_p, [ctypes.c_int]),
@@ -520,6 +522,17 @@ def rl_profile_read() -> dict:
     _check(lib.rl_profile_read(ctypes.cast(ms, ctypes.c_void_p), ctypes.cast(n, ctypes.c_void_p)))
     return {lib.rl_profile_kind_name(k).decode(): (float(ms[k]), int(n[k]))
             for k in range(RL_PROF_KINDS) if n[k] > 0}
+
+
+RL_OPT_GEMM_PAIR = 1
+
+
+def rl_set_option(key: int, value: int) -> None:
+    _check(load().rl_set_option(int(key), int(value)))
+
+
+def rl_get_option(key: int) -> int:
+    return int(load().rl_get_option(int(key)))
 
 
 def status_names(bits: int):

@@ -323,8 +323,10 @@ int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, 
 
 int num_sms();
 
+// pair = 1: m_blocks counts 256-row blocks of the two-CTA kernel.
 GemmPlan make_plan(int64_t M, int64_t N, int64_t K, int passes, int n_splits, int m_fastest,
-                   int32_t* status, int a_mn = 0, int b_mn = 0);
+                   int32_t* status, int a_mn = 0, int b_mn = 0, int pair = 0);
+int gemm_pair_mode();
 
 // Launch `gemm_tc_kernel<Epi>`; A2 may equal A when passes == 1.
 template <class Epi>

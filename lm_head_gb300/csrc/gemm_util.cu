@@ -1,7 +1,7 @@
 // rl_gemm_bf16_tn: the head contraction alone, D[M, N] (fp32) = A[M, K] B[N, K]^T with
 // bf16 K-major operands, through the same tcgen05 pipeline as the fused kernels and a
 // plain store epilogue.  Used to unit-test and time the tensor-core path in isolation.
-#include "gemm_tc.cuh"
+#include "gemm_tc2.cuh"
 #include "internal.h"
 
 namespace rl {
@@ -38,11 +38,19 @@ struct EpiStore {
 int gemm_util_impl(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
                    float* D, int32_t* status, cudaStream_t stream) {
     CUtensorMap ta, tb;
+    const int pair = gemm_pair_mode() && !a_mn && !b_mn;
     int rc = a_mn ? make_tmap_bf16(&ta, A, K, M, M, 64) : make_tmap_bf16(&ta, A, M, K, K, kBM);
     if (rc != RL_OK) return rc;
-    rc = b_mn ? make_tmap_bf16(&tb, B, K, N, N, 64) : make_tmap_bf16(&tb, B, N, K, K, kBN);
+    rc = b_mn ? make_tmap_bf16(&tb, B, K, N, N, 64) : make_tmap_bf16(&tb, B, N, K, K, pair ? kBN / 2 : kBN);
     if (rc != RL_OK) return rc;
-    const GemmPlan plan = make_plan(M, N, K, 1, 1 << 30, 1, status, a_mn, b_mn);
+    const GemmPlan plan = make_plan(M, N, K, 1, 1 << 30, 1, status, a_mn, b_mn, pair);
+    if (pair) {
+        EpiStore::Params ep{M, N, D};
+        ProfScope ps(RL_PROF_GEMM_UTIL, stream);
+        rc = launch_gemm_pair<EpiStore>(ta, ta, tb, plan, ep, stream);
+        count_launch();
+        return rc;
+    }
     EpiStore::Params ep{M, N, D};
     {
         ProfScope ps(RL_PROF_GEMM_UTIL, stream);

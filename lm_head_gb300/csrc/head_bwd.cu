@@ -17,7 +17,7 @@
 
 #include <cuda_fp16.h>
 
-#include "gemm_tc.cuh"
+#include "gemm_tc2.cuh"
 #include "internal.h"
 
 namespace rl {
@@ -659,9 +659,9 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
     if (rc != RL_OK) return rc;
 
     CUtensorMap tmW, tmWt;
-    rc = make_tmap_bf16(&tmW, b->weight, V, H, H, kBN);
+    rc = make_tmap_b(&tmW, b->weight, V, H, H);
     if (rc != RL_OK) return rc;
-    rc = make_tmap_bf16(&tmWt, w.Wt, H, V, V, kBN);
+    rc = make_tmap_b(&tmWt, w.Wt, H, V, V);
     if (rc != RL_OK) return rc;
     const int passes = w.split ? 2 : 1;
     for (int64_t c0 = 0; c0 < N; c0 += w.chunk) {
@@ -673,7 +673,7 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
         if ((rc = make_tmap_bf16(&tmX, Xc, n, H, H, kBM)) != RL_OK) return rc;
         if ((rc = make_tmap_bf16(&tmG, w.G, n, V, V, kBM)) != RL_OK) return rc;
         if ((rc = make_tmap_bf16(&tmGt, w.Gt, V, n, w.chunk, kBM)) != RL_OK) return rc;
-        if ((rc = make_tmap_bf16(&tmXt, w.Xt, H, n, w.chunk, kBN)) != RL_OK) return rc;
+        if ((rc = make_tmap_b(&tmXt, w.Xt, H, n, w.chunk)) != RL_OK) return rc;
         tmGlo = tmG;
         tmGtlo = tmGt;
         if (w.split) {
@@ -684,24 +684,24 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
         EpiGrad::Params gp{n, static_cast<int32_t>(V), 1.0f / prm->temperature, sv.lse + c0, dloss + c0,
                            sv.dcoef + c0, static_cast<uint16_t*>(w.G), static_cast<uint16_t*>(w.Gt),
                            static_cast<uint16_t*>(w.G_lo), static_cast<uint16_t*>(w.Gt_lo), w.chunk};
-        const GemmPlan p1 = make_plan(n, V, H, 1, 1 << 30, 1, status);
+        const GemmPlan p1 = make_plan_auto(n, V, H, 1, 1 << 30, 1, status);
         {
             ProfScope ps(RL_PROF_GEMM_GRAD, stream);
-            if ((rc = launch_gemm<EpiGrad>(tmX, tmX, tmW, p1, gp, stream)) != RL_OK) return rc;
+            if ((rc = launch_gemm_auto<EpiGrad>(tmX, tmX, tmW, p1, gp, stream)) != RL_OK) return rc;
         }
         // dX chunk = G W + sparse part
         EpiDx::Params dp{n, static_cast<int32_t>(H), w.dxs + c0 * H, static_cast<uint16_t*>(dhidden) + c0 * H};
-        const GemmPlan p2 = make_plan(n, H, V, passes, 1 << 30, 0, status);
+        const GemmPlan p2 = make_plan_auto(n, H, V, passes, 1 << 30, 0, status);
         {
             ProfScope ps(RL_PROF_GEMM_DX, stream);
-            if ((rc = launch_gemm<EpiDx>(tmG, tmGlo, tmWt, p2, dp, stream)) != RL_OK) return rc;
+            if ((rc = launch_gemm_auto<EpiDx>(tmG, tmGlo, tmWt, p2, dp, stream)) != RL_OK) return rc;
         }
         // dW += G^T X
         EpiDw::Params wp{V, static_cast<int32_t>(H), (c0 > 0 || accumulate) ? 1 : 0, dW};
-        const GemmPlan p3 = make_plan(V, H, n, passes, 1 << 30, 0, status);
+        const GemmPlan p3 = make_plan_auto(V, H, n, passes, 1 << 30, 0, status);
         {
             ProfScope ps(RL_PROF_GEMM_DW, stream);
-            if ((rc = launch_gemm<EpiDw>(tmGt, tmGtlo, tmXt, p3, wp, stream)) != RL_OK) return rc;
+            if ((rc = launch_gemm_auto<EpiDw>(tmGt, tmGtlo, tmXt, p3, wp, stream)) != RL_OK) return rc;
         }
         count_launch(3);
     }
@@ -897,7 +897,7 @@ int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_
     rc = transpose_bf16(b->weight, V, H, H, w.Wt, V, stream);
     if (rc != RL_OK) return rc;
     CUtensorMap tmWt;
-    if ((rc = make_tmap_bf16(&tmWt, w.Wt, H, V, V, kBN)) != RL_OK) return rc;
+    if ((rc = make_tmap_b(&tmWt, w.Wt, H, V, V)) != RL_OK) return rc;
     const int passes = w.split ? 2 : 1;
     for (int64_t c0 = 0; c0 < N; c0 += f.chunk) {
         const int64_t n = N - c0 < f.chunk ? N - c0 : f.chunk;
@@ -927,7 +927,7 @@ int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_
         CUtensorMap tmG, tmGlo, tmGt, tmGtlo, tmXt;
         if ((rc = make_tmap_bf16(&tmG, w.G, n, V, V, kBM)) != RL_OK) return rc;
         if ((rc = make_tmap_bf16(&tmGt, w.Gt, V, n, f.chunk, kBM)) != RL_OK) return rc;
-        if ((rc = make_tmap_bf16(&tmXt, w.Xt, H, n, f.chunk, kBN)) != RL_OK) return rc;
+        if ((rc = make_tmap_b(&tmXt, w.Xt, H, n, f.chunk)) != RL_OK) return rc;
         tmGlo = tmG;
         tmGtlo = tmGt;
         if (w.split) {
@@ -935,16 +935,16 @@ int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_
             if ((rc = make_tmap_bf16(&tmGtlo, w.Gt_lo, V, n, f.chunk, kBM)) != RL_OK) return rc;
         }
         EpiDx::Params dp{n, static_cast<int32_t>(H), w.dxs, static_cast<uint16_t*>(dhidden) + c0 * H};
-        const GemmPlan p2 = make_plan(n, H, V, passes, 1 << 30, 0, status);
+        const GemmPlan p2 = make_plan_auto(n, H, V, passes, 1 << 30, 0, status);
         {
             ProfScope ps(RL_PROF_GEMM_DX, stream);
-            if ((rc = launch_gemm<EpiDx>(tmG, tmGlo, tmWt, p2, dp, stream)) != RL_OK) return rc;
+            if ((rc = launch_gemm_auto<EpiDx>(tmG, tmGlo, tmWt, p2, dp, stream)) != RL_OK) return rc;
         }
         EpiDw::Params wp{V, static_cast<int32_t>(H), (c0 > 0 || accumulate) ? 1 : 0, dW};
-        const GemmPlan p3 = make_plan(V, H, n, passes, 1 << 30, 0, status);
+        const GemmPlan p3 = make_plan_auto(V, H, n, passes, 1 << 30, 0, status);
         {
             ProfScope ps(RL_PROF_GEMM_DW, stream);
-            if ((rc = launch_gemm<EpiDw>(tmGt, tmGtlo, tmXt, p3, wp, stream)) != RL_OK) return rc;
+            if ((rc = launch_gemm_auto<EpiDw>(tmGt, tmGtlo, tmXt, p3, wp, stream)) != RL_OK) return rc;
         }
         count_launch(2);
     }

@@ -16,7 +16,7 @@
 
 #include <cuda_fp16.h>
 
-#include "gemm_tc.cuh"
+#include "gemm_tc2.cuh"
 #include "internal.h"
 
 namespace rl {
@@ -60,8 +60,9 @@ FwdWs fwd_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz, size
 // Split count for the forward GEMM: units = m_blocks * splits spread over the SMs; pick
 // the count that fills the last wave best (ties -> fewer splits).
 static int choose_splits(int64_t N, int64_t V) {
-    const int m_blocks = static_cast<int>((N + kBM - 1) / kBM);
-    const int P = num_sms();
+    const int pair = gemm_pair_mode();
+    const int m_blocks = static_cast<int>((N + (pair ? 2 * kBM : kBM) - 1) / (pair ? 2 * kBM : kBM));
+    const int P = pair ? num_sms() / 2 : num_sms();
     const int smax = max_splits(V);
     int best = 1;
     double best_eff = 0.0;
@@ -703,9 +704,9 @@ int fwd_rows(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs
     const uint16_t* Xc = static_cast<const uint16_t*>(b->hidden) + c0 * H;
     int rc = make_tmap_bf16(&tmX, Xc, n, H, H, kBM);
     if (rc != RL_OK) return rc;
-    rc = make_tmap_bf16(&tmW, b->weight, V, H, H, kBN);
+    rc = make_tmap_b(&tmW, b->weight, V, H, H);
     if (rc != RL_OK) return rc;
-    const GemmPlan plan = make_plan(n, V, H, 1, S, 1, status);
+    const GemmPlan plan = make_plan_auto(n, V, H, 1, S, 1, status);
     CUtensorMap tmE;
     std::memset(&tmE, 0, sizeof(tmE));
     if (E32 != nullptr)
@@ -733,7 +734,7 @@ int fwd_rows(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs
                         tmE};
     {
         ProfScope ps(RL_PROF_GEMM_FWD, stream);
-        rc = launch_gemm<EpiStats>(tmX, tmX, tmW, plan, ep, stream);
+        rc = launch_gemm_auto<EpiStats>(tmX, tmX, tmW, plan, ep, stream);
     }
     count_launch();
     if (rc != RL_OK) return rc;

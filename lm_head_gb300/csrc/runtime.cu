@@ -13,6 +13,9 @@
 namespace rl {
 
 static std::atomic<int64_t> g_launches{0};
+static std::atomic<int> g_gemm_pair{1};
+
+int gemm_pair_mode() { return g_gemm_pair.load(std::memory_order_relaxed); }
 static thread_local char g_last_error[256] = "";
 
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
@@ -148,9 +151,10 @@ int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, 
 }
 
 GemmPlan make_plan(int64_t M, int64_t N, int64_t K, int passes, int n_splits, int m_fastest,
-                   int32_t* status, int a_mn, int b_mn) {
+                   int32_t* status, int a_mn, int b_mn, int pair) {
     GemmPlan p;
-    p.m_blocks = static_cast<int>((M + kBM - 1) / kBM);
+    const int64_t rows = pair ? 2 * kBM : kBM;
+    p.m_blocks = static_cast<int>((M + rows - 1) / rows);
     p.n_blocks = static_cast<int>((N + kBN - 1) / kBN);
     if (n_splits < 1) n_splits = 1;
     if (n_splits > p.n_blocks) n_splits = p.n_blocks;
@@ -171,6 +175,20 @@ GemmPlan make_plan(int64_t M, int64_t N, int64_t K, int passes, int n_splits, in
 int64_t rl_launch_counter_value() { return rl::g_launches.load(std::memory_order_relaxed); }
 
 extern "C" const char* rl_last_error(void) { return rl::g_last_error; }
+
+extern "C" int rl_set_option(int key, int value) {
+    if (key == RL_OPT_GEMM_PAIR) {
+        rl::g_gemm_pair.store(value ? 1 : 0, std::memory_order_relaxed);
+        return RL_OK;
+    }
+    rl::set_last_error("unknown option");
+    return RL_ERR_ARG;
+}
+
+extern "C" int rl_get_option(int key) {
+    if (key == RL_OPT_GEMM_PAIR) return rl::g_gemm_pair.load(std::memory_order_relaxed);
+    return -1;
+}
 
 extern "C" int rl_profile_enable(int on) {
     rl::Prof& p = rl::prof();
