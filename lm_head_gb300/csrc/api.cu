@@ -105,7 +105,8 @@ int rl_head_loss_fwd(const rl_head_batch* batch, const rl_params* params, const 
     int rc = check_batch(batch);
     if (rc != RL_OK) return rc;
     if ((rc = check_params(params)) != RL_OK) return rc;
-    if (!out || !out->loss || !saved || !dev_status) return fail(RL_ERR_ARG, "out/loss/saved/dev_status NULL");
+    if (!out || (batch->N > 0 && (!out->loss || !saved)) || !dev_status)
+        return fail(RL_ERR_ARG, "out/loss/saved/dev_status NULL");
     if (ws_bytes < rl_head_fwd_workspace_bytes(batch->N, batch->H, batch->V, batch->support.nnz, params))
         return fail(RL_ERR_WORKSPACE, "forward workspace too small");
     if (!ws) return fail(RL_ERR_ARG, "ws is NULL");
@@ -119,7 +120,7 @@ int rl_head_loss_bwd(const rl_head_batch* batch, const rl_params* params, const 
     int rc = check_batch(batch);
     if (rc != RL_OK) return rc;
     if ((rc = check_params(params)) != RL_OK) return rc;
-    if (!saved || !dloss || !dW || !dev_status || (batch->N > 0 && !dhidden))
+    if ((batch->N > 0 && (!saved || !dloss || !dhidden)) || !dW || !dev_status)
         return fail(RL_ERR_ARG, "saved/dloss/dhidden/dW/dev_status NULL");
     if (!aligned16(dW) || !aligned16(dhidden)) return fail(RL_ERR_ARG, "dW/dhidden not 16-byte aligned");
     if (ws_bytes < rl_head_bwd_workspace_bytes(batch->N, batch->H, batch->V, batch->support.nnz, params))
@@ -141,7 +142,8 @@ int rl_head_loss_fwd_bwd(const rl_head_batch* batch, const rl_params* params, co
     int rc = check_batch(batch);
     if (rc != RL_OK) return rc;
     if ((rc = check_params(params)) != RL_OK) return rc;
-    if (!out || !out->loss || !saved || !dev_status || !dloss || !dW || (batch->N > 0 && !dhidden))
+    const bool any = batch->N > 0;
+    if (!out || (any && (!out->loss || !saved || !dloss || !dhidden)) || !dev_status || !dW)
         return fail(RL_ERR_ARG, "out/loss/saved/dev_status/dloss/dhidden/dW NULL");
     if (!aligned16(dW) || !aligned16(dhidden)) return fail(RL_ERR_ARG, "dW/dhidden not 16-byte aligned");
     if (ws_bytes < rl_head_fwd_bwd_workspace_bytes(batch->N, batch->H, batch->V, batch->support.nnz, params))

@@ -151,12 +151,16 @@ def token_forward(z: np.ndarray, label: int, label_logq: float, adv: float, age:
 
 
 def token_grad_z(z: np.ndarray, label: int, adv: float, ids: np.ndarray, replayed: bool,
-                 fwd: dict, p: HeadParams) -> np.ndarray:
+                 fwd: dict, p: HeadParams, want_abs: bool = False):
     """d loss_t / d z_t over the whole vocabulary, with w, c, u held constant.
 
     d log P(v) / d z_j = delta_vj - P_j, where P is the full softmax of z, or for a
     replayed token the softmax restricted to S (zero off S).  The sum over entries uses
     np.add.at so duplicate draw ids each contribute.
+
+    ``want_abs`` also returns the sum of the magnitudes of the terms that make up each
+    component (the scale a finite-precision evaluation of the gradient is measured
+    against; the terms can cancel in the gradient itself).
     """
     z = np.asarray(z, dtype=np.float64)
     ids = np.asarray(ids, dtype=np.int64)
@@ -185,7 +189,23 @@ def token_grad_z(z: np.ndarray, label: int, adv: float, ids: np.ndarray, replaye
         else:
             d_kl = -dlogP(label)
         grad = grad + fwd["beta"] * d_kl
-    return grad
+    if not want_abs:
+        return grad
+    onehot_abs_c = np.zeros(V)
+    np.add.at(onehot_abs_c, ids, np.abs(fwd["c"]))
+    sum_abs_c = float(np.sum(np.abs(fwd["c"])))
+    at = abs(p.adv_tau * adv)
+    mag = at * (abs(fwd["w_label"]) * P + onehot_abs_c + sum_abs_c * P)
+    mag[label] += at * abs(fwd["w_label"])
+    if fwd["beta"] != 0.0:
+        if p.kl_estimator == KL_EXACT:
+            onehot_u = np.zeros(V)
+            np.add.at(onehot_u, ids, fwd["u"])
+            mag = mag + fwd["beta"] * (onehot_u + float(np.sum(fwd["u"])) * P)
+        else:
+            mag = mag + fwd["beta"] * P
+            mag[label] += fwd["beta"]
+    return grad, mag
 
 
 def _rows(inputs: dict):
@@ -269,8 +289,11 @@ def head_backward(inputs: dict, p: HeadParams, dloss: np.ndarray, chunk: int = 6
     G_tj = dloss_t / T * d loss_t / d z_tj;  dX = G W;  dW = G^T X.
 
     ``rows`` restricts dX to those tokens (dW then sums over those tokens only).
-    ``want_bounds`` also returns |G| |W| and |G|^T |X| (the magnitudes a finite-precision
-    evaluation of the two products is measured against).
+    ``want_bounds`` also returns the magnitudes a finite-precision evaluation is measured
+    against, as a dict: ``X`` = |G| |W| and ``W`` = |G|^T |X| with |G| the sum of the
+    magnitudes of the terms forming each G entry, and ``zX`` / ``zW`` the same products
+    with each |G| entry weighted by |z_tj| + |logsumexp_t| (how far an error in the
+    logits, proportional to their size, moves G).
     """
     off = _rows(inputs)
     N = off.shape[0] - 1
@@ -280,12 +303,19 @@ def head_backward(inputs: dict, p: HeadParams, dloss: np.ndarray, chunk: int = 6
     V, H = W.shape
     dX = np.zeros((rows.shape[0], H))
     dW = np.zeros((V, H)) if want_dW else None
-    bX = np.zeros((rows.shape[0], H)) if want_bounds else None
-    bW = np.zeros((V, H)) if (want_bounds and want_dW) else None
+    bnd = {}
+    if want_bounds:
+        bnd["X"] = np.zeros((rows.shape[0], H))
+        bnd["zX"] = np.zeros((rows.shape[0], H))
+        if want_dW:
+            bnd["W"] = np.zeros((V, H))
+            bnd["zW"] = np.zeros((V, H))
     for c0 in range(0, rows.shape[0], chunk):
         rr = rows[c0:c0 + chunk]
         Z = head_token_logits(inputs, rr, p.temperature)
         G = np.zeros_like(Z)
+        Gm = np.zeros_like(Z) if want_bounds else None
+        Zm = np.zeros_like(Z) if want_bounds else None
         for j, t in enumerate(rr):
             if not inputs["loss_mask"][t] or dloss[t] == 0.0:
                 continue
@@ -294,18 +324,27 @@ def head_backward(inputs: dict, p: HeadParams, dloss: np.ndarray, chunk: int = 6
             fw = token_forward(Z[j], int(inputs["labels"][t]), float(inputs["label_logq"][t]),
                                float(inputs["adv"][t]), int(inputs["age"][t]), ids,
                                inputs["logq"][s:e], bool(inputs["replayed"][t]), p)
-            G[j] = (float(dloss[t]) / p.temperature) * token_grad_z(
-                Z[j], int(inputs["labels"][t]), float(inputs["adv"][t]), ids,
-                bool(inputs["replayed"][t]), fw, p)
+            scale = float(dloss[t]) / p.temperature
+            res = token_grad_z(Z[j], int(inputs["labels"][t]), float(inputs["adv"][t]), ids,
+                               bool(inputs["replayed"][t]), fw, p, want_abs=want_bounds)
+            if want_bounds:
+                G[j] = scale * res[0]
+                Gm[j] = abs(scale) * res[1]
+                Zm[j] = np.abs(Z[j]) + abs(fw["lse_s"])
+            else:
+                G[j] = scale * res
         dX[c0:c0 + rr.shape[0]] = G @ W
         if want_dW:
             dW += G.T @ Xall[rr]
         if want_bounds:
-            bX[c0:c0 + rr.shape[0]] = np.abs(G) @ np.abs(W)
+            aW, aX = np.abs(W), np.abs(Xall[rr])
+            bnd["X"][c0:c0 + rr.shape[0]] = Gm @ aW
+            bnd["zX"][c0:c0 + rr.shape[0]] = (Gm * Zm) @ aW
             if want_dW:
-                bW += np.abs(G).T @ np.abs(Xall[rr])
+                bnd["W"] += Gm.T @ aX
+                bnd["zW"] += (Gm * Zm).T @ aX
     if want_bounds:
-        return dX, dW, bX, bW
+        return dX, dW, bnd
     return dX, dW
 
 

@@ -1,0 +1,133 @@
+"""GPU-vs-oracle comparison helpers shared by the GPU parity tests (no tests here)."""
+import dataclasses
+
+import numpy as np
+import torch
+
+import lm_head_gb300 as rh
+import oracle
+from parity_util import (LOGP_TOL, grad_check, logp_tol, loss_check, loss_prop_tol, margin, oracle_params,
+                         weight_keep_fp64)
+
+
+def _close(gpu, ref, tol, what):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    bad = np.abs(gpu - ref) > tol
+    assert not bad.any(), (what, int(bad.sum()), float(np.max(np.abs(gpu - ref) / tol)))
+
+
+def entry_rows(offsets):
+    off = np.asarray(offsets, np.int64)
+    return np.repeat(np.arange(len(off) - 1), np.diff(off))
+
+
+def _forward(case, hp):
+    dev = case.to("cuda")
+    batch = rh.HeadBatch.from_case(dev)
+    fwd = rh.rl_head_loss_fwd(batch, hp)
+    torch.cuda.synchronize()
+    return dev, batch, fwd
+
+
+def check_forward(case, hp, fwd, ref):
+    """Compare every forward output; returns the oracle result for reuse."""
+    st = fwd.status_bits()
+    assert st == 0, rh.status_names(st)
+    op = oracle_params(hp)
+    inp = case.numpy()
+    H = inp["hidden"].shape[1]
+    er = entry_rows(inp["offsets"])
+    z_lab = ref["logp_label"] + ref["lse_s"]
+    z_sup = ref["logp_support"] + ref["lse_s"][er]
+    _close(fwd.lse.cpu().numpy(), ref["lse"], logp_tol(H, ref["lse"], ref["lse"]), "lse")
+    _close(fwd.entropy.cpu().numpy(), ref["entropy"], logp_tol(H, ref["lse"], ref["lse"]), "entropy")
+    lab_tol = logp_tol(H, z_lab, ref["lse_s"])
+    sup_tol = logp_tol(H, z_sup, ref["lse_s"][er])
+    _close(fwd.logp_label.cpu().numpy(), ref["logp_label"], lab_tol, "logp_label")
+    _close(fwd.logp_support.cpu().numpy(), ref["logp_support"], sup_tol, "logp_support")
+    # masks: bit-exact against the oracle's fp64 predicate on the GPU's log-probs ...
+    gm_lab = fwd.mask_label.cpu().numpy()
+    gm_sup = fwd.mask_support.cpu().numpy()
+    np.testing.assert_array_equal(gm_lab, weight_keep_fp64(fwd.logp_label.cpu().numpy(), inp["label_logq"], op))
+    np.testing.assert_array_equal(gm_sup, weight_keep_fp64(fwd.logp_support.cpu().numpy(), inp["logq"], op))
+    # ... and against the oracle's own masks except within the log-prob tolerance of a threshold
+    near_lab = margin(ref["logp_label"], inp["label_logq"], op) < 4 * lab_tol
+    near_sup = margin(ref["logp_support"], inp["logq"], op) < 4 * sup_tol
+    assert np.all((gm_lab == ref["mask_label"]) | near_lab)
+    assert np.all((gm_sup == ref["mask_support"]) | near_sup)
+    # loss
+    mask = inp["loss_mask"].astype(bool)
+    ptol = loss_prop_tol(ref, inp, op)
+    loss_check(fwd.loss.cpu().double().numpy()[mask], ref["loss"][mask], ptol[mask])
+    assert np.all(fwd.loss.cpu().numpy()[~mask] == 0)
+    # metrics: counts equal the counts of the GPU's own masks; sums within tolerance
+    gm = fwd.metrics()
+    rm = ref["metrics"]
+    assert gm["n_rl"] == rm["n_rl"] == int(mask.sum())
+    assert gm["masked"] == int(((gm_lab == 0) & mask).sum())
+    flips = int(((gm_lab != ref["mask_label"]) & mask).sum())
+    assert abs(gm["masked"] - rm["masked"]) <= flips
+    assert gm["n_age0"] == rm["n_age0"]
+    for k in ("loss", "mismatch_kl", "support_mass", "mask_tv", "kl", "beta", "kl_age0", "entropy"):
+        tol = 1e-4 * max(abs(rm[k]), 1e-3 * rm["n_rl"]) + 1e-5 * rm["n_rl"] * (1 if k in ("mismatch_kl", "kl") else 0)
+        if k == "mask_tv":
+            tol += 2.0 * flips
+        assert abs(gm[k] - rm[k]) <= tol, (k, gm[k], rm[k])
+    return ref
+
+
+def check_backward(case, hp, batch, fwd, reading=None, dloss=None, both=True):
+    """Backward in hp's gradient precision, against the oracle.  SPLIT is held to the
+    element reading, BF16 to the operand reading; with ``both`` the other precision is
+    run and checked too (the forward's saved state does not depend on it)."""
+    inp = case.numpy()
+    op = oracle_params(hp)
+    mask = inp["loss_mask"].astype(bool)
+    if dloss is None:
+        dloss = mask.astype(np.float32) / max(int(mask.sum()), 1)   # token mean over RL tokens
+    dl = torch.from_numpy(np.asarray(dloss, np.float32)).cuda()
+    rX, rW, bnd = oracle.head_backward(inp, op, np.asarray(dloss, np.float64), want_bounds=True)
+    H = inp["hidden"].shape[1]
+    precisions = [hp.grad_precision]
+    if both:
+        precisions.append(rh.RL_GRAD_SPLIT if hp.grad_precision == rh.RL_GRAD_BF16 else rh.RL_GRAD_BF16)
+    out = None
+    for prec in precisions:
+        hpp = dataclasses.replace(hp, grad_precision=prec)
+        dX, dW, st = rh.rl_head_loss_bwd(batch, hpp, fwd.saved, dl)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, rh.status_names(int(st.item()))
+        rd = reading or ("element" if prec == rh.RL_GRAD_SPLIT else "operand")
+        wx = grad_check(dX.float().cpu().numpy(), rX, rd, "dX", bnd, "X", H)
+        ww = grad_check(dW.cpu().numpy(), rW, rd, "dW", bnd, "W", H)
+        if out is None:
+            out = (dX, dW, (wx, ww))
+    return out
+
+
+
+def check_fused(case, hp, reading=None, dloss=None):
+    """rl_head_loss_fwd_bwd (dloss given up front) against the oracle: every forward
+    output and both gradients, in the gradient precision of hp."""
+    dev = case.to("cuda")
+    batch = rh.HeadBatch.from_case(dev)
+    inp = case.numpy()
+    op = oracle_params(hp)
+    mask = inp["loss_mask"].astype(bool)
+    if dloss is None:
+        dloss = mask.astype(np.float32) / np.float32(max(int(mask.sum()), 1))
+    dl = torch.from_numpy(np.asarray(dloss, np.float32)).cuda()
+    fwd, dX, dW = rh.rl_head_loss_fwd_bwd(batch, hp, dl)
+    torch.cuda.synchronize()
+    ref = oracle.head_forward(inp, op)
+    check_forward(case, hp, fwd, ref)
+    rX, rW, bnd = oracle.head_backward(inp, op, np.asarray(dloss, np.float64), want_bounds=True)
+    H = inp["hidden"].shape[1]
+    rd = reading or ("element" if hp.grad_precision == rh.RL_GRAD_SPLIT else "operand")
+    H = inp["hidden"].shape[1]
+    grad_check(dX.float().cpu().numpy(), rX, rd, "dX", bnd, "X", H)
+    grad_check(dW.cpu().numpy(), rW, rd, "dW", bnd, "W", H)
+    return fwd, dX, dW
+
+

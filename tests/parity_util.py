@@ -17,6 +17,19 @@ import oracle
 
 LOGP_TOL = 1e-5
 LOSS_REL = 1e-4
+EPS32 = 2.0 ** -24
+
+
+def acc_tol(H: int, zmag):
+    """fp32-accumulation allowance of a logit built from H bf16 products: the rounding of
+    an fp32 running sum of H terms grows like 2^-24 sqrt(H) times the size of the sum;
+    two such 4-sigma-ish allowances (the entry and the logsumexp it is taken against)."""
+    return 2.0 * EPS32 * np.sqrt(H) * np.asarray(zmag, dtype=np.float64)
+
+
+def logp_tol(H: int, z_abs, lse_abs):
+    """Log-prob bar: 1e-5 absolute plus the fp32-accumulation allowance of |z| + |lse|."""
+    return LOGP_TOL + acc_tol(H, np.abs(z_abs) + np.abs(lse_abs))
 
 
 def f32(x):
@@ -43,16 +56,34 @@ def to_bf16(x):
     return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
 
 
-def grad_check(gpu, ref, reading: str, what: str, bound=None):
+def grad_check(gpu, ref, reading: str, what: str, bounds=None, key="X", H=2048, block=8192):
+    """Row-blocked grad_check_block (bounded host memory for [V, H] arrays).  ``bounds`` is
+    the oracle's dict (keys X / zX for dX, W / zW for dW; ``key`` names the first)."""
+    worst = 0.0
+    n = np.asarray(ref).shape[0]
+    b = None if bounds is None else np.asarray(bounds[key])
+    zb = None if bounds is None else np.asarray(bounds["z" + key])
+    for r0 in range(0, max(n, 1), block):
+        sl = slice(r0, min(n, r0 + block))
+        worst = max(worst, grad_check_block(np.asarray(gpu)[sl], np.asarray(ref)[sl], reading, what,
+                                            None if b is None else b[sl], None if zb is None else zb[sl], H))
+    return worst
+
+
+def grad_check_block(gpu, ref, reading: str, what: str, bound=None, zbound=None, H=2048):
     """Assert the gradient bar; returns the worst ratio err / allowed.
 
     readings: "element" (2 ulp of max(|ref|, 2^-8 rowmax)), "row" (2 ulp of the row max),
     "operand" (2 ulp of |ref| plus 2^-8 of the magnitude bound |G||W| / |G|^T|X|: the
-    result is exact to the precision of its bf16-rounded softmax-gradient operand)."""
+    result is exact to the precision of its bf16-rounded softmax-gradient operand).
+    Every reading also carries the logits' fp32-accumulation allowance carried into G
+    (acc_tol on zbound, the |G| |z|-weighted magnitude)."""
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     rb = to_bf16(ref)
     err = np.abs(gpu - rb)
+    zallow = 0.0 if zbound is None else acc_tol(H, zbound)
+    err = np.maximum(err - zallow, 0.0)
     rowmax = np.max(np.abs(ref), axis=1, keepdims=True)
     if reading == "operand":
         allowed = 2 * ulp_bf16(ref) * (ref != 0) + 2.0 ** -8 * np.asarray(bound, np.float64)
