@@ -142,7 +142,9 @@ typedef struct rl_head_metrics {
     int64_t masked_low;   /* ... with P below the band (ipo: P < q - eps; icepop: r < low) */
     int64_t masked_high;  /* ... with P above the band */
     int64_t n_age0;       /* RL tokens with age 0 */
-    int64_t reserved;
+    int64_t recomputed_chunks; /* rl_head_loss_fwd_bwd, bf16 gradients: token chunks whose dense
+                                  backward recomputed the logits because a row's stored softmax
+                                  numerators left their range (0 elsewhere) */
 } rl_head_metrics;
 
 typedef struct rl_head_outputs {
@@ -283,11 +285,12 @@ int rl_gemm_bf16(const void* A, int a_mn_major, const void* B, int b_mn_major, i
  * rl_profile_enable(1) also clears the counters.  rl_profile_read waits for the recorded
  * events, then fills ms[k] (summed device milliseconds) and launches[k] for every kind
  * k < RL_PROF_KINDS; either pointer may be NULL.  Host arrays. */
-#define RL_PROF_KINDS 16
+#define RL_PROF_KINDS 17
 enum { RL_PROF_VALIDATE = 0, RL_PROF_GEMM_FWD = 1, RL_PROF_TOKEN_LOSS = 2, RL_PROF_METRICS = 3,
        RL_PROF_TRANSPOSE = 4, RL_PROF_GEMM_GRAD = 5, RL_PROF_GEMM_DX = 6, RL_PROF_GEMM_DW = 7,
        RL_PROF_SPARSE_DX = 8, RL_PROF_SPARSE_DW = 9, RL_PROF_POLICY = 10, RL_PROF_GEMM_UTIL = 11,
-       RL_PROF_MEMSET = 12, RL_PROF_OTHER = 13, RL_PROF_RESID = 14, RL_PROF_GRAD_E = 15 };
+       RL_PROF_MEMSET = 12, RL_PROF_OTHER = 13, RL_PROF_RESID = 14, RL_PROF_GRAD_E = 15,
+       RL_PROF_REF_LOGIT = 16 };
 int rl_profile_enable(int on);
 int rl_profile_read(double* ms, int64_t* launches);
 const char* rl_profile_kind_name(int kind);

@@ -60,7 +60,7 @@ class RlHeadMetrics(ctypes.Structure):
     _fields_ = [(k, ctypes.c_double) for k in ("loss", "mismatch_kl", "support_mass", "mask_tv", "kl",
                                                "beta", "kl_age0", "entropy")] + \
                [(k, ctypes.c_int64) for k in ("n_rl", "masked", "masked_low", "masked_high", "n_age0",
-                                              "reserved")]
+                                              "recomputed_chunks")]
 
 
 class RlHeadOutputs(ctypes.Structure):
@@ -259,7 +259,7 @@ class HeadForward:
 
     def metrics(self) -> dict:
         m = RlHeadMetrics.from_buffer_copy(bytes(self.metrics_dev.cpu().numpy().tobytes()))
-        return {f: getattr(m, f) for f, _ in RlHeadMetrics._fields_ if f != "reserved"}
+        return {f: getattr(m, f) for f, _ in RlHeadMetrics._fields_}
 
     def status_bits(self) -> int:
         return int(self.status.item())
@@ -401,7 +401,7 @@ def rl_mismatch_metrics(batch: HeadBatch, saved: torch.Tensor, params: HeadParam
     cb = batch.c()
     _check(lib.rl_mismatch_metrics(ctypes.byref(cb), _ptr(saved), _ptr(m), _ptr(ws), ws.numel(), _stream(stream)))
     mm = RlHeadMetrics.from_buffer_copy(bytes(m.cpu().numpy().tobytes()))
-    return {f: getattr(mm, f) for f, _ in RlHeadMetrics._fields_ if f != "reserved"}
+    return {f: getattr(mm, f) for f, _ in RlHeadMetrics._fields_}
 
 
 @dataclasses.dataclass
@@ -507,7 +507,7 @@ def rl_kernel_launch_count() -> int:
     return int(load().rl_kernel_launch_count())
 
 
-RL_PROF_KINDS = 16
+RL_PROF_KINDS = 17
 
 
 def rl_profile_enable(on: bool = True) -> None:

@@ -95,6 +95,17 @@ RL_DEVINL void tmem_load_row32(uint32_t taddr, uint32_t (&r)[32]) {
                  : "memory");
 }
 
+// An epilogue policy may carry `const int* gate` in its Params: the launch then does no work
+// unless *gate != 0, a decision an earlier kernel of the stream wrote to device memory.
+template <class P>
+RL_DEVINL auto epi_gate_open(const P& p, int) -> decltype(p.gate, bool()) {
+    return p.gate == nullptr || *p.gate != 0;
+}
+template <class P>
+RL_DEVINL bool epi_gate_open(const P&, long) {
+    return true;
+}
+
 // Epilogue policy interface (all device, per thread; `row` in [0, 128), `half` 0/1 says
 // which 128 columns of every 256-column tile this thread sees; `col_begin` is the first
 // column it will see in the unit; `stage` is the warp's kEpiStageBytes of shared memory
@@ -110,6 +121,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                    const __grid_constant__ CUtensorMap tmB, const GemmPlan plan,
                    const __grid_constant__ typename Epi::Params ep) {
+    if (!epi_gate_open(ep, 0)) return;   // uniform over the grid
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -317,9 +329,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 int make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
                    int box_rows);
 
-// General 2-D tensor map: [rows, cols] with row stride `ld` elements, box box_rows x box_cols.
+// General 2-D tensor map: [rows, cols] with row stride `ld` elements, box box_rows x box_cols,
+// swizzle_bytes 0 (none), 64 or 128.
 int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, int64_t rows,
-                 int64_t cols, int64_t ld, int box_cols, int box_rows, int swizzle128);
+                 int64_t cols, int64_t ld, int box_cols, int box_rows, int swizzle_bytes);
 
 int num_sms();
 

@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                     const __grid_constant__ CUtensorMap tmB, const GemmPlan plan,
                     const __grid_constant__ typename Epi::Params ep) {
+    if (!epi_gate_open(ep, 0)) return;   // uniform over the grid: both CTAs of a pair leave
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));

@@ -15,7 +15,6 @@
 #include <climits>
 #include <cmath>
 
-#include <cuda_fp16.h>
 
 #include "gemm_tc2.cuh"
 #include "internal.h"
@@ -114,6 +113,7 @@ struct EpiGrad {
         uint16_t* G_lo;
         uint16_t* Gt_lo;
         int64_t ldt;
+        const int* gate;      // fused path: run only when the chunk's range flag is set
     };
     int64_t t;
     bool valid;
@@ -171,31 +171,38 @@ struct EpiGrad {
     RL_DEVINL void end_unit(const Params&, int, int) {}
 };
 
-// dX rows of the chunk: bf16(acc + dxs) for columns < H.
+// dX rows of the chunk: bf16(rs_t acc + dxs) for columns < H, where rs_t is the row scale
+// of the stored e (fused path; 1 when rs is absent or the chunk's range flag is set).
 struct EpiDx {
     struct Params {
         int64_t n;
         int32_t H;
         const float* dxs;   // chunk-relative [n, H]
         uint16_t* out;      // chunk-relative [n, H] bf16
+        const float* rs;    // chunk-relative [n], or nullptr
+        const int* flag;    // with rs
     };
     int64_t t;
     bool valid;
+    float scale;
     RL_DEVINL void begin_unit(const Params& p, int row, int, int m_blk, int, int) {
         t = static_cast<int64_t>(m_blk) * kBM + row;
         valid = t < p.n;
+        scale = 1.f;
+        if (valid && p.rs != nullptr && *p.flag == 0) scale = p.rs[t];
     }
     RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0, uint8_t*, int) {
         if (!valid || col0 >= p.H) return;
         const float4* s = reinterpret_cast<const float4*>(p.dxs + t * p.H + col0);
         uint4* o = reinterpret_cast<uint4*>(p.out + t * p.H + col0);
+        const float c = scale;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const float4 a = s[2 * q], b = s[2 * q + 1];
-            o[q] = make_uint4(pack_bf16x2(__uint_as_float(acc[8 * q + 0]) + a.x, __uint_as_float(acc[8 * q + 1]) + a.y),
-                              pack_bf16x2(__uint_as_float(acc[8 * q + 2]) + a.z, __uint_as_float(acc[8 * q + 3]) + a.w),
-                              pack_bf16x2(__uint_as_float(acc[8 * q + 4]) + b.x, __uint_as_float(acc[8 * q + 5]) + b.y),
-                              pack_bf16x2(__uint_as_float(acc[8 * q + 6]) + b.z, __uint_as_float(acc[8 * q + 7]) + b.w));
+            o[q] = make_uint4(pack_bf16x2(fmaf(__uint_as_float(acc[8 * q + 0]), c, a.x), fmaf(__uint_as_float(acc[8 * q + 1]), c, a.y)),
+                              pack_bf16x2(fmaf(__uint_as_float(acc[8 * q + 2]), c, a.z), fmaf(__uint_as_float(acc[8 * q + 3]), c, a.w)),
+                              pack_bf16x2(fmaf(__uint_as_float(acc[8 * q + 4]), c, b.x), fmaf(__uint_as_float(acc[8 * q + 5]), c, b.y)),
+                              pack_bf16x2(fmaf(__uint_as_float(acc[8 * q + 6]), c, b.z), fmaf(__uint_as_float(acc[8 * q + 7]), c, b.w)));
         }
     }
     RL_DEVINL void end_unit(const Params&, int, int) {}
@@ -236,18 +243,24 @@ struct EpiDw {
 };
 
 // ----------------------------------------------------------------------------------
-// Transpose (bf16): out[c, r] = in[r, c] for r < rows, c < cols
+// Transpose (bf16): out[c, r] = in[r, c] for r < rows, c < cols; with a row scale,
+// out[c, r] = bf16(rs_r in[r, c]) (rs ignored when *flag is set)
 // ----------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* in, int64_t rows,
                                                              int64_t cols, int64_t ld_in,
-                                                             uint16_t* out, int64_t ld_out) {
+                                                             uint16_t* out, int64_t ld_out,
+                                                             const float* rs, const int* flag) {
     __shared__ uint16_t tile[64][66];
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64;
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 64;
     const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
+    const bool scaled = rs != nullptr && *flag == 0;
     for (int i = ty; i < 64; i += 4) {
         const int64_t r = r0 + i, c = c0 + tx;
-        tile[i][tx] = (r < rows && c < cols) ? in[r * ld_in + c] : 0;
+        uint16_t v = (r < rows && c < cols) ? in[r * ld_in + c] : 0;
+        if (scaled && r < rows)
+            v = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(rs[r], bf16_bits_to_float(v))));
+        tile[i][tx] = v;
     }
     __syncthreads();
     for (int i = ty; i < 64; i += 4) {
@@ -257,13 +270,13 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* in,
 }
 
 static int transpose_bf16(const void* in, int64_t rows, int64_t cols, int64_t ld_in, void* out,
-                          int64_t ld_out, cudaStream_t s) {
+                          int64_t ld_out, cudaStream_t s, const float* rs = nullptr, const int* flag = nullptr) {
     if (rows <= 0 || cols <= 0) return RL_OK;
     dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
     if (grid.y > 65535u) return RL_ERR_UNSUPPORTED;
     ProfScope ps(RL_PROF_TRANSPOSE, s);
     transpose_bf16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(in), rows, cols, ld_in,
-                                               static_cast<uint16_t*>(out), ld_out);
+                                               static_cast<uint16_t*>(out), ld_out, rs, flag);
     count_launch();
     return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }
@@ -303,7 +316,7 @@ RL_DEVINL bool row_contains(const int32_t* ids, int64_t b, int64_t e, int32_t v)
 
 // Residual at one spike: the exact fp32 dense value g_true = alpha exp(z - lse) minus what
 // the dense GEMMs consume there (bf16 hi, and lo with the split), where g_gemm is either
-// g_true itself (recompute path) or F * e from the stored fp16 e (fused path).
+// g_true itself (recompute path) or F * e from the stored fp32 e (fused path, hi/lo).
 RL_DEVINL float spike_residual(float g_true, float g_gemm, bool split) {
     const float hi = __bfloat162float(__float2bfloat16_rn(g_gemm));
     float r = __fsub_rn(g_true, hi);
@@ -328,13 +341,16 @@ struct ResidArgs {
     const float* zsup;
     float inv_T;
     int split;
-    // fused path: e [n, V] (fp16, or fp32 in E32) and m2 [n, ldm], chunk-relative;
-    // both nullptr = recompute path
-    const uint16_t* E;
+    float* resid;             // [nnz + N]
+    // fused path, hi/lo: fp32 e [n, V] and m2 [n, ldm], chunk-relative
     const float* E32;
     const float* M2;
     int64_t ldm;
-    float* resid;             // [nnz + N]
+    // fused path, bf16: e [n, V] relative to the row reference, row scale rs [n], range flag
+    const uint16_t* Eb;
+    const float* rs;
+    const int* flag;
+    // none of the above: recompute path
 };
 
 // One warp per token of [t0, t0 + n): residual at the label and at the first entry of each
@@ -349,14 +365,15 @@ __global__ void __launch_bounds__(256) resid_kernel(ResidArgs a) {
     e = e < b ? b : (e > a.nnz ? a.nnz : e);
     const float alpha = dense_alpha(a.dloss[t], a.dcoef[t], a.inv_T);
     const float lse = a.lse[t];
+    const float sc = (a.Eb != nullptr && *a.flag == 0) ? a.rs[r] : 1.f;
     auto resid_at = [&](int32_t v, float z) -> float {
         if (alpha == 0.f || v < 0 || v >= a.V) return 0.f;
         const float g_true = dense_grad(alpha, z, lse);
+        if (a.Eb != nullptr)   // the GEMMs use sc * e (e = G itself after a recompute)
+            return __fsub_rn(g_true, __fmul_rn(sc, bf16_bits_to_float(a.Eb[r * a.V + v])));
         float g_gemm = g_true;
-        if (a.E != nullptr || a.E32 != nullptr) {
-            const float ev = a.E32 ? a.E32[r * a.V + v] : __half2float(__ushort_as_half(a.E[r * a.V + v]));
-            g_gemm = __fmul_rn(fused_factor(alpha, a.M2[r * a.ldm + (v >> 5)], lse), ev);
-        }
+        if (a.E32 != nullptr)
+            g_gemm = __fmul_rn(fused_factor(alpha, a.M2[r * a.ldm + (v >> 5)], lse), a.E32[r * a.V + v]);
         return spike_residual(g_true, g_gemm, a.split != 0);
     };
     for (int64_t j = b + lane; j < e; j += 32) {
@@ -647,8 +664,8 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
     }
 
     ResidArgs ra{0, N, V, nnz, b->labels, b->support.offsets, b->support.ids, dloss, sv.dcoef, sv.lse,
-                 sv.zlab, sv.zsup, 1.0f / prm->temperature, w.split ? 1 : 0, nullptr, nullptr, nullptr, 0,
-                 w.resid};
+                 sv.zlab, sv.zsup, 1.0f / prm->temperature, w.split ? 1 : 0, w.resid,
+                 nullptr, nullptr, 0, nullptr, nullptr, nullptr};
     if ((rc = launch_resid(ra, stream)) != RL_OK) return rc;
     {
         ProfScope ps(RL_PROF_SPARSE_DX, stream);
@@ -710,14 +727,56 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
 
 // ----------------------------------------------------------------------------------
 // Fused forward + backward (dloss known before the forward): no logit recompute.
-// Per token chunk the forward GEMM also stores e = 2^(z log2(e) - m2) in fp16 with its
-// running-max reference m2 per 32-column chunk; once the chunk's logsumexp is known,
-// G = alpha 2^(m2 - lse log2(e)) e (one factor per row and 32-column chunk) is written in
-// both layouts, and the dX / dW GEMMs follow.  6 N H V tensor flops per step.
+//
+// bf16 gradient precision.  Before a chunk's forward GEMM, each row gets a reference
+// cref = z_label log2(e) (ref_logit_kernel).  The GEMM epilogue stores
+// e = 2^(z log2(e) - cref) in bf16 twice, as Eb [n, V] and Ebt [V, n], and once the
+// chunk's logsumexp is known the dense softmax gradient is G = rs * e with one scale per
+// row, rs = alpha 2^(cref - lse log2(e)).  The scale is applied where it is free: in the
+// dX epilogue (dX = rs * (e W)) and in the copy of X^T that dW consumes
+// (dW += e^T (rs X)).  So the backward reads e straight from the forward's output.
+// If a row's logits leave the range of that representation (max logit more than 2^64
+// above the reference, or a scale out of range) the chunk's flag is set and a gated GEMM
+// recomputes G into Eb / Ebt with rs = 1 (the two-call path's arithmetic).
+//
+// hi/lo gradient precision.  The forward stores e = 2^(z log2(e) - m2) in fp32 with its
+// running-max reference per 32-column chunk, and grad_from_e_kernel forms
+// G = alpha 2^(m2 - lse log2(e)) e and its bf16 hi/lo split in both layouts.
+// 6 N H V tensor flops per step either way (x2 for the dX / dW GEMMs with hi/lo).
 // ----------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) ref_logit_kernel(const uint16_t* X, const uint16_t* W, const int32_t* labels,
+                                                        int64_t n, int64_t H, int64_t V, float c2, float* cref,
+                                                        int* flag) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (blockIdx.x == 0 && threadIdx.x == 0) *flag = 0;
+    if (t >= n) return;
+    const int32_t lab = labels[t];
+    const bool ok = lab >= 0 && lab < V;
+    float acc = 0.f;
+    if (ok) {
+        const uint16_t* x = X + t * H;
+        const uint16_t* w = W + static_cast<int64_t>(lab) * H;
+        for (int64_t h = lane * 8; h < H; h += 256) {
+            const uint4 xv = *reinterpret_cast<const uint4*>(x + h);
+            const uint4 wv = *reinterpret_cast<const uint4*>(w + h);
+            const uint32_t xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                acc = fmaf(__uint_as_float(xa[k] << 16), __uint_as_float(wa[k] << 16), acc);
+                acc = fmaf(__uint_as_float(xa[k] & 0xFFFF0000u), __uint_as_float(wa[k] & 0xFFFF0000u), acc);
+            }
+        }
+    }
+    acc = warp_sum(acc);
+    if (lane == 0) {
+        const float c = acc * c2;
+        cref[t] = (ok && isfinite(c)) ? c : 0.f;
+    }
+}
+
 struct GradEArgs {
     int64_t n, V, ldm, ldt;
-    const uint16_t* E;    // fp16 e, or
     const float* E32;     // fp32 e
     const float* M2;
     const float* dloss;   // chunk-relative
@@ -734,11 +793,11 @@ constexpr int kGradTileT = 64;    // tokens per block
 constexpr int kGradTileV = 128;   // vocabulary ids per block
 constexpr int kGradPitch = 72;    // smem row pitch (halfwords): 144 B keeps 16-byte rows
 
-// G = F e with one factor F = alpha 2^(m2 - lse log2 e) per row and 32-column chunk.
-// Row-major pass: 16 threads cover one token's 128 columns (8 each), so loads of e and
-// stores of G are full 256-byte row segments.  The tile is kept transposed in shared
-// memory (token index XOR-swizzled by 8 per 8-column group against bank conflicts) and
-// written as G^T with 16-byte stores, 8 threads per vocabulary row.
+// G = F e with one factor F = alpha 2^(m2 - lse log2 e) per row and 32-column chunk, and
+// its bf16 hi/lo split.  Row-major pass: 16 threads cover one token's 128 columns (8
+// each), so loads of e and stores of G are full row segments.  The tile is kept
+// transposed in shared memory (token index XOR-swizzled by 8 per 8-column group against
+// bank conflicts) and written as G^T with 16-byte stores, 8 threads per vocabulary row.
 __global__ void __launch_bounds__(256) grad_from_e_kernel(GradEArgs a) {
     __shared__ __align__(16) uint16_t th[kGradTileV][kGradPitch];
     __shared__ __align__(16) uint16_t tl[kGradTileV][kGradPitch];
@@ -746,7 +805,6 @@ __global__ void __launch_bounds__(256) grad_from_e_kernel(GradEArgs a) {
     const int g = tid & 15;
     const int sw = (g & 7) << 3;
     const int64_t v = static_cast<int64_t>(blockIdx.x) * kGradTileV + g * 8;
-    const bool split = a.G_lo != nullptr;
     for (int pass = 0; pass < kGradTileT / 16; ++pass) {
         const int r = pass * 16 + (tid >> 4);
         const int64_t t = static_cast<int64_t>(blockIdx.y) * kGradTileT + r;
@@ -754,38 +812,24 @@ __global__ void __launch_bounds__(256) grad_from_e_kernel(GradEArgs a) {
         if (t < a.n && v < a.V) {
             const float alpha = dense_alpha(a.dloss[t], a.dcoef[t], a.inv_T);
             const float F = fused_factor(alpha, a.M2[t * a.ldm + (v >> 5)], a.lse[t]);
-            float e[8];
-            if (a.E32) {
-                const float4* src = reinterpret_cast<const float4*>(a.E32 + t * a.V + v);
-                const float4 x0 = src[0], x1 = src[1];
-                e[0] = x0.x; e[1] = x0.y; e[2] = x0.z; e[3] = x0.w;
-                e[4] = x1.x; e[5] = x1.y; e[6] = x1.z; e[7] = x1.w;
-            } else {
-                const uint4 x = *reinterpret_cast<const uint4*>(a.E + t * a.V + v);
-                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    e[2 * k] = __half2float(__ushort_as_half(static_cast<uint16_t>(w[k] & 0xFFFFu)));
-                    e[2 * k + 1] = __half2float(__ushort_as_half(static_cast<uint16_t>(w[k] >> 16)));
-                }
-            }
+            const float4* src = reinterpret_cast<const float4*>(a.E32 + t * a.V + v);
+            const float4 x0 = src[0], x1 = src[1];
+            const float e[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const float g0 = __fmul_rn(F, e[2 * k]), g1 = __fmul_rn(F, e[2 * k + 1]);
                 hi[k] = pack_bf16x2(g0, g1);
-                if (split) {
-                    const float h0 = bf16_bits_to_float(static_cast<uint16_t>(hi[k] & 0xFFFFu));
-                    const float h1 = bf16_bits_to_float(static_cast<uint16_t>(hi[k] >> 16));
-                    lo[k] = pack_bf16x2(g0 - h0, g1 - h1);
-                }
+                const float h0 = bf16_bits_to_float(static_cast<uint16_t>(hi[k] & 0xFFFFu));
+                const float h1 = bf16_bits_to_float(static_cast<uint16_t>(hi[k] >> 16));
+                lo[k] = pack_bf16x2(g0 - h0, g1 - h1);
             }
             *reinterpret_cast<uint4*>(a.G + t * a.V + v) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            if (split) *reinterpret_cast<uint4*>(a.G_lo + t * a.V + v) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            *reinterpret_cast<uint4*>(a.G_lo + t * a.V + v) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             th[g * 8 + k][r ^ sw] = static_cast<uint16_t>((k & 1) ? (hi[k >> 1] >> 16) : (hi[k >> 1] & 0xFFFFu));
-            if (split) tl[g * 8 + k][r ^ sw] = static_cast<uint16_t>((k & 1) ? (lo[k >> 1] >> 16) : (lo[k >> 1] & 0xFFFFu));
+            tl[g * 8 + k][r ^ sw] = static_cast<uint16_t>((k & 1) ? (lo[k >> 1] >> 16) : (lo[k >> 1] & 0xFFFFu));
         }
     }
     __syncthreads();
@@ -798,11 +842,11 @@ __global__ void __launch_bounds__(256) grad_from_e_kernel(GradEArgs a) {
         const int64_t tt = tbase + j;
         if (tt + 8 <= a.n) {
             *reinterpret_cast<uint4*>(a.Gt + vr * a.ldt + tt) = *reinterpret_cast<const uint4*>(&th[row][jp]);
-            if (split) *reinterpret_cast<uint4*>(a.Gt_lo + vr * a.ldt + tt) = *reinterpret_cast<const uint4*>(&tl[row][jp]);
+            *reinterpret_cast<uint4*>(a.Gt_lo + vr * a.ldt + tt) = *reinterpret_cast<const uint4*>(&tl[row][jp]);
         } else {
             for (int k = 0; k < 8 && tt + k < a.n; ++k) {
                 a.Gt[vr * a.ldt + tt + k] = th[row][jp + k];
-                if (split) a.Gt_lo[vr * a.ldt + tt + k] = tl[row][jp + k];
+                a.Gt_lo[vr * a.ldt + tt + k] = tl[row][jp + k];
             }
         }
     }
@@ -810,40 +854,51 @@ __global__ void __launch_bounds__(256) grad_from_e_kernel(GradEArgs a) {
 
 struct FusedWs {
     int64_t chunk;
+    int64_t nchunks;
     FwdWs fw;
-    uint16_t* E;     // fp16 e (bf16 gradient precision)
-    float* E32;      // fp32 e (hi/lo gradient precision)
-    float* M2;
+    // bf16 gradient precision
+    uint16_t* Eb;    // [chunk, V]
+    uint16_t* Ebt;   // [V, chunk]
+    float* cref;     // [chunk]
+    float* rs;       // [chunk]
+    int* flags;      // [nchunks] range flag per chunk
+    // hi/lo gradient precision
+    float* E32;      // [chunk, V]
+    float* M2;       // [chunk, ldm]
     int64_t ldm;
-    BwdWs bw;   // G, Gt, G_lo, Gt_lo, Wt, Xt, dxs [chunk, H], resid, sort buffers
+    BwdWs bw;   // Wt, Xt, dxs [chunk, H], resid, sort buffers; G, Gt, G_lo, Gt_lo with hi/lo
 };
 
 static FusedWs fused_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* prm,
                              size_t* bytes) {
     FusedWs f{};
     f.chunk = bwd_chunk(N, prm);
+    f.nchunks = (N + f.chunk - 1) / f.chunk;
     size_t fb = 0;
     f.fw = fwd_ws_view(base, f.chunk, H, V, nnz, &fb);
     Carve c(base ? static_cast<uint8_t*>(base) + fb : nullptr);
     c.off = 0;
     f.ldm = (V + 31) / 32;
-    if (prm->grad_precision == RL_GRAD_SPLIT)
-        f.E32 = c.take<float>(static_cast<size_t>(f.chunk) * V);
-    else
-        f.E = c.take<uint16_t>(static_cast<size_t>(f.chunk) * V);
-    f.M2 = c.take<float>(static_cast<size_t>(f.chunk) * f.ldm);
     BwdWs& w = f.bw;
     w.dense = true;
     w.split = prm->grad_precision == RL_GRAD_SPLIT;
     w.chunk = f.chunk;
-    w.Wt = c.take<uint16_t>(static_cast<size_t>(V) * H);
-    w.Xt = c.take<uint16_t>(static_cast<size_t>(H) * f.chunk);
-    w.G = c.take<uint16_t>(static_cast<size_t>(f.chunk) * V);
-    w.Gt = c.take<uint16_t>(static_cast<size_t>(V) * f.chunk);
     if (w.split) {
+        f.E32 = c.take<float>(static_cast<size_t>(f.chunk) * V);
+        f.M2 = c.take<float>(static_cast<size_t>(f.chunk) * f.ldm);
+        w.G = c.take<uint16_t>(static_cast<size_t>(f.chunk) * V);
+        w.Gt = c.take<uint16_t>(static_cast<size_t>(V) * f.chunk);
         w.G_lo = c.take<uint16_t>(static_cast<size_t>(f.chunk) * V);
         w.Gt_lo = c.take<uint16_t>(static_cast<size_t>(V) * f.chunk);
+    } else {
+        f.Eb = c.take<uint16_t>(static_cast<size_t>(f.chunk) * V);
+        f.Ebt = c.take<uint16_t>(static_cast<size_t>(V) * f.chunk);
+        f.cref = c.take<float>(f.chunk);
+        f.rs = c.take<float>(f.chunk);
     }
+    f.flags = c.take<int>(f.nchunks > 0 ? f.nchunks : 1);
+    w.Wt = c.take<uint16_t>(static_cast<size_t>(V) * H);
+    w.Xt = c.take<uint16_t>(static_cast<size_t>(H) * f.chunk);
     w.dxs = c.take<float>(static_cast<size_t>(f.chunk) * H);
     w.resid = c.take<float>(nnz + N);
     const int64_t items = nnz + N;
@@ -896,60 +951,102 @@ int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_
                   b->labels, b->support.offsets, b->support.ids, dloss, sv.labcoef, sv.entcoef, inv_T, w.resid};
     rc = transpose_bf16(b->weight, V, H, H, w.Wt, V, stream);
     if (rc != RL_OK) return rc;
-    CUtensorMap tmWt;
+    CUtensorMap tmW, tmWt;
+    if ((rc = make_tmap_b(&tmW, b->weight, V, H, H)) != RL_OK) return rc;
     if ((rc = make_tmap_b(&tmWt, w.Wt, H, V, V)) != RL_OK) return rc;
     const int passes = w.split ? 2 : 1;
-    for (int64_t c0 = 0; c0 < N; c0 += f.chunk) {
+    for (int64_t c0 = 0, ci = 0; c0 < N; c0 += f.chunk, ++ci) {
         const int64_t n = N - c0 < f.chunk ? N - c0 : f.chunk;
-        // forward GEMM (+ e store) and per-token loss for the chunk
-        if ((rc = fwd_rows(b, prm, out, sv, f.fw, c0, n, f.E, f.E32, f.M2, 0, status, stream)) != RL_OK) return rc;
-        // spike residuals of the chunk's tokens, then G / G^T from e
-        ResidArgs ra{c0, n, V, nnz, b->labels, b->support.offsets, b->support.ids, dloss, sv.dcoef, sv.lse,
-                     sv.zlab, sv.zsup, inv_T, w.split ? 1 : 0, f.E, f.E32, f.M2, f.ldm, w.resid};
-        if ((rc = launch_resid(ra, stream)) != RL_OK) return rc;
-        {
-            GradEArgs ga{n, V, f.ldm, f.chunk, f.E, f.E32, f.M2, dloss + c0, sv.dcoef + c0, sv.lse + c0, inv_T,
-                         static_cast<uint16_t*>(w.G), static_cast<uint16_t*>(w.Gt),
-                         static_cast<uint16_t*>(w.G_lo), static_cast<uint16_t*>(w.Gt_lo)};
-            dim3 grid(static_cast<unsigned>((V + kGradTileV - 1) / kGradTileV),
-                      static_cast<unsigned>((n + kGradTileT - 1) / kGradTileT));
-            ProfScope ps(RL_PROF_GRAD_E, stream);
-            grad_from_e_kernel<<<grid, 256, 0, stream>>>(ga);
-            count_launch();
-        }
         const uint16_t* Xc = static_cast<const uint16_t*>(b->hidden) + c0 * H;
-        if ((rc = transpose_bf16(Xc, n, H, H, w.Xt, f.chunk, stream)) != RL_OK) return rc;
+        int* flag = f.flags + ci;
+        CUtensorMap tmA, tmAlo, tmAt, tmAtlo, tmXt;
+        EStore es;
+        if (!w.split) {
+            es.Eb = f.Eb;
+            es.Ebt = f.Ebt;
+            es.ldt = f.chunk;
+            es.cref = f.cref;
+            es.flag = flag;
+            es.rs = f.rs;
+            es.dloss = dloss + c0;
+            {
+                ProfScope ps(RL_PROF_REF_LOGIT, stream);
+                ref_logit_kernel<<<static_cast<unsigned>((n + 7) / 8), 256, 0, stream>>>(
+                    Xc, static_cast<const uint16_t*>(b->weight), b->labels + c0, n, H, V, kLog2e * inv_T, f.cref, flag);
+                count_launch();
+            }
+        } else {
+            es.E32 = f.E32;
+            es.M2 = f.M2;
+        }
+        // forward GEMM (+ e store) and per-token loss for the chunk
+        if ((rc = fwd_rows(b, prm, out, sv, f.fw, c0, n, &es, 0, status, stream)) != RL_OK) return rc;
+        if (!w.split) {
+            // out-of-range chunk only: G recomputed from the logits into Eb / Ebt (rs := 1)
+            CUtensorMap tmX;
+            if ((rc = make_tmap_bf16(&tmX, Xc, n, H, H, kBM)) != RL_OK) return rc;
+            EpiGrad::Params gp{n, static_cast<int32_t>(V), inv_T, sv.lse + c0, dloss + c0, sv.dcoef + c0,
+                               f.Eb, f.Ebt, nullptr, nullptr, f.chunk, flag};
+            const GemmPlan pg = make_plan_auto(n, V, H, 1, 1 << 30, 1, status);
+            {
+                ProfScope ps(RL_PROF_GEMM_GRAD, stream);
+                if ((rc = launch_gemm_auto<EpiGrad>(tmX, tmX, tmW, pg, gp, stream)) != RL_OK) return rc;
+            }
+            count_launch();
+            ResidArgs ra{c0, n, V, nnz, b->labels, b->support.offsets, b->support.ids, dloss, sv.dcoef, sv.lse,
+                         sv.zlab, sv.zsup, inv_T, 0, w.resid, nullptr, nullptr, 0, f.Eb, f.rs, flag};
+            if ((rc = launch_resid(ra, stream)) != RL_OK) return rc;
+            if ((rc = transpose_bf16(Xc, n, H, H, w.Xt, f.chunk, stream, f.rs, flag)) != RL_OK) return rc;
+            if ((rc = make_tmap_bf16(&tmA, f.Eb, n, V, V, kBM)) != RL_OK) return rc;
+            if ((rc = make_tmap_bf16(&tmAt, f.Ebt, V, n, f.chunk, kBM)) != RL_OK) return rc;
+            tmAlo = tmA;
+            tmAtlo = tmAt;
+        } else {
+            // spike residuals of the chunk's tokens, then G / G^T (hi/lo) from e
+            ResidArgs ra{c0, n, V, nnz, b->labels, b->support.offsets, b->support.ids, dloss, sv.dcoef, sv.lse,
+                         sv.zlab, sv.zsup, inv_T, 1, w.resid, f.E32, f.M2, f.ldm, nullptr, nullptr, nullptr};
+            if ((rc = launch_resid(ra, stream)) != RL_OK) return rc;
+            {
+                GradEArgs ga{n, V, f.ldm, f.chunk, f.E32, f.M2, dloss + c0, sv.dcoef + c0, sv.lse + c0, inv_T,
+                             static_cast<uint16_t*>(w.G), static_cast<uint16_t*>(w.Gt),
+                             static_cast<uint16_t*>(w.G_lo), static_cast<uint16_t*>(w.Gt_lo)};
+                dim3 grid(static_cast<unsigned>((V + kGradTileV - 1) / kGradTileV),
+                          static_cast<unsigned>((n + kGradTileT - 1) / kGradTileT));
+                ProfScope ps(RL_PROF_GRAD_E, stream);
+                grad_from_e_kernel<<<grid, 256, 0, stream>>>(ga);
+                count_launch();
+            }
+            if ((rc = transpose_bf16(Xc, n, H, H, w.Xt, f.chunk, stream)) != RL_OK) return rc;
+            if ((rc = make_tmap_bf16(&tmA, w.G, n, V, V, kBM)) != RL_OK) return rc;
+            if ((rc = make_tmap_bf16(&tmAt, w.Gt, V, n, f.chunk, kBM)) != RL_OK) return rc;
+            if ((rc = make_tmap_bf16(&tmAlo, w.G_lo, n, V, V, kBM)) != RL_OK) return rc;
+            if ((rc = make_tmap_bf16(&tmAtlo, w.Gt_lo, V, n, f.chunk, kBM)) != RL_OK) return rc;
+        }
         {
             ProfScope ps(RL_PROF_SPARSE_DX, stream);
             sparse_dx_kernel<false><<<static_cast<unsigned>(n), 256, 0, stream>>>(sa, c0, w.dxs, nullptr);
             count_launch();
         }
-        CUtensorMap tmG, tmGlo, tmGt, tmGtlo, tmXt;
-        if ((rc = make_tmap_bf16(&tmG, w.G, n, V, V, kBM)) != RL_OK) return rc;
-        if ((rc = make_tmap_bf16(&tmGt, w.Gt, V, n, f.chunk, kBM)) != RL_OK) return rc;
         if ((rc = make_tmap_b(&tmXt, w.Xt, H, n, f.chunk)) != RL_OK) return rc;
-        tmGlo = tmG;
-        tmGtlo = tmGt;
-        if (w.split) {
-            if ((rc = make_tmap_bf16(&tmGlo, w.G_lo, n, V, V, kBM)) != RL_OK) return rc;
-            if ((rc = make_tmap_bf16(&tmGtlo, w.Gt_lo, V, n, f.chunk, kBM)) != RL_OK) return rc;
-        }
-        EpiDx::Params dp{n, static_cast<int32_t>(H), w.dxs, static_cast<uint16_t*>(dhidden) + c0 * H};
+        EpiDx::Params dp{n, static_cast<int32_t>(H), w.dxs, static_cast<uint16_t*>(dhidden) + c0 * H,
+                         w.split ? nullptr : f.rs, flag};
         const GemmPlan p2 = make_plan_auto(n, H, V, passes, 1 << 30, 0, status);
         {
             ProfScope ps(RL_PROF_GEMM_DX, stream);
-            if ((rc = launch_gemm_auto<EpiDx>(tmG, tmGlo, tmWt, p2, dp, stream)) != RL_OK) return rc;
+            if ((rc = launch_gemm_auto<EpiDx>(tmA, tmAlo, tmWt, p2, dp, stream)) != RL_OK) return rc;
         }
         EpiDw::Params wp{V, static_cast<int32_t>(H), (c0 > 0 || accumulate) ? 1 : 0, dW};
         const GemmPlan p3 = make_plan_auto(V, H, n, passes, 1 << 30, 0, status);
         {
             ProfScope ps(RL_PROF_GEMM_DW, stream);
-            if ((rc = launch_gemm_auto<EpiDw>(tmGt, tmGtlo, tmXt, p3, wp, stream)) != RL_OK) return rc;
+            if ((rc = launch_gemm_auto<EpiDw>(tmAt, tmAtlo, tmXt, p3, wp, stream)) != RL_OK) return rc;
         }
         count_launch(2);
     }
     if ((rc = sparse_dw(sa, w, dW, stream)) != RL_OK) return rc;
-    if (out->metrics) return metrics_run(b, saved, out->metrics, f.fw.mpart, stream);
+    if (out->metrics)
+        return metrics_run(b, saved, out->metrics, f.fw.mpart, stream, w.split ? nullptr : f.flags,
+                           w.split ? 0 : static_cast<int>(f.nchunks));
     return RL_OK;
 }
 

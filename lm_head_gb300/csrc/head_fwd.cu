@@ -14,7 +14,7 @@
 #include <climits>
 #include <cstring>
 
-#include <cuda_fp16.h>
+#include <cuda_bf16.h>
 
 #include "gemm_tc2.cuh"
 #include "internal.h"
@@ -201,17 +201,24 @@ struct EpiStats {
         float* part_m;
         float* part_s;
         float* part_u;
-        // optional (fused forward + backward): e = 2^(z log2(e) - m2) as fp16 [N, V] and
-        // the running max m2 it is relative to, per 32-column chunk [N, ldm]
-        uint16_t* E;
-        float* E32;      // fp32 instead of fp16 (hi/lo gradient precision)
+        // fused forward + backward, bf16 gradient precision (Eb != nullptr): e relative to
+        // the row reference cref, stored as bf16 in both layouts through TMA
+        uint16_t* Eb;
+        const float* cref;
+        int* flag;
+        CUtensorMap tmEb;    // over Eb [N, V]: box 32 rows x 32 columns, 64-byte swizzle
+        CUtensorMap tmEbt;   // over Ebt [V, ldt]: box 32 vocabulary rows x 32 tokens, no swizzle
+        // fused forward + backward, hi/lo gradient precision (E32 != nullptr): fp32 e relative
+        // to the running max m2, which is stored per 32-column chunk [N, ldm]
+        float* E32;
         float* M2;
         int64_t ldm;
-        CUtensorMap tmE;  // over E (fp16) or E32 ([N, V], box 32 x 32, no swizzle)
+        CUtensorMap tmE32;   // over E32 [N, V]: box 32 x 32, 128-byte swizzle
     };
     int64_t t;
     bool valid;
     float m2, s, sc, u2, uc;
+    float cr;
     int64_t ptr, end;
     int32_t next_id;
     int32_t label;
@@ -223,10 +230,12 @@ struct EpiStats {
         valid = t < p.N;
         m2 = -INFINITY;
         s = sc = u2 = uc = 0.f;
+        cr = 0.f;
         ptr = end = 0;
         next_id = INT_MAX;
         label = -1;
         if (!valid) return;
+        if (p.cref != nullptr) cr = p.cref[t];
         label = p.labels[t];
         int64_t b = p.offsets[t], e = p.offsets[t + 1];
         b = b < 0 ? 0 : (b > p.nnz ? p.nnz : b);
@@ -253,49 +262,70 @@ struct EpiStats {
 #pragma unroll
             for (int k = 0; k < 32; ++k) ev[k] = 0.f;
         }
-        if (p.E != nullptr || p.E32 != nullptr) store_e(p, ev, col0, stage, lane);
+        if (p.Eb != nullptr)
+            store_eb(p, ev, col0, stage, lane);
+        else if (p.E32 != nullptr)
+            store_e32(p, ev, col0, stage, lane);
     }
 
-    // The warp's 32 rows of e go through shared memory and TMA stores (rows past N and
-    // columns past V are clipped by the tensor map).  The 4 KB staging tile uses the
-    // 128-byte swizzle (16-byte chunk c of row r at c ^ (r % 8)), so the 32 lanes write
-    // without bank conflicts.  fp32: one 32-column store per chunk; fp16: one 64-column
-    // store per pair of chunks.
-    RL_DEVINL void store_e(const Params& p, const float (&ev)[32], int col0, uint8_t* stage, int lane) {
-        const bool f32 = p.E32 != nullptr;
-        const int par = (col0 >> 5) & 1;
-        if (f32 || par == 0) {
-            if (lane == 0) bulk_wait_read<0>();   // the previous store has read the tile
-            __syncwarp();
+    // bf16 e relative to the row reference: 2^(z' - cref) = 2^(z' - m2) 2^(m2 - cref), one
+    // EX2 per row and chunk.  The warp's 32 x 32 block goes through shared memory twice per
+    // chunk: row-major (2 KB, 64-byte swizzle: 16-byte piece c of row r at c ^ ((r >> 1) & 3),
+    // so the 32 lanes' 16-byte writes hit distinct banks) and transposed (2 KB, vocabulary
+    // row k holds the 32 lanes' values at 2-byte steps), then two TMA stores.  Rows past N
+    // and columns past V are clipped by the tensor maps.
+    RL_DEVINL void store_eb(const Params& p, const float (&ev)[32], int col0, uint8_t* stage, int lane) {
+        float kf = 0.f;
+        if (valid) {
+            const float dm = m2 - cr;
+            if (dm > kRefRangeLog2) *p.flag = 1;   // beyond the bf16 store's range: recompute
+            kf = exp2_approx(fminf(dm, 126.f));
         }
+        uint32_t h[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const __nv_bfloat162 v = __floats2bfloat162_rn(ev[2 * k] * kf, ev[2 * k + 1] * kf);
+            h[k] = *reinterpret_cast<const uint32_t*>(&v);
+        }
+        if (lane == 0) bulk_wait_read<0>();   // the previous chunk's stores have read the tiles
+        __syncwarp();
+        uint8_t* row = stage + lane * 64;
+        const int sw = (lane >> 1) & 3;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(row + ((q ^ sw) << 4)) = make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+        uint16_t* col = reinterpret_cast<uint16_t*>(stage + 2048) + lane;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            col[(2 * k) * 32] = static_cast<uint16_t>(h[k] & 0xFFFFu);
+            col[(2 * k + 1) * 32] = static_cast<uint16_t>(h[k] >> 16);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && t < p.N) {   // lane 0 holds the warp's first row
+            tma_store_2d(&p.tmEb, stage, col0, static_cast<int32_t>(t));
+            tma_store_2d(&p.tmEbt, stage + 2048, static_cast<int32_t>(t), col0);
+            bulk_commit();
+        }
+    }
+
+    // fp32 e relative to m2 (the running max at this chunk), one 32 x 32 tile per chunk
+    // (4 KB, 128-byte swizzle: 16-byte piece c of row r at c ^ (r % 8)), and m2 itself.
+    RL_DEVINL void store_e32(const Params& p, const float (&ev)[32], int col0, uint8_t* stage, int lane) {
+        if (lane == 0) bulk_wait_read<0>();   // the previous store has read the tile
+        __syncwarp();
         uint8_t* row = stage + lane * 128;
         const int sw = lane & 7;
-        if (f32) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                *reinterpret_cast<float4*>(row + ((q ^ sw) << 4)) =
-                    make_float4(ev[4 * q], ev[4 * q + 1], ev[4 * q + 2], ev[4 * q + 3]);
-        } else {
-            uint32_t h[16];
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const __half2 v = __floats2half2_rn(ev[2 * k], ev[2 * k + 1]);
-                h[k] = *reinterpret_cast<const uint32_t*>(&v);
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(row + (((par * 4 + q) ^ sw) << 4)) =
-                    make_uint4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-        }
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(row + ((q ^ sw) << 4)) =
+                make_float4(ev[4 * q], ev[4 * q + 1], ev[4 * q + 2], ev[4 * q + 3]);
         if (valid) p.M2[t * p.ldm + (col0 >> 5)] = m2;
-        const bool flush = f32 || par == 1 || col0 + 32 >= p.V;
-        if (flush) {
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {   // lane 0 holds the warp's first row
-                tma_store_2d(&p.tmE, stage, f32 ? col0 : (col0 & ~63), static_cast<int32_t>(t));
-                bulk_commit();
-            }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && t < p.N) {
+            tma_store_2d(&p.tmE32, stage, col0, static_cast<int32_t>(t));
+            bulk_commit();
         }
     }
 
@@ -398,6 +428,12 @@ struct TokenArgs {
     uint8_t* mask_support;
     SavedView sv;
     int32_t* status;
+    // fused forward + backward with bf16 e (rs != nullptr): the row scale of the stored e
+    const float* cref;
+    const float* dloss;
+    float inv_T;
+    float* rs;
+    int* flag;
 };
 
 struct WeightOut {
@@ -603,6 +639,18 @@ __global__ void __launch_bounds__(256) token_loss_kernel(TokenArgs a) {
         mt[6] = ent;
         mt[7] = __int_as_float(flags);
         if (!isfinite(lse) || !isfinite(loss)) set_status(a.status, RL_STATUS_NONFINITE);
+        if (a.rs != nullptr) {
+            // G = alpha exp(z - lse) = rs e with e = 2^(z log2(e) - cref); alpha is formed as
+            // the backward forms it (dloss dcoef / T, rounded in that order)
+            const float alpha = __fmul_rn(__fmul_rn(a.dloss[t], dco), a.inv_T);
+            float r = 0.f;
+            if (alpha != 0.f) {
+                const float gap = __fsub_rn(a.cref[t], __fmul_rn(lse, kLog2e));
+                r = __fmul_rn(alpha, exp2_approx(gap));
+                if (!(gap >= -kRefRangeLog2 && gap <= kRefRangeLog2) || !isfinite(r)) *a.flag = 1;
+            }
+            a.rs[t] = r;
+        }
     }
 }
 
@@ -648,7 +696,8 @@ __global__ void __launch_bounds__(256) metrics_partial_kernel(const float* mterm
     }
 }
 
-__global__ void metrics_final_kernel(const double* part, int nblk, rl_head_metrics* out) {
+__global__ void metrics_final_kernel(const double* part, int nblk, const int* flags, int nflags,
+                                     rl_head_metrics* out) {
     const int k = threadIdx.x;
     if (k >= kMetricFields) return;
     double s = 0.0;
@@ -667,7 +716,12 @@ __global__ void metrics_final_kernel(const double* part, int nblk, rl_head_metri
         case 10: out->masked_low = static_cast<int64_t>(s); break;
         case 11: out->masked_high = static_cast<int64_t>(s); break;
         case 12: out->n_age0 = static_cast<int64_t>(s); break;
-        case 13: out->reserved = 0; break;
+        case 13: {
+            int64_t r = 0;
+            for (int c = 0; c < nflags; ++c) r += flags[c] != 0 ? 1 : 0;
+            out->recomputed_chunks = r;
+            break;
+        }
         default: break;
     }
 }
@@ -679,11 +733,11 @@ int metrics_impl(const rl_head_batch* b, const void* saved, rl_head_metrics* met
 }
 
 int metrics_run(const rl_head_batch* b, const void* saved, rl_head_metrics* metrics, double* mpart,
-                cudaStream_t stream) {
+                cudaStream_t stream, const int* flags, int nflags) {
     const SavedView sv = saved_view(const_cast<void*>(saved), b->N, b->support.nnz, nullptr);
     ProfScope ps(RL_PROF_METRICS, stream);
     metrics_partial_kernel<<<kMetricBlocks, 256, 0, stream>>>(sv.mterm, b->N, mpart);
-    metrics_final_kernel<<<1, 32, 0, stream>>>(mpart, kMetricBlocks, metrics);
+    metrics_final_kernel<<<1, 32, 0, stream>>>(mpart, kMetricBlocks, flags, nflags, metrics);
     count_launch(2);
     return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }
@@ -692,11 +746,11 @@ int metrics_run(const rl_head_batch* b, const void* saved, rl_head_metrics* metr
 // Entry
 // ----------------------------------------------------------------------------------
 // GEMM + per-token loss for token rows [c0, c0 + n): per-token pointers are offset by c0,
-// CSR entry arrays stay absolute.  With E != nullptr the GEMM also stores the fp16 e
-// values and their per-chunk reference (fused forward + backward).
+// CSR entry arrays stay absolute.  With `es` (fused forward + backward) the GEMM also
+// stores e for the backward, in the layout EStore describes.
 int fwd_rows(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out, const SavedView& sv,
-             const FwdWs& w, int64_t c0, int64_t n, uint16_t* E, float* E32, float* M2, int sparse,
-             int32_t* status, cudaStream_t stream) {
+             const FwdWs& w, int64_t c0, int64_t n, const EStore* es, int sparse, int32_t* status,
+             cudaStream_t stream) {
     const int64_t H = b->H, V = b->V, nnz = b->support.nnz;
     if (n <= 0) return RL_OK;
     const int S = choose_splits(n, V);
@@ -707,31 +761,37 @@ int fwd_rows(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs
     rc = make_tmap_b(&tmW, b->weight, V, H, H);
     if (rc != RL_OK) return rc;
     const GemmPlan plan = make_plan_auto(n, V, H, 1, S, 1, status);
-    CUtensorMap tmE;
-    std::memset(&tmE, 0, sizeof(tmE));
-    if (E32 != nullptr)
-        rc = make_tmap_2d(&tmE, E32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, n, V, V, 32, 32, 1);
-    else if (E != nullptr)
-        rc = make_tmap_2d(&tmE, E, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, n, V, V, 64, 32, 1);
-    if (rc != RL_OK) return rc;
-    EpiStats::Params ep{n,
-                        static_cast<int32_t>(V),
-                        1.0f / prm->temperature,
-                        kLog2e / prm->temperature,
-                        nnz,
-                        b->labels + c0,
-                        b->support.offsets + c0,
-                        b->support.ids,
-                        sv.zlab + c0,
-                        sv.zsup,
-                        w.part_m,
-                        w.part_s,
-                        w.part_u,
-                        E,
-                        E32,
-                        M2,
-                        (V + 31) / 32,
-                        tmE};
+    EpiStats::Params ep;
+    std::memset(&ep, 0, sizeof(ep));
+    ep.N = n;
+    ep.V = static_cast<int32_t>(V);
+    ep.inv_T = 1.0f / prm->temperature;
+    ep.c2 = kLog2e / prm->temperature;
+    ep.nnz = nnz;
+    ep.labels = b->labels + c0;
+    ep.offsets = b->support.offsets + c0;
+    ep.ids = b->support.ids;
+    ep.zlab = sv.zlab + c0;
+    ep.zsup = sv.zsup;
+    ep.part_m = w.part_m;
+    ep.part_s = w.part_s;
+    ep.part_u = w.part_u;
+    ep.ldm = (V + 31) / 32;
+    if (es != nullptr && es->Eb != nullptr) {
+        ep.Eb = es->Eb;
+        ep.cref = es->cref;
+        ep.flag = es->flag;
+        if ((rc = make_tmap_2d(&ep.tmEb, es->Eb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, n, V, V, 32, 32, 64)) != RL_OK)
+            return rc;
+        if ((rc = make_tmap_2d(&ep.tmEbt, es->Ebt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, V, n, es->ldt, 32, 32, 0)) !=
+            RL_OK)
+            return rc;
+    } else if (es != nullptr && es->E32 != nullptr) {
+        ep.E32 = es->E32;
+        ep.M2 = es->M2;
+        if ((rc = make_tmap_2d(&ep.tmE32, es->E32, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, n, V, V, 32, 32, 128)) != RL_OK)
+            return rc;
+    }
     {
         ProfScope ps(RL_PROF_GEMM_FWD, stream);
         rc = launch_gemm_auto<EpiStats>(tmX, tmX, tmW, plan, ep, stream);
@@ -784,6 +844,12 @@ int fwd_rows(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs
     ta.sv.mterm = sv.mterm + c0 * 8;
     ta.sv.zlab = sv.zlab + c0;
     ta.status = status;
+    const bool rows_scale = es != nullptr && es->Eb != nullptr;
+    ta.cref = rows_scale ? es->cref : nullptr;
+    ta.dloss = rows_scale ? es->dloss : nullptr;
+    ta.inv_T = 1.0f / prm->temperature;
+    ta.rs = rows_scale ? es->rs : nullptr;
+    ta.flag = rows_scale ? es->flag : nullptr;
     {
         ProfScope ps(RL_PROF_TOKEN_LOSS, stream);
         token_loss_kernel<<<static_cast<unsigned>((n + 7) / 8), 256, 0, stream>>>(ta);
@@ -800,7 +866,7 @@ int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_ou
     if (N == 0) return RL_OK;
     const SavedView sv = saved_view(saved, N, nnz, nullptr);
     const FwdWs w = fwd_ws_view(ws, N, H, V, nnz, nullptr);
-    rc = fwd_rows(b, prm, out, sv, w, 0, N, nullptr, nullptr, nullptr, !bwd_is_dense(prm), status, stream);
+    rc = fwd_rows(b, prm, out, sv, w, 0, N, nullptr, !bwd_is_dense(prm), status, stream);
     if (rc != RL_OK) return rc;
     if (out->metrics) return metrics_impl(b, saved, out->metrics, ws, stream);
     return RL_OK;

@@ -90,11 +90,35 @@ int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_ou
                   void* saved, void* ws, int32_t* status, cudaStream_t stream);
 int metrics_impl(const rl_head_batch* b, const void* saved, rl_head_metrics* metrics, void* ws,
                  cudaStream_t stream);
+// flags / nflags: the fused path's per-chunk range flags (counted into recomputed_chunks)
 int metrics_run(const rl_head_batch* b, const void* saved, rl_head_metrics* metrics, double* mpart,
-                cudaStream_t stream);
+                cudaStream_t stream, const int* flags = nullptr, int nflags = 0);
+// What the forward GEMM of the fused forward + backward leaves for the backward of one
+// token chunk (all per-token arrays chunk-relative).
+//  bf16 gradient precision:  Eb [n, V] and Ebt [V, ldt] hold e = 2^(z log2(e) - cref) in
+//    bf16, one reference cref per row (the label logit, log2 units), so that the dense
+//    softmax gradient is G = rs * e with one scale rs = alpha 2^(cref - lse log2(e)) per
+//    row (token_loss writes rs).  *flag = 1 when a row's values leave the range where that
+//    holds; the chunk's dense backward then recomputes G from the logits instead.
+//  hi/lo gradient precision: E32 [n, V] holds e = 2^(z log2(e) - m2) in fp32 with the
+//    running max m2 it is relative to per 32-column chunk in M2 [n, ldm].
+struct EStore {
+    uint16_t* Eb = nullptr;
+    uint16_t* Ebt = nullptr;
+    int64_t ldt = 0;
+    const float* cref = nullptr;
+    int* flag = nullptr;
+    float* rs = nullptr;
+    const float* dloss = nullptr;
+    float* E32 = nullptr;
+    float* M2 = nullptr;
+};
+// Largest |log2| distance between a row's logits and its reference that the bf16 store
+// accepts; beyond it the chunk takes the recompute path.
+constexpr float kRefRangeLog2 = 64.f;
 int fwd_rows(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out, const SavedView& sv,
-             const FwdWs& w, int64_t c0, int64_t n, uint16_t* E, float* E32, float* M2, int sparse,
-             int32_t* status, cudaStream_t stream);
+             const FwdWs& w, int64_t c0, int64_t n, const EStore* es, int sparse, int32_t* status,
+             cudaStream_t stream);
 int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out,
                     const float* dloss, void* dhidden, float* dW, int accumulate, void* saved, void* ws,
                     int32_t* status, cudaStream_t stream);

@@ -125,7 +125,7 @@ int make_tmap_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t col
 }
 
 int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elem_bytes, int64_t rows,
-                 int64_t cols, int64_t ld, int box_cols, int box_rows, int swizzle128) {
+                 int64_t cols, int64_t ld, int box_cols, int box_rows, int swizzle_bytes) {
     auto fn = encode_fn();
     if (!fn) {
         set_last_error("cuTensorMapEncodeTiled unavailable");
@@ -141,7 +141,9 @@ int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, 
     cuuint32_t estride[2] = {1, 1};
     CUresult r = fn(map, dtype, 2, const_cast<void*>(base), gdim, gstride, box, estride,
                     CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                    : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                          : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         set_last_error("cuTensorMapEncodeTiled failed");
@@ -233,6 +235,6 @@ extern "C" const char* rl_profile_kind_name(int kind) {
     static const char* names[RL_PROF_KINDS] = {
         "validate", "gemm_fwd_stats", "token_loss", "metrics", "transpose", "gemm_bwd_grad",
         "gemm_bwd_dx", "gemm_bwd_dw", "sparse_dx", "sparse_dw", "policy", "gemm_util", "memset", "other",
-        "spike_resid", "grad_from_e"};
+        "spike_resid", "grad_from_e", "ref_logit"};
     return (kind >= 0 && kind < RL_PROF_KINDS) ? names[kind] : "unknown";
 }

@@ -69,11 +69,18 @@ def check_forward(case, hp, fwd, ref):
     flips = int(((gm_lab != ref["mask_label"]) & mask).sum())
     assert abs(gm["masked"] - rm["masked"]) <= flips
     assert gm["n_age0"] == rm["n_age0"]
+    # sums of per-token terms: 1e-4 relative plus, for the terms built from log-probs, the
+    # per-token log-prob bar summed over the tokens (twice: gpu and reference each within it)
+    tok_lp = np.maximum(lab_tol, 0.0)
+    if len(er):
+        np.maximum.at(tok_lp, er, sup_tol)      # worst log-prob bar of the token's entries
+    ent_tol = logp_tol(H, ref["lse"], ref["lse"])
+    age0 = np.asarray(inp["age"]) == 0 if inp.get("age") is not None else np.ones_like(mask)
+    extra = {"loss": ptol[mask].sum(), "mismatch_kl": 2 * lab_tol[mask].sum(), "kl": 2 * tok_lp[mask].sum(),
+             "kl_age0": 2 * tok_lp[mask & age0].sum(), "entropy": 2 * ent_tol[mask].sum(), "mask_tv": 2.0 * flips}
     for k in ("loss", "mismatch_kl", "support_mass", "mask_tv", "kl", "beta", "kl_age0", "entropy"):
-        tol = 1e-4 * max(abs(rm[k]), 1e-3 * rm["n_rl"]) + 1e-5 * rm["n_rl"] * (1 if k in ("mismatch_kl", "kl") else 0)
-        if k == "mask_tv":
-            tol += 2.0 * flips
-        assert abs(gm[k] - rm[k]) <= tol, (k, gm[k], rm[k])
+        tol = 1e-4 * max(abs(rm[k]), 1e-3 * rm["n_rl"]) + extra.get(k, 0.0)
+        assert abs(gm[k] - rm[k]) <= tol, (k, gm[k], rm[k], tol)
     return ref
 
 
@@ -107,9 +114,10 @@ def check_backward(case, hp, batch, fwd, reading=None, dloss=None, both=True):
 
 
 
-def check_fused(case, hp, reading=None, dloss=None):
+def check_fused(case, hp, reading=None, dloss=None, recomputed=0):
     """rl_head_loss_fwd_bwd (dloss given up front) against the oracle: every forward
-    output and both gradients, in the gradient precision of hp."""
+    output and both gradients, in the gradient precision of hp; ``recomputed`` is the
+    number of token chunks expected to take the recompute fallback."""
     dev = case.to("cuda")
     batch = rh.HeadBatch.from_case(dev)
     inp = case.numpy()
@@ -125,9 +133,9 @@ def check_fused(case, hp, reading=None, dloss=None):
     rX, rW, bnd = oracle.head_backward(inp, op, np.asarray(dloss, np.float64), want_bounds=True)
     H = inp["hidden"].shape[1]
     rd = reading or ("element" if hp.grad_precision == rh.RL_GRAD_SPLIT else "operand")
-    H = inp["hidden"].shape[1]
     grad_check(dX.float().cpu().numpy(), rX, rd, "dX", bnd, "X", H)
     grad_check(dW.cpu().numpy(), rW, rd, "dW", bnd, "W", H)
+    assert fwd.metrics()["recomputed_chunks"] == recomputed
     return fwd, dX, dW
 
 

@@ -133,8 +133,15 @@ def test_c4_full_size_sampled():
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     # same arithmetic, but the fused call runs the forward per 16k-token chunk (its own
-    # vocabulary split count), so the logsumexp partials combine in another order
-    torch.testing.assert_close(f2.loss, fwd.loss, rtol=1e-5, atol=1e-6)
+    # vocabulary split count), so the logsumexp partials combine in another order: each
+    # call's log-probs lie within logp_tol of the oracle, so per token the two losses differ
+    # by at most that bar twice, carried through |dloss/dlogP| <= |adv_tau A| (w + sum|c|)
+    # + beta sum u <= |adv_tau A| 2 cap + beta (ipo: w <= cap; K draws: sum u = 1)
+    lse2 = f2.lse.cpu().double().numpy()
+    np.testing.assert_array_less(np.abs(lse2 - fwd.lse.cpu().double().numpy()), 2 * logp_tol(H, lse2, lse2))
+    gain = np.abs(hp.adv_tau * inp["adv"]) * 2 * hp.max_importance_ratio + hp.kl_coeff
+    l1, l2 = fwd.loss.cpu().double().numpy(), f2.loss.cpu().double().numpy()
+    np.testing.assert_array_less(np.abs(l1 - l2), gain * 2 * logp_tol(H, lse2, lse2) + 1e-4 * np.abs(l2))
     scale = dW2.abs().max().item()
     assert (dW - dW2).abs().max().item() <= 2 ** -7 * scale
     assert (dX.float() - dX2.float()).abs().max().item() <= 2 ** -7 * dX2.float().abs().max().item()

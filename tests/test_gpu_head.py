@@ -178,6 +178,24 @@ def test_fused_c1_and_matches_unfused():
     assert (dW - dW2).abs().max().item() <= 2 ** -7 * scale
 
 
+def test_fused_recompute_fallback_when_label_far_below_max():
+    """Rows whose label logit lies ~86 nats below the row's max logit: numerators stored
+    relative to the label would leave bf16's range, so the fused call sends their token
+    chunk (and only it) through the gated logit recompute.  Everything still matches the
+    oracle, and the metrics count the one chunk."""
+    case = workloads.make_head_case("c1", n_tokens=300, hidden_scale=60.0, noise=0.1, seed=121)
+    inp = case.numpy()
+    z = inp["hidden"] @ inp["W"].T
+    for t in (140, 141, 200):   # all in the second chunk of 128 tokens
+        v = int(np.argmin(z[t]))
+        lse = float(np.max(z[t]) + np.log(np.sum(np.exp(z[t] - np.max(z[t])))))
+        case.labels[t] = v
+        case.label_logq[t] = float(z[t, v] - lse)
+    hp = rh.HeadParams(loss_type=rh.RL_LOSS_IPO, eps=0.3, max_importance_ratio=10.0, kl_coeff=0.02,
+                       bwd_mode=rh.RL_BWD_DENSE, token_chunk=128)
+    check_fused(case, hp, recomputed=1)
+
+
 def test_fused_sparse_mode_and_replay():
     case = workloads.make_head_case("c1", n_tokens=200, support="replay", top_p=0.9, hidden_scale=6.0,
                                     noise=0.3, seed=91)
