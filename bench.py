@@ -169,6 +169,51 @@ def cpu_baseline(case_host: dict, n_tokens: int, threads: int):
                       f"forward + backward incl. dW; {dt:.1f} s"}
 
 
+def elementwise_side(rh, torch, dev, flush, steps: int, warmup: int, peaks: dict):
+    """The elementwise PPO / dual-clip / decoupled-TIS / mismatch path on its own workload
+    (1.8M valid tokens in sequences of 64..4096, padded to 4096), against the HBM roofline.
+    Each pass follows a 1 GB memset (an L2 flush long enough that the host has queued the
+    pass before the GPU reaches it) and is timed by the library's own event pair around
+    its launches (rl_profile), so host launch gaps stay out of a pass of some 20 us.
+    Algorithmic bytes per slot: four fp32 inputs and the mask byte read, four fp32
+    outputs written (33 B)."""
+    import workloads
+    c = workloads.make_policy_case()
+    ins = [torch.from_numpy(x).to(dev) for x in (c.lp_theta, c.lp_old, c.lp_samp, c.adv, c.mask)]
+    T = int(ins[0].numel())
+    pp = rh.PgParams()
+    outs = tuple(torch.empty(T, dtype=torch.float32, device=dev) for _ in range(4))
+    met = torch.zeros(rh.ctypes.sizeof(rh.RlPgMetrics), dtype=torch.uint8, device=dev)
+    ws = torch.empty(rh.rl_policy_workspace_bytes(T), dtype=torch.uint8, device=dev)
+    run = lambda: rh.rl_policy_loss_elementwise(*ins, pp, outputs=outs, ws=ws, metrics_dev=met)
+    big = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    per = []
+    for _ in range(steps):
+        big.zero_()
+        rh.rl_profile_enable(True)
+        run()
+        prof = rh.rl_profile_read()
+        rh.rl_profile_enable(False)
+        per.append(sum(t for t, _ in prof.values()))
+    del big
+    ms = statistics.median(per)
+    nbytes = T * (4 * 4 + 1) + T * 4 * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    n_valid = int(c.mask.sum())
+    return {"workload": f"c5: {n_valid} valid tokens, {len(c.seq_lens)} sequences of 64..4096 padded to "
+                        f"{c.max_len} (T={T} slots); PPO clip 0.2/0.2 + dual clip 3, decoupled TIS, "
+                        "10-point IPO curve, IcePop band, mismatch KL",
+            "us_per_pass": ms * 1e3, "tokens_per_s": n_valid / (ms / 1e3), "passes": steps,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": None, "algorithmic_bytes_per_pass": nbytes,
+                         "peak_kind": f"hbm_gbs ({peaks['source']})"},
+            "l2": "1 GB memset before each pass (outside the events)"}
+
+
 def host_inputs(case):
     """The batch as numpy (fp64 copies of bf16 values) for the oracle."""
     return case.numpy()
@@ -375,6 +420,8 @@ def run_ours(args):
             "e2e": {"value": e_value, "unit": "tokens/s", "ms_per_step": e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "clocks": clocks, "gpu_launches": int(launches), "input_gen_s": t_gen}
+    if not args.no_elementwise:
+        line["elementwise"] = elementwise_side(rh, torch, dev, flush, max(args.steps, 10), args.warmup, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = host_inputs(case_first(case, args.cpu_tokens))
         line["cpu_baseline"] = cpu_baseline(host, args.cpu_tokens, os.cpu_count() or 1)
@@ -424,6 +471,7 @@ def main(argv=None):
     ap.add_argument("--tokens", type=int, default=None, help="fewer tokens, same shapes (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true", help="skip the two-call side figure")
+    ap.add_argument("--no-elementwise", action="store_true", help="skip the elementwise-path side figure")
     ap.add_argument("--gemm-pair", type=int, choices=[0, 1], default=None,
                     help="tensor-core GEMMs on SM pairs (1) or single SMs (0); default: library default")
     args = ap.parse_args(argv)

@@ -250,8 +250,8 @@ int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const
  * where an extra cudaMalloc would fail or compete with that pool, or plain C code with
  * no device allocator at hand.  This variant takes no workspace and allocates nothing:
  * its scratch (the per-block partial sums of the metric reduction) is a file-scope
- * device array of 229376 bytes, enough for 1024 blocks; a launch uses at most 4 blocks
- * per SM, so a device with more than 256 SMs is rejected with RL_ERR_WORKSPACE.
+ * device array of 229376 bytes, enough for 1024 blocks; a launch uses at most 2 blocks
+ * per SM, so a device with more than 512 SMs is rejected with RL_ERR_WORKSPACE.
  *   - Every GPU that loads the library holds that array until the process exits.
  *   - The first call on a device looks the array's device address up (once per
  *     device); make that first call before any stream capture.

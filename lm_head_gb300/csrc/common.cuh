@@ -44,7 +44,7 @@ RL_DEVINL float warp_max(float v) {
     return v;
 }
 
-RL_DEVINL float exp2_approx(float x) {  // hardware 2^x (MUFU), x <= 0 in every use here
+RL_DEVINL float exp2_approx(float x) {  // hardware 2^x (MUFU EX2, about 2 ulp; subnormal results flush to 0)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;

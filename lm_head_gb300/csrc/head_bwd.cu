@@ -6,7 +6,8 @@
 //     G_tj = alpha_t * P_full,tj  +  sum over spikes (label, support entries)
 // where alpha_t = g_t * dcoef_t / T is non-zero only on untruncated rows whose gradient
 // has a dense softmax part (the forward folds a replayed row's renormalised-softmax term
-// into its support entries).  The spikes always go through the sparse path:
+// into its support entries).  In the two-call path (and the fused hi/lo path) the spikes
+// go through the sparse path exactly:
 //     dX_t += sum_e c_e W[v_e],    dW[v] += sum_{e: v_e = v} c_e x_t     (fixed order)
 // and the dense part, chunk by chunk over tokens, through three tcgen05 GEMMs:
 //     G_c  = alpha * exp(X_c W^T / T - lse)      (EpiGrad: writes G_c [n, V] and G_c^T)
@@ -181,24 +182,27 @@ struct EpiDx {
         uint16_t* out;      // chunk-relative [n, H] bf16
         const float* rs;    // chunk-relative [n], or nullptr
         const int* flag;    // with rs
+        const int* dxs_gate;   // optional: dxs holds data only when *dxs_gate != 0
     };
     int64_t t;
-    bool valid;
+    bool valid, with_dxs;
     float scale;
     RL_DEVINL void begin_unit(const Params& p, int row, int, int m_blk, int, int) {
         t = static_cast<int64_t>(m_blk) * kBM + row;
         valid = t < p.n;
         scale = 1.f;
         if (valid && p.rs != nullptr && *p.flag == 0) scale = p.rs[t];
+        with_dxs = p.dxs_gate == nullptr || *p.dxs_gate != 0;
     }
     RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0, uint8_t*, int) {
         if (!valid || col0 >= p.H) return;
         const float4* s = reinterpret_cast<const float4*>(p.dxs + t * p.H + col0);
         uint4* o = reinterpret_cast<uint4*>(p.out + t * p.H + col0);
         const float c = scale;
+        const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float4 a = s[2 * q], b = s[2 * q + 1];
+            const float4 a = with_dxs ? s[2 * q] : zero, b = with_dxs ? s[2 * q + 1] : zero;
             o[q] = make_uint4(pack_bf16x2(fmaf(__uint_as_float(acc[8 * q + 0]), c, a.x), fmaf(__uint_as_float(acc[8 * q + 1]), c, a.y)),
                               pack_bf16x2(fmaf(__uint_as_float(acc[8 * q + 2]), c, a.z), fmaf(__uint_as_float(acc[8 * q + 3]), c, a.w)),
                               pack_bf16x2(fmaf(__uint_as_float(acc[8 * q + 4]), c, b.x), fmaf(__uint_as_float(acc[8 * q + 5]), c, b.y)),
@@ -299,7 +303,11 @@ struct SparseArgs {
     // dense mode only (nullptr otherwise): per gradient item, what the bf16 dense GEMM
     // operand dropped at that (token, vocab id); non-zero once per distinct pair
     const float* resid;
+    // optional: the sparse kernels do nothing unless *gate != 0 (device-side decision)
+    const int* gate;
 };
+
+RL_DEVINL bool gate_closed(const int* gate) { return gate != nullptr && *gate == 0; }
 
 // True when `v` occurs among ids[b, e) (ascending).
 RL_DEVINL bool row_contains(const int32_t* ids, int64_t b, int64_t e, int32_t v) {
@@ -407,6 +415,7 @@ RL_DEVINL void fma_row8(float (&acc)[8], const uint16_t* row, float c) {
 
 template <bool kToBf16>
 __global__ void __launch_bounds__(256) sparse_dx_kernel(SparseArgs a, int64_t t0, float* dxs, uint16_t* dx_bf16) {
+    if (gate_closed(a.gate)) return;
     const int64_t t = t0 + blockIdx.x;   // output row blockIdx.x (chunk-relative)
     const float g = a.dloss[t] * a.inv_T;
     int64_t b = a.offsets[t], e = a.offsets[t + 1];
@@ -443,6 +452,7 @@ __global__ void __launch_bounds__(256) sparse_dx_kernel(SparseArgs a, int64_t t0
 // vocab id sums its items in item order (items: support entries 0..nnz-1, then labels).
 // ----------------------------------------------------------------------------------
 __global__ void items_init_kernel(SparseArgs a, int32_t* item_tok, int32_t* keys, int32_t* vals) {
+    if (gate_closed(a.gate)) return;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (t >= a.N) return;
@@ -466,7 +476,8 @@ __global__ void items_init_kernel(SparseArgs a, int32_t* item_tok, int32_t* keys
 
 // Entries with a corrupt row range never get a token; mark them out of range.
 __global__ void items_guard_kernel(const int64_t* offsets, int64_t N, int64_t nnz, int32_t V,
-                                   int32_t* item_tok, int32_t* keys) {
+                                   int32_t* item_tok, int32_t* keys, const int* gate) {
+    if (gate_closed(gate)) return;
     const int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (j >= nnz) return;
     const int32_t t = item_tok[j];
@@ -482,7 +493,8 @@ __global__ void items_guard_kernel(const int64_t* offsets, int64_t N, int64_t nn
 }
 
 __global__ void __launch_bounds__(256) radix_hist_kernel(const int32_t* keys, int64_t n, int shift,
-                                                         int32_t* hist, int64_t tiles) {
+                                                         int32_t* hist, int64_t tiles, const int* gate) {
+    if (gate_closed(gate)) return;
     __shared__ int cnt[kDigits];
     for (int i = threadIdx.x; i < kDigits; i += blockDim.x) cnt[i] = 0;
     __syncthreads();
@@ -496,7 +508,8 @@ __global__ void __launch_bounds__(256) radix_hist_kernel(const int32_t* keys, in
 }
 
 // Exclusive scan over hist in digit-major order (single block).
-__global__ void __launch_bounds__(1024) radix_scan_kernel(int32_t* hist, int64_t len) {
+__global__ void __launch_bounds__(1024) radix_scan_kernel(int32_t* hist, int64_t len, const int* gate) {
+    if (gate_closed(gate)) return;
     __shared__ int64_t part[1024];
     const int64_t per = (len + blockDim.x - 1) / blockDim.x;
     const int64_t b = threadIdx.x * per;
@@ -527,7 +540,8 @@ __global__ void __launch_bounds__(1024) radix_scan_kernel(int32_t* hist, int64_t
 __global__ void __launch_bounds__(32) radix_scatter_kernel(const int32_t* keys_in, const int32_t* vals_in,
                                                            int64_t n, int shift, const int32_t* hist,
                                                            int64_t tiles, int32_t* keys_out,
-                                                           int32_t* vals_out) {
+                                                           int32_t* vals_out, const int* gate) {
+    if (gate_closed(gate)) return;
     __shared__ int base[kDigits];
     const int lane = threadIdx.x;
     for (int i = lane; i < kDigits; i += 32) base[i] = hist[static_cast<int64_t>(i) * tiles + blockIdx.x];
@@ -554,7 +568,8 @@ __global__ void __launch_bounds__(32) radix_scatter_kernel(const int32_t* keys_i
 }
 
 // bucket[v] = first sorted position whose key >= v, for v in [0, V + 1].
-__global__ void bucket_kernel(const int32_t* keys, int64_t n, int32_t V, int64_t* bucket) {
+__global__ void bucket_kernel(const int32_t* keys, int64_t n, int32_t V, int64_t* bucket, const int* gate) {
+    if (gate_closed(gate)) return;
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i > n) return;
     const int64_t prev = i == 0 ? -1 : keys[i - 1];
@@ -565,6 +580,7 @@ __global__ void bucket_kernel(const int32_t* keys, int64_t n, int32_t V, int64_t
 __global__ void __launch_bounds__(256) sparse_dw_kernel(SparseArgs a, const int32_t* vals,
                                                         const int32_t* item_tok, const int64_t* bucket,
                                                         float* dW) {
+    if (gate_closed(a.gate)) return;
     const int64_t v = blockIdx.x;
     const int64_t b = bucket[v], e = bucket[v + 1];
     if (e <= b) return;
@@ -603,7 +619,7 @@ static int sparse_dw(const SparseArgs& a, const BwdWs& w, float* dW, cudaStream_
     items_init_kernel<<<static_cast<unsigned>((a.N + 7) / 8), 256, 0, s>>>(a, w.item_tok, w.keys_a, w.vals_a);
     if (a.nnz > 0)
         items_guard_kernel<<<static_cast<unsigned>((a.nnz + 255) / 256), 256, 0, s>>>(
-            a.offsets, a.N, a.nnz, static_cast<int32_t>(a.V), w.item_tok, w.keys_a);
+            a.offsets, a.N, a.nnz, static_cast<int32_t>(a.V), w.item_tok, w.keys_a, a.gate);
     count_launch(2);
     const int64_t tiles = (n + kSortTile - 1) / kSortTile;
     int bits = 1;
@@ -612,9 +628,10 @@ static int sparse_dw(const SparseArgs& a, const BwdWs& w, float* dW, cudaStream_
     int32_t *kin = w.keys_a, *vin = w.vals_a, *kout = w.keys_b, *vout = w.vals_b;
     for (int p = 0; p < passes; ++p) {
         const int shift = p * kDigitBits;
-        radix_hist_kernel<<<static_cast<unsigned>(tiles), 256, 0, s>>>(kin, n, shift, w.hist, tiles);
-        radix_scan_kernel<<<1, 1024, 0, s>>>(w.hist, tiles * kDigits);
-        radix_scatter_kernel<<<static_cast<unsigned>(tiles), 32, 0, s>>>(kin, vin, n, shift, w.hist, tiles, kout, vout);
+        radix_hist_kernel<<<static_cast<unsigned>(tiles), 256, 0, s>>>(kin, n, shift, w.hist, tiles, a.gate);
+        radix_scan_kernel<<<1, 1024, 0, s>>>(w.hist, tiles * kDigits, a.gate);
+        radix_scatter_kernel<<<static_cast<unsigned>(tiles), 32, 0, s>>>(kin, vin, n, shift, w.hist, tiles, kout,
+                                                                         vout, a.gate);
         count_launch(3);
         int32_t* tk = kin;
         kin = kout;
@@ -623,7 +640,8 @@ static int sparse_dw(const SparseArgs& a, const BwdWs& w, float* dW, cudaStream_
         vin = vout;
         vout = tv;
     }
-    bucket_kernel<<<static_cast<unsigned>((n + 1 + 255) / 256), 256, 0, s>>>(kin, n, static_cast<int32_t>(a.V), w.bucket);
+    bucket_kernel<<<static_cast<unsigned>((n + 1 + 255) / 256), 256, 0, s>>>(kin, n, static_cast<int32_t>(a.V), w.bucket,
+                                                                             a.gate);
     sparse_dw_kernel<<<static_cast<unsigned>(a.V), 256, 0, s>>>(a, vin, w.item_tok, w.bucket, dW);
     count_launch(2);
     return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
@@ -737,7 +755,9 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
 // (dW += e^T (rs X)).  So the backward reads e straight from the forward's output.
 // If a row's logits leave the range of that representation (max logit more than 2^64
 // above the reference, or a scale out of range) the chunk's flag is set and a gated GEMM
-// recomputes G into Eb / Ebt with rs = 1 (the two-call path's arithmetic).
+// recomputes G into Eb / Ebt with rs = 1 (the two-call path's arithmetic).  The spikes
+// are then folded into e (fold_kernel), so the dense GEMMs carry the whole gradient and
+// the sparse kernels run (gated) only for rows without a dense part.
 //
 // hi/lo gradient precision.  The forward stores e = 2^(z log2(e) - m2) in fp32 with its
 // running-max reference per 32-column chunk, and grad_from_e_kernel forms
@@ -773,6 +793,90 @@ __global__ void __launch_bounds__(256) ref_logit_kernel(const uint16_t* X, const
         const float c = acc * c2;
         cref[t] = (ok && isfinite(c)) ? c : 0.f;
     }
+}
+
+// Spikes (label and support coefficients, pull request #4233's loss_t differentiated with
+// w, c, u held constant) folded into the stored e of their row: with the dense gradient
+// G = rs e, the total gradient at (t, v) is rs (e + c / rs), so e[t, v] becomes
+// bf16(e + c / rs) in both layouts and the dense GEMMs carry the spikes too.  e is
+// re-formed there in fp32 from the forward's fp32 logit (zsup / zlab), so the stored
+// value is rounded to bf16 once.  c sums every coefficient at that id (duplicate draws, a
+// label that is also a support id) in entry order.  After a recompute (flag set) the
+// stored value is G itself (rs = 1) and the fp32 value is alpha exp(z - lse).  A row with
+// rs = 0 (no dense part: replayed, or a zero coefficient) cannot fold; its spikes stay on
+// the sparse path, which gets dls_t = dloss_t for it (0 for folded rows), and the chunk's
+// and the call's sparse gates open.  One warp per token.
+struct FoldArgs {
+    int64_t t0, n, V, nnz, ldt;
+    const int32_t* labels;    // absolute
+    const int64_t* offsets;   // absolute
+    const int32_t* ids;
+    const float* dloss;       // absolute
+    const float* labcoef;     // absolute
+    const float* entcoef;
+    const float* zlab;        // absolute
+    const float* zsup;
+    const float* dcoef;       // absolute
+    const float* lse;         // absolute
+    float inv_T;
+    const float* cref;        // chunk-relative
+    const float* rs;          // chunk-relative
+    const int* flag;
+    uint16_t* Eb;             // [n, V] chunk
+    uint16_t* Ebt;            // [V, ldt] chunk
+    float* dls;               // absolute [N]
+    int* open_chunk;
+    int* open_any;
+};
+
+RL_DEVINL void fold_at(const FoldArgs& a, int64_t r, int32_t v, float x) {
+    const uint16_t nv = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+    a.Eb[r * a.V + v] = nv;
+    a.Ebt[static_cast<int64_t>(v) * a.ldt + r] = nv;
+}
+
+__global__ void __launch_bounds__(256) fold_kernel(FoldArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (r >= a.n) return;
+    const int64_t t = a.t0 + r;
+    int64_t b = a.offsets[t], e = a.offsets[t + 1];
+    b = b < 0 ? 0 : (b > a.nnz ? a.nnz : b);
+    e = e < b ? b : (e > a.nnz ? a.nnz : e);
+    const float g = a.dloss[t] * a.inv_T;   // as the sparse path forms it
+    const float sc = *a.flag != 0 ? 1.f : a.rs[r];
+    const int32_t lab = a.labels[t];
+    const float cl = g * a.labcoef[t];
+    if (sc == 0.f) {
+        bool any = false;
+        for (int64_t j = b + lane; j < e; j += 32) any |= g * a.entcoef[j] != 0.f;
+        any = __any_sync(0xffffffffu, any) || cl != 0.f;
+        if (lane == 0) {
+            a.dls[t] = a.dloss[t];
+            if (any) {
+                *a.open_chunk = 1;
+                *a.open_any = 1;
+            }
+        }
+        return;
+    }
+    if (lane == 0) a.dls[t] = 0.f;
+    const bool rec = *a.flag != 0;
+    const float alpha = dense_alpha(a.dloss[t], a.dcoef[t], a.inv_T);
+    const float lse = a.lse[t], cr = a.cref[r];
+    auto dense_at = [&](float z) -> float {   // the stored quantity before rounding
+        return rec ? dense_grad(alpha, z, lse) : exp2_approx(__fsub_rn(__fmul_rn(z, kLog2e), cr));
+    };
+    for (int64_t j = b + lane; j < e; j += 32) {
+        const int32_t id = a.ids[j];
+        if ((j > b && a.ids[j - 1] == id) || id < 0 || id >= a.V) continue;   // first entry of its id only
+        float c = 0.f;
+        for (int64_t k = j; k < e && a.ids[k] == id; ++k) c = __fadd_rn(c, g * a.entcoef[k]);
+        if (id == lab) c = __fadd_rn(c, cl);
+        if (c != 0.f) fold_at(a, r, id, __fadd_rn(dense_at(a.zsup[j]), c / sc));
+    }
+    if (lane == 0 && lab >= 0 && lab < a.V && cl != 0.f && !row_contains(a.ids, b, e, lab))
+        fold_at(a, r, lab, __fadd_rn(dense_at(a.zlab[t]), cl / sc));
 }
 
 struct GradEArgs {
@@ -861,6 +965,8 @@ struct FusedWs {
     uint16_t* Ebt;   // [V, chunk]
     float* cref;     // [chunk]
     float* rs;       // [chunk]
+    float* dls;      // [N] dloss for the rows whose spikes stay on the sparse path, else 0
+    int* gates;      // [nchunks + 1] sparse-path gate per chunk, then for the whole call
     int* flags;      // [nchunks] range flag per chunk
     // hi/lo gradient precision
     float* E32;      // [chunk, V]
@@ -895,6 +1001,8 @@ static FusedWs fused_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_
         f.Ebt = c.take<uint16_t>(static_cast<size_t>(V) * f.chunk);
         f.cref = c.take<float>(f.chunk);
         f.rs = c.take<float>(f.chunk);
+        f.dls = c.take<float>(N);
+        f.gates = c.take<int>(f.nchunks + 1);
     }
     f.flags = c.take<int>(f.nchunks > 0 ? f.nchunks : 1);
     w.Wt = c.take<uint16_t>(static_cast<size_t>(V) * H);
@@ -946,9 +1054,14 @@ int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_
     const FusedWs f = fused_ws_view(ws, N, H, V, nnz, prm, nullptr);
     const BwdWs& w = f.bw;
     const float inv_T = 1.0f / prm->temperature;
+    // hi/lo: exact spikes on the sparse path (with the residuals of the dense operands);
+    // bf16: spikes folded into e, the sparse path only for rows that cannot fold
     SparseArgs sa{N, H, V, nnz,
                   static_cast<const uint16_t*>(b->weight), static_cast<const uint16_t*>(b->hidden),
-                  b->labels, b->support.offsets, b->support.ids, dloss, sv.labcoef, sv.entcoef, inv_T, w.resid};
+                  b->labels, b->support.offsets, b->support.ids, w.split ? dloss : f.dls, sv.labcoef, sv.entcoef,
+                  inv_T, w.split ? w.resid : nullptr, w.split ? nullptr : f.gates + f.nchunks};
+    if (!w.split && cudaMemsetAsync(f.gates, 0, sizeof(int) * (f.nchunks + 1), stream) != cudaSuccess)
+        return RL_ERR_CUDA;
     rc = transpose_bf16(b->weight, V, H, H, w.Wt, V, stream);
     if (rc != RL_OK) return rc;
     CUtensorMap tmW, tmWt;
@@ -993,9 +1106,14 @@ int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_
                 if ((rc = launch_gemm_auto<EpiGrad>(tmX, tmX, tmW, pg, gp, stream)) != RL_OK) return rc;
             }
             count_launch();
-            ResidArgs ra{c0, n, V, nnz, b->labels, b->support.offsets, b->support.ids, dloss, sv.dcoef, sv.lse,
-                         sv.zlab, sv.zsup, inv_T, 0, w.resid, nullptr, nullptr, 0, f.Eb, f.rs, flag};
-            if ((rc = launch_resid(ra, stream)) != RL_OK) return rc;
+            {
+                FoldArgs fa{c0, n, V, nnz, f.chunk, b->labels, b->support.offsets, b->support.ids, dloss,
+                            sv.labcoef, sv.entcoef, sv.zlab, sv.zsup, sv.dcoef, sv.lse, inv_T, f.cref, f.rs, flag,
+                            f.Eb, f.Ebt, f.dls, f.gates + ci, f.gates + f.nchunks};
+                ProfScope ps(RL_PROF_RESID, stream);
+                fold_kernel<<<static_cast<unsigned>((n + 7) / 8), 256, 0, stream>>>(fa);
+                count_launch();
+            }
             if ((rc = transpose_bf16(Xc, n, H, H, w.Xt, f.chunk, stream, f.rs, flag)) != RL_OK) return rc;
             if ((rc = make_tmap_bf16(&tmA, f.Eb, n, V, V, kBM)) != RL_OK) return rc;
             if ((rc = make_tmap_bf16(&tmAt, f.Ebt, V, n, f.chunk, kBM)) != RL_OK) return rc;
@@ -1023,13 +1141,15 @@ int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_
             if ((rc = make_tmap_bf16(&tmAtlo, w.Gt_lo, V, n, f.chunk, kBM)) != RL_OK) return rc;
         }
         {
+            SparseArgs sc = sa;
+            if (!w.split) sc.gate = f.gates + ci;
             ProfScope ps(RL_PROF_SPARSE_DX, stream);
-            sparse_dx_kernel<false><<<static_cast<unsigned>(n), 256, 0, stream>>>(sa, c0, w.dxs, nullptr);
+            sparse_dx_kernel<false><<<static_cast<unsigned>(n), 256, 0, stream>>>(sc, c0, w.dxs, nullptr);
             count_launch();
         }
         if ((rc = make_tmap_b(&tmXt, w.Xt, H, n, f.chunk)) != RL_OK) return rc;
         EpiDx::Params dp{n, static_cast<int32_t>(H), w.dxs, static_cast<uint16_t*>(dhidden) + c0 * H,
-                         w.split ? nullptr : f.rs, flag};
+                         w.split ? nullptr : f.rs, flag, w.split ? nullptr : f.gates + ci};
         const GemmPlan p2 = make_plan_auto(n, H, V, passes, 1 << 30, 0, status);
         {
             ProfScope ps(RL_PROF_GEMM_DX, stream);

@@ -696,12 +696,16 @@ __global__ void __launch_bounds__(256) metrics_partial_kernel(const float* mterm
     }
 }
 
+// One warp per field: lane l sums the block partials b = l, l + 32, ... in order, then a
+// fixed shuffle tree.
 __global__ void metrics_final_kernel(const double* part, int nblk, const int* flags, int nflags,
                                      rl_head_metrics* out) {
-    const int k = threadIdx.x;
+    const int k = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (k >= kMetricFields) return;
     double s = 0.0;
-    for (int b = 0; b < nblk; ++b) s += part[b * kMetricFields + k];
+    for (int b = lane; b < nblk; b += 32) s += part[b * kMetricFields + k];
+    s = warp_sum(s);
+    if (lane != 0) return;
     switch (k) {
         case 0: out->loss = s; break;
         case 1: out->mismatch_kl = s; break;
@@ -737,7 +741,7 @@ int metrics_run(const rl_head_batch* b, const void* saved, rl_head_metrics* metr
     const SavedView sv = saved_view(const_cast<void*>(saved), b->N, b->support.nnz, nullptr);
     ProfScope ps(RL_PROF_METRICS, stream);
     metrics_partial_kernel<<<kMetricBlocks, 256, 0, stream>>>(sv.mterm, b->N, mpart);
-    metrics_final_kernel<<<1, 32, 0, stream>>>(mpart, kMetricBlocks, flags, nflags, metrics);
+    metrics_final_kernel<<<1, 32 * kMetricFields, 0, stream>>>(mpart, kMetricBlocks, flags, nflags, metrics);
     count_launch(2);
     return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }

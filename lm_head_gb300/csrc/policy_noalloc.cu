@@ -65,7 +65,7 @@ extern "C" int rl_policy_loss_elementwise_noalloc(const float* lp_theta, const f
     const size_t need = policy_ws_need(T);
     if (need > kNoAllocScratchBytes) {
         set_last_error("rl_policy_loss_elementwise_noalloc: this launch needs more partial-sum scratch "
-                       "than the 229376-byte static array holds (more than 256 SMs)");
+                       "than the 229376-byte static array holds (more than 512 SMs)");
         return RL_ERR_WORKSPACE;
     }
     void* scratch = nullptr;

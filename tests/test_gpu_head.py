@@ -196,6 +196,31 @@ def test_fused_recompute_fallback_when_label_far_below_max():
     check_fused(case, hp, recomputed=1)
 
 
+def _concat_cases(a, b):
+    """Tokens of a, then tokens of b, on a's weights (b's sampler evidence stays valid
+    input: the checks on it do not involve the trainer's weights)."""
+    import dataclasses as dc
+    cat = lambda f: torch.cat([getattr(a, f), getattr(b, f)])
+    off = torch.cat([a.offsets, b.offsets[1:] + a.offsets[-1]])
+    return dc.replace(a, hidden=cat("hidden"), labels=cat("labels"), label_logq=cat("label_logq"), adv=cat("adv"),
+                      loss_mask=cat("loss_mask"), age=cat("age"), replayed=cat("replayed"), offsets=off,
+                      ids=cat("ids"), logq=cat("logq"))
+
+
+def test_fused_mixed_replayed_and_draw_rows():
+    """Dense fused backward over draw rows (spikes folded into the dense operand) and
+    replayed rows (no dense part: spikes on the gated sparse path) in one batch; chunks of
+    128 give one all-draw chunk, one mixed, one all-replayed."""
+    a = workloads.make_head_case("c1", n_tokens=160, hidden_scale=8.0, noise=0.7, age_max=4, seed=131)
+    b = workloads.make_head_case("c1", n_tokens=140, support="replay", top_p=0.9, hidden_scale=8.0, noise=0.3,
+                                 age_max=4, seed=132)
+    case = _concat_cases(a, b)
+    hp = rh.HeadParams(loss_type=rh.RL_LOSS_IPO, eps=0.3, max_importance_ratio=10.0, kl_coeff=0.02,
+                       kl_estimator=rh.RL_KL_EXACT, kl_staleness=rh.RL_STALE_INV_SQRT, bwd_mode=rh.RL_BWD_DENSE,
+                       token_chunk=128)
+    check_fused(case, hp)
+
+
 def test_fused_sparse_mode_and_replay():
     case = workloads.make_head_case("c1", n_tokens=200, support="replay", top_p=0.9, hidden_scale=6.0,
                                     noise=0.3, seed=91)
