@@ -172,9 +172,10 @@ def cpu_baseline(case_host: dict, n_tokens: int, threads: int):
 def elementwise_side(rh, torch, dev, flush, steps: int, warmup: int, peaks: dict):
     """The elementwise PPO / dual-clip / decoupled-TIS / mismatch path on its own workload
     (1.8M valid tokens in sequences of 64..4096, padded to 4096), against the HBM roofline.
-    Each pass follows a 1 GB memset (an L2 flush long enough that the host has queued the
-    pass before the GPU reaches it) and is timed by the library's own event pair around
-    its launches (rl_profile), so host launch gaps stay out of a pass of some 20 us.
+    Each pass follows a 4 GB memset (an L2 flush that keeps the GPU busy for about half a
+    millisecond, long enough for the host to queue the pass before the GPU reaches it) and
+    is timed by the library's own event pair around its launches (rl_profile), so host
+    launch gaps stay out of a pass of a few tens of microseconds.
     Algorithmic bytes per slot: four fp32 inputs and the mask byte read, four fp32
     outputs written (33 B)."""
     import workloads
@@ -186,7 +187,7 @@ def elementwise_side(rh, torch, dev, flush, steps: int, warmup: int, peaks: dict
     met = torch.zeros(rh.ctypes.sizeof(rh.RlPgMetrics), dtype=torch.uint8, device=dev)
     ws = torch.empty(rh.rl_policy_workspace_bytes(T), dtype=torch.uint8, device=dev)
     run = lambda: rh.rl_policy_loss_elementwise(*ins, pp, outputs=outs, ws=ws, metrics_dev=met)
-    big = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    big = torch.empty(4 << 30, dtype=torch.uint8, device=dev)
     for _ in range(warmup):
         run()
     torch.cuda.synchronize()
@@ -211,7 +212,7 @@ def elementwise_side(rh, torch, dev, flush, steps: int, warmup: int, peaks: dict
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "traffic": None, "algorithmic_bytes_per_pass": nbytes,
                          "peak_kind": f"hbm_gbs ({peaks['source']})"},
-            "l2": "1 GB memset before each pass (outside the events)"}
+            "l2": "4 GB memset before each pass (outside the events)"}
 
 
 def host_inputs(case):

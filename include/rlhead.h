@@ -234,6 +234,9 @@ typedef struct rl_pg_metrics {
     int64_t ipo_curve[RL_PG_MAX_CURVE];   /* count of |e^lp_old - e^lp_samp| > curve_eps[k] */
 } rl_pg_metrics;
 
+/* Workspace bytes for T tokens: block partials (any device up to 256 SMs) and a list of
+ * max(4096, T / 16) tokens whose decisions are re-taken in fp64.  A smaller list is
+ * allowed down to the partials' size: its overflow only costs a slower exact pass. */
 size_t rl_policy_workspace_bytes(int64_t T);
 /* All arrays device [T] fp32 (mask uint8, 1 = valid response token).  Output arrays may
  * be NULL to skip; masked tokens get 0.  metrics: device, overwritten; NULL to skip. */
@@ -249,9 +252,10 @@ int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const
  * trainer or inference engine whose device memory is reserved up front by its own pool,
  * where an extra cudaMalloc would fail or compete with that pool, or plain C code with
  * no device allocator at hand.  This variant takes no workspace and allocates nothing:
- * its scratch (the per-block partial sums of the metric reduction) is a file-scope
- * device array of 229376 bytes, enough for 1024 blocks; a launch uses at most 2 blocks
- * per SM, so a device with more than 512 SMs is rejected with RL_ERR_WORKSPACE.
+ * its scratch (the per-block partial sums of the metric reduction, a few accumulators
+ * and the list of tokens whose decisions are re-taken in fp64) is a file-scope device
+ * array of 524288 bytes; a launch needs 1344 bytes per SM of it, so a device with more
+ * than 389 SMs is rejected with RL_ERR_WORKSPACE.
  *   - Every GPU that loads the library holds that array until the process exits.
  *   - The first call on a device looks the array's device address up (once per
  *     device); make that first call before any stream capture.

@@ -182,7 +182,7 @@ int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const
     if (T == 0 && !metrics) return RL_OK;
     if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
     return policy_impl(lp_theta, lp_old, lp_samp, adv, mask, T, params, loss_ppo, loss_dec, grad_ppo, grad_dec,
-                       metrics, ws, as_stream(stream));
+                       metrics, ws, ws_bytes, as_stream(stream));
 }
 
 int rl_gemm_bf16(const void* A, int a_mn_major, const void* B, int b_mn_major, int64_t M, int64_t N,

@@ -131,9 +131,9 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
 int policy_impl(const float* lt, const float* lo, const float* ls, const float* adv,
                 const uint8_t* mask, int64_t T, const rl_pg_params* p, float* loss_ppo,
                 float* loss_dec, float* grad_ppo, float* grad_dec, rl_pg_metrics* metrics,
-                void* ws, cudaStream_t stream);
+                void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t policy_ws_bytes(int64_t T);
-size_t policy_ws_need(int64_t T);   // bytes of block partials one launch for T tokens writes
+size_t policy_ws_need(int64_t T);   // least workspace a launch on this device needs (no band list)
 int gemm_util_impl(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
                    float* D, int32_t* status, cudaStream_t stream);
 

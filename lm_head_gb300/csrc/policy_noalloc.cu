@@ -1,6 +1,7 @@
 // rl_policy_loss_elementwise_noalloc: the elementwise PPO / TIS / mismatch path for callers
 // that cannot allocate device memory.  Its scratch (the per-block partial sums that the
-// final reduction reads) lives in a file-scope device array instead of a caller workspace.
+// final reduction reads, the fixed-point accumulators and the band-token list) lives in a
+// file-scope device array instead of a caller workspace.
 #include <mutex>
 
 #include "common.cuh"
@@ -8,8 +9,9 @@
 
 namespace rl {
 
-// 224 KiB: room for 1024 blocks of partial sums (the launch uses at most 4 blocks per SM).
-constexpr size_t kNoAllocScratchBytes = 229376;
+// 512 KiB: the block partials of a launch (6 blocks per SM, 1344 bytes per SM) and, in the
+// room left, the band-token list (about 80k entries on a 152-SM device).
+constexpr size_t kNoAllocScratchBytes = 524288;
 static __device__ __align__(256) double g_policy_scratch[kNoAllocScratchBytes / sizeof(double)];
 
 // Device address of g_policy_scratch for the current device, looked up once per device
@@ -65,12 +67,12 @@ extern "C" int rl_policy_loss_elementwise_noalloc(const float* lp_theta, const f
     const size_t need = policy_ws_need(T);
     if (need > kNoAllocScratchBytes) {
         set_last_error("rl_policy_loss_elementwise_noalloc: this launch needs more partial-sum scratch "
-                       "than the 229376-byte static array holds (more than 512 SMs)");
+                       "than the 524288-byte static array holds (more than 389 SMs)");
         return RL_ERR_WORKSPACE;
     }
     void* scratch = nullptr;
     int rc = scratch_address(&scratch);
     if (rc != RL_OK) return rc;
     return policy_impl(lp_theta, lp_old, lp_samp, adv, mask, T, params, loss_ppo, loss_dec, grad_ppo,
-                       grad_dec, metrics, scratch, static_cast<cudaStream_t>(stream));
+                       grad_dec, metrics, scratch, kNoAllocScratchBytes, static_cast<cudaStream_t>(stream));
 }

@@ -88,3 +88,50 @@ def test_exact_threshold_ties_are_bit_exact():
     ls = (lo - vals).astype(np.float32)
     for A in (1.0, -1.0, 0.0):
         _compare(lt, lo, ls, np.full(T, A, np.float32), np.ones(T, np.uint8), rh.PgParams())
+
+
+def _band_case(T, frac, seed):
+    """Random tokens, with a fraction frac placed on the clip boundary r = 1 - 0.2 (within
+    fp32 rounding), where every decision is re-taken in fp64."""
+    rng = np.random.default_rng(seed)
+    ls = np.log(1.0 / (1.0 + np.exp(-rng.normal(-1, 2.5, T)))).astype(np.float32)
+    lo = (ls + rng.normal(0, 0.3, T)).astype(np.float32)
+    lo = np.minimum(lo, -1e-6).astype(np.float32)
+    lt = (lo + rng.normal(0, 0.1, T)).astype(np.float32)
+    on = rng.random(T) < frac
+    lt[on] = (lo[on].astype(np.float64) + np.log(0.8) + rng.normal(0, 2e-7, int(on.sum()))).astype(np.float32)
+    A = rng.normal(0, 1, T).astype(np.float32)
+    m = (rng.random(T) < 0.9).astype(np.uint8)
+    return lt, lo, ls, A, m
+
+
+def test_many_band_tokens_fixup_path():
+    """About 10% of 20000 tokens sit on a clip threshold: all of them go through the fp64
+    fix-up list (below its 4096-entry floor) and every count stays exact."""
+    _compare(*_band_case(20000, 0.1, 5), rh.PgParams())
+
+
+def test_band_list_overflow_falls_back_to_exact_pass():
+    """Half of 200000 tokens on a clip threshold overflow the band list (T / 16 entries):
+    the gated exact pass replaces the fast one; results equal the oracle's."""
+    _compare(*_band_case(200_000, 0.5, 6), rh.PgParams())
+
+
+def test_curve_band_tokens_exact():
+    """About 10% of 20000 tokens with |p_old - p_samp| within fp32 rounding of one of the
+    curve's eps values: the curve counts re-taken exactly equal the oracle's."""
+    rng = np.random.default_rng(9)
+    T = 20000
+    ls = np.log(1.0 / (1.0 + np.exp(-rng.normal(-1, 2.5, T))))
+    eps = np.asarray(rh.PgParams().curve_eps, np.float64)
+    po = np.exp(ls) + eps[rng.integers(0, len(eps), T)] + rng.normal(0, 3e-8, T)
+    po = np.clip(po, 1e-6, 1 - 1e-6)
+    lo = np.log(po)
+    far = rng.random(T) > 0.1
+    lo[far] = ls[far] + rng.normal(0, 0.3, int(far.sum()))
+    lo = np.minimum(lo, -1e-6)
+    lt = lo + rng.normal(0, 0.1, T)
+    A = rng.normal(0, 1, T)
+    m = (rng.random(T) < 0.9).astype(np.uint8)
+    f = lambda x: np.asarray(x, np.float32)
+    _compare(f(lt), f(lo), f(ls), f(A), m, rh.PgParams())
