@@ -434,8 +434,8 @@ def run_ours(args):
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of each kernel, from the ncu
-# captures summarised under profiles/ (None until measured for the current kernel code).
-TRAFFIC = {}
+# captures summarised under profiles/ (one launch at the bench's 16384-token chunk).
+TRAFFIC = {"gemm_fwd_stats": 13573747712 + 9941863168}
 
 
 def ctypes_metrics_size(rh):
