@@ -169,11 +169,12 @@ def cpu_baseline(case_host: dict, n_tokens: int, threads: int):
                       f"forward + backward incl. dW; {dt:.1f} s"}
 
 
-def elementwise_side(rh, torch, dev, flush, steps: int, warmup: int, peaks: dict):
+def elementwise_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb: int = 4096):
     """The elementwise PPO / dual-clip / decoupled-TIS / mismatch path on its own workload
     (1.8M valid tokens in sequences of 64..4096, padded to 4096), against the HBM roofline.
-    Each pass follows a 4 GB memset (an L2 flush that keeps the GPU busy for about half a
-    millisecond, long enough for the host to queue the pass before the GPU reaches it) and
+    Each pass follows a memset of flush_mb MB (default 4 GB: an L2 flush that keeps the GPU
+    busy for about half a millisecond, long enough for the host to queue the pass before
+    the GPU reaches it; profiling runs pass a smaller one) and
     is timed by the library's own event pair around its launches (rl_profile), so host
     launch gaps stay out of a pass of a few tens of microseconds.
     Algorithmic bytes per slot: four fp32 inputs and the mask byte read, four fp32
@@ -187,7 +188,7 @@ def elementwise_side(rh, torch, dev, flush, steps: int, warmup: int, peaks: dict
     met = torch.zeros(rh.ctypes.sizeof(rh.RlPgMetrics), dtype=torch.uint8, device=dev)
     ws = torch.empty(rh.rl_policy_workspace_bytes(T), dtype=torch.uint8, device=dev)
     run = lambda: rh.rl_policy_loss_elementwise(*ins, pp, outputs=outs, ws=ws, metrics_dev=met)
-    big = torch.empty(4 << 30, dtype=torch.uint8, device=dev)
+    big = torch.empty(flush_mb << 20, dtype=torch.uint8, device=dev)
     for _ in range(warmup):
         run()
     torch.cuda.synchronize()
@@ -212,7 +213,7 @@ def elementwise_side(rh, torch, dev, flush, steps: int, warmup: int, peaks: dict
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "traffic": None, "algorithmic_bytes_per_pass": nbytes,
                          "peak_kind": f"hbm_gbs ({peaks['source']})"},
-            "l2": "4 GB memset before each pass (outside the events)"}
+            "l2": f"{flush_mb} MB memset before each pass (outside the events)"}
 
 
 def host_inputs(case):
@@ -249,6 +250,21 @@ def run_reference(args):
                              "sample": f"first {n_sample} tokens of the 64k-token batch per step"},
             "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_elementwise_only(args):
+    """The elementwise path alone (profiling runs): one JSON line with its side figure."""
+    import torch
+
+    import lm_head_gb300 as rh
+    from lm_head_gb300 import build
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    build.build()
+    rh.load()
+    ew = elementwise_side(rh, torch, dev, args.steps, args.warmup, load_peaks(), args.flush_mb)
+    print(json.dumps({"elementwise": ew, "gpu_launches_total": int(rh.rl_kernel_launch_count())}), flush=True)
     return 0
 
 
@@ -422,7 +438,7 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h},
             "clocks": clocks, "gpu_launches": int(launches), "input_gen_s": t_gen}
     if not args.no_elementwise:
-        line["elementwise"] = elementwise_side(rh, torch, dev, flush, max(args.steps, 10), args.warmup, peaks)
+        line["elementwise"] = elementwise_side(rh, torch, dev, max(args.steps, 10), args.warmup, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = host_inputs(case_first(case, args.cpu_tokens))
         line["cpu_baseline"] = cpu_baseline(host, args.cpu_tokens, os.cpu_count() or 1)
@@ -473,6 +489,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true", help="skip the two-call side figure")
     ap.add_argument("--no-elementwise", action="store_true", help="skip the elementwise-path side figure")
+    ap.add_argument("--elementwise-only", action="store_true",
+                    help="time only the elementwise path (profiling runs); prints its side figure")
+    ap.add_argument("--flush-mb", type=int, default=4096, help="memset before each elementwise pass, MB")
     ap.add_argument("--gemm-pair", type=int, choices=[0, 1], default=None,
                     help="tensor-core GEMMs on SM pairs (1) or single SMs (0); default: library default")
     args = ap.parse_args(argv)
@@ -480,6 +499,8 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.elementwise_only:
+        return run_elementwise_only(args)
     return run_ours(args)
 
 

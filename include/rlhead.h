@@ -235,7 +235,7 @@ typedef struct rl_pg_metrics {
 } rl_pg_metrics;
 
 /* Workspace bytes for T tokens: block partials (any device up to 256 SMs) and a list of
- * max(4096, T / 16) tokens whose decisions are re-taken in fp64.  A smaller list is
+ * max(4096, T / 16) tokens whose decisions are re-taken exactly.  A smaller list is
  * allowed down to the partials' size: its overflow only costs a slower exact pass. */
 size_t rl_policy_workspace_bytes(int64_t T);
 /* All arrays device [T] fp32 (mask uint8, 1 = valid response token).  Output arrays may
@@ -253,7 +253,7 @@ int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const
  * where an extra cudaMalloc would fail or compete with that pool, or plain C code with
  * no device allocator at hand.  This variant takes no workspace and allocates nothing:
  * its scratch (the per-block partial sums of the metric reduction, a few accumulators
- * and the list of tokens whose decisions are re-taken in fp64) is a file-scope device
+ * and the list of tokens whose decisions are re-taken exactly) is a file-scope device
  * array of 524288 bytes; a launch needs 1344 bytes per SM of it, so a device with more
  * than 389 SMs is rejected with RL_ERR_WORKSPACE.
  *   - Every GPU that loads the library holds that array until the process exits.
