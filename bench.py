@@ -216,6 +216,56 @@ def elementwise_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush
             "l2": f"{flush_mb} MB memset before each pass (outside the events)"}
 
 
+def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb: int = 4096):
+    """Rollout correction (IS / RS weights over sequences, veto, batch normalisation,
+    mismatch metrics) on the elementwise workload: the 879 padded rows are the sequences,
+    lp_old the trainer's log-probs, lp_samp the rollout engine's.  Knobs: sequence-level
+    TIS clipped to [0.1, 10] with batch normalisation, geometric RS in [0.9, 1.1], veto
+    1e-4.  Timed as elementwise_side.  Algorithmic bytes per slot: two fp32 inputs and the
+    mask read, the fp32 weight and the keep byte written (14 B), plus the weight read and
+    written again by the normalisation (8 B): the factor needs every token first."""
+    import numpy as np
+    import workloads
+    c = workloads.make_policy_case()
+    B = len(c.seq_lens)
+    off = torch.arange(B + 1, dtype=torch.int64, device=dev) * c.max_len
+    ins = [torch.from_numpy(x).to(dev) for x in (c.lp_old, c.lp_samp, c.mask)]
+    T = int(ins[0].numel())
+    rp = rh.RcParams(tis_mode="clip", tis_level="sequence", tis_lower_bound=0.1, tis_upper_bound=10.0,
+                     tis_batch_normalize=True, use_rs=True, rs_level="geometric", rs_lower_bound=0.9,
+                     rs_upper_bound=1.1, rs_veto_threshold=1e-4)
+    outs = (torch.empty(T, dtype=torch.float32, device=dev), torch.empty(T, dtype=torch.uint8, device=dev))
+    met = torch.zeros(rh.ctypes.sizeof(rh.RlRcMetrics), dtype=torch.uint8, device=dev)
+    ws = torch.empty(rh.rl_rollout_correction_workspace_bytes(B), dtype=torch.uint8, device=dev)
+    run = lambda: rh.rl_rollout_correction(*ins, off, rp, outputs=outs, ws=ws, metrics_dev=met)
+    big = torch.empty(flush_mb << 20, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    per = []
+    for _ in range(steps):
+        big.zero_()
+        rh.rl_profile_enable(True)
+        run()
+        prof = rh.rl_profile_read()
+        rh.rl_profile_enable(False)
+        per.append(sum(t for t, _ in prof.values()))
+    del big
+    ms = statistics.median(per)
+    nbytes = T * (4 + 4 + 1) + T * (4 + 1) + T * 8
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    n_valid = int(c.mask.sum())
+    return {"workload": f"c5 as {B} sequences (padded rows of {c.max_len}, T={T} slots, {n_valid} response "
+                        "tokens); sequence-level TIS clip [0.1, 10] + batch normalisation, geometric RS "
+                        "[0.9, 1.1], veto 1e-4, mismatch metrics",
+            "us_per_pass": ms * 1e3, "tokens_per_s": n_valid / (ms / 1e3), "passes": steps,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": None, "algorithmic_bytes_per_pass": nbytes,
+                         "peak_kind": f"hbm_gbs ({peaks['source']})"},
+            "l2": f"{flush_mb} MB memset before each pass (outside the events)"}
+
+
 def host_inputs(case):
     """The batch as numpy (fp64 copies of bf16 values) for the oracle."""
     return case.numpy()
@@ -254,7 +304,7 @@ def run_reference(args):
 
 
 def run_elementwise_only(args):
-    """The elementwise path alone (profiling runs): one JSON line with its side figure."""
+    """The elementwise paths alone (profiling runs): one JSON line with their side figures."""
     import torch
 
     import lm_head_gb300 as rh
@@ -264,7 +314,9 @@ def run_elementwise_only(args):
     build.build()
     rh.load()
     ew = elementwise_side(rh, torch, dev, args.steps, args.warmup, load_peaks(), args.flush_mb)
-    print(json.dumps({"elementwise": ew, "gpu_launches_total": int(rh.rl_kernel_launch_count())}), flush=True)
+    rc = rollout_side(rh, torch, dev, args.steps, args.warmup, load_peaks(), args.flush_mb)
+    print(json.dumps({"elementwise": ew, "rollout_correction": rc,
+                      "gpu_launches_total": int(rh.rl_kernel_launch_count())}), flush=True)
     return 0
 
 
@@ -439,6 +491,7 @@ def run_ours(args):
             "clocks": clocks, "gpu_launches": int(launches), "input_gen_s": t_gen}
     if not args.no_elementwise:
         line["elementwise"] = elementwise_side(rh, torch, dev, max(args.steps, 10), args.warmup, peaks)
+        line["rollout_correction"] = rollout_side(rh, torch, dev, max(args.steps, 10), args.warmup, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = host_inputs(case_first(case, args.cpu_tokens))
         line["cpu_baseline"] = cpu_baseline(host, args.cpu_tokens, os.cpu_count() or 1)

@@ -232,11 +232,13 @@ typedef struct rl_pg_metrics {
     double tis_sum;              /* sum of truncated TIS weights */
     int64_t n_valid, n_clip, n_clip_lower, icepop_low, icepop_high, n_tis_trunc;
     int64_t ipo_curve[RL_PG_MAX_CURVE];   /* count of |e^lp_old - e^lp_samp| > curve_eps[k] */
+    int64_t status;              /* RL_STATUS_* bits: RL_STATUS_TIMEOUT if a wait for a copy ran
+                                    out (the outputs and metrics are then incomplete) */
 } rl_pg_metrics;
 
-/* Workspace bytes for T tokens: block partials (any device up to 256 SMs) and a list of
- * max(4096, T / 16) tokens whose decisions are re-taken exactly.  A smaller list is
- * allowed down to the partials' size: its overflow only costs a slower exact pass. */
+/* Workspace bytes for T tokens: a 256-byte header (counters and the metric accumulators)
+ * and a list of max(4096, T / 16) tokens whose decisions are re-taken exactly.  A smaller
+ * list is allowed down to the header alone: its overflow only costs a slower exact pass. */
 size_t rl_policy_workspace_bytes(int64_t T);
 /* All arrays device [T] fp32 (mask uint8, 1 = valid response token).  Output arrays may
  * be NULL to skip; masked tokens get 0.  metrics: device, overwritten; NULL to skip. */
@@ -252,10 +254,8 @@ int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const
  * trainer or inference engine whose device memory is reserved up front by its own pool,
  * where an extra cudaMalloc would fail or compete with that pool, or plain C code with
  * no device allocator at hand.  This variant takes no workspace and allocates nothing:
- * its scratch (the per-block partial sums of the metric reduction, a few accumulators
- * and the list of tokens whose decisions are re-taken exactly) is a file-scope device
- * array of 524288 bytes; a launch needs 1344 bytes per SM of it, so a device with more
- * than 389 SMs is rejected with RL_ERR_WORKSPACE.
+ * its scratch (counters, the metric accumulators and the list of tokens whose decisions
+ * are re-taken exactly) is a file-scope device array of 524288 bytes.
  *   - Every GPU that loads the library holds that array until the process exits.
  *   - The first call on a device looks the array's device address up (once per
  *     device); make that first call before any stream capture.
@@ -270,6 +270,79 @@ int rl_policy_loss_elementwise_noalloc(const float* lp_theta, const float* lp_ol
                                        const rl_pg_params* params, float* loss_ppo,
                                        float* loss_dec, float* grad_ppo, float* grad_dec,
                                        rl_pg_metrics* metrics, void* stream);
+
+/* ---- rollout correction: IS / RS weights and mismatch metrics over sequences -------
+ * "Rollout Correction Methods": "Config keys", "Importance Sampling", "Rejection
+ * Sampling" (with the veto) and "Mismatch Metrics".  Per response token i of sequence s,
+ * d_i = lp_train_i - lp_rollout_i (lp_train: the trainer's log-probs, pi_old; lp_rollout:
+ * the inference engine's):
+ *   IS weight  w_i = exp(d_i) (token) | exp(sum_s d) (sequence) | exp(mean_s d) (geometric)
+ *   bounding   truncate: min(w, U); clip: clamp(w, L, U); mask: w if L <= w <= U else 0
+ *   RS         reject token i if exp(d_i) is outside [rL, rU] (token), or all of s if its
+ *              mean token weight (sequence) / geometric-mean weight (geometric) is
+ *   veto       reject all of s if some exp(d_i) < veto (whatever use_tis / use_rs say)
+ *   keep_i     = response token, not rejected; weights_i = w'_i * factor on kept tokens,
+ *              0 elsewhere; factor = 1, or (batch normalisation) n_kept / sum_kept w'.
+ * A weight equal to a bound is inside it.  Every decision (bounds, RS, veto) is the exact
+ * predicate on the fp32 inputs (the log-ratio sums carried in float-float); weight values
+ * are fp32 (a raw sequence weight past the fp32 range is inf, its bounded value exact).
+ * The metric struct holds sums and counts; the named metrics of "Mismatch Metrics" are
+ * their ratios (the Python binding forms them). */
+typedef enum { RL_TIS_TRUNCATE = 0, RL_TIS_CLIP = 1, RL_TIS_MASK = 2 } rl_tis_mode;
+typedef enum { RL_LEVEL_TOKEN = 0, RL_LEVEL_SEQUENCE = 1, RL_LEVEL_GEOMETRIC = 2 } rl_is_level;
+typedef struct rl_rc_params {
+    int32_t use_tis;                  /* 0: weights 1 on kept tokens (RS, veto, metrics only) */
+    int32_t tis_mode;                 /* rl_tis_mode */
+    int32_t tis_level;                /* rl_is_level */
+    int32_t tis_batch_normalize;      /* 1: kept weights scaled to mean 1 */
+    float tis_lower_bound, tis_upper_bound;   /* L, U; 0 <= L <= U */
+    int32_t use_rs;
+    int32_t rs_level;                 /* rl_is_level */
+    float rs_lower_bound, rs_upper_bound;     /* NaN: the tis bound */
+    float rs_veto_threshold;          /* <= 0 or NaN: no veto */
+} rl_rc_params;
+
+typedef struct rl_rc_metrics {
+    /* IS / RS (sums over response tokens unless noted) */
+    double w_before_sum;        /* raw IS weights at tis_level */
+    double w_after_sum;         /* bounded weights */
+    double kept_w_sum;          /* bounded weights of kept tokens */
+    double batch_norm_factor;   /* factor (1 when off) */
+    double final_sum, final_min, final_max;   /* final weights of kept tokens */
+    /* mismatch monitoring */
+    double mis_kl_sum;          /* sum (lp_rollout - lp_train) */
+    double k3_sum;              /* sum (e^d - d - 1) */
+    double abs_diff_sum;        /* sum |d| */
+    double chi2_token_sum;      /* sum e^(2d) */
+    double train_lppl_sum;      /* over sequences: -mean_s lp_train */
+    double rollout_lppl_sum;    /* over sequences: -mean_s lp_rollout */
+    double lppl_diff_sum;       /* over sequences: train - rollout log-ppl */
+    double lppl_abs_diff_sum;   /* over sequences: |train - rollout log-ppl| */
+    double ppl_ratio_sum;       /* over sequences: exp(train - rollout log-ppl) */
+    double chi2_seq_sum;        /* over sequences: exp(2 sum_s d) */
+    int64_t n_valid;            /* response tokens */
+    int64_t n_seq;              /* sequences with at least one response token */
+    int64_t n_kept;             /* kept tokens */
+    int64_t n_tis_low, n_tis_high;     /* response tokens with raw weight < L / > U */
+    int64_t n_rs_low, n_rs_high;       /* response tokens rejected by RS below / above */
+    int64_t n_cat_tokens;       /* response tokens with exp(d) < veto */
+    int64_t n_cat_seqs;         /* sequences holding one */
+    int64_t status;             /* RL_STATUS_OFFSETS if seq_offsets was not a partition of
+                                   [0, T) (bad sequences then count as empty) */
+} rl_rc_metrics;
+
+/* Workspace bytes for B sequences (per-sequence partial sums and a small header). */
+size_t rl_rollout_correction_workspace_bytes(int64_t B);
+/* lp_train, lp_rollout: device [T] fp32; mask: device [T] uint8 (1 = response token);
+ * seq_offsets: device [B + 1] int64, sequence s = tokens [seq_offsets[s], seq_offsets[s+1])
+ * (padded rows: s * row_length; packed: cumulative lengths).  Outputs, device: weights
+ * [T] fp32 and keep [T] uint8 (either may be NULL), metrics (overwritten, may be NULL).
+ * Errors: RL_ERR_ARG (NULL input, B < 0, T < 0, bad enum, L > U or negative bound),
+ * RL_ERR_WORKSPACE; bad offsets are reported in metrics->status, not trapped. */
+int rl_rollout_correction(const float* lp_train, const float* lp_rollout, const uint8_t* mask,
+                          const int64_t* seq_offsets, int64_t B, int64_t T,
+                          const rl_rc_params* params, float* weights, uint8_t* keep,
+                          rl_rc_metrics* metrics, void* ws, size_t ws_bytes, void* stream);
 
 /* ---- utilities ------------------------------------------------------------------ */
 /* The head contraction alone: D[M, N] fp32 = A[M, K] * B[N, K]^T, A and B bf16 row-major
@@ -289,12 +362,12 @@ int rl_gemm_bf16(const void* A, int a_mn_major, const void* B, int b_mn_major, i
  * rl_profile_enable(1) also clears the counters.  rl_profile_read waits for the recorded
  * events, then fills ms[k] (summed device milliseconds) and launches[k] for every kind
  * k < RL_PROF_KINDS; either pointer may be NULL.  Host arrays. */
-#define RL_PROF_KINDS 17
+#define RL_PROF_KINDS 18
 enum { RL_PROF_VALIDATE = 0, RL_PROF_GEMM_FWD = 1, RL_PROF_TOKEN_LOSS = 2, RL_PROF_METRICS = 3,
        RL_PROF_TRANSPOSE = 4, RL_PROF_GEMM_GRAD = 5, RL_PROF_GEMM_DX = 6, RL_PROF_GEMM_DW = 7,
        RL_PROF_SPARSE_DX = 8, RL_PROF_SPARSE_DW = 9, RL_PROF_POLICY = 10, RL_PROF_GEMM_UTIL = 11,
        RL_PROF_MEMSET = 12, RL_PROF_OTHER = 13, RL_PROF_RESID = 14, RL_PROF_GRAD_E = 15,
-       RL_PROF_REF_LOGIT = 16 };
+       RL_PROF_REF_LOGIT = 16, RL_PROF_ROLLOUT = 17 };
 int rl_profile_enable(int on);
 int rl_profile_read(double* ms, int64_t* launches);
 const char* rl_profile_kind_name(int kind);

@@ -82,7 +82,25 @@ class RlPgMetrics(ctypes.Structure):
                                                "tis_sum")] + \
                [(k, ctypes.c_int64) for k in ("n_valid", "n_clip", "n_clip_lower", "icepop_low",
                                               "icepop_high", "n_tis_trunc")] + \
-               [("ipo_curve", ctypes.c_int64 * RL_PG_MAX_CURVE)]
+               [("ipo_curve", ctypes.c_int64 * RL_PG_MAX_CURVE), ("status", ctypes.c_int64)]
+
+
+class RlRcParams(ctypes.Structure):
+    _fields_ = [("use_tis", ctypes.c_int32), ("tis_mode", ctypes.c_int32), ("tis_level", ctypes.c_int32),
+                ("tis_batch_normalize", ctypes.c_int32), ("tis_lower_bound", ctypes.c_float),
+                ("tis_upper_bound", ctypes.c_float), ("use_rs", ctypes.c_int32), ("rs_level", ctypes.c_int32),
+                ("rs_lower_bound", ctypes.c_float), ("rs_upper_bound", ctypes.c_float),
+                ("rs_veto_threshold", ctypes.c_float)]
+
+
+class RlRcMetrics(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_double) for k in (
+        "w_before_sum", "w_after_sum", "kept_w_sum", "batch_norm_factor", "final_sum", "final_min", "final_max",
+        "mis_kl_sum", "k3_sum", "abs_diff_sum", "chi2_token_sum", "train_lppl_sum", "rollout_lppl_sum",
+        "lppl_diff_sum", "lppl_abs_diff_sum", "ppl_ratio_sum", "chi2_seq_sum")] + \
+               [(k, ctypes.c_int64) for k in (
+                   "n_valid", "n_seq", "n_kept", "n_tis_low", "n_tis_high", "n_rs_low", "n_rs_high",
+                   "n_cat_tokens", "n_cat_seqs", "status")]
 
 
 _lib = None
@@ -101,6 +119,9 @@ _SIGS = {
                                                                     ctypes.c_size_t, ctypes.c_void_p,
                                                                     ctypes.c_void_p]),
     "rl_policy_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64]),
+    "rl_rollout_correction_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64]),
+    "rl_rollout_correction": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 2 + [ctypes.c_void_p] * 5
+                              + [ctypes.c_size_t, ctypes.c_void_p]),
     "rl_policy_loss_elementwise": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int64] + [ctypes.c_void_p] * 7
                                    + [ctypes.c_size_t, ctypes.c_void_p]),
     "rl_policy_loss_elementwise_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int64]
@@ -461,6 +482,97 @@ def rl_policy_loss_elementwise_noalloc(lp_theta, lp_old, lp_samp, adv, mask, par
     return (*outputs, metrics_dev)
 
 
+RL_TIS_TRUNCATE, RL_TIS_CLIP, RL_TIS_MASK = 0, 1, 2
+RL_LEVEL_TOKEN, RL_LEVEL_SEQUENCE, RL_LEVEL_GEOMETRIC = 0, 1, 2
+_TIS_MODES = {"truncate": RL_TIS_TRUNCATE, "clip": RL_TIS_CLIP, "mask": RL_TIS_MASK}
+_LEVELS = {"token": RL_LEVEL_TOKEN, "sequence": RL_LEVEL_SEQUENCE, "geometric": RL_LEVEL_GEOMETRIC}
+
+
+@dataclasses.dataclass
+class RcParams:
+    """Rollout-correction knobs ("Rollout Correction Methods", "Config keys")."""
+    use_tis: bool = True
+    tis_mode: str = "truncate"
+    tis_lower_bound: float = 0.5
+    tis_upper_bound: float = 2.0
+    tis_level: str = "token"
+    tis_batch_normalize: bool = False
+    use_rs: bool = False
+    rs_lower_bound: Optional[float] = None      # None: the tis bound
+    rs_upper_bound: Optional[float] = None
+    rs_level: str = "token"
+    rs_veto_threshold: Optional[float] = None   # None: no veto
+
+    def c(self) -> RlRcParams:
+        nan = float("nan")
+        return RlRcParams(int(self.use_tis), _TIS_MODES[self.tis_mode], _LEVELS[self.tis_level],
+                          int(self.tis_batch_normalize), self.tis_lower_bound, self.tis_upper_bound,
+                          int(self.use_rs), _LEVELS[self.rs_level],
+                          nan if self.rs_lower_bound is None else self.rs_lower_bound,
+                          nan if self.rs_upper_bound is None else self.rs_upper_bound,
+                          nan if self.rs_veto_threshold is None else self.rs_veto_threshold)
+
+
+def rl_rollout_correction_workspace_bytes(B: int) -> int:
+    return int(load().rl_rollout_correction_workspace_bytes(B))
+
+
+def rl_rollout_correction(lp_train, lp_rollout, mask, seq_offsets, params: RcParams, *, outputs=None,
+                          ws: Optional[torch.Tensor] = None, metrics_dev: Optional[torch.Tensor] = None,
+                          stream=None):
+    """Returns (weights [T] fp32, keep [T] uint8, metrics_dev); metrics via rc_metrics()."""
+    lib = load()
+    _require_cuda(lp_train, lp_rollout, mask, seq_offsets)
+    T = int(lp_train.numel())
+    B = int(seq_offsets.numel()) - 1
+    dev = lp_train.device
+    if outputs is None:
+        outputs = (torch.empty(T, dtype=torch.float32, device=dev), torch.empty(T, dtype=torch.uint8, device=dev))
+    if metrics_dev is None:
+        metrics_dev = torch.zeros(ctypes.sizeof(RlRcMetrics), dtype=torch.uint8, device=dev)
+    if ws is None:
+        ws = _u8(rl_rollout_correction_workspace_bytes(B), dev)
+    p = params.c()
+    _check(lib.rl_rollout_correction(_ptr(lp_train), _ptr(lp_rollout), _ptr(mask), _ptr(seq_offsets), B, T,
+                                     ctypes.byref(p), _ptr(outputs[0]), _ptr(outputs[1]), _ptr(metrics_dev),
+                                     _ptr(ws), ws.numel(), _stream(stream)))
+    return (*outputs, metrics_dev)
+
+
+def rc_metrics(metrics_dev: torch.Tensor) -> dict:
+    m = RlRcMetrics.from_buffer_copy(bytes(metrics_dev.cpu().numpy().tobytes()))
+    return {f: getattr(m, f) for f, _ in RlRcMetrics._fields_}
+
+
+def rc_metrics_named(m: dict, params: RcParams) -> dict:
+    """The page's metric names from the sums and counts ("Mismatch Metrics" tables):
+    token means over response tokens, sequence means over sequences with response tokens."""
+    import math
+    nv, ns, nk = max(m["n_valid"], 1), max(m["n_seq"], 1), max(m["n_kept"], 1)
+    tr, ro = m["train_lppl_sum"] / ns, m["rollout_lppl_sum"] / ns
+    out = {"training_log_ppl": tr, "training_ppl": math.exp(tr), "rollout_log_ppl": ro, "rollout_ppl": math.exp(ro),
+           "kl": m["mis_kl_sum"] / nv, "k3_kl": m["k3_sum"] / nv, "log_ppl_diff": m["lppl_diff_sum"] / ns,
+           "log_ppl_abs_diff": m["lppl_abs_diff_sum"] / ns, "ppl_ratio": m["ppl_ratio_sum"] / ns,
+           "chi2_token": m["chi2_token_sum"] / nv - 1.0, "chi2_seq": m["chi2_seq_sum"] / ns - 1.0,
+           "train_rollout_logprob_abs_diff": m["abs_diff_sum"] / nv,
+           "tis_weight_before_bound": m["w_before_sum"] / nv, "tis_weight_after_bound": m["w_after_sum"] / nv,
+           "is_ratio_mean_after_tis_rs": m["kept_w_sum"] / nk, "batch_norm_factor": m["batch_norm_factor"],
+           "is_ratio_mean_final": m["final_sum"] / nk, "is_ratio_min_final": m["final_min"],
+           "is_ratio_max_final": m["final_max"],
+           "rs_catastrophic_token_fraction": m["n_cat_tokens"] / nv,
+           "rs_catastrophic_seq_fraction": m["n_cat_seqs"] / ns}
+    lo, hi = m["n_tis_low"] / nv, m["n_tis_high"] / nv
+    if params.tis_mode == "truncate":
+        out["tis_truncate_fraction"] = hi
+    elif params.tis_mode == "clip":
+        out["tis_clip_fraction_low"], out["tis_clip_fraction_high"] = lo, hi
+    else:
+        out["tis_mask_fraction_low"], out["tis_mask_fraction_high"] = lo, hi
+    if params.use_rs:
+        out["rs_mask_fraction_low"], out["rs_mask_fraction_high"] = m["n_rs_low"] / nv, m["n_rs_high"] / nv
+    return out
+
+
 def pg_metrics(metrics_dev: torch.Tensor, n_curve: int = 10) -> dict:
     m = RlPgMetrics.from_buffer_copy(bytes(metrics_dev.cpu().numpy().tobytes()))
     d = {f: getattr(m, f) for f, _ in RlPgMetrics._fields_ if f != "ipo_curve"}
@@ -507,7 +619,7 @@ def rl_kernel_launch_count() -> int:
     return int(load().rl_kernel_launch_count())
 
 
-RL_PROF_KINDS = 17
+RL_PROF_KINDS = 18
 
 
 def rl_profile_enable(on: bool = True) -> None:

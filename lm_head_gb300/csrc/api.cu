@@ -185,6 +185,34 @@ int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const
                        metrics, ws, ws_bytes, as_stream(stream));
 }
 
+size_t rl_rollout_correction_workspace_bytes(int64_t B) { return B < 0 ? 0 : rollout_ws_bytes(B); }
+
+int rl_rollout_correction(const float* lp_train, const float* lp_rollout, const uint8_t* mask,
+                          const int64_t* seq_offsets, int64_t B, int64_t T, const rl_rc_params* params,
+                          float* weights, uint8_t* keep, rl_rc_metrics* metrics, void* ws, size_t ws_bytes,
+                          void* stream) {
+    if (T < 0 || B < 0) return fail(RL_ERR_ARG, "T < 0 or B < 0");
+    if (B >= (int64_t(1) << 31)) return fail(RL_ERR_UNSUPPORTED, "B >= 2^31");
+    if (!params) return fail(RL_ERR_ARG, "params NULL");
+    const rl_rc_params& p = *params;
+    auto level_ok = [](int l) { return l == RL_LEVEL_TOKEN || l == RL_LEVEL_SEQUENCE || l == RL_LEVEL_GEOMETRIC; };
+    if (p.tis_mode != RL_TIS_TRUNCATE && p.tis_mode != RL_TIS_CLIP && p.tis_mode != RL_TIS_MASK)
+        return fail(RL_ERR_ARG, "bad tis_mode");
+    if (!level_ok(p.tis_level) || !level_ok(p.rs_level)) return fail(RL_ERR_ARG, "bad level");
+    if (!(p.tis_lower_bound >= 0.f) || !(p.tis_upper_bound >= p.tis_lower_bound))
+        return fail(RL_ERR_ARG, "tis bounds: need 0 <= lower <= upper");
+    const float rl = std::isnan(p.rs_lower_bound) ? p.tis_lower_bound : p.rs_lower_bound;
+    const float ru = std::isnan(p.rs_upper_bound) ? p.tis_upper_bound : p.rs_upper_bound;
+    if (!(rl >= 0.f) || !(ru >= rl)) return fail(RL_ERR_ARG, "rs bounds: need 0 <= lower <= upper");
+    if (B > 0 && !seq_offsets) return fail(RL_ERR_ARG, "seq_offsets NULL");
+    if (T > 0 && (!lp_train || !lp_rollout || !mask)) return fail(RL_ERR_ARG, "input NULL");
+    if (!ws || ws_bytes < rl_rollout_correction_workspace_bytes(B))
+        return fail(RL_ERR_WORKSPACE, "rollout-correction workspace too small");
+    if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
+    return rollout_impl(lp_train, lp_rollout, mask, seq_offsets, B, T, params, weights, keep, metrics, ws,
+                        ws_bytes, as_stream(stream));
+}
+
 int rl_gemm_bf16(const void* A, int a_mn_major, const void* B, int b_mn_major, int64_t M, int64_t N,
                  int64_t K, float* D, int32_t* dev_status, void* stream) {
     if (!A || !B || !D || !dev_status) return fail(RL_ERR_ARG, "NULL pointer");

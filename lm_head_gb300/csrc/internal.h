@@ -133,7 +133,10 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
                 float* loss_dec, float* grad_ppo, float* grad_dec, rl_pg_metrics* metrics,
                 void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t policy_ws_bytes(int64_t T);
-size_t policy_ws_need(int64_t T);   // least workspace a launch on this device needs (no band list)
+int rollout_impl(const float* lt, const float* lr, const uint8_t* mask, const int64_t* off, int64_t B, int64_t T,
+                 const rl_rc_params* p, float* w, uint8_t* keep, rl_rc_metrics* metrics, void* ws,
+                 size_t ws_bytes, cudaStream_t stream);
+size_t rollout_ws_bytes(int64_t B);
 int gemm_util_impl(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
                    float* D, int32_t* status, cudaStream_t stream);
 

@@ -15,28 +15,31 @@
 //     parts and a degree-5 Taylor polynomial), built on the error-free TwoSum (Knuth) and
 //     FMA TwoProduct.
 //
-//  1. policy_fast_kernel   one streaming pass, two tokens per thread and round with the
-//                          next round's loads in flight (registers), branch-free fp32
-//                          math, thresholds and their bands prepared on the host, the IPO
-//                          curve as a per-thread histogram over the sorted eps (binary
-//                          search; only the two neighbouring eps are band-checked).  A token
-//                          inside a band goes to its block's list in shared memory (or, if
-//                          that is full, to a global spill list); after its loop the block
-//                          takes its listed tokens with exact decisions (outputs rewritten,
-//                          contributions added in 2^-16 fixed point, exact and so
-//                          independent of the list order) and writes its partial.
+//  1. policy_fast_kernel   one streaming pass: stages of 512 slots dealt round-robin to
+//                          the blocks, each block's through a ring of shared-memory stages
+//                          that a producer warp fills with bulk copies (cp.async.bulk,
+//                          mbarriers); branch-free fp32 math, thresholds and their bands
+//                          prepared on the host, the IPO curve as a per-thread histogram
+//                          over the sorted eps (binary search; only the two neighbouring
+//                          eps are band-checked).  A token inside a band goes to its
+//                          block's list in shared memory (or, if that is full, to a global
+//                          spill list); an exact warp takes the block's listed tokens
+//                          while the stream goes on (outputs rewritten, contributions in
+//                          2^-24 fixed point, exact and so independent of the list order).
 //  2. policy_slow_kernel   the whole pass with exact decisions in the bands, for inputs the
-//                          fast pass does not take (odd length, unaligned, T >= 2^31).
-//  3. policy_final_kernel  one block of 1024 threads: the spill list's tokens, then the
-//                          block partials in fixed order into the metrics.  If the spill
-//                          list overflowed, it redoes the whole batch with exact decisions
-//                          instead (slow, correct).
+//                          fast pass does not take (unaligned, T >= 2^31).
+//  Each block adds its partial (fp32 sums in a fixed order within the block, then in 2^-24
+//  fixed point; counts) to the batch accumulators with integer atomics, whose total does
+//  not depend on the order of arrival; the last block to arrive (an arrival counter)
+//  takes the spill list's tokens and writes the metrics.  If the spill list overflowed,
+//  that block redoes the whole batch with exact decisions instead (slow, correct).
 //
 // Results are bitwise reproducible for a given device and T.
 #include <cmath>
 #include <climits>
 
 #include "common.cuh"
+#include "ff.cuh"
 #include "internal.h"
 
 namespace rl {
@@ -46,96 +49,13 @@ constexpr int kPgSums = 6;
 constexpr int kPgCounts = 6 + RL_PG_MAX_CURVE;
 constexpr int kPgFields = kPgSums + kPgCounts;
 constexpr int kPgBins = RL_PG_MAX_CURVE + 1;
-constexpr int kPgFastPerSm = 4;   // resident blocks per SM of the fast pass
+constexpr int kPgFastPerSm = 2;   // resident blocks per SM of the fast pass
+constexpr int kPgStageSlots = 2 * kPgThreads;   // token slots per stage of the fast pass
+constexpr int kPgDepth = 6;       // stages in its ring
 constexpr int kPgSlowPerSm = 2;
-constexpr float kPgFix = 65536.f;   // 2^16: fixed-point scale of the band-token sums
+constexpr float kPgFix = 16777216.f;   // 2^24: fixed-point scale of the metric sums
 constexpr int kPgBlockBand = 1024;  // band tokens a fast-pass block keeps in shared memory
 constexpr int kPgBandRows = 64;     // band tokens taken per step (one shared-memory row each)
-constexpr int kPgFinalThreads = 1024;
-
-// ----------------------------------------------------------------------------------
-// Float-float arithmetic (value = hi + lo, |lo| <= ulp(hi) / 2)
-// ----------------------------------------------------------------------------------
-struct FF {
-    float hi, lo;
-};
-RL_DEVINL FF two_sum(float a, float b) {   // exact: a + b = s + e
-    const float s = __fadd_rn(a, b);
-    const float bb = __fsub_rn(s, a);
-    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
-    return {s, e};
-}
-RL_DEVINL FF fast_two_sum(float a, float b) {   // exact when |a| >= |b|
-    const float s = __fadd_rn(a, b);
-    return {s, __fsub_rn(b, __fsub_rn(s, a))};
-}
-RL_DEVINL FF two_prod(float a, float b) {   // exact: a * b = p + e
-    const float p = __fmul_rn(a, b);
-    return {p, fmaf(a, b, -p)};
-}
-RL_DEVINL FF ff_add(FF a, FF b) {
-    const FF s = two_sum(a.hi, b.hi);
-    return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
-}
-RL_DEVINL FF ff_mul(FF a, FF b) {
-    const FF p = two_prod(a.hi, b.hi);
-    return fast_two_sum(p.hi, fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, p.lo)));
-}
-RL_DEVINL bool ff_gt(FF a, FF b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
-RL_DEVINL bool ff_lt(FF a, FF b) { return ff_gt(b, a); }
-
-// 2^(j/64), j = 0..63, as float-float pairs
-__device__ __constant__ float kExp2Hi[64] = {
-    1.000000000e+00f, 1.010889292e+00f, 1.021897197e+00f, 1.033024907e+00f, 1.044273734e+00f, 1.055645227e+00f,
-    1.067140460e+00f, 1.078760743e+00f, 1.090507746e+00f, 1.102382541e+00f, 1.114386797e+00f, 1.126521587e+00f,
-    1.138788581e+00f, 1.151189208e+00f, 1.163724899e+00f, 1.176396966e+00f, 1.189207077e+00f, 1.202156782e+00f,
-    1.215247393e+00f, 1.228480577e+00f, 1.241857767e+00f, 1.255380750e+00f, 1.269050956e+00f, 1.282870054e+00f,
-    1.296839595e+00f, 1.310961246e+00f, 1.325236678e+00f, 1.339667559e+00f, 1.354255557e+00f, 1.369002461e+00f,
-    1.383909941e+00f, 1.398979664e+00f, 1.414213538e+00f, 1.429613352e+00f, 1.445180774e+00f, 1.460917830e+00f,
-    1.476826191e+00f, 1.492907763e+00f, 1.509164453e+00f, 1.525598168e+00f, 1.542210817e+00f, 1.559004426e+00f,
-    1.575980902e+00f, 1.593142152e+00f, 1.610490322e+00f, 1.628027439e+00f, 1.645755529e+00f, 1.663676620e+00f,
-    1.681792855e+00f, 1.700106382e+00f, 1.718619347e+00f, 1.737333894e+00f, 1.756252170e+00f, 1.775376439e+00f,
-    1.794709086e+00f, 1.814252138e+00f, 1.834008098e+00f, 1.853979111e+00f, 1.874167681e+00f, 1.894575953e+00f,
-    1.915206552e+00f, 1.936061740e+00f, 1.957144141e+00f, 1.978456020e+00f};
-__device__ __constant__ float kExp2Lo[64] = {
-    0.000000000e+00f, -5.711605411e-09f, -4.811559862e-08f, -2.809089317e-08f, 4.833470157e-08f,
-    -4.907169426e-08f, -5.933751979e-08f, 5.461594554e-08f, -1.307753994e-08f, 4.260501996e-08f,
-    -5.435540018e-08f, 3.123641434e-08f, 5.386222313e-08f, 2.192228266e-08f, -4.051441493e-08f,
-    2.566975077e-08f, 3.797635273e-08f, -5.069756526e-08f, -3.267394888e-08f, -4.136200360e-08f,
-    4.496838102e-08f, 7.322237483e-09f, 1.419333318e-09f, -3.816621685e-08f, -4.018999533e-08f,
-    -3.496571566e-08f, -3.496373324e-08f, -3.461673970e-08f, -1.012334927e-08f, -3.845881835e-08f,
-    -5.875577358e-08f, 8.689434061e-09f, 2.420323497e-08f, -1.342992917e-08f, 3.324199938e-08f,
-    -3.628657552e-08f, -4.500898854e-08f, -3.423620143e-08f, -2.495937323e-08f, -1.762856883e-08f,
-    8.070904833e-09f, -2.576466507e-08f, -5.661025426e-08f, -4.903136785e-10f, 9.836217174e-09f,
-    -1.726008314e-08f, -5.124972091e-08f, -3.920298752e-08f, -2.475532668e-08f, -2.865147231e-08f,
-    -4.849617596e-08f, -5.850223417e-08f, -9.235770371e-09f, 5.343197884e-08f, -1.141504491e-08f,
-    3.736258236e-08f, -1.123927795e-08f, 1.436561181e-08f, -4.663005626e-08f, 2.810338451e-08f,
-    9.845328108e-09f, 5.357072297e-08f, -1.702180441e-08f, 6.032726318e-09f};
-
-// e^x (x an fp32 value) as a float-float pair, about 2^-46 relative (Tang's table-driven
-// method): x = (64 k + j) ln2/64 + s with ln2/64 = C1 + C2 + C3 (C1, C2 with 10 significant
-// bits, so n C1 and n C2 are exact for |n| < 2^14), |s| <= ln2/128; e^s by a degree-5
-// Taylor polynomial; e^x = 2^k 2^(j/64) e^s.
-RL_DEVINL FF exp_ff(float x) {
-    if (x < -103.f) return {0.f, 0.f};
-    if (x > 88.f) return {INFINITY, 0.f};
-    const float n = rintf(x * 92.33248138427734f);   // 64 / ln 2
-    const float C1 = 0.0108184814453125f, C2 = 1.1935830116271973e-05f, C3 = 7.420820402614936e-09f;
-    FF r = two_sum(x, -(n * C1));
-    r = ff_add(r, {-(n * C2), 0.f});
-    r = ff_add(r, two_prod(-n, C3));
-    // 1 + s + s^2/2 + s^3/6 + s^4/24 + s^5/120 by Horner (1/6, 1/24, 1/120 as float-float)
-    FF p = {8.333333768e-03f, -4.346172033e-10f};
-    p = ff_add(ff_mul(p, r), {4.166666791e-02f, -1.241763470e-09f});
-    p = ff_add(ff_mul(p, r), {1.666666716e-01f, -4.967053879e-09f});
-    p = ff_add(ff_mul(p, r), {0.5f, 0.f});
-    p = ff_add(ff_mul(p, r), {1.f, 0.f});
-    p = ff_add(ff_mul(p, r), {1.f, 0.f});
-    const int ni = static_cast<int>(n);
-    const int k = ni >> 6, j = ni - (k << 6);
-    p = ff_mul(p, {kExp2Hi[j], kExp2Lo[j]});
-    return {ldexpf(p.hi, k), ldexpf(p.lo, k)};
-}
 
 // ----------------------------------------------------------------------------------
 // Parameters
@@ -166,11 +86,11 @@ struct PgArgs {
     float* loss_dec;
     float* grad_ppo;
     float* grad_dec;
-    float* psum;                  // block partials, field-major: psum[k * nb + block]
-    int* pcnt;                    // pcnt[k * nb + block]
-    int nb;                       // blocks of the pass that wrote them
-    int64_t rot_step;             // per-round rotation of the thread -> slot map (warp-aligned)
+    long long* acc;               // [kPgFields] the batch's sums (2^-24 fixed point) and counts
+    int nb;                       // blocks of the pass
     int* count;                   // global spill list: length (may exceed cap: overflow)
+    int* done;                    // blocks that have written their partial
+    int32_t* status;              // RL_STATUS_* bits of this call
     int* list;
     int cap;
     rl_pg_metrics* metrics;       // or nullptr
@@ -291,6 +211,13 @@ RL_DEVINL void pg_token(float lt, float lo, float ls, float A, bool valid, const
     for (int k = 0; k < RL_PG_MAX_CURVE; ++k) acc.cnt[6 + k] += (curve >> k) & 1u;
 }
 
+// pg_token for one listed band token (always valid), outputs into out[4].  Inline like
+// every helper here: a kernel parameter passed by reference to an out-of-line function
+// would be copied to local memory, and each access through it would be a local load.
+RL_DEVINL void pg_token_listed(float lt, float lo, float ls, float A, const PgPrep& q, float* out, PgAcc& acc) {
+    pg_token(lt, lo, ls, A, true, q, out[0], out[1], out[2], out[3], acc);
+}
+
 // Every token of [tid, T) with stride nthreads on the exact path (scalar loads, any
 // alignment and length); outputs written.
 RL_DEVINL void pg_exact_pass(const PgArgs& a, int64_t tid, int64_t nthreads, PgAcc& acc) {
@@ -357,11 +284,11 @@ RL_DEVINL void pg_write_metric(int k, double s, rl_pg_metrics* out) {
 }
 
 // Exact-path tokens list[0, n), kPgBandRows at a time (thread i < kPgBandRows takes one
-// and fills its shared-memory row: sums in 2^-16 fixed point, counts), then thread
+// and fills its shared-memory row: sums in 2^-24 fixed point, counts), then thread
 // k < kPgFields adds column k into fix[k] (shared).  Integer sums are exact, so the order
 // of the list does not matter.  Outputs of the listed tokens are rewritten.  Called by
 // every thread of the block.
-__device__ __noinline__ void pg_band_tokens(const PgArgs& a, const int* list, int n, long long* fix) {
+RL_DEVINL void pg_band_tokens(const PgArgs& a, const int* list, int n, long long* fix) {
     __shared__ long long rows[kPgBandRows][kPgFields];
     for (int c0 = 0; c0 < n; c0 += kPgBandRows) {
         if (threadIdx.x < kPgBandRows) {
@@ -371,12 +298,12 @@ __device__ __noinline__ void pg_band_tokens(const PgArgs& a, const int* list, in
                 const int64_t t = list[e];
                 PgAcc one;
                 pg_zero(one);
-                float lp, ld, gp, gd;
-                pg_token(a.lt[t], a.lo[t], a.ls[t], a.adv[t], true, a.q, lp, ld, gp, gd, one);
-                if (a.loss_ppo) a.loss_ppo[t] = lp;
-                if (a.loss_dec) a.loss_dec[t] = ld;
-                if (a.grad_ppo) a.grad_ppo[t] = gp;
-                if (a.grad_dec) a.grad_dec[t] = gd;
+                float o[4];
+                pg_token_listed(a.lt[t], a.lo[t], a.ls[t], a.adv[t], a.q, o, one);
+                if (a.loss_ppo) a.loss_ppo[t] = o[0];
+                if (a.loss_dec) a.loss_dec[t] = o[1];
+                if (a.grad_ppo) a.grad_ppo[t] = o[2];
+                if (a.grad_dec) a.grad_dec[t] = o[3];
                 for (int f = 0; f < kPgSums; ++f) row[f] = __float2ll_rn(one.sum[f] * kPgFix);
                 for (int f = 0; f < kPgCounts; ++f) row[kPgSums + f] = one.cnt[f];
             } else {
@@ -394,6 +321,62 @@ __device__ __noinline__ void pg_band_tokens(const PgArgs& a, const int* list, in
 }
 
 // ----------------------------------------------------------------------------------
+// Batch totals
+// ----------------------------------------------------------------------------------
+// A block's partial goes into the batch accumulators with integer atomics (sums in 2^-24
+// fixed point, counts as they are): integer addition does not depend on the order the
+// blocks arrive in, so the totals are reproducible.  v: this field's value (thread k < kPgFields).
+RL_DEVINL void pg_add_partial(const PgArgs& a, int k, float sum, long long count) {
+    const long long x = k < kPgSums ? __float2ll_rn(sum * kPgFix) + count : count;
+    if (x != 0) atomicAdd(reinterpret_cast<unsigned long long*>(a.acc + k), static_cast<unsigned long long>(x));
+}
+
+// The last block of the pass to finish: the spill list's tokens, then the accumulators
+// into the metrics.  If the spill list overflowed, the whole batch again with exact
+// decisions instead (slow, correct).  Called by every thread of the last block.
+RL_DEVINL void pg_final(const PgArgs& a) {
+    const int cnt = __ldcg(a.count);
+    if (cnt > a.cap) {
+        PgAcc acc;
+        pg_zero(acc);
+        pg_exact_pass(a, threadIdx.x, blockDim.x, acc);
+        __shared__ float sums[kPgSums];
+        __shared__ int cnts[kPgCounts];
+        pg_block_reduce(acc, sums, cnts);
+        if (a.metrics && threadIdx.x < kPgFields) {
+            const int k = threadIdx.x;
+            pg_write_metric(k, k < kPgSums ? static_cast<double>(sums[k]) : static_cast<double>(cnts[k - kPgSums]),
+                            a.metrics);
+        }
+        if (a.metrics && threadIdx.x == 0) a.metrics->status = __ldcg(a.status);
+        return;
+    }
+    __shared__ long long fix[kPgFields];
+    if (threadIdx.x < kPgFields) fix[threadIdx.x] = 0;
+    __syncthreads();
+    if (cnt > 0) pg_band_tokens(a, a.list, cnt, fix);
+    if (!a.metrics) return;
+    const int k = threadIdx.x;
+    if (k < kPgFields) {
+        const long long v = static_cast<long long>(__ldcg(reinterpret_cast<const unsigned long long*>(a.acc + k))) + fix[k];
+        pg_write_metric(k, k < kPgSums ? static_cast<double>(v) * (1.0 / kPgFix) : static_cast<double>(v), a.metrics);
+    }
+    if (k == 0) a.metrics->status = __ldcg(a.status);
+}
+
+// Every block calls this after adding its partial; the last one to arrive finishes.
+RL_DEVINL void pg_finish(const PgArgs& a) {
+    __shared__ int last;
+    __threadfence();   // this thread's outputs and atomics before the arrival count
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(a.done, 1) == a.nb - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    pg_final(a);
+}
+
+// ----------------------------------------------------------------------------------
 // Slow pass
 // ----------------------------------------------------------------------------------
 __global__ void __launch_bounds__(kPgThreads, kPgSlowPerSm) policy_slow_kernel(PgArgs a) {
@@ -406,9 +389,10 @@ __global__ void __launch_bounds__(kPgThreads, kPgSlowPerSm) policy_slow_kernel(P
     pg_block_reduce(acc, sums, cnts);
     const int k = threadIdx.x;
     if (k < kPgSums)
-        a.psum[k * a.nb + blockIdx.x] = sums[k];
+        pg_add_partial(a, k, sums[k], 0);
     else if (k < kPgFields)
-        a.pcnt[(k - kPgSums) * a.nb + blockIdx.x] = cnts[k - kPgSums];
+        pg_add_partial(a, k, 0.f, cnts[k - kPgSums]);
+    pg_finish(a);
 }
 
 // ----------------------------------------------------------------------------------
@@ -422,7 +406,7 @@ struct PgTok {
     bool band;                     // some value lies inside a threshold's band
 };
 
-// One token, fp32 decisions, no branches (the tokens of a round interleave freely).
+// One token, fp32 decisions, no branches (the tokens of a thread interleave freely).
 // |p_old - p_samp| = p_samp |rho - 1| with rho = e^(lp_old - lp_samp) (one EX2 less).
 RL_DEVINL PgTok pg_fast(float lt, float lo, float ls, float A, const PgPrep& q) {
     PgTok o;
@@ -500,224 +484,324 @@ RL_DEVINL void pg_append(const PgArgs& a, int64_t t) {
     if (s < a.cap) a.list[s] = static_cast<int>(t);
 }
 
-// Two tokens per thread and round; rounds of nthreads pairs with a warp-aligned rotation
-// (rot_step) so a thread does not meet the same position of a padded sequence layout in
-// every round (a grid stride that is a multiple of the padding period would give some
-// threads only valid tokens and others only padding).  The next round's inputs are
-// loaded before this round's math.
-__global__ void __launch_bounds__(kPgThreads, kPgFastPerSm) policy_fast_kernel(PgArgs a) {
+// One stage of the ring: kPgStageSlots consecutive token slots of the five inputs.
+struct alignas(16) PgStage {
+    float lt[kPgStageSlots], lo[kPgStageSlots], ls[kPgStageSlots], A[kPgStageSlots];
+    uint8_t m[kPgStageSlots];
+};
+constexpr int kPgStageBytes = static_cast<int>(sizeof(PgStage));
+constexpr int kPgStreamSmem = kPgDepth * kPgStageBytes;
+
+// One bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16),
+// completion counted on an mbarrier of this CTA.
+RL_DEVINL void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Stages of kPgStageSlots slots are dealt round-robin to the blocks (block b takes stages
+// b, b + nb, b + 2 nb, ... with nb odd, so a block's stages walk through every phase of a
+// power-of-two padding period and the valid tokens, where the arithmetic is, spread
+// evenly).  Warp-specialised, 320 threads:
+//   * warps 0-7 (consumers) take 2 consecutive slots each per stage (vector shared-memory
+//     reads, streaming stores) and release the stage on its "empty" mbarrier (one
+//     arrival per warp), so no consumer waits for another; a token inside a band goes to
+//     the block's list;
+//   * warp 8 (producer): lane 0 fills a ring of kPgDepth shared-memory stages with bulk
+//     copies, five per stage, one "full" mbarrier per stage;
+//   * warp 9 (exact): takes the listed band tokens while the stream goes on (exact
+//     decisions, outputs rewritten, contributions into the block's fixed-point sums), so
+//     their latency stays off the block's tail.
+// The last T mod 16 slots go to the last block with scalar loads.  Every wait is bounded:
+// on a timeout the block records RL_STATUS_TIMEOUT, stops, and waits (bounded) for the
+// copies it still has in flight.
+__global__ void __launch_bounds__(kPgThreads + 64, kPgFastPerSm) policy_fast_kernel(PgArgs a) {
+    extern __shared__ __align__(128) uint8_t pg_smem[];
+    PgStage* ring = reinterpret_cast<PgStage*>(pg_smem);
+    __shared__ __align__(8) uint64_t full[kPgDepth];
+    __shared__ __align__(8) uint64_t empty[kPgDepth];
     __shared__ int hist_s[kPgBins * kPgThreads];   // bin-major: thread t's bin b at b * 256 + t
-    __shared__ int blist[kPgBlockBand];            // this block's band tokens
+    __shared__ int blist[kPgBlockBand];            // this block's band tokens (-1: not yet written)
     __shared__ int bcount;
+    __shared__ int cons_done;                      // consumer warps past their last listing
+    __shared__ int abort_flag;
     __shared__ long long bfix[kPgFields];
-    for (int b = 0; b <= a.q.n; ++b) hist_s[b * kPgThreads + threadIdx.x] = 0;
-    if (threadIdx.x == 0) bcount = 0;
+
+    const int64_t n16 = a.T >> 4;
+    const int64_t nstages = (n16 * 16 + kPgStageSlots - 1) / kPgStageSlots;
+    const int64_t mine = blockIdx.x < nstages ? (nstages - blockIdx.x + a.nb - 1) / a.nb : 0;
+    const int nst = static_cast<int>(mine);
+    const bool consumer = threadIdx.x < kPgThreads;
+    const bool producer = threadIdx.x >= kPgThreads && threadIdx.x < kPgThreads + 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == kPgThreads) {
+        for (int s = 0; s < kPgDepth; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, kPgThreads / 32);
+        }
+        fence_mbar_init();
+    }
+    if (threadIdx.x == 0) {
+        bcount = 0;
+        cons_done = 0;
+        abort_flag = 0;
+    }
+    if (consumer)
+        for (int b = 0; b <= a.q.n; ++b) hist_s[b * kPgThreads + threadIdx.x] = 0;
+    for (int i = threadIdx.x; i < kPgBlockBand; i += blockDim.x) blist[i] = -1;
     if (threadIdx.x < kPgFields) bfix[threadIdx.x] = 0;
     __syncthreads();
-    int* hist = hist_s + threadIdx.x;
-    auto band = [&](int64_t t) {
-        const int s = atomicAdd(&bcount, 1);
-        if (s < kPgBlockBand)
-            blist[s] = static_cast<int>(t);
-        else
-            pg_append(a, t);   // spill to the global list (the last block takes it)
-    };
+
     PgFastAcc acc;
 #pragma unroll
     for (int k = 0; k < kPgSums; ++k) acc.sum[k] = 0.f;
 #pragma unroll
     for (int k = 0; k < 6; ++k) acc.cnt[k] = 0;
-    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t n2 = a.T / 2;
-    int64_t rot = 0;
-    auto next = [&](int64_t base) -> int64_t {
-        int64_t idx = tid + rot;
-        if (idx >= nthreads) idx -= nthreads;
-        rot += a.rot_step;
-        if (rot >= nthreads) rot -= nthreads;
-        return base + idx;
+    auto band = [&](int64_t t) {
+        const int s = atomicAdd(&bcount, 1);
+        if (s < kPgBlockBand)
+            atomicExch(blist + s, static_cast<int>(t));
+        else
+            pg_append(a, t);   // spill to the global list (the last block takes it)
     };
-    float2 lt = make_float2(0.f, 0.f), lo = lt, ls = lt, A = lt;
-    uchar2 m = make_uchar2(0, 0);
-    auto load = [&](int64_t k) {
-        if (k < n2) {
-            lt = __ldcs(reinterpret_cast<const float2*>(a.lt) + k);
-            lo = __ldcs(reinterpret_cast<const float2*>(a.lo) + k);
-            ls = __ldcs(reinterpret_cast<const float2*>(a.ls) + k);
-            A = __ldcs(reinterpret_cast<const float2*>(a.adv) + k);
-            m = __ldcs(reinterpret_cast<const uchar2*>(a.mask) + k);
+    auto stage_start = [&](int i) { return (static_cast<int64_t>(i) * a.nb + blockIdx.x) * kPgStageSlots; };
+    volatile int* vflag = &abort_flag;
+
+    if (warp == kPgThreads / 32 + 1) {
+        // exact warp: lane l takes listed entries done + l; loops until the consumers are
+        // past their last listing and every listed entry is taken (bounded)
+        volatile int* vcount = &bcount;
+        volatile int* vdone = &cons_done;
+        volatile int* vlist = blist;
+        const uint64_t t0 = globaltimer_ns();
+        int taken = 0;
+        while (true) {
+            const int finished = *vdone;
+            int avail = *vcount;
+            avail = avail < kPgBlockBand ? avail : kPgBlockBand;
+            if (taken < avail) {
+                const int e = taken + lane;
+                if (e < avail) {
+                    int t = vlist[e];
+                    while (t < 0 && globaltimer_ns() - t0 < kWaitLimitNs) t = vlist[e];
+                    if (t >= 0) {
+                        __threadfence_block();   // the consumer's stores to t before ours
+                        PgAcc one;
+                        pg_zero(one);
+                        float o[4];
+                        pg_token_listed(a.lt[t], a.lo[t], a.ls[t], a.adv[t], a.q, o, one);
+                        if (a.loss_ppo) a.loss_ppo[t] = o[0];
+                        if (a.loss_dec) a.loss_dec[t] = o[1];
+                        if (a.grad_ppo) a.grad_ppo[t] = o[2];
+                        if (a.grad_dec) a.grad_dec[t] = o[3];
+                        for (int f = 0; f < kPgSums; ++f)
+                            atomicAdd(reinterpret_cast<unsigned long long*>(bfix + f),
+                                      static_cast<unsigned long long>(__float2ll_rn(one.sum[f] * kPgFix)));
+                        for (int f = 0; f < kPgCounts; ++f)
+                            if (one.cnt[f] != 0)
+                                atomicAdd(reinterpret_cast<unsigned long long*>(bfix + kPgSums + f),
+                                          static_cast<unsigned long long>(one.cnt[f]));
+                    } else {
+                        set_status(a.status, RL_STATUS_TIMEOUT);
+                    }
+                }
+                taken = avail < taken + 32 ? avail : taken + 32;
+                continue;
+            }
+            if (finished == kPgThreads / 32 || *vflag) break;   // every listing is in avail
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                set_status(a.status, RL_STATUS_TIMEOUT);
+                break;
+            }
+            __nanosleep(200);
         }
-    };
-    int64_t i = next(0);
-    load(i);
-    for (int64_t base = 0; base < n2; base += nthreads) {
-        const float2 clt = lt, clo = lo, cls = ls, cA = A;
-        const uchar2 cm = m;
-        const int64_t ci = i;
-        i = next(base + nthreads);
-        load(i);
-        if (ci >= n2) continue;
-        float2 lp = make_float2(0.f, 0.f), ld = lp, gp = lp, gd = lp;
-        if ((cm.x | cm.y) != 0) {
-            const PgTok tx = pg_fast(clt.x, clo.x, cls.x, cA.x, a.q);
-            const PgTok ty = pg_fast(clt.y, clo.y, cls.y, cA.y, a.q);
-            pg_take(tx, cm.x != 0, hist, acc, lp.x, ld.x, gp.x, gd.x);
-            pg_take(ty, cm.y != 0, hist, acc, lp.y, ld.y, gp.y, gd.y);
-            if ((cm.x != 0) & tx.band) band(2 * ci);
-            if ((cm.y != 0) & ty.band) band(2 * ci + 1);
+    } else if (producer) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < nst; ++i) {
+                const int slot = i % kPgDepth;
+                if (i >= kPgDepth &&
+                    !mbar_wait(empty + slot, static_cast<uint32_t>((i / kPgDepth - 1) & 1), a.status)) {
+                    atomicExch(&abort_flag, 1);
+                    break;
+                }
+                if (*vflag) break;
+                const int64_t g = stage_start(i);
+                const int64_t left = n16 * 16 - g;
+                const uint32_t L = static_cast<uint32_t>(left < kPgStageSlots ? left : kPgStageSlots);
+                PgStage& st = ring[slot];
+                mbar_arrive_expect_tx(full + slot, 17u * L);
+                bulk_load(st.lt, a.lt + g, 4u * L, full + slot);
+                bulk_load(st.lo, a.lo + g, 4u * L, full + slot);
+                bulk_load(st.ls, a.ls + g, 4u * L, full + slot);
+                bulk_load(st.A, a.adv + g, 4u * L, full + slot);
+                bulk_load(st.m, a.mask + g, L, full + slot);
+                issued = i + 1;
+            }
+            if (*vflag) {
+                // the last kPgDepth stages issued may still be in flight: wait for them
+                // (bounded) before the block's shared memory goes away
+                for (int i = issued > kPgDepth ? issued - kPgDepth : 0; i < issued; ++i)
+                    mbar_wait(full + i % kPgDepth, static_cast<uint32_t>((i / kPgDepth) & 1), a.status);
+            }
         }
-        if (a.loss_ppo) __stcs(reinterpret_cast<float2*>(a.loss_ppo) + ci, lp);
-        if (a.loss_dec) __stcs(reinterpret_cast<float2*>(a.loss_dec) + ci, ld);
-        if (a.grad_ppo) __stcs(reinterpret_cast<float2*>(a.grad_ppo) + ci, gp);
-        if (a.grad_dec) __stcs(reinterpret_cast<float2*>(a.grad_dec) + ci, gd);
+    } else {
+        int* hist = hist_s + threadIdx.x;
+        const int j = 2 * threadIdx.x;
+        for (int i = 0; i < nst; ++i) {
+            const int slot = i % kPgDepth;
+            if (!mbar_wait(full + slot, static_cast<uint32_t>((i / kPgDepth) & 1), a.status)) {
+                atomicExch(&abort_flag, 1);
+                break;
+            }
+            if (*vflag) break;
+            const int64_t g = stage_start(i);
+            if (g + j < n16 * 16) {
+                const PgStage& st = ring[slot];
+                const float2 lt = *reinterpret_cast<const float2*>(st.lt + j);
+                const float2 lo = *reinterpret_cast<const float2*>(st.lo + j);
+                const float2 ls = *reinterpret_cast<const float2*>(st.ls + j);
+                const float2 A = *reinterpret_cast<const float2*>(st.A + j);
+                const uint32_t mw = *reinterpret_cast<const uint16_t*>(st.m + j);
+                float2 lp = make_float2(0.f, 0.f), ld = lp, gp = lp, gd = lp;
+                bool b0 = false, b1 = false;
+                if (mw != 0u) {
+                    const bool v0 = (mw & 0xffu) != 0u, v1 = (mw & 0xff00u) != 0u;
+                    const PgTok t0 = pg_fast(lt.x, lo.x, ls.x, A.x, a.q);
+                    const PgTok t1 = pg_fast(lt.y, lo.y, ls.y, A.y, a.q);
+                    pg_take(t0, v0, hist, acc, lp.x, ld.x, gp.x, gd.x);
+                    pg_take(t1, v1, hist, acc, lp.y, ld.y, gp.y, gd.y);
+                    b0 = v0 & t0.band;
+                    b1 = v1 & t1.band;
+                }
+                if (a.loss_ppo) __stcs(reinterpret_cast<float2*>(a.loss_ppo + g + j), lp);
+                if (a.loss_dec) __stcs(reinterpret_cast<float2*>(a.loss_dec + g + j), ld);
+                if (a.grad_ppo) __stcs(reinterpret_cast<float2*>(a.grad_ppo + g + j), gp);
+                if (a.grad_dec) __stcs(reinterpret_cast<float2*>(a.grad_dec + g + j), gd);
+                // a band token's outputs are zero above; it is listed only after those
+                // stores (fenced), so the exact warp's rewrite lands after them
+                if (b0 | b1) {
+                    __threadfence_block();
+                    if (b0) band(g + j);
+                    if (b1) band(g + j + 1);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + slot);
+        }
+        // the last T mod 16 slots, scalar loads
+        if (blockIdx.x == a.nb - 1) {
+            const int64_t t = n16 * 16 + threadIdx.x;
+            if (t < a.T) {
+                float lp = 0.f, ld = 0.f, gp = 0.f, gd = 0.f;
+                bool bt = false;
+                if (a.mask[t] != 0) {
+                    const PgTok tk = pg_fast(a.lt[t], a.lo[t], a.ls[t], a.adv[t], a.q);
+                    pg_take(tk, true, hist, acc, lp, ld, gp, gd);
+                    bt = tk.band;
+                }
+                if (a.loss_ppo) a.loss_ppo[t] = lp;
+                if (a.loss_dec) a.loss_dec[t] = ld;
+                if (a.grad_ppo) a.grad_ppo[t] = gp;
+                if (a.grad_dec) a.grad_dec[t] = gd;
+                if (bt) {
+                    __threadfence_block();
+                    band(t);
+                }
+            }
+        }
+        __threadfence_block();   // this warp's listings before its arrival below
+        __syncwarp();
+        if (lane == 0) atomicAdd(&cons_done, 1);
     }
-    // this block's band tokens on the exact path (few: fp32 float-float work, spread over
-    // all blocks), into bfix
     __syncthreads();
-    const int nband = bcount < kPgBlockBand ? bcount : kPgBlockBand;
-    if (nband > 0) pg_band_tokens(a, blist, nband, bfix);
-    // block partial: warp trees (fp32 sums, exact int32 counts), then the 8 warps in order
-    // plus the band tokens' terms; the curve counts from the histogram, cnt_k = #(j > k),
-    // back in the caller's order
+    // block partial: warp trees (fp32 sums, exact int32 counts), then the 8 consumer warps
+    // in order plus the band tokens' fixed-point terms, into the batch accumulators; the
+    // curve counts from the histogram, cnt_k = #(j > k), back in the caller's order
     __shared__ float shs[kPgThreads / 32][kPgSums];
     __shared__ int shc[kPgThreads / 32][6];
     __shared__ int bins[kPgBins];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-    for (int k = 0; k < kPgSums; ++k) {
-        const float v = warp_sum(acc.sum[k]);
-        if (lane == 0) shs[warp][k] = v;
+    for (int f = 0; f < kPgSums; ++f) {
+        const float v = warp_sum(acc.sum[f]);
+        if (lane == 0 && consumer) shs[warp][f] = v;
     }
 #pragma unroll
-    for (int k = 0; k < 6; ++k) {
-        const int v = __reduce_add_sync(0xffffffffu, acc.cnt[k]);
-        if (lane == 0) shc[warp][k] = v;
+    for (int f = 0; f < 6; ++f) {
+        const int v = __reduce_add_sync(0xffffffffu, acc.cnt[f]);
+        if (lane == 0 && consumer) shc[warp][f] = v;
     }
     __syncthreads();
-    for (int b = warp; b <= a.q.n; b += kPgThreads / 32) {
-        int v = 0;
-        for (int t = lane; t < kPgThreads; t += 32) v += hist_s[b * kPgThreads + t];
-        v = __reduce_add_sync(0xffffffffu, v);
-        if (lane == 0) bins[b] = v;
-    }
+    if (consumer)
+        for (int b = warp; b <= a.q.n; b += kPgThreads / 32) {
+            int v = 0;
+            for (int t = lane; t < kPgThreads; t += 32) v += hist_s[b * kPgThreads + t];
+            v = __reduce_add_sync(0xffffffffu, v);
+            if (lane == 0) bins[b] = v;
+        }
     __syncthreads();
-    const int k = threadIdx.x;
-    if (k < kPgSums) {
+    const int f = threadIdx.x;
+    if (f < kPgSums) {
         float v = 0.f;
-        for (int w = 0; w < kPgThreads / 32; ++w) v += shs[w][k];
-        a.psum[k * a.nb + blockIdx.x] = v + static_cast<float>(bfix[k]) / kPgFix;
-    } else if (k < kPgSums + 6) {
+        for (int w = 0; w < kPgThreads / 32; ++w) v += shs[w][f];
+        pg_add_partial(a, f, v, bfix[f]);
+    } else if (f < kPgSums + 6) {
         int v = 0;
-        for (int w = 0; w < kPgThreads / 32; ++w) v += shc[w][k - kPgSums];
-        a.pcnt[(k - kPgSums) * a.nb + blockIdx.x] = v + static_cast<int>(bfix[k]);
-    } else if (k < kPgFields) {
-        const int c = k - kPgSums - 6;        // caller's curve index
+        for (int w = 0; w < kPgThreads / 32; ++w) v += shc[w][f - kPgSums];
+        pg_add_partial(a, f, 0.f, v + bfix[f]);
+    } else if (f < kPgFields) {
+        const int c = f - kPgSums - 6;        // caller's curve index
         int v = 0;
         if (c < a.q.n) {
             int js = 0;                        // its sorted position
             while (a.q.perm[js] != c) ++js;
             for (int b = js + 1; b <= a.q.n; ++b) v += bins[b];
         }
-        a.pcnt[(k - kPgSums) * a.nb + blockIdx.x] = v + static_cast<int>(bfix[k]);
+        pg_add_partial(a, f, 0.f, v + bfix[f]);
     }
-}
-
-// ----------------------------------------------------------------------------------
-// Final reduction
-// ----------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kPgFinalThreads) policy_final_kernel(PgArgs a) {
-    const int cnt = *a.count;
-    if (cnt > a.cap) {   // the spill list overflowed: every token again, exact decisions
-        PgAcc acc;
-        pg_zero(acc);
-        pg_exact_pass(a, threadIdx.x, blockDim.x, acc);
-        __shared__ float sums[kPgSums];
-        __shared__ int cnts[kPgCounts];
-        pg_block_reduce(acc, sums, cnts);
-        if (a.metrics && threadIdx.x < kPgFields) {
-            const int k = threadIdx.x;
-            pg_write_metric(k, k < kPgSums ? static_cast<double>(sums[k]) : static_cast<double>(cnts[k - kPgSums]),
-                            a.metrics);
-        }
-        return;
-    }
-    __shared__ long long fix[kPgFields];
-    if (threadIdx.x < kPgFields) fix[threadIdx.x] = 0;
-    __syncthreads();
-    if (cnt > 0) pg_band_tokens(a, a.list, cnt, fix);
-    if (!a.metrics) return;
-    // warp k: field k over the partials, lane l adding b = l, l + 32, ... in order
-    const int k = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (k >= kPgFields) return;
-    double s;
-    if (k < kPgSums) {
-        float v = 0.f;
-        for (int b = lane; b < a.nb; b += 32) v += a.psum[k * a.nb + b];
-        s = static_cast<double>(warp_sum(v)) + static_cast<double>(fix[k]) / static_cast<double>(kPgFix);
-    } else {
-        long long v = 0;
-        for (int b = lane; b < a.nb; b += 32) v += a.pcnt[(k - kPgSums) * a.nb + b];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        s = static_cast<double>(v + fix[k]);
-    }
-    if (lane == 0) pg_write_metric(k, s, a.metrics);
+    pg_finish(a);
 }
 
 // ----------------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------------
-// Workspace: a 256-byte header (spill-list length), the block partials (field-major),
-// then the spill list in whatever room is left.
+// Workspace: a 256-byte header (spill-list length, arrival count, status word, and at
+// byte 16 the kPgFields accumulators), then the spill list in whatever room is left.
 struct PgWs {
     int* count;
-    float* psum;
-    int* pcnt;
+    int* done;
+    int32_t* status;
+    long long* acc;
     int* list;
     int cap;
 };
 constexpr size_t kPgHeader = 256;
+static_assert(16 + kPgFields * 8 <= kPgHeader, "accumulators must fit the header");
 
 static int fast_blocks(int sms) { return sms * kPgFastPerSm; }
 static int slow_blocks(int sms) { return sms * kPgSlowPerSm; }
-static int max_blocks(int sms) { return fast_blocks(sms) > slow_blocks(sms) ? fast_blocks(sms) : slow_blocks(sms); }
 
-static size_t fixed_bytes(int sms) {
-    return kPgHeader + align_up(static_cast<size_t>(max_blocks(sms)) * kPgFields * 4, 256);
-}
-
-static PgWs pg_ws(void* ws, size_t ws_bytes, int sms) {
+static PgWs pg_ws(void* ws, size_t ws_bytes) {
     PgWs w;
     uint8_t* b = static_cast<uint8_t*>(ws);
     w.count = reinterpret_cast<int*>(b);
-    w.psum = reinterpret_cast<float*>(b + kPgHeader);
-    w.pcnt = reinterpret_cast<int*>(w.psum + static_cast<size_t>(max_blocks(sms)) * kPgSums);
-    const size_t fixed = fixed_bytes(sms);
-    w.list = reinterpret_cast<int*>(b + fixed);
-    const size_t room = ws_bytes > fixed ? (ws_bytes - fixed) / sizeof(int) : 0;
+    w.done = reinterpret_cast<int*>(b + 4);
+    w.status = reinterpret_cast<int32_t*>(b + 8);
+    w.acc = reinterpret_cast<long long*>(b + 16);
+    w.list = reinterpret_cast<int*>(b + kPgHeader);
+    const size_t room = ws_bytes > kPgHeader ? (ws_bytes - kPgHeader) / sizeof(int) : 0;
     w.cap = room > static_cast<size_t>(INT32_MAX) ? INT32_MAX : static_cast<int>(room);
     return w;
 }
 
-size_t policy_ws_need(int64_t T) {
-    (void)T;
-    return fixed_bytes(num_sms());
-}
-
 size_t policy_ws_bytes(int64_t T) {
-    // any device up to 256 SMs, and a band list of max(4096, T / 16) entries (the expected
-    // share of band tokens is well under 1e-3; an overflow only costs the slow fallback)
+    // the header and a band list of max(4096, T / 16) entries (the expected share of band
+    // tokens is well under 1e-3; an overflow only costs the slow fallback)
     const int64_t list = T / 16 > 4096 ? T / 16 : 4096;
-    return align_up(fixed_bytes(256) + static_cast<size_t>(list) * sizeof(int), 256);
-}
-
-// ln t as a float-float pair (hi = the float nearest ln t, lo = the float nearest the rest)
-static FF ln_ff(double t) {
-    if (!(t > 0.0)) return {-INFINITY, 0.f};
-    const double l = std::log(t);
-    const float hi = static_cast<float>(l);
-    return {hi, static_cast<float>(l - static_cast<double>(hi))};
+    return align_up(kPgHeader + static_cast<size_t>(list) * sizeof(int), 256);
 }
 
 static PgPrep prepare(const rl_pg_params& p) {
@@ -758,26 +842,16 @@ static PgPrep prepare(const rl_pg_params& p) {
     return q;
 }
 
-// Warp-aligned rotation per round: about 0.618 of the warps with an odd residue near
-// 0.6 x 32 modulo 32 warps, so successive rounds spread over the phases of any
-// power-of-two padding period instead of creeping by one warp.
-static int64_t rotation(int nb) {
-    const int64_t nwarps = static_cast<int64_t>(nb) * (kPgThreads / 32);
-    int64_t kw = (nwarps * 618 / 1000) / 32 * 32 + 19;
-    while (kw >= nwarps && kw > 0) kw -= 32;
-    return (kw < 0 ? 0 : kw) * 32;
-}
-
 int policy_impl(const float* lt, const float* lo, const float* ls, const float* adv,
                 const uint8_t* mask, int64_t T, const rl_pg_params* p, float* loss_ppo,
                 float* loss_dec, float* grad_ppo, float* grad_dec, rl_pg_metrics* metrics,
                 void* ws, size_t ws_bytes, cudaStream_t stream) {
     const int sms = num_sms();
-    if (ws_bytes < fixed_bytes(sms)) return RL_ERR_WORKSPACE;
-    const PgWs w = pg_ws(ws, ws_bytes, sms);
-    auto al = [](const void* ptr, uintptr_t n) { return (reinterpret_cast<uintptr_t>(ptr) & (n - 1)) == 0; };
-    const bool fast = T % 2 == 0 && T < (int64_t(1) << 31) && al(lt, 8) && al(lo, 8) && al(ls, 8) && al(adv, 8) &&
-                      al(mask, 2) && al(loss_ppo, 8) && al(loss_dec, 8) && al(grad_ppo, 8) && al(grad_dec, 8);
+    if (ws_bytes < kPgHeader) return RL_ERR_WORKSPACE;
+    const PgWs w = pg_ws(ws, ws_bytes);
+    auto al = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+    const bool fast = T < (int64_t(1) << 31) && al(lt) && al(lo) && al(ls) && al(adv) && al(mask) &&
+                      al(loss_ppo) && al(loss_dec) && al(grad_ppo) && al(grad_dec);
     PgArgs a{};
     a.lt = lt;
     a.lo = lo;
@@ -792,23 +866,32 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
     a.grad_ppo = grad_ppo;
     a.grad_dec = grad_dec;
     a.count = w.count;
+    a.done = w.done;
+    a.status = w.status;
     a.list = w.list;
     a.cap = w.cap;
-    a.psum = w.psum;
-    a.pcnt = w.pcnt;
+    a.acc = w.acc;
     a.metrics = metrics;
+    static int smem_set[64] = {0};   // per device: the fast pass's shared-memory opt-in
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RL_ERR_CUDA;
+    if (fast && !smem_set[dev]) {
+        if (cudaFuncSetAttribute(policy_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPgStreamSmem) !=
+            cudaSuccess)
+            return RL_ERR_CUDA;
+        smem_set[dev] = 1;
+    }
     ProfScope ps(RL_PROF_POLICY, stream);
-    if (cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return RL_ERR_CUDA;   // spill count
+    // spill count, arrival count, status, accumulators
+    if (cudaMemsetAsync(ws, 0, kPgHeader, stream) != cudaSuccess) return RL_ERR_CUDA;
     if (fast) {
-        a.nb = fast_blocks(sms);
-        a.rot_step = rotation(a.nb);
-        policy_fast_kernel<<<a.nb, kPgThreads, 0, stream>>>(a);
+        a.nb = fast_blocks(sms) - 1;   // odd: see policy_fast_kernel
+        policy_fast_kernel<<<a.nb, kPgThreads + 64, kPgStreamSmem, stream>>>(a);
     } else {
         a.nb = slow_blocks(sms);
         policy_slow_kernel<<<a.nb, kPgThreads, 0, stream>>>(a);
     }
-    policy_final_kernel<<<1, kPgFinalThreads, 0, stream>>>(a);
-    count_launch(2);
+    count_launch(1);
     return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }
 

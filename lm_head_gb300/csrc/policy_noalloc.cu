@@ -1,7 +1,7 @@
 // rl_policy_loss_elementwise_noalloc: the elementwise PPO / TIS / mismatch path for callers
-// that cannot allocate device memory.  Its scratch (the per-block partial sums that the
-// final reduction reads, the fixed-point accumulators and the band-token list) lives in a
-// file-scope device array instead of a caller workspace.
+// that cannot allocate device memory.  Its scratch (counters, the fixed-point metric
+// accumulators and the band-token list) lives in a file-scope device array instead of a
+// caller workspace.
 #include <mutex>
 
 #include "common.cuh"
@@ -9,8 +9,7 @@
 
 namespace rl {
 
-// 512 KiB: the block partials of a launch (6 blocks per SM, 1344 bytes per SM) and, in the
-// room left, the band-token list (about 80k entries on a 152-SM device).
+// 512 KiB: a 256-byte header and, in the room left, the band-token list (131008 entries).
 constexpr size_t kNoAllocScratchBytes = 524288;
 static __device__ __align__(256) double g_policy_scratch[kNoAllocScratchBytes / sizeof(double)];
 
@@ -64,12 +63,7 @@ extern "C" int rl_policy_loss_elementwise_noalloc(const float* lp_theta, const f
         set_last_error("needs an sm_100-family GPU");
         return RL_ERR_UNSUPPORTED;
     }
-    const size_t need = policy_ws_need(T);
-    if (need > kNoAllocScratchBytes) {
-        set_last_error("rl_policy_loss_elementwise_noalloc: this launch needs more partial-sum scratch "
-                       "than the 524288-byte static array holds (more than 389 SMs)");
-        return RL_ERR_WORKSPACE;
-    }
+    static_assert(kNoAllocScratchBytes >= 4096, "the scratch must hold the header");
     void* scratch = nullptr;
     int rc = scratch_address(&scratch);
     if (rc != RL_OK) return rc;

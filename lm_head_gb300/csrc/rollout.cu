@@ -1,0 +1,533 @@
+// Rollout correction over a batch of sequences ("Rollout Correction Methods": "Config
+// keys", "Importance Sampling", "Rejection Sampling" with the veto, "Mismatch Metrics"):
+// per-token importance weights at token, sequence or geometric level, bounded by
+// truncate / clip / mask, rejection sampling at any level, the veto, batch
+// normalisation, and the IS / RS and mismatch-monitoring sums.
+//
+// Every decision (a bound, a rejection, the veto) is the exact predicate on the fp32
+// inputs: a token's log-ratio d = lp_train - lp_rollout is formed exactly as a
+// float-float pair, a sequence's sum of log-ratios (and, for sequence-level rejection,
+// its sum of token weights) is carried in float-float, and each comparison is taken
+// against a threshold's logarithm (or n times it) prepared on the host as a float-float
+// pair.  Weight values are fp32.
+//
+//  1. rc_seq_kernel     one block per sequence: a pass over its tokens for the sequence
+//                       sums, the sequence's decisions by one thread, a second pass (the
+//                       tokens are now in L2) writing weights and keep flags; one record
+//                       of partial sums per sequence.
+//  2. rc_reduce_kernel  one block, one warp per field: the records summed in sequence
+//                       order (fixed tree), so results are reproducible; then the
+//                       batch-normalisation factor and the metrics.
+//  3. rc_scale_kernel   (batch normalisation only) weights *= factor.
+#include <cmath>
+#include <climits>
+
+#include "common.cuh"
+#include "ff.cuh"
+#include "internal.h"
+
+namespace rl {
+
+constexpr int kRcThreads = 256;
+// per-sequence record: double sums, int64 counts, then the kept weights' min and max
+enum {
+    RD_W_BEFORE, RD_W_AFTER, RD_KEPT_W, RD_MIS_KL, RD_K3, RD_ABS, RD_CHI2T, RD_TRAIN_LPPL, RD_ROLL_LPPL,
+    RD_LPPL_DIFF, RD_LPPL_ABS, RD_PPL_RATIO, RD_CHI2S, kRcD
+};
+enum { RC_VALID, RC_SEQ, RC_KEPT, RC_TIS_LO, RC_TIS_HI, RC_RS_LO, RC_RS_HI, RC_CAT_TOK, RC_CAT_SEQ, kRcC };
+constexpr int kRcFields = kRcD + kRcC + 2;   // + min, max
+
+struct RcPrep {
+    int use_tis, mode, level, norm, use_rs, rs_level, veto;
+    float L, U, rsL, rsU;
+    FF lnL, lnU, lnRsL, lnRsU, lnVeto;
+};
+
+struct RcArgs {
+    const float* lt;
+    const float* lr;
+    const uint8_t* mask;
+    const int64_t* off;
+    int64_t B, T;
+    RcPrep q;
+    float* w;
+    uint8_t* keep;
+    double* pd;          // [kRcD][B]
+    long long* pc;       // [kRcC][B]
+    float* pmin;         // [B]
+    float* pmax;         // [B]
+    int32_t* status;
+    float* factor;       // batch-normalisation factor for rc_scale_kernel
+    rl_rc_metrics* metrics;
+};
+
+// Fixed-order reductions: a butterfly within each warp (every lane ends with the same
+// value, the same operands in the same order on both lanes of an exchange), then the
+// warps in order by one thread.
+RL_DEVINL float warp_sum_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+RL_DEVINL int warp_sum_i(int v) { return __reduce_add_sync(0xffffffffu, v); }
+RL_DEVINL FF warp_sum_ff(FF v) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const FF u = {__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+        v = (lane & o) ? ff_add(u, v) : ff_add(v, u);
+    }
+    return v;
+}
+template <typename T, typename Op>
+RL_DEVINL T rc_block_reduce(T v, T* sh, Op op) {   // sh: one slot per warp
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    if (lane == 0) sh[warp] = v;
+    __syncthreads();
+    T r = sh[0];
+    for (int i = 1; i < nw; ++i) r = op(r, sh[i]);
+    return r;
+}
+
+// e^(hi + lo) for a float-float exponent: e^hi (float-float) times 1 + lo (|lo| tiny).
+RL_DEVINL FF exp_ff2(FF d) { return ff_mul(exp_ff(d.hi), two_sum(1.f, d.lo)); }
+
+struct RcSeq {   // one sequence's decisions (thread 0 -> block)
+    int n, tis_lo, tis_hi, rs_lo, rs_hi, veto;
+    float wseq;
+};
+
+// A sequence is walked in tiles of kRcTile tokens: thread t takes tokens
+// o0 + kRcTile k + kRcThreads j + t, j < kRcPer (coalesced loads, no alignment needed).
+// The first kRcCached tiles stay in registers between the two passes.
+constexpr int kRcPer = 4;
+constexpr int kRcTile = kRcThreads * kRcPer;
+constexpr int kRcCached = 4;
+constexpr int kRcW = kRcThreads / 32;
+
+__global__ void __launch_bounds__(kRcThreads) rc_seq_kernel(RcArgs a) {
+    __shared__ FF shff[kRcW][4];
+    __shared__ float shf[kRcW][5];
+    __shared__ int shi[kRcW][6];
+    __shared__ RcSeq sq;
+    const RcPrep& q = a.q;
+    const int64_t b = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int64_t o0 = a.off[b], o1 = a.off[b + 1];
+    const bool bad = o0 < 0 || o1 < o0 || o1 > a.T || (b == 0 && o0 != 0) || (b == a.B - 1 && o1 != a.T);
+    if (bad) {
+        if (threadIdx.x == 0) set_status(a.status, RL_STATUS_OFFSETS);
+        o0 = o0 < 0 ? 0 : (o0 > a.T ? a.T : o0);
+        o1 = o1 < o0 ? o0 : (o1 > a.T ? a.T : o1);
+    }
+    const bool rs_seq = q.use_rs && q.rs_level == RL_LEVEL_SEQUENCE;
+    const int ntiles = static_cast<int>((o1 - o0 + kRcTile - 1) / kRcTile);
+
+    // pass 1: the sequence's sums; the first tiles' inputs kept in registers
+    float clt[kRcCached][kRcPer], clr[kRcCached][kRcPer];
+    uint32_t cm[kRcCached];
+    int n = 0, cat = 0;
+    FF S = {0.f, 0.f}, St = {0.f, 0.f}, Sr = {0.f, 0.f}, E = {0.f, 0.f};
+    float mis = 0.f, k3 = 0.f, ad = 0.f, c2 = 0.f;
+    auto load_tile = [&](int k, float (&lt)[kRcPer], float (&lr)[kRcPer], uint32_t& m) {
+        m = 0;
+#pragma unroll
+        for (int j = 0; j < kRcPer; ++j) {
+            const int64_t i = o0 + static_cast<int64_t>(k) * kRcTile + j * kRcThreads + threadIdx.x;
+            const bool in = i < o1;
+            lt[j] = in ? a.lt[i] : 0.f;
+            lr[j] = in ? a.lr[i] : 0.f;
+            m |= (in && a.mask[i] != 0 ? 1u : 0u) << j;
+        }
+    };
+    auto stats = [&](const float (&lt)[kRcPer], const float (&lr)[kRcPer], uint32_t m) {
+#pragma unroll
+        for (int j = 0; j < kRcPer; ++j) {
+            if (!((m >> j) & 1u)) continue;
+            const FF d = two_sum(lt[j], -lr[j]);
+            ++n;
+            S = ff_add(S, d);
+            St = ff_add(St, {lt[j], 0.f});
+            Sr = ff_add(Sr, {lr[j], 0.f});
+            if (rs_seq) E = ff_add(E, exp_ff2(d));
+            if (q.veto) cat += ff_lt(d, q.lnVeto) ? 1 : 0;
+            const float df = d.hi;
+            const float ed = expf(df);
+            mis -= df;
+            k3 += ed - df - 1.f;
+            ad += fabsf(df);
+            c2 += ed * ed;
+        }
+    };
+#pragma unroll
+    for (int k = 0; k < kRcCached; ++k) {
+        if (k < ntiles) load_tile(k, clt[k], clr[k], cm[k]);
+        else cm[k] = 0;
+    }
+#pragma unroll
+    for (int k = 0; k < kRcCached; ++k) stats(clt[k], clr[k], cm[k]);
+    for (int k = kRcCached; k < ntiles; ++k) {
+        float lt[kRcPer], lr[kRcPer];
+        uint32_t m;
+        load_tile(k, lt, lr, m);
+        stats(lt, lr, m);
+    }
+    {
+        const FF w4[4] = {warp_sum_ff(S), warp_sum_ff(St), warp_sum_ff(Sr), rs_seq ? warp_sum_ff(E) : FF{0.f, 0.f}};
+        const float f4[4] = {warp_sum_f(mis), warp_sum_f(k3), warp_sum_f(ad), warp_sum_f(c2)};
+        const int i2[2] = {warp_sum_i(n), warp_sum_i(cat)};
+        if (lane == 0) {
+            for (int f = 0; f < 4; ++f) shff[warp][f] = w4[f];
+            for (int f = 0; f < 4; ++f) shf[warp][f] = f4[f];
+            for (int f = 0; f < 2; ++f) shi[warp][f] = i2[f];
+        }
+    }
+    __syncthreads();
+    double seqd[7] = {0, 0, 0, 0, 0, 0, 0};   // w_before (sequence levels), lppl terms, chi2_seq
+    float tok1[4] = {0.f, 0.f, 0.f, 0.f};      // mis, k3, |d|, e^2d
+    int nt = 0, catt = 0;
+    if (threadIdx.x == 0) {
+        FF R[4] = {shff[0][0], shff[0][1], shff[0][2], shff[0][3]};
+        for (int f = 0; f < 4; ++f) tok1[f] = shf[0][f];
+        nt = shi[0][0];
+        catt = shi[0][1];
+        for (int w = 1; w < kRcW; ++w) {
+            for (int f = 0; f < 4; ++f) R[f] = ff_add(R[f], shff[w][f]);
+            for (int f = 0; f < 4; ++f) tok1[f] += shf[w][f];
+            nt += shi[w][0];
+            catt += shi[w][1];
+        }
+        const FF Sb = R[0], Stb = R[1], Srb = R[2], Eb = R[3];
+        RcSeq s{};
+        s.n = nt;
+        if (nt > 0) {
+            // fp32 and float-float here: fp64 is a slow pipe on this part and this thread
+            // is on the block's critical path
+            const FF nf = {static_cast<float>(nt), 0.f};   // exact below 2^24 tokens per sequence
+            const float rn = 1.f / static_cast<float>(nt);
+            if (q.level == RL_LEVEL_SEQUENCE) {
+                s.tis_lo = ff_lt(Sb, q.lnL);
+                s.tis_hi = ff_gt(Sb, q.lnU);
+                s.wseq = expf(Sb.hi) * (1.f + Sb.lo);
+                seqd[0] = Sb.hi < 88.f ? static_cast<double>(s.wseq) * nt : exp(static_cast<double>(Sb.hi)) * nt;
+            } else if (q.level == RL_LEVEL_GEOMETRIC) {
+                s.tis_lo = ff_lt(Sb, ff_mul(nf, q.lnL));
+                s.tis_hi = ff_gt(Sb, ff_mul(nf, q.lnU));
+                s.wseq = expf((Sb.hi + Sb.lo) * rn);
+                seqd[0] = static_cast<double>(s.wseq) * nt;
+            }
+            if (q.use_rs && q.rs_level == RL_LEVEL_SEQUENCE) {   // mean token weight vs the bounds
+                s.rs_lo = ff_lt(Eb, two_prod(static_cast<float>(nt), q.rsL));
+                s.rs_hi = !s.rs_lo && ff_gt(Eb, two_prod(static_cast<float>(nt), q.rsU));
+            } else if (q.use_rs && q.rs_level == RL_LEVEL_GEOMETRIC) {
+                s.rs_lo = ff_lt(Sb, ff_mul(nf, q.lnRsL));
+                s.rs_hi = !s.rs_lo && ff_gt(Sb, ff_mul(nf, q.lnRsU));
+            }
+            s.veto = catt > 0;
+            const float tr = -(Stb.hi + Stb.lo) * rn;
+            const float ro = -(Srb.hi + Srb.lo) * rn;
+            const float df = -(ff_add(Stb, FF{-Srb.hi, -Srb.lo}).hi) * rn;   // tr - ro, from the exact sums
+            seqd[1] = tr;
+            seqd[2] = ro;
+            seqd[3] = df;
+            seqd[4] = fabsf(df);
+            seqd[5] = expf(df);
+            // e^(2 S): fp32 while it fits, fp64 (one call) past the fp32 range
+            seqd[6] = Sb.hi < 44.f ? static_cast<double>(expf(2.f * Sb.hi) * (1.f + 2.f * Sb.lo))
+                                   : exp(2.0 * (static_cast<double>(Sb.hi) + static_cast<double>(Sb.lo)));
+        }
+        sq = s;
+    }
+    __syncthreads();
+    const RcSeq s = sq;
+
+    // pass 2: weights and keep flags
+    float wb_sum = 0.f, kept_sum = 0.f, wraw_sum = 0.f, mn = INFINITY, mx = -INFINITY;
+    int kept = 0, tlo = 0, thi = 0, rlo = 0, rhi = 0;
+    auto weights = [&](int k, const float (&lt)[kRcPer], const float (&lr)[kRcPer], uint32_t m) {
+#pragma unroll
+        for (int j = 0; j < kRcPer; ++j) {
+            const int64_t i = o0 + static_cast<int64_t>(k) * kRcTile + j * kRcThreads + threadIdx.x;
+            if (i >= o1) continue;
+            float wout = 0.f;
+            uint8_t kp8 = 0;
+            if ((m >> j) & 1u) {
+                const FF d = two_sum(lt[j], -lr[j]);
+                float w;
+                bool lo, hi;
+                if (q.level == RL_LEVEL_TOKEN) {
+                    w = expf(d.hi) * (1.f + d.lo);
+                    lo = ff_lt(d, q.lnL);
+                    hi = ff_gt(d, q.lnU);
+                    wraw_sum += w;
+                } else {
+                    w = s.wseq;
+                    lo = s.tis_lo;
+                    hi = s.tis_hi;
+                }
+                float wb;
+                if (!q.use_tis)
+                    wb = 1.f;
+                else if (q.mode == RL_TIS_TRUNCATE)
+                    wb = hi ? q.U : w;
+                else if (q.mode == RL_TIS_CLIP)
+                    wb = lo ? q.L : (hi ? q.U : w);
+                else
+                    wb = (lo || hi) ? 0.f : w;
+                bool r_lo = false, r_hi = false;
+                if (q.use_rs && q.rs_level == RL_LEVEL_TOKEN) {
+                    r_lo = ff_lt(d, q.lnRsL);
+                    r_hi = !r_lo && ff_gt(d, q.lnRsU);
+                } else if (q.use_rs) {
+                    r_lo = s.rs_lo;
+                    r_hi = s.rs_hi;
+                }
+                tlo += lo;
+                thi += hi;
+                rlo += r_lo;
+                rhi += r_hi;
+                wb_sum += wb;
+                if (!r_lo && !r_hi && !s.veto) {
+                    kp8 = 1;
+                    wout = wb;
+                    ++kept;
+                    kept_sum += wb;
+                    mn = fminf(mn, wb);
+                    mx = fmaxf(mx, wb);
+                }
+            }
+            if (a.w) a.w[i] = wout;
+            if (a.keep) a.keep[i] = kp8;
+        }
+    };
+#pragma unroll
+    for (int k = 0; k < kRcCached; ++k)
+        if (k < ntiles) weights(k, clt[k], clr[k], cm[k]);
+    for (int k = kRcCached; k < ntiles; ++k) {
+        float lt[kRcPer], lr[kRcPer];
+        uint32_t m;
+        load_tile(k, lt, lr, m);
+        weights(k, lt, lr, m);
+    }
+    {
+        float f5[5] = {warp_sum_f(wb_sum), warp_sum_f(kept_sum), warp_sum_f(wraw_sum), mn, mx};
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            f5[3] = fminf(f5[3], __shfl_xor_sync(0xffffffffu, f5[3], o));
+            f5[4] = fmaxf(f5[4], __shfl_xor_sync(0xffffffffu, f5[4], o));
+        }
+        const int i5[5] = {warp_sum_i(kept), warp_sum_i(tlo), warp_sum_i(thi), warp_sum_i(rlo), warp_sum_i(rhi)};
+        if (lane == 0) {
+            for (int f = 0; f < 5; ++f) shf[warp][f] = f5[f];
+            for (int f = 0; f < 5; ++f) shi[warp][f] = i5[f];
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float F[5];
+        int I[5];
+        for (int f = 0; f < 5; ++f) F[f] = shf[0][f];
+        for (int f = 0; f < 5; ++f) I[f] = shi[0][f];
+        for (int w = 1; w < kRcW; ++w) {
+            for (int f = 0; f < 3; ++f) F[f] += shf[w][f];
+            F[3] = fminf(F[3], shf[w][3]);
+            F[4] = fmaxf(F[4], shf[w][4]);
+            for (int f = 0; f < 5; ++f) I[f] += shi[w][f];
+        }
+        const int64_t B = a.B;
+        const double d[kRcD] = {q.level == RL_LEVEL_TOKEN ? static_cast<double>(F[2]) : seqd[0],
+                                F[0], F[1], tok1[0], tok1[1], tok1[2], tok1[3],
+                                seqd[1], seqd[2], seqd[3], seqd[4], seqd[5], seqd[6]};
+        for (int f = 0; f < kRcD; ++f) a.pd[f * B + b] = d[f];
+        const long long c[kRcC] = {nt, nt > 0 ? 1 : 0, I[0], I[1], I[2], I[3], I[4], catt, catt > 0 ? 1 : 0};
+        for (int f = 0; f < kRcC; ++f) a.pc[f * B + b] = c[f];
+        a.pmin[b] = F[3];
+        a.pmax[b] = F[4];
+    }
+}
+
+// One block of kRcFields warps: warp f sums field f of the records over the sequences in
+// order (lane l takes b = l, l + 32, ..., eight loads in flight ahead of their adds, then
+// a butterfly); thread 0 then forms the factor and writes the metrics.
+constexpr int kRcReduceThreads = 32 * kRcFields;
+__global__ void __launch_bounds__(kRcReduceThreads) rc_reduce_kernel(RcArgs a) {
+    __shared__ double tot[kRcFields];
+    const int f = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t B = a.B;
+    if (f < kRcD) {
+        const double* src = a.pd + f * B;
+        double v = 0.0;
+        for (int64_t b0 = lane; b0 < B; b0 += 32 * 8) {
+            double x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : 0.0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v += x[i];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) tot[f] = v;
+    } else if (f < kRcD + kRcC) {
+        const long long* src = a.pc + (f - kRcD) * B;
+        long long v = 0;
+        for (int64_t b0 = lane; b0 < B; b0 += 32 * 8) {
+            long long x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v += x[i];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) tot[f] = static_cast<double>(v);
+    } else {
+        const bool is_min = f == kRcD + kRcC;
+        const float* src = is_min ? a.pmin : a.pmax;
+        float v = is_min ? INFINITY : -INFINITY;
+        for (int64_t b0 = lane; b0 < B; b0 += 32 * 8) {
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : v;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v = is_min ? fminf(v, x[i]) : fmaxf(v, x[i]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float u = __shfl_xor_sync(0xffffffffu, v, o);
+            v = is_min ? fminf(v, u) : fmaxf(v, u);
+        }
+        if (lane == 0) tot[f] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    const double* t = tot;
+    const double kept_w = t[RD_KEPT_W], n_kept = t[kRcD + RC_KEPT];
+    const double factor = (a.q.use_tis && a.q.norm && n_kept > 0 && kept_w > 0) ? n_kept / kept_w : 1.0;
+    *a.factor = static_cast<float>(factor);
+    rl_rc_metrics* m = a.metrics;
+    if (!m) return;
+    m->w_before_sum = t[RD_W_BEFORE];
+    m->w_after_sum = t[RD_W_AFTER];
+    m->kept_w_sum = kept_w;
+    m->batch_norm_factor = factor;
+    m->final_sum = kept_w * factor;
+    m->final_min = n_kept > 0 ? t[kRcD + kRcC] * factor : 0.0;
+    m->final_max = n_kept > 0 ? t[kRcD + kRcC + 1] * factor : 0.0;
+    m->mis_kl_sum = t[RD_MIS_KL];
+    m->k3_sum = t[RD_K3];
+    m->abs_diff_sum = t[RD_ABS];
+    m->chi2_token_sum = t[RD_CHI2T];
+    m->train_lppl_sum = t[RD_TRAIN_LPPL];
+    m->rollout_lppl_sum = t[RD_ROLL_LPPL];
+    m->lppl_diff_sum = t[RD_LPPL_DIFF];
+    m->lppl_abs_diff_sum = t[RD_LPPL_ABS];
+    m->ppl_ratio_sum = t[RD_PPL_RATIO];
+    m->chi2_seq_sum = t[RD_CHI2S];
+    m->n_valid = static_cast<int64_t>(t[kRcD + RC_VALID]);
+    m->n_seq = static_cast<int64_t>(t[kRcD + RC_SEQ]);
+    m->n_kept = static_cast<int64_t>(n_kept);
+    m->n_tis_low = static_cast<int64_t>(t[kRcD + RC_TIS_LO]);
+    m->n_tis_high = static_cast<int64_t>(t[kRcD + RC_TIS_HI]);
+    m->n_rs_low = static_cast<int64_t>(t[kRcD + RC_RS_LO]);
+    m->n_rs_high = static_cast<int64_t>(t[kRcD + RC_RS_HI]);
+    m->n_cat_tokens = static_cast<int64_t>(t[kRcD + RC_CAT_TOK]);
+    m->n_cat_seqs = static_cast<int64_t>(t[kRcD + RC_CAT_SEQ]);
+    m->status = *a.status;
+}
+
+// w *= factor: float4 over the 16-byte-aligned body, scalars at the two ends.
+__global__ void rc_scale_kernel(float* w, int64_t T, const float* factor) {
+    const float f = *factor;
+    const int64_t head = ((16 - (reinterpret_cast<uintptr_t>(w) & 15)) & 15) / 4;
+    const int64_t h = head < T ? head : T;
+    const int64_t n4 = (T - h) / 4;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    float4* w4 = reinterpret_cast<float4*>(w + h);
+    for (int64_t i = tid; i < n4; i += nth) {
+        float4 v = w4[i];
+        v.x *= f;
+        v.y *= f;
+        v.z *= f;
+        v.w *= f;
+        w4[i] = v;
+    }
+    if (tid < h) w[tid] *= f;
+    const int64_t t0 = h + 4 * n4;
+    if (tid < T - t0) w[t0 + tid] *= f;
+}
+
+// ----------------------------------------------------------------------------------
+// Host side
+// ----------------------------------------------------------------------------------
+// Workspace: a 256-byte header (status, factor), then the per-sequence records.
+constexpr size_t kRcHeader = 256;
+
+static size_t rc_record_bytes(int64_t B) {
+    return align_up(static_cast<size_t>(B) * (kRcD * 8 + kRcC * 8 + 2 * 4) + 64, 256);
+}
+
+size_t rollout_ws_bytes(int64_t B) { return kRcHeader + rc_record_bytes(B < 1 ? 1 : B); }
+
+int rollout_impl(const float* lt, const float* lr, const uint8_t* mask, const int64_t* off, int64_t B, int64_t T,
+                 const rl_rc_params* p, float* w, uint8_t* keep, rl_rc_metrics* metrics, void* ws,
+                 size_t ws_bytes, cudaStream_t stream) {
+    if (ws_bytes < rollout_ws_bytes(B)) return RL_ERR_WORKSPACE;
+    RcArgs a{};
+    a.lt = lt;
+    a.lr = lr;
+    a.mask = mask;
+    a.off = off;
+    a.B = B;
+    a.T = T;
+    RcPrep& q = a.q;
+    q.use_tis = p->use_tis != 0;
+    q.mode = p->tis_mode;
+    q.level = p->tis_level;
+    q.norm = p->tis_batch_normalize != 0;
+    q.use_rs = p->use_rs != 0;
+    q.rs_level = p->rs_level;
+    q.L = p->tis_lower_bound;
+    q.U = p->tis_upper_bound;
+    q.rsL = std::isnan(p->rs_lower_bound) ? q.L : p->rs_lower_bound;
+    q.rsU = std::isnan(p->rs_upper_bound) ? q.U : p->rs_upper_bound;
+    q.veto = p->rs_veto_threshold > 0.f;   // NaN compares false: no veto
+    q.lnL = ln_ff(q.L);
+    q.lnU = ln_ff(q.U);
+    q.lnRsL = ln_ff(q.rsL);
+    q.lnRsU = ln_ff(q.rsU);
+    q.lnVeto = ln_ff(q.veto ? p->rs_veto_threshold : 0.0);
+    a.w = w;
+    a.keep = keep;
+    uint8_t* base = static_cast<uint8_t*>(ws);
+    a.status = reinterpret_cast<int32_t*>(base + 4);
+    a.factor = reinterpret_cast<float*>(base + 8);
+    uint8_t* rec = base + kRcHeader;
+    a.pd = reinterpret_cast<double*>(rec);
+    a.pc = reinterpret_cast<long long*>(a.pd + kRcD * B);
+    a.pmin = reinterpret_cast<float*>(a.pc + kRcC * B);
+    a.pmax = a.pmin + B;
+    a.metrics = metrics;
+    ProfScope ps(RL_PROF_ROLLOUT, stream);
+    if (cudaMemsetAsync(ws, 0, 16, stream) != cudaSuccess) return RL_ERR_CUDA;
+    int launches = 0;
+    if (B > 0) {
+        rc_seq_kernel<<<static_cast<unsigned>(B), kRcThreads, 0, stream>>>(a);
+        ++launches;
+    }
+    rc_reduce_kernel<<<1, kRcReduceThreads, 0, stream>>>(a);
+    ++launches;
+    if (q.use_tis && q.norm && w != nullptr && T > 0) {
+        const int64_t blocks = (T / 4 + 255) / 256 + 1;
+        const int64_t cap = 4L * num_sms();
+        rc_scale_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, stream>>>(w, T, a.factor);
+        ++launches;
+    }
+    count_launch(launches);
+    return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
+}  // namespace rl

@@ -235,6 +235,6 @@ extern "C" const char* rl_profile_kind_name(int kind) {
     static const char* names[RL_PROF_KINDS] = {
         "validate", "gemm_fwd_stats", "token_loss", "metrics", "transpose", "gemm_bwd_grad",
         "gemm_bwd_dx", "gemm_bwd_dw", "sparse_dx", "sparse_dw", "policy", "gemm_util", "memset", "other",
-        "spike_resid", "grad_from_e", "ref_logit"};
+        "spike_resid", "grad_from_e", "ref_logit", "rollout"};
     return (kind >= 0 && kind < RL_PROF_KINDS) ? names[kind] : "unknown";
 }

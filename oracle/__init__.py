@@ -9,7 +9,8 @@ Every function cites the page and section it restates.  The pages:
   * "IPO (INTELLECT Policy Optimization)" (prime-rl docs): "Masking by Probability,
     Not Ratio", "Choosing eps".
   * "Rollout Correction Methods" (miles docs): "Algorithms" (standard / bypass /
-    decoupled 3-policy PPO), "Importance Sampling", "Mismatch Metrics".
+    decoupled 3-policy PPO), "Config keys", "Importance Sampling", "Rejection Sampling",
+    "Mismatch Metrics".
   * "10-KL-clip-entropy" (verl blog): section 2 (PPO clip, dual clip, clip metrics,
     default constants).
   * prime-rl pull request #4233 ("One RL loss for ipo, icepop and the new reinforce"):
@@ -25,6 +26,7 @@ from .rl_head import (HeadParams, LOSS_IPO, LOSS_ICEPOP, LOSS_REINFORCE, KL_EXAC
                       STALE_NONE, STALE_INV_SQRT, head_forward, head_backward, head_loss_total,
                       head_token_logits, token_forward)
 from .policy import PolicyParams, policy_loss_elementwise, IPO_CURVE_EPS
+from .rollout import RolloutParams, rollout_correction, rollout_metrics_named
 
 PARITY_UNPINNED = (
     "mask_tv metric: the pages name it without a definition; reading R9 "
@@ -32,10 +34,13 @@ PARITY_UNPINNED = (
     "kl_staleness=inv_sqrt: the pages name it without a formula; reading R6 "
     "beta_t = kl_coeff / sqrt(1 + age_t) is consistency-checked only",
     "decoupled TIS bound: the pages give no value; reading R11 (token-level truncate at 2.0)",
+    "rollout correction defaults: the pages give no bound values; tests set every bound "
+    "explicitly, and the defaults (tis bounds [0.5, 2.0]) are a reading only",
 )
 
 __all__ = [
     "HeadParams", "LOSS_IPO", "LOSS_ICEPOP", "LOSS_REINFORCE", "KL_EXACT", "KL_K1", "STALE_NONE",
     "STALE_INV_SQRT", "head_forward", "head_backward", "head_loss_total", "head_token_logits",
     "token_forward", "PolicyParams", "policy_loss_elementwise", "IPO_CURVE_EPS", "PARITY_UNPINNED",
+    "RolloutParams", "rollout_correction", "rollout_metrics_named",
 ]

@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_struct_sizes_match_the_header_layout():
     assert ctypes.sizeof(rh.RlParams) == 14 * 4
     assert ctypes.sizeof(rh.RlHeadMetrics) == 8 * 8 + 6 * 8
-    assert ctypes.sizeof(rh.RlPgMetrics) == 6 * 8 + 6 * 8 + 16 * 8
+    assert ctypes.sizeof(rh.RlPgMetrics) == 6 * 8 + 6 * 8 + 16 * 8 + 8   # ..., ipo_curve[16], status
 
 
 def test_workspace_queries(lib):

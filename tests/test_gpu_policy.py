@@ -28,15 +28,25 @@ def _oracle_pp(pp: rh.PgParams):
                                curve_eps=tuple(f32(e) for e in pp.curve_eps))
 
 
-def _run(lt, lo, ls, A, m, pp):
-    d = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (lt, lo, ls, A, m)]
+def _dev(x, offset):
+    """x on the device, starting offset elements past the start of its allocation."""
+    x = np.ascontiguousarray(x)
+    buf = torch.empty(x.size + offset, dtype=torch.from_numpy(x[:0]).dtype, device="cuda")
+    view = buf[offset:]
+    view.copy_(torch.from_numpy(x))
+    return view
+
+
+def _run(lt, lo, ls, A, m, pp, offset=0):
+    d = [_dev(x, offset) for x in (lt, lo, ls, A, m)]
     out = rh.rl_policy_loss_elementwise(*d, pp)
     torch.cuda.synchronize()
     return [o.cpu().double().numpy() for o in out[:4]], rh.pg_metrics(out[4], len(pp.curve_eps))
 
 
-def _compare(lt, lo, ls, A, m, pp):
-    (lp, ld, gp, gd), gm = _run(lt, lo, ls, A, m, pp)
+def _compare(lt, lo, ls, A, m, pp, offset=0):
+    (lp, ld, gp, gd), gm = _run(lt, lo, ls, A, m, pp, offset)
+    assert gm["status"] == 0
     ref = oracle.policy_loss_elementwise(lt, lo, ls, A, m, _oracle_pp(pp))
     rm = ref["metrics"]
     for g, k in ((lp, "loss_ppo"), (ld, "loss_dec"), (gp, "grad_ppo"), (gd, "grad_dec")):
@@ -62,8 +72,10 @@ def test_c5_full_size():
     assert gm["n_valid"] == 1_800_000
 
 
-@pytest.mark.parametrize("T", [1, 3, 5, 1001])
+@pytest.mark.parametrize("T", [1, 3, 5, 16, 1001, 1024 * 304 * 3 + 7])
 def test_ragged_and_scalar_path(T):
+    """Lengths below one 16-slot group, a ragged tail after whole groups, and several ring
+    stages per block of the streaming pass."""
     rng = np.random.default_rng(T)
     lt = rng.normal(-1, 0.5, T).astype(np.float32)
     lo = (lt + rng.normal(0, 0.3, T)).astype(np.float32)
@@ -92,7 +104,7 @@ def test_exact_threshold_ties_are_bit_exact():
 
 def _band_case(T, frac, seed):
     """Random tokens, with a fraction frac placed on the clip boundary r = 1 - 0.2 (within
-    fp32 rounding), where every decision is re-taken in fp64."""
+    fp32 rounding), where every decision is re-taken exactly."""
     rng = np.random.default_rng(seed)
     ls = np.log(1.0 / (1.0 + np.exp(-rng.normal(-1, 2.5, T)))).astype(np.float32)
     lo = (ls + rng.normal(0, 0.3, T)).astype(np.float32)
@@ -106,7 +118,7 @@ def _band_case(T, frac, seed):
 
 
 def test_many_band_tokens_fixup_path():
-    """About 10% of 20000 tokens sit on a clip threshold: all of them go through the fp64
+    """About 10% of 20000 tokens sit on a clip threshold: all of them go through the exact
     fix-up list (below its 4096-entry floor) and every count stays exact."""
     _compare(*_band_case(20000, 0.1, 5), rh.PgParams())
 
@@ -135,3 +147,17 @@ def test_curve_band_tokens_exact():
     m = (rng.random(T) < 0.9).astype(np.uint8)
     f = lambda x: np.asarray(x, np.float32)
     _compare(f(lt), f(lo), f(ls), f(A), m, rh.PgParams())
+
+
+@pytest.mark.parametrize("offset", [1, 2])
+def test_unaligned_inputs_take_the_exact_pass(offset):
+    """Inputs that start 4 or 8 bytes past a 16-byte boundary cannot be bulk-copied: the
+    scalar pass with exact decisions in the bands takes them, with the same results."""
+    rng = np.random.default_rng(40 + offset)
+    T = 50_001
+    lt = rng.normal(-1, 0.5, T).astype(np.float32)
+    lo = (lt + rng.normal(0, 0.3, T)).astype(np.float32)
+    ls = (lo + rng.normal(0, 0.5, T)).astype(np.float32)
+    A = rng.normal(0, 1, T).astype(np.float32)
+    m = (rng.random(T) < 0.8).astype(np.uint8)
+    _compare(lt, lo, ls, A, m, rh.PgParams(), offset=offset)

@@ -1,0 +1,145 @@
+"""GPU parity of the rollout-correction path (IS / RS weights at token, sequence and
+geometric level, the veto, batch normalisation, mismatch metrics) through the C ABI,
+against the fp64 oracle, on the 1.8M-token synthetic replay (padded rows as sequences)
+and on packed, ragged and degenerate layouts.
+
+Bars: keep flags and every count bit-exact (the decisions are exact predicates on the
+fp32 inputs on both sides); weights within 4e-6 relative (an fp32 exponential of an
+exact log-ratio, times an fp32 factor); sums within 1e-5 relative plus 1e-6 per term
+(fp32 terms summed per sequence, then in fp64)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import lm_head_gb300 as rh
+import workloads
+from oracle.rollout import RolloutParams, rollout_correction
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from lm_head_gb300 import build
+    build.build()
+    rh.load()
+
+
+def _oracle_params(p: rh.RcParams) -> RolloutParams:
+    f = lambda x: None if x is None else float(np.float32(x))
+    return RolloutParams(use_tis=p.use_tis, tis_mode=p.tis_mode, tis_lower_bound=f(p.tis_lower_bound),
+                         tis_upper_bound=f(p.tis_upper_bound), tis_level=p.tis_level,
+                         tis_batch_normalize=p.tis_batch_normalize, use_rs=p.use_rs,
+                         rs_lower_bound=f(p.rs_lower_bound), rs_upper_bound=f(p.rs_upper_bound),
+                         rs_level=p.rs_level, rs_veto_threshold=f(p.rs_veto_threshold))
+
+
+def _run(lt, lr, m, off, p):
+    d = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (lt, lr, m, np.asarray(off, np.int64))]
+    w, k, met = rh.rl_rollout_correction(*d, p)
+    torch.cuda.synchronize()
+    return w.cpu().double().numpy(), k.cpu().numpy(), rh.rc_metrics(met)
+
+
+def _compare(lt, lr, m, off, p):
+    w, k, gm = _run(lt, lr, m, off, p)
+    ref = rollout_correction(lt, lr, m, off, _oracle_params(p))
+    rm = ref["metrics"]
+    assert gm["status"] == 0
+    np.testing.assert_array_equal(k, ref["keep"])
+    rw = ref["weights"]
+    assert np.all(np.abs(w - rw) <= 4e-6 * np.abs(rw) + 1e-30), float(np.max(np.abs(w - rw) / np.maximum(np.abs(rw), 1e-30)))
+    for key in ("n_valid", "n_seq", "n_kept", "n_tis_low", "n_tis_high", "n_rs_low", "n_rs_high", "n_cat_tokens",
+                "n_cat_seqs"):
+        assert gm[key] == rm[key], (key, gm[key], rm[key])
+    nv, ns = max(rm["n_valid"], 1), max(rm["n_seq"], 1)
+    tok_terms = ("w_before_sum", "w_after_sum", "kept_w_sum", "final_sum", "mis_kl_sum", "k3_sum", "abs_diff_sum",
+                 "chi2_token_sum")
+    seq_terms = ("train_lppl_sum", "rollout_lppl_sum", "lppl_diff_sum", "lppl_abs_diff_sum", "ppl_ratio_sum",
+                 "chi2_seq_sum")
+    for key in tok_terms + seq_terms:
+        n = nv if key in tok_terms else ns
+        g, r = gm[key], rm[key]
+        if math.isinf(r):
+            assert g == r, key
+            continue
+        assert abs(g - r) <= 1e-5 * abs(r) + 1e-6 * n, (key, g, r)
+    for key in ("batch_norm_factor", "final_min", "final_max"):
+        assert gm[key] == pytest.approx(rm[key], rel=4e-6, abs=1e-30), key
+    return gm, rm
+
+
+def _c5():
+    c = workloads.make_policy_case()
+    B = len(c.seq_lens)
+    off = np.arange(B + 1, dtype=np.int64) * c.max_len
+    return c.lp_old, c.lp_samp, c.mask, off
+
+
+CONFIGS = [
+    rh.RcParams(),                                                            # token, truncate
+    rh.RcParams(tis_mode="clip", tis_level="sequence", tis_lower_bound=0.1, tis_upper_bound=10.0,
+                tis_batch_normalize=True, use_rs=True, rs_level="geometric", rs_lower_bound=0.9,
+                rs_upper_bound=1.1, rs_veto_threshold=1e-4),
+    rh.RcParams(tis_mode="mask", tis_level="geometric", tis_lower_bound=0.95, tis_upper_bound=1.05,
+                use_rs=True, rs_level="sequence", rs_lower_bound=0.8, rs_upper_bound=1.3, rs_veto_threshold=1e-3),
+    rh.RcParams(use_tis=False, use_rs=True, rs_level="token", rs_lower_bound=0.5, rs_upper_bound=2.0),
+    rh.RcParams(tis_mode="clip", tis_batch_normalize=True, rs_veto_threshold=0.05),
+]
+
+
+@pytest.mark.parametrize("cfg", range(len(CONFIGS)))
+def test_c5_full_size(cfg):
+    """879 padded rows of up to 4096 tokens, 1.8M response tokens, five knob settings."""
+    gm, rm = _compare(*_c5(), CONFIGS[cfg])
+    assert gm["n_valid"] == 1_800_000
+
+
+def test_packed_ragged_sequences_and_empty_ones():
+    """Packed layout (cumulative lengths), lengths 0..700 with empty and fully masked
+    sequences, T not a multiple of anything in particular."""
+    rng = np.random.default_rng(11)
+    lens = rng.integers(0, 700, size=97)
+    lens[[3, 40, 41]] = 0
+    T = int(lens.sum())
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    lr = np.log(rng.random(T) * 0.98 + 0.01).astype(np.float32)
+    lt = (lr + rng.normal(0, 0.2, T)).astype(np.float32)
+    lt = np.minimum(lt, 0).astype(np.float32)
+    m = (rng.random(T) < 0.85).astype(np.uint8)
+    m[off[10]:off[11]] = 0
+    for p in CONFIGS:
+        _compare(lt, lr, m, off, p)
+
+
+def test_exact_bounds_and_single_long_sequence():
+    """Token log-ratios on and one float step around ln(bound) for every bound, in one
+    sequence of 40000 tokens (one block walks it)."""
+    vals = []
+    for bnd in (0.5, 2.0, 0.9, 1.1):
+        x = np.float32(np.log(bnd))
+        vals += [np.nextafter(x, np.float32(-np.inf)), x, np.nextafter(x, np.float32(np.inf))]
+    T = 40000
+    rng = np.random.default_rng(12)
+    d = rng.normal(0, 0.3, T).astype(np.float32)
+    d[:len(vals)] = vals
+    lr = np.full(T, -2.0, np.float32)
+    lt = (lr + d).astype(np.float32)
+    m = np.ones(T, np.uint8)
+    for p in (rh.RcParams(tis_mode="mask"), rh.RcParams(use_rs=True, rs_lower_bound=0.9, rs_upper_bound=1.1),
+              rh.RcParams(tis_mode="clip", tis_level="geometric", use_rs=True, rs_level="sequence")):
+        _compare(lt, lr, m, [0, T], p)
+
+
+def test_bad_offsets_set_the_status_bit():
+    T = 1000
+    lt = np.zeros(T, np.float32)
+    off = torch.tensor([0, 600, 400, T], dtype=torch.int64, device="cuda")   # decreasing
+    w, k, met = rh.rl_rollout_correction(torch.zeros(T, device="cuda"), torch.zeros(T, device="cuda"),
+                                         torch.ones(T, dtype=torch.uint8, device="cuda"), off, rh.RcParams())
+    torch.cuda.synchronize()
+    assert rh.rc_metrics(met)["status"] & 0x1
