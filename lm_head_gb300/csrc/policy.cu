@@ -87,6 +87,8 @@ struct PgArgs {
     float* grad_ppo;
     float* grad_dec;
     long long* acc;               // [kPgFields] the batch's sums (2^-24 fixed point) and counts
+    int* range;                   // set when a sum term is too large for the fixed point
+    float range_lim;              // |term| bound that keeps every accumulator inside int64
     int nb;                       // blocks of the pass
     int* count;                   // global spill list: length (may exceed cap: overflow)
     int* done;                    // blocks that have written their partial
@@ -283,6 +285,14 @@ RL_DEVINL void pg_write_metric(int k, double s, rl_pg_metrics* out) {
     }
 }
 
+// A sum term in 2^-24 fixed point, or 0 with the range flag raised when |v| is at or past
+// the bound that keeps the batch's accumulators inside int64 (or v is not finite).
+RL_DEVINL long long pg_fix(const PgArgs& a, float v) {
+    if (fabsf(v) < a.range_lim) return __float2ll_rn(v * kPgFix);
+    atomicOr(a.range, 1);
+    return 0;
+}
+
 // Exact-path tokens list[0, n), kPgBandRows at a time (thread i < kPgBandRows takes one
 // and fills its shared-memory row: sums in 2^-24 fixed point, counts), then thread
 // k < kPgFields adds column k into fix[k] (shared).  Integer sums are exact, so the order
@@ -304,7 +314,7 @@ RL_DEVINL void pg_band_tokens(const PgArgs& a, const int* list, int n, long long
                 if (a.loss_dec) a.loss_dec[t] = o[1];
                 if (a.grad_ppo) a.grad_ppo[t] = o[2];
                 if (a.grad_dec) a.grad_dec[t] = o[3];
-                for (int f = 0; f < kPgSums; ++f) row[f] = __float2ll_rn(one.sum[f] * kPgFix);
+                for (int f = 0; f < kPgSums; ++f) row[f] = pg_fix(a, one.sum[f]);
                 for (int f = 0; f < kPgCounts; ++f) row[kPgSums + f] = one.cnt[f];
             } else {
                 for (int f = 0; f < kPgFields; ++f) row[f] = 0;
@@ -325,18 +335,25 @@ RL_DEVINL void pg_band_tokens(const PgArgs& a, const int* list, int n, long long
 // ----------------------------------------------------------------------------------
 // A block's partial goes into the batch accumulators with integer atomics (sums in 2^-24
 // fixed point, counts as they are): integer addition does not depend on the order the
-// blocks arrive in, so the totals are reproducible.  v: this field's value (thread k < kPgFields).
+// blocks arrive in, so the totals are reproducible.  A sum too large for the fixed point
+// raises the range flag instead, and the last block then redoes the metrics (below).
 RL_DEVINL void pg_add_partial(const PgArgs& a, int k, float sum, long long count) {
-    const long long x = k < kPgSums ? __float2ll_rn(sum * kPgFix) + count : count;
+    const long long x = k < kPgSums ? pg_fix(a, sum) + count : count;
     if (x != 0) atomicAdd(reinterpret_cast<unsigned long long*>(a.acc + k), static_cast<unsigned long long>(x));
 }
 
 // The last block of the pass to finish: the spill list's tokens, then the accumulators
-// into the metrics.  If the spill list overflowed, the whole batch again with exact
-// decisions instead (slow, correct).  Called by every thread of the last block.
+// into the metrics.  If the spill list overflowed, or a sum term was too large for the
+// fixed point, the whole batch again with exact decisions and fp32 sums instead (one
+// block: slow, correct).  Called by every thread of the last block.
 RL_DEVINL void pg_final(const PgArgs& a) {
     const int cnt = __ldcg(a.count);
-    if (cnt > a.cap) {
+    __shared__ long long fix[kPgFields];
+    if (threadIdx.x < kPgFields) fix[threadIdx.x] = 0;
+    __syncthreads();
+    if (cnt > 0 && cnt <= a.cap) pg_band_tokens(a, a.list, cnt, fix);
+    __syncthreads();
+    if (cnt > a.cap || __ldcg(a.range) != 0) {
         PgAcc acc;
         pg_zero(acc);
         pg_exact_pass(a, threadIdx.x, blockDim.x, acc);
@@ -351,10 +368,6 @@ RL_DEVINL void pg_final(const PgArgs& a) {
         if (a.metrics && threadIdx.x == 0) a.metrics->status = __ldcg(a.status);
         return;
     }
-    __shared__ long long fix[kPgFields];
-    if (threadIdx.x < kPgFields) fix[threadIdx.x] = 0;
-    __syncthreads();
-    if (cnt > 0) pg_band_tokens(a, a.list, cnt, fix);
     if (!a.metrics) return;
     const int k = threadIdx.x;
     if (k < kPgFields) {
@@ -529,6 +542,7 @@ __global__ void __launch_bounds__(kPgThreads + 64, kPgFastPerSm) policy_fast_ker
     __shared__ int cons_done;                      // consumer warps past their last listing
     __shared__ int abort_flag;
     __shared__ long long bfix[kPgFields];
+    __shared__ long long xrow[32][kPgFields];      // the exact warp's per-lane fixed-point sums
 
     const int64_t n16 = a.T >> 4;
     const int64_t nstages = (n16 * 16 + kPgStageSlots - 1) / kPgStageSlots;
@@ -553,6 +567,7 @@ __global__ void __launch_bounds__(kPgThreads + 64, kPgFastPerSm) policy_fast_ker
         for (int b = 0; b <= a.q.n; ++b) hist_s[b * kPgThreads + threadIdx.x] = 0;
     for (int i = threadIdx.x; i < kPgBlockBand; i += blockDim.x) blist[i] = -1;
     if (threadIdx.x < kPgFields) bfix[threadIdx.x] = 0;
+    for (int i = threadIdx.x; i < 32 * kPgFields; i += blockDim.x) (&xrow[0][0])[i] = 0;
     __syncthreads();
 
     PgFastAcc acc;
@@ -597,13 +612,9 @@ __global__ void __launch_bounds__(kPgThreads + 64, kPgFastPerSm) policy_fast_ker
                         if (a.loss_dec) a.loss_dec[t] = o[1];
                         if (a.grad_ppo) a.grad_ppo[t] = o[2];
                         if (a.grad_dec) a.grad_dec[t] = o[3];
-                        for (int f = 0; f < kPgSums; ++f)
-                            atomicAdd(reinterpret_cast<unsigned long long*>(bfix + f),
-                                      static_cast<unsigned long long>(__float2ll_rn(one.sum[f] * kPgFix)));
-                        for (int f = 0; f < kPgCounts; ++f)
-                            if (one.cnt[f] != 0)
-                                atomicAdd(reinterpret_cast<unsigned long long*>(bfix + kPgSums + f),
-                                          static_cast<unsigned long long>(one.cnt[f]));
+                        long long* row = xrow[lane];
+                        for (int f = 0; f < kPgSums; ++f) row[f] += pg_fix(a, one.sum[f]);
+                        for (int f = 0; f < kPgCounts; ++f) row[kPgSums + f] += one.cnt[f];
                     } else {
                         set_status(a.status, RL_STATUS_TIMEOUT);
                     }
@@ -718,6 +729,11 @@ __global__ void __launch_bounds__(kPgThreads + 64, kPgFastPerSm) policy_fast_ker
         if (lane == 0) atomicAdd(&cons_done, 1);
     }
     __syncthreads();
+    if (threadIdx.x < kPgFields) {   // the exact warp's rows, in lane order
+        long long v = 0;
+        for (int l = 0; l < 32; ++l) v += xrow[l][threadIdx.x];
+        bfix[threadIdx.x] = v;
+    }
     // block partial: warp trees (fp32 sums, exact int32 counts), then the 8 consumer warps
     // in order plus the band tokens' fixed-point terms, into the batch accumulators; the
     // curve counts from the histogram, cnt_k = #(j > k), back in the caller's order
@@ -768,12 +784,14 @@ __global__ void __launch_bounds__(kPgThreads + 64, kPgFastPerSm) policy_fast_ker
 // ----------------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------------
-// Workspace: a 256-byte header (spill-list length, arrival count, status word, and at
-// byte 16 the kPgFields accumulators), then the spill list in whatever room is left.
+// Workspace: a 256-byte header (spill-list length, arrival count, status word, range
+// flag, and at byte 16 the kPgFields accumulators), then the spill list in whatever room
+// is left.
 struct PgWs {
     int* count;
     int* done;
     int32_t* status;
+    int* range;
     long long* acc;
     int* list;
     int cap;
@@ -790,6 +808,7 @@ static PgWs pg_ws(void* ws, size_t ws_bytes) {
     w.count = reinterpret_cast<int*>(b);
     w.done = reinterpret_cast<int*>(b + 4);
     w.status = reinterpret_cast<int32_t*>(b + 8);
+    w.range = reinterpret_cast<int*>(b + 12);
     w.acc = reinterpret_cast<long long*>(b + 16);
     w.list = reinterpret_cast<int*>(b + kPgHeader);
     const size_t room = ws_bytes > kPgHeader ? (ws_bytes - kPgHeader) / sizeof(int) : 0;
@@ -871,6 +890,7 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
     a.list = w.list;
     a.cap = w.cap;
     a.acc = w.acc;
+    a.range = w.range;
     a.metrics = metrics;
     static int smem_set[64] = {0};   // per device: the fast pass's shared-memory opt-in
     int dev = 0;
@@ -884,11 +904,12 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
     ProfScope ps(RL_PROF_POLICY, stream);
     // spill count, arrival count, status, accumulators
     if (cudaMemsetAsync(ws, 0, kPgHeader, stream) != cudaSuccess) return RL_ERR_CUDA;
+    a.nb = fast ? fast_blocks(sms) - 1 : slow_blocks(sms);   // fast: odd, see policy_fast_kernel
+    // a term below 2^38 / nb keeps each accumulator's total below 2^62 in 2^-24 units
+    a.range_lim = ldexpf(1.f, 38) / static_cast<float>(a.nb);
     if (fast) {
-        a.nb = fast_blocks(sms) - 1;   // odd: see policy_fast_kernel
         policy_fast_kernel<<<a.nb, kPgThreads + 64, kPgStreamSmem, stream>>>(a);
     } else {
-        a.nb = slow_blocks(sms);
         policy_slow_kernel<<<a.nb, kPgThreads, 0, stream>>>(a);
     }
     count_launch(1);

@@ -100,15 +100,16 @@ struct RcSeq {   // one sequence's decisions (thread 0 -> block)
     float wseq;
 };
 
-// A sequence is walked in tiles of kRcTile tokens: thread t takes tokens
-// o0 + kRcTile k + kRcThreads j + t, j < kRcPer (coalesced loads, no alignment needed).
-// The first kRcCached tiles stay in registers between the two passes.
-constexpr int kRcPer = 4;
-constexpr int kRcTile = kRcThreads * kRcPer;
-constexpr int kRcCached = 4;
+// A sequence is staged in shared memory kRcChunk tokens at a time (coalesced loads,
+// no alignment needed); a sequence of at most kRcChunk tokens is read from memory once
+// for both passes, a longer one chunk by chunk in each pass.  Loops stay rolled: the
+// code is fetched cold by every block, so its size is part of the latency.
+constexpr int kRcChunk = 4096;
 constexpr int kRcW = kRcThreads / 32;
 
-__global__ void __launch_bounds__(kRcThreads) rc_seq_kernel(RcArgs a) {
+__global__ void __launch_bounds__(kRcThreads, 4) rc_seq_kernel(RcArgs a) {
+    __shared__ float s_lt[kRcChunk], s_lr[kRcChunk];
+    __shared__ uint8_t s_m[kRcChunk];
     __shared__ FF shff[kRcW][4];
     __shared__ float shf[kRcW][5];
     __shared__ int shi[kRcW][6];
@@ -124,34 +125,39 @@ __global__ void __launch_bounds__(kRcThreads) rc_seq_kernel(RcArgs a) {
         o1 = o1 < o0 ? o0 : (o1 > a.T ? a.T : o1);
     }
     const bool rs_seq = q.use_rs && q.rs_level == RL_LEVEL_SEQUENCE;
-    const int ntiles = static_cast<int>((o1 - o0 + kRcTile - 1) / kRcTile);
+    const int64_t len = o1 - o0;
+    const int nchunks = static_cast<int>((len + kRcChunk - 1) / kRcChunk);
+    auto stage = [&](int c) {   // chunk c into shared memory; returns its length
+        const int64_t c0 = o0 + static_cast<int64_t>(c) * kRcChunk;
+        const int n = static_cast<int>(o1 - c0 < kRcChunk ? o1 - c0 : kRcChunk);
+#pragma unroll 4
+        for (int i = threadIdx.x; i < n; i += kRcThreads) {
+            s_lt[i] = a.lt[c0 + i];
+            s_lr[i] = a.lr[c0 + i];
+            s_m[i] = a.mask[c0 + i];
+        }
+        __syncthreads();
+        return n;
+    };
 
-    // pass 1: the sequence's sums; the first tiles' inputs kept in registers
-    float clt[kRcCached][kRcPer], clr[kRcCached][kRcPer];
-    uint32_t cm[kRcCached];
+    // pass 1: the sequence's sums
     int n = 0, cat = 0;
     FF S = {0.f, 0.f}, St = {0.f, 0.f}, Sr = {0.f, 0.f}, E = {0.f, 0.f};
     float mis = 0.f, k3 = 0.f, ad = 0.f, c2 = 0.f;
-    auto load_tile = [&](int k, float (&lt)[kRcPer], float (&lr)[kRcPer], uint32_t& m) {
-        m = 0;
-#pragma unroll
-        for (int j = 0; j < kRcPer; ++j) {
-            const int64_t i = o0 + static_cast<int64_t>(k) * kRcTile + j * kRcThreads + threadIdx.x;
-            const bool in = i < o1;
-            lt[j] = in ? a.lt[i] : 0.f;
-            lr[j] = in ? a.lr[i] : 0.f;
-            m |= (in && a.mask[i] != 0 ? 1u : 0u) << j;
-        }
-    };
-    auto stats = [&](const float (&lt)[kRcPer], const float (&lr)[kRcPer], uint32_t m) {
-#pragma unroll
-        for (int j = 0; j < kRcPer; ++j) {
-            if (!((m >> j) & 1u)) continue;
-            const FF d = two_sum(lt[j], -lr[j]);
+    int staged = -1;
+    for (int c = 0; c < nchunks; ++c) {
+        if (c > 0) __syncthreads();   // the previous chunk's readers are done
+        const int cn = stage(c);
+        staged = c;
+#pragma unroll 1
+        for (int i = threadIdx.x; i < cn; i += kRcThreads) {
+            if (s_m[i] == 0) continue;
+            const float x = s_lt[i], y = s_lr[i];
+            const FF d = two_sum(x, -y);
             ++n;
             S = ff_add(S, d);
-            St = ff_add(St, {lt[j], 0.f});
-            Sr = ff_add(Sr, {lr[j], 0.f});
+            St = ff_add(St, {x, 0.f});
+            Sr = ff_add(Sr, {y, 0.f});
             if (rs_seq) E = ff_add(E, exp_ff2(d));
             if (q.veto) cat += ff_lt(d, q.lnVeto) ? 1 : 0;
             const float df = d.hi;
@@ -161,19 +167,6 @@ __global__ void __launch_bounds__(kRcThreads) rc_seq_kernel(RcArgs a) {
             ad += fabsf(df);
             c2 += ed * ed;
         }
-    };
-#pragma unroll
-    for (int k = 0; k < kRcCached; ++k) {
-        if (k < ntiles) load_tile(k, clt[k], clr[k], cm[k]);
-        else cm[k] = 0;
-    }
-#pragma unroll
-    for (int k = 0; k < kRcCached; ++k) stats(clt[k], clr[k], cm[k]);
-    for (int k = kRcCached; k < ntiles; ++k) {
-        float lt[kRcPer], lr[kRcPer];
-        uint32_t m;
-        load_tile(k, lt, lr, m);
-        stats(lt, lr, m);
     }
     {
         const FF w4[4] = {warp_sum_ff(S), warp_sum_ff(St), warp_sum_ff(Sr), rs_seq ? warp_sum_ff(E) : FF{0.f, 0.f}};
@@ -244,18 +237,27 @@ __global__ void __launch_bounds__(kRcThreads) rc_seq_kernel(RcArgs a) {
     __syncthreads();
     const RcSeq s = sq;
 
-    // pass 2: weights and keep flags
+    // pass 2: weights and keep flags (the staged chunk is reused when it is the only one)
     float wb_sum = 0.f, kept_sum = 0.f, wraw_sum = 0.f, mn = INFINITY, mx = -INFINITY;
     int kept = 0, tlo = 0, thi = 0, rlo = 0, rhi = 0;
-    auto weights = [&](int k, const float (&lt)[kRcPer], const float (&lr)[kRcPer], uint32_t m) {
-#pragma unroll
-        for (int j = 0; j < kRcPer; ++j) {
-            const int64_t i = o0 + static_cast<int64_t>(k) * kRcTile + j * kRcThreads + threadIdx.x;
-            if (i >= o1) continue;
+    // the last chunk of pass 1 is still staged: take the chunks from the last one down
+    for (int c = nchunks - 1; c >= 0; --c) {
+        int cn;
+        if (c == staged) {
+            const int64_t rest = len - static_cast<int64_t>(c) * kRcChunk;
+            cn = static_cast<int>(rest < kRcChunk ? rest : kRcChunk);
+        } else {
+            __syncthreads();
+            cn = stage(c);
+            staged = c;
+        }
+        const int64_t c0 = o0 + static_cast<int64_t>(c) * kRcChunk;
+#pragma unroll 1
+        for (int i = threadIdx.x; i < cn; i += kRcThreads) {
             float wout = 0.f;
             uint8_t kp8 = 0;
-            if ((m >> j) & 1u) {
-                const FF d = two_sum(lt[j], -lr[j]);
+            if (s_m[i] != 0) {
+                const FF d = two_sum(s_lt[i], -s_lr[i]);
                 float w;
                 bool lo, hi;
                 if (q.level == RL_LEVEL_TOKEN) {
@@ -299,18 +301,9 @@ __global__ void __launch_bounds__(kRcThreads) rc_seq_kernel(RcArgs a) {
                     mx = fmaxf(mx, wb);
                 }
             }
-            if (a.w) a.w[i] = wout;
-            if (a.keep) a.keep[i] = kp8;
+            if (a.w) a.w[c0 + i] = wout;
+            if (a.keep) a.keep[c0 + i] = kp8;
         }
-    };
-#pragma unroll
-    for (int k = 0; k < kRcCached; ++k)
-        if (k < ntiles) weights(k, clt[k], clr[k], cm[k]);
-    for (int k = kRcCached; k < ntiles; ++k) {
-        float lt[kRcPer], lr[kRcPer];
-        uint32_t m;
-        load_tile(k, lt, lr, m);
-        weights(k, lt, lr, m);
     }
     {
         float f5[5] = {warp_sum_f(wb_sum), warp_sum_f(kept_sum), warp_sum_f(wraw_sum), mn, mx};
@@ -320,6 +313,7 @@ __global__ void __launch_bounds__(kRcThreads) rc_seq_kernel(RcArgs a) {
             f5[4] = fmaxf(f5[4], __shfl_xor_sync(0xffffffffu, f5[4], o));
         }
         const int i5[5] = {warp_sum_i(kept), warp_sum_i(tlo), warp_sum_i(thi), warp_sum_i(rlo), warp_sum_i(rhi)};
+        __syncthreads();   // the shared rows of pass 1 are read
         if (lane == 0) {
             for (int f = 0; f < 5; ++f) shf[warp][f] = f5[f];
             for (int f = 0; f < 5; ++f) shi[warp][f] = i5[f];

@@ -161,3 +161,20 @@ def test_unaligned_inputs_take_the_exact_pass(offset):
     A = rng.normal(0, 1, T).astype(np.float32)
     m = (rng.random(T) < 0.8).astype(np.uint8)
     _compare(lt, lo, ls, A, m, rh.PgParams(), offset=offset)
+
+
+def test_huge_sum_terms_take_the_exact_metric_pass():
+    """A few tokens with log pi_old - log pi_rollout = 30 (k3 terms near e^30): too large
+    for the fixed-point batch accumulators, so the last block redoes the metrics in fp32
+    over the whole batch; outputs and metrics still match the oracle."""
+    rng = np.random.default_rng(21)
+    T = 100_000
+    ls = np.log(rng.random(T) * 0.9 + 0.05).astype(np.float32)
+    lo = (ls + rng.normal(0, 0.2, T)).astype(np.float32)
+    lo = np.minimum(lo, -1e-6).astype(np.float32)
+    ls[::9999] = (lo[::9999] - 30.0).astype(np.float32)
+    lt = (lo + rng.normal(0, 0.1, T)).astype(np.float32)
+    A = rng.normal(0, 1, T).astype(np.float32)
+    m = np.ones(T, np.uint8)
+    gm, rm = _compare(lt, lo, ls, A, m, rh.PgParams())
+    assert rm["k3"] > 1e13
