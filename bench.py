@@ -504,7 +504,7 @@ def run_ours(args):
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of each kernel, from the ncu
 # captures summarised under profiles/ (one launch at the bench's 16384-token chunk).
-TRAFFIC = {"gemm_fwd_stats": 13573747712 + 9941863168}
+TRAFFIC = {"gemm_fwd_stats": 8134179328 + 9935567360}
 
 
 def ctypes_metrics_size(rh):

@@ -123,6 +123,16 @@ RL_DEVINL void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x, 
                  "r"(x), "r"(y), "r"(smem_addr(src))
                  : "memory");
 }
+// The same store with an L2 evict-first hint: for tiles written once and read much later
+// (by another kernel), so they do not push the operands still being reused out of L2.
+RL_DEVINL void tma_store_2d_evict_first(const CUtensorMap* map, const void* src, int32_t x, int32_t y) {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(smem_addr(src)), "l"(pol)
+                 : "memory");
+}
 RL_DEVINL void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N committed bulk groups still read their shared-memory source.
 template <int N>

@@ -303,8 +303,10 @@ struct EpiStats {
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && t < p.N) {   // lane 0 holds the warp's first row
-            tma_store_2d(&p.tmEb, stage, col0, static_cast<int32_t>(t));
-            tma_store_2d(&p.tmEbt, stage + 2048, static_cast<int32_t>(t), col0);
+            // evict-first: e is read only by the backward GEMMs, after this kernel; keeping
+            // it out of the way leaves L2 to the X and W tiles this kernel reuses
+            tma_store_2d_evict_first(&p.tmEb, stage, col0, static_cast<int32_t>(t));
+            tma_store_2d_evict_first(&p.tmEbt, stage + 2048, static_cast<int32_t>(t), col0);
             bulk_commit();
         }
     }

@@ -44,6 +44,7 @@ class HeadParams:
     kl_coeff: float = 0.0
     kl_estimator: int = KL_EXACT
     kl_staleness: int = STALE_NONE
+    entropy_coeff: float = 0.0          # "10-KL-clip-entropy" section 3: loss -= coeff * entropy
 
 
 def _logsumexp(x: np.ndarray) -> float:
@@ -137,6 +138,9 @@ def token_forward(z: np.ndarray, label: int, label_logq: float, adv: float, age:
         raise ValueError(f"unknown kl estimator {p.kl_estimator}")
     beta = kl_beta(age, p)
     loss = -p.adv_tau * adv * (w_lab * logP_lab - center) + beta * kl
+    # exploration regulariser ("10-KL-clip-entropy", section 3): policy_loss -= entropy_coeff
+    # * entropy, the token entropy of the full-vocabulary softmax of the logits
+    loss -= p.entropy_coeff * entropy
     ratio_ent = np.exp(logP_ent - logq)
     return dict(
         loss=loss, lse=lse, lse_s=lse_s, entropy=entropy, logp_label=logP_lab,
@@ -189,6 +193,11 @@ def token_grad_z(z: np.ndarray, label: int, adv: float, ids: np.ndarray, replaye
         else:
             d_kl = -dlogP(label)
         grad = grad + fwd["beta"] * d_kl
+    # d(-c H)/dz_j = c p_j (log p_j + H), p the full softmax (dH/dz_j = -p_j (log p_j + H))
+    logp_full = z - fwd["lse"]
+    pf = np.exp(logp_full)
+    if p.entropy_coeff != 0.0:
+        grad = grad + p.entropy_coeff * pf * (logp_full + fwd["entropy"])
     if not want_abs:
         return grad
     onehot_abs_c = np.zeros(V)
@@ -205,6 +214,8 @@ def token_grad_z(z: np.ndarray, label: int, adv: float, ids: np.ndarray, replaye
         else:
             mag = mag + fwd["beta"] * P
             mag[label] += fwd["beta"]
+    if p.entropy_coeff != 0.0:
+        mag = mag + p.entropy_coeff * pf * (np.abs(logp_full) + fwd["entropy"])
     return grad, mag
 
 

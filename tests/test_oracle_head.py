@@ -341,17 +341,18 @@ def _random_case(rng, N=6, H=5, V=9, mixed=True):
     return inp, T
 
 
-@pytest.mark.parametrize("loss_type,est,stale", [
-    (LOSS_IPO, KL_EXACT, oracle.STALE_INV_SQRT),
-    (LOSS_ICEPOP, KL_K1, oracle.STALE_NONE),
-    (LOSS_REINFORCE, KL_EXACT, oracle.STALE_NONE),
+@pytest.mark.parametrize("loss_type,est,stale,ent", [
+    (LOSS_IPO, KL_EXACT, oracle.STALE_INV_SQRT, 0.0),
+    (LOSS_ICEPOP, KL_K1, oracle.STALE_NONE, 0.0),
+    (LOSS_REINFORCE, KL_EXACT, oracle.STALE_NONE, 0.0),
+    (LOSS_IPO, KL_EXACT, oracle.STALE_NONE, 0.05),     # with the entropy regulariser
 ])
-def test_finite_differences(loss_type, est, stale):
+def test_finite_differences(loss_type, est, stale, ent):
     rng = np.random.default_rng(7 + loss_type)
     inp, T = _random_case(rng)
     hp = HeadParams(loss_type=loss_type, eps=0.15, max_importance_ratio=1.4, icepop_low=0.8,
                     icepop_high=1.25, adv_tau=0.9, temperature=T, kl_coeff=0.07,
-                    kl_estimator=est, kl_staleness=stale)
+                    kl_estimator=est, kl_staleness=stale, entropy_coeff=ent)
     N = inp["hidden"].shape[0]
     dloss = rng.normal(0, 1, N)
     base = oracle.head_forward(inp, hp)
@@ -395,3 +396,33 @@ def test_temperature_is_a_logit_scale():
     b = oracle.head_forward(inp2, HeadParams(temperature=2 * T, kl_coeff=0.05))
     np.testing.assert_allclose(a["loss"], b["loss"], rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(a["logp_support"], b["logp_support"], rtol=1e-12)
+
+
+def test_entropy_regulariser_closed_forms():
+    """"10-KL-clip-entropy", section 3: loss -= entropy_coeff * entropy.  Uniform logits:
+    the entropy is log V and a maximum (zero gradient), so the regulariser shifts the loss
+    by -c log V and adds nothing to the gradient; with non-uniform logits it adds
+    c p (log p + H), which sums to zero over the vocabulary (a softmax gradient)."""
+    V = 11
+    z = np.zeros(V)
+    base = dict(label=2, label_logq=math.log(1 / V), adv=0.7, age=0, ids=np.array([1, 2, 5]),
+                logq=np.log(np.full(3, 1 / V)), replayed=False)
+    p0 = HeadParams(kl_coeff=0.0)
+    p1 = HeadParams(kl_coeff=0.0, entropy_coeff=0.3)
+    f0 = oracle.token_forward(z, p=p0, **base)
+    f1 = oracle.token_forward(z, p=p1, **base)
+    assert f1["entropy"] == pytest.approx(math.log(V))
+    assert f1["loss"] - f0["loss"] == pytest.approx(-0.3 * math.log(V))
+    g0 = oracle.rl_head.token_grad_z(z, 2, 0.7, base["ids"], False, f0, p0)
+    g1 = oracle.rl_head.token_grad_z(z, 2, 0.7, base["ids"], False, f1, p1)
+    np.testing.assert_allclose(g1, g0, atol=1e-15)
+    z2 = np.linspace(-1.0, 2.0, V)
+    f0 = oracle.token_forward(z2, p=p0, **base)
+    f1 = oracle.token_forward(z2, p=p1, **base)
+    g0 = oracle.rl_head.token_grad_z(z2, 2, 0.7, base["ids"], False, f0, p0)
+    g1 = oracle.rl_head.token_grad_z(z2, 2, 0.7, base["ids"], False, f1, p1)
+    d = g1 - g0
+    pf = np.exp(z2 - f1["lse"])
+    assert abs(d.sum()) < 1e-14
+    # the entropy gradient points away from the most likely id (lowering its logit raises H)
+    assert d[np.argmax(pf)] > 0 > d[np.argmin(pf)]
