@@ -98,6 +98,12 @@ typedef struct rl_params {
     float temperature;            /* T > 0; logits are (W h) / T */
     float kl_coeff;               /* >= 0; default 0 */
     int32_t token_chunk;          /* backward token chunk (multiple of 128); 0 = library default */
+    float entropy_coeff;          /* >= 0; default 0.  "10-KL-clip-entropy", section 3: the
+                                     exploration regulariser, loss_t -= entropy_coeff * H_t with
+                                     H_t the full-vocabulary token entropy; its gradient is dense
+                                     over the vocabulary, so a nonzero value rules out the sparse
+                                     backward (RL_BWD_SPARSE then returns RL_ERR_ARG) and makes
+                                     the fused BF16 backward recompute the logits (8 N H V) */
 } rl_params;
 
 /* Ragged per-token sampler support, CSR over tokens ("TokenSupport", pull request #4233,

@@ -41,7 +41,8 @@ class RlParams(ctypes.Structure):
                 ("eps", ctypes.c_float), ("max_importance_ratio", ctypes.c_float),
                 ("icepop_low", ctypes.c_float), ("icepop_high", ctypes.c_float),
                 ("adv_tau", ctypes.c_float), ("temperature", ctypes.c_float),
-                ("kl_coeff", ctypes.c_float), ("token_chunk", ctypes.c_int32)]
+                ("kl_coeff", ctypes.c_float), ("token_chunk", ctypes.c_int32),
+                ("entropy_coeff", ctypes.c_float)]
 
 
 class RlSupport(ctypes.Structure):
@@ -202,12 +203,13 @@ class HeadParams:
     grad_precision: int = RL_GRAD_BF16
     all_replayed: int = 0
     token_chunk: int = 0
+    entropy_coeff: float = 0.0
 
     def c(self) -> RlParams:
         return RlParams(self.loss_type, self.kl_estimator, self.kl_staleness, self.bwd_mode,
                         self.grad_precision, self.all_replayed, self.eps, self.max_importance_ratio,
                         self.icepop_low, self.icepop_high, self.adv_tau, self.temperature,
-                        self.kl_coeff, self.token_chunk)
+                        self.kl_coeff, self.token_chunk, self.entropy_coeff)
 
 
 @dataclasses.dataclass

@@ -31,6 +31,9 @@ int check_params(const rl_params* p) {
     if (!(p->temperature > 0.f) || !std::isfinite(p->temperature)) return fail(RL_ERR_ARG, "bad temperature");
     if (!(p->kl_coeff >= 0.f) || !std::isfinite(p->adv_tau)) return fail(RL_ERR_ARG, "bad kl_coeff / adv_tau");
     if (p->token_chunk < 0 || p->token_chunk % 128 != 0) return fail(RL_ERR_ARG, "token_chunk must be a multiple of 128");
+    if (!(p->entropy_coeff >= 0.f) || !std::isfinite(p->entropy_coeff)) return fail(RL_ERR_ARG, "bad entropy_coeff");
+    if (p->entropy_coeff != 0.f && p->bwd_mode == RL_BWD_SPARSE)
+        return fail(RL_ERR_ARG, "the entropy term's gradient is dense: no sparse backward with entropy_coeff > 0");
     return RL_OK;
 }
 

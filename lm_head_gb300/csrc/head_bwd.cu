@@ -25,6 +25,7 @@ namespace rl {
 bool bwd_is_dense(const rl_params* prm) {
     if (prm->bwd_mode == RL_BWD_DENSE) return true;
     if (prm->bwd_mode == RL_BWD_SPARSE) return false;
+    if (prm->entropy_coeff != 0.f) return true;   // the entropy gradient is dense
     const bool knobs_sparse = prm->loss_type == RL_LOSS_REINFORCE && prm->kl_coeff == 0.f;
     return !(knobs_sparse || prm->all_replayed != 0);
 }
@@ -90,6 +91,19 @@ RL_DEVINL float dense_grad(float alpha, float z, float lse) {
     if (alpha == 0.f) return 0.f;
     return __fmul_rn(alpha, exp2_approx(__fmul_rn(__fsub_rn(z, lse), kLog2e)));
 }
+// With the entropy regulariser ("10-KL-clip-entropy", section 3: loss -= c H) the dense
+// part of G also holds (dloss / T) c p (log p + H): kappa = dloss c / T on an RL token
+// (bit 0 of the saved metric flags), 0 otherwise; x = z - lse = log p.
+RL_DEVINL float dense_kappa(float dloss, float ent_coeff, float inv_T, float mflags) {
+    if (ent_coeff == 0.f || (__float_as_int(mflags) & 1) == 0) return 0.f;
+    return __fmul_rn(__fmul_rn(dloss, ent_coeff), inv_T);
+}
+RL_DEVINL float dense_grad2(float alpha, float kappa, float ent, float z, float lse) {
+    if (kappa == 0.f) return dense_grad(alpha, z, lse);
+    const float x = __fsub_rn(z, lse);
+    const float pv = exp2_approx(__fmul_rn(x, kLog2e));
+    return __fmul_rn(pv, fmaf(kappa, __fadd_rn(x, ent), alpha));
+}
 // What the bf16 operand(s) of the dense GEMMs drop from g: g - bf16(g), or with the hi/lo
 // split g - hi - lo.  Both differences are exact in fp32.
 RL_DEVINL float dense_residual(float g, bool split) {
@@ -115,19 +129,27 @@ struct EpiGrad {
         uint16_t* Gt_lo;
         int64_t ldt;
         const int* gate;      // fused path: run only when the chunk's range flag is set
+        const float* mterm;   // chunk-relative [n, 8] saved metric terms (entropy, flags)
+        float ent_coeff;
     };
     int64_t t;
     bool valid;
-    float alpha, lse;
+    float alpha, lse, kappa, ent;
 
     RL_DEVINL void begin_unit(const Params& p, int row, int, int m_blk, int, int) {
         t = static_cast<int64_t>(m_blk) * kBM + row;
         valid = t < p.n;
         alpha = 0.f;
         lse = 0.f;
+        kappa = 0.f;
+        ent = 0.f;
         if (valid) {
             alpha = dense_alpha(p.dloss[t], p.dcoef[t], p.inv_T);
             lse = p.lse[t];
+            if (p.ent_coeff != 0.f) {
+                kappa = dense_kappa(p.dloss[t], p.ent_coeff, p.inv_T, p.mterm[t * 8 + 7]);
+                ent = p.mterm[t * 8 + 6];
+            }
         }
     }
     RL_DEVINL void chunk(const Params& p, const uint32_t (&acc)[32], int col0, uint8_t*, int) {
@@ -135,7 +157,8 @@ struct EpiGrad {
         const int nvalid = p.V - col0 < 32 ? p.V - col0 : 32;  // multiple of 8
         float g[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) g[k] = dense_grad(alpha, __fmul_rn(__uint_as_float(acc[k]), p.inv_T), lse);
+        for (int k = 0; k < 32; ++k)
+            g[k] = dense_grad2(alpha, kappa, ent, __fmul_rn(__uint_as_float(acc[k]), p.inv_T), lse);
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -336,6 +359,16 @@ RL_DEVINL float fused_factor(float alpha, float m2, float lse) {
     if (alpha == 0.f) return 0.f;
     return __fmul_rn(alpha, exp2_approx(__fsub_rn(m2, __fmul_rn(lse, kLog2e))));
 }
+// G of one element on the fused hi/lo path, e = 2^(z log2(e) - m2): F e, plus the entropy
+// term kappa p (log p + H) with p = 2^(m2 - lse log2(e)) e.
+RL_DEVINL float fused_grad(float F, float kappa, float ent, float m2, float lse, float e) {
+    if (kappa == 0.f) return __fmul_rn(F, e);
+    if (e == 0.f) return 0.f;
+    const float l2 = __fsub_rn(m2, __fmul_rn(lse, kLog2e));
+    const float pv = __fmul_rn(exp2_approx(l2), e);
+    const float lnp = __fmul_rn(__fadd_rn(__log2f(e), l2), 0.6931471805599453f);
+    return fmaf(__fmul_rn(pv, kappa), __fadd_rn(lnp, ent), __fmul_rn(F, e));
+}
 
 struct ResidArgs {
     int64_t t0, n, V, nnz;
@@ -359,6 +392,8 @@ struct ResidArgs {
     const float* rs;
     const int* flag;
     // none of the above: recompute path
+    const float* mterm;       // absolute [N, 8]: entropy and flags for the entropy term
+    float ent_coeff;
 };
 
 // One warp per token of [t0, t0 + n): residual at the label and at the first entry of each
@@ -373,15 +408,19 @@ __global__ void __launch_bounds__(256) resid_kernel(ResidArgs a) {
     e = e < b ? b : (e > a.nnz ? a.nnz : e);
     const float alpha = dense_alpha(a.dloss[t], a.dcoef[t], a.inv_T);
     const float lse = a.lse[t];
+    const float kappa = a.ent_coeff != 0.f ? dense_kappa(a.dloss[t], a.ent_coeff, a.inv_T, a.mterm[t * 8 + 7]) : 0.f;
+    const float ent = a.ent_coeff != 0.f ? a.mterm[t * 8 + 6] : 0.f;
     const float sc = (a.Eb != nullptr && *a.flag == 0) ? a.rs[r] : 1.f;
     auto resid_at = [&](int32_t v, float z) -> float {
-        if (alpha == 0.f || v < 0 || v >= a.V) return 0.f;
-        const float g_true = dense_grad(alpha, z, lse);
+        if ((alpha == 0.f && kappa == 0.f) || v < 0 || v >= a.V) return 0.f;
+        const float g_true = dense_grad2(alpha, kappa, ent, z, lse);
         if (a.Eb != nullptr)   // the GEMMs use sc * e (e = G itself after a recompute)
             return __fsub_rn(g_true, __fmul_rn(sc, bf16_bits_to_float(a.Eb[r * a.V + v])));
         float g_gemm = g_true;
-        if (a.E32 != nullptr)
-            g_gemm = __fmul_rn(fused_factor(alpha, a.M2[r * a.ldm + (v >> 5)], lse), a.E32[r * a.V + v]);
+        if (a.E32 != nullptr) {
+            const float m2 = a.M2[r * a.ldm + (v >> 5)];
+            g_gemm = fused_grad(fused_factor(alpha, m2, lse), kappa, ent, m2, lse, a.E32[r * a.V + v]);
+        }
         return spike_residual(g_true, g_gemm, a.split != 0);
     };
     for (int64_t j = b + lane; j < e; j += 32) {
@@ -683,7 +722,7 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
 
     ResidArgs ra{0, N, V, nnz, b->labels, b->support.offsets, b->support.ids, dloss, sv.dcoef, sv.lse,
                  sv.zlab, sv.zsup, 1.0f / prm->temperature, w.split ? 1 : 0, w.resid,
-                 nullptr, nullptr, 0, nullptr, nullptr, nullptr};
+                 nullptr, nullptr, 0, nullptr, nullptr, nullptr, sv.mterm, prm->entropy_coeff};
     if ((rc = launch_resid(ra, stream)) != RL_OK) return rc;
     {
         ProfScope ps(RL_PROF_SPARSE_DX, stream);
@@ -718,7 +757,8 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
         // G chunk (recomputed logits -> softmax gradient), both layouts
         EpiGrad::Params gp{n, static_cast<int32_t>(V), 1.0f / prm->temperature, sv.lse + c0, dloss + c0,
                            sv.dcoef + c0, static_cast<uint16_t*>(w.G), static_cast<uint16_t*>(w.Gt),
-                           static_cast<uint16_t*>(w.G_lo), static_cast<uint16_t*>(w.Gt_lo), w.chunk};
+                           static_cast<uint16_t*>(w.G_lo), static_cast<uint16_t*>(w.Gt_lo), w.chunk, nullptr,
+                           sv.mterm + c0 * 8, prm->entropy_coeff};
         const GemmPlan p1 = make_plan_auto(n, V, H, 1, 1 << 30, 1, status);
         {
             ProfScope ps(RL_PROF_GEMM_GRAD, stream);
@@ -827,6 +867,8 @@ struct FoldArgs {
     float* dls;               // absolute [N]
     int* open_chunk;
     int* open_any;
+    const float* mterm;       // absolute [N, 8]
+    float ent_coeff;
 };
 
 RL_DEVINL void fold_at(const FoldArgs& a, int64_t r, int32_t v, float x) {
@@ -864,8 +906,10 @@ __global__ void __launch_bounds__(256) fold_kernel(FoldArgs a) {
     const bool rec = *a.flag != 0;
     const float alpha = dense_alpha(a.dloss[t], a.dcoef[t], a.inv_T);
     const float lse = a.lse[t], cr = a.cref[r];
+    const float kappa = a.ent_coeff != 0.f ? dense_kappa(a.dloss[t], a.ent_coeff, a.inv_T, a.mterm[t * 8 + 7]) : 0.f;
+    const float ent = a.ent_coeff != 0.f ? a.mterm[t * 8 + 6] : 0.f;
     auto dense_at = [&](float z) -> float {   // the stored quantity before rounding
-        return rec ? dense_grad(alpha, z, lse) : exp2_approx(__fsub_rn(__fmul_rn(z, kLog2e), cr));
+        return rec ? dense_grad2(alpha, kappa, ent, z, lse) : exp2_approx(__fsub_rn(__fmul_rn(z, kLog2e), cr));
     };
     for (int64_t j = b + lane; j < e; j += 32) {
         const int32_t id = a.ids[j];
@@ -891,6 +935,8 @@ struct GradEArgs {
     uint16_t* Gt;
     uint16_t* G_lo;
     uint16_t* Gt_lo;
+    const float* mterm;   // chunk-relative [n, 8]
+    float ent_coeff;
 };
 
 constexpr int kGradTileT = 64;    // tokens per block
@@ -915,13 +961,18 @@ __global__ void __launch_bounds__(256) grad_from_e_kernel(GradEArgs a) {
         uint32_t hi[4] = {0u, 0u, 0u, 0u}, lo[4] = {0u, 0u, 0u, 0u};
         if (t < a.n && v < a.V) {
             const float alpha = dense_alpha(a.dloss[t], a.dcoef[t], a.inv_T);
-            const float F = fused_factor(alpha, a.M2[t * a.ldm + (v >> 5)], a.lse[t]);
+            const float m2 = a.M2[t * a.ldm + (v >> 5)];
+            const float F = fused_factor(alpha, m2, a.lse[t]);
+            const float kappa =
+                a.ent_coeff != 0.f ? dense_kappa(a.dloss[t], a.ent_coeff, a.inv_T, a.mterm[t * 8 + 7]) : 0.f;
+            const float ent = a.ent_coeff != 0.f ? a.mterm[t * 8 + 6] : 0.f;
             const float4* src = reinterpret_cast<const float4*>(a.E32 + t * a.V + v);
             const float4 x0 = src[0], x1 = src[1];
             const float e[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float g0 = __fmul_rn(F, e[2 * k]), g1 = __fmul_rn(F, e[2 * k + 1]);
+                const float g0 = fused_grad(F, kappa, ent, m2, a.lse[t], e[2 * k]);
+                const float g1 = fused_grad(F, kappa, ent, m2, a.lse[t], e[2 * k + 1]);
                 hi[k] = pack_bf16x2(g0, g1);
                 const float h0 = bf16_bits_to_float(static_cast<uint16_t>(hi[k] & 0xFFFFu));
                 const float h1 = bf16_bits_to_float(static_cast<uint16_t>(hi[k] >> 16));
@@ -1094,12 +1145,16 @@ int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_
         }
         // forward GEMM (+ e store) and per-token loss for the chunk
         if ((rc = fwd_rows(b, prm, out, sv, f.fw, c0, n, &es, 0, status, stream)) != RL_OK) return rc;
+        // the entropy term is not a row scale of e: such a chunk takes the recompute path
+        if (!w.split && prm->entropy_coeff != 0.f && cudaMemsetAsync(flag, 1, 1, stream) != cudaSuccess)
+            return RL_ERR_CUDA;
         if (!w.split) {
             // out-of-range chunk only: G recomputed from the logits into Eb / Ebt (rs := 1)
             CUtensorMap tmX;
             if ((rc = make_tmap_bf16(&tmX, Xc, n, H, H, kBM)) != RL_OK) return rc;
             EpiGrad::Params gp{n, static_cast<int32_t>(V), inv_T, sv.lse + c0, dloss + c0, sv.dcoef + c0,
-                               f.Eb, f.Ebt, nullptr, nullptr, f.chunk, flag};
+                               f.Eb, f.Ebt, nullptr, nullptr, f.chunk, flag, sv.mterm + c0 * 8,
+                               prm->entropy_coeff};
             const GemmPlan pg = make_plan_auto(n, V, H, 1, 1 << 30, 1, status);
             {
                 ProfScope ps(RL_PROF_GEMM_GRAD, stream);
@@ -1109,7 +1164,7 @@ int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_
             {
                 FoldArgs fa{c0, n, V, nnz, f.chunk, b->labels, b->support.offsets, b->support.ids, dloss,
                             sv.labcoef, sv.entcoef, sv.zlab, sv.zsup, sv.dcoef, sv.lse, inv_T, f.cref, f.rs, flag,
-                            f.Eb, f.Ebt, f.dls, f.gates + ci, f.gates + f.nchunks};
+                            f.Eb, f.Ebt, f.dls, f.gates + ci, f.gates + f.nchunks, sv.mterm, prm->entropy_coeff};
                 ProfScope ps(RL_PROF_RESID, stream);
                 fold_kernel<<<static_cast<unsigned>((n + 7) / 8), 256, 0, stream>>>(fa);
                 count_launch();
@@ -1122,12 +1177,14 @@ int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_
         } else {
             // spike residuals of the chunk's tokens, then G / G^T (hi/lo) from e
             ResidArgs ra{c0, n, V, nnz, b->labels, b->support.offsets, b->support.ids, dloss, sv.dcoef, sv.lse,
-                         sv.zlab, sv.zsup, inv_T, 1, w.resid, f.E32, f.M2, f.ldm, nullptr, nullptr, nullptr};
+                         sv.zlab, sv.zsup, inv_T, 1, w.resid, f.E32, f.M2, f.ldm, nullptr, nullptr, nullptr,
+                         sv.mterm, prm->entropy_coeff};
             if ((rc = launch_resid(ra, stream)) != RL_OK) return rc;
             {
                 GradEArgs ga{n, V, f.ldm, f.chunk, f.E32, f.M2, dloss + c0, sv.dcoef + c0, sv.lse + c0, inv_T,
                              static_cast<uint16_t*>(w.G), static_cast<uint16_t*>(w.Gt),
-                             static_cast<uint16_t*>(w.G_lo), static_cast<uint16_t*>(w.Gt_lo)};
+                             static_cast<uint16_t*>(w.G_lo), static_cast<uint16_t*>(w.Gt_lo), sv.mterm + c0 * 8,
+                             prm->entropy_coeff};
                 dim3 grid(static_cast<unsigned>((V + kGradTileV - 1) / kGradTileV),
                           static_cast<unsigned>((n + kGradTileT - 1) / kGradTileT));
                 ProfScope ps(RL_PROF_GRAD_E, stream);

@@ -420,7 +420,7 @@ struct TokenArgs {
     const float* logq;
     const uint8_t* replayed;
     int32_t loss_type, kl_est, kl_stale, sparse;
-    float eps, cap, lo, hi, adv_tau, kl_coeff;
+    float eps, cap, lo, hi, adv_tau, kl_coeff, ent_coeff;
     float* loss;
     float* logp_label;
     float* logp_support;
@@ -583,6 +583,8 @@ __global__ void __launch_bounds__(256) token_loss_kernel(TokenArgs a) {
     const float A = a.adv[t];
     const float at = a.adv_tau * A;
     float loss = -at * (wl.w * logP_lab - cen) + beta * kl;
+    // exploration regulariser ("10-KL-clip-entropy", section 3): loss -= c H, full-vocab H
+    if (a.ent_coeff != 0.f) loss = fmaf(-a.ent_coeff, ent, loss);
     // d loss / d z_j = d * P_j + spikes; d multiplies the (full or renormalised) softmax
     const float d = at * (wl.w - C) + beta * (exact ? U : 1.f);
     float labc = -at * wl.w - (exact ? 0.f : beta);
@@ -835,6 +837,7 @@ int fwd_rows(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs
     ta.hi = prm->icepop_high;
     ta.adv_tau = prm->adv_tau;
     ta.kl_coeff = prm->kl_coeff;
+    ta.ent_coeff = prm->entropy_coeff;
     ta.loss = out->loss + c0;
     ta.logp_label = off(out->logp_label);
     ta.logp_support = out->logp_support;

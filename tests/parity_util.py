@@ -49,7 +49,7 @@ def oracle_params(hp: rh.HeadParams) -> oracle.HeadParams:
                              icepop_low=f32(hp.icepop_low), icepop_high=f32(hp.icepop_high),
                              adv_tau=f32(hp.adv_tau), temperature=f32(hp.temperature),
                              kl_coeff=f32(hp.kl_coeff), kl_estimator=hp.kl_estimator,
-                             kl_staleness=hp.kl_staleness)
+                             kl_staleness=hp.kl_staleness, entropy_coeff=f32(hp.entropy_coeff))
 
 
 def ulp_bf16(x):
@@ -113,9 +113,10 @@ def grad_check_block(gpu, ref, reading: str, what: str, bound=None, zbound=None,
 
 def loss_prop_tol(ref: dict, inp: dict, op: oracle.HeadParams):
     """Per-token loss bar: the 1e-5 log-prob bar carried through the loss to first order,
-    |d loss_t| <= |adv_tau A_t| (|w_a| + sum_e |c_e|) * 1e-5 + beta_t * (sum_e u_e or 1) * 1e-5,
-    doubled.  (A per-token loss is a difference of O(1) log-prob terms, so where it
-    cancels a relative bar alone cannot hold.)"""
+    |d loss_t| <= |adv_tau A_t| (|w_a| + sum_e |c_e|) * 1e-5 + beta_t * (sum_e u_e or 1) * 1e-5
+    (+ entropy_coeff times the entropy's bar, the logsumexp's), doubled.  (A per-token loss
+    is a difference of O(1) log-prob terms, so where it cancels a relative bar alone cannot
+    hold.)"""
     off = np.asarray(inp["offsets"], np.int64)
     abs_c = np.add.reduceat(np.abs(ref["c_support"]), off[:-1]) if ref["c_support"].size else np.zeros(len(off) - 1)
     sum_u = np.add.reduceat(ref["u_support"], off[:-1]) if ref["u_support"].size else np.zeros(len(off) - 1)
@@ -124,7 +125,9 @@ def loss_prop_tol(ref: dict, inp: dict, op: oracle.HeadParams):
     sum_u = np.where(empty, 0.0, sum_u)
     kl_w = sum_u if op.kl_estimator == oracle.KL_EXACT else np.ones_like(sum_u)
     A = np.abs(op.adv_tau * np.asarray(inp["adv"], np.float64))
-    return 2 * LOGP_TOL * (A * (np.abs(ref["w_label"]) + abs_c) + np.asarray(ref["beta"]) * kl_w)
+    H = np.asarray(inp["hidden"]).shape[1]
+    ent = op.entropy_coeff * logp_tol(H, ref["lse"], ref["lse"]) / LOGP_TOL if op.entropy_coeff else 0.0
+    return 2 * LOGP_TOL * (A * (np.abs(ref["w_label"]) + abs_c) + np.asarray(ref["beta"]) * kl_w + ent)
 
 
 def loss_check(gpu, ref, prop_tol=None, what="loss"):

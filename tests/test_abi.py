@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_struct_sizes_match_the_header_layout():
-    assert ctypes.sizeof(rh.RlParams) == 14 * 4
+    assert ctypes.sizeof(rh.RlParams) == 15 * 4
     assert ctypes.sizeof(rh.RlHeadMetrics) == 8 * 8 + 6 * 8
     assert ctypes.sizeof(rh.RlPgMetrics) == 6 * 8 + 6 * 8 + 16 * 8 + 8   # ..., ipo_curve[16], status
 
@@ -83,11 +83,13 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
     assert _fwd(lib, _batch(V=1001), good) == rh.RL_ERR_UNSUPPORTED
     assert _fwd(lib, _batch(N=-1), good) == rh.RL_ERR_ARG
     for field, val in (("temperature", 0.0), ("eps", -0.1), ("loss_type", 7), ("icepop_low", 3.0),
-                       ("token_chunk", 100), ("kl_coeff", -1.0)):
+                       ("token_chunk", 100), ("kl_coeff", -1.0), ("entropy_coeff", -0.5)):
         bad = rh.HeadParams().c()
         setattr(bad, field, val)
         assert _fwd(lib, _batch(), bad) == rh.RL_ERR_ARG, field
     assert _fwd(lib, _batch(), good, ws_bytes=16) == rh.RL_ERR_WORKSPACE
+    sparse_ent = rh.HeadParams(bwd_mode=rh.RL_BWD_SPARSE, entropy_coeff=0.01).c()
+    assert _fwd(lib, _batch(), sparse_ent) == rh.RL_ERR_ARG     # the entropy gradient is dense
     assert lib.rl_status_read(None, None) == rh.RL_ERR_ARG
     assert lib.rl_error_string(rh.RL_ERR_WORKSPACE) == b"workspace too small"
     pp = rh.PgParams(clip_ratio_c=0.5).c()

@@ -236,3 +236,24 @@ def test_recompute_path_multi_chunk():
     ref = oracle.head_forward(case.numpy(), oracle_params(hp))
     check_forward(case, hp, fwd, ref)
     check_backward(case, hp, batch, fwd)
+
+
+@pytest.mark.parametrize("prec", [rh.RL_GRAD_BF16, rh.RL_GRAD_SPLIT])
+def test_entropy_regulariser_fused_and_two_call(prec):
+    """loss -= entropy_coeff * H ("10-KL-clip-entropy", section 3), on draw rows and
+    replayed rows (whose renormalised part is sparse but whose entropy gradient is dense),
+    through the fused call (BF16: every chunk takes the logit recompute) and through the
+    two-call forward / dense backward, in both gradient precisions."""
+    a = workloads.make_head_case("c1", n_tokens=160, hidden_scale=8.0, noise=0.7, age_max=4, loss_mask_frac=0.1,
+                                 seed=141)
+    b = workloads.make_head_case("c1", n_tokens=140, support="replay", top_p=0.9, hidden_scale=8.0, noise=0.3,
+                                 age_max=4, seed=142)
+    case = _concat_cases(a, b)
+    hp = rh.HeadParams(loss_type=rh.RL_LOSS_IPO, eps=0.3, max_importance_ratio=10.0, kl_coeff=0.02,
+                       kl_estimator=rh.RL_KL_EXACT, kl_staleness=rh.RL_STALE_INV_SQRT, bwd_mode=rh.RL_BWD_AUTO,
+                       grad_precision=prec, token_chunk=128, entropy_coeff=0.05)
+    check_fused(case, hp, recomputed=3 if prec == rh.RL_GRAD_BF16 else 0)
+    dev, batch, fwd = _forward(case, hp)
+    ref = oracle.head_forward(case.numpy(), oracle_params(hp))
+    check_forward(case, hp, fwd, ref)
+    check_backward(case, hp, batch, fwd, both=False)
