@@ -142,7 +142,8 @@ __global__ void __launch_bounds__(kRcThreads, 4) rc_seq_kernel(RcArgs a) {
 
     // pass 1: the sequence's sums
     int n = 0, cat = 0;
-    FF S = {0.f, 0.f}, St = {0.f, 0.f}, Sr = {0.f, 0.f}, E = {0.f, 0.f};
+    FF S = {0.f, 0.f}, E = {0.f, 0.f};   // the decisions' sums, float-float
+    float st = 0.f, sr = 0.f;            // metric sums: fp32 per thread
     float mis = 0.f, k3 = 0.f, ad = 0.f, c2 = 0.f;
     int staged = -1;
     for (int c = 0; c < nchunks; ++c) {
@@ -156,8 +157,8 @@ __global__ void __launch_bounds__(kRcThreads, 4) rc_seq_kernel(RcArgs a) {
             const FF d = two_sum(x, -y);
             ++n;
             S = ff_add(S, d);
-            St = ff_add(St, {x, 0.f});
-            Sr = ff_add(Sr, {y, 0.f});
+            st += x;
+            sr += y;
             if (rs_seq) E = ff_add(E, exp_ff2(d));
             if (q.veto) cat += ff_lt(d, q.lnVeto) ? 1 : 0;
             const float df = d.hi;
@@ -169,7 +170,8 @@ __global__ void __launch_bounds__(kRcThreads, 4) rc_seq_kernel(RcArgs a) {
         }
     }
     {
-        const FF w4[4] = {warp_sum_ff(S), warp_sum_ff(St), warp_sum_ff(Sr), rs_seq ? warp_sum_ff(E) : FF{0.f, 0.f}};
+        const FF w4[4] = {warp_sum_ff(S), rs_seq ? warp_sum_ff(E) : FF{0.f, 0.f}, {warp_sum_f(st), 0.f},
+                          {warp_sum_f(sr), 0.f}};
         const float f4[4] = {warp_sum_f(mis), warp_sum_f(k3), warp_sum_f(ad), warp_sum_f(c2)};
         const int i2[2] = {warp_sum_i(n), warp_sum_i(cat)};
         if (lane == 0) {
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(kRcThreads, 4) rc_seq_kernel(RcArgs a) {
             nt += shi[w][0];
             catt += shi[w][1];
         }
-        const FF Sb = R[0], Stb = R[1], Srb = R[2], Eb = R[3];
+        const FF Sb = R[0], Eb = R[1], Stb = R[2], Srb = R[3];
         RcSeq s{};
         s.n = nt;
         if (nt > 0) {
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(kRcThreads, 4) rc_seq_kernel(RcArgs a) {
             s.veto = catt > 0;
             const float tr = -(Stb.hi + Stb.lo) * rn;
             const float ro = -(Srb.hi + Srb.lo) * rn;
-            const float df = -(ff_add(Stb, FF{-Srb.hi, -Srb.lo}).hi) * rn;   // tr - ro, from the exact sums
+            const float df = -(Sb.hi + Sb.lo) * rn;   // tr - ro = -S / n, from the exact sum of d
             seqd[1] = tr;
             seqd[2] = ro;
             seqd[3] = df;
@@ -257,7 +259,8 @@ __global__ void __launch_bounds__(kRcThreads, 4) rc_seq_kernel(RcArgs a) {
             float wout = 0.f;
             uint8_t kp8 = 0;
             if (s_m[i] != 0) {
-                const FF d = two_sum(s_lt[i], -s_lr[i]);
+                const bool tok = q.level == RL_LEVEL_TOKEN || (q.use_rs && q.rs_level == RL_LEVEL_TOKEN);
+                const FF d = tok ? two_sum(s_lt[i], -s_lr[i]) : FF{0.f, 0.f};
                 float w;
                 bool lo, hi;
                 if (q.level == RL_LEVEL_TOKEN) {

@@ -1,0 +1,55 @@
+"""The N > 1 logic of bench.py on CPU: two gloo ranks (127.0.0.1), each timing its own
+replica batch.  The job's figure is the slowest rank's time and the sum of the ranks'
+tokens (weak scaling, no collective on the data path); the reference arm runs on rank 0
+only."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    r, w, local = bench.dist_env()
+    assert (r, w, local) == (rank, world, rank)
+    ms, tokens, value = bench.aggregate(10.0 + 5.0 * rank, 1000 * (rank + 1), w)
+    with open(os.path.join(out_dir, f"rank{rank}.txt"), "w") as f:
+        f.write(f"{ms} {tokens} {value}\n")
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_max_time_and_sum_tokens(tmp_path):
+    world = 2
+    mp.spawn(_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True)
+    for rank in range(world):
+        ms, tokens, value = open(tmp_path / f"rank{rank}.txt").read().split()
+        assert float(ms) == 15.0                       # the slower rank's time
+        assert int(tokens) == 3000                     # every rank's tokens
+        assert float(value) == pytest.approx(3000 / 0.015)
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+    assert bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out == ""
