@@ -9,7 +9,9 @@
 // beside the epilogue staging tiles.
 //
 // * Both CTAs: warp 0 lane 0 loads its A and B halves with TMA (.cta_group::2), the
-//   completion bytes of both CTAs counted on the even CTA's full barrier.
+//   completion bytes of both CTAs counted on the even CTA's full barrier.  An operand
+//   stored M- (or N-) contiguous comes in as two 64 x 64 boxes per CTA (plan.a_mn / b_mn)
+//   and is described to the MMA as MN-major.
 // * Even CTA only: warp 1 lane 0 issues tcgen05.mma.cta_group::2 (M=256, N=256, K=16) and
 //   commits with multicast to both CTAs' "stage empty" and "accumulator full" barriers.
 // * Both CTAs: warps 2-9 drain their own TMEM (same epilogue policies as gemm_tc_kernel,
@@ -161,9 +163,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         if (leader) mbar_arrive_expect_tx(full + stage, 2 * kStageBytes2);
                         const int pass = kb / plan.kb_per_pass;
                         const int kx = (kb - pass * plan.kb_per_pass) * kBK;
-                        tma_load_2d_pair(pass ? &tmA2 : &tmA, bar, sa, kx,
-                                         (c.m_blk * 2 + static_cast<int>(rank)) * kBM);
-                        tma_load_2d_pair(&tmB, bar, sb, kx, nb * kBN + static_cast<int>(rank) * (kBN / 2));
+                        const int m0 = (c.m_blk * 2 + static_cast<int>(rank)) * kBM;
+                        const int n0 = nb * kBN + static_cast<int>(rank) * (kBN / 2);
+                        const CUtensorMap* ma = pass ? &tmA2 : &tmA;
+                        if (plan.a_mn) {   // [K, M] storage: two 64 x 64 boxes, M contiguous
+                            tma_load_2d_pair(ma, bar, sa, m0, kx);
+                            tma_load_2d_pair(ma, bar, sa + 8192, m0 + 64, kx);
+                        } else {
+                            tma_load_2d_pair(ma, bar, sa, kx, m0);
+                        }
+                        if (plan.b_mn) {
+                            tma_load_2d_pair(&tmB, bar, sb, n0, kx);
+                            tma_load_2d_pair(&tmB, bar, sb + 8192, n0 + 64, kx);
+                        } else {
+                            tma_load_2d_pair(&tmB, bar, sb, kx, n0);
+                        }
                         issued = true;
                         if (++stage == kStages2) {
                             stage = 0;
@@ -185,6 +199,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             uint32_t stage = 0, phase = 0, abuf = 0, aphase = 0;
             bool ok = true;
             bool any = false;
+            const uint32_t idesc = kIdesc2 | (plan.a_mn ? (1u << 15) : 0u) | (plan.b_mn ? (1u << 16) : 0u);
             for (int u = pair; u < plan.num_units && ok; u += npairs) {
                 const UnitCoords c = decode_unit(plan, u);
                 for (int nb = c.nb_begin; nb < c.nb_end && ok; ++nb) {
@@ -205,9 +220,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const uint32_t sa = smem_addr(smem + stage * kStageBytes2);
                         const uint32_t sb = sa + kATileBytes2;
 #pragma unroll
-                        for (int k = 0; k < kBK / 16; ++k)
-                            umma_bf16_pair(d_tmem, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32),
-                                           kIdesc2, (kb | k) != 0 ? 1u : 0u);
+                        for (int k = 0; k < kBK / 16; ++k) {
+                            const uint64_t da = plan.a_mn ? sdesc_mnmajor_sw128(sa + k * 2048, 8192)
+                                                          : sdesc_kmajor_sw128(sa + k * 32);
+                            const uint64_t db = plan.b_mn ? sdesc_mnmajor_sw128(sb + k * 2048, 8192)
+                                                          : sdesc_kmajor_sw128(sb + k * 32);
+                            umma_bf16_pair(d_tmem, da, db, idesc, (kb | k) != 0 ? 1u : 0u);
+                        }
                         any = true;
                         umma_commit_pair_multicast(empty + stage, 0x3);
                         if (++stage == kStages2) {
@@ -307,8 +326,8 @@ inline int make_tmap_b(CUtensorMap* map, const void* base, int64_t rows, int64_t
     return make_tmap_bf16(map, base, rows, cols, ld, gemm_pair_mode() ? kBN / 2 : kBN);
 }
 inline GemmPlan make_plan_auto(int64_t M, int64_t N, int64_t K, int passes, int n_splits, int m_fastest,
-                               int32_t* status) {
-    return make_plan(M, N, K, passes, n_splits, m_fastest, status, 0, 0, gemm_pair_mode());
+                               int32_t* status, int a_mn = 0) {
+    return make_plan(M, N, K, passes, n_splits, m_fastest, status, a_mn, 0, gemm_pair_mode());
 }
 template <class Epi>
 int launch_gemm_auto(const CUtensorMap& tmA, const CUtensorMap& tmA2, const CUtensorMap& tmB,

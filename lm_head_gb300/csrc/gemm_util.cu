@@ -38,7 +38,7 @@ struct EpiStore {
 int gemm_util_impl(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
                    float* D, int32_t* status, cudaStream_t stream) {
     CUtensorMap ta, tb;
-    const int pair = gemm_pair_mode() && !a_mn && !b_mn;
+    const int pair = gemm_pair_mode();
     int rc = a_mn ? make_tmap_bf16(&ta, A, K, M, M, 64) : make_tmap_bf16(&ta, A, M, K, K, kBM);
     if (rc != RL_OK) return rc;
     rc = b_mn ? make_tmap_bf16(&tb, B, K, N, N, 64) : make_tmap_bf16(&tb, B, N, K, K, pair ? kBN / 2 : kBN);
