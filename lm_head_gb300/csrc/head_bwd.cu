@@ -277,22 +277,61 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const uint16_t* in,
                                                              int64_t cols, int64_t ld_in,
                                                              uint16_t* out, int64_t ld_out,
                                                              const float* rs, const int* flag) {
-    __shared__ uint16_t tile[64][66];
+    // 64 x 64 tile; 16-byte global loads and stores (8 elements), the transpose in shared
+    // memory with a 65-element pitch (the rows 8 apart that a warp's lanes gather fall in
+    // distinct banks)
+    __shared__ uint16_t tile[64][65];
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64;
     const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 64;
-    const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;  // 64 x 4
     const bool scaled = rs != nullptr && *flag == 0;
-    for (int i = ty; i < 64; i += 4) {
-        const int64_t r = r0 + i, c = c0 + tx;
-        uint16_t v = (r < rows && c < cols) ? in[r * ld_in + c] : 0;
-        if (scaled && r < rows)
-            v = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(rs[r], bf16_bits_to_float(v))));
-        tile[i][tx] = v;
+    const bool vec_in = ((ld_in & 7) == 0) && ((reinterpret_cast<uintptr_t>(in) & 15) == 0);
+    const bool vec_out = ((ld_out & 7) == 0) && ((reinterpret_cast<uintptr_t>(out) & 15) == 0);
+    const int cv = (threadIdx.x & 7) * 8;   // column group of 8
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int i = (threadIdx.x >> 3) + 32 * k;   // tile row
+        const int64_t r = r0 + i, c = c0 + cv;
+        uint16_t v[8];
+        if (r < rows && vec_in && c + 8 <= cols) {
+            const uint4 q = *reinterpret_cast<const uint4*>(in + r * ld_in + c);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[2 * j] = static_cast<uint16_t>(w[j] & 0xFFFFu);
+                v[2 * j + 1] = static_cast<uint16_t>(w[j] >> 16);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = (r < rows && c + j < cols) ? in[r * ld_in + c + j] : 0;
+        }
+        if (scaled && r < rows) {
+            const float sc = rs[r];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(sc, bf16_bits_to_float(v[j]))));
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) tile[i][cv + j] = v[j];
     }
     __syncthreads();
-    for (int i = ty; i < 64; i += 4) {
-        const int64_t c = c0 + i, r = r0 + tx;
-        if (c < cols && r < rows) out[c * ld_out + r] = tile[tx][i];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int i = (threadIdx.x >> 3) + 32 * k;   // output row = input column c0 + i
+        const int64_t c = c0 + i, r = r0 + cv;
+        if (c >= cols) continue;
+        uint16_t v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = tile[cv + j][i];
+        if (vec_out && r + 8 <= rows) {
+            uint4 q;
+            q.x = v[0] | (static_cast<uint32_t>(v[1]) << 16);
+            q.y = v[2] | (static_cast<uint32_t>(v[3]) << 16);
+            q.z = v[4] | (static_cast<uint32_t>(v[5]) << 16);
+            q.w = v[6] | (static_cast<uint32_t>(v[7]) << 16);
+            *reinterpret_cast<uint4*>(out + c * ld_out + r) = q;
+        } else {
+            for (int j = 0; j < 8 && r + j < rows; ++j) out[c * ld_out + r + j] = v[j];
+        }
     }
 }
 
