@@ -15,11 +15,10 @@
 //                       sums, the sequence's decisions by one thread, a second pass (the
 //                       tokens are now in L2) writing weights and keep flags; one record
 //                       of partial sums per sequence.
-//     The records are reduced in two ordered levels inside the same kernel: the last
-//     block of each group of 32 sequences sums its group's records in sequence order,
-//     the last group to finish sums the group totals in group order and writes the
-//     batch-normalisation factor and the metrics (reproducible totals, no extra launch).
-//  2. rc_scale_kernel   (batch normalisation only) weights *= factor.
+//  2. rc_reduce_kernel  one block, one warp per field: the records summed in sequence
+//                       order (fixed tree), so results are reproducible; then the
+//                       batch-normalisation factor and the metrics.
+//  3. rc_scale_kernel   (batch normalisation only) weights *= factor.
 #include <cmath>
 #include <climits>
 
@@ -37,7 +36,6 @@ enum {
 };
 enum { RC_VALID, RC_SEQ, RC_KEPT, RC_TIS_LO, RC_TIS_HI, RC_RS_LO, RC_RS_HI, RC_CAT_TOK, RC_CAT_SEQ, kRcC };
 constexpr int kRcFields = kRcD + kRcC + 2;   // + min, max
-constexpr int kRcGroup = 32;                  // sequences per group of the ordered reduction
 
 struct RcPrep {
     int use_tis, mode, level, norm, use_rs, rs_level, veto;
@@ -61,10 +59,6 @@ struct RcArgs {
     int32_t* status;
     float* factor;       // batch-normalisation factor for rc_scale_kernel
     rl_rc_metrics* metrics;
-    int64_t ngroups;     // groups of kRcGroup sequences
-    int* gcount;         // [ngroups] sequences of the group done
-    int* done;           // groups done
-    double* gd;          // [kRcFields][ngroups] group totals
 };
 
 // Fixed-order reductions: a butterfly within each warp (every lane ends with the same
@@ -100,56 +94,6 @@ RL_DEVINL T rc_block_reduce(T v, T* sh, Op op) {   // sh: one slot per warp
 
 // e^(hi + lo) for a float-float exponent: e^hi (float-float) times 1 + lo (|lo| tiny).
 RL_DEVINL FF exp_ff2(FF d) { return ff_mul(exp_ff(d.hi), two_sum(1.f, d.lo)); }
-
-// Field f of sequence b's record as a double; fields combine by sum except the kept
-// weights' min (kRcD + kRcC) and max (kRcD + kRcC + 1).
-RL_DEVINL double rc_record(const RcArgs& a, int f, int64_t b) {
-    if (f < kRcD) return __ldcg(a.pd + f * a.B + b);
-    if (f < kRcD + kRcC) return static_cast<double>(__ldcg(a.pc + (f - kRcD) * a.B + b));
-    return static_cast<double>(__ldcg((f == kRcD + kRcC ? a.pmin : a.pmax) + b));
-}
-RL_DEVINL double rc_combine(int f, double x, double y) {
-    return f < kRcD + kRcC ? x + y : (f == kRcD + kRcC ? fmin(x, y) : fmax(x, y));
-}
-RL_DEVINL double rc_identity(int f) {
-    return f < kRcD + kRcC ? 0.0 : (f == kRcD + kRcC ? INFINITY : -INFINITY);
-}
-
-// The batch-normalisation factor and the metrics from the batch totals t (one thread).
-RL_DEVINL void rc_finish(const RcArgs& a, const double* t) {
-    const double kept_w = t[RD_KEPT_W], n_kept = t[kRcD + RC_KEPT];
-    const double factor = (a.q.use_tis && a.q.norm && n_kept > 0 && kept_w > 0) ? n_kept / kept_w : 1.0;
-    *a.factor = static_cast<float>(factor);
-    rl_rc_metrics* m = a.metrics;
-    if (!m) return;
-    m->w_before_sum = t[RD_W_BEFORE];
-    m->w_after_sum = t[RD_W_AFTER];
-    m->kept_w_sum = kept_w;
-    m->batch_norm_factor = factor;
-    m->final_sum = kept_w * factor;
-    m->final_min = n_kept > 0 ? t[kRcD + kRcC] * factor : 0.0;
-    m->final_max = n_kept > 0 ? t[kRcD + kRcC + 1] * factor : 0.0;
-    m->mis_kl_sum = t[RD_MIS_KL];
-    m->k3_sum = t[RD_K3];
-    m->abs_diff_sum = t[RD_ABS];
-    m->chi2_token_sum = t[RD_CHI2T];
-    m->train_lppl_sum = t[RD_TRAIN_LPPL];
-    m->rollout_lppl_sum = t[RD_ROLL_LPPL];
-    m->lppl_diff_sum = t[RD_LPPL_DIFF];
-    m->lppl_abs_diff_sum = t[RD_LPPL_ABS];
-    m->ppl_ratio_sum = t[RD_PPL_RATIO];
-    m->chi2_seq_sum = t[RD_CHI2S];
-    m->n_valid = static_cast<int64_t>(t[kRcD + RC_VALID]);
-    m->n_seq = static_cast<int64_t>(t[kRcD + RC_SEQ]);
-    m->n_kept = static_cast<int64_t>(n_kept);
-    m->n_tis_low = static_cast<int64_t>(t[kRcD + RC_TIS_LO]);
-    m->n_tis_high = static_cast<int64_t>(t[kRcD + RC_TIS_HI]);
-    m->n_rs_low = static_cast<int64_t>(t[kRcD + RC_RS_LO]);
-    m->n_rs_high = static_cast<int64_t>(t[kRcD + RC_RS_HI]);
-    m->n_cat_tokens = static_cast<int64_t>(t[kRcD + RC_CAT_TOK]);
-    m->n_cat_seqs = static_cast<int64_t>(t[kRcD + RC_CAT_SEQ]);
-    m->status = __ldcg(a.status);
-}
 
 struct RcSeq {   // one sequence's decisions (thread 0 -> block)
     int n, tis_lo, tis_hi, rs_lo, rs_hi, veto;
@@ -400,49 +344,95 @@ __global__ void __launch_bounds__(kRcThreads, 4) rc_seq_kernel(RcArgs a) {
         a.pmin[b] = F[3];
         a.pmax[b] = F[4];
     }
-
-    // ordered reduction in two levels, by the last block of each group of kRcGroup
-    // sequences and then by the last group to finish (arrival counters; sequence order and
-    // group order fixed, so the totals are reproducible)
-    __shared__ int last;
-    __shared__ double tot[kRcFields];
-    __threadfence();
-    __syncthreads();
-    const int64_t g = b / kRcGroup, gb0 = g * kRcGroup;
-    const int64_t gb1 = gb0 + kRcGroup < a.B ? gb0 + kRcGroup : a.B;
-    if (threadIdx.x == 0) last = atomicAdd(a.gcount + g, 1) == static_cast<int>(gb1 - gb0) - 1;
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    if (threadIdx.x < kRcFields) {
-        const int f = threadIdx.x;
-        double v = rc_identity(f);
-#pragma unroll 8
-        for (int64_t bb = gb0; bb < gb1; ++bb) v = rc_combine(f, v, rc_record(a, f, bb));
-        a.gd[f * a.ngroups + g] = v;
-    }
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) last = atomicAdd(a.done, 1) == static_cast<int>(a.ngroups) - 1;
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    if (threadIdx.x < kRcFields) {
-        const int f = threadIdx.x;
-        double v = rc_identity(f);
-#pragma unroll 8
-        for (int64_t gg = 0; gg < a.ngroups; ++gg) v = rc_combine(f, v, __ldcg(a.gd + f * a.ngroups + gg));
-        tot[f] = v;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) rc_finish(a, tot);
 }
 
-// An empty batch: factor 1, zero metrics.
-__global__ void rc_empty_kernel(RcArgs a) {
-    double t[kRcFields];
-    for (int f = 0; f < kRcFields; ++f) t[f] = 0.0;
-    rc_finish(a, t);
+// One block of kRcFields warps: warp f sums field f of the records over the sequences in
+// order (lane l takes b = l, l + 32, ..., eight loads in flight ahead of their adds, then
+// a butterfly); thread 0 then forms the factor and writes the metrics.
+constexpr int kRcReduceThreads = 32 * kRcFields;
+__global__ void __launch_bounds__(kRcReduceThreads) rc_reduce_kernel(RcArgs a) {
+    __shared__ double tot[kRcFields];
+    const int f = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t B = a.B;
+    if (f < kRcD) {
+        const double* src = a.pd + f * B;
+        double v = 0.0;
+        for (int64_t b0 = lane; b0 < B; b0 += 32 * 8) {
+            double x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : 0.0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v += x[i];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) tot[f] = v;
+    } else if (f < kRcD + kRcC) {
+        const long long* src = a.pc + (f - kRcD) * B;
+        long long v = 0;
+        for (int64_t b0 = lane; b0 < B; b0 += 32 * 8) {
+            long long x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v += x[i];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) tot[f] = static_cast<double>(v);
+    } else {
+        const bool is_min = f == kRcD + kRcC;
+        const float* src = is_min ? a.pmin : a.pmax;
+        float v = is_min ? INFINITY : -INFINITY;
+        for (int64_t b0 = lane; b0 < B; b0 += 32 * 8) {
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : v;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v = is_min ? fminf(v, x[i]) : fmaxf(v, x[i]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float u = __shfl_xor_sync(0xffffffffu, v, o);
+            v = is_min ? fminf(v, u) : fmaxf(v, u);
+        }
+        if (lane == 0) tot[f] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    const double* t = tot;
+    const double kept_w = t[RD_KEPT_W], n_kept = t[kRcD + RC_KEPT];
+    const double factor = (a.q.use_tis && a.q.norm && n_kept > 0 && kept_w > 0) ? n_kept / kept_w : 1.0;
+    *a.factor = static_cast<float>(factor);
+    rl_rc_metrics* m = a.metrics;
+    if (!m) return;
+    m->w_before_sum = t[RD_W_BEFORE];
+    m->w_after_sum = t[RD_W_AFTER];
+    m->kept_w_sum = kept_w;
+    m->batch_norm_factor = factor;
+    m->final_sum = kept_w * factor;
+    m->final_min = n_kept > 0 ? t[kRcD + kRcC] * factor : 0.0;
+    m->final_max = n_kept > 0 ? t[kRcD + kRcC + 1] * factor : 0.0;
+    m->mis_kl_sum = t[RD_MIS_KL];
+    m->k3_sum = t[RD_K3];
+    m->abs_diff_sum = t[RD_ABS];
+    m->chi2_token_sum = t[RD_CHI2T];
+    m->train_lppl_sum = t[RD_TRAIN_LPPL];
+    m->rollout_lppl_sum = t[RD_ROLL_LPPL];
+    m->lppl_diff_sum = t[RD_LPPL_DIFF];
+    m->lppl_abs_diff_sum = t[RD_LPPL_ABS];
+    m->ppl_ratio_sum = t[RD_PPL_RATIO];
+    m->chi2_seq_sum = t[RD_CHI2S];
+    m->n_valid = static_cast<int64_t>(t[kRcD + RC_VALID]);
+    m->n_seq = static_cast<int64_t>(t[kRcD + RC_SEQ]);
+    m->n_kept = static_cast<int64_t>(n_kept);
+    m->n_tis_low = static_cast<int64_t>(t[kRcD + RC_TIS_LO]);
+    m->n_tis_high = static_cast<int64_t>(t[kRcD + RC_TIS_HI]);
+    m->n_rs_low = static_cast<int64_t>(t[kRcD + RC_RS_LO]);
+    m->n_rs_high = static_cast<int64_t>(t[kRcD + RC_RS_HI]);
+    m->n_cat_tokens = static_cast<int64_t>(t[kRcD + RC_CAT_TOK]);
+    m->n_cat_seqs = static_cast<int64_t>(t[kRcD + RC_CAT_SEQ]);
+    m->status = *a.status;
 }
 
 // w *= factor: float4 over the 16-byte-aligned body, scalars at the two ends.
@@ -470,23 +460,14 @@ __global__ void rc_scale_kernel(float* w, int64_t T, const float* factor) {
 // ----------------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------------
-// Workspace: a 256-byte header (groups done, status, factor), the per-group arrival counts,
-// the group totals, then the per-sequence records.
+// Workspace: a 256-byte header (status, factor), then the per-sequence records.
 constexpr size_t kRcHeader = 256;
 
 static size_t rc_record_bytes(int64_t B) {
     return align_up(static_cast<size_t>(B) * (kRcD * 8 + kRcC * 8 + 2 * 4) + 64, 256);
 }
 
-static int64_t rc_groups(int64_t B) { return (B + kRcGroup - 1) / kRcGroup; }
-static size_t rc_count_bytes(int64_t B) { return align_up(static_cast<size_t>(rc_groups(B) > 0 ? rc_groups(B) : 1) * 4, 256); }
-static size_t rc_group_bytes(int64_t B) {
-    return align_up(static_cast<size_t>(rc_groups(B) > 0 ? rc_groups(B) : 1) * kRcFields * 8, 256);
-}
-
-size_t rollout_ws_bytes(int64_t B) {
-    return kRcHeader + rc_count_bytes(B) + rc_group_bytes(B) + rc_record_bytes(B < 1 ? 1 : B);
-}
+size_t rollout_ws_bytes(int64_t B) { return kRcHeader + rc_record_bytes(B < 1 ? 1 : B); }
 
 int rollout_impl(const float* lt, const float* lr, const uint8_t* mask, const int64_t* off, int64_t B, int64_t T,
                  const rl_rc_params* p, float* w, uint8_t* keep, rl_rc_metrics* metrics, void* ws,
@@ -519,26 +500,23 @@ int rollout_impl(const float* lt, const float* lr, const uint8_t* mask, const in
     a.w = w;
     a.keep = keep;
     uint8_t* base = static_cast<uint8_t*>(ws);
-    a.done = reinterpret_cast<int*>(base);
     a.status = reinterpret_cast<int32_t*>(base + 4);
     a.factor = reinterpret_cast<float*>(base + 8);
-    a.ngroups = rc_groups(B);
-    a.gcount = reinterpret_cast<int*>(base + kRcHeader);
-    a.gd = reinterpret_cast<double*>(base + kRcHeader + rc_count_bytes(B));
-    uint8_t* rec = base + kRcHeader + rc_count_bytes(B) + rc_group_bytes(B);
+    uint8_t* rec = base + kRcHeader;
     a.pd = reinterpret_cast<double*>(rec);
     a.pc = reinterpret_cast<long long*>(a.pd + kRcD * B);
     a.pmin = reinterpret_cast<float*>(a.pc + kRcC * B);
     a.pmax = a.pmin + B;
     a.metrics = metrics;
     ProfScope ps(RL_PROF_ROLLOUT, stream);
-    // counters: the header and the per-group arrival counts
-    if (cudaMemsetAsync(ws, 0, kRcHeader + rc_count_bytes(B), stream) != cudaSuccess) return RL_ERR_CUDA;
-    int launches = 1;
-    if (B > 0)
+    if (cudaMemsetAsync(ws, 0, 16, stream) != cudaSuccess) return RL_ERR_CUDA;
+    int launches = 0;
+    if (B > 0) {
         rc_seq_kernel<<<static_cast<unsigned>(B), kRcThreads, 0, stream>>>(a);
-    else
-        rc_empty_kernel<<<1, 1, 0, stream>>>(a);
+        ++launches;
+    }
+    rc_reduce_kernel<<<1, kRcReduceThreads, 0, stream>>>(a);
+    ++launches;
     if (q.use_tis && q.norm && w != nullptr && T > 0) {
         const int64_t blocks = (T / 4 + 255) / 256 + 1;
         const int64_t cap = 4L * num_sms();
