@@ -183,3 +183,18 @@ def test_no_rl_tokens():
     torch.cuda.synchronize()
     assert float(fwd.loss.abs().max()) == 0.0 and float(dX.float().abs().max()) == 0.0
     assert float(dW.abs().max()) == 0.0 and fwd.metrics()["n_rl"] == 0
+
+
+def test_sampler_equals_trainer_and_zero_advantages():
+    """q = p (sampler logits = trainer logits, no noise) and A = 0 on every third token:
+    every weight is 1 up to rounding, nothing is masked, the mismatch KL vanishes to the
+    log-prob bar, and tokens with A = 0 keep only their KL part (the oracle agrees)."""
+    case = _small(200, V=1024, H=128, noise=0.0, age_max=2, seed=77)
+    case.adv[::3] = 0.0
+    hp = _hp_c4(bwd_mode=rh.RL_BWD_DENSE)
+    fwd, dX, dW = check_fused(case, hp)
+    m = fwd.metrics()
+    assert m["masked"] == 0
+    assert abs(m["mismatch_kl"]) <= 1e-4 * m["n_rl"]
+    dev, batch, fwd2 = _forward(case, hp)
+    check_backward(case, hp, batch, fwd2)
