@@ -189,7 +189,8 @@ def test_sampler_equals_trainer_and_zero_advantages():
     """q = p (sampler logits = trainer logits, no noise) and A = 0 on every third token:
     every weight is 1 up to rounding, nothing is masked, the mismatch KL vanishes to the
     log-prob bar, and tokens with A = 0 keep only their KL part (the oracle agrees)."""
-    case = _small(200, V=1024, H=128, noise=0.0, age_max=2, seed=77)
+    case = workloads.make_head_case("c1", n_tokens=200, H=128, V=1024, hidden_scale=4.0, noise=0.0, age_max=2,
+                                    seed=77)
     case.adv[::3] = 0.0
     hp = _hp_c4(bwd_mode=rh.RL_BWD_DENSE)
     fwd, dX, dW = check_fused(case, hp)
