@@ -242,9 +242,8 @@ typedef struct rl_pg_metrics {
                                     out (the outputs and metrics are then incomplete) */
 } rl_pg_metrics;
 
-/* Workspace bytes for T tokens: a 256-byte header (counters and the metric accumulators)
- * and a list of max(4096, T / 16) tokens whose decisions are re-taken exactly.  A smaller
- * list is allowed down to the header alone: its overflow only costs a slower exact pass. */
+/* Workspace bytes for T tokens: 256 bytes (counters and the metric accumulators), for any
+ * T.  The argument stays so that callers need not change if a later layout depends on T. */
 size_t rl_policy_workspace_bytes(int64_t T);
 /* All arrays device [T] fp32 (mask uint8, 1 = valid response token).  Output arrays may
  * be NULL to skip; masked tokens get 0.  metrics: device, overwritten; NULL to skip. */
@@ -260,8 +259,8 @@ int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const
  * trainer or inference engine whose device memory is reserved up front by its own pool,
  * where an extra cudaMalloc would fail or compete with that pool, or plain C code with
  * no device allocator at hand.  This variant takes no workspace and allocates nothing:
- * its scratch (counters, the metric accumulators and the list of tokens whose decisions
- * are re-taken exactly) is a file-scope device array of 524288 bytes.
+ * its scratch (counters and the metric accumulators) is a file-scope device array of 4096
+ * bytes.
  *   - Every GPU that loads the library holds that array until the process exits.
  *   - The first call on a device looks the array's device address up (once per
  *     device); make that first call before any stream capture.

@@ -21,18 +21,15 @@
 //                          mbarriers); branch-free fp32 math, thresholds and their bands
 //                          prepared on the host, the IPO curve as a per-thread histogram
 //                          over the sorted eps (binary search; only the two neighbouring
-//                          eps are band-checked).  A token inside a band goes to its
-//                          block's list in shared memory (or, if that is full, to a global
-//                          spill list); an exact warp takes the block's listed tokens
-//                          while the stream goes on (outputs rewritten, contributions in
-//                          2^-24 fixed point, exact and so independent of the list order).
+//                          eps are band-checked).  A token inside a band is re-decided
+//                          exactly by the thread that met it.
 //  2. policy_slow_kernel   the whole pass with exact decisions in the bands, for inputs the
 //                          fast pass does not take (unaligned, T >= 2^31).
 //  Each block adds its partial (fp32 sums in a fixed order within the block, then in 2^-24
 //  fixed point; counts) to the batch accumulators with integer atomics, whose total does
 //  not depend on the order of arrival; the last block to arrive (an arrival counter)
-//  takes the spill list's tokens and writes the metrics.  If the spill list overflowed,
-//  that block redoes the whole batch with exact decisions instead (slow, correct).
+//  writes the metrics.  If a block's sum was too large for the fixed point, that block
+//  redoes the whole batch's metrics with exact decisions instead (slow, correct).
 //
 // Results are bitwise reproducible for a given device and T.
 #include <cmath>
@@ -54,8 +51,6 @@ constexpr int kPgStageSlots = 2 * kPgThreads;   // token slots per stage of the 
 constexpr int kPgDepth = 6;       // stages in its ring
 constexpr int kPgSlowPerSm = 2;
 constexpr float kPgFix = 16777216.f;   // 2^24: fixed-point scale of the metric sums
-constexpr int kPgBlockBand = 1024;  // band tokens a fast-pass block keeps in shared memory
-constexpr int kPgBandRows = 64;     // band tokens taken per step (one shared-memory row each)
 
 // ----------------------------------------------------------------------------------
 // Parameters
@@ -90,11 +85,8 @@ struct PgArgs {
     int* range;                   // set when a sum term is too large for the fixed point
     float range_lim;              // |term| bound that keeps every accumulator inside int64
     int nb;                       // blocks of the pass
-    int* count;                   // global spill list: length (may exceed cap: overflow)
     int* done;                    // blocks that have written their partial
     int32_t* status;              // RL_STATUS_* bits of this call
-    int* list;
-    int cap;
     rl_pg_metrics* metrics;       // or nullptr
 };
 
@@ -123,6 +115,7 @@ RL_DEVINL float exp_fast(float x) { return exp2_approx(x * kLog2e); }
 struct PgExact {
     bool clip, dual, tis_trunc, ice_lo, ice_hi;
     unsigned curve;   // bit k: |p_old - p_samp| > curve_eps[k] (caller's order)
+    int j;            // how many of the sorted eps lie below |p_old - p_samp|
 };
 
 // With x = lp_theta - lp_old and d = lp_old - lp_samp exact:
@@ -143,8 +136,12 @@ RL_DEVINL PgExact pg_exact(float lt, float lo, float ls, float A, const PgPrep& 
     FF diff = ff_add(eo, {-es.hi, -es.lo});
     if (diff.hi < 0.f) diff = {-diff.hi, -diff.lo};
     e.curve = 0u;
+    e.j = 0;
     for (int k = 0; k < q.n; ++k)
-        if (ff_gt(diff, {q.eps[k], 0.f})) e.curve |= 1u << q.perm[k];
+        if (ff_gt(diff, {q.eps[k], 0.f})) {
+            e.curve |= 1u << q.perm[k];
+            ++e.j;
+        }
     return e;
 }
 
@@ -211,13 +208,6 @@ RL_DEVINL void pg_token(float lt, float lo, float ls, float A, bool valid, const
     acc.cnt[5] += tis_trunc ? 1 : 0;
 #pragma unroll
     for (int k = 0; k < RL_PG_MAX_CURVE; ++k) acc.cnt[6 + k] += (curve >> k) & 1u;
-}
-
-// pg_token for one listed band token (always valid), outputs into out[4].  Inline like
-// every helper here: a kernel parameter passed by reference to an out-of-line function
-// would be copied to local memory, and each access through it would be a local load.
-RL_DEVINL void pg_token_listed(float lt, float lo, float ls, float A, const PgPrep& q, float* out, PgAcc& acc) {
-    pg_token(lt, lo, ls, A, true, q, out[0], out[1], out[2], out[3], acc);
 }
 
 // Every token of [tid, T) with stride nthreads on the exact path (scalar loads, any
@@ -293,43 +283,6 @@ RL_DEVINL long long pg_fix(const PgArgs& a, float v) {
     return 0;
 }
 
-// Exact-path tokens list[0, n), kPgBandRows at a time (thread i < kPgBandRows takes one
-// and fills its shared-memory row: sums in 2^-24 fixed point, counts), then thread
-// k < kPgFields adds column k into fix[k] (shared).  Integer sums are exact, so the order
-// of the list does not matter.  Outputs of the listed tokens are rewritten.  Called by
-// every thread of the block.
-RL_DEVINL void pg_band_tokens(const PgArgs& a, const int* list, int n, long long* fix) {
-    __shared__ long long rows[kPgBandRows][kPgFields];
-    for (int c0 = 0; c0 < n; c0 += kPgBandRows) {
-        if (threadIdx.x < kPgBandRows) {
-            long long* row = rows[threadIdx.x];
-            const int e = c0 + threadIdx.x;
-            if (e < n) {
-                const int64_t t = list[e];
-                PgAcc one;
-                pg_zero(one);
-                float o[4];
-                pg_token_listed(a.lt[t], a.lo[t], a.ls[t], a.adv[t], a.q, o, one);
-                if (a.loss_ppo) a.loss_ppo[t] = o[0];
-                if (a.loss_dec) a.loss_dec[t] = o[1];
-                if (a.grad_ppo) a.grad_ppo[t] = o[2];
-                if (a.grad_dec) a.grad_dec[t] = o[3];
-                for (int f = 0; f < kPgSums; ++f) row[f] = pg_fix(a, one.sum[f]);
-                for (int f = 0; f < kPgCounts; ++f) row[kPgSums + f] = one.cnt[f];
-            } else {
-                for (int f = 0; f < kPgFields; ++f) row[f] = 0;
-            }
-        }
-        __syncthreads();
-        if (threadIdx.x < kPgFields) {
-            long long v = 0;
-            for (int r = 0; r < kPgBandRows; ++r) v += rows[r][threadIdx.x];
-            fix[threadIdx.x] += v;
-        }
-        __syncthreads();
-    }
-}
-
 // ----------------------------------------------------------------------------------
 // Batch totals
 // ----------------------------------------------------------------------------------
@@ -342,18 +295,11 @@ RL_DEVINL void pg_add_partial(const PgArgs& a, int k, float sum, long long count
     if (x != 0) atomicAdd(reinterpret_cast<unsigned long long*>(a.acc + k), static_cast<unsigned long long>(x));
 }
 
-// The last block of the pass to finish: the spill list's tokens, then the accumulators
-// into the metrics.  If the spill list overflowed, or a sum term was too large for the
-// fixed point, the whole batch again with exact decisions and fp32 sums instead (one
-// block: slow, correct).  Called by every thread of the last block.
+// The last block of the pass to finish: the accumulators into the metrics.  If a sum
+// term was too large for the fixed point, the whole batch again with exact decisions and
+// fp32 sums instead (one block: slow, correct).  Called by every thread of the last block.
 RL_DEVINL void pg_final(const PgArgs& a) {
-    const int cnt = __ldcg(a.count);
-    __shared__ long long fix[kPgFields];
-    if (threadIdx.x < kPgFields) fix[threadIdx.x] = 0;
-    __syncthreads();
-    if (cnt > 0 && cnt <= a.cap) pg_band_tokens(a, a.list, cnt, fix);
-    __syncthreads();
-    if (cnt > a.cap || __ldcg(a.range) != 0) {
+    if (__ldcg(a.range) != 0) {
         PgAcc acc;
         pg_zero(acc);
         pg_exact_pass(a, threadIdx.x, blockDim.x, acc);
@@ -371,7 +317,7 @@ RL_DEVINL void pg_final(const PgArgs& a) {
     if (!a.metrics) return;
     const int k = threadIdx.x;
     if (k < kPgFields) {
-        const long long v = static_cast<long long>(__ldcg(reinterpret_cast<const unsigned long long*>(a.acc + k))) + fix[k];
+        const long long v = static_cast<long long>(__ldcg(reinterpret_cast<const unsigned long long*>(a.acc + k)));
         pg_write_metric(k, k < kPgSums ? static_cast<double>(v) * (1.0 / kPgFix) : static_cast<double>(v), a.metrics);
     }
     if (k == 0) a.metrics->status = __ldcg(a.status);
@@ -465,13 +411,35 @@ RL_DEVINL PgTok pg_fast(float lt, float lo, float ls, float A, const PgPrep& q) 
     return o;
 }
 
+// A token inside a band, re-decided exactly (float-float) by the thread that met it: the
+// decisions, then the outputs and the sum term that depend on them (loss_ppo and the two
+// gradients); the values no decision touches stay as pg_fast formed them.
+RL_DEVINL void pg_resolve(PgTok& o, float lt, float lo, float ls, float A, const PgPrep& q) {
+    const PgExact e = pg_exact(lt, lo, ls, A, q);
+    const float r = exp_fast(lt - lo);
+    const float lc = fmaxf(-A * r, -A * fminf(fmaxf(r, q.lo_b), q.hi_b));
+    const float rho = fminf(exp_fast(lo - ls), q.tis);
+    const float loss_ppo = e.dual ? -A * q.cc : lc;
+    const float g_c = e.clip ? 0.f : -A * r;
+    o.lp = loss_ppo;
+    o.gp = e.dual ? 0.f : g_c;
+    o.gd = rho * g_c;
+    o.s[0] = loss_ppo;
+    o.clip = e.clip;
+    o.dual = e.dual;
+    o.ice_lo = e.ice_lo;
+    o.ice_hi = e.ice_hi;
+    o.tis = e.tis_trunc;
+    o.j = e.j;
+    o.band = false;
+}
+
 struct PgFastAcc {
     float sum[kPgSums];
     int cnt[6];
 };
 
-// Take one token's values unless it is masked out or in a band (then outputs are 0 here;
-// a band token goes to the list).
+// Take one token's values unless it is masked out (band tokens are resolved first).
 RL_DEVINL void pg_take(const PgTok& t, bool valid, int* hist, PgFastAcc& acc, float& lp, float& ld, float& gp,
                        float& gd) {
     const bool use = valid & !t.band;
@@ -492,10 +460,6 @@ RL_DEVINL void pg_take(const PgTok& t, bool valid, int* hist, PgFastAcc& acc, fl
     hist[t.j * kPgThreads] += u;
 }
 
-RL_DEVINL void pg_append(const PgArgs& a, int64_t t) {
-    const int s = atomicAdd(a.count, 1);
-    if (s < a.cap) a.list[s] = static_cast<int>(t);
-}
 
 // One stage of the ring: kPgStageSlots consecutive token slots of the five inputs.
 struct alignas(16) PgStage {
@@ -518,38 +482,31 @@ RL_DEVINL void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* b
 // Stages of kPgStageSlots slots are dealt round-robin to the blocks (block b takes stages
 // b, b + nb, b + 2 nb, ... with nb odd, so a block's stages walk through every phase of a
 // power-of-two padding period and the valid tokens, where the arithmetic is, spread
-// evenly).  Warp-specialised, 320 threads:
+// evenly).  Warp-specialised, 288 threads:
 //   * warps 0-7 (consumers) take 2 consecutive slots each per stage (vector shared-memory
 //     reads, streaming stores) and release the stage on its "empty" mbarrier (one
-//     arrival per warp), so no consumer waits for another; a token inside a band goes to
-//     the block's list;
+//     arrival per warp), so no consumer waits for another; a token inside a band is
+//     re-decided exactly on the spot by the thread that met it (rare: the warp waits
+//     for that lane, the other warps go on);
 //   * warp 8 (producer): lane 0 fills a ring of kPgDepth shared-memory stages with bulk
-//     copies, five per stage, one "full" mbarrier per stage;
-//   * warp 9 (exact): takes the listed band tokens while the stream goes on (exact
-//     decisions, outputs rewritten, contributions into the block's fixed-point sums), so
-//     their latency stays off the block's tail.
-// The last T mod 16 slots go to the last block with scalar loads.  Every wait is bounded:
-// on a timeout the block records RL_STATUS_TIMEOUT, stops, and waits (bounded) for the
-// copies it still has in flight.
-__global__ void __launch_bounds__(kPgThreads + 64, kPgFastPerSm) policy_fast_kernel(PgArgs a) {
+//     copies, five per stage, one "full" mbarrier per stage.
+// A thread's tokens and their order are fixed by the stage assignment, so its fp32 sums,
+// and with them the block partial, are reproducible.  The last T mod 16 slots go to the
+// last block with scalar loads.  Every wait is bounded: on a timeout the block records
+// RL_STATUS_TIMEOUT, stops, and waits (bounded) for the copies it still has in flight.
+__global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_kernel(PgArgs a) {
     extern __shared__ __align__(128) uint8_t pg_smem[];
     PgStage* ring = reinterpret_cast<PgStage*>(pg_smem);
     __shared__ __align__(8) uint64_t full[kPgDepth];
     __shared__ __align__(8) uint64_t empty[kPgDepth];
     __shared__ int hist_s[kPgBins * kPgThreads];   // bin-major: thread t's bin b at b * 256 + t
-    __shared__ int blist[kPgBlockBand];            // this block's band tokens (-1: not yet written)
-    __shared__ int bcount;
-    __shared__ int cons_done;                      // consumer warps past their last listing
     __shared__ int abort_flag;
-    __shared__ long long bfix[kPgFields];
-    __shared__ long long xrow[32][kPgFields];      // the exact warp's per-lane fixed-point sums
 
     const int64_t n16 = a.T >> 4;
     const int64_t nstages = (n16 * 16 + kPgStageSlots - 1) / kPgStageSlots;
     const int64_t mine = blockIdx.x < nstages ? (nstages - blockIdx.x + a.nb - 1) / a.nb : 0;
     const int nst = static_cast<int>(mine);
     const bool consumer = threadIdx.x < kPgThreads;
-    const bool producer = threadIdx.x >= kPgThreads && threadIdx.x < kPgThreads + 32;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (threadIdx.x == kPgThreads) {
         for (int s = 0; s < kPgDepth; ++s) {
@@ -558,16 +515,9 @@ __global__ void __launch_bounds__(kPgThreads + 64, kPgFastPerSm) policy_fast_ker
         }
         fence_mbar_init();
     }
-    if (threadIdx.x == 0) {
-        bcount = 0;
-        cons_done = 0;
-        abort_flag = 0;
-    }
+    if (threadIdx.x == 0) abort_flag = 0;
     if (consumer)
         for (int b = 0; b <= a.q.n; ++b) hist_s[b * kPgThreads + threadIdx.x] = 0;
-    for (int i = threadIdx.x; i < kPgBlockBand; i += blockDim.x) blist[i] = -1;
-    if (threadIdx.x < kPgFields) bfix[threadIdx.x] = 0;
-    for (int i = threadIdx.x; i < 32 * kPgFields; i += blockDim.x) (&xrow[0][0])[i] = 0;
     __syncthreads();
 
     PgFastAcc acc;
@@ -575,61 +525,10 @@ __global__ void __launch_bounds__(kPgThreads + 64, kPgFastPerSm) policy_fast_ker
     for (int k = 0; k < kPgSums; ++k) acc.sum[k] = 0.f;
 #pragma unroll
     for (int k = 0; k < 6; ++k) acc.cnt[k] = 0;
-    auto band = [&](int64_t t) {
-        const int s = atomicAdd(&bcount, 1);
-        if (s < kPgBlockBand)
-            atomicExch(blist + s, static_cast<int>(t));
-        else
-            pg_append(a, t);   // spill to the global list (the last block takes it)
-    };
     auto stage_start = [&](int i) { return (static_cast<int64_t>(i) * a.nb + blockIdx.x) * kPgStageSlots; };
     volatile int* vflag = &abort_flag;
 
-    if (warp == kPgThreads / 32 + 1) {
-        // exact warp: lane l takes listed entries done + l; loops until the consumers are
-        // past their last listing and every listed entry is taken (bounded)
-        volatile int* vcount = &bcount;
-        volatile int* vdone = &cons_done;
-        volatile int* vlist = blist;
-        const uint64_t t0 = globaltimer_ns();
-        int taken = 0;
-        while (true) {
-            const int finished = *vdone;
-            int avail = *vcount;
-            avail = avail < kPgBlockBand ? avail : kPgBlockBand;
-            if (taken < avail) {
-                const int e = taken + lane;
-                if (e < avail) {
-                    int t = vlist[e];
-                    while (t < 0 && globaltimer_ns() - t0 < kWaitLimitNs) t = vlist[e];
-                    if (t >= 0) {
-                        __threadfence_block();   // the consumer's stores to t before ours
-                        PgAcc one;
-                        pg_zero(one);
-                        float o[4];
-                        pg_token_listed(a.lt[t], a.lo[t], a.ls[t], a.adv[t], a.q, o, one);
-                        if (a.loss_ppo) a.loss_ppo[t] = o[0];
-                        if (a.loss_dec) a.loss_dec[t] = o[1];
-                        if (a.grad_ppo) a.grad_ppo[t] = o[2];
-                        if (a.grad_dec) a.grad_dec[t] = o[3];
-                        long long* row = xrow[lane];
-                        for (int f = 0; f < kPgSums; ++f) row[f] += pg_fix(a, one.sum[f]);
-                        for (int f = 0; f < kPgCounts; ++f) row[kPgSums + f] += one.cnt[f];
-                    } else {
-                        set_status(a.status, RL_STATUS_TIMEOUT);
-                    }
-                }
-                taken = avail < taken + 32 ? avail : taken + 32;
-                continue;
-            }
-            if (finished == kPgThreads / 32 || *vflag) break;   // every listing is in avail
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                set_status(a.status, RL_STATUS_TIMEOUT);
-                break;
-            }
-            __nanosleep(200);
-        }
-    } else if (producer) {
+    if (!consumer) {
         if (lane == 0) {
             int issued = 0;
             for (int i = 0; i < nst; ++i) {
@@ -678,27 +577,19 @@ __global__ void __launch_bounds__(kPgThreads + 64, kPgFastPerSm) policy_fast_ker
                 const float2 A = *reinterpret_cast<const float2*>(st.A + j);
                 const uint32_t mw = *reinterpret_cast<const uint16_t*>(st.m + j);
                 float2 lp = make_float2(0.f, 0.f), ld = lp, gp = lp, gd = lp;
-                bool b0 = false, b1 = false;
                 if (mw != 0u) {
                     const bool v0 = (mw & 0xffu) != 0u, v1 = (mw & 0xff00u) != 0u;
-                    const PgTok t0 = pg_fast(lt.x, lo.x, ls.x, A.x, a.q);
-                    const PgTok t1 = pg_fast(lt.y, lo.y, ls.y, A.y, a.q);
+                    PgTok t0 = pg_fast(lt.x, lo.x, ls.x, A.x, a.q);
+                    PgTok t1 = pg_fast(lt.y, lo.y, ls.y, A.y, a.q);
+                    if (v0 & t0.band) pg_resolve(t0, lt.x, lo.x, ls.x, A.x, a.q);
+                    if (v1 & t1.band) pg_resolve(t1, lt.y, lo.y, ls.y, A.y, a.q);
                     pg_take(t0, v0, hist, acc, lp.x, ld.x, gp.x, gd.x);
                     pg_take(t1, v1, hist, acc, lp.y, ld.y, gp.y, gd.y);
-                    b0 = v0 & t0.band;
-                    b1 = v1 & t1.band;
                 }
                 if (a.loss_ppo) __stcs(reinterpret_cast<float2*>(a.loss_ppo + g + j), lp);
                 if (a.loss_dec) __stcs(reinterpret_cast<float2*>(a.loss_dec + g + j), ld);
                 if (a.grad_ppo) __stcs(reinterpret_cast<float2*>(a.grad_ppo + g + j), gp);
                 if (a.grad_dec) __stcs(reinterpret_cast<float2*>(a.grad_dec + g + j), gd);
-                // a band token's outputs are zero above; it is listed only after those
-                // stores (fenced), so the exact warp's rewrite lands after them
-                if (b0 | b1) {
-                    __threadfence_block();
-                    if (b0) band(g + j);
-                    if (b1) band(g + j + 1);
-                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty + slot);
@@ -708,35 +599,23 @@ __global__ void __launch_bounds__(kPgThreads + 64, kPgFastPerSm) policy_fast_ker
             const int64_t t = n16 * 16 + threadIdx.x;
             if (t < a.T) {
                 float lp = 0.f, ld = 0.f, gp = 0.f, gd = 0.f;
-                bool bt = false;
                 if (a.mask[t] != 0) {
-                    const PgTok tk = pg_fast(a.lt[t], a.lo[t], a.ls[t], a.adv[t], a.q);
+                    const float xt = a.lt[t], xo = a.lo[t], xs = a.ls[t], xa = a.adv[t];
+                    PgTok tk = pg_fast(xt, xo, xs, xa, a.q);
+                    if (tk.band) pg_resolve(tk, xt, xo, xs, xa, a.q);
                     pg_take(tk, true, hist, acc, lp, ld, gp, gd);
-                    bt = tk.band;
                 }
                 if (a.loss_ppo) a.loss_ppo[t] = lp;
                 if (a.loss_dec) a.loss_dec[t] = ld;
                 if (a.grad_ppo) a.grad_ppo[t] = gp;
                 if (a.grad_dec) a.grad_dec[t] = gd;
-                if (bt) {
-                    __threadfence_block();
-                    band(t);
-                }
             }
         }
-        __threadfence_block();   // this warp's listings before its arrival below
-        __syncwarp();
-        if (lane == 0) atomicAdd(&cons_done, 1);
     }
     __syncthreads();
-    if (threadIdx.x < kPgFields) {   // the exact warp's rows, in lane order
-        long long v = 0;
-        for (int l = 0; l < 32; ++l) v += xrow[l][threadIdx.x];
-        bfix[threadIdx.x] = v;
-    }
     // block partial: warp trees (fp32 sums, exact int32 counts), then the 8 consumer warps
-    // in order plus the band tokens' fixed-point terms, into the batch accumulators; the
-    // curve counts from the histogram, cnt_k = #(j > k), back in the caller's order
+    // in order, into the batch accumulators; the curve counts from the histogram,
+    // cnt_k = #(j > k), back in the caller's order
     __shared__ float shs[kPgThreads / 32][kPgSums];
     __shared__ int shc[kPgThreads / 32][6];
     __shared__ int bins[kPgBins];
@@ -763,11 +642,11 @@ __global__ void __launch_bounds__(kPgThreads + 64, kPgFastPerSm) policy_fast_ker
     if (f < kPgSums) {
         float v = 0.f;
         for (int w = 0; w < kPgThreads / 32; ++w) v += shs[w][f];
-        pg_add_partial(a, f, v, bfix[f]);
+        pg_add_partial(a, f, v, 0);
     } else if (f < kPgSums + 6) {
         int v = 0;
         for (int w = 0; w < kPgThreads / 32; ++w) v += shc[w][f - kPgSums];
-        pg_add_partial(a, f, 0.f, v + bfix[f]);
+        pg_add_partial(a, f, 0.f, v);
     } else if (f < kPgFields) {
         const int c = f - kPgSums - 6;        // caller's curve index
         int v = 0;
@@ -776,7 +655,7 @@ __global__ void __launch_bounds__(kPgThreads + 64, kPgFastPerSm) policy_fast_ker
             while (a.q.perm[js] != c) ++js;
             for (int b = js + 1; b <= a.q.n; ++b) v += bins[b];
         }
-        pg_add_partial(a, f, 0.f, v + bfix[f]);
+        pg_add_partial(a, f, 0.f, v);
     }
     pg_finish(a);
 }
@@ -784,17 +663,13 @@ __global__ void __launch_bounds__(kPgThreads + 64, kPgFastPerSm) policy_fast_ker
 // ----------------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------------
-// Workspace: a 256-byte header (spill-list length, arrival count, status word, range
-// flag, and at byte 16 the kPgFields accumulators), then the spill list in whatever room
-// is left.
+// Workspace: a 256-byte header (arrival count, status word, range flag, and at byte 16
+// the kPgFields accumulators).
 struct PgWs {
-    int* count;
     int* done;
     int32_t* status;
     int* range;
     long long* acc;
-    int* list;
-    int cap;
 };
 constexpr size_t kPgHeader = 256;
 static_assert(16 + kPgFields * 8 <= kPgHeader, "accumulators must fit the header");
@@ -802,25 +677,19 @@ static_assert(16 + kPgFields * 8 <= kPgHeader, "accumulators must fit the header
 static int fast_blocks(int sms) { return sms * kPgFastPerSm; }
 static int slow_blocks(int sms) { return sms * kPgSlowPerSm; }
 
-static PgWs pg_ws(void* ws, size_t ws_bytes) {
+static PgWs pg_ws(void* ws) {
     PgWs w;
     uint8_t* b = static_cast<uint8_t*>(ws);
-    w.count = reinterpret_cast<int*>(b);
     w.done = reinterpret_cast<int*>(b + 4);
     w.status = reinterpret_cast<int32_t*>(b + 8);
     w.range = reinterpret_cast<int*>(b + 12);
     w.acc = reinterpret_cast<long long*>(b + 16);
-    w.list = reinterpret_cast<int*>(b + kPgHeader);
-    const size_t room = ws_bytes > kPgHeader ? (ws_bytes - kPgHeader) / sizeof(int) : 0;
-    w.cap = room > static_cast<size_t>(INT32_MAX) ? INT32_MAX : static_cast<int>(room);
     return w;
 }
 
 size_t policy_ws_bytes(int64_t T) {
-    // the header and a band list of max(4096, T / 16) entries (the expected share of band
-    // tokens is well under 1e-3; an overflow only costs the slow fallback)
-    const int64_t list = T / 16 > 4096 ? T / 16 : 4096;
-    return align_up(kPgHeader + static_cast<size_t>(list) * sizeof(int), 256);
+    (void)T;
+    return kPgHeader;
 }
 
 static PgPrep prepare(const rl_pg_params& p) {
@@ -867,7 +736,7 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
                 void* ws, size_t ws_bytes, cudaStream_t stream) {
     const int sms = num_sms();
     if (ws_bytes < kPgHeader) return RL_ERR_WORKSPACE;
-    const PgWs w = pg_ws(ws, ws_bytes);
+    const PgWs w = pg_ws(ws);
     auto al = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
     const bool fast = T < (int64_t(1) << 31) && al(lt) && al(lo) && al(ls) && al(adv) && al(mask) &&
                       al(loss_ppo) && al(loss_dec) && al(grad_ppo) && al(grad_dec);
@@ -884,11 +753,8 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
     a.loss_dec = loss_dec;
     a.grad_ppo = grad_ppo;
     a.grad_dec = grad_dec;
-    a.count = w.count;
     a.done = w.done;
     a.status = w.status;
-    a.list = w.list;
-    a.cap = w.cap;
     a.acc = w.acc;
     a.range = w.range;
     a.metrics = metrics;
@@ -902,13 +768,13 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
         smem_set[dev] = 1;
     }
     ProfScope ps(RL_PROF_POLICY, stream);
-    // spill count, arrival count, status, accumulators
+    // arrival count, status, range flag, accumulators
     if (cudaMemsetAsync(ws, 0, kPgHeader, stream) != cudaSuccess) return RL_ERR_CUDA;
     a.nb = fast ? fast_blocks(sms) - 1 : slow_blocks(sms);   // fast: odd, see policy_fast_kernel
     // a term below 2^38 / nb keeps each accumulator's total below 2^62 in 2^-24 units
     a.range_lim = ldexpf(1.f, 38) / static_cast<float>(a.nb);
     if (fast) {
-        policy_fast_kernel<<<a.nb, kPgThreads + 64, kPgStreamSmem, stream>>>(a);
+        policy_fast_kernel<<<a.nb, kPgThreads + 32, kPgStreamSmem, stream>>>(a);
     } else {
         policy_slow_kernel<<<a.nb, kPgThreads, 0, stream>>>(a);
     }

@@ -1,7 +1,6 @@
 // rl_policy_loss_elementwise_noalloc: the elementwise PPO / TIS / mismatch path for callers
-// that cannot allocate device memory.  Its scratch (counters, the fixed-point metric
-// accumulators and the band-token list) lives in a file-scope device array instead of a
-// caller workspace.
+// that cannot allocate device memory.  Its scratch (counters and the fixed-point metric
+// accumulators) lives in a file-scope device array instead of a caller workspace.
 #include <mutex>
 
 #include "common.cuh"
@@ -9,8 +8,8 @@
 
 namespace rl {
 
-// 512 KiB: a 256-byte header and, in the room left, the band-token list (131008 entries).
-constexpr size_t kNoAllocScratchBytes = 524288;
+// 4 KiB: room for the 256-byte header the elementwise pass uses.
+constexpr size_t kNoAllocScratchBytes = 4096;
 static __device__ __align__(256) double g_policy_scratch[kNoAllocScratchBytes / sizeof(double)];
 
 // Device address of g_policy_scratch for the current device, looked up once per device
@@ -63,7 +62,7 @@ extern "C" int rl_policy_loss_elementwise_noalloc(const float* lp_theta, const f
         set_last_error("needs an sm_100-family GPU");
         return RL_ERR_UNSUPPORTED;
     }
-    static_assert(kNoAllocScratchBytes >= 4096, "the scratch must hold the header");
+    static_assert(kNoAllocScratchBytes >= 256, "the scratch must hold the header");
     void* scratch = nullptr;
     int rc = scratch_address(&scratch);
     if (rc != RL_OK) return rc;

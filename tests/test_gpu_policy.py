@@ -118,14 +118,14 @@ def _band_case(T, frac, seed):
 
 
 def test_many_band_tokens_fixup_path():
-    """About 10% of 20000 tokens sit on a clip threshold: all of them go through the exact
-    fix-up list (below its 4096-entry floor) and every count stays exact."""
+    """About 10% of 20000 tokens sit on a clip threshold: each is re-decided exactly by
+    the thread that meets it, and every count stays exact."""
     _compare(*_band_case(20000, 0.1, 5), rh.PgParams())
 
 
-def test_band_list_overflow_falls_back_to_exact_pass():
-    """Half of 200000 tokens on a clip threshold overflow the band list (T / 16 entries):
-    the gated exact pass replaces the fast one; results equal the oracle's."""
+def test_half_the_tokens_in_a_band():
+    """Half of 200000 tokens on a clip threshold: the exact re-decisions dominate the pass
+    (a worst case for its time, not its results); results equal the oracle's."""
     _compare(*_band_case(200_000, 0.5, 6), rh.PgParams())
 
 
