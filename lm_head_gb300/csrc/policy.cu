@@ -443,13 +443,12 @@ struct PgFastAcc {
 RL_DEVINL void pg_take(const PgTok& t, bool valid, int* hist, PgFastAcc& acc, float& lp, float& ld, float& gp,
                        float& gd) {
     const bool use = valid & !t.band;
-    const float f = use ? 1.f : 0.f;
     lp = use ? t.lp : 0.f;
     ld = use ? t.ld : 0.f;
     gp = use ? t.gp : 0.f;
     gd = use ? t.gd : 0.f;
 #pragma unroll
-    for (int k = 0; k < kPgSums; ++k) acc.sum[k] = fmaf(f, t.s[k], acc.sum[k]);
+    for (int k = 0; k < kPgSums; ++k) acc.sum[k] += use ? t.s[k] : 0.f;   // a select: a masked NaN stays out
     const int u = use;
     acc.cnt[0] += u;
     acc.cnt[1] += u & t.clip;

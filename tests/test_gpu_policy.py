@@ -178,3 +178,60 @@ def test_huge_sum_terms_take_the_exact_metric_pass():
     m = np.ones(T, np.uint8)
     gm, rm = _compare(lt, lo, ls, A, m, rh.PgParams())
     assert rm["k3"] > 1e13
+
+
+def _padding_case(seed):
+    """Masks that leave whole 512-slot stages empty, put single valid tokens on stage
+    edges (their pair partner is padding), valid prefixes of random length, a ragged
+    16-slot group and a scalar tail; every padded slot holds NaN or +-inf."""
+    rng = np.random.default_rng(seed)
+    T = 512 * 303 * 5 + 512 * 7 + 48 + 5
+    lt = rng.normal(-1, 0.5, T).astype(np.float32)
+    lo = (lt + rng.normal(0, 0.3, T)).astype(np.float32)
+    ls = (lo + rng.normal(0, 0.5, T)).astype(np.float32)
+    A = rng.normal(0, 1, T).astype(np.float32)
+    m = np.zeros(T, np.uint8)
+    for k in range((T + 511) // 512):
+        b = 512 * k
+        kind = k % 5
+        if kind == 1:
+            m[b:b + 512] = 1
+        elif kind == 2:
+            m[b] = 1
+        elif kind == 3:
+            m[min(b + 511, T - 1)] = 1
+        elif kind == 4:
+            m[b:b + int(rng.integers(1, 512))] = 1
+    m[-3:] = (1, 0, 7)          # any nonzero mask byte is a valid token
+    pad = m == 0
+    for x in (lt, lo, ls, A):
+        x[pad] = rng.choice(np.array([np.nan, np.inf, -np.inf], np.float32), int(pad.sum()))
+    return lt, lo, ls, A, m
+
+
+def test_padding_stages_and_nonfinite_padding():
+    """Whole 512-slot stages of padding, and valid tokens whose neighbour in the same
+    two-slot step is padding: the values in padded slots (here NaN and inf) reach
+    neither the outputs nor the sums."""
+    lt, lo, ls, A, m = _padding_case(12)
+    with np.errstate(invalid="ignore", over="ignore"):
+        gm, rm = _compare(lt, lo, ls, A, m, rh.PgParams())
+    assert gm["n_valid"] == int((m != 0).sum())
+    for k in ("loss_ppo", "loss_dec", "tis_sum", "ppo_kl", "mis_kl", "k3"):
+        assert np.isfinite(gm[k]), k
+
+
+def test_all_padding():
+    """No valid token at all, every input NaN: zero outputs, zero counts and sums."""
+    T = 512 * 400 + 16 + 3
+    nan = np.full(T, np.nan, np.float32)
+    pp = rh.PgParams()
+    (lp, ld, gp, gd), gm = _run(nan, nan, nan, nan, np.zeros(T, np.uint8), pp)
+    assert gm["status"] == 0 and gm["n_valid"] == 0
+    for o in (lp, ld, gp, gd):
+        assert not np.any(o)
+    for k in ("loss_ppo", "loss_dec", "tis_sum", "ppo_kl", "mis_kl", "k3"):
+        assert gm[k] == 0.0, k
+    for k in ("n_clip", "n_clip_lower", "icepop_low", "icepop_high", "n_tis_trunc"):
+        assert gm[k] == 0, k
+    assert gm["ipo_curve"] == [0] * len(pp.curve_eps)
