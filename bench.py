@@ -504,7 +504,7 @@ def run_ours(args):
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of each kernel, from the ncu
 # captures summarised under profiles/ (one launch at the bench's 16384-token chunk).
-TRAFFIC = {"gemm_fwd_stats": 8134179328 + 9935567360}
+TRAFFIC = {"gemm_fwd_stats": 12292000000 + 9935062272}
 
 
 def ctypes_metrics_size(rh):

@@ -184,3 +184,21 @@ def test_masked_tokens_contribute_nothing():
     assert a["metrics"]["n_valid"] == b["metrics"]["n_valid"]
     assert abs(a["metrics"]["loss_ppo"] - b["metrics"]["loss_ppo"]) < 1e-12
     assert np.all(a["loss_ppo"][m == 0] == 0)
+
+
+def test_nonfinite_padding_changes_nothing():
+    """NaN / inf in padded slots: every output and metric equals the run with finite
+    padding (padding does not count at all)."""
+    rng = np.random.default_rng(6)
+    T = 200
+    m = (rng.random(T) < 0.5).astype(np.uint8)
+    args = [rng.normal(-1, 0.3, T), rng.normal(-1, 0.3, T), rng.normal(-1, 0.3, T), rng.normal(0, 1, T)]
+    a = policy_loss_elementwise(*args, m, PolicyParams())
+    bad = [x.copy() for x in args]
+    for x in bad:
+        x[m == 0] = rng.choice([np.nan, np.inf, -np.inf], int((m == 0).sum()))
+    with np.errstate(invalid="ignore", over="ignore"):
+        b = policy_loss_elementwise(*bad, m, PolicyParams())
+    for k in ("loss_ppo", "loss_dec", "grad_ppo", "grad_dec"):
+        assert np.array_equal(a[k], b[k]), k
+    assert a["metrics"] == b["metrics"]

@@ -203,3 +203,30 @@ def test_log_perplexity_is_a_mean_over_sequences():
     assert nm["training_ppl"] == pytest.approx(math.exp(2.0))
     # chi2_seq with the sequence weights exp(0) and exp(30 * 0.5)
     assert nm["chi2_seq"] == pytest.approx((1.0 + math.exp(30.0)) / 2 - 1.0)
+
+
+def test_nonfinite_padding_changes_nothing():
+    """NaN / inf in masked slots: weights, keep flags and metrics equal the run with
+    finite values there (padding does not count at all)."""
+    rng = np.random.default_rng(14)
+    lens = [7, 0, 12, 5]
+    T = sum(lens)
+    off = np.concatenate([[0], np.cumsum(lens)])
+    lr = np.log(rng.random(T) * 0.9 + 0.05)
+    lt = np.minimum(lr + rng.normal(0, 0.3, T), 0.0)
+    m = (rng.random(T) < 0.6).astype(np.uint8)
+    bad_t, bad_r = lt.copy(), lr.copy()
+    pad = m == 0
+    bad_t[pad] = rng.choice([np.nan, np.inf, -np.inf], int(pad.sum()))
+    bad_r[pad] = rng.choice([np.nan, np.inf, -np.inf], int(pad.sum()))
+    for rp in (RolloutParams(tis_mode=TIS_CLIP, tis_lower_bound=0.5, tis_upper_bound=2.0, tis_level=LEVEL_SEQUENCE,
+                             tis_batch_normalize=True, use_rs=True, rs_level=LEVEL_GEOMETRIC, rs_lower_bound=0.5,
+                             rs_upper_bound=2.0, rs_veto_threshold=1e-3),
+               RolloutParams(tis_lower_bound=0.5, tis_upper_bound=2.0, use_rs=True, rs_level=LEVEL_TOKEN,
+                             rs_lower_bound=0.5, rs_upper_bound=2.0)):
+        a = rollout_correction(lt, lr, m, off, rp)
+        with np.errstate(invalid="ignore", over="ignore"):
+            b = rollout_correction(bad_t, bad_r, m, off, rp)
+        np.testing.assert_array_equal(a["weights"], b["weights"])
+        np.testing.assert_array_equal(a["keep"], b["keep"])
+        assert a["metrics"] == b["metrics"]
