@@ -235,3 +235,18 @@ def test_all_padding():
     for k in ("n_clip", "n_clip_lower", "icepop_low", "icepop_high", "n_tis_trunc"):
         assert gm[k] == 0, k
     assert gm["ipo_curve"] == [0] * len(pp.curve_eps)
+
+
+def test_bitwise_reproducible():
+    """Three c5 passes give identical bytes: metrics (integer accumulators, whatever the
+    order in which blocks arrive) and outputs."""
+    c = workloads.make_policy_case()
+    d = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (c.lp_theta, c.lp_old, c.lp_samp, c.adv, c.mask)]
+    runs = []
+    for _ in range(3):
+        out = rh.rl_policy_loss_elementwise(*d, rh.PgParams())
+        torch.cuda.synchronize()
+        runs.append((bytes(out[4].cpu().numpy().tobytes()), [o.cpu().numpy().tobytes() for o in out[:4]]))
+    for r in runs[1:]:
+        assert r[0] == runs[0][0]
+        assert r[1] == runs[0][1]

@@ -143,3 +143,16 @@ def test_bad_offsets_set_the_status_bit():
                                          torch.ones(T, dtype=torch.uint8, device="cuda"), off, rh.RcParams())
     torch.cuda.synchronize()
     assert rh.rc_metrics(met)["status"] & 0x1
+
+
+def test_nonfinite_padding():
+    """NaN / inf in every masked slot of the c5 rows (their padding and the masked tokens
+    inside): results equal the oracle's, which ignores them."""
+    lt, lr, m, off = (np.array(x) for x in _c5())
+    rng = np.random.default_rng(15)
+    pad = m == 0
+    lt[pad] = rng.choice(np.array([np.nan, np.inf, -np.inf], np.float32), int(pad.sum()))
+    lr[pad] = rng.choice(np.array([np.nan, np.inf, -np.inf], np.float32), int(pad.sum()))
+    with np.errstate(invalid="ignore", over="ignore"):
+        for cfg in (1, 2, 3):
+            _compare(lt, lr, m, off, CONFIGS[cfg])
