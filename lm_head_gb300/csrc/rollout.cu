@@ -17,8 +17,10 @@
 //                       of partial sums per sequence.
 //  2. rc_reduce_kernel  one block, one warp per field: the records summed in sequence
 //                       order (fixed tree), so results are reproducible; then the
-//                       batch-normalisation factor and the metrics.
-//  3. rc_scale_kernel   (batch normalisation only) weights *= factor.
+//                       metrics.  Without batch normalisation only.
+//  2'. rc_scale_kernel  with batch normalisation, instead: every block forms the factor
+//                       from the records in the same order (block 0 also all fields and
+//                       the metrics), then weights *= factor.
 #include <cmath>
 #include <climits>
 
@@ -28,7 +30,7 @@
 
 namespace rl {
 
-constexpr int kRcThreads = 256;
+constexpr int kRcThreads = 128;
 // per-sequence record: double sums, int64 counts, then the kept weights' min and max
 enum {
     RD_W_BEFORE, RD_W_AFTER, RD_KEPT_W, RD_MIS_KL, RD_K3, RD_ABS, RD_CHI2T, RD_TRAIN_LPPL, RD_ROLL_LPPL,
@@ -102,12 +104,16 @@ struct RcSeq {   // one sequence's decisions (thread 0 -> block)
 
 // A sequence is staged in shared memory kRcChunk tokens at a time (coalesced loads,
 // no alignment needed); a sequence of at most kRcChunk tokens is read from memory once
-// for both passes, a longer one chunk by chunk in each pass.  Loops stay rolled: the
-// code is fetched cold by every block, so its size is part of the latency.
-constexpr int kRcChunk = 4096;
+// for both passes, a longer one chunk by chunk in each pass (pass 2 starts from the chunk
+// still staged; the earlier ones come back from L2).  128 threads and 2048-token chunks
+// keep eight blocks on an SM, so a batch of up to 8 x SMs sequences is resident at once
+// (256 threads with 4096-token chunks, four per SM: 4 % slower on 879 sequences of 4096
+// slots).  Loops stay rolled: the code is fetched cold by every block, so its size is
+// part of the latency.
+constexpr int kRcChunk = 2048;
 constexpr int kRcW = kRcThreads / 32;
 
-__global__ void __launch_bounds__(kRcThreads, 4) rc_seq_kernel(RcArgs a) {
+__global__ void __launch_bounds__(kRcThreads, 8) rc_seq_kernel(RcArgs a) {
     __shared__ float s_lt[kRcChunk], s_lr[kRcChunk];
     __shared__ uint8_t s_m[kRcChunk];
     __shared__ FF shff[kRcW][4];
@@ -346,14 +352,16 @@ __global__ void __launch_bounds__(kRcThreads, 4) rc_seq_kernel(RcArgs a) {
     }
 }
 
-// One block of kRcFields warps: warp f sums field f of the records over the sequences in
-// order (lane l takes b = l, l + 32, ..., eight loads in flight ahead of their adds, then
-// a butterfly); thread 0 then forms the factor and writes the metrics.
+// Warp f sums field f of the records over the sequences in order (lane l takes
+// b = l, l + 32, ..., eight loads in flight ahead of their adds, then a butterfly) into
+// tot[f].  With only_factor, just the two fields the batch-normalisation factor needs.
+// Every block that calls it computes the same bits.
 constexpr int kRcReduceThreads = 32 * kRcFields;
-__global__ void __launch_bounds__(kRcReduceThreads) rc_reduce_kernel(RcArgs a) {
-    __shared__ double tot[kRcFields];
+RL_DEVINL void rc_reduce_fields(const RcArgs& a, double* tot, bool only_factor) {
     const int f = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t B = a.B;
+    if (f >= kRcFields) return;
+    if (only_factor && f != RD_KEPT_W && f != kRcD + RC_KEPT) return;
     if (f < kRcD) {
         const double* src = a.pd + f * B;
         double v = 0.0;
@@ -398,11 +406,17 @@ __global__ void __launch_bounds__(kRcReduceThreads) rc_reduce_kernel(RcArgs a) {
         }
         if (lane == 0) tot[f] = v;
     }
-    __syncthreads();
-    if (threadIdx.x != 0) return;
-    const double* t = tot;
+}
+
+RL_DEVINL double rc_factor(const RcArgs& a, const double* t) {
     const double kept_w = t[RD_KEPT_W], n_kept = t[kRcD + RC_KEPT];
-    const double factor = (a.q.use_tis && a.q.norm && n_kept > 0 && kept_w > 0) ? n_kept / kept_w : 1.0;
+    return (a.q.use_tis && a.q.norm && n_kept > 0 && kept_w > 0) ? n_kept / kept_w : 1.0;
+}
+
+// The factor and the metrics from the reduced fields (one thread).
+RL_DEVINL void rc_write_metrics(const RcArgs& a, const double* t) {
+    const double kept_w = t[RD_KEPT_W], n_kept = t[kRcD + RC_KEPT];
+    const double factor = rc_factor(a, t);
     *a.factor = static_cast<float>(factor);
     rl_rc_metrics* m = a.metrics;
     if (!m) return;
@@ -435,9 +449,33 @@ __global__ void __launch_bounds__(kRcReduceThreads) rc_reduce_kernel(RcArgs a) {
     m->status = *a.status;
 }
 
-// w *= factor: float4 over the 16-byte-aligned body, scalars at the two ends.
-__global__ void rc_scale_kernel(float* w, int64_t T, const float* factor) {
-    const float f = *factor;
+
+// One block of kRcFields warps: the fields in sequence order, then the factor and the
+// metrics (used when no batch normalisation follows).
+__global__ void __launch_bounds__(kRcReduceThreads) rc_reduce_kernel(RcArgs a) {
+    __shared__ double tot[kRcFields];
+    rc_reduce_fields(a, tot, false);
+    __syncthreads();
+    if (threadIdx.x == 0) rc_write_metrics(a, tot);
+}
+
+// Batch normalisation: every block first forms the factor itself (the two fields it needs,
+// in the order rc_reduce_kernel uses, so every block has the same bits), block 0 all the
+// fields and the metrics; then w *= factor, float4 over the 16-byte-aligned body and
+// scalars at the two ends.  One launch where a reduce and a scale kernel would take two.
+__global__ void __launch_bounds__(kRcReduceThreads) rc_scale_kernel(RcArgs a) {
+    __shared__ double tot[kRcFields];
+    __shared__ float fac;
+    rc_reduce_fields(a, tot, blockIdx.x != 0);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        fac = static_cast<float>(rc_factor(a, tot));
+        if (blockIdx.x == 0) rc_write_metrics(a, tot);
+    }
+    __syncthreads();
+    const float f = fac;
+    float* w = a.w;
+    const int64_t T = a.T;
     const int64_t head = ((16 - (reinterpret_cast<uintptr_t>(w) & 15)) & 15) / 4;
     const int64_t h = head < T ? head : T;
     const int64_t n4 = (T - h) / 4;
@@ -515,14 +553,15 @@ int rollout_impl(const float* lt, const float* lr, const uint8_t* mask, const in
         rc_seq_kernel<<<static_cast<unsigned>(B), kRcThreads, 0, stream>>>(a);
         ++launches;
     }
-    rc_reduce_kernel<<<1, kRcReduceThreads, 0, stream>>>(a);
-    ++launches;
     if (q.use_tis && q.norm && w != nullptr && T > 0) {
-        const int64_t blocks = (T / 4 + 255) / 256 + 1;
-        const int64_t cap = 4L * num_sms();
-        rc_scale_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), 256, 0, stream>>>(w, T, a.factor);
-        ++launches;
+        // the reduction rides along with the scaling (every block forms the factor)
+        const int64_t blocks = (T / 4 + kRcReduceThreads - 1) / kRcReduceThreads + 1;
+        const int64_t cap = 2L * num_sms();
+        rc_scale_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), kRcReduceThreads, 0, stream>>>(a);
+    } else {
+        rc_reduce_kernel<<<1, kRcReduceThreads, 0, stream>>>(a);
     }
+    ++launches;
     count_launch(launches);
     return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }
