@@ -342,8 +342,9 @@ size_t rl_rollout_correction_workspace_bytes(int64_t B);
  * seq_offsets: device [B + 1] int64, sequence s = tokens [seq_offsets[s], seq_offsets[s+1])
  * (padded rows: s * row_length; packed: cumulative lengths).  Outputs, device: weights
  * [T] fp32 and keep [T] uint8 (either may be NULL), metrics (overwritten, may be NULL).
- * Errors: RL_ERR_ARG (NULL input, B < 0, T < 0, bad enum, L > U or negative bound),
- * RL_ERR_WORKSPACE; bad offsets are reported in metrics->status, not trapped. */
+ * Errors: RL_ERR_ARG (NULL input, B < 0, T < 0, B == 0 with T > 0, bad enum, L > U or
+ * negative bound), RL_ERR_WORKSPACE; bad offsets are reported in metrics->status, not
+ * trapped. */
 int rl_rollout_correction(const float* lp_train, const float* lp_rollout, const uint8_t* mask,
                           const int64_t* seq_offsets, int64_t B, int64_t T,
                           const rl_rc_params* params, float* weights, uint8_t* keep,

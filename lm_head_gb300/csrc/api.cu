@@ -195,6 +195,7 @@ int rl_rollout_correction(const float* lp_train, const float* lp_rollout, const 
                           float* weights, uint8_t* keep, rl_rc_metrics* metrics, void* ws, size_t ws_bytes,
                           void* stream) {
     if (T < 0 || B < 0) return fail(RL_ERR_ARG, "T < 0 or B < 0");
+    if (B == 0 && T > 0) return fail(RL_ERR_ARG, "T > 0 with no sequence: the offsets must cover [0, T)");
     if (B >= (int64_t(1) << 31)) return fail(RL_ERR_UNSUPPORTED, "B >= 2^31");
     if (!params) return fail(RL_ERR_ARG, "params NULL");
     const rl_rc_params& p = *params;

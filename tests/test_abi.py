@@ -95,6 +95,14 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
     pp = rh.PgParams(clip_ratio_c=0.5).c()
     assert lib.rl_policy_loss_elementwise(None, None, None, None, None, 10, ctypes.byref(pp), None, None, None,
                                           None, None, None, 0, None) == rh.RL_ERR_ARG
+    rp = rh.RcParams().c()
+    ws = ctypes.create_string_buffer(4096)
+    # tokens but no sequence: nothing could assign them a weight
+    assert lib.rl_rollout_correction(None, None, None, None, 0, 5, ctypes.byref(rp), None, None, None, ws,
+                                     4096, None) == rh.RL_ERR_ARG
+    bad = rh.RcParams(tis_lower_bound=2.0, tis_upper_bound=1.0).c()
+    assert lib.rl_rollout_correction(None, None, None, None, 0, 0, ctypes.byref(bad), None, None, None, ws,
+                                     4096, None) == rh.RL_ERR_ARG
 
 
 def _declared_arity():
