@@ -7,6 +7,8 @@
   against the oracle one by one; counts that hold at any size; the identity
   <dW, W> = <dX, X> (both equal T * sum G*z); the fused backward against the two-call
   (recompute) backward.
+* The full c2 (4096 tokens) and c3 (16384 tokens) batches the same way; c3's sparse CSR
+  backward against its dense backward over the whole batch.
 * Degenerate cases: empty batch, one token, no RL tokens, one draw per row, a vocabulary
   that is not a multiple of the tile width, the smallest hidden size.
 """
@@ -18,7 +20,7 @@ import lm_head_gb300 as rh
 import oracle
 import workloads
 from gpu_checks import _forward, check_backward, check_forward, check_fused
-from parity_util import grad_check, logp_tol, loss_check, loss_prop_tol, oracle_params
+from parity_util import grad_check, logp_tol, loss_check, loss_prop_tol, margin, oracle_params, weight_keep_fp64
 
 pytestmark = pytest.mark.gpu
 
@@ -78,25 +80,21 @@ def test_c4_shapes_draws_exact_kl(prec):
         check_backward(case, hp, batch, fwd, both=False)
 
 
-def test_c4_full_size_sampled():
-    """The 64k-token batch exactly as bench.py runs it; sampled outputs vs the oracle."""
-    case = workloads.make_head_case("c4", device="cuda", seed=workloads.BASE_SEED + 4)
-    N = case.N
-    hp = _hp_c4(bwd_mode=rh.RL_BWD_DENSE)
-    batch = rh.HeadBatch.from_case(case)
-    dloss_t = (case.loss_mask.float() / case.loss_mask.float().sum()).contiguous()
-    fwd, dX, dW = rh.rl_head_loss_fwd_bwd(batch, hp, dloss_t)
-    torch.cuda.synchronize()
-    assert fwd.status_bits() == 0, rh.status_names(fwd.status_bits())
+def _sampled_rows(N, seed):
+    """Tile edges (128-row halves, 256-row pairs, 16k chunks), the ends, random rows."""
+    rng = np.random.default_rng(seed)
+    fixed = [r for r in (0, 1, 127, 128, 255, 256, 16383, 16384, 32767, 49152, N // 2, N - 1) if r < N]
+    return np.unique(np.r_[fixed, rng.integers(0, N, 13)]).astype(np.int64)
+
+
+def _check_sampled_rows(case, hp, fwd, dX, dloss_t, rows, reading="operand"):
+    """Sampled tokens' forward outputs and dX rows against the oracle, one by one."""
+    N, H = case.N, case.H
     inp = case.numpy()
     op = oracle_params(hp)
-    rng = np.random.default_rng(7)
-    rows = np.unique(np.r_[0, 1, 127, 128, 255, 256, 16383, 16384, 32767, 49152, N - 1,
-                           rng.integers(0, N, 13)]).astype(np.int64)
     ref = oracle.head_forward(inp, op, rows=rows, chunk=8)
     off = inp["offsets"]
     ent = np.concatenate([np.arange(off[t], off[t + 1]) for t in rows])
-    H = case.H
     ltol = logp_tol(H, ref["lse"], ref["lse"])
     assert np.all(np.abs(fwd.lse.cpu().double().numpy()[rows] - ref["lse"]) <= ltol)
     assert np.all(np.abs(fwd.entropy.cpu().double().numpy()[rows] - ref["entropy"]) <= ltol)
@@ -107,14 +105,38 @@ def test_c4_full_size_sampled():
     zs = ref["logp_support"] + ref["lse_s"][er]
     assert np.all(np.abs(fwd.logp_support.cpu().double().numpy()[ent] - ref["logp_support"])
                   <= logp_tol(H, zs, ref["lse_s"][er]))
+    # masks: bit-exact against the fp64 predicate on the GPU's log-probs, and equal to the
+    # oracle's own except within the log-prob tolerance of a threshold
+    lab_tol = logp_tol(H, zl, ref["lse_s"])
+    gm_lab = fwd.mask_label.cpu().numpy()[rows]
+    gm_sup = fwd.mask_support.cpu().numpy()[ent]
+    np.testing.assert_array_equal(gm_lab, weight_keep_fp64(fwd.logp_label.cpu().numpy()[rows],
+                                                           inp["label_logq"][rows], op))
+    np.testing.assert_array_equal(gm_sup, weight_keep_fp64(fwd.logp_support.cpu().numpy()[ent], inp["logq"][ent], op))
+    assert np.all((gm_lab == ref["mask_label"]) | (margin(ref["logp_label"], inp["label_logq"][rows], op) < 4 * lab_tol))
     sub = {k: (v[rows] if isinstance(v, np.ndarray) and v.shape[:1] == (N,) else v) for k, v in inp.items()}
     ptol = loss_prop_tol(dict(ref, c_support=ref["c_support"], u_support=ref["u_support"]),
                          dict(sub, offsets=np.r_[0, np.cumsum(off[rows + 1] - off[rows])]), op)
     loss_check(fwd.loss.cpu().double().numpy()[rows], ref["loss"], ptol)
-    # dX rows against the oracle (operand reading: bf16 softmax-gradient operand)
     dl = dloss_t.cpu().double().numpy()
     rX, _, bnd = oracle.head_backward(inp, op, dl, rows=rows, want_dW=False, want_bounds=True, chunk=8)
-    grad_check(dX.float().cpu().numpy()[rows], rX, "operand", "dX", bnd, "X", H)
+    grad_check(dX.float().cpu().numpy()[rows], rX, reading, "dX", bnd, "X", H)
+    return inp
+
+
+def test_c4_full_size_sampled():
+    """The 64k-token batch exactly as bench.py runs it; sampled outputs vs the oracle."""
+    case = workloads.make_head_case("c4", device="cuda", seed=workloads.BASE_SEED + 4)
+    N = case.N
+    hp = _hp_c4(bwd_mode=rh.RL_BWD_DENSE)
+    batch = rh.HeadBatch.from_case(case)
+    dloss_t = (case.loss_mask.float() / case.loss_mask.float().sum()).contiguous()
+    fwd, dX, dW = rh.rl_head_loss_fwd_bwd(batch, hp, dloss_t)
+    torch.cuda.synchronize()
+    assert fwd.status_bits() == 0, rh.status_names(fwd.status_bits())
+    # dX rows against the oracle (operand reading: bf16 softmax-gradient operand)
+    inp = _check_sampled_rows(case, hp, fwd, dX, dloss_t, _sampled_rows(N, 7))
+    H = case.H
     # counts that hold at any size
     m = fwd.metrics()
     assert m["n_rl"] == N
@@ -145,6 +167,45 @@ def test_c4_full_size_sampled():
     scale = dW2.abs().max().item()
     assert (dW - dW2).abs().max().item() <= 2 ** -7 * scale
     assert (dX.float() - dX2.float()).abs().max().item() <= 2 ** -7 * dX2.float().abs().max().item()
+
+
+def test_c2_full_size_sampled():
+    """The 4096-token replayed top-p 0.97 batch (the pages' sharp rows), icepop, through
+    the fused call in its default launch shape: sampled outputs and dX rows vs the oracle,
+    <dW, W> = <dX, X>."""
+    case = workloads.make_head_case("c2", device="cuda", variant="pages")
+    assert case.N == 4096
+    hp = _hp_c2(all_replayed=0)
+    batch = rh.HeadBatch.from_case(case)
+    dloss_t = (case.loss_mask.float() / case.loss_mask.float().sum()).contiguous()
+    fwd, dX, dW = rh.rl_head_loss_fwd_bwd(batch, hp, dloss_t)
+    torch.cuda.synchronize()
+    assert fwd.status_bits() == 0, rh.status_names(fwd.status_bits())
+    _check_sampled_rows(case, hp, fwd, dX, dloss_t, _sampled_rows(case.N, 8))
+    lhs = float((dW.double() * case.W.double()).sum())
+    rhs = float((dX.double() * case.hidden.double()).sum())
+    assert abs(lhs - rhs) <= 1e-2 * float((dX.double() * case.hidden.double()).abs().sum())
+
+
+def test_c3_full_size_sparse_against_dense():
+    """The 16384-token replayed top-p batch with exact centering, ipo: the deterministic
+    CSR sparse backward against the dense backward over the whole batch (dW and dX), and
+    the sparse call's sampled outputs and dX rows vs the oracle (element reading: the
+    sparse gradient is formed in fp32)."""
+    case = workloads.make_head_case("c3", device="cuda", variant="pages")
+    assert case.N == 16384
+    batch = rh.HeadBatch.from_case(case)
+    dloss_t = (case.loss_mask.float() / case.loss_mask.float().sum()).contiguous()
+    hp_s = _hp_c3(all_replayed=1)                        # AUTO -> sparse CSR matmul
+    hp_d = _hp_c3(bwd_mode=rh.RL_BWD_DENSE)
+    fs, dXs, dWs = rh.rl_head_loss_fwd_bwd(batch, hp_s, dloss_t)
+    fd, dXd, dWd = rh.rl_head_loss_fwd_bwd(batch, hp_d, dloss_t)
+    torch.cuda.synchronize()
+    assert fs.status_bits() == 0 and fd.status_bits() == 0
+    torch.testing.assert_close(fs.loss, fd.loss, rtol=1e-5, atol=1e-6)   # the same forward arithmetic
+    torch.testing.assert_close(dWs, dWd, rtol=1e-5, atol=1e-9)
+    torch.testing.assert_close(dXs.float(), dXd.float(), rtol=1e-2, atol=1e-8)
+    _check_sampled_rows(case, hp_s, fs, dXs, dloss_t, _sampled_rows(case.N, 9), reading="element")
 
 
 def _small(N, V=1000, H=64, **kw):
