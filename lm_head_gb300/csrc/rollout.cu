@@ -59,7 +59,14 @@ struct RcArgs {
     float* pmin;         // [B]
     float* pmax;         // [B]
     int32_t* status;
-    float* factor;       // batch-normalisation factor for rc_scale_kernel
+    float* factor;       // the batch-normalisation factor applied
+    // batch normalisation: kept tokens and their weight sum over all sequences, exact
+    // integer totals (the weight in 2^-24 fixed point); kept_range set if a sequence's sum
+    // was too large for that (the factor then comes from the ordered record reduction)
+    long long* kept_n;
+    long long* kept_wfix;
+    int* kept_range;
+    float kept_lim;
     rl_rc_metrics* metrics;
 };
 
@@ -102,8 +109,8 @@ struct RcSeq {   // one sequence's decisions (thread 0 -> block)
     float wseq;
 };
 
-// A sequence is staged in shared memory kRcChunk tokens at a time (coalesced loads,
-// no alignment needed); a sequence of at most kRcChunk tokens is read from memory once
+// A sequence is staged in shared memory kRcChunk tokens at a time (coalesced loads, 16
+// bytes wide where the chunk is aligned, scalar otherwise); a sequence of at most kRcChunk tokens is read from memory once
 // for both passes, a longer one chunk by chunk in each pass (pass 2 starts from the chunk
 // still staged; the earlier ones come back from L2).  128 threads and 2048-token chunks
 // keep eight blocks on an SM, so a batch of up to 8 x SMs sequences is resident at once
@@ -114,8 +121,9 @@ constexpr int kRcChunk = 2048;
 constexpr int kRcW = kRcThreads / 32;
 
 __global__ void __launch_bounds__(kRcThreads, 8) rc_seq_kernel(RcArgs a) {
-    __shared__ float s_lt[kRcChunk], s_lr[kRcChunk];
-    __shared__ uint8_t s_m[kRcChunk];
+    __shared__ __align__(16) float s_lt[kRcChunk];
+    __shared__ __align__(16) float s_lr[kRcChunk];
+    __shared__ __align__(16) uint8_t s_m[kRcChunk];
     __shared__ FF shff[kRcW][4];
     __shared__ float shf[kRcW][5];
     __shared__ int shi[kRcW][6];
@@ -136,11 +144,30 @@ __global__ void __launch_bounds__(kRcThreads, 8) rc_seq_kernel(RcArgs a) {
     auto stage = [&](int c) {   // chunk c into shared memory; returns its length
         const int64_t c0 = o0 + static_cast<int64_t>(c) * kRcChunk;
         const int n = static_cast<int>(o1 - c0 < kRcChunk ? o1 - c0 : kRcChunk);
+        const float* lt = a.lt + c0;
+        const float* lr = a.lr + c0;
+        const uint8_t* mk = a.mask + c0;
+        int i0 = 0;
+        if ((((reinterpret_cast<uintptr_t>(lt) | reinterpret_cast<uintptr_t>(lr)) & 15) |
+             (reinterpret_cast<uintptr_t>(mk) & 3)) == 0) {
+            // 16-byte loads (4-byte for the mask), all of a thread's loads in flight at once
+            const int n4 = n >> 2;
 #pragma unroll 4
-        for (int i = threadIdx.x; i < n; i += kRcThreads) {
-            s_lt[i] = a.lt[c0 + i];
-            s_lr[i] = a.lr[c0 + i];
-            s_m[i] = a.mask[c0 + i];
+            for (int i = threadIdx.x; i < n4; i += kRcThreads) {
+                const float4 x = reinterpret_cast<const float4*>(lt)[i];
+                const float4 y = reinterpret_cast<const float4*>(lr)[i];
+                const uchar4 m = reinterpret_cast<const uchar4*>(mk)[i];
+                reinterpret_cast<float4*>(s_lt)[i] = x;
+                reinterpret_cast<float4*>(s_lr)[i] = y;
+                reinterpret_cast<uchar4*>(s_m)[i] = m;
+            }
+            i0 = 4 * n4;
+        }
+#pragma unroll 4
+        for (int i = i0 + threadIdx.x; i < n; i += kRcThreads) {
+            s_lt[i] = lt[i];
+            s_lr[i] = lr[i];
+            s_m[i] = mk[i];
         }
         __syncthreads();
         return n;
@@ -349,6 +376,15 @@ __global__ void __launch_bounds__(kRcThreads, 8) rc_seq_kernel(RcArgs a) {
         for (int f = 0; f < kRcC; ++f) a.pc[f * B + b] = c[f];
         a.pmin[b] = F[3];
         a.pmax[b] = F[4];
+        if (q.use_tis && q.norm) {   // the factor's two totals, in any order of arrival
+            if (I[0] != 0) atomicAdd(reinterpret_cast<unsigned long long*>(a.kept_n), static_cast<unsigned long long>(I[0]));
+            if (fabsf(F[1]) < a.kept_lim) {
+                const long long x = __float2ll_rn(F[1] * 16777216.f);
+                if (x != 0) atomicAdd(reinterpret_cast<unsigned long long*>(a.kept_wfix), static_cast<unsigned long long>(x));
+            } else {
+                atomicExch(a.kept_range, 1);
+            }
+        }
     }
 }
 
@@ -408,9 +444,20 @@ RL_DEVINL void rc_reduce_fields(const RcArgs& a, double* tot, bool only_factor) 
     }
 }
 
+// The batch-normalisation factor n_kept / sum of kept weights: from the integer totals the
+// sequence blocks accumulated (t may then be null), else from the reduced fields t.
+RL_DEVINL bool rc_factor_fixed(const RcArgs& a) { return a.q.use_tis && a.q.norm && *a.kept_range == 0; }
 RL_DEVINL double rc_factor(const RcArgs& a, const double* t) {
-    const double kept_w = t[RD_KEPT_W], n_kept = t[kRcD + RC_KEPT];
-    return (a.q.use_tis && a.q.norm && n_kept > 0 && kept_w > 0) ? n_kept / kept_w : 1.0;
+    if (!(a.q.use_tis && a.q.norm)) return 1.0;
+    double kept_w, n_kept;
+    if (rc_factor_fixed(a)) {
+        n_kept = static_cast<double>(*a.kept_n);
+        kept_w = static_cast<double>(*a.kept_wfix) * (1.0 / 16777216.0);
+    } else {
+        kept_w = t[RD_KEPT_W];
+        n_kept = t[kRcD + RC_KEPT];
+    }
+    return (n_kept > 0 && kept_w > 0) ? n_kept / kept_w : 1.0;
 }
 
 // The factor and the metrics from the reduced fields (one thread).
@@ -459,29 +506,35 @@ __global__ void __launch_bounds__(kRcReduceThreads) rc_reduce_kernel(RcArgs a) {
     if (threadIdx.x == 0) rc_write_metrics(a, tot);
 }
 
-// Batch normalisation: every block first forms the factor itself (the two fields it needs,
-// in the order rc_reduce_kernel uses, so every block has the same bits), block 0 all the
-// fields and the metrics; then w *= factor, float4 over the 16-byte-aligned body and
-// scalars at the two ends.  One launch where a reduce and a scale kernel would take two.
+// Batch normalisation: every block forms the factor (from the integer totals, or, when a
+// sequence's sum was out of their range, from the two fields it needs in the order
+// rc_reduce_kernel uses, so every block has the same bits), block 0 also reduces all the
+// fields and writes the metrics while the other blocks scale: w *= factor, float4 over the
+// 16-byte-aligned body (four loads in flight per thread) and scalars at the two ends.  One
+// launch where a reduce and a scale kernel would take two.
 __global__ void __launch_bounds__(kRcReduceThreads) rc_scale_kernel(RcArgs a) {
     __shared__ double tot[kRcFields];
     __shared__ float fac;
-    rc_reduce_fields(a, tot, blockIdx.x != 0);
+    if (blockIdx.x == 0 || !rc_factor_fixed(a)) rc_reduce_fields(a, tot, blockIdx.x != 0);
     __syncthreads();
     if (threadIdx.x == 0) {
         fac = static_cast<float>(rc_factor(a, tot));
         if (blockIdx.x == 0) rc_write_metrics(a, tot);
     }
     __syncthreads();
+    // block 0 (the metrics) takes no share of the scaling when there are other blocks
+    if (gridDim.x > 1 && blockIdx.x == 0) return;
+    const int64_t sb = gridDim.x > 1 ? blockIdx.x - 1 : 0, nsb = gridDim.x > 1 ? gridDim.x - 1 : 1;
     const float f = fac;
     float* w = a.w;
     const int64_t T = a.T;
     const int64_t head = ((16 - (reinterpret_cast<uintptr_t>(w) & 15)) & 15) / 4;
     const int64_t h = head < T ? head : T;
     const int64_t n4 = (T - h) / 4;
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t tid = sb * blockDim.x + threadIdx.x;
+    const int64_t nth = nsb * blockDim.x;
     float4* w4 = reinterpret_cast<float4*>(w + h);
+#pragma unroll 4
     for (int64_t i = tid; i < n4; i += nth) {
         float4 v = w4[i];
         v.x *= f;
@@ -498,7 +551,8 @@ __global__ void __launch_bounds__(kRcReduceThreads) rc_scale_kernel(RcArgs a) {
 // ----------------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------------
-// Workspace: a 256-byte header (status, factor), then the per-sequence records.
+// Workspace: a 256-byte header (status, factor, the factor's range flag and integer
+// totals), then the per-sequence records.
 constexpr size_t kRcHeader = 256;
 
 static size_t rc_record_bytes(int64_t B) {
@@ -540,6 +594,11 @@ int rollout_impl(const float* lt, const float* lr, const uint8_t* mask, const in
     uint8_t* base = static_cast<uint8_t*>(ws);
     a.status = reinterpret_cast<int32_t*>(base + 4);
     a.factor = reinterpret_cast<float*>(base + 8);
+    a.kept_range = reinterpret_cast<int*>(base + 12);
+    a.kept_n = reinterpret_cast<long long*>(base + 16);
+    a.kept_wfix = reinterpret_cast<long long*>(base + 24);
+    // a sequence's kept-weight sum below 2^38 / B keeps the total below 2^62 in 2^-24 units
+    a.kept_lim = static_cast<float>(ldexp(1.0, 38) / static_cast<double>(B > 0 ? B : 1));
     uint8_t* rec = base + kRcHeader;
     a.pd = reinterpret_cast<double*>(rec);
     a.pc = reinterpret_cast<long long*>(a.pd + kRcD * B);
@@ -547,7 +606,7 @@ int rollout_impl(const float* lt, const float* lr, const uint8_t* mask, const in
     a.pmax = a.pmin + B;
     a.metrics = metrics;
     ProfScope ps(RL_PROF_ROLLOUT, stream);
-    if (cudaMemsetAsync(ws, 0, 16, stream) != cudaSuccess) return RL_ERR_CUDA;
+    if (cudaMemsetAsync(ws, 0, 32, stream) != cudaSuccess) return RL_ERR_CUDA;   // status .. kept_wfix
     int launches = 0;
     if (B > 0) {
         rc_seq_kernel<<<static_cast<unsigned>(B), kRcThreads, 0, stream>>>(a);

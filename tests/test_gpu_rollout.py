@@ -156,3 +156,22 @@ def test_nonfinite_padding():
     with np.errstate(invalid="ignore", over="ignore"):
         for cfg in (1, 2, 3):
             _compare(lt, lr, m, off, CONFIGS[cfg])
+
+
+def test_normalisation_past_the_integer_totals_range():
+    """Batch normalisation whose kept weights reach ~2e17 (log-ratios of 40; e^(2 x 40)
+    still fits the fp32 chi^2 terms): a sequence's kept-weight sum is past the range of
+    the integer totals the factor normally comes from, so the factor is taken from the
+    records reduced in sequence order instead; the results equal the oracle's either way."""
+    rng = np.random.default_rng(16)
+    lens = np.array([300, 500, 200])
+    T = int(lens.sum())
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    lr = np.log(rng.random(T) * 0.9 + 0.05)
+    lt = np.minimum(lr + rng.normal(0, 0.3, T), 0.0)
+    lr[::97] = -52.0
+    lt[::97] = -12.0
+    m = np.ones(T, np.uint8)
+    for p in (rh.RcParams(tis_mode="truncate", tis_upper_bound=1e30, tis_batch_normalize=True),
+              rh.RcParams(tis_mode="clip", tis_lower_bound=0.1, tis_upper_bound=10.0, tis_batch_normalize=True)):
+        _compare(lt.astype(np.float32), lr.astype(np.float32), m, off, p)
