@@ -245,8 +245,10 @@ typedef struct rl_pg_metrics {
 /* Workspace bytes for T tokens: 256 bytes (counters and the metric accumulators), for any
  * T.  The argument stays so that callers need not change if a later layout depends on T. */
 size_t rl_policy_workspace_bytes(int64_t T);
-/* All arrays device [T] fp32 (mask uint8, 1 = valid response token).  Output arrays may
- * be NULL to skip; masked tokens get 0.  metrics: device, overwritten; NULL to skip. */
+/* All arrays device [T] fp32 (mask uint8, 1 = valid response token; any nonzero byte
+ * counts as valid).  A masked slot's inputs are never used, whatever they hold (NaN and
+ * inf included).  Output arrays may be NULL to skip; masked tokens get 0.  metrics:
+ * device, overwritten; NULL to skip. */
 int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const float* lp_samp,
                                const float* adv, const uint8_t* mask, int64_t T,
                                const rl_pg_params* params, float* loss_ppo, float* loss_dec,
@@ -340,8 +342,12 @@ typedef struct rl_rc_metrics {
 size_t rl_rollout_correction_workspace_bytes(int64_t B);
 /* lp_train, lp_rollout: device [T] fp32; mask: device [T] uint8 (1 = response token);
  * seq_offsets: device [B + 1] int64, sequence s = tokens [seq_offsets[s], seq_offsets[s+1])
- * (padded rows: s * row_length; packed: cumulative lengths).  Outputs, device: weights
- * [T] fp32 and keep [T] uint8 (either may be NULL), metrics (overwritten, may be NULL).
+ * (padded rows: s * row_length; packed: cumulative lengths).  A token whose mask byte is 0
+ * is not a response token and its log-probs are never used (NaN and inf included).
+ * Outputs, device: weights [T] fp32 and keep [T] uint8 (either may be NULL), metrics
+ * (overwritten, may be NULL).  Batch normalisation: each sequence's kept weights are summed
+ * in fp32 and the sequences' sums added exactly in 2^-24 fixed point (a sequence sum at or
+ * past 2^38 / B instead sends the factor through an fp64 sum in sequence order).
  * Errors: RL_ERR_ARG (NULL input, B < 0, T < 0, B == 0 with T > 0, bad enum, L > U or
  * negative bound), RL_ERR_WORKSPACE; bad offsets are reported in metrics->status, not
  * trapped. */
