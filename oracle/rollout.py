@@ -22,7 +22,7 @@ TEST INFRASTRUCTURE: see the package docstring.  Source: "Rollout Correction Met
     masked fractions, the RS fractions, catastrophic token / sequence fractions, the mean
     after TIS and RS, the batch normalisation factor, final mean / min / max).
 
-Readings where the page is silent (each marked READING below; listed in the design doc):
+Readings where the page is silent (each marked READING below):
   * RC1 "out of threshold" keeps a weight equal to a bound (lower <= w <= upper is kept).
   * RC2 truncate bounds from above only (w -> min(w, upper)); clip clamps to [lower, upper];
     mask zeroes a weight outside [lower, upper] (the token stays in the average).

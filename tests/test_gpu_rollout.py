@@ -80,7 +80,7 @@ def _c5():
     return c.lp_old, c.lp_samp, c.mask, off
 
 
-CONFIGS = [
+SETTINGS = [
     rh.RcParams(),                                                            # token, truncate
     rh.RcParams(tis_mode="clip", tis_level="sequence", tis_lower_bound=0.1, tis_upper_bound=10.0,
                 tis_batch_normalize=True, use_rs=True, rs_level="geometric", rs_lower_bound=0.9,
@@ -92,10 +92,10 @@ CONFIGS = [
 ]
 
 
-@pytest.mark.parametrize("cfg", range(len(CONFIGS)))
+@pytest.mark.parametrize("cfg", range(len(SETTINGS)))
 def test_c5_full_size(cfg):
     """879 padded rows of up to 4096 tokens, 1.8M response tokens, five knob settings."""
-    gm, rm = _compare(*_c5(), CONFIGS[cfg])
+    gm, rm = _compare(*_c5(), SETTINGS[cfg])
     assert gm["n_valid"] == 1_800_000
 
 
@@ -112,7 +112,7 @@ def test_packed_ragged_sequences_and_empty_ones():
     lt = np.minimum(lt, 0).astype(np.float32)
     m = (rng.random(T) < 0.85).astype(np.uint8)
     m[off[10]:off[11]] = 0
-    for p in CONFIGS:
+    for p in SETTINGS:
         _compare(lt, lr, m, off, p)
 
 
@@ -155,7 +155,7 @@ def test_nonfinite_padding():
     lr[pad] = rng.choice(np.array([np.nan, np.inf, -np.inf], np.float32), int(pad.sum()))
     with np.errstate(invalid="ignore", over="ignore"):
         for cfg in (1, 2, 3):
-            _compare(lt, lr, m, off, CONFIGS[cfg])
+            _compare(lt, lr, m, off, SETTINGS[cfg])
 
 
 def test_normalisation_past_the_integer_totals_range():
