@@ -5,8 +5,20 @@ kernels.  PyTorch provides device memory and the current stream.  There is no CP
 fallback: if the extension is missing or no sm_100-family GPU is present, calls raise.
 
 Functions carry the C names:
-  rl_validate_support, rl_head_loss_fwd, rl_head_loss_bwd, rl_mismatch_metrics,
-  rl_policy_loss_elementwise, rl_status_read, rl_kernel_launch_count
+  head:        rl_validate_support, rl_head_loss_fwd, rl_head_loss_bwd,
+               rl_head_loss_fwd_bwd (one call when dloss is known before the forward),
+               rl_mismatch_metrics
+  elementwise: rl_policy_loss_elementwise (+ rl_policy_loss_elementwise_noalloc in C)
+  rollout:     rl_rollout_correction (IS / RS weights, veto, batch normalisation, metrics)
+  utilities:   rl_gemm_bf16, rl_gemm_bf16_tn, rl_status_read, rl_profile_enable /
+               rl_profile_read, rl_kernel_launch_count, the *_workspace_bytes queries
+
+Typical use (device tensors; see the tests for every option):
+  batch = HeadBatch.from_case(case)                 # hidden, W, labels, CSR support, ...
+  hp = HeadParams(loss_type=RL_LOSS_IPO, eps=0.3, max_importance_ratio=10.0)
+  fwd, dX, dW = rl_head_loss_fwd_bwd(batch, hp, dloss)   # fused forward + backward
+  fwd = rl_head_loss_fwd(batch, hp)                 # or: forward now ...
+  dX, dW, status = rl_head_loss_bwd(batch, hp, fwd.saved, dloss)   # ... backward later
 """
 from __future__ import annotations
 
