@@ -766,9 +766,11 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
             return RL_ERR_CUDA;
         smem_set[dev] = 1;
     }
-    ProfScope ps(RL_PROF_POLICY, stream);
-    // arrival count, status, range flag, accumulators
-    if (cudaMemsetAsync(ws, 0, kPgHeader, stream) != cudaSuccess) return RL_ERR_CUDA;
+    {   // arrival count, status, range flag, accumulators
+        ProfScope pm(RL_PROF_MEMSET, stream);
+        if (cudaMemsetAsync(ws, 0, kPgHeader, stream) != cudaSuccess) return RL_ERR_CUDA;
+    }
+    ProfScope ps(RL_PROF_POLICY, stream);   // the kernel launch alone
     a.nb = fast ? fast_blocks(sms) - 1 : slow_blocks(sms);   // fast: odd, see policy_fast_kernel
     // a term below 2^38 / nb keeps each accumulator's total below 2^62 in 2^-24 units
     a.range_lim = ldexpf(1.f, 38) / static_cast<float>(a.nb);

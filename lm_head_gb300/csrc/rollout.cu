@@ -605,8 +605,11 @@ int rollout_impl(const float* lt, const float* lr, const uint8_t* mask, const in
     a.pmin = reinterpret_cast<float*>(a.pc + kRcC * B);
     a.pmax = a.pmin + B;
     a.metrics = metrics;
-    ProfScope ps(RL_PROF_ROLLOUT, stream);
-    if (cudaMemsetAsync(ws, 0, 32, stream) != cudaSuccess) return RL_ERR_CUDA;   // status .. kept_wfix
+    {
+        ProfScope pm(RL_PROF_MEMSET, stream);
+        if (cudaMemsetAsync(ws, 0, 32, stream) != cudaSuccess) return RL_ERR_CUDA;   // status .. kept_wfix
+    }
+    ProfScope ps(RL_PROF_ROLLOUT, stream);   // the kernel launches alone
     int launches = 0;
     if (B > 0) {
         rc_seq_kernel<<<static_cast<unsigned>(B), kRcThreads, 0, stream>>>(a);
