@@ -266,9 +266,12 @@ int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const
  *   - Every GPU that loads the library holds that array until the process exits.
  *   - The first call on a device looks the array's device address up (once per
  *     device); make that first call before any stream capture.
- *   - All calls share the one array and it keeps the last call's contents.  Each call
- *     writes every partial it reads before reading it, so nothing has to start at zero.
- *     Calls that overlap on the GPU (other streams, other threads) race on the array:
+ *   - All calls share the one array and it keeps the last call's contents.  Its header
+ *     (the arrival counter, the status word, the range flag and the accumulators, which
+ *     the kernel's blocks add into with atomics) must start at zero, so each call first
+ *     zeroes those 256 bytes with a memset on its own stream, then launches the kernel.
+ *     That ordering is why calls one after another on one stream are safe, and why
+ *     calls that overlap on the GPU (other streams, other threads) race on the array:
  *     serialise them.
  * Arguments, outputs and errors as rl_policy_loss_elementwise, without ws / ws_bytes. */
 int rl_policy_loss_elementwise_noalloc(const float* lp_theta, const float* lp_old,
@@ -293,8 +296,8 @@ int rl_policy_loss_elementwise_noalloc(const float* lp_theta, const float* lp_ol
  * A weight equal to a bound is inside it.  Every decision (bounds, RS, veto) is the exact
  * predicate on the fp32 inputs (the log-ratio sums carried in float-float); weight values
  * are fp32 (a raw sequence weight past the fp32 range is inf, its bounded value exact).
- * The metric struct holds sums and counts; the named metrics of "Mismatch Metrics" are
- * their ratios (the Python binding forms them). */
+ * The metric struct holds sums and counts (they compose across calls); the named
+ * metrics of "Mismatch Metrics" come from them through rl_rollout_metrics_named. */
 typedef enum { RL_TIS_TRUNCATE = 0, RL_TIS_CLIP = 1, RL_TIS_MASK = 2 } rl_tis_mode;
 typedef enum { RL_LEVEL_TOKEN = 0, RL_LEVEL_SEQUENCE = 1, RL_LEVEL_GEOMETRIC = 2 } rl_is_level;
 typedef struct rl_rc_params {
@@ -356,6 +359,51 @@ int rl_rollout_correction(const float* lp_train, const float* lp_rollout, const 
                           const rl_rc_params* params, float* weights, uint8_t* keep,
                           rl_rc_metrics* metrics, void* ws, size_t ws_bytes, void* stream);
 
+/* The named metrics of "Rollout Correction Methods", "Mismatch Metrics" (the "Mismatch
+ * Monitoring Metrics" and "IS/RS Correction Metrics" tables), under the names the page
+ * logs them by without the mis_ prefix.  Readings where the page names a metric without
+ * a formula:
+ *   - a mean E[.] is over response tokens; the log-perplexities are per sequence (mean of
+ *     -log pi over its response tokens) averaged over the sequences holding one; the
+ *     perplexity is exp of that average; the log-perplexity difference (training minus
+ *     rollout), its absolute value and the perplexity ratio exp(difference) are taken per
+ *     sequence and averaged over sequences;
+ *   - chi^2 of the two policies, estimated under the rollout policy, is E[w^2] - 1 with
+ *     w = exp(lp_train - lp_rollout) per token (token) or exp of the sequence's summed
+ *     log-ratio (sequence, averaged over sequences);
+ *   - the fractions count response tokens (catastrophic sequences: sequences);
+ *   - is_ratio_mean_after_tis_rs and the final mean / min / max are over kept tokens.
+ * A mean over an empty set is 0 (a perplexity over no sequence is exp(0) = 1).  A metric
+ * the page emits only under some settings ("Emitted when": use_tis for the IS/RS weight
+ * statistics, the tis_mode for its fractions, use_rs, a set veto threshold) is NaN when
+ * the settings given here do not emit it. */
+typedef struct rl_rc_named {
+    /* Mismatch Monitoring Metrics (always emitted) */
+    double training_log_ppl, training_ppl, rollout_log_ppl, rollout_ppl;
+    double kl;                  /* E[lp_rollout - lp_train] */
+    double k3_kl;               /* E[e^d - d - 1], d = lp_train - lp_rollout */
+    double log_ppl_diff, log_ppl_abs_diff, ppl_ratio;
+    double chi2_token, chi2_seq;
+    double train_rollout_logprob_abs_diff;   /* E|d| */
+    /* IS/RS Correction Metrics */
+    double tis_weight_before_bound, tis_weight_after_bound;      /* use_tis: token means */
+    double tis_truncate_fraction;                                /* use_tis, truncate */
+    double tis_clip_fraction_low, tis_clip_fraction_high;        /* use_tis, clip */
+    double tis_mask_fraction_low, tis_mask_fraction_high;        /* use_tis, mask */
+    double rs_mask_fraction_low, rs_mask_fraction_high;          /* use_rs */
+    double rs_catastrophic_token_fraction, rs_catastrophic_seq_fraction;   /* veto set */
+    double is_ratio_mean_after_tis_rs, batch_norm_factor;        /* use_tis */
+    double is_ratio_mean_final, is_ratio_min_final, is_ratio_max_final;    /* use_tis */
+} rl_rc_named;
+
+/* metrics: device, as rl_rollout_correction wrote it (or sums the caller added up over
+ * several calls, with the min / max / factor fields of one of them); params: host, the
+ * settings of those calls; named: device, overwritten.  One device thread, enqueued on
+ * `stream` after the call that wrote `metrics`.  Errors: RL_ERR_ARG (NULL pointer, bad
+ * enum). */
+int rl_rollout_metrics_named(const rl_rc_metrics* metrics, const rl_rc_params* params,
+                             rl_rc_named* named, void* stream);
+
 /* ---- utilities ------------------------------------------------------------------ */
 /* The head contraction alone: D[M, N] fp32 = A[M, K] * B[N, K]^T, A and B bf16 row-major
  * (K contiguous), device pointers, 16-byte aligned; K % 8 == 0, N % 4 == 0.  Same tcgen05
@@ -384,13 +432,32 @@ int rl_profile_enable(int on);
 int rl_profile_read(double* ms, int64_t* launches);
 const char* rl_profile_kind_name(int kind);
 
-/* Library options (process-wide, host side).  RL_OPT_GEMM_PAIR: 1 (the default) runs the
- * tensor-core GEMMs on pairs of SMs (two-CTA clusters, tcgen05 cta_group::2, 256 x 256
- * tiles); 0 on single SMs (128 x 256 tiles).  Results are the same to fp32 rounding.
- * rl_set_option returns RL_ERR_ARG for an unknown key; rl_get_option returns -1. */
+/* Library options (process-wide, host side, read when a call enqueues its kernels).
+ *   RL_OPT_GEMM_PAIR: 1 (the default) runs the tensor-core GEMMs on pairs of SMs (two-CTA
+ *     clusters, tcgen05 cta_group::2, 256 x 256 tiles); 0 on single SMs (128 x 256 tiles).
+ *     Results are the same to fp32 rounding.
+ *   RL_OPT_WAIT_LIMIT_US: how long (microseconds, 1 .. 10,000,000; default 1,000,000) a
+ *     kernel's wait for its own copies or tensor-core work may last before it gives up,
+ *     ORs RL_STATUS_TIMEOUT into the status word (rl_pg_metrics.status for the
+ *     elementwise path) and unwinds; the outputs of that call are then invalid.  An
+ *     unwinding kernel still waits (up to 1 s, whatever this option says) for the copies
+ *     and MMAs it has in flight before it releases its shared memory and TMEM, so a short
+ *     limit makes a call fail, never fault.  A limit below a few milliseconds is for tests.
+ * rl_set_option returns RL_ERR_ARG for an unknown key or a value out of range;
+ * rl_get_option returns -1 for an unknown key. */
 #define RL_OPT_GEMM_PAIR 1
+#define RL_OPT_WAIT_LIMIT_US 2
 int rl_set_option(int key, int value);
 int rl_get_option(int key);
+
+/* Self-test of the bounded waits: one block waits on a shared-memory mbarrier that nothing
+ * ever signals, with the RL_OPT_WAIT_LIMIT_US limit; the wait runs out, ORs
+ * RL_STATUS_TIMEOUT into *dev_status (device) and the kernel returns normally, so the
+ * context stays usable.  This is the failure path of every wait in the library
+ * ("checked once per step before the optimizer": pull request #4233, GPU validation of the
+ * sampler evidence, whose device status word this reuses), made to happen on purpose
+ * without a fault.  Takes about the limit to run. */
+int rl_wait_selftest(int32_t* dev_status, void* stream);
 
 /* Synchronous device->host copy of the status word.  Call after the stream is done. */
 int rl_status_read(const int32_t* dev_status, int32_t* host_out);

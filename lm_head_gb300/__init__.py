@@ -9,9 +9,11 @@ Functions carry the C names:
                rl_head_loss_fwd_bwd (one call when dloss is known before the forward),
                rl_mismatch_metrics
   elementwise: rl_policy_loss_elementwise (+ rl_policy_loss_elementwise_noalloc in C)
-  rollout:     rl_rollout_correction (IS / RS weights, veto, batch normalisation, metrics)
-  utilities:   rl_gemm_bf16, rl_gemm_bf16_tn, rl_status_read, rl_profile_enable /
-               rl_profile_read, rl_kernel_launch_count, the *_workspace_bytes queries
+  rollout:     rl_rollout_correction (IS / RS weights, veto, batch normalisation, metric
+               sums), rl_rollout_metrics_named (the page's named metrics from those sums)
+  utilities:   rl_gemm_bf16, rl_gemm_bf16_tn, rl_status_read, rl_wait_selftest,
+               rl_set_option / rl_get_option, rl_profile_enable / rl_profile_read,
+               rl_kernel_launch_count, the *_workspace_bytes queries
 
 Typical use (device tensors; see the tests for every option):
   batch = HeadBatch.from_case(case)                 # hidden, W, labels, CSR support, ...
@@ -116,6 +118,17 @@ class RlRcMetrics(ctypes.Structure):
                    "n_cat_tokens", "n_cat_seqs", "status")]
 
 
+class RlRcNamed(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_double) for k in (
+        "training_log_ppl", "training_ppl", "rollout_log_ppl", "rollout_ppl", "kl", "k3_kl", "log_ppl_diff",
+        "log_ppl_abs_diff", "ppl_ratio", "chi2_token", "chi2_seq", "train_rollout_logprob_abs_diff",
+        "tis_weight_before_bound", "tis_weight_after_bound", "tis_truncate_fraction", "tis_clip_fraction_low",
+        "tis_clip_fraction_high", "tis_mask_fraction_low", "tis_mask_fraction_high", "rs_mask_fraction_low",
+        "rs_mask_fraction_high", "rs_catastrophic_token_fraction", "rs_catastrophic_seq_fraction",
+        "is_ratio_mean_after_tis_rs", "batch_norm_factor", "is_ratio_mean_final", "is_ratio_min_final",
+        "is_ratio_max_final")]
+
+
 _lib = None
 
 _SIGS = {
@@ -133,6 +146,7 @@ _SIGS = {
                                                                     ctypes.c_void_p]),
     "rl_policy_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64]),
     "rl_rollout_correction_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64]),
+    "rl_rollout_metrics_named": (ctypes.c_int, [ctypes.c_void_p] * 4),
     "rl_rollout_correction": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 2 + [ctypes.c_void_p] * 5
                               + [ctypes.c_size_t, ctypes.c_void_p]),
     "rl_policy_loss_elementwise": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int64] + [ctypes.c_void_p] * 7
@@ -140,6 +154,7 @@ _SIGS = {
     "rl_policy_loss_elementwise_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int64]
                                            + [ctypes.c_void_p] * 7),
     "rl_status_read": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "rl_wait_selftest": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
     "rl_gemm_bf16_tn": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int64] * 3
                         + [ctypes.c_void_p] * 3),
     "rl_gemm_bf16": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]
@@ -558,33 +573,17 @@ def rc_metrics(metrics_dev: torch.Tensor) -> dict:
     return {f: getattr(m, f) for f, _ in RlRcMetrics._fields_}
 
 
-def rc_metrics_named(m: dict, params: RcParams) -> dict:
-    """The page's metric names from the sums and counts ("Mismatch Metrics" tables):
-    token means over response tokens, sequence means over sequences with response tokens."""
+def rl_rollout_metrics_named(metrics_dev: torch.Tensor, params: RcParams, stream=None) -> dict:
+    """The named metrics of "Mismatch Metrics" (include/rlhead.h, rl_rc_named), formed on
+    the device by the library from the sums and counts of rl_rollout_correction; the
+    metrics these settings do not emit are NaN there and left out here."""
     import math
-    nv, ns, nk = max(m["n_valid"], 1), max(m["n_seq"], 1), max(m["n_kept"], 1)
-    tr, ro = m["train_lppl_sum"] / ns, m["rollout_lppl_sum"] / ns
-    out = {"training_log_ppl": tr, "training_ppl": math.exp(tr), "rollout_log_ppl": ro, "rollout_ppl": math.exp(ro),
-           "kl": m["mis_kl_sum"] / nv, "k3_kl": m["k3_sum"] / nv, "log_ppl_diff": m["lppl_diff_sum"] / ns,
-           "log_ppl_abs_diff": m["lppl_abs_diff_sum"] / ns, "ppl_ratio": m["ppl_ratio_sum"] / ns,
-           "chi2_token": m["chi2_token_sum"] / nv - 1.0, "chi2_seq": m["chi2_seq_sum"] / ns - 1.0,
-           "train_rollout_logprob_abs_diff": m["abs_diff_sum"] / nv,
-           "tis_weight_before_bound": m["w_before_sum"] / nv, "tis_weight_after_bound": m["w_after_sum"] / nv,
-           "is_ratio_mean_after_tis_rs": m["kept_w_sum"] / nk, "batch_norm_factor": m["batch_norm_factor"],
-           "is_ratio_mean_final": m["final_sum"] / nk, "is_ratio_min_final": m["final_min"],
-           "is_ratio_max_final": m["final_max"],
-           "rs_catastrophic_token_fraction": m["n_cat_tokens"] / nv,
-           "rs_catastrophic_seq_fraction": m["n_cat_seqs"] / ns}
-    lo, hi = m["n_tis_low"] / nv, m["n_tis_high"] / nv
-    if params.tis_mode == "truncate":
-        out["tis_truncate_fraction"] = hi
-    elif params.tis_mode == "clip":
-        out["tis_clip_fraction_low"], out["tis_clip_fraction_high"] = lo, hi
-    else:
-        out["tis_mask_fraction_low"], out["tis_mask_fraction_high"] = lo, hi
-    if params.use_rs:
-        out["rs_mask_fraction_low"], out["rs_mask_fraction_high"] = m["n_rs_low"] / nv, m["n_rs_high"] / nv
-    return out
+    _require_cuda(metrics_dev)
+    out = torch.empty(ctypes.sizeof(RlRcNamed), dtype=torch.uint8, device=metrics_dev.device)
+    p = params.c()
+    _check(load().rl_rollout_metrics_named(_ptr(metrics_dev), ctypes.byref(p), _ptr(out), _stream(stream)))
+    n = RlRcNamed.from_buffer_copy(bytes(out.cpu().numpy().tobytes()))
+    return {f: getattr(n, f) for f, _ in RlRcNamed._fields_ if not math.isnan(getattr(n, f))}
 
 
 def pg_metrics(metrics_dev: torch.Tensor, n_curve: int = 10) -> dict:
@@ -629,6 +628,15 @@ def rl_status_read(status: torch.Tensor) -> int:
     return int(out.value)
 
 
+def rl_wait_selftest(status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """A wait on an mbarrier nothing signals: runs out after RL_OPT_WAIT_LIMIT_US and sets
+    RL_STATUS_TIMEOUT in the returned device status word."""
+    st = torch.zeros(1, dtype=torch.int32, device="cuda") if status is None else status
+    _require_cuda(st)
+    _check(load().rl_wait_selftest(_ptr(st), _stream(stream)))
+    return st
+
+
 def rl_kernel_launch_count() -> int:
     return int(load().rl_kernel_launch_count())
 
@@ -651,6 +659,7 @@ def rl_profile_read() -> dict:
 
 
 RL_OPT_GEMM_PAIR = 1
+RL_OPT_WAIT_LIMIT_US = 2
 
 
 def rl_set_option(key: int, value: int) -> None:

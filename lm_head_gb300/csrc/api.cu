@@ -217,6 +217,15 @@ int rl_rollout_correction(const float* lp_train, const float* lp_rollout, const 
                         ws_bytes, as_stream(stream));
 }
 
+int rl_rollout_metrics_named(const rl_rc_metrics* metrics, const rl_rc_params* params, rl_rc_named* named,
+                             void* stream) {
+    if (!metrics || !params || !named) return fail(RL_ERR_ARG, "NULL pointer");
+    if (params->tis_mode != RL_TIS_TRUNCATE && params->tis_mode != RL_TIS_CLIP && params->tis_mode != RL_TIS_MASK)
+        return fail(RL_ERR_ARG, "bad tis_mode");
+    if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
+    return rollout_named_impl(metrics, params, named, as_stream(stream));
+}
+
 int rl_gemm_bf16(const void* A, int a_mn_major, const void* B, int b_mn_major, int64_t M, int64_t N,
                  int64_t K, float* D, int32_t* dev_status, void* stream) {
     if (!A || !B || !D || !dev_status) return fail(RL_ERR_ARG, "NULL pointer");
@@ -232,6 +241,12 @@ int rl_gemm_bf16(const void* A, int a_mn_major, const void* B, int b_mn_major, i
 int rl_gemm_bf16_tn(const void* A, const void* B, int64_t M, int64_t N, int64_t K, float* D,
                     int32_t* dev_status, void* stream) {
     return rl_gemm_bf16(A, 0, B, 0, M, N, K, D, dev_status, stream);
+}
+
+int rl_wait_selftest(int32_t* dev_status, void* stream) {
+    if (!dev_status) return fail(RL_ERR_ARG, "dev_status is NULL");
+    if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
+    return wait_selftest_impl(dev_status, as_stream(stream));
 }
 
 int rl_status_read(const int32_t* dev_status, int32_t* host_out) {

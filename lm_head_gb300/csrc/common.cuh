@@ -19,7 +19,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // A wait that has not completed after this many nanoseconds gives up, sets
 // RL_STATUS_TIMEOUT and lets the kernel unwind (no legitimate wait here is longer
-// than a few hundred microseconds).
+// than a few hundred microseconds).  The waits of the work loops take the limit the
+// launch was given (RL_OPT_WAIT_LIMIT_US, this value by default); the waits of an
+// unwinding kernel for its own copies and MMAs still in flight always take this one, so
+// a short work limit can never let a CTA leave while hardware still writes its memory.
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
 
 RL_DEVINL void set_status(int32_t* status, int32_t bits) {
@@ -85,7 +88,7 @@ RL_DEVINL bool mbar_try_wait(uint32_t addr, uint32_t parity) {
 }
 // Bounded wait for the phase with the given parity.  Returns false (and sets the
 // timeout status bit) if the limit ran out.
-RL_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
+RL_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status, uint64_t limit_ns = kWaitLimitNs) {
     const uint32_t a = smem_addr(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -93,7 +96,7 @@ RL_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(a, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             set_status(status, RL_STATUS_TIMEOUT);
             return false;
         }

@@ -24,9 +24,11 @@
 // processed in order by one CTA, so a policy can carry per-row state across the range
 // (the online logsumexp of the LM-head forward does).
 //
-// Every mbarrier wait is bounded (kWaitLimitNs); a wait that runs out sets
+// Every mbarrier wait is bounded (plan.wait_ns); a wait that runs out sets
 // RL_STATUS_TIMEOUT, raises a CTA-wide abort flag, and all roles unwind, wait for their
-// own copies / MMAs in flight (bounded again), and release TMEM.
+// own copies / MMAs in flight (bounded again, by the fixed kWaitLimitNs), and release
+// TMEM.  The MMA issuer waits for its last MMAs before TMEM is released whether or not it
+// aborted itself: an epilogue that gave up no longer proves the accumulators are done.
 #pragma once
 
 #include "common.cuh"
@@ -60,6 +62,7 @@ struct GemmPlan {
     int a_mn;            // A stored [K, M] (MN-major): tensor map over [K, M], 64 x 64 boxes
     int b_mn;            // B stored [K, N]
     int32_t* status;
+    uint64_t wait_ns;    // limit of the work loops' waits (RL_OPT_WAIT_LIMIT_US)
 };
 
 struct UnitCoords {
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const UnitCoords c = decode_unit(plan, u);
                 for (int nb = c.nb_begin; nb < c.nb_end && ok; ++nb) {
                     for (int kb = 0; kb < kb_total; ++kb) {
-                        if (!mbar_wait(empty + stage, phase ^ 1u, plan.status) || *abort_flag) {
+                        if (!mbar_wait(empty + stage, phase ^ 1u, plan.status, plan.wait_ns) || *abort_flag) {
                             *abort_flag = 1;
                             ok = false;
                             break;
@@ -231,7 +234,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int u = blockIdx.x; u < plan.num_units && ok; u += gridDim.x) {
                 const UnitCoords c = decode_unit(plan, u);
                 for (int nb = c.nb_begin; nb < c.nb_end && ok; ++nb) {
-                    if (!mbar_wait(acce + abuf, aphase ^ 1u, plan.status) || *abort_flag) {
+                    if (!mbar_wait(acce + abuf, aphase ^ 1u, plan.status, plan.wait_ns) || *abort_flag) {
                         *abort_flag = 1;
                         ok = false;
                         break;
@@ -239,7 +242,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + abuf * kBN;
                     for (int kb = 0; kb < kb_total; ++kb) {
-                        if (!mbar_wait(full + stage, phase, plan.status) || *abort_flag) {
+                        if (!mbar_wait(full + stage, phase, plan.status, plan.wait_ns) || *abort_flag) {
                             *abort_flag = 1;
                             ok = false;
                             break;
@@ -268,8 +271,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (abuf == 0) aphase ^= 1u;
                 }
             }
-            if (!ok && issued) {
-                // Every MMA issued so far must finish before TMEM is released.
+            if (issued) {
+                // Every MMA issued so far must finish before TMEM is released (also after a
+                // normal end of the loop: the epilogue may have given up on its waits).
                 umma_commit(done_bar);
                 mbar_wait(done_bar, 0, plan.status);
             }
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             Epi epi;
             epi.begin_unit(ep, row, half, c.m_blk, c.split, c.nb_begin * kBN + half * (kBN / 2));
             for (int nb = c.nb_begin; nb < c.nb_end; ++nb) {
-                if (!mbar_wait(accf + abuf, aphase, plan.status) || *abort_flag) {
+                if (!mbar_wait(accf + abuf, aphase, plan.status, plan.wait_ns) || *abort_flag) {
                     *abort_flag = 1;
                     ok = false;
                     break;
@@ -335,6 +339,7 @@ int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, 
                  int64_t cols, int64_t ld, int box_cols, int box_rows, int swizzle_bytes);
 
 int num_sms();
+uint64_t wait_limit_ns();
 
 // pair = 1: m_blocks counts 256-row blocks of the two-CTA kernel.
 GemmPlan make_plan(int64_t M, int64_t N, int64_t K, int passes, int n_splits, int m_fastest,

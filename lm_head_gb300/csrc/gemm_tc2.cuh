@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const UnitCoords c = decode_unit(plan, u);
                 for (int nb = c.nb_begin; nb < c.nb_end && ok; ++nb) {
                     for (int kb = 0; kb < kb_total; ++kb) {
-                        if (!mbar_wait(empty + stage, phase ^ 1u, plan.status) || *abort_flag) {
+                        if (!mbar_wait(empty + stage, phase ^ 1u, plan.status, plan.wait_ns) || *abort_flag) {
                             *abort_flag = 1;
                             ok = false;
                             break;
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int u = pair; u < plan.num_units && ok; u += npairs) {
                 const UnitCoords c = decode_unit(plan, u);
                 for (int nb = c.nb_begin; nb < c.nb_end && ok; ++nb) {
-                    if (!mbar_wait(acce + abuf, aphase ^ 1u, plan.status) || *abort_flag) {
+                    if (!mbar_wait(acce + abuf, aphase ^ 1u, plan.status, plan.wait_ns) || *abort_flag) {
                         *abort_flag = 1;
                         ok = false;
                         break;
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + abuf * kBN;
                     for (int kb = 0; kb < kb_total; ++kb) {
-                        if (!mbar_wait(full + stage, phase, plan.status) || *abort_flag) {
+                        if (!mbar_wait(full + stage, phase, plan.status, plan.wait_ns) || *abort_flag) {
                             *abort_flag = 1;
                             ok = false;
                             break;
@@ -240,7 +240,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (abuf == 0) aphase ^= 1u;
                 }
             }
-            if (!ok && any) {
+            if (any) {
+                // the MMAs must be done before either CTA releases TMEM or its stages, also
+                // after a normal end of the loop (an epilogue may have given up its waits)
                 umma_commit_pair_multicast(done_bar, 0x1);
                 mbar_wait(done_bar, 0, plan.status);
             }
@@ -259,7 +261,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int m_blk = c.m_blk * 2 + static_cast<int>(rank);
             epi.begin_unit(ep, row, half, m_blk, c.split, c.nb_begin * kBN + half * (kBN / 2));
             for (int nb = c.nb_begin; nb < c.nb_end; ++nb) {
-                if (!mbar_wait(accf + abuf, aphase, plan.status) || *abort_flag) {
+                if (!mbar_wait(accf + abuf, aphase, plan.status, plan.wait_ns) || *abort_flag) {
                     *abort_flag = 1;
                     ok = false;
                     break;

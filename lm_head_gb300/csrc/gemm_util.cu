@@ -60,4 +60,21 @@ int gemm_util_impl(const void* A, int a_mn, const void* B, int b_mn, int64_t M, 
     return rc;
 }
 
+// One thread waits, with the work-loop limit, on an mbarrier of its block that nothing
+// arrives on: the wait runs out, ORs RL_STATUS_TIMEOUT into *status and returns false;
+// the kernel then ends normally (no copy or MMA is in flight, so nothing to drain).
+__global__ void wait_selftest_kernel(int32_t* status, uint64_t wait_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_wait(&bar, 0, status, wait_ns);
+}
+
+int wait_selftest_impl(int32_t* status, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(status, wait_limit_ns());
+    count_launch();
+    return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
 }  // namespace rl

@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(256) validate_kernel(ValidateArgs a) {
     if (lane == 0) {
         if (rep && rl) {
             if (!found) bad |= RL_STATUS_LABEL_MISSING;
-            if (fabsf(mass - 1.f) > 1e-3f) bad |= RL_STATUS_SUPPORT_MASS;
+            if (!(fabsf(mass - 1.f) <= 1e-3f)) bad |= RL_STATUS_SUPPORT_MASS;   // a NaN mass too
         }
         set_status(a.status, bad);
     }

@@ -85,6 +85,8 @@ struct ProfScope {
 };
 void set_last_error(const char* msg);
 int num_sms();
+// Limit of the kernels' work-loop waits, ns (RL_OPT_WAIT_LIMIT_US; read at each launch).
+uint64_t wait_limit_ns();
 
 int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out,
                   void* saved, void* ws, int32_t* status, cudaStream_t stream);
@@ -137,6 +139,8 @@ int rollout_impl(const float* lt, const float* lr, const uint8_t* mask, const in
                  const rl_rc_params* p, float* w, uint8_t* keep, rl_rc_metrics* metrics, void* ws,
                  size_t ws_bytes, cudaStream_t stream);
 size_t rollout_ws_bytes(int64_t B);
+int rollout_named_impl(const rl_rc_metrics* m, const rl_rc_params* p, rl_rc_named* named, cudaStream_t stream);
+int wait_selftest_impl(int32_t* status, cudaStream_t stream);
 int gemm_util_impl(const void* A, int a_mn, const void* B, int b_mn, int64_t M, int64_t N, int64_t K,
                    float* D, int32_t* status, cudaStream_t stream);
 

@@ -32,6 +32,7 @@
 //  redoes the whole batch's metrics with exact decisions instead (slow, correct).
 //
 // Results are bitwise reproducible for a given device and T.
+#include <atomic>
 #include <cmath>
 #include <climits>
 
@@ -87,6 +88,7 @@ struct PgArgs {
     int nb;                       // blocks of the pass
     int* done;                    // blocks that have written their partial
     int32_t* status;              // RL_STATUS_* bits of this call
+    uint64_t wait_ns;             // limit of the streaming loop's waits (RL_OPT_WAIT_LIMIT_US)
     rl_pg_metrics* metrics;       // or nullptr
 };
 
@@ -533,7 +535,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
             for (int i = 0; i < nst; ++i) {
                 const int slot = i % kPgDepth;
                 if (i >= kPgDepth &&
-                    !mbar_wait(empty + slot, static_cast<uint32_t>((i / kPgDepth - 1) & 1), a.status)) {
+                    !mbar_wait(empty + slot, static_cast<uint32_t>((i / kPgDepth - 1) & 1), a.status, a.wait_ns)) {
                     atomicExch(&abort_flag, 1);
                     break;
                 }
@@ -552,7 +554,8 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
             }
             if (*vflag) {
                 // the last kPgDepth stages issued may still be in flight: wait for them
-                // (bounded) before the block's shared memory goes away
+                // (bounded by the fixed kWaitLimitNs, whatever the work loop's limit)
+                // before the block's shared memory goes away
                 for (int i = issued > kPgDepth ? issued - kPgDepth : 0; i < issued; ++i)
                     mbar_wait(full + i % kPgDepth, static_cast<uint32_t>((i / kPgDepth) & 1), a.status);
             }
@@ -562,7 +565,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
         const int j = 2 * threadIdx.x;
         for (int i = 0; i < nst; ++i) {
             const int slot = i % kPgDepth;
-            if (!mbar_wait(full + slot, static_cast<uint32_t>((i / kPgDepth) & 1), a.status)) {
+            if (!mbar_wait(full + slot, static_cast<uint32_t>((i / kPgDepth) & 1), a.status, a.wait_ns)) {
                 atomicExch(&abort_flag, 1);
                 break;
             }
@@ -757,14 +760,17 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
     a.acc = w.acc;
     a.range = w.range;
     a.metrics = metrics;
-    static int smem_set[64] = {0};   // per device: the fast pass's shared-memory opt-in
+    a.wait_ns = wait_limit_ns();
+    // per device: the fast pass's shared-memory opt-in (set once; concurrent first calls
+    // from several host threads at worst set the same attribute twice)
+    static std::atomic<int> smem_set[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RL_ERR_CUDA;
-    if (fast && !smem_set[dev]) {
+    if (fast && !smem_set[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(policy_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPgStreamSmem) !=
             cudaSuccess)
             return RL_ERR_CUDA;
-        smem_set[dev] = 1;
+        smem_set[dev].store(1, std::memory_order_release);
     }
     {   // arrival count, status, range flag, accumulators
         ProfScope pm(RL_PROF_MEMSET, stream);

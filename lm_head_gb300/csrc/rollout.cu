@@ -549,6 +549,69 @@ __global__ void __launch_bounds__(kRcReduceThreads) rc_scale_kernel(RcArgs a) {
 }
 
 // ----------------------------------------------------------------------------------
+// Named metrics ("Mismatch Metrics" tables) from the sums and counts
+// ----------------------------------------------------------------------------------
+struct RcEmit {
+    int use_tis, mode, use_rs, veto;
+};
+
+// Mean of a sum over a count; an empty set gives 0.
+RL_DEVINL double rc_mean(double sum, int64_t n) { return n > 0 ? sum / static_cast<double>(n) : 0.0; }
+
+__global__ void rc_named_kernel(const rl_rc_metrics* m, RcEmit e, rl_rc_named* o) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    const double nan = __longlong_as_double(0x7ff8000000000000ll);
+    const int64_t nv = m->n_valid, ns = m->n_seq, nk = m->n_kept;
+    // per-sequence log-perplexities averaged over sequences, perplexity = exp(average)
+    const double tr = rc_mean(m->train_lppl_sum, ns), ro = rc_mean(m->rollout_lppl_sum, ns);
+    o->training_log_ppl = tr;
+    o->training_ppl = exp(tr);
+    o->rollout_log_ppl = ro;
+    o->rollout_ppl = exp(ro);
+    o->kl = rc_mean(m->mis_kl_sum, nv);
+    o->k3_kl = rc_mean(m->k3_sum, nv);
+    o->log_ppl_diff = rc_mean(m->lppl_diff_sum, ns);
+    o->log_ppl_abs_diff = rc_mean(m->lppl_abs_diff_sum, ns);
+    o->ppl_ratio = rc_mean(m->ppl_ratio_sum, ns);
+    // chi^2 under the rollout policy: E[w^2] - 1 (nothing to average over: 0)
+    o->chi2_token = nv > 0 ? m->chi2_token_sum / static_cast<double>(nv) - 1.0 : 0.0;
+    o->chi2_seq = ns > 0 ? m->chi2_seq_sum / static_cast<double>(ns) - 1.0 : 0.0;
+    o->train_rollout_logprob_abs_diff = rc_mean(m->abs_diff_sum, nv);
+    const double lo = rc_mean(static_cast<double>(m->n_tis_low), nv);
+    const double hi = rc_mean(static_cast<double>(m->n_tis_high), nv);
+    o->tis_weight_before_bound = e.use_tis ? rc_mean(m->w_before_sum, nv) : nan;
+    o->tis_weight_after_bound = e.use_tis ? rc_mean(m->w_after_sum, nv) : nan;
+    o->tis_truncate_fraction = e.use_tis && e.mode == RL_TIS_TRUNCATE ? hi : nan;
+    o->tis_clip_fraction_low = e.use_tis && e.mode == RL_TIS_CLIP ? lo : nan;
+    o->tis_clip_fraction_high = e.use_tis && e.mode == RL_TIS_CLIP ? hi : nan;
+    o->tis_mask_fraction_low = e.use_tis && e.mode == RL_TIS_MASK ? lo : nan;
+    o->tis_mask_fraction_high = e.use_tis && e.mode == RL_TIS_MASK ? hi : nan;
+    o->rs_mask_fraction_low = e.use_rs ? rc_mean(static_cast<double>(m->n_rs_low), nv) : nan;
+    o->rs_mask_fraction_high = e.use_rs ? rc_mean(static_cast<double>(m->n_rs_high), nv) : nan;
+    o->rs_catastrophic_token_fraction = e.veto ? rc_mean(static_cast<double>(m->n_cat_tokens), nv) : nan;
+    o->rs_catastrophic_seq_fraction = e.veto ? rc_mean(static_cast<double>(m->n_cat_seqs), ns) : nan;
+    o->is_ratio_mean_after_tis_rs = e.use_tis ? rc_mean(m->kept_w_sum, nk) : nan;
+    o->batch_norm_factor = e.use_tis ? m->batch_norm_factor : nan;
+    o->is_ratio_mean_final = e.use_tis ? rc_mean(m->final_sum, nk) : nan;
+    o->is_ratio_min_final = e.use_tis ? m->final_min : nan;
+    o->is_ratio_max_final = e.use_tis ? m->final_max : nan;
+}
+
+int rollout_named_impl(const rl_rc_metrics* m, const rl_rc_params* p, rl_rc_named* named, cudaStream_t stream) {
+    RcEmit e;
+    e.use_tis = p->use_tis != 0;
+    e.mode = p->tis_mode;
+    e.use_rs = p->use_rs != 0;
+    e.veto = p->rs_veto_threshold > 0.f;   // NaN compares false: no veto, as rl_rollout_correction
+    {
+        ProfScope ps(RL_PROF_ROLLOUT, stream);
+        rc_named_kernel<<<1, 32, 0, stream>>>(m, e, named);
+    }
+    count_launch();
+    return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------------
 // Workspace: a 256-byte header (status, factor, the factor's range flag and integer

@@ -14,8 +14,12 @@ namespace rl {
 
 static std::atomic<int64_t> g_launches{0};
 static std::atomic<int> g_gemm_pair{1};
+constexpr int kWaitLimitUsDefault = 1000000;          // 1 s, the device-side kWaitLimitNs
+constexpr int kWaitLimitUsMax = 10000000;
+static std::atomic<int> g_wait_limit_us{kWaitLimitUsDefault};
 
 int gemm_pair_mode() { return g_gemm_pair.load(std::memory_order_relaxed); }
+uint64_t wait_limit_ns() { return 1000ull * static_cast<uint64_t>(g_wait_limit_us.load(std::memory_order_relaxed)); }
 static thread_local char g_last_error[256] = "";
 
 void count_launch(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
@@ -73,14 +77,15 @@ void set_last_error(const char* msg) {
 int num_sms() {
     int dev = 0;
     cudaGetDevice(&dev);
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];   // zero-initialised (static storage); one per device
     if (dev < 0 || dev >= 64) return 148;
-    if (cached[dev] == 0) {
-        int n = 0;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = n > 0 ? n : 148;
+        n = n > 0 ? n : 148;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -169,6 +174,7 @@ GemmPlan make_plan(int64_t M, int64_t N, int64_t K, int passes, int n_splits, in
     p.a_mn = a_mn;
     p.b_mn = b_mn;
     p.status = status;
+    p.wait_ns = wait_limit_ns();
     return p;
 }
 
@@ -183,12 +189,21 @@ extern "C" int rl_set_option(int key, int value) {
         rl::g_gemm_pair.store(value ? 1 : 0, std::memory_order_relaxed);
         return RL_OK;
     }
+    if (key == RL_OPT_WAIT_LIMIT_US) {
+        if (value < 1 || value > rl::kWaitLimitUsMax) {
+            rl::set_last_error("wait limit out of [1, 10000000] us");
+            return RL_ERR_ARG;
+        }
+        rl::g_wait_limit_us.store(value, std::memory_order_relaxed);
+        return RL_OK;
+    }
     rl::set_last_error("unknown option");
     return RL_ERR_ARG;
 }
 
 extern "C" int rl_get_option(int key) {
     if (key == RL_OPT_GEMM_PAIR) return rl::g_gemm_pair.load(std::memory_order_relaxed);
+    if (key == RL_OPT_WAIT_LIMIT_US) return rl::g_wait_limit_us.load(std::memory_order_relaxed);
     return -1;
 }
 

@@ -24,15 +24,11 @@ differences, except the items listed in ``PARITY_UNPINNED``.
 """
 from .rl_head import (HeadParams, LOSS_IPO, LOSS_ICEPOP, LOSS_REINFORCE, KL_EXACT, KL_K1,
                       STALE_NONE, STALE_INV_SQRT, head_forward, head_backward, head_loss_total,
-                      head_token_logits, token_forward)
+                      head_token_logits, token_forward, validate_support)
 from .policy import PolicyParams, policy_loss_elementwise, IPO_CURVE_EPS
 from .rollout import RolloutParams, rollout_correction, rollout_metrics_named
 
 PARITY_UNPINNED = (
-    "mask_tv metric: the pages name it without a definition; reading R9 "
-    "(u-weighted trainer mass removed by the mask) is consistency-checked only",
-    "kl_staleness=inv_sqrt: the pages name it without a formula; reading R6 "
-    "beta_t = kl_coeff / sqrt(1 + age_t) is consistency-checked only",
     "decoupled TIS bound: the pages give no value; reading R11 (token-level truncate at 2.0)",
     "rollout correction defaults: the pages give no bound values; tests set every bound "
     "explicitly, and the defaults (tis bounds [0.5, 2.0]) are a reading only",
@@ -41,6 +37,6 @@ PARITY_UNPINNED = (
 __all__ = [
     "HeadParams", "LOSS_IPO", "LOSS_ICEPOP", "LOSS_REINFORCE", "KL_EXACT", "KL_K1", "STALE_NONE",
     "STALE_INV_SQRT", "head_forward", "head_backward", "head_loss_total", "head_token_logits",
-    "token_forward", "PolicyParams", "policy_loss_elementwise", "IPO_CURVE_EPS", "PARITY_UNPINNED",
+    "token_forward", "validate_support", "PolicyParams", "policy_loss_elementwise", "IPO_CURVE_EPS", "PARITY_UNPINNED",
     "RolloutParams", "rollout_correction", "rollout_metrics_named",
 ]

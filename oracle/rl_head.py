@@ -151,6 +151,9 @@ def token_forward(z: np.ndarray, label: int, label_logq: float, adv: float, age:
         mismatch_kl=float(label_logq - logP_lab),
         support_mass=float(np.sum(u * np.exp(logp_full[ids] - logq))),
         mask_tv=float(np.sum(u * (~keep_ent) * ratio_ent)),
+        # the row's largest logit magnitude: the scale of the rounding an fp32 evaluation
+        # of these logits carries (what a finite-precision result is compared against)
+        zmax=float(np.max(np.abs(z))),
     )
 
 
@@ -219,6 +222,66 @@ def token_grad_z(z: np.ndarray, label: int, adv: float, ids: np.ndarray, replaye
     return grad, mag
 
 
+STATUS_OFFSETS, STATUS_ID_RANGE, STATUS_LOGQ, STATUS_LABEL_MISSING = 0x1, 0x2, 0x4, 0x8
+STATUS_SUPPORT_MASS, STATUS_EMPTY_ROW, STATUS_ROW_ORDER = 0x10, 0x20, 0x40
+
+
+def validate_support(inputs: dict, V: int) -> int:
+    """The sampler-evidence checks of pull request #4233 ("What changes": the CSR entries
+    are validated on the GPU once per step, before the optimizer), as status bits:
+
+      OFFSETS        offsets[0] != 0, offsets[N] != nnz, or a row whose bounds are
+                     negative, decreasing or past nnz (such a row is not looked into)
+      ID_RANGE       a label or a support id outside [0, V)
+      LOGQ           a log q (label or entry) that is not finite or is above 1e-6
+      LABEL_MISSING  a replayed RL row that does not hold its label
+      SUPPORT_MASS   a replayed RL row whose q does not sum to 1 within 1e-3 (READING R2)
+      EMPTY_ROW      an RL token with no support entry
+      ROW_ORDER      ids not ascending within a row (strictly ascending when replayed;
+                     repeated draws are adjacent, READING R3)
+    """
+    off = np.asarray(inputs["offsets"], dtype=np.int64)
+    ids = np.asarray(inputs["ids"], dtype=np.int64)
+    logq = np.asarray(inputs["logq"], dtype=np.float64)
+    N = off.shape[0] - 1
+    nnz = ids.shape[0]
+    rl_mask = inputs.get("loss_mask")
+    bits = 0
+    if N > 0 and (off[0] != 0 or off[N] != nnz):
+        bits |= STATUS_OFFSETS
+    for t in range(N):
+        b, e = int(off[t]), int(off[t + 1])
+        if b < 0 or e < b or e > nnz:
+            bits |= STATUS_OFFSETS
+            continue
+        rl = True if rl_mask is None else bool(rl_mask[t])
+        rep = bool(inputs["replayed"][t])
+        label = int(inputs["labels"][t])
+        llq = float(inputs["label_logq"][t])
+        if not 0 <= label < V:
+            bits |= STATUS_ID_RANGE
+        if not math.isfinite(llq) or llq > 1e-6:
+            bits |= STATUS_LOGQ
+        if rl and e == b:
+            bits |= STATUS_EMPTY_ROW
+        row, lq = ids[b:e], logq[b:e]
+        if np.any((row < 0) | (row >= V)):
+            bits |= STATUS_ID_RANGE
+        if np.any(~np.isfinite(lq) | (lq > 1e-6)):
+            bits |= STATUS_LOGQ
+        steps = np.diff(row)
+        if np.any(steps <= 0) if rep else np.any(steps < 0):
+            bits |= STATUS_ROW_ORDER
+        if rep and rl:
+            if label not in set(row.tolist()):
+                bits |= STATUS_LABEL_MISSING
+            with np.errstate(over="ignore", invalid="ignore"):
+                mass = float(np.sum(np.exp(lq)))
+            if not abs(mass - 1.0) <= 1e-3:
+                bits |= STATUS_SUPPORT_MASS
+    return bits
+
+
 def _rows(inputs: dict):
     off = np.asarray(inputs["offsets"], dtype=np.int64)
     return off
@@ -244,7 +307,7 @@ def head_forward(inputs: dict, p: HeadParams, rows=None, chunk: int = 64) -> dic
     rows = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
     n = rows.shape[0]
     out = {k: np.zeros(n) for k in ("loss", "lse", "lse_s", "entropy", "logp_label", "w_label",
-                                    "kl", "beta", "center")}
+                                    "kl", "beta", "center", "zmax")}
     out["mask_label"] = np.zeros(n, dtype=np.uint8)
     ent_lp, ent_mask, ent_w, ent_c, ent_u = [], [], [], [], []
     met = dict(n_rl=0, loss=0.0, mismatch_kl=0.0, masked=0, masked_low=0, masked_high=0, support_mass=0.0,
@@ -261,7 +324,7 @@ def head_forward(inputs: dict, p: HeadParams, rows=None, chunk: int = 64) -> dic
                                bool(inputs["replayed"][t]), p)
             rl = bool(inputs["loss_mask"][t])
             out["loss"][i] = fw["loss"] if rl else 0.0
-            for k in ("lse", "lse_s", "entropy", "logp_label", "w_label", "kl", "beta", "center"):
+            for k in ("lse", "lse_s", "entropy", "logp_label", "w_label", "kl", "beta", "center", "zmax"):
                 out[k][i] = fw[k]
             out["mask_label"][i] = 1 if fw["keep_label"] else 0
             ent_lp.append(fw["logp_support"])
@@ -295,16 +358,19 @@ def head_forward(inputs: dict, p: HeadParams, rows=None, chunk: int = 64) -> dic
 
 
 def head_backward(inputs: dict, p: HeadParams, dloss: np.ndarray, chunk: int = 64,
-                  rows=None, want_dW: bool = True, want_bounds: bool = False):
+                  rows=None, want_dW: bool = True, want_bounds: bool = False, want_dX: bool = True,
+                  vrows=None):
     """dX [N,H] and dW [V,H] of sum_t dloss_t * loss_t, fp64, by the chain rule:
     G_tj = dloss_t / T * d loss_t / d z_tj;  dX = G W;  dW = G^T X.
 
     ``rows`` restricts dX to those tokens (dW then sums over those tokens only).
+    ``vrows`` keeps only those vocabulary rows of dW (in that order); ``want_dX=False``
+    skips dX (and its bounds), returning None for it.
     ``want_bounds`` also returns the magnitudes a finite-precision evaluation is measured
     against, as a dict: ``X`` = |G| |W| and ``W`` = |G|^T |X| with |G| the sum of the
     magnitudes of the terms forming each G entry, and ``zX`` / ``zW`` the same products
-    with each |G| entry weighted by |z_tj| + |logsumexp_t| (how far an error in the
-    logits, proportional to their size, moves G).
+    with each |G| entry of token t weighted by max_j |z_tj| (an error in token t's logits
+    of that relative size moves G_t by as much).
     """
     off = _rows(inputs)
     N = off.shape[0] - 1
@@ -312,15 +378,17 @@ def head_backward(inputs: dict, p: HeadParams, dloss: np.ndarray, chunk: int = 6
     W = np.asarray(inputs["W"], dtype=np.float64)
     Xall = np.asarray(inputs["hidden"], dtype=np.float64)
     V, H = W.shape
-    dX = np.zeros((rows.shape[0], H))
-    dW = np.zeros((V, H)) if want_dW else None
+    vsel = np.arange(V) if vrows is None else np.asarray(vrows, dtype=np.int64)
+    dX = np.zeros((rows.shape[0], H)) if want_dX else None
+    dW = np.zeros((vsel.shape[0], H)) if want_dW else None
     bnd = {}
     if want_bounds:
-        bnd["X"] = np.zeros((rows.shape[0], H))
-        bnd["zX"] = np.zeros((rows.shape[0], H))
+        if want_dX:
+            bnd["X"] = np.zeros((rows.shape[0], H))
+            bnd["zX"] = np.zeros((rows.shape[0], H))
         if want_dW:
-            bnd["W"] = np.zeros((V, H))
-            bnd["zW"] = np.zeros((V, H))
+            bnd["W"] = np.zeros((vsel.shape[0], H))
+            bnd["zW"] = np.zeros((vsel.shape[0], H))
     for c0 in range(0, rows.shape[0], chunk):
         rr = rows[c0:c0 + chunk]
         Z = head_token_logits(inputs, rr, p.temperature)
@@ -341,19 +409,22 @@ def head_backward(inputs: dict, p: HeadParams, dloss: np.ndarray, chunk: int = 6
             if want_bounds:
                 G[j] = scale * res[0]
                 Gm[j] = abs(scale) * res[1]
-                Zm[j] = np.abs(Z[j]) + abs(fw["lse_s"])
+                Zm[j] = fw["zmax"]
             else:
                 G[j] = scale * res
-        dX[c0:c0 + rr.shape[0]] = G @ W
+        if want_dX:
+            dX[c0:c0 + rr.shape[0]] = G @ W
         if want_dW:
-            dW += G.T @ Xall[rr]
+            dW += G[:, vsel].T @ Xall[rr]
         if want_bounds:
-            aW, aX = np.abs(W), np.abs(Xall[rr])
-            bnd["X"][c0:c0 + rr.shape[0]] = Gm @ aW
-            bnd["zX"][c0:c0 + rr.shape[0]] = (Gm * Zm) @ aW
+            aX = np.abs(Xall[rr])
+            if want_dX:
+                aW = np.abs(W)
+                bnd["X"][c0:c0 + rr.shape[0]] = Gm @ aW
+                bnd["zX"][c0:c0 + rr.shape[0]] = (Gm * Zm) @ aW
             if want_dW:
-                bnd["W"] += Gm.T @ aX
-                bnd["zW"] += (Gm * Zm).T @ aX
+                bnd["W"] += Gm[:, vsel].T @ aX
+                bnd["zW"] += (Gm * Zm)[:, vsel].T @ aX
     if want_bounds:
         return dX, dW, bnd
     return dX, dW

@@ -201,7 +201,11 @@ def _rollout_correction(lp_train, lp_rollout, mask, seq_offsets, rp: RolloutPara
 
 
 def rollout_metrics_named(m: dict, rp: RolloutParams) -> dict:
-    """The page's metric names from the sums and counts ("Mismatch Metrics" tables)."""
+    """The page's metric names from the sums and counts ("Mismatch Metrics" tables), for
+    the metrics those settings emit: the monitoring metrics always; the IS/RS metrics by
+    the "Emitted when" column of the "IS/RS Correction Metrics" table (use_tis for the
+    weight statistics, the tis_mode for its fractions, use_rs, a set veto threshold).
+    A mean over an empty set is 0."""
     nv, ns, nk = max(m["n_valid"], 1), max(m["n_seq"], 1), max(m["n_kept"], 1)
     train_lppl = m["train_lppl_sum"] / ns
     rollout_lppl = m["rollout_lppl_sum"] / ns
@@ -211,23 +215,27 @@ def rollout_metrics_named(m: dict, rp: RolloutParams) -> dict:
         "kl": m["mis_kl_sum"] / nv, "k3_kl": m["k3_sum"] / nv,
         "log_ppl_diff": m["lppl_diff_sum"] / ns, "log_ppl_abs_diff": m["lppl_abs_diff_sum"] / ns,
         "ppl_ratio": m["ppl_ratio_sum"] / ns,
-        "chi2_token": m["chi2_token_sum"] / nv - 1.0, "chi2_seq": m["chi2_seq_sum"] / ns - 1.0,
+        "chi2_token": m["chi2_token_sum"] / nv - 1.0 if m["n_valid"] else 0.0,
+        "chi2_seq": m["chi2_seq_sum"] / ns - 1.0 if m["n_seq"] else 0.0,
         "train_rollout_logprob_abs_diff": m["abs_diff_sum"] / nv,
-        "tis_weight_before_bound": m["w_before_sum"] / nv, "tis_weight_after_bound": m["w_after_sum"] / nv,
-        "is_ratio_mean_after_tis_rs": m["kept_w_sum"] / nk, "batch_norm_factor": m["batch_norm_factor"],
-        "is_ratio_mean_final": m["final_sum"] / nk, "is_ratio_min_final": m["final_min"],
-        "is_ratio_max_final": m["final_max"],
-        "rs_catastrophic_token_fraction": m["n_cat_tokens"] / nv,
-        "rs_catastrophic_seq_fraction": m["n_cat_seqs"] / ns,
     }
-    lo, hi = m["n_tis_low"] / nv, m["n_tis_high"] / nv
-    if rp.tis_mode == TIS_TRUNCATE:
-        out["tis_truncate_fraction"] = hi
-    elif rp.tis_mode == TIS_CLIP:
-        out["tis_clip_fraction_low"], out["tis_clip_fraction_high"] = lo, hi
-    else:
-        out["tis_mask_fraction_low"], out["tis_mask_fraction_high"] = lo, hi
+    if rp.use_tis:
+        out.update({
+            "tis_weight_before_bound": m["w_before_sum"] / nv, "tis_weight_after_bound": m["w_after_sum"] / nv,
+            "is_ratio_mean_after_tis_rs": m["kept_w_sum"] / nk, "batch_norm_factor": m["batch_norm_factor"],
+            "is_ratio_mean_final": m["final_sum"] / nk, "is_ratio_min_final": m["final_min"],
+            "is_ratio_max_final": m["final_max"]})
+        lo, hi = m["n_tis_low"] / nv, m["n_tis_high"] / nv
+        if rp.tis_mode == TIS_TRUNCATE:
+            out["tis_truncate_fraction"] = hi
+        elif rp.tis_mode == TIS_CLIP:
+            out["tis_clip_fraction_low"], out["tis_clip_fraction_high"] = lo, hi
+        else:
+            out["tis_mask_fraction_low"], out["tis_mask_fraction_high"] = lo, hi
     if rp.use_rs:
         out["rs_mask_fraction_low"] = m["n_rs_low"] / nv
         out["rs_mask_fraction_high"] = m["n_rs_high"] / nv
+    if rp.rs_veto_threshold is not None and rp.rs_veto_threshold > 0:
+        out["rs_catastrophic_token_fraction"] = m["n_cat_tokens"] / nv
+        out["rs_catastrophic_seq_fraction"] = m["n_cat_seqs"] / ns
     return out

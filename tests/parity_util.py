@@ -1,17 +1,27 @@
 """Tolerances and comparison helpers for the GPU-vs-oracle parity tests.
 
-The bars (stated for this path): logprobs within 1e-5 absolute; loss within 1e-4
-relative; masks, gathers and masked counts bit-exact; gradients within 2 bf16 ulp of
-the oracle rounded to bf16.  Readings of the gradient bar:
+The bars (stated for this path): logprobs within 1e-5 absolute (fp32 accumulate); loss
+within 1e-4 relative; masks, gathers and masked counts bit-exact; gradients within 2
+bf16 ulp of the oracle rounded to bf16.
+
+Log-prob bar.  A logit z_tj is an fp32 accumulation of H bf16 products; its rounding is
+modelled as 2^-24 sqrt(H) times the row's largest logit magnitude Z_t = max_j |z_tj| (the
+random-walk growth of H fp32 roundings of partial sums no larger than about Z_t), taken
+twice: once for the gathered logit, once for the logsumexp it is measured against (a
+p-weighted mean of the same logit errors).  The logsumexp itself and the subtraction
+z - lse each round to fp32 once more: two ulps of lse.  So
+    |gpu - ref| <= 1e-5 + 2 * 2^-24 sqrt(H) Z_t + 2 ulp_fp32(lse_t).
+At H = 2048 with Z_t ~ 4.5 (the literal c2-c4 scales) that is 1e-5 + 2.4e-5 + 2e-6.
+
+Readings of the gradient bar (a row is one token of dX or one vocabulary id of dW):
   element   |gpu - bf16(ref)| <= 2 ulp(max(|ref|, 2^-8 * rowmax|ref|))  (grad_precision SPLIT)
-  row       max_h |gpu - bf16(ref)| <= 2 ulp(rowmax|ref|)
+  row       max_h |gpu - bf16(ref)| <= 2 ulp(rowmax|ref|)              (grad_precision BF16)
+and, reported as diagnostics only (not asserted):
   operand   |gpu - bf16(ref)| <= 2 ulp(ref) + 2^-8 * bound             (one bf16 GEMM operand
-            rounded: dX, and dW of the two-call path; bound = sum of term magnitudes)
-  operand2  |gpu - bf16(ref)| <= 2 ulp(ref) + 2^-7 * bound             (both GEMM operands
-            rounded: dW of the fused bf16 path, whose second operand is bf16(rs_t x_t))
-where a row is one token of dX or one vocabulary id of dW, and 2^-8 is bf16's unit
-roundoff (half an ulp at the bottom of a binade), so 2^-7 * bound is 2 ulp of the term
-magnitudes.
+            rounded; bound = sum of term magnitudes)
+  operand2  |gpu - bf16(ref)| <= 2 ulp(ref) + 2^-7 * bound             (both operands rounded)
+2^-8 is bf16's unit roundoff.  Every reading first subtracts the logits' fp32
+accumulation allowance carried into G (acc_tol of the |G| Z_t-weighted magnitudes).
 """
 import math
 
@@ -26,16 +36,22 @@ LOSS_REL = 1e-4
 EPS32 = 2.0 ** -24
 
 
-def acc_tol(H: int, zmag):
-    """fp32-accumulation allowance of a logit built from H bf16 products: the rounding of
-    an fp32 running sum of H terms grows like 2^-24 sqrt(H) times the size of the sum;
-    two such 4-sigma-ish allowances (the entry and the logsumexp it is taken against)."""
-    return 2.0 * EPS32 * np.sqrt(H) * np.asarray(zmag, dtype=np.float64)
+def acc_tol(H: int, zmax):
+    """fp32-accumulation allowance of logits built from H bf16 products, for a row whose
+    largest logit magnitude is zmax: 2^-24 sqrt(H) zmax, twice (the gathered logit and
+    the logsumexp it is taken against)."""
+    return 2.0 * EPS32 * np.sqrt(H) * np.asarray(zmax, dtype=np.float64)
 
 
-def logp_tol(H: int, z_abs, lse_abs):
-    """Log-prob bar: 1e-5 absolute plus the fp32-accumulation allowance of |z| + |lse|."""
-    return LOGP_TOL + acc_tol(H, np.abs(z_abs) + np.abs(lse_abs))
+def ulp32(x):
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    return 2.0 ** (np.floor(np.log2(np.maximum(x, 2.0 ** -126))) - 23)
+
+
+def logp_tol(H: int, zmax, lse):
+    """Log-prob bar of a token whose largest logit magnitude is zmax and whose logsumexp
+    (full, or over the replayed support) is lse: 1e-5 + acc_tol + 2 fp32 ulps of lse."""
+    return LOGP_TOL + acc_tol(H, zmax) + 2.0 * ulp32(lse)
 
 
 def f32(x):
@@ -62,9 +78,10 @@ def to_bf16(x):
     return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
 
 
-def grad_check(gpu, ref, reading: str, what: str, bounds=None, key="X", H=2048, block=8192):
+def grad_check(gpu, ref, reading: str, what: str, bounds=None, key="X", H=2048, block=8192, strict=True):
     """Row-blocked grad_check_block (bounded host memory for [V, H] arrays).  ``bounds`` is
-    the oracle's dict (keys X / zX for dX, W / zW for dW; ``key`` names the first)."""
+    the oracle's dict (keys X / zX for dX, W / zW for dW; ``key`` names the first).
+    ``strict=False`` only measures (a diagnostic reading)."""
     worst = 0.0
     n = np.asarray(ref).shape[0]
     b = None if bounds is None else np.asarray(bounds[key])
@@ -72,19 +89,20 @@ def grad_check(gpu, ref, reading: str, what: str, bounds=None, key="X", H=2048, 
     for r0 in range(0, max(n, 1), block):
         sl = slice(r0, min(n, r0 + block))
         worst = max(worst, grad_check_block(np.asarray(gpu)[sl], np.asarray(ref)[sl], reading, what,
-                                            None if b is None else b[sl], None if zb is None else zb[sl], H))
+                                            None if b is None else b[sl], None if zb is None else zb[sl], H,
+                                            strict))
     return worst
 
 
-def grad_check_block(gpu, ref, reading: str, what: str, bound=None, zbound=None, H=2048):
-    """Assert the gradient bar; returns the worst ratio err / allowed.
+def grad_check_block(gpu, ref, reading: str, what: str, bound=None, zbound=None, H=2048, strict=True):
+    """Assert the gradient bar (unless ``strict`` is False); returns the worst ratio
+    err / allowed.
 
     readings: "element" (2 ulp of max(|ref|, 2^-8 rowmax)), "row" (2 ulp of the row max),
-    "operand" (2 ulp of |ref| plus 2^-8 of the magnitude bound |G||W| / |G|^T|X|: the
-    result is exact to the precision of its bf16-rounded softmax-gradient operand),
+    "operand" (2 ulp of |ref| plus 2^-8 of the magnitude bound |G||W| / |G|^T|X|),
     "operand2" (2^-7 of the bound: both operands of each product rounded to bf16).
     Every reading also carries the logits' fp32-accumulation allowance carried into G
-    (acc_tol on zbound, the |G| |z|-weighted magnitude)."""
+    (acc_tol on zbound, the |G| Z_t-weighted magnitude)."""
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     rb = to_bf16(ref)
@@ -97,7 +115,7 @@ def grad_check_block(gpu, ref, reading: str, what: str, bound=None, zbound=None,
         allowed = 2 * ulp_bf16(ref) * (ref != 0) + frac * np.asarray(bound, np.float64)
         ratio = np.where(allowed > 0, err / np.maximum(allowed, 1e-300), np.where(err > 0, np.inf, 0.0))
         worst = float(np.max(ratio)) if ratio.size else 0.0
-        assert worst <= 1.0, f"{what}: worst err/allowed = {worst:.3f} ({reading} reading)"
+        assert worst <= 1.0 or not strict, f"{what}: worst err/allowed = {worst:.3f} ({reading} reading)"
         return worst
     if reading == "element":
         allowed = 2 * ulp_bf16(np.maximum(np.abs(ref), 2.0 ** -8 * rowmax))
@@ -107,15 +125,15 @@ def grad_check_block(gpu, ref, reading: str, what: str, bound=None, zbound=None,
         ratio = np.max(err, axis=1, keepdims=True) / allowed
     ratio = np.where(rowmax > 0, ratio, np.where(np.max(err, axis=1, keepdims=True) > 0, np.inf, 0.0))
     worst = float(np.max(ratio)) if ratio.size else 0.0
-    assert worst <= 1.0, f"{what}: worst err/allowed = {worst:.3f} ({reading} reading)"
+    assert worst <= 1.0 or not strict, f"{what}: worst err/allowed = {worst:.3f} ({reading} reading)"
     return worst
 
 
 def loss_prop_tol(ref: dict, inp: dict, op: oracle.HeadParams):
-    """Per-token loss bar: the 1e-5 log-prob bar carried through the loss to first order,
-    |d loss_t| <= |adv_tau A_t| (|w_a| + sum_e |c_e|) * 1e-5 + beta_t * (sum_e u_e or 1) * 1e-5
-    (+ entropy_coeff times the entropy's bar, the logsumexp's), doubled.  (A per-token loss
-    is a difference of O(1) log-prob terms, so where it cancels a relative bar alone cannot
+    """Per-token loss bar: the token's log-prob bar (logp_tol) carried through the loss to
+    first order, |d loss_t| <= |adv_tau A_t| (|w_a| + sum_e |c_e|) lp_t + beta_t (sum_e u_e
+    or 1) lp_t (+ entropy_coeff times the entropy's bar), doubled.  (A per-token loss is a
+    difference of O(1) log-prob terms, so where it cancels a relative bar alone cannot
     hold.)"""
     off = np.asarray(inp["offsets"], np.int64)
     abs_c = np.add.reduceat(np.abs(ref["c_support"]), off[:-1]) if ref["c_support"].size else np.zeros(len(off) - 1)
@@ -126,8 +144,9 @@ def loss_prop_tol(ref: dict, inp: dict, op: oracle.HeadParams):
     kl_w = sum_u if op.kl_estimator == oracle.KL_EXACT else np.ones_like(sum_u)
     A = np.abs(op.adv_tau * np.asarray(inp["adv"], np.float64))
     H = np.asarray(inp["hidden"]).shape[1]
-    ent = op.entropy_coeff * logp_tol(H, ref["lse"], ref["lse"]) / LOGP_TOL if op.entropy_coeff else 0.0
-    return 2 * LOGP_TOL * (A * (np.abs(ref["w_label"]) + abs_c) + np.asarray(ref["beta"]) * kl_w + ent)
+    lp = logp_tol(H, ref["zmax"], ref["lse_s"])
+    ent = op.entropy_coeff * logp_tol(H, ref["zmax"], ref["lse"]) if op.entropy_coeff else 0.0
+    return 2 * (lp * (A * (np.abs(ref["w_label"]) + abs_c) + np.asarray(ref["beta"]) * kl_w) + ent)
 
 
 def loss_check(gpu, ref, prop_tol=None, what="loss"):

@@ -124,3 +124,21 @@ def test_binding_signatures_match_header_arity():
     for name, (_, args) in rh._SIGS.items():
         assert name in declared, name
         assert len(args) == declared[name], (name, len(args), declared[name])
+
+
+def test_options_and_new_entry_points_check_their_arguments(lib):
+    assert lib.rl_get_option(rh.RL_OPT_WAIT_LIMIT_US) == 1_000_000          # 1 s by default
+    for bad in (0, -5, 10_000_001):
+        assert lib.rl_set_option(rh.RL_OPT_WAIT_LIMIT_US, bad) == rh.RL_ERR_ARG
+    assert lib.rl_set_option(rh.RL_OPT_WAIT_LIMIT_US, 2500) == rh.RL_OK
+    assert lib.rl_get_option(rh.RL_OPT_WAIT_LIMIT_US) == 2500
+    assert lib.rl_set_option(rh.RL_OPT_WAIT_LIMIT_US, 1_000_000) == rh.RL_OK
+    assert lib.rl_set_option(99, 1) == rh.RL_ERR_ARG and lib.rl_get_option(99) == -1
+    assert lib.rl_wait_selftest(None, None) == rh.RL_ERR_ARG
+    rp = rh.RcParams().c()
+    assert lib.rl_rollout_metrics_named(None, ctypes.byref(rp), ctypes.c_void_p(1 << 20), None) == rh.RL_ERR_ARG
+    bad = rh.RcParams().c()
+    bad.tis_mode = 5
+    assert lib.rl_rollout_metrics_named(ctypes.c_void_p(1 << 20), ctypes.byref(bad), ctypes.c_void_p(1 << 20),
+                                        None) == rh.RL_ERR_ARG
+    assert ctypes.sizeof(rh.RlRcNamed) == 28 * 8

@@ -15,7 +15,7 @@ import torch
 
 import lm_head_gb300 as rh
 import workloads
-from oracle.rollout import RolloutParams, rollout_correction
+from oracle.rollout import RolloutParams, rollout_correction, rollout_metrics_named
 
 pytestmark = pytest.mark.gpu
 
@@ -175,3 +175,66 @@ def test_normalisation_past_the_integer_totals_range():
     for p in (rh.RcParams(tis_mode="truncate", tis_upper_bound=1e30, tis_batch_normalize=True),
               rh.RcParams(tis_mode="clip", tis_lower_bound=0.1, tis_upper_bound=10.0, tis_batch_normalize=True)):
         _compare(lt.astype(np.float32), lr.astype(np.float32), m, off, p)
+
+
+def _named_tolerance(key, rm, rn):
+    """Bar of a named metric, from the bars of the sums it is formed from (1e-5 relative
+    plus 1e-6 per term, divided by the count it is a mean over); counts are bit-exact, so
+    the fractions are equal outright; the factor and the min / max to 4e-6 relative."""
+    nv, ns, nk = max(rm["n_valid"], 1), max(rm["n_seq"], 1), max(rm["n_kept"], 1)
+    tok = {"kl": "mis_kl_sum", "k3_kl": "k3_sum", "train_rollout_logprob_abs_diff": "abs_diff_sum",
+           "chi2_token": "chi2_token_sum", "tis_weight_before_bound": "w_before_sum",
+           "tis_weight_after_bound": "w_after_sum"}
+    seq = {"training_log_ppl": "train_lppl_sum", "rollout_log_ppl": "rollout_lppl_sum", "log_ppl_diff": "lppl_diff_sum",
+           "log_ppl_abs_diff": "lppl_abs_diff_sum", "ppl_ratio": "ppl_ratio_sum", "chi2_seq": "chi2_seq_sum"}
+    kept = {"is_ratio_mean_after_tis_rs": "kept_w_sum", "is_ratio_mean_final": "final_sum"}
+    if key in tok:
+        return (1e-5 * abs(rm[tok[key]]) + 1e-6 * nv) / nv
+    if key in seq:
+        return (1e-5 * abs(rm[seq[key]]) + 1e-6 * ns) / ns
+    if key in kept:
+        return (1e-5 * abs(rm[kept[key]]) + 1e-6 * nv) / nk
+    if key in ("training_ppl", "rollout_ppl"):
+        base = "training_log_ppl" if key == "training_ppl" else "rollout_log_ppl"
+        return 1.01 * rn[key] * _named_tolerance(base, rm, rn)
+    if key in ("batch_norm_factor", "is_ratio_min_final", "is_ratio_max_final"):
+        return 4e-6 * abs(rn[key])
+    return 0.0                                          # fractions of exact counts
+
+
+def _named_compare(lt, lr, m, off, p):
+    d = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (lt, lr, m, np.asarray(off, np.int64))]
+    _, _, met = rh.rl_rollout_correction(*d, p)
+    named = rh.rl_rollout_metrics_named(met, p)
+    torch.cuda.synchronize()
+    op = _oracle_params(p)
+    ref = rollout_correction(lt, lr, m, off, op)
+    rn = rollout_metrics_named(ref["metrics"], op)
+    assert set(named) == set(rn), (set(named) ^ set(rn))
+    for k, r in rn.items():
+        g = named[k]
+        if math.isinf(r):
+            assert g == r, k
+            continue
+        assert abs(g - r) <= _named_tolerance(k, ref["metrics"], rn), (k, g, r)
+
+
+@pytest.mark.parametrize("cfg", range(len(SETTINGS)))
+def test_named_metrics_c5_against_the_oracle(cfg):
+    """The page's named metrics, formed on the device from the sums, against the oracle's
+    named metrics: the emitted set per the "Emitted when" column, and every value."""
+    _named_compare(*_c5(), SETTINGS[cfg])
+
+
+def test_named_metrics_ragged_against_the_oracle():
+    rng = np.random.default_rng(19)
+    lens = rng.integers(0, 500, size=61)
+    lens[[2, 30]] = 0
+    T = int(lens.sum())
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    lr = np.log(rng.random(T) * 0.98 + 0.01).astype(np.float32)
+    lt = np.minimum(lr + rng.normal(0, 0.25, T), 0).astype(np.float32)
+    m = (rng.random(T) < 0.8).astype(np.uint8)
+    for p in SETTINGS + [rh.RcParams(use_tis=False, rs_veto_threshold=1e-3),
+                         rh.RcParams(tis_mode="mask", tis_lower_bound=0.8, tis_upper_bound=1.25)]:
+        _named_compare(lt, lr, m, off, p)

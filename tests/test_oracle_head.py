@@ -426,3 +426,149 @@ def test_entropy_regulariser_closed_forms():
     assert abs(d.sum()) < 1e-14
     # the entropy gradient points away from the most likely id (lowering its logit raises H)
     assert d[np.argmax(pf)] > 0 > d[np.argmin(pf)]
+
+
+# --------------------------------------------------------------------------------------
+# mask_tv (reading R9) and the inv_sqrt staleness (reading R6)
+# --------------------------------------------------------------------------------------
+def _tv_mask_removes(P, keep):
+    """Total variation between P and P conditioned on the kept set, by enumeration."""
+    P = np.asarray(P, np.float64)
+    Pk = np.where(keep, P, 0.0)
+    Pk = Pk / Pk.sum()
+    return 0.5 * float(np.abs(P - Pk).sum())
+
+
+@pytest.mark.parametrize("loss_type,knobs", [(LOSS_IPO, dict(eps=0.04)),
+                                             (LOSS_ICEPOP, dict(icepop_low=0.7, icepop_high=1.3))])
+def test_mask_tv_is_the_total_variation_the_mask_removes_under_exact_replay(loss_type, knobs):
+    """Under exact replay (u = q over the support S), mask_tv of a token equals
+    TV(P, P | kept entries): the trainer mass the mask takes off the centering support.
+    P, q and the masks are enumerated here from their definitions on a 24-id vocabulary
+    (truncated supports of 9..24 ids)."""
+    rng = np.random.default_rng(21)
+    V = 24
+    p = HeadParams(loss_type=loss_type, **knobs)
+    for trial in range(12):
+        z = rng.normal(0, 1.2, size=(1, V))
+        k = int(rng.integers(9, V + 1))
+        S = np.sort(rng.choice(V, size=k, replace=False))
+        qs = scipy.special.softmax(z[0, S] + rng.normal(0, 0.6, size=k))     # sampler, renormalised on S
+        label = int(S[int(rng.integers(k))])
+        inp = identity_case(z, [label], [math.log(qs[list(S).index(label)])], [(list(S), list(np.log(qs)))], [1])
+        out = oracle.head_forward(inp, p)
+        PS = scipy.special.softmax(z[0, S])                                   # trainer, renormalised on S
+        if loss_type == LOSS_IPO:
+            keep = np.abs(PS - qs) <= p.eps
+        else:
+            keep = (PS / qs >= p.icepop_low) & (PS / qs <= p.icepop_high)
+        if keep.all() or not keep.any():
+            assert out["metrics"]["mask_tv"] == pytest.approx(0.0 if keep.all() else 1.0, abs=1e-12)
+            continue
+        assert out["metrics"]["mask_tv"] == pytest.approx(_tv_mask_removes(PS, keep), rel=1e-12)
+
+
+def test_mask_tv_with_draws_estimates_the_masked_trainer_mass():
+    """With K i.i.d. draws from q (u = 1/K), mask_tv is the importance-weighted estimate
+    of the full-vocabulary trainer mass the mask removes, sum_v p_v 1(v masked) =
+    TV(p, p | kept): within 5 sigma (CLT) for K = 20000, sigma from the exact variance of
+    (1 - m) p / q under q."""
+    rng = np.random.default_rng(22)
+    V = 20
+    z = rng.normal(0, 1.0, size=(1, V))
+    pf = scipy.special.softmax(z[0])
+    q = scipy.special.softmax(z[0] + rng.normal(0, 0.7, size=V))
+    p = HeadParams(loss_type=LOSS_IPO, eps=0.02)
+    keep = np.abs(pf - q) <= p.eps
+    assert 0 < keep.sum() < V
+    K = 20000
+    draws = np.sort(rng.choice(V, size=K, p=q))
+    inp = identity_case(z, [int(draws[0])], [math.log(q[draws[0]])], [(list(draws), list(np.log(q[draws])))], [0])
+    got = oracle.head_forward(inp, p)["metrics"]["mask_tv"]
+    f = (~keep) * pf / q
+    mean = float((q * f).sum())
+    sd = math.sqrt(float((q * f ** 2).sum()) - mean ** 2) / math.sqrt(K)
+    assert mean == pytest.approx(_tv_mask_removes(pf, keep), rel=1e-12)
+    assert abs(got - mean) <= 5 * sd
+
+
+def test_inv_sqrt_beta_follows_its_stated_properties():
+    """Reading R6: age 0 takes the full kl_coeff, beta falls strictly with the policy age,
+    and halves by age 3; no staleness leaves kl_coeff at every age."""
+    c = 0.04
+    stale = HeadParams(kl_coeff=c, kl_staleness=oracle.STALE_INV_SQRT)
+    betas = [oracle.rl_head.kl_beta(a, stale) for a in range(12)]
+    assert betas[0] == c
+    assert all(b1 < b0 for b0, b1 in zip(betas, betas[1:]))
+    assert betas[3] == pytest.approx(c / 2, rel=1e-15)
+    assert all(oracle.rl_head.kl_beta(a, HeadParams(kl_coeff=c)) == c for a in range(12))
+    # and beta scales the KL term of the loss: the loss moves by (beta_1 - beta_0) KL
+    z = np.array([[0.3, -0.2, 1.1, 0.0]])
+    q = scipy.special.softmax([0.1, 0.0, 0.9, 0.2])
+    sup = ([0, 1, 2, 3], list(np.log(q)))
+    l0 = oracle.head_forward(identity_case(z, [2], [math.log(q[2])], [sup], [1], age=[0]), stale)
+    l1 = oracle.head_forward(identity_case(z, [2], [math.log(q[2])], [sup], [1], age=[1]), stale)
+    kl = float((q * (np.log(q) - np.log(scipy.special.softmax(z[0])))).sum())
+    assert l1["loss"][0] - l0["loss"][0] == pytest.approx((c / math.sqrt(2) - c) * kl, rel=1e-10)
+
+
+# --------------------------------------------------------------------------------------
+# Sampler-evidence validation (pull request #4233, GPU validation of the CSR entries)
+# --------------------------------------------------------------------------------------
+def _valid_case():
+    rng = np.random.default_rng(23)
+    V = 50
+    z = rng.normal(0, 1, size=(4, V))
+    sup, lq = [], []
+    for t in range(4):
+        if t % 2 == 0:                          # replayed, renormalised q, label inside
+            S = np.sort(rng.choice(V, size=8, replace=False))
+            q = scipy.special.softmax(rng.normal(0, 1, 8))
+            sup.append((list(S), list(np.log(q))))
+            lq.append(float(np.log(q[3])))
+        else:                                   # draws, duplicates allowed, ascending
+            d = np.sort(rng.integers(0, V, 6))
+            sup.append((list(d), list(np.log(np.full(6, 0.02)))))
+            lq.append(math.log(0.05))
+    labels = [int(sup[0][0][3]), 7, int(sup[2][0][3]), 9]
+    return identity_case(z, labels, lq, sup, [1, 0, 1, 0]), V
+
+
+def test_validation_accepts_a_clean_batch_and_names_each_fault():
+    inp, V = _valid_case()
+    check = lambda d: oracle.validate_support(d, V)
+    assert check(inp) == 0
+    S = oracle.rl_head
+
+    def mod(**kw):
+        d = {k: (v.copy() if isinstance(v, np.ndarray) else v) for k, v in inp.items()}
+        for k, f in kw.items():
+            f(d[k])
+        return d
+
+    def setitem(i, v):
+        def f(a):
+            a[i] = v
+        return f
+    assert check(mod(offsets=setitem(0, 1))) & S.STATUS_OFFSETS
+    assert check(mod(offsets=setitem(2, 3))) & S.STATUS_OFFSETS           # decreasing: row 1 bad
+    assert check(mod(offsets=setitem(4, 99))) == S.STATUS_OFFSETS         # past nnz, last row skipped
+    assert check(mod(ids=setitem(7, V))) == S.STATUS_ID_RANGE            # last of its row: order kept
+    assert check(mod(labels=setitem(1, -1))) == S.STATUS_ID_RANGE
+    assert check(mod(logq=setitem(9, 0.5))) == S.STATUS_LOGQ              # log q > 1e-6
+    assert check(mod(logq=setitem(9, np.nan))) == S.STATUS_LOGQ
+    assert check(mod(label_logq=setitem(1, np.inf))) == S.STATUS_LOGQ
+    row0 = list(inp["ids"][:8])
+    missing = next(v for v in range(V) if v not in row0)
+    assert check(mod(labels=setitem(0, missing))) == S.STATUS_LABEL_MISSING
+    assert check(mod(logq=lambda a: a.__setitem__(slice(0, 8), a[:8] + math.log(0.9)))) == S.STATUS_SUPPORT_MASS
+    assert check(mod(ids=lambda a: a.__setitem__(slice(2, 4), a[2:4][::-1].copy()))) == S.STATUS_ROW_ORDER
+    # a draw row may repeat an id (ascending, not strictly); a replayed row may not
+    dup = mod(ids=lambda a: a.__setitem__(9, a[8]))
+    assert check(dup) == 0
+    assert check(mod(ids=lambda a: a.__setitem__(1, a[0]))) & S.STATUS_ROW_ORDER
+    # an RL token with an empty row; a non-RL one may have it
+    e = dict(inp, offsets=np.array([0, 8, 8, 16, 22]), ids=np.concatenate([inp["ids"][:8], inp["ids"][14:]]),
+             logq=np.concatenate([inp["logq"][:8], inp["logq"][14:]]))
+    assert check(e) == S.STATUS_EMPTY_ROW
+    assert check(dict(e, loss_mask=np.array([1, 0, 1, 1], np.uint8))) == 0

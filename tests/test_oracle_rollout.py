@@ -148,7 +148,7 @@ def test_identical_policies_have_no_mismatch():
                            RolloutParams(use_rs=True, rs_level=LEVEL_GEOMETRIC, rs_veto_threshold=1e-4,
                                          tis_batch_normalize=True))
     assert np.all(r["weights"] == 1.0) and np.all(r["keep"] == 1)
-    nm = rollout_metrics_named(r["metrics"], RolloutParams())
+    nm = rollout_metrics_named(r["metrics"], RolloutParams(rs_veto_threshold=1e-4))
     for k in ("kl", "k3_kl", "log_ppl_diff", "log_ppl_abs_diff", "chi2_token", "chi2_seq",
               "train_rollout_logprob_abs_diff", "tis_truncate_fraction", "rs_catastrophic_token_fraction"):
         assert nm[k] == pytest.approx(0.0, abs=1e-12), k
@@ -230,3 +230,29 @@ def test_nonfinite_padding_changes_nothing():
         np.testing.assert_array_equal(a["weights"], b["weights"])
         np.testing.assert_array_equal(a["keep"], b["keep"])
         assert a["metrics"] == b["metrics"]
+
+
+def test_named_metrics_follow_the_emitted_when_column():
+    """"IS/RS Correction Metrics", "Emitted when": the weight statistics need use_tis, a
+    mode's fractions that mode, the RS fractions use_rs, the catastrophic fractions a veto
+    threshold; the monitoring metrics are always there."""
+    rng = np.random.default_rng(6)
+    lr = np.log(rng.random(200) * 0.9 + 0.05)
+    lt = np.minimum(lr + rng.normal(0, 0.3, 200), 0.0)
+    m = np.ones(200, np.uint8)
+    always = {"training_log_ppl", "training_ppl", "rollout_log_ppl", "rollout_ppl", "kl", "k3_kl", "log_ppl_diff",
+              "log_ppl_abs_diff", "ppl_ratio", "chi2_token", "chi2_seq", "train_rollout_logprob_abs_diff"}
+    weights = {"tis_weight_before_bound", "tis_weight_after_bound", "is_ratio_mean_after_tis_rs",
+               "batch_norm_factor", "is_ratio_mean_final", "is_ratio_min_final", "is_ratio_max_final"}
+    for rp, extra in ((RolloutParams(use_tis=False), set()),
+                      (RolloutParams(), weights | {"tis_truncate_fraction"}),
+                      (RolloutParams(tis_mode=TIS_CLIP, use_rs=True), weights | {
+                          "tis_clip_fraction_low", "tis_clip_fraction_high", "rs_mask_fraction_low",
+                          "rs_mask_fraction_high"}),
+                      (RolloutParams(tis_mode=TIS_MASK, use_tis=False, rs_veto_threshold=1e-3), {
+                          "rs_catastrophic_token_fraction", "rs_catastrophic_seq_fraction"}),
+                      (RolloutParams(tis_mode=TIS_MASK, rs_veto_threshold=1e-3), weights | {
+                          "tis_mask_fraction_low", "tis_mask_fraction_high", "rs_catastrophic_token_fraction",
+                          "rs_catastrophic_seq_fraction"})):
+        r = rollout_correction(lt, lr, m, [0, 80, 200], rp)
+        assert set(rollout_metrics_named(r["metrics"], rp)) == always | extra
