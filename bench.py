@@ -169,61 +169,97 @@ def cpu_baseline(case_host: dict, n_tokens: int, threads: int):
                       f"forward + backward incl. dW; {dt:.1f} s"}
 
 
-def elementwise_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb: int = 4096):
-    """The elementwise PPO / dual-clip / decoupled-TIS / mismatch path on its own workload
-    (1.8M valid tokens in sequences of 64..4096, padded to 4096), against the HBM roofline.
-    Each pass follows a memset of flush_mb MB (default 4 GB: an L2 flush that keeps the GPU
-    busy for about half a millisecond, long enough for the host to queue the pass before
-    the GPU reaches it; profiling runs pass a smaller one).  The library's own event pairs
-    (rl_profile) time the call in two parts, the 256-byte workspace memset and the kernel
-    launch: their sum is the pass (us_per_pass, tokens_per_s), the launch alone
-    (kernel_us_per_pass) is what the roofline divides by.
-    Algorithmic bytes per slot: four fp32 inputs and the mask byte read, four fp32
-    outputs written (33 B)."""
+def _rotating_sets(torch, dev, arrays, min_bytes):
+    """Copies of the input arrays, enough of them that one round over the copies moves
+    more than min_bytes (so a pass never finds its inputs in L2 from the previous round)."""
+    one = sum(a.nbytes for a in arrays if a is not None)
+    n = max(2, -(-int(min_bytes) // max(one, 1)))
+    return [[None if a is None else torch.from_numpy(a).to(dev) for a in arrays] for _ in range(n)]
+
+
+def _time_back_to_back(torch, calls, passes):
+    """Average device time per call over `passes` calls issued back to back between one
+    pair of CUDA events on the current stream (each call takes the next input set)."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(passes):
+        calls[i % len(calls)]()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / passes
+
+
+def elementwise_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb: int = 4096, packed: bool = True):
+    """The elementwise PPO / dual-clip / decoupled-TIS / mismatch path on its own workload,
+    1.8M valid tokens in sequences of 64..4096, against the HBM roofline.
+
+    packed (the default and the roofline line): the valid tokens end to end, no mask; per
+    token 16 B read (four fp32 inputs) and 16 B written (four fp32 outputs).  Otherwise the
+    sequences padded to 4096 slots with a response mask: 17 B read and 16 B written per slot.
+
+    Timing: `passes` calls back to back between one event pair, over rotating copies of the
+    inputs whose total is more than twice L2 (no pass finds its inputs in L2); per call
+    that is the workspace memset and the kernel launch, the figure the roofline divides
+    by.  The library's own per-launch event pairs (rl_profile) time single calls after an
+    L2-flushing memset as well (kernel_us_single_launch), a figure that includes an event
+    pair's own ~2 us."""
+    import numpy as np
     import workloads
     c = workloads.make_policy_case()
-    ins = [torch.from_numpy(x).to(dev) for x in (c.lp_theta, c.lp_old, c.lp_samp, c.adv, c.mask)]
-    T = int(ins[0].numel())
+    if packed:
+        p = c.packed()
+        arrays = [p["lp_theta"], p["lp_old"], p["lp_samp"], p["adv"], None]
+    else:
+        arrays = [c.lp_theta, c.lp_old, c.lp_samp, c.adv, c.mask]
+    T = int(arrays[0].shape[0])
     pp = rh.PgParams()
+    sets = _rotating_sets(torch, dev, arrays, 2 * 129 * 2 ** 20 + 1)
     outs = tuple(torch.empty(T, dtype=torch.float32, device=dev) for _ in range(4))
     met = torch.zeros(rh.ctypes.sizeof(rh.RlPgMetrics), dtype=torch.uint8, device=dev)
-    ws = torch.empty(rh.rl_policy_workspace_bytes(T), dtype=torch.uint8, device=dev)
-    run = lambda: rh.rl_policy_loss_elementwise(*ins, pp, outputs=outs, ws=ws, metrics_dev=met)
-    big = torch.empty(flush_mb << 20, dtype=torch.uint8, device=dev)
-    for _ in range(warmup):
-        run()
+    ws = torch.zeros(rh.rl_policy_workspace_bytes(T), dtype=torch.uint8, device=dev)   # zeroed once
+    calls = [(lambda ins=ins: rh.rl_policy_loss_elementwise(*ins, pp, outputs=outs, ws=ws, metrics_dev=met))
+             for ins in sets]
+    for i in range(max(warmup, 3)):
+        calls[i % len(calls)]()
     torch.cuda.synchronize()
-    per, kern = [], []
-    for _ in range(steps):
+    passes = max(steps, 10) * len(calls)
+    ms = _time_back_to_back(torch, calls, passes)
+    # single calls after an L2 flush, each timed by the library's event pairs
+    big = torch.empty(flush_mb << 20, dtype=torch.uint8, device=dev)
+    kern = []
+    for i in range(max(steps, 10)):
         big.zero_()
         rh.rl_profile_enable(True)
-        run()
+        calls[i % len(calls)]()
         prof = rh.rl_profile_read()
         rh.rl_profile_enable(False)
-        per.append(sum(t for t, _ in prof.values()))
         kern.append(sum(t for k, (t, _) in prof.items() if k == "policy"))
     del big
-    ms = statistics.median(per)        # the whole call: workspace memset + kernel launches
-    kms = statistics.median(kern)      # the kernel launches alone (the roofline's duration)
-    nbytes = T * (4 * 4 + 1) + T * 4 * 4
-    gbs = nbytes / (kms / 1e3) / 1e9
-    peak = float(peaks["hbm_gbs"])
+    kms = statistics.median(kern)
     n_valid = int(c.mask.sum())
-    return {"workload": f"c5: {n_valid} valid tokens, {len(c.seq_lens)} sequences of 64..4096 padded to "
-                        f"{c.max_len} (T={T} slots); PPO clip 0.2/0.2 + dual clip 3, decoupled TIS, "
-                        "10-point IPO curve, IcePop band, mismatch KL",
-            "us_per_pass": ms * 1e3, "kernel_us_per_pass": kms * 1e3, "tokens_per_s": n_valid / (ms / 1e3),
-            "passes": steps,
+    nbytes = T * (16 + (0 if packed else 1)) + T * 16
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peak = float(peaks["hbm_gbs"])
+    layout = (f"packed: {n_valid} valid tokens end to end, no mask" if packed else
+              f"padded: {len(c.seq_lens)} sequences of 64..4096 padded to {c.max_len} (T={T} slots) with a mask")
+    return {"workload": f"c5 {layout}; PPO clip 0.2/0.2 + dual clip 3, decoupled TIS, 10-point IPO curve, "
+                        "IcePop band, mismatch KL",
+            "us_per_call_back_to_back": ms * 1e3, "kernel_us_single_launch": kms * 1e3,
+            "tokens_per_s": n_valid / (ms / 1e3), "passes": passes, "input_sets": len(sets),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "traffic": None, "algorithmic_bytes_per_pass": nbytes,
+                         "duration": "average per call, back to back (workspace memset + kernel)",
                          "peak_kind": f"hbm_gbs ({peaks['source']})"},
-            "l2": f"{flush_mb} MB memset before each pass (outside the events)"}
+            "l2": f"{len(sets)} rotating input sets of {sum(a.nbytes for a in arrays if a is not None) >> 20} MB "
+                  "(more than 2x L2 per round)"}
 
 
-def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb: int = 4096):
+def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb: int = 4096, packed: bool = True):
     """Rollout correction (IS / RS weights over sequences, veto, batch normalisation,
-    mismatch metrics) on the elementwise workload: the 879 padded rows are the sequences,
-    lp_old the trainer's log-probs, lp_samp the rollout engine's.  Knobs: sequence-level
+    mismatch metrics) on the elementwise workload: lp_old is the trainer's log-probs,
+    lp_samp the rollout engine's; packed (the default): the 879 sequences end to end
+    (cumulative lengths, every mask byte 1), else the padded rows.  Knobs: sequence-level
     TIS clipped to [0.1, 10] with batch normalisation, geometric RS in [0.9, 1.1], veto
     1e-4.  Timed as elementwise_side.  Algorithmic bytes per slot: two fp32 inputs and the
     mask read, the fp32 weight and the keep byte written (14 B), plus the weight read and
@@ -232,45 +268,158 @@ def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb:
     import workloads
     c = workloads.make_policy_case()
     B = len(c.seq_lens)
-    off = torch.arange(B + 1, dtype=torch.int64, device=dev) * c.max_len
-    ins = [torch.from_numpy(x).to(dev) for x in (c.lp_old, c.lp_samp, c.mask)]
-    T = int(ins[0].numel())
+    if packed:
+        p = c.packed()
+        arrays = [p["lp_old"], p["lp_samp"], np.ones(len(p["lp_old"]), np.uint8)]
+        off_h = p["cu_seqlens"]
+    else:
+        arrays = [c.lp_old, c.lp_samp, c.mask]
+        off_h = np.arange(B + 1, dtype=np.int64) * c.max_len
+    off = torch.from_numpy(off_h).to(dev)
+    T = int(arrays[0].shape[0])
     rp = rh.RcParams(tis_mode="clip", tis_level="sequence", tis_lower_bound=0.1, tis_upper_bound=10.0,
                      tis_batch_normalize=True, use_rs=True, rs_level="geometric", rs_lower_bound=0.9,
                      rs_upper_bound=1.1, rs_veto_threshold=1e-4)
+    sets = _rotating_sets(torch, dev, arrays, 2 * 129 * 2 ** 20 + 1)
     outs = (torch.empty(T, dtype=torch.float32, device=dev), torch.empty(T, dtype=torch.uint8, device=dev))
     met = torch.zeros(rh.ctypes.sizeof(rh.RlRcMetrics), dtype=torch.uint8, device=dev)
     ws = torch.empty(rh.rl_rollout_correction_workspace_bytes(B), dtype=torch.uint8, device=dev)
-    run = lambda: rh.rl_rollout_correction(*ins, off, rp, outputs=outs, ws=ws, metrics_dev=met)
-    big = torch.empty(flush_mb << 20, dtype=torch.uint8, device=dev)
-    for _ in range(warmup):
-        run()
+    calls = [(lambda ins=ins: rh.rl_rollout_correction(*ins, off, rp, outputs=outs, ws=ws, metrics_dev=met))
+             for ins in sets]
+    for i in range(max(warmup, 3)):
+        calls[i % len(calls)]()
     torch.cuda.synchronize()
-    per, kern = [], []
-    for _ in range(steps):
+    passes = max(steps, 10) * len(calls)
+    ms = _time_back_to_back(torch, calls, passes)
+    big = torch.empty(flush_mb << 20, dtype=torch.uint8, device=dev)
+    kern = []
+    for i in range(max(steps, 10)):
         big.zero_()
         rh.rl_profile_enable(True)
-        run()
+        calls[i % len(calls)]()
         prof = rh.rl_profile_read()
         rh.rl_profile_enable(False)
-        per.append(sum(t for t, _ in prof.values()))
         kern.append(sum(t for k, (t, _) in prof.items() if k == "rollout"))
     del big
-    ms = statistics.median(per)        # the whole call: workspace memset + kernel launches
-    kms = statistics.median(kern)      # the kernel launches alone (the roofline's duration)
+    kms = statistics.median(kern)
     nbytes = T * (4 + 4 + 1) + T * (4 + 1) + T * 8
-    gbs = nbytes / (kms / 1e3) / 1e9
+    gbs = nbytes / (ms / 1e3) / 1e9
     peak = float(peaks["hbm_gbs"])
     n_valid = int(c.mask.sum())
-    return {"workload": f"c5 as {B} sequences (padded rows of {c.max_len}, T={T} slots, {n_valid} response "
-                        "tokens); sequence-level TIS clip [0.1, 10] + batch normalisation, geometric RS "
+    layout = (f"{B} sequences packed end to end (T={T} tokens, mask all 1)" if packed else
+              f"{B} padded rows of {c.max_len} (T={T} slots, {n_valid} response tokens)")
+    return {"workload": f"c5 as {layout}; sequence-level TIS clip [0.1, 10] + batch normalisation, geometric RS "
                         "[0.9, 1.1], veto 1e-4, mismatch metrics",
-            "us_per_pass": ms * 1e3, "kernel_us_per_pass": kms * 1e3, "tokens_per_s": n_valid / (ms / 1e3),
-            "passes": steps,
+            "us_per_call_back_to_back": ms * 1e3, "kernel_us_single_launch": kms * 1e3,
+            "tokens_per_s": n_valid / (ms / 1e3), "passes": passes, "input_sets": len(sets),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "traffic": None, "algorithmic_bytes_per_pass": nbytes,
+                         "duration": "average per call, back to back (workspace memset + kernels)",
                          "peak_kind": f"hbm_gbs ({peaks['source']})"},
-            "l2": f"{flush_mb} MB memset before each pass (outside the events)"}
+            "l2": f"{len(sets)} rotating input sets (more than 2x L2 per round)"}
+
+
+def time_head_config(rh, torch, dev, case, hp, steps: int, warmup: int, peaks: dict, what: str) -> dict:
+    """One side configuration of the head path: the fused forward + backward step timed as
+    the headline (CUDA events around each step, a 256 MB memset between steps), with the
+    memory it holds beyond its inputs (workspace, saved state, outputs, gradients) and its
+    roofline: 6 N H V flop at the burst bf16 peak for a dense backward; for the sparse
+    backward the forward's 2 N H V flop at that peak plus, at the HBM peak, the bytes the
+    step must move (W and X read once, the W rows and X rows each label / support entry
+    gathers, dX and the overwritten dW written)."""
+    N, H, V, nnz = case.N, case.H, case.V, case.nnz
+    batch = rh.HeadBatch.from_case(case)
+    dloss = (case.loss_mask.float() / case.loss_mask.float().sum()).contiguous()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+    ws = torch.empty(rh.rl_head_fwd_bwd_workspace_bytes(N, H, V, nnz, hp), dtype=torch.uint8, device=dev)
+    saved = torch.empty(rh.rl_head_saved_bytes(N, nnz), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    dX = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
+    dW = torch.empty(V, H, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    step = lambda: rh.rl_head_loss_fwd_bwd(batch, hp, dloss, dhidden=dX, dW=dW, ws=ws, saved=saved, status=status)[0]
+    for _ in range(max(warmup, 2)):
+        f = step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"{what}: device status {rh.status_names(int(status.item()))}")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    rh.rl_profile_enable(True)
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        f = step()
+        b.record()
+    torch.cuda.synchronize()
+    prof = rh.rl_profile_read()
+    rh.rl_profile_enable(False)
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    held = (torch.cuda.max_memory_allocated(dev) - base - flush.numel()) / 2 ** 30
+    m = f.metrics()
+    burst = float(peaks["bf16_tflops"])
+    hbm = float(peaks["hbm_gbs"])
+    out = {"workload": what, "N": N, "nnz": nnz, "ms_per_step": ms, "tokens_per_s": N / (ms / 1e3),
+           "token_chunk": hp.token_chunk or min(8192, (N + 127) // 128 * 128),
+           "grad_precision": "split" if hp.grad_precision == rh.RL_GRAD_SPLIT else "bf16",
+           "held_gib": held, "recomputed_chunks": int(m["recomputed_chunks"]),
+           "kernels_ms_per_step": {k: t / steps for k, (t, n) in sorted(prof.items(), key=lambda kv: -kv[1][0])}}
+    sparse = hp.bwd_mode == rh.RL_BWD_SPARSE or (hp.bwd_mode == rh.RL_BWD_AUTO and hp.all_replayed)
+    if sparse:
+        flop = 2.0 * N * H * V
+        nbytes = V * H * 2 + N * H * 2 + 2 * (nnz + N) * H * 2 + V * H * 4 + N * H * 2
+        t_roof = flop / (burst * 1e12) + nbytes / (hbm * 1e9)
+        out["roofline"] = {"bound": "tensor+hbm", "algorithmic_flops": flop, "algorithmic_bytes": nbytes,
+                           "roofline_ms": t_roof * 1e3, "frac": t_roof * 1e3 / ms,
+                           "peak": f"bf16_tflops {burst} + hbm_gbs {hbm} ({peaks['source']})"}
+        for k, kb in (("sparse_dx", (nnz + N) * H * 2 + N * H * 2), ("sparse_dw", (nnz + N) * H * 2 + V * H * 4)):
+            if k in prof:
+                t, n = prof[k]
+                out.setdefault("hbm_kernels", {})[k] = {"ms_per_step": t / steps, "algorithmic_bytes": kb,
+                                                       "gbs": kb / (t / steps / 1e3) / 1e9,
+                                                       "frac": kb / (t / steps / 1e3) / 1e9 / hbm}
+    else:
+        tf = 6.0 * N * H * V / (ms / 1e3) / 1e12
+        out["roofline"] = {"bound": "tensor", "step_tflops_6NHV": tf, "peak": burst, "frac": tf / burst,
+                           "peak_kind": f"bf16_tflops ({peaks['source']})"}
+        if hp.grad_precision == rh.RL_GRAD_SPLIT:
+            out["roofline"]["tensor_work_tflops_10NHV"] = 10.0 * N * H * V / (ms / 1e3) / 1e12
+    del ws, saved, dX, dW, flush
+    torch.cuda.empty_cache()
+    return out
+
+
+def side_configs(rh, torch, dev, case4, steps: int, warmup: int, peaks: dict) -> dict:
+    """The other configurations of the head path, each timed as the headline: c4 with the
+    hi/lo (SPLIT) gradient operand, c4 at token chunks 4096 / 8192 / 16384 / 32768 (time
+    against memory), c2 (4096 tokens, replayed top-p 0.97, icepop, dense), c3 (16384 tokens,
+    replayed top-p 0.97, ipo) with the sparse CSR backward and with the dense one."""
+    import dataclasses
+    import workloads
+    steps = max(3, min(steps, 8))
+    base = head_params(rh, "bf16")
+    out = {"c4_split": time_head_config(rh, torch, dev, case4, dataclasses.replace(base, grad_precision=rh.RL_GRAD_SPLIT),
+                                        steps, warmup, peaks, "c4, grad_precision SPLIT (bf16 hi + lo operand)")}
+    out["c4_chunks"] = [time_head_config(rh, torch, dev, case4, dataclasses.replace(base, token_chunk=c), steps, warmup,
+                                         peaks, f"c4, token_chunk {c}") for c in (4096, 8192, 16384, 32768)]
+    c2 = workloads.make_head_case("c2", device=dev, variant="pages")
+    hp2 = rh.HeadParams(loss_type=rh.RL_LOSS_ICEPOP, icepop_low=0.5, icepop_high=2.0, bwd_mode=rh.RL_BWD_DENSE)
+    out["c2"] = time_head_config(rh, torch, dev, c2, hp2, steps, warmup, peaks,
+                                 "c2: N=4096 (16 x 256), replayed top-p 0.97 (pages-shaped kept counts), icepop "
+                                 "[0.5, 2], dense backward")
+    del c2
+    c3 = workloads.make_head_case("c3", device=dev, variant="pages")
+    hp3 = rh.HeadParams(loss_type=rh.RL_LOSS_IPO, eps=0.3, max_importance_ratio=10.0, all_replayed=1)
+    what3 = "c3: N=16384 (64 x 256), replayed top-p 0.97 (pages-shaped kept counts), ipo 0.3 cap 10"
+    out["c3_sparse"] = time_head_config(rh, torch, dev, c3, hp3, steps, warmup, peaks, what3 + ", sparse CSR backward")
+    out["c3_dense"] = time_head_config(rh, torch, dev, c3, dataclasses.replace(hp3, all_replayed=0,
+                                                                                bwd_mode=rh.RL_BWD_DENSE),
+                                       steps, warmup, peaks, what3 + ", dense backward")
+    del c3
+    torch.cuda.empty_cache()
+    return out
 
 
 def host_inputs(case):
@@ -321,8 +470,9 @@ def run_elementwise_only(args):
     build.build()
     rh.load()
     ew = elementwise_side(rh, torch, dev, args.steps, args.warmup, load_peaks(), args.flush_mb)
+    ewp = elementwise_side(rh, torch, dev, args.steps, args.warmup, load_peaks(), args.flush_mb, packed=False)
     rc = rollout_side(rh, torch, dev, args.steps, args.warmup, load_peaks(), args.flush_mb)
-    print(json.dumps({"elementwise": ew, "rollout_correction": rc,
+    print(json.dumps({"elementwise": ew, "elementwise_padded": ewp, "rollout_correction": rc,
                       "gpu_launches_total": int(rh.rl_kernel_launch_count())}), flush=True)
     return 0
 
@@ -456,10 +606,18 @@ def run_ours(args):
     e_ms, _, e_value = aggregate(e_ms, N, world)
 
     # ---- roofline of the dominant kernel (live CUDA-event times from the timed region) ----
-    chunk = min(16384, (N + 127) // 128 * 128)
-    flops_per_launch = {"gemm_fwd_stats": 2.0 * chunk * H * V}     # fused path: one launch per chunk
-    for k in ("gemm_bwd_grad", "gemm_bwd_dx", "gemm_bwd_dw"):
-        flops_per_launch[k] = 2.0 * chunk * H * V * (2 if (args.grad_precision == "split" and k != "gemm_bwd_grad") else 1)
+    # per step the forward GEMM does 2 N H V flop, dX and dW 2 N H V each (twice that with the
+    # hi/lo operand), spread over one launch per token chunk
+    per_step = {"gemm_fwd_stats": 2.0 * N * H * V}
+    for k in ("gemm_bwd_dx", "gemm_bwd_dw"):
+        per_step[k] = 2.0 * N * H * V * (2 if args.grad_precision == "split" else 1)
+    flops_per_launch = {k: v / (prof[k][1] / args.steps) for k, v in per_step.items() if k in prof}
+    # the logit-recompute GEMM is gated on the device: it does its 2 chunk H V flop only for
+    # the chunks whose range flag was raised (the metrics' recomputed_chunks), else exits
+    recomputed = int(f.metrics()["recomputed_chunks"])
+    if recomputed and "gemm_bwd_grad" in prof:
+        n_chunks = prof["gemm_fwd_stats"][1] / args.steps
+        flops_per_launch["gemm_bwd_grad"] = 2.0 * N * H * V / n_chunks * recomputed / (prof["gemm_bwd_grad"][1] / args.steps)
     dom = max(prof.items(), key=lambda kv: kv[1][0])
     dom_name, (dom_ms, dom_n) = dom
     peak_sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
@@ -469,6 +627,7 @@ def run_ours(args):
         ach = flops_per_launch[dom_name] / ((dom_ms / dom_n) / 1e3) / 1e12
         roof = {"kernel": dom_name, "bound": "tensor", "achieved": ach, "peak": peak_sus, "unit": "TFLOP/s",
                 "frac": ach / peak_sus, "traffic": TRAFFIC.get(dom_name),
+                "traffic_source": TRAFFIC_SOURCE if dom_name in TRAFFIC else None,
                 "peak_kind": f"bf16_tflops_sustained ({peaks['source']})",
                 "frac_of_burst": ach / peak_burst,
                 "algorithmic_flops_per_launch": flops_per_launch[dom_name]}
@@ -495,9 +654,16 @@ def run_ours(args):
             "roofline": roof, "kernels": kernels,
             "e2e": {"value": e_value, "unit": "tokens/s", "ms_per_step": e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "clocks": clocks, "gpu_launches": int(launches), "input_gen_s": t_gen}
+            "clocks": clocks, "gpu_launches": int(launches), "input_gen_s": t_gen,
+            "recomputed_chunks_per_step": recomputed}
+    if not args.no_side_configs:
+        del ws_fb
+        torch.cuda.empty_cache()
+        line["configs"] = side_configs(rh, torch, dev, case, args.steps, args.warmup, peaks)
     if not args.no_elementwise:
         line["elementwise"] = elementwise_side(rh, torch, dev, max(args.steps, 10), args.warmup, peaks)
+        line["elementwise_padded"] = elementwise_side(rh, torch, dev, max(args.steps, 10), args.warmup, peaks,
+                                                      packed=False)
         line["rollout_correction"] = rollout_side(rh, torch, dev, max(args.steps, 10), args.warmup, peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = host_inputs(case_first(case, args.cpu_tokens))
@@ -510,8 +676,10 @@ def run_ours(args):
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of each kernel, from the ncu
-# captures summarised under profiles/ (one launch at the bench's 16384-token chunk).
-TRAFFIC = {"gemm_fwd_stats": 12292000000 + 9935062272}
+# capture of the kernel as it stands, summarised under profiles/ (one launch at the
+# library's default 8192-token chunk); empty until that capture exists.
+TRAFFIC = {}
+TRAFFIC_SOURCE = None
 
 
 def ctypes_metrics_size(rh):
@@ -549,6 +717,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true", help="skip the two-call side figure")
     ap.add_argument("--no-elementwise", action="store_true", help="skip the elementwise-path side figure")
+    ap.add_argument("--no-side-configs", action="store_true",
+                    help="skip the c2 / c3 / c4-SPLIT / token-chunk side configurations")
     ap.add_argument("--elementwise-only", action="store_true",
                     help="time only the elementwise path (profiling runs); prints its side figure")
     ap.add_argument("--flush-mb", type=int, default=4096, help="memset before each elementwise pass, MB")

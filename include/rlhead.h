@@ -97,7 +97,9 @@ typedef struct rl_params {
     float adv_tau;                /* advantage scale */
     float temperature;            /* T > 0; logits are (W h) / T */
     float kl_coeff;               /* >= 0; default 0 */
-    int32_t token_chunk;          /* backward token chunk (multiple of 128); 0 = library default */
+    int32_t token_chunk;          /* backward token chunk (multiple of 128); 0 = library default
+                                     (8192): memory held grows with it (about chunk x V x 4 bytes
+                                     for the bf16 softmax numerators of the fused call) */
     float entropy_coeff;          /* >= 0; default 0.  "10-KL-clip-entropy", section 3: the
                                      exploration regulariser, loss_t -= entropy_coeff * H_t with
                                      H_t the full-vocabulary token entropy; its gradient is dense
@@ -242,13 +244,19 @@ typedef struct rl_pg_metrics {
                                     out (the outputs and metrics are then incomplete) */
 } rl_pg_metrics;
 
-/* Workspace bytes for T tokens: 256 bytes (counters and the metric accumulators), for any
- * T.  The argument stays so that callers need not change if a later layout depends on T. */
+/* Workspace bytes for T tokens: 65,792 (an arrival counter and one 128-byte partial record
+ * per block of the pass), for any T and device.  The argument stays so that callers need
+ * not change if a later layout depends on T.  Zero the workspace once before its first
+ * use (a cudaMemset when it is allocated): every call is one kernel launch whose last
+ * block leaves the arrival counter at zero again, so later calls need no clearing.  Calls
+ * that overlap on the GPU must not share a workspace. */
 size_t rl_policy_workspace_bytes(int64_t T);
 /* All arrays device [T] fp32 (mask uint8, 1 = valid response token; any nonzero byte
  * counts as valid).  A masked slot's inputs are never used, whatever they hold (NaN and
- * inf included).  Output arrays may be NULL to skip; masked tokens get 0.  metrics:
- * device, overwritten; NULL to skip. */
+ * inf included).  mask == NULL: packed input, every one of the T slots is a valid token
+ * (the response tokens of a batch laid end to end, as for the sequences' cumulative
+ * lengths; nothing is read for the mask).  Output arrays may be NULL to skip; masked
+ * tokens get 0.  metrics: device, overwritten; NULL to skip. */
 int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const float* lp_samp,
                                const float* adv, const uint8_t* mask, int64_t T,
                                const rl_pg_params* params, float* loss_ppo, float* loss_dec,
@@ -261,18 +269,17 @@ int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const
  * trainer or inference engine whose device memory is reserved up front by its own pool,
  * where an extra cudaMalloc would fail or compete with that pool, or plain C code with
  * no device allocator at hand.  This variant takes no workspace and allocates nothing:
- * its scratch (counters and the metric accumulators) is a file-scope device array of 4096
- * bytes.
+ * its scratch (the arrival counter and the blocks' partial records) is a file-scope
+ * device array of 65,792 bytes, the size rl_policy_workspace_bytes returns.
  *   - Every GPU that loads the library holds that array until the process exits.
  *   - The first call on a device looks the array's device address up (once per
  *     device); make that first call before any stream capture.
- *   - All calls share the one array and it keeps the last call's contents.  Its header
- *     (the arrival counter, the status word, the range flag and the accumulators, which
- *     the kernel's blocks add into with atomics) must start at zero, so each call first
- *     zeroes those 256 bytes with a memset on its own stream, then launches the kernel.
- *     That ordering is why calls one after another on one stream are safe, and why
- *     calls that overlap on the GPU (other streams, other threads) race on the array:
- *     serialise them.
+ *   - All calls share the one array and it keeps the last call's contents.  The array
+ *     starts at zero when the library is loaded; every block of a call writes its own
+ *     record before the last block reads it, and that last block sets the arrival counter
+ *     back to zero, so each call leaves the array ready for the next.  Calls one after
+ *     another on one stream are therefore safe; calls that overlap on the GPU (other
+ *     streams, other threads) race on the array: serialise them.
  * Arguments, outputs and errors as rl_policy_loss_elementwise, without ws / ws_bytes. */
 int rl_policy_loss_elementwise_noalloc(const float* lp_theta, const float* lp_old,
                                        const float* lp_samp, const float* adv,

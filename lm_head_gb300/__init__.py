@@ -479,6 +479,7 @@ def rl_policy_loss_elementwise(lp_theta, lp_old, lp_samp, adv, mask, params: PgP
                                ws: Optional[torch.Tensor] = None, metrics_dev: Optional[torch.Tensor] = None,
                                stream=None):
     """Returns (loss_ppo, loss_dec, grad_ppo, grad_dec, metrics_dev); metrics via pg_metrics()."""
+    """mask None: packed input, every slot a valid token."""
     lib = load()
     _require_cuda(lp_theta, lp_old, lp_samp, adv, mask)
     T = int(lp_theta.numel())
@@ -487,8 +488,8 @@ def rl_policy_loss_elementwise(lp_theta, lp_old, lp_samp, adv, mask, params: PgP
         outputs = tuple(torch.empty(T, dtype=torch.float32, device=dev) for _ in range(4))
     if metrics_dev is None:
         metrics_dev = torch.zeros(ctypes.sizeof(RlPgMetrics), dtype=torch.uint8, device=dev)
-    if ws is None:
-        ws = _u8(rl_policy_workspace_bytes(T), dev)
+    if ws is None:   # zeroed once before its first use (include/rlhead.h)
+        ws = torch.zeros(rl_policy_workspace_bytes(T), dtype=torch.uint8, device=dev)
     p = params.c()
     _check(lib.rl_policy_loss_elementwise(_ptr(lp_theta), _ptr(lp_old), _ptr(lp_samp), _ptr(adv), _ptr(mask), T,
                                           ctypes.byref(p), *[_ptr(o) for o in outputs], _ptr(metrics_dev),

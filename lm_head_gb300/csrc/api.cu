@@ -180,7 +180,7 @@ int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const
     if (!(params->clip_ratio_low >= 0.f) || !(params->clip_ratio_high >= 0.f) || !(params->clip_ratio_c > 1.f) ||
         !(params->tis_upper > 0.f) || !(params->icepop_low <= params->icepop_high))
         return fail(RL_ERR_ARG, "bad pg params");
-    if (T > 0 && (!lp_theta || !lp_old || !lp_samp || !adv || !mask)) return fail(RL_ERR_ARG, "input NULL");
+    if (T > 0 && (!lp_theta || !lp_old || !lp_samp || !adv)) return fail(RL_ERR_ARG, "input NULL");
     if (ws_bytes < rl_policy_workspace_bytes(T) || !ws) return fail(RL_ERR_WORKSPACE, "policy workspace too small");
     if (T == 0 && !metrics) return RL_OK;
     if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");

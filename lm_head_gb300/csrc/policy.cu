@@ -25,11 +25,13 @@
 //                          exactly by the thread that met it.
 //  2. policy_slow_kernel   the whole pass with exact decisions in the bands, for inputs the
 //                          fast pass does not take (unaligned, T >= 2^31).
-//  Each block adds its partial (fp32 sums in a fixed order within the block, then in 2^-24
-//  fixed point; counts) to the batch accumulators with integer atomics, whose total does
-//  not depend on the order of arrival; the last block to arrive (an arrival counter)
-//  writes the metrics.  If a block's sum was too large for the fixed point, that block
-//  redoes the whole batch's metrics with exact decisions instead (slow, correct).
+//  With no mask (packed input: every slot a valid token) the mask is neither read nor
+//  copied: 16 bytes in per token instead of 17.
+//  Each block writes its partial (fp32 sums in a fixed order within the block, counts, the
+//  status bits of its waits) to its own record in the workspace; the last block to arrive
+//  (an arrival counter) sums the records in block order (fp64 sums, int64 counts), writes
+//  the metrics and sets the counter back to zero.  So a workspace zeroed once before its
+//  first use needs no clearing before later calls, and a call is one kernel launch.
 //
 // Results are bitwise reproducible for a given device and T.
 #include <atomic>
@@ -51,7 +53,6 @@ constexpr int kPgFastPerSm = 2;   // resident blocks per SM of the fast pass
 constexpr int kPgStageSlots = 2 * kPgThreads;   // token slots per stage of the fast pass
 constexpr int kPgDepth = 6;       // stages in its ring
 constexpr int kPgSlowPerSm = 2;
-constexpr float kPgFix = 16777216.f;   // 2^24: fixed-point scale of the metric sums
 
 // ----------------------------------------------------------------------------------
 // Parameters
@@ -82,15 +83,23 @@ struct PgArgs {
     float* loss_dec;
     float* grad_ppo;
     float* grad_dec;
-    long long* acc;               // [kPgFields] the batch's sums (2^-24 fixed point) and counts
-    int* range;                   // set when a sum term is too large for the fixed point
-    float range_lim;              // |term| bound that keeps every accumulator inside int64
+    struct PgSlot* slots;         // [nb] one partial record per block
+    unsigned int* arrive;         // blocks of this launch that have written their record (0 between calls)
     int nb;                       // blocks of the pass
-    int* done;                    // blocks that have written their partial
-    int32_t* status;              // RL_STATUS_* bits of this call
     uint64_t wait_ns;             // limit of the streaming loop's waits (RL_OPT_WAIT_LIMIT_US)
     rl_pg_metrics* metrics;       // or nullptr
 };
+
+// A block's partial: fp32 sums in the block's fixed order, counts (the curve in the
+// caller's order), the RL_STATUS_* bits its waits raised.  128 bytes.
+struct alignas(16) PgSlot {
+    float sum[kPgSums];
+    int cnt[6];
+    int curve[RL_PG_MAX_CURVE];
+    int status;
+    int pad[3];
+};
+static_assert(sizeof(PgSlot) == 128, "one record per 128 bytes");
 
 struct PgAcc {
     float sum[kPgSums];
@@ -217,7 +226,7 @@ RL_DEVINL void pg_token(float lt, float lo, float ls, float A, bool valid, const
 RL_DEVINL void pg_exact_pass(const PgArgs& a, int64_t tid, int64_t nthreads, PgAcc& acc) {
     for (int64_t i = tid; i < a.T; i += nthreads) {
         float lp, ld, gp, gd;
-        pg_token(a.lt[i], a.lo[i], a.ls[i], a.adv[i], a.mask[i] != 0, a.q, lp, ld, gp, gd, acc);
+        pg_token(a.lt[i], a.lo[i], a.ls[i], a.adv[i], a.mask == nullptr || a.mask[i] != 0, a.q, lp, ld, gp, gd, acc);
         if (a.loss_ppo) a.loss_ppo[i] = lp;
         if (a.loss_dec) a.loss_dec[i] = ld;
         if (a.grad_ppo) a.grad_ppo[i] = gp;
@@ -277,60 +286,79 @@ RL_DEVINL void pg_write_metric(int k, double s, rl_pg_metrics* out) {
     }
 }
 
-// A sum term in 2^-24 fixed point, or 0 with the range flag raised when |v| is at or past
-// the bound that keeps the batch's accumulators inside int64 (or v is not finite).
-RL_DEVINL long long pg_fix(const PgArgs& a, float v) {
-    if (fabsf(v) < a.range_lim) return __float2ll_rn(v * kPgFix);
-    atomicOr(a.range, 1);
-    return 0;
-}
-
 // ----------------------------------------------------------------------------------
 // Batch totals
 // ----------------------------------------------------------------------------------
-// A block's partial goes into the batch accumulators with integer atomics (sums in 2^-24
-// fixed point, counts as they are): integer addition does not depend on the order the
-// blocks arrive in, so the totals are reproducible.  A sum too large for the fixed point
-// raises the range flag instead, and the last block then redoes the metrics (below).
-RL_DEVINL void pg_add_partial(const PgArgs& a, int k, float sum, long long count) {
-    const long long x = k < kPgSums ? pg_fix(a, sum) + count : count;
-    if (x != 0) atomicAdd(reinterpret_cast<unsigned long long*>(a.acc + k), static_cast<unsigned long long>(x));
-}
-
-// The last block of the pass to finish: the accumulators into the metrics.  If a sum
-// term was too large for the fixed point, the whole batch again with exact decisions and
-// fp32 sums instead (one block: slow, correct).  Called by every thread of the last block.
+// The last block: every record summed in block order (each thread its blocks t, t + nt,
+// ..., then a fixed butterfly within warps and the warps in order), into the metrics.  The
+// sums are carried as float-float pairs (about 44 significant bits; fp64 is a slow pipe on
+// this part), the counts as integers.
 RL_DEVINL void pg_final(const PgArgs& a) {
-    if (__ldcg(a.range) != 0) {
-        PgAcc acc;
-        pg_zero(acc);
-        pg_exact_pass(a, threadIdx.x, blockDim.x, acc);
-        __shared__ float sums[kPgSums];
-        __shared__ int cnts[kPgCounts];
-        pg_block_reduce(acc, sums, cnts);
-        if (a.metrics && threadIdx.x < kPgFields) {
-            const int k = threadIdx.x;
-            pg_write_metric(k, k < kPgSums ? static_cast<double>(sums[k]) : static_cast<double>(cnts[k - kPgSums]),
-                            a.metrics);
+    constexpr int kC = 6 + RL_PG_MAX_CURVE;
+    FF v[kPgSums];
+    int c[kC];
+    int st = 0;
+#pragma unroll
+    for (int f = 0; f < kPgSums; ++f) v[f] = {0.f, 0.f};
+#pragma unroll
+    for (int f = 0; f < kC; ++f) c[f] = 0;
+    for (int b = threadIdx.x; b < a.nb; b += blockDim.x) {
+        const PgSlot* r = a.slots + b;
+#pragma unroll
+        for (int f = 0; f < kPgSums; ++f) v[f] = ff_add(v[f], {__ldcg(r->sum + f), 0.f});
+#pragma unroll
+        for (int f = 0; f < 6; ++f) c[f] += __ldcg(r->cnt + f);
+#pragma unroll
+        for (int f = 0; f < RL_PG_MAX_CURVE; ++f) c[6 + f] += __ldcg(r->curve + f);
+        st |= __ldcg(&r->status);
+    }
+    __shared__ FF red_s[kPgSums][(kPgThreads + 32) / 32];
+    __shared__ int red_c[kC][(kPgThreads + 32) / 32];
+    __shared__ int red_st[(kPgThreads + 32) / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+#pragma unroll
+    for (int f = 0; f < kPgSums; ++f) {
+        FF x = v[f];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const FF y = {__shfl_xor_sync(0xffffffffu, x.hi, o), __shfl_xor_sync(0xffffffffu, x.lo, o)};
+            x = (lane & o) ? ff_add(y, x) : ff_add(x, y);   // the same operands in the same order on both lanes
         }
-        if (a.metrics && threadIdx.x == 0) a.metrics->status = __ldcg(a.status);
-        return;
+        if (lane == 0) red_s[f][warp] = x;
     }
+#pragma unroll
+    for (int f = 0; f < kC; ++f) {
+        const int x = __reduce_add_sync(0xffffffffu, c[f]);
+        if (lane == 0) red_c[f][warp] = x;
+    }
+    st = __reduce_or_sync(0xffffffffu, st);
+    if (lane == 0) red_st[warp] = st;
+    __syncthreads();
+    if (threadIdx.x == 0) *a.arrive = 0u;   // every block has arrived: ready for the next call
     if (!a.metrics) return;
-    const int k = threadIdx.x;
-    if (k < kPgFields) {
-        const long long v = static_cast<long long>(__ldcg(reinterpret_cast<const unsigned long long*>(a.acc + k)));
-        pg_write_metric(k, k < kPgSums ? static_cast<double>(v) * (1.0 / kPgFix) : static_cast<double>(v), a.metrics);
+    const int f = threadIdx.x;
+    if (f < kPgSums) {
+        FF x = red_s[f][0];
+        for (int w = 1; w < nw; ++w) x = ff_add(x, red_s[f][w]);
+        pg_write_metric(f, static_cast<double>(x.hi) + static_cast<double>(x.lo), a.metrics);
+    } else if (f < kPgSums + kC) {
+        int x = 0;
+        for (int w = 0; w < nw; ++w) x += red_c[f - kPgSums][w];
+        pg_write_metric(f, static_cast<double>(x), a.metrics);
+    } else if (f == kPgSums + kC) {
+        int s2 = 0;
+        for (int w = 0; w < nw; ++w) s2 |= red_st[w];
+        a.metrics->status = s2;
     }
-    if (k == 0) a.metrics->status = __ldcg(a.status);
 }
 
-// Every block calls this after adding its partial; the last one to arrive finishes.
+// Every thread of every block calls this after the block's record is written; the last
+// block to arrive finishes.
 RL_DEVINL void pg_finish(const PgArgs& a) {
     __shared__ int last;
-    __threadfence();   // this thread's outputs and atomics before the arrival count
+    __threadfence();   // this block's record (and outputs) before its arrival
     __syncthreads();
-    if (threadIdx.x == 0) last = atomicAdd(a.done, 1) == a.nb - 1;
+    if (threadIdx.x == 0) last = atomicAdd(a.arrive, 1u) == static_cast<unsigned int>(a.nb - 1);
     __syncthreads();
     if (!last) return;
     __threadfence();
@@ -348,11 +376,16 @@ __global__ void __launch_bounds__(kPgThreads, kPgSlowPerSm) policy_slow_kernel(P
     __shared__ float sums[kPgSums];
     __shared__ int cnts[kPgCounts];
     pg_block_reduce(acc, sums, cnts);
+    PgSlot* rec = a.slots + blockIdx.x;
     const int k = threadIdx.x;
     if (k < kPgSums)
-        pg_add_partial(a, k, sums[k], 0);
+        rec->sum[k] = sums[k];
+    else if (k < kPgSums + 6)
+        rec->cnt[k - kPgSums] = cnts[k - kPgSums];
     else if (k < kPgFields)
-        pg_add_partial(a, k, 0.f, cnts[k - kPgSums]);
+        rec->curve[k - kPgSums - 6] = cnts[k - kPgSums];
+    else if (k == kPgFields)
+        rec->status = 0;
     pg_finish(a);
 }
 
@@ -480,6 +513,63 @@ RL_DEVINL void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* b
         : "memory");
 }
 
+// The block's partial into its record: warp trees (fp32 sums, exact int32 counts), then the
+// eight consumer warps in order; the curve counts from the histogram, cnt_k = #(j > k),
+// back in the caller's order.  Called by every thread of a streaming block (288).
+RL_DEVINL void pg_block_record(const PgArgs& a, const PgFastAcc& acc, const int* hist_s, const int32_t* blk_status) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool consumer = threadIdx.x < kPgThreads;
+    __shared__ float shs[kPgThreads / 32][kPgSums];
+    __shared__ int shc[kPgThreads / 32][6];
+    __shared__ int bins[kPgBins];
+    __syncthreads();
+#pragma unroll
+    for (int f = 0; f < kPgSums; ++f) {
+        const float v = warp_sum(acc.sum[f]);
+        if (lane == 0 && consumer) shs[warp][f] = v;
+    }
+#pragma unroll
+    for (int f = 0; f < 6; ++f) {
+        const int v = __reduce_add_sync(0xffffffffu, acc.cnt[f]);
+        if (lane == 0 && consumer) shc[warp][f] = v;
+    }
+    __syncthreads();
+    if (consumer)
+        for (int b = warp; b <= a.q.n; b += kPgThreads / 32) {
+            int v = 0;
+            for (int t = lane; t < kPgThreads; t += 32) v += hist_s[b * kPgThreads + t];
+            v = __reduce_add_sync(0xffffffffu, v);
+            if (lane == 0) bins[b] = v;
+        }
+    __syncthreads();
+    PgSlot* rec = a.slots + blockIdx.x;
+    const int f = threadIdx.x;
+    if (f < kPgSums) {
+        float v = 0.f;
+        for (int w = 0; w < kPgThreads / 32; ++w) v += shs[w][f];
+        rec->sum[f] = v;
+    } else if (f < kPgSums + 6) {
+        int v = 0;
+        for (int w = 0; w < kPgThreads / 32; ++w) v += shc[w][f - kPgSums];
+        rec->cnt[f - kPgSums] = v;
+    } else if (f < kPgFields) {
+        const int c = f - kPgSums - 6;        // caller's curve index
+        int v = 0;
+        if (c < a.q.n) {
+            int js = 0;                        // its sorted position
+            while (a.q.perm[js] != c) ++js;
+            for (int b = js + 1; b <= a.q.n; ++b) v += bins[b];
+        }
+        rec->curve[c] = v;
+    } else if (f == kPgFields) {
+        rec->status = *blk_status;
+    }
+}
+
+// Packed-input variant of pg_fast: the curve bin from the bucket table (pk_curve).
+RL_DEVINL PgTok pg_fast_packed(float lt, float lo, float ls, float A, const PgPrep& q, const int* lut, const float* eps,
+                               const float* weps);
+
 // Stages of kPgStageSlots slots are dealt round-robin to the blocks (block b takes stages
 // b, b + nb, b + 2 nb, ... with nb odd, so a block's stages walk through every phase of a
 // power-of-two padding period and the valid tokens, where the arithmetic is, spread
@@ -502,6 +592,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
     __shared__ __align__(8) uint64_t empty[kPgDepth];
     __shared__ int hist_s[kPgBins * kPgThreads];   // bin-major: thread t's bin b at b * 256 + t
     __shared__ int abort_flag;
+    __shared__ int32_t blk_status;                  // RL_STATUS_* bits of this block's waits
 
     const int64_t n16 = a.T >> 4;
     const int64_t nstages = (n16 * 16 + kPgStageSlots - 1) / kPgStageSlots;
@@ -516,7 +607,10 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
         }
         fence_mbar_init();
     }
-    if (threadIdx.x == 0) abort_flag = 0;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        blk_status = 0;
+    }
     if (consumer)
         for (int b = 0; b <= a.q.n; ++b) hist_s[b * kPgThreads + threadIdx.x] = 0;
     __syncthreads();
@@ -535,7 +629,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
             for (int i = 0; i < nst; ++i) {
                 const int slot = i % kPgDepth;
                 if (i >= kPgDepth &&
-                    !mbar_wait(empty + slot, static_cast<uint32_t>((i / kPgDepth - 1) & 1), a.status, a.wait_ns)) {
+                    !mbar_wait(empty + slot, static_cast<uint32_t>((i / kPgDepth - 1) & 1), &blk_status, a.wait_ns)) {
                     atomicExch(&abort_flag, 1);
                     break;
                 }
@@ -544,12 +638,12 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
                 const int64_t left = n16 * 16 - g;
                 const uint32_t L = static_cast<uint32_t>(left < kPgStageSlots ? left : kPgStageSlots);
                 PgStage& st = ring[slot];
-                mbar_arrive_expect_tx(full + slot, 17u * L);
+                mbar_arrive_expect_tx(full + slot, (a.mask ? 17u : 16u) * L);
                 bulk_load(st.lt, a.lt + g, 4u * L, full + slot);
                 bulk_load(st.lo, a.lo + g, 4u * L, full + slot);
                 bulk_load(st.ls, a.ls + g, 4u * L, full + slot);
                 bulk_load(st.A, a.adv + g, 4u * L, full + slot);
-                bulk_load(st.m, a.mask + g, L, full + slot);
+                if (a.mask) bulk_load(st.m, a.mask + g, L, full + slot);
                 issued = i + 1;
             }
             if (*vflag) {
@@ -557,7 +651,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
                 // (bounded by the fixed kWaitLimitNs, whatever the work loop's limit)
                 // before the block's shared memory goes away
                 for (int i = issued > kPgDepth ? issued - kPgDepth : 0; i < issued; ++i)
-                    mbar_wait(full + i % kPgDepth, static_cast<uint32_t>((i / kPgDepth) & 1), a.status);
+                    mbar_wait(full + i % kPgDepth, static_cast<uint32_t>((i / kPgDepth) & 1), &blk_status);
             }
         }
     } else {
@@ -565,7 +659,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
         const int j = 2 * threadIdx.x;
         for (int i = 0; i < nst; ++i) {
             const int slot = i % kPgDepth;
-            if (!mbar_wait(full + slot, static_cast<uint32_t>((i / kPgDepth) & 1), a.status, a.wait_ns)) {
+            if (!mbar_wait(full + slot, static_cast<uint32_t>((i / kPgDepth) & 1), &blk_status, a.wait_ns)) {
                 atomicExch(&abort_flag, 1);
                 break;
             }
@@ -577,7 +671,8 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
                 const float2 lo = *reinterpret_cast<const float2*>(st.lo + j);
                 const float2 ls = *reinterpret_cast<const float2*>(st.ls + j);
                 const float2 A = *reinterpret_cast<const float2*>(st.A + j);
-                const uint32_t mw = *reinterpret_cast<const uint16_t*>(st.m + j);
+                // packed input (no mask): every slot is a valid token
+                const uint32_t mw = a.mask ? *reinterpret_cast<const uint16_t*>(st.m + j) : 0x0101u;
                 float2 lp = make_float2(0.f, 0.f), ld = lp, gp = lp, gd = lp;
                 if (mw != 0u) {
                     const bool v0 = (mw & 0xffu) != 0u, v1 = (mw & 0xff00u) != 0u;
@@ -601,7 +696,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
             const int64_t t = n16 * 16 + threadIdx.x;
             if (t < a.T) {
                 float lp = 0.f, ld = 0.f, gp = 0.f, gd = 0.f;
-                if (a.mask[t] != 0) {
+                if (a.mask == nullptr || a.mask[t] != 0) {
                     const float xt = a.lt[t], xo = a.lo[t], xs = a.ls[t], xa = a.adv[t];
                     PgTok tk = pg_fast(xt, xo, xs, xa, a.q);
                     if (tk.band) pg_resolve(tk, xt, xo, xs, xa, a.q);
@@ -614,84 +709,274 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
             }
         }
     }
-    __syncthreads();
-    // block partial: warp trees (fp32 sums, exact int32 counts), then the 8 consumer warps
-    // in order, into the batch accumulators; the curve counts from the histogram,
-    // cnt_k = #(j > k), back in the caller's order
-    __shared__ float shs[kPgThreads / 32][kPgSums];
-    __shared__ int shc[kPgThreads / 32][6];
-    __shared__ int bins[kPgBins];
-#pragma unroll
-    for (int f = 0; f < kPgSums; ++f) {
-        const float v = warp_sum(acc.sum[f]);
-        if (lane == 0 && consumer) shs[warp][f] = v;
+    pg_block_record(a, acc, hist_s, &blk_status);
+    pg_finish(a);
+}
+
+// ----------------------------------------------------------------------------------
+// Packed pass (no mask: every slot a valid token)
+// ----------------------------------------------------------------------------------
+// Each block takes one contiguous range of the tokens (an equal share, in groups of four),
+// streamed through a ring of 1024-token stages by a producer warp (four bulk copies per
+// stage); each consumer thread takes four consecutive tokens of a stage (16-byte shared
+// loads, 16-byte streaming stores).  Every token's values enter the sums and counts
+// without a select (there is no padding to keep out); a token inside a band is re-decided
+// exactly first.  The IPO-curve bin comes from a 1024-bucket table of |p_old - p_samp|
+// built in shared memory at block start: a bucket records how many curve eps lie below
+// it, the one eps inside it (compared exactly), or that the token needs the full search
+// (two eps inside, or an eps whose band reaches into the bucket).
+constexpr int kPkStage = 1024;                 // tokens per stage
+constexpr int kPkDepth = 5;                    // stages in the ring
+constexpr int kPkLut = 1024;                   // buckets of |p_old - p_samp| over [0, 1]
+struct alignas(16) PkStage {
+    float lt[kPkStage], lo[kPkStage], ls[kPkStage], A[kPkStage];
+};
+constexpr int kPkSmem = kPkDepth * static_cast<int>(sizeof(PkStage));
+
+// Curve bin and band of one |p_old - p_samp| value from the bucket table.
+RL_DEVINL void pk_curve(float adiff, const int* lut, const float* eps, const float* weps, int n, int& j, bool& band) {
+    int b = static_cast<int>(adiff * static_cast<float>(kPkLut));   // exact scaling: bucket edges are exact
+    b = b < 0 ? 0 : (b > kPkLut - 1 ? kPkLut - 1 : b);
+    const int e = lut[b];
+    j = e & 31;
+    const int kin = (e >> 8) & 31;
+    if (kin) {
+        j += adiff > eps[kin - 1] ? 1 : 0;
+        band = band | (fabsf(adiff - eps[kin - 1]) <= weps[kin - 1]);
     }
-#pragma unroll
-    for (int f = 0; f < 6; ++f) {
-        const int v = __reduce_add_sync(0xffffffffu, acc.cnt[f]);
-        if (lane == 0 && consumer) shc[warp][f] = v;
-    }
-    __syncthreads();
-    if (consumer)
-        for (int b = warp; b <= a.q.n; b += kPgThreads / 32) {
-            int v = 0;
-            for (int t = lane; t < kPgThreads; t += 32) v += hist_s[b * kPgThreads + t];
-            v = __reduce_add_sync(0xffffffffu, v);
-            if (lane == 0) bins[b] = v;
+    if (e >> 16) {   // the full search
+        j = 0;
+        for (int k = 0; k < n; ++k) {
+            j += adiff > eps[k] ? 1 : 0;
+            band = band | (fabsf(adiff - eps[k]) <= weps[k]);
         }
-    __syncthreads();
-    const int f = threadIdx.x;
-    if (f < kPgSums) {
-        float v = 0.f;
-        for (int w = 0; w < kPgThreads / 32; ++w) v += shs[w][f];
-        pg_add_partial(a, f, v, 0);
-    } else if (f < kPgSums + 6) {
-        int v = 0;
-        for (int w = 0; w < kPgThreads / 32; ++w) v += shc[w][f - kPgSums];
-        pg_add_partial(a, f, 0.f, v);
-    } else if (f < kPgFields) {
-        const int c = f - kPgSums - 6;        // caller's curve index
-        int v = 0;
-        if (c < a.q.n) {
-            int js = 0;                        // its sorted position
-            while (a.q.perm[js] != c) ++js;
-            for (int b = js + 1; b <= a.q.n; ++b) v += bins[b];
-        }
-        pg_add_partial(a, f, 0.f, v);
     }
+}
+
+RL_DEVINL PgTok pg_fast_packed(float lt, float lo, float ls, float A, const PgPrep& q, const int* lut, const float* eps,
+                               const float* weps) {
+    PgTok o;
+    const float r = exp_fast(lt - lo);
+    const float l1 = -A * r;
+    const float l2 = -A * fminf(fmaxf(r, q.lo_b), q.hi_b);
+    const float lc = fmaxf(l1, l2);
+    const float l3 = -A * q.cc;
+    const float d = lo - ls;
+    const float rho_raw = exp_fast(d);
+    const float adiff = exp_fast(ls) * fabsf(rho_raw - 1.f);
+    bool band = ((A < 0.f) & ((fabsf(r - q.lo_b) <= q.w_lo_b) | (fabsf(r - q.cc) <= q.w_cc))) |
+                ((A > 0.f) & (fabsf(r - q.hi_b) <= q.w_hi_b)) | (fabsf(rho_raw - q.tis) <= q.w_tis) |
+                (fabsf(rho_raw - q.ice_lo) <= q.w_ice_lo) | (fabsf(rho_raw - q.ice_hi) <= q.w_ice_hi);
+    int j;
+    pk_curve(adiff, lut, eps, weps, q.n, j, band);
+    const bool dual = (A < 0.f) & (r > q.cc);   // on the ratio, as in pg_token
+    const bool clip = ((A > 0.f) & (r > q.hi_b)) | ((A < 0.f) & (r < q.lo_b));
+    const float loss_ppo = dual ? l3 : lc;
+    const float g_c = clip ? 0.f : -A * r;
+    const float rho = fminf(rho_raw, q.tis);
+    o.lp = loss_ppo;
+    o.ld = rho * lc;
+    o.gp = dual ? 0.f : g_c;
+    o.gd = rho * g_c;
+    o.s[0] = loss_ppo;
+    o.s[1] = rho * lc;
+    o.s[2] = lo - lt;
+    o.s[3] = ls - lo;
+    o.s[4] = rho_raw - d - 1.f;
+    o.s[5] = rho;
+    o.clip = clip;
+    o.dual = dual;
+    o.ice_lo = rho_raw < q.ice_lo;
+    o.ice_hi = rho_raw > q.ice_hi;
+    o.tis = rho_raw > q.tis;
+    o.j = j;
+    o.band = band;
+    return o;
+}
+
+__global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_kernel(PgArgs a) {
+    extern __shared__ __align__(128) uint8_t pk_smem[];
+    PkStage* ring = reinterpret_cast<PkStage*>(pk_smem);
+    __shared__ __align__(8) uint64_t full[kPkDepth];
+    __shared__ __align__(8) uint64_t empty[kPkDepth];
+    __shared__ int hist_s[kPgBins * kPgThreads];   // bin-major: thread t's bin b at b * 256 + t
+    __shared__ int lut[kPkLut];
+    __shared__ float s_eps[RL_PG_MAX_CURVE], s_weps[RL_PG_MAX_CURVE];
+    __shared__ int abort_flag;
+    __shared__ int32_t blk_status;
+
+    const PgPrep& q = a.q;
+    const int64_t n4 = a.T >> 2;                   // groups of four tokens
+    const int64_t g0 = static_cast<int64_t>(blockIdx.x) * n4 / a.nb;
+    const int64_t g1 = static_cast<int64_t>(blockIdx.x + 1) * n4 / a.nb;
+    const int64_t t0 = 4 * g0, ntok = 4 * (g1 - g0);
+    const int nst = static_cast<int>((ntok + kPkStage - 1) / kPkStage);
+    const bool consumer = threadIdx.x < kPgThreads;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x == kPgThreads) {
+        for (int s = 0; s < kPkDepth; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, kPgThreads / 32);
+        }
+        fence_mbar_init();
+    }
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        blk_status = 0;
+    }
+    if (consumer) {
+        for (int b = 0; b <= q.n; ++b) hist_s[b * kPgThreads + threadIdx.x] = 0;
+        if (threadIdx.x < q.n) {
+            s_eps[threadIdx.x] = q.eps[threadIdx.x];
+            s_weps[threadIdx.x] = q.weps[threadIdx.x];
+        }
+        for (int i = threadIdx.x; i < kPkLut; i += kPgThreads) {   // the bucket table
+            const float blo = static_cast<float>(i) / static_cast<float>(kPkLut);
+            const float bhi = static_cast<float>(i + 1) / static_cast<float>(kPkLut);
+            int below = 0, inside = 0, kin = 0, slow = 0;
+            for (int k = 0; k < q.n; ++k) {
+                const float e = q.eps[k];
+                if (e < blo) {
+                    ++below;
+                    slow |= (blo - e <= q.weps[k]);
+                } else if (e < bhi || i == kPkLut - 1) {
+                    ++inside;
+                    kin = k + 1;
+                } else {
+                    slow |= (e - bhi <= q.weps[k]);
+                }
+            }
+            slow |= inside > 1;
+            lut[i] = below | (kin << 8) | (slow << 16);
+        }
+    }
+    __syncthreads();
+
+    PgFastAcc acc;
+#pragma unroll
+    for (int k = 0; k < kPgSums; ++k) acc.sum[k] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 6; ++k) acc.cnt[k] = 0;
+    volatile int* vflag = &abort_flag;
+
+    if (!consumer) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < nst; ++i) {
+                const int slot = i % kPkDepth;
+                if (i >= kPkDepth &&
+                    !mbar_wait(empty + slot, static_cast<uint32_t>((i / kPkDepth - 1) & 1), &blk_status, a.wait_ns)) {
+                    atomicExch(&abort_flag, 1);
+                    break;
+                }
+                if (*vflag) break;
+                const int64_t g = t0 + static_cast<int64_t>(i) * kPkStage;
+                const int64_t left = t0 + ntok - g;
+                const uint32_t L = static_cast<uint32_t>(left < kPkStage ? left : kPkStage);
+                PkStage& st = ring[slot];
+                mbar_arrive_expect_tx(full + slot, 16u * L);
+                bulk_load(st.lt, a.lt + g, 4u * L, full + slot);
+                bulk_load(st.lo, a.lo + g, 4u * L, full + slot);
+                bulk_load(st.ls, a.ls + g, 4u * L, full + slot);
+                bulk_load(st.A, a.adv + g, 4u * L, full + slot);
+                issued = i + 1;
+            }
+            if (*vflag) {
+                // the last stages issued may still be in flight: wait for them (bounded by
+                // the fixed kWaitLimitNs) before the block's shared memory goes away
+                for (int i = issued > kPkDepth ? issued - kPkDepth : 0; i < issued; ++i)
+                    mbar_wait(full + i % kPkDepth, static_cast<uint32_t>((i / kPkDepth) & 1), &blk_status);
+            }
+        }
+    } else {
+        int* hist = hist_s + threadIdx.x;
+        const int j4 = 4 * threadIdx.x;
+        for (int i = 0; i < nst; ++i) {
+            const int slot = i % kPkDepth;
+            if (!mbar_wait(full + slot, static_cast<uint32_t>((i / kPkDepth) & 1), &blk_status, a.wait_ns)) {
+                atomicExch(&abort_flag, 1);
+                break;
+            }
+            if (*vflag) break;
+            const int64_t g = t0 + static_cast<int64_t>(i) * kPkStage;
+            if (g + j4 < t0 + ntok) {
+                const PkStage& st = ring[slot];
+                const float4 lt4 = *reinterpret_cast<const float4*>(st.lt + j4);
+                const float4 lo4 = *reinterpret_cast<const float4*>(st.lo + j4);
+                const float4 ls4 = *reinterpret_cast<const float4*>(st.ls + j4);
+                const float4 A4 = *reinterpret_cast<const float4*>(st.A + j4);
+                const float vt[4] = {lt4.x, lt4.y, lt4.z, lt4.w}, vo[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
+                const float vs[4] = {ls4.x, ls4.y, ls4.z, ls4.w}, vA[4] = {A4.x, A4.y, A4.z, A4.w};
+                float lp[4], ld[4], gp[4], gd[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    PgTok t = pg_fast_packed(vt[u], vo[u], vs[u], vA[u], q, lut, s_eps, s_weps);
+                    if (t.band) pg_resolve(t, vt[u], vo[u], vs[u], vA[u], q);
+                    lp[u] = t.lp;
+                    ld[u] = t.ld;
+                    gp[u] = t.gp;
+                    gd[u] = t.gd;
+#pragma unroll
+                    for (int k = 0; k < kPgSums; ++k) acc.sum[k] += t.s[k];
+                    acc.cnt[1] += t.clip;
+                    acc.cnt[2] += t.dual;
+                    acc.cnt[3] += t.ice_lo;
+                    acc.cnt[4] += t.ice_hi;
+                    acc.cnt[5] += t.tis;
+                    hist[t.j * kPgThreads] += 1;
+                }
+                acc.cnt[0] += 4;
+                if (a.loss_ppo) __stcs(reinterpret_cast<float4*>(a.loss_ppo + g + j4), make_float4(lp[0], lp[1], lp[2], lp[3]));
+                if (a.loss_dec) __stcs(reinterpret_cast<float4*>(a.loss_dec + g + j4), make_float4(ld[0], ld[1], ld[2], ld[3]));
+                if (a.grad_ppo) __stcs(reinterpret_cast<float4*>(a.grad_ppo + g + j4), make_float4(gp[0], gp[1], gp[2], gp[3]));
+                if (a.grad_dec) __stcs(reinterpret_cast<float4*>(a.grad_dec + g + j4), make_float4(gd[0], gd[1], gd[2], gd[3]));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + slot);
+        }
+        // the last T mod 4 tokens, scalar loads
+        if (blockIdx.x == a.nb - 1) {
+            const int64_t t = 4 * n4 + threadIdx.x;
+            if (t < a.T) {
+                float lp, ld, gp, gd;
+                const float xt = a.lt[t], xo = a.lo[t], xs = a.ls[t], xa = a.adv[t];
+                PgTok tk = pg_fast_packed(xt, xo, xs, xa, q, lut, s_eps, s_weps);
+                if (tk.band) pg_resolve(tk, xt, xo, xs, xa, q);
+                pg_take(tk, true, hist, acc, lp, ld, gp, gd);
+                if (a.loss_ppo) a.loss_ppo[t] = lp;
+                if (a.loss_dec) a.loss_dec[t] = ld;
+                if (a.grad_ppo) a.grad_ppo[t] = gp;
+                if (a.grad_dec) a.grad_dec[t] = gd;
+            }
+        }
+    }
+    pg_block_record(a, acc, hist_s, &blk_status);
     pg_finish(a);
 }
 
 // ----------------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------------
-// Workspace: a 256-byte header (arrival count, status word, range flag, and at byte 16
-// the kPgFields accumulators).
-struct PgWs {
-    int* done;
-    int32_t* status;
-    int* range;
-    long long* acc;
-};
+// Workspace: a 256-byte header (the arrival counter at byte 0: zero before the first call,
+// and the last block of every call leaves it zero), then one 128-byte partial record per
+// block.  At most kPgMaxBlocks blocks run (fewer than two per SM on a part with
+// more than 256 SMs), so the workspace size does not depend on the device.
+constexpr int kPgMaxBlocks = 512;
 constexpr size_t kPgHeader = 256;
-static_assert(16 + kPgFields * 8 <= kPgHeader, "accumulators must fit the header");
+static_assert(kPgHeader + kPgMaxBlocks * sizeof(PgSlot) == kPolicyWorkspaceBytes, "workspace layout");
 
-static int fast_blocks(int sms) { return sms * kPgFastPerSm; }
-static int slow_blocks(int sms) { return sms * kPgSlowPerSm; }
-
-static PgWs pg_ws(void* ws) {
-    PgWs w;
-    uint8_t* b = static_cast<uint8_t*>(ws);
-    w.done = reinterpret_cast<int*>(b + 4);
-    w.status = reinterpret_cast<int32_t*>(b + 8);
-    w.range = reinterpret_cast<int*>(b + 12);
-    w.acc = reinterpret_cast<long long*>(b + 16);
-    return w;
+static int fast_blocks(int sms) {   // odd: see policy_fast_kernel
+    const int n = sms * kPgFastPerSm - 1;
+    return n < kPgMaxBlocks ? n : kPgMaxBlocks - 1;
+}
+static int slow_blocks(int sms) {
+    const int n = sms * kPgSlowPerSm;
+    return n < kPgMaxBlocks ? n : kPgMaxBlocks;
 }
 
 size_t policy_ws_bytes(int64_t T) {
     (void)T;
-    return kPgHeader;
+    return kPolicyWorkspaceBytes;
 }
 
 static PgPrep prepare(const rl_pg_params& p) {
@@ -737,8 +1022,7 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
                 float* loss_dec, float* grad_ppo, float* grad_dec, rl_pg_metrics* metrics,
                 void* ws, size_t ws_bytes, cudaStream_t stream) {
     const int sms = num_sms();
-    if (ws_bytes < kPgHeader) return RL_ERR_WORKSPACE;
-    const PgWs w = pg_ws(ws);
+    if (ws_bytes < policy_ws_bytes(T)) return RL_ERR_WORKSPACE;
     auto al = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
     const bool fast = T < (int64_t(1) << 31) && al(lt) && al(lo) && al(ls) && al(adv) && al(mask) &&
                       al(loss_ppo) && al(loss_dec) && al(grad_ppo) && al(grad_dec);
@@ -755,10 +1039,8 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
     a.loss_dec = loss_dec;
     a.grad_ppo = grad_ppo;
     a.grad_dec = grad_dec;
-    a.done = w.done;
-    a.status = w.status;
-    a.acc = w.acc;
-    a.range = w.range;
+    a.arrive = static_cast<unsigned int*>(ws);
+    a.slots = reinterpret_cast<PgSlot*>(static_cast<uint8_t*>(ws) + kPgHeader);
     a.metrics = metrics;
     a.wait_ns = wait_limit_ns();
     // per device: the fast pass's shared-memory opt-in (set once; concurrent first calls
@@ -768,19 +1050,17 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RL_ERR_CUDA;
     if (fast && !smem_set[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(policy_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPgStreamSmem) !=
-            cudaSuccess)
+                cudaSuccess ||
+            cudaFuncSetAttribute(policy_packed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPkSmem) !=
+                cudaSuccess)
             return RL_ERR_CUDA;
         smem_set[dev].store(1, std::memory_order_release);
     }
-    {   // arrival count, status, range flag, accumulators
-        ProfScope pm(RL_PROF_MEMSET, stream);
-        if (cudaMemsetAsync(ws, 0, kPgHeader, stream) != cudaSuccess) return RL_ERR_CUDA;
-    }
-    ProfScope ps(RL_PROF_POLICY, stream);   // the kernel launch alone
-    a.nb = fast ? fast_blocks(sms) - 1 : slow_blocks(sms);   // fast: odd, see policy_fast_kernel
-    // a term below 2^38 / nb keeps each accumulator's total below 2^62 in 2^-24 units
-    a.range_lim = ldexpf(1.f, 38) / static_cast<float>(a.nb);
-    if (fast) {
+    ProfScope ps(RL_PROF_POLICY, stream);   // the kernel launch
+    a.nb = fast ? fast_blocks(sms) : slow_blocks(sms);
+    if (fast && mask == nullptr) {
+        policy_packed_kernel<<<a.nb, kPgThreads + 32, kPkSmem, stream>>>(a);
+    } else if (fast) {
         policy_fast_kernel<<<a.nb, kPgThreads + 32, kPgStreamSmem, stream>>>(a);
     } else {
         policy_slow_kernel<<<a.nb, kPgThreads, 0, stream>>>(a);

@@ -1,6 +1,6 @@
 // rl_policy_loss_elementwise_noalloc: the elementwise PPO / TIS / mismatch path for callers
-// that cannot allocate device memory.  Its scratch (counters and the fixed-point metric
-// accumulators) lives in a file-scope device array instead of a caller workspace.
+// that cannot allocate device memory.  Its scratch (the arrival counter and the blocks'
+// partial records) lives in a file-scope device array instead of a caller workspace.
 #include <mutex>
 
 #include "common.cuh"
@@ -8,8 +8,9 @@
 
 namespace rl {
 
-// 4 KiB: room for the 256-byte header the elementwise pass uses.
-constexpr size_t kNoAllocScratchBytes = 4096;
+// 65,792 bytes: the elementwise pass's workspace (a 256-byte header and 512 per-block
+// partial records of 128 bytes).
+constexpr size_t kNoAllocScratchBytes = kPolicyWorkspaceBytes;
 static __device__ __align__(256) double g_policy_scratch[kNoAllocScratchBytes / sizeof(double)];
 
 // Device address of g_policy_scratch for the current device, looked up once per device
@@ -51,7 +52,7 @@ extern "C" int rl_policy_loss_elementwise_noalloc(const float* lp_theta, const f
         set_last_error("bad pg params");
         return RL_ERR_ARG;
     }
-    if (T > 0 && (!lp_theta || !lp_old || !lp_samp || !adv || !mask)) {
+    if (T > 0 && (!lp_theta || !lp_old || !lp_samp || !adv)) {
         set_last_error("input NULL");
         return RL_ERR_ARG;
     }
@@ -62,7 +63,7 @@ extern "C" int rl_policy_loss_elementwise_noalloc(const float* lp_theta, const f
         set_last_error("needs an sm_100-family GPU");
         return RL_ERR_UNSUPPORTED;
     }
-    static_assert(kNoAllocScratchBytes >= 256, "the scratch must hold the header");
+    static_assert(kNoAllocScratchBytes >= kPolicyWorkspaceBytes, "the scratch must hold the pass's workspace");
     void* scratch = nullptr;
     int rc = scratch_address(&scratch);
     if (rc != RL_OK) return rc;

@@ -82,9 +82,10 @@ def test_c4_shapes_draws_exact_kl(prec):
 
 
 def _sampled_rows(N, seed):
-    """Tile edges (128-row halves, 256-row pairs, 16k chunks), the ends, random rows."""
+    """Tile edges (128-row halves, 256-row pairs, 8k / 16k chunks), the ends, random rows."""
     rng = np.random.default_rng(seed)
-    fixed = [r for r in (0, 1, 127, 128, 255, 256, 16383, 16384, 32767, 49152, N // 2, N - 1) if r < N]
+    fixed = [r for r in (0, 1, 127, 128, 255, 256, 8191, 8192, 16383, 16384, 32767, 49152, N // 2, N - 1)
+             if r < N]
     return np.unique(np.r_[fixed, rng.integers(0, N, 13)]).astype(np.int64)
 
 
@@ -139,7 +140,7 @@ def test_c4_full_size_sampled():
     # dX rows against the oracle (row reading of the bf16 bar)
     inp = _check_sampled_rows(case, hp, fwd, dX, dloss_t, _sampled_rows(N, 7), tag="c4-full")
     H = case.H
-    # sampled vocabulary rows of dW, accumulated over the four 16k-token chunks, against
+    # sampled vocabulary rows of dW, accumulated over the eight 8k-token chunks, against
     # the oracle's dW over the whole batch (its full-vocabulary logsumexp of every token:
     # about 4e13 fp64 flop, spread over the host's cores)
     ids = case.ids.cpu().numpy()
@@ -171,7 +172,7 @@ def test_c4_full_size_sampled():
     dX2, dW2, st = rh.rl_head_loss_bwd(batch, hp, f2.saved, dloss_t)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    # same arithmetic, but the fused call runs the forward per 16k-token chunk (its own
+    # same arithmetic, but the fused call runs the forward per 8k-token chunk (its own
     # vocabulary split count), so the logsumexp partials combine in another order: each
     # call's log-probs lie within logp_tol of the oracle, so per token the two losses differ
     # by at most that bar twice, carried through |dloss/dlogP| <= |adv_tau A| (w + sum|c|)

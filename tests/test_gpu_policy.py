@@ -38,7 +38,8 @@ def _dev(x, offset):
 
 
 def _run(lt, lo, ls, A, m, pp, offset=0):
-    d = [_dev(x, offset) for x in (lt, lo, ls, A, m)]
+    """m None: packed input (no mask; every slot valid)."""
+    d = [_dev(x, offset) for x in (lt, lo, ls, A)] + [None if m is None else _dev(m, offset)]
     out = rh.rl_policy_loss_elementwise(*d, pp)
     torch.cuda.synchronize()
     return [o.cpu().double().numpy() for o in out[:4]], rh.pg_metrics(out[4], len(pp.curve_eps))
@@ -47,7 +48,8 @@ def _run(lt, lo, ls, A, m, pp, offset=0):
 def _compare(lt, lo, ls, A, m, pp, offset=0):
     (lp, ld, gp, gd), gm = _run(lt, lo, ls, A, m, pp, offset)
     assert gm["status"] == 0
-    ref = oracle.policy_loss_elementwise(lt, lo, ls, A, m, _oracle_pp(pp))
+    ref = oracle.policy_loss_elementwise(lt, lo, ls, A, np.ones(len(lt), np.uint8) if m is None else m,
+                                         _oracle_pp(pp))
     rm = ref["metrics"]
     for g, k in ((lp, "loss_ppo"), (ld, "loss_dec"), (gp, "grad_ppo"), (gd, "grad_dec")):
         r = ref[k]
@@ -70,6 +72,30 @@ def test_c5_full_size():
     c = workloads.make_policy_case()
     gm, rm = _compare(c.lp_theta, c.lp_old, c.lp_samp, c.adv, c.mask, rh.PgParams())
     assert gm["n_valid"] == 1_800_000
+
+
+def test_c5_packed():
+    """The same 1.8M valid tokens laid end to end with no mask (the packed layout):
+    against the oracle, and every count equal to the padded run's."""
+    c = workloads.make_policy_case()
+    p = c.packed()
+    gm, rm = _compare(p["lp_theta"], p["lp_old"], p["lp_samp"], p["adv"], None, rh.PgParams())
+    assert gm["n_valid"] == 1_800_000 == len(p["lp_theta"])
+    _, gpad = _run(c.lp_theta, c.lp_old, c.lp_samp, c.adv, c.mask, rh.PgParams())
+    for k in ("n_valid", "n_clip", "n_clip_lower", "icepop_low", "icepop_high", "n_tis_trunc", "ipo_curve"):
+        assert gm[k] == gpad[k], k
+
+
+@pytest.mark.parametrize("T,offset", [(1, 0), (17, 0), (5000, 1), (1024 * 304 * 3 + 7, 0), (300_001, 3)])
+def test_packed_ragged_and_unaligned(T, offset):
+    """Packed input of every length class, aligned (streaming pass) and not (exact pass)."""
+    rng = np.random.default_rng(T + offset)
+    lt = rng.normal(-1, 0.5, T).astype(np.float32)
+    lo = (lt + rng.normal(0, 0.3, T)).astype(np.float32)
+    ls = (lo + rng.normal(0, 0.5, T)).astype(np.float32)
+    A = rng.normal(0, 1, T).astype(np.float32)
+    gm, _ = _compare(lt, lo, ls, A, None, rh.PgParams(), offset)
+    assert gm["n_valid"] == T
 
 
 @pytest.mark.parametrize("T", [1, 3, 5, 16, 1001, 1024 * 304 * 3 + 7])
@@ -163,10 +189,10 @@ def test_unaligned_inputs_take_the_exact_pass(offset):
     _compare(lt, lo, ls, A, m, rh.PgParams(), offset=offset)
 
 
-def test_huge_sum_terms_take_the_exact_metric_pass():
-    """A few tokens with log pi_old - log pi_rollout = 30 (k3 terms near e^30): too large
-    for the fixed-point batch accumulators, so the last block redoes the metrics in fp32
-    over the whole batch; outputs and metrics still match the oracle."""
+def test_huge_sum_terms():
+    """A few tokens with log pi_old - log pi_rollout = 30 (k3 terms near e^30, beside terms
+    of order 1): block partials in fp32, the batch in fp64; outputs and metrics still match
+    the oracle."""
     rng = np.random.default_rng(21)
     T = 100_000
     ls = np.log(rng.random(T) * 0.9 + 0.05).astype(np.float32)
@@ -238,8 +264,8 @@ def test_all_padding():
 
 
 def test_bitwise_reproducible():
-    """Three c5 passes give identical bytes: metrics (integer accumulators, whatever the
-    order in which blocks arrive) and outputs."""
+    """Three c5 passes give identical bytes: metrics (the blocks' records summed in block
+    order, whatever the order in which blocks arrive) and outputs."""
     c = workloads.make_policy_case()
     d = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (c.lp_theta, c.lp_old, c.lp_samp, c.adv, c.mask)]
     runs = []
@@ -250,3 +276,23 @@ def test_bitwise_reproducible():
     for r in runs[1:]:
         assert r[0] == runs[0][0]
         assert r[1] == runs[0][1]
+
+
+def test_one_workspace_across_calls():
+    """A workspace zeroed once serves calls of different sizes, layouts and knobs in a row
+    (each call's last block leaves the arrival counter at zero): every call equals the
+    same call on a fresh workspace, byte for byte."""
+    ws = torch.zeros(rh.rl_policy_workspace_bytes(0), dtype=torch.uint8, device="cuda")
+    c = workloads.make_policy_case(total_tokens=250_000, seed=31)
+    p = c.packed()
+    cases = [((c.lp_theta, c.lp_old, c.lp_samp, c.adv, c.mask), rh.PgParams()),
+             ((p["lp_theta"], p["lp_old"], p["lp_samp"], p["adv"], None), rh.PgParams(curve_eps=(0.2, 0.1))),
+             ((c.lp_theta[:1001], c.lp_old[:1001], c.lp_samp[:1001], c.adv[:1001], c.mask[:1001]), rh.PgParams()),
+             ((p["lp_theta"][1:], p["lp_old"][1:], p["lp_samp"][1:], p["adv"][1:], None), rh.PgParams())]
+    for arrays, pp in cases * 2:
+        d = [None if x is None else torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in arrays]
+        fresh = rh.rl_policy_loss_elementwise(*d, pp)
+        reused = rh.rl_policy_loss_elementwise(*d, pp, ws=ws)
+        torch.cuda.synchronize()
+        for a, b in zip(fresh, reused):
+            assert torch.equal(a, b)

@@ -251,7 +251,9 @@ def test_kernels_under_a_one_microsecond_limit_finish_or_unwind(pair):
 @pytest.mark.parametrize("kind", ["draws", "replay"])
 def test_standalone_mismatch_metrics_against_the_oracle(kind):
     case = (workloads.make_head_case("c1", n_tokens=256, hidden_scale=10.0, noise=1.0, age_max=3, seed=93,
-                                     loss_mask_frac=0.2) if kind == "draws" else _replay())
+                                     loss_mask_frac=0.2) if kind == "draws" else
+            workloads.make_head_case("c1", n_tokens=256, support="replay", top_p=0.9, hidden_scale=6.0, noise=1.0,
+                                     age_max=3, seed=94, loss_mask_frac=0.2))
     hp = rh.HeadParams(loss_type=rh.RL_LOSS_IPO, eps=0.05, max_importance_ratio=3.0, kl_coeff=0.02,
                        kl_staleness=rh.RL_STALE_INV_SQRT, bwd_mode=rh.RL_BWD_DENSE)
     dev = case.to("cuda")

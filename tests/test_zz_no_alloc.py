@@ -2,12 +2,12 @@
 callers that hold only their input and output buffers and cannot allocate device memory
 (for example a loss or metrics hook inside an engine whose memory is reserved up front
 by its own pool).  It runs the same kernel as the workspace entry point on the same
-inputs, with the same deterministic integer-atomic totals, so its outputs and its metrics
-struct must equal that entry point's bit for bit, on several calls in a row: its static
-scratch keeps the previous call's contents, so each call here changes the size, the
-knobs (curve length and eps values, clip bounds) or takes the batch-wide fallback that a
-too-large sum term raises, which a stale counter, accumulator, curve count or range flag
-would all show.  This file is collected last on purpose."""
+inputs, with the same deterministic reduction of the blocks' records, so its outputs and
+its metrics struct must equal that entry point's bit for bit, on several calls in a row:
+its static scratch keeps the previous call's contents, so each call here changes the
+size, the knobs (curve length and eps values, clip bounds) or puts huge terms in the sums,
+which a stale arrival count, record or curve count would all show.  This file is
+collected last on purpose."""
 import ctypes
 
 import numpy as np
@@ -33,7 +33,7 @@ def _dev(case, big_adv_every=0):
     t = [torch.from_numpy(np.ascontiguousarray(x)).cuda()
          for x in (case.lp_theta, case.lp_old, case.lp_samp, case.adv, case.mask)]
     if big_adv_every:
-        t[3][::big_adv_every] = 1e12      # a loss term past the fixed-point range: range flag
+        t[3][::big_adv_every] = 1e12      # huge loss terms in the sums
     return t
 
 

@@ -242,6 +242,15 @@ class PolicyCase:
     def T(self) -> int:
         return int(self.lp_theta.shape[0])
 
+    def packed(self) -> dict:
+        """The same valid tokens laid end to end (no padding, no mask): lp_theta, lp_old,
+        lp_samp, adv as [n_valid] fp32 arrays and the sequences' cumulative lengths
+        cu_seqlens [B + 1] int64."""
+        keep = self.mask.astype(bool)
+        out = {k: np.ascontiguousarray(getattr(self, k)[keep]) for k in ("lp_theta", "lp_old", "lp_samp", "adv")}
+        out["cu_seqlens"] = np.concatenate([[0], np.cumsum(self.seq_lens)]).astype(np.int64)
+        return out
+
 
 def make_policy_case(total_tokens: int = 1_800_000, *, min_len: int = 64, max_len: int = 4096,
                      seed: Optional[int] = None, x_mean: float = -1.0, x_std: float = 2.5,
