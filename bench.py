@@ -178,16 +178,26 @@ def _rotating_sets(torch, dev, arrays, min_bytes):
 
 
 def _time_back_to_back(torch, calls, passes):
-    """Average device time per call over `passes` calls issued back to back between one
-    pair of CUDA events on the current stream (each call takes the next input set)."""
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    """Average device time per call over `passes` calls back to back between one pair of
+    CUDA events: one round over the input sets is captured in a CUDA graph and the graph
+    replayed, so the host's per-call cost (the Python binding takes longer than a call's
+    device time) does not leave gaps between the launches."""
+    g = torch.cuda.CUDAGraph()
     torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        for c in calls:
+            c()
+    g.replay()
+    torch.cuda.synchronize()
+    rounds = max(1, passes // len(calls))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for i in range(passes):
-        calls[i % len(calls)]()
+    for _ in range(rounds):
+        g.replay()
     e1.record()
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / passes
+    del g
+    return e0.elapsed_time(e1) / (rounds * len(calls))
 
 
 def elementwise_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb: int = 4096, packed: bool = True):
@@ -198,10 +208,10 @@ def elementwise_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush
     token 16 B read (four fp32 inputs) and 16 B written (four fp32 outputs).  Otherwise the
     sequences padded to 4096 slots with a response mask: 17 B read and 16 B written per slot.
 
-    Timing: `passes` calls back to back between one event pair, over rotating copies of the
-    inputs whose total is more than twice L2 (no pass finds its inputs in L2); per call
-    that is the workspace memset and the kernel launch, the figure the roofline divides
-    by.  The library's own per-launch event pairs (rl_profile) time single calls after an
+    Timing: `passes` calls back to back (a CUDA graph of one round over rotating copies of
+    the inputs whose total is more than twice L2, so no pass finds its inputs in L2,
+    replayed between one event pair); per call that is the kernel launch, the figure the
+    roofline divides by.  The library's own per-launch event pairs (rl_profile) time single calls after an
     L2-flushing memset as well (kernel_us_single_launch), a figure that includes an event
     pair's own ~2 us."""
     import numpy as np
@@ -249,7 +259,7 @@ def elementwise_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush
             "tokens_per_s": n_valid / (ms / 1e3), "passes": passes, "input_sets": len(sets),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "traffic": None, "algorithmic_bytes_per_pass": nbytes,
-                         "duration": "average per call, back to back (workspace memset + kernel)",
+                         "duration": "average per call, back to back in a CUDA graph (one kernel launch per call)",
                          "peak_kind": f"hbm_gbs ({peaks['source']})"},
             "l2": f"{len(sets)} rotating input sets of {sum(a.nbytes for a in arrays if a is not None) >> 20} MB "
                   "(more than 2x L2 per round)"}
@@ -314,7 +324,7 @@ def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb:
             "tokens_per_s": n_valid / (ms / 1e3), "passes": passes, "input_sets": len(sets),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "traffic": None, "algorithmic_bytes_per_pass": nbytes,
-                         "duration": "average per call, back to back (workspace memset + kernels)",
+                         "duration": "average per call, back to back in a CUDA graph (workspace memset + kernels)",
                          "peak_kind": f"hbm_gbs ({peaks['source']})"},
             "l2": f"{len(sets)} rotating input sets (more than 2x L2 per round)"}
 

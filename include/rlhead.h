@@ -208,6 +208,44 @@ int rl_head_loss_fwd_bwd(const rl_head_batch* batch, const rl_params* params,
                          int accumulate_dW, void* saved, void* ws, size_t ws_bytes,
                          int32_t* dev_status, void* stream);
 
+/* ---- the head split by vocabulary across ranks ---------------------------------------
+ * Each of R ranks holds a contiguous range [vocab_begin, vocab_end) of W's rows (pull request
+ * #4233, "What changes": the support is sharded with the head); every rank holds the whole
+ * batch.  Per step (lm_head_gb300/vocab_parallel.py drives it with torch.distributed):
+ *   forward   1. rl_head_shard_remap: the labels' and support ids' local numbering;
+ *             2. rl_head_shard_stats on the rank's rows: per token the logsumexp statistics
+ *                over its columns (m = max z, s = sum e^(z - m), u = sum e^(z - m)(z - m))
+ *                and the label / support logits it owns (0 for the others);
+ *             3. all-gather of the statistics (rank order), all-reduce (sum) of the owned
+ *                logits: every logit is nonzero on exactly its owner;
+ *             4. rl_head_loss_from_shard_stats on every rank: the loss, log-probs, masks,
+ *                metrics and saved state, combining the R statistics as the single-GPU
+ *                forward combines its vocabulary splits (the same bits on every rank).
+ *   backward  rl_head_loss_bwd on the rank's rows with the local ids and the saved state of
+ *             step 4: dW of its rows, and its part of dX (bf16), which the ranks all-reduce.
+ * Unmeasured on hardware with more than one GPU: one process here emulates the ranks. */
+
+/* ids_local[i] = ids[i] - vocab_begin for an id inside [vocab_begin, vocab_end), -1 below
+ * the range, vocab_end - vocab_begin above it (a row stays in ascending order; an id the
+ * shard does not own matches none of its columns).  Device arrays of n int32. */
+int rl_head_shard_remap(const int32_t* ids, int64_t n, int64_t vocab_begin, int64_t vocab_end, int32_t* ids_local,
+                        void* stream);
+/* shard: the batch with weight = the rank's rows of W (V = their count) and labels / support
+ * ids in local numbering (rl_head_shard_remap); params: temperature only.  Outputs, device:
+ * stats [3][N] fp32 (m, then s, then u, per token over the shard's columns), zlab [N] and
+ * zsup [nnz] fp32 (the logits / T of the labels and entries the shard owns, 0 elsewhere).
+ * Workspace: rl_head_fwd_workspace_bytes(N, H, V_shard, nnz).  No validation here. */
+int rl_head_shard_stats(const rl_head_batch* shard, const rl_params* params, float* stats, float* zlab, float* zsup,
+                        void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+/* batch: the whole batch in global numbering (weight unused, may be NULL; V the full
+ * vocabulary); stats_all [n_shards][3][N]: the shards' statistics in rank order; zlab, zsup:
+ * the owned logits summed over the ranks.  Outputs and saved state as rl_head_loss_fwd
+ * (validation included); workspace rl_head_fwd_workspace_bytes(N, H, V, nnz). */
+int rl_head_loss_from_shard_stats(const rl_head_batch* batch, const rl_params* params, int32_t n_shards,
+                                  const float* stats_all, const float* zlab, const float* zsup,
+                                  const rl_head_outputs* out, void* saved, void* ws, size_t ws_bytes,
+                                  int32_t* dev_status, void* stream);
+
 /* Reduce the per-token metric terms in `saved` (written by rl_head_loss_fwd for the same
  * batch) into *metrics (device).  rl_head_loss_fwd calls it when out->metrics != NULL. */
 int rl_mismatch_metrics(const rl_head_batch* batch, const void* saved,

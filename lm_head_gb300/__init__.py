@@ -7,7 +7,9 @@ fallback: if the extension is missing or no sm_100-family GPU is present, calls 
 Functions carry the C names:
   head:        rl_validate_support, rl_head_loss_fwd, rl_head_loss_bwd,
                rl_head_loss_fwd_bwd (one call when dloss is known before the forward),
-               rl_mismatch_metrics
+               rl_mismatch_metrics; vocabulary shards: rl_head_shard_remap,
+               rl_head_shard_stats, rl_head_loss_from_shard_stats (rank logic in
+               lm_head_gb300.vocab_parallel)
   elementwise: rl_policy_loss_elementwise (+ rl_policy_loss_elementwise_noalloc in C)
   rollout:     rl_rollout_correction (IS / RS weights, veto, batch normalisation, metric
                sums), rl_rollout_metrics_named (the page's named metrics from those sums)
@@ -140,6 +142,11 @@ _SIGS = {
     "rl_head_loss_bwd": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
                                                                 ctypes.c_void_p, ctypes.c_void_p]),
     "rl_mismatch_metrics": (ctypes.c_int, [ctypes.c_void_p] * 4 + [ctypes.c_size_t, ctypes.c_void_p]),
+    "rl_head_shard_remap": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_void_p, ctypes.c_void_p]),
+    "rl_head_shard_stats": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+    "rl_head_loss_from_shard_stats": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32]
+                                      + [ctypes.c_void_p] * 6 + [ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
     "rl_head_fwd_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 4 + [ctypes.c_void_p]),
     "rl_head_loss_fwd_bwd": (ctypes.c_int, [ctypes.c_void_p] * 6 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                                                     ctypes.c_size_t, ctypes.c_void_p,
@@ -270,7 +277,9 @@ class HeadBatch:
     def nnz(self):
         return int(self.ids.shape[0])
 
-    def c(self) -> RlHeadBatch:
+    def c(self, V: Optional[int] = None) -> RlHeadBatch:
+        """The C struct; V overrides the vocabulary size (the whole vocabulary when `weight`
+        holds only one rank's rows)."""
         _require_cuda(self.hidden, self.weight, self.labels, self.label_logq, self.adv, self.offsets,
                       self.ids, self.logq, self.replayed, self.loss_mask, self.age)
         for name, t, dt in (("hidden", self.hidden, torch.bfloat16), ("weight", self.weight, torch.bfloat16),
@@ -282,7 +291,7 @@ class HeadBatch:
                 raise RLHeadError(f"{name}: expected contiguous {dt}, got {t.dtype}")
         sup = RlSupport(self.offsets.data_ptr(), self.ids.data_ptr() if self.nnz else None,
                         self.logq.data_ptr() if self.nnz else None, self.replayed.data_ptr(), self.nnz)
-        return RlHeadBatch(self.hidden.data_ptr(), self.weight.data_ptr(), self.N, self.H, self.V,
+        return RlHeadBatch(self.hidden.data_ptr(), self.weight.data_ptr(), self.N, self.H, self.V if V is None else V,
                            self.labels.data_ptr(), self.label_logq.data_ptr(), self.adv.data_ptr(),
                            None if self.loss_mask is None else self.loss_mask.data_ptr(),
                            None if self.age is None else self.age.data_ptr(), sup)
@@ -452,6 +461,72 @@ def rl_mismatch_metrics(batch: HeadBatch, saved: torch.Tensor, params: HeadParam
     _check(lib.rl_mismatch_metrics(ctypes.byref(cb), _ptr(saved), _ptr(m), _ptr(ws), ws.numel(), _stream(stream)))
     mm = RlHeadMetrics.from_buffer_copy(bytes(m.cpu().numpy().tobytes()))
     return {f: getattr(mm, f) for f, _ in RlHeadMetrics._fields_}
+
+
+def rl_head_shard_remap(ids: torch.Tensor, vocab_begin: int, vocab_end: int, out: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    """Global ids (int32, device) in the local numbering of the vocabulary rows
+    [vocab_begin, vocab_end): -1 below, vocab_end - vocab_begin above (include/rlhead.h)."""
+    _require_cuda(ids)
+    out = torch.empty_like(ids) if out is None else out
+    _check(load().rl_head_shard_remap(_ptr(ids), int(ids.numel()), int(vocab_begin), int(vocab_end), _ptr(out),
+                                      _stream(stream)))
+    return out
+
+
+def rl_head_shard_stats(shard: HeadBatch, params: HeadParams, *, ws: Optional[torch.Tensor] = None,
+                        status: Optional[torch.Tensor] = None, stream=None):
+    """One rank's logsumexp statistics [3, N] (m, s, u) and owned label / support logits."""
+    lib = load()
+    dev = shard.hidden.device
+    N, nnz = shard.N, shard.nnz
+    stats = torch.empty(3, N, dtype=torch.float32, device=dev)
+    zlab = torch.empty(N, dtype=torch.float32, device=dev)
+    zsup = torch.empty(max(nnz, 1), dtype=torch.float32, device=dev)[:nnz]
+    st = torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status
+    if ws is None:
+        ws = _u8(rl_head_fwd_workspace_bytes(N, shard.H, shard.V, nnz, params), dev)
+    p = params.c()
+    cb = shard.c()
+    _check(lib.rl_head_shard_stats(ctypes.byref(cb), ctypes.byref(p), _ptr(stats), _ptr(zlab),
+                                   _ptr(zsup) if nnz else None, _ptr(ws), ws.numel(), _ptr(st), _stream(stream)))
+    return stats, zlab, zsup
+
+
+def rl_head_loss_from_shard_stats(batch: HeadBatch, params: HeadParams, stats_all: torch.Tensor, zlab: torch.Tensor,
+                                  zsup: torch.Tensor, *, V: int, ws: Optional[torch.Tensor] = None,
+                                  status: Optional[torch.Tensor] = None, want_metrics: bool = True,
+                                  stream=None) -> HeadForward:
+    """The forward's outputs from the ranks' gathered statistics [R, 3, N] and the summed
+    owned logits; `batch` in global numbering, V the whole vocabulary."""
+    lib = load()
+    _require_cuda(stats_all, zlab, zsup)
+    dev = batch.hidden.device
+    N, nnz = batch.N, batch.nnz
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = HeadForward(
+        loss=torch.empty(N, **f32), logp_label=torch.empty(N, **f32),
+        logp_support=torch.empty(max(nnz, 1), **f32)[:nnz], entropy=torch.empty(N, **f32),
+        lse=torch.empty(N, **f32), mask_label=torch.empty(N, dtype=torch.uint8, device=dev),
+        mask_support=torch.empty(max(nnz, 1), dtype=torch.uint8, device=dev)[:nnz],
+        metrics_dev=torch.zeros(ctypes.sizeof(RlHeadMetrics), dtype=torch.uint8, device=dev),
+        saved=_u8(rl_head_saved_bytes(N, nnz), dev),
+        status=torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status)
+    if ws is None:
+        ws = _u8(rl_head_fwd_workspace_bytes(N, batch.H, V, nnz, params), dev)
+    p = params.c()
+    cb = batch.c(V=V)
+    co = RlHeadOutputs(out.loss.data_ptr(), out.logp_label.data_ptr(),
+                       out.logp_support.data_ptr() if nnz else None, out.entropy.data_ptr(),
+                       out.lse.data_ptr(), out.mask_label.data_ptr(),
+                       out.mask_support.data_ptr() if nnz else None,
+                       out.metrics_dev.data_ptr() if want_metrics else None)
+    R = int(stats_all.shape[0])
+    _check(lib.rl_head_loss_from_shard_stats(ctypes.byref(cb), ctypes.byref(p), R, _ptr(stats_all.contiguous()),
+                                             _ptr(zlab), _ptr(zsup) if nnz else None, ctypes.byref(co),
+                                             _ptr(out.saved), _ptr(ws), ws.numel(), _ptr(out.status),
+                                             _stream(stream)))
+    return out
 
 
 @dataclasses.dataclass

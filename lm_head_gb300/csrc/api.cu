@@ -157,6 +157,51 @@ int rl_head_loss_fwd_bwd(const rl_head_batch* batch, const rl_params* params, co
                            as_stream(stream));
 }
 
+int rl_head_shard_remap(const int32_t* ids, int64_t n, int64_t vocab_begin, int64_t vocab_end, int32_t* ids_local,
+                        void* stream) {
+    if (n < 0 || vocab_begin < 0 || vocab_end <= vocab_begin || vocab_end >= (int64_t(1) << 30))
+        return fail(RL_ERR_ARG, "bad shard range or size");
+    if (n > 0 && (!ids || !ids_local)) return fail(RL_ERR_ARG, "ids NULL");
+    if (n > 0 && !sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
+    return shard_remap_impl(ids, n, vocab_begin, vocab_end, ids_local, as_stream(stream));
+}
+
+int rl_head_shard_stats(const rl_head_batch* shard, const rl_params* params, float* stats, float* zlab, float* zsup,
+                        void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+    int rc = check_batch(shard);
+    if (rc != RL_OK) return rc;
+    if ((rc = check_params(params)) != RL_OK) return rc;
+    if (shard->N > 0 && (!stats || !zlab || (shard->support.nnz > 0 && !zsup))) return fail(RL_ERR_ARG, "output NULL");
+    if (!dev_status) return fail(RL_ERR_ARG, "dev_status NULL");
+    if (ws_bytes < rl_head_fwd_workspace_bytes(shard->N, shard->H, shard->V, shard->support.nnz, params) || !ws)
+        return fail(RL_ERR_WORKSPACE, "shard workspace too small");
+    if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
+    return shard_stats_impl(shard, params, stats, zlab, zsup, ws, dev_status, as_stream(stream));
+}
+
+int rl_head_loss_from_shard_stats(const rl_head_batch* batch, const rl_params* params, int32_t n_shards,
+                                  const float* stats_all, const float* zlab, const float* zsup,
+                                  const rl_head_outputs* out, void* saved, void* ws, size_t ws_bytes,
+                                  int32_t* dev_status, void* stream) {
+    if (!batch) return fail(RL_ERR_ARG, "batch is NULL");
+    int rc = check_shape(batch->N, batch->H, batch->V, batch->support.nnz);
+    if (rc != RL_OK) return rc;
+    if ((rc = check_params(params)) != RL_OK) return rc;
+    if (n_shards < 1 || n_shards > 4096) return fail(RL_ERR_ARG, "n_shards out of [1, 4096]");
+    const bool any = batch->N > 0;
+    if (any && (!batch->labels || !batch->label_logq || !batch->adv || !batch->support.offsets ||
+                !batch->support.replayed || (batch->support.nnz > 0 && (!batch->support.ids || !batch->support.logq))))
+        return fail(RL_ERR_ARG, "required batch pointer is NULL");
+    if (!out || (any && (!out->loss || !saved || !stats_all || !zlab || (batch->support.nnz > 0 && !zsup))) ||
+        !dev_status)
+        return fail(RL_ERR_ARG, "out/loss/saved/stats/zlab/zsup/dev_status NULL");
+    if (ws_bytes < rl_head_fwd_workspace_bytes(batch->N, batch->H, batch->V, batch->support.nnz, params) || !ws)
+        return fail(RL_ERR_WORKSPACE, "forward workspace too small");
+    if (!sm100_family()) return fail(RL_ERR_UNSUPPORTED, "needs an sm_100-family GPU");
+    return loss_from_shards_impl(batch, params, n_shards, stats_all, zlab, zsup, out, saved, ws, dev_status,
+                                 as_stream(stream));
+}
+
 int rl_mismatch_metrics(const rl_head_batch* batch, const void* saved, rl_head_metrics* metrics, void* ws,
                         size_t ws_bytes, void* stream) {
     int rc = check_batch(batch);

@@ -405,6 +405,7 @@ struct TokenArgs {
     int32_t V;
     int32_t S;
     int64_t nnz;
+    int64_t pstride;   // distance between the partials of consecutive splits (N, or 3 N for shard triplets)
     const float* part_m;
     const float* part_s;
     const float* part_u;
@@ -493,11 +494,11 @@ __global__ void __launch_bounds__(256) token_loss_kernel(TokenArgs a) {
     if (t >= a.N) return;
     // combine the per-split (m, s, u) statistics: logsumexp and entropy of the full row
     float M = -INFINITY;
-    for (int i = lane; i < a.S; i += 32) M = fmaxf(M, a.part_m[static_cast<int64_t>(i) * a.N + t]);
+    for (int i = lane; i < a.S; i += 32) M = fmaxf(M, a.part_m[static_cast<int64_t>(i) * a.pstride + t]);
     M = warp_max(M);
     float s = 0.f, u = 0.f;
     for (int i = lane; i < a.S; i += 32) {
-        const int64_t k = static_cast<int64_t>(i) * a.N + t;
+        const int64_t k = static_cast<int64_t>(i) * a.pstride + t;
         const float mi = a.part_m[k], si = a.part_s[k], ui = a.part_u[k];
         const float f = expf(mi - M);
         s += f * si;
@@ -813,6 +814,7 @@ int fwd_rows(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs
     ta.V = static_cast<int32_t>(V);
     ta.S = 2 * plan.n_splits;
     ta.nnz = nnz;
+    ta.pstride = n;
     ta.part_m = w.part_m;
     ta.part_s = w.part_s;
     ta.part_u = w.part_u;
@@ -865,6 +867,158 @@ int fwd_rows(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs
     }
     count_launch();
     return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------------------------
+// Vocabulary shards: the head split by rows of W (each rank a contiguous vocabulary range)
+// ----------------------------------------------------------------------------------
+// Global ids to a shard's local ids: id - v0 inside [v0, v1), -1 below, v1 - v0 above, so a
+// row's ids stay in ascending order and the ids the shard does not own never match one of
+// its columns.
+__global__ void shard_remap_kernel(const int32_t* in, int64_t n, int32_t v0, int32_t v1, int32_t* out) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int32_t id = in[i];
+    out[i] = id < v0 ? -1 : (id >= v1 ? v1 - v0 : id - v0);
+}
+
+// One (m, s, u) per token over the shard's columns from the GEMM's split partials (the same
+// combination as token_loss_kernel's); stats [3][N]: m, then s, then u.
+__global__ void shard_combine_kernel(const float* pm, const float* ps, const float* pu, int32_t S, int64_t N,
+                                     float* stats) {
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (t >= N) return;
+    float M = -INFINITY;
+    for (int i = 0; i < S; ++i) M = fmaxf(M, pm[static_cast<int64_t>(i) * N + t]);
+    float sv = 0.f, uv = 0.f;
+    for (int i = 0; i < S; ++i) {
+        const int64_t k = static_cast<int64_t>(i) * N + t;
+        const float f = expf(pm[k] - M);
+        sv += f * ps[k];
+        uv += f * (pu[k] + (pm[k] - M) * ps[k]);
+    }
+    stats[t] = M;
+    stats[N + t] = sv;
+    stats[2 * N + t] = uv;
+}
+
+int shard_remap_impl(const int32_t* in, int64_t n, int64_t v0, int64_t v1, int32_t* out, cudaStream_t stream) {
+    if (n <= 0) return RL_OK;
+    ProfScope ps(RL_PROF_OTHER, stream);
+    shard_remap_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+        in, n, static_cast<int32_t>(v0), static_cast<int32_t>(v1), out);
+    count_launch();
+    return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
+int shard_stats_impl(const rl_head_batch* b, const rl_params* prm, float* stats, float* zlab, float* zsup, void* ws,
+                     int32_t* status, cudaStream_t stream) {
+    const int64_t N = b->N, H = b->H, V = b->V, nnz = b->support.nnz;
+    if (N == 0) return RL_OK;
+    const FwdWs w = fwd_ws_view(ws, N, H, V, nnz, nullptr);
+    if (cudaMemsetAsync(zlab, 0, N * sizeof(float), stream) != cudaSuccess) return RL_ERR_CUDA;
+    if (nnz > 0 && cudaMemsetAsync(zsup, 0, nnz * sizeof(float), stream) != cudaSuccess) return RL_ERR_CUDA;
+    const int S = choose_splits(N, V);
+    CUtensorMap tmX, tmW;
+    int rc = make_tmap_bf16(&tmX, b->hidden, N, H, H, kBM);
+    if (rc != RL_OK) return rc;
+    rc = make_tmap_b(&tmW, b->weight, V, H, H);
+    if (rc != RL_OK) return rc;
+    const GemmPlan plan = make_plan_auto(N, V, H, 1, S, 1, status);
+    EpiStats::Params ep;
+    std::memset(&ep, 0, sizeof(ep));
+    ep.N = N;
+    ep.V = static_cast<int32_t>(V);
+    ep.inv_T = 1.0f / prm->temperature;
+    ep.c2 = kLog2e / prm->temperature;
+    ep.nnz = nnz;
+    ep.labels = b->labels;
+    ep.offsets = b->support.offsets;
+    ep.ids = b->support.ids;
+    ep.zlab = zlab;
+    ep.zsup = zsup;
+    ep.part_m = w.part_m;
+    ep.part_s = w.part_s;
+    ep.part_u = w.part_u;
+    ep.ldm = (V + 31) / 32;
+    {
+        ProfScope ps(RL_PROF_GEMM_FWD, stream);
+        rc = launch_gemm_auto<EpiStats>(tmX, tmX, tmW, plan, ep, stream);
+    }
+    count_launch();
+    if (rc != RL_OK) return rc;
+    {
+        ProfScope ps(RL_PROF_TOKEN_LOSS, stream);
+        shard_combine_kernel<<<static_cast<unsigned>((N + 255) / 256), 256, 0, stream>>>(
+            w.part_m, w.part_s, w.part_u, 2 * plan.n_splits, N, stats);
+    }
+    count_launch();
+    return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
+}
+
+int loss_from_shards_impl(const rl_head_batch* b, const rl_params* prm, int32_t R, const float* stats_all,
+                          const float* zlab, const float* zsup, const rl_head_outputs* out, void* saved, void* ws,
+                          int32_t* status, cudaStream_t stream) {
+    const int64_t N = b->N, nnz = b->support.nnz;
+    int rc = validate_impl(b, status, stream);
+    if (rc != RL_OK) return rc;
+    if (N == 0) return RL_OK;
+    const SavedView sv = saved_view(saved, N, nnz, nullptr);
+    if (cudaMemcpyAsync(sv.zlab, zlab, N * sizeof(float), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+        return RL_ERR_CUDA;
+    if (nnz > 0 && cudaMemcpyAsync(sv.zsup, zsup, nnz * sizeof(float), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+        return RL_ERR_CUDA;
+    auto opt = [](auto* p) { return p; };
+    TokenArgs ta;
+    std::memset(&ta, 0, sizeof(ta));
+    ta.N = N;
+    ta.V = static_cast<int32_t>(b->V);
+    ta.S = R;
+    ta.nnz = nnz;
+    ta.pstride = 3 * N;
+    ta.part_m = stats_all;
+    ta.part_s = stats_all + N;
+    ta.part_u = stats_all + 2 * N;
+    ta.zlab = sv.zlab;
+    ta.zsup = sv.zsup;
+    ta.labels = b->labels;
+    ta.label_logq = b->label_logq;
+    ta.adv = b->adv;
+    ta.loss_mask = b->loss_mask;
+    ta.age = b->age;
+    ta.offsets = b->support.offsets;
+    ta.ids = b->support.ids;
+    ta.logq = b->support.logq;
+    ta.replayed = b->support.replayed;
+    ta.loss_type = prm->loss_type;
+    ta.kl_est = prm->kl_estimator;
+    ta.kl_stale = prm->kl_staleness;
+    ta.sparse = !bwd_is_dense(prm);
+    ta.eps = prm->eps;
+    ta.cap = prm->max_importance_ratio;
+    ta.lo = prm->icepop_low;
+    ta.hi = prm->icepop_high;
+    ta.adv_tau = prm->adv_tau;
+    ta.kl_coeff = prm->kl_coeff;
+    ta.ent_coeff = prm->entropy_coeff;
+    ta.loss = out->loss;
+    ta.logp_label = opt(out->logp_label);
+    ta.logp_support = out->logp_support;
+    ta.entropy = opt(out->entropy);
+    ta.lse_out = opt(out->lse);
+    ta.mask_label = opt(out->mask_label);
+    ta.mask_support = out->mask_support;
+    ta.sv = sv;
+    ta.status = status;
+    ta.inv_T = 1.0f / prm->temperature;
+    {
+        ProfScope ps(RL_PROF_TOKEN_LOSS, stream);
+        token_loss_kernel<<<static_cast<unsigned>((N + 7) / 8), 256, 0, stream>>>(ta);
+    }
+    count_launch();
+    if (cudaPeekAtLastError() != cudaSuccess) return RL_ERR_CUDA;
+    if (out->metrics) return metrics_impl(b, saved, out->metrics, ws, stream);
+    return RL_OK;
 }
 
 int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out,

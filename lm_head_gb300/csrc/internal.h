@@ -126,6 +126,12 @@ int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_
                     int32_t* status, cudaStream_t stream);
 size_t fused_ws_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* prm);
 int validate_impl(const rl_head_batch* b, int32_t* status, cudaStream_t stream);
+int shard_remap_impl(const int32_t* in, int64_t n, int64_t v0, int64_t v1, int32_t* out, cudaStream_t stream);
+int shard_stats_impl(const rl_head_batch* b, const rl_params* prm, float* stats, float* zlab, float* zsup, void* ws,
+                     int32_t* status, cudaStream_t stream);
+int loss_from_shards_impl(const rl_head_batch* b, const rl_params* prm, int32_t R, const float* stats_all,
+                          const float* zlab, const float* zsup, const rl_head_outputs* out, void* saved, void* ws,
+                          int32_t* status, cudaStream_t stream);
 int64_t bwd_chunk(int64_t N, const rl_params* prm);
 int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* saved,
                   const float* dloss, void* dhidden, float* dW, int accumulate, void* ws,

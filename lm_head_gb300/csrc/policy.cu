@@ -23,8 +23,11 @@
 //                          over the sorted eps (binary search; only the two neighbouring
 //                          eps are band-checked).  A token inside a band is re-decided
 //                          exactly by the thread that met it.
+//  1'. policy_packed_kernel the same pass for packed input (no mask): an equal contiguous
+//                          range per block, four tokens per thread, no selects, the curve
+//                          bin from a bucket table.
 //  2. policy_slow_kernel   the whole pass with exact decisions in the bands, for inputs the
-//                          fast pass does not take (unaligned, T >= 2^31).
+//                          fast passes do not take (unaligned, T >= 2^31).
 //  With no mask (packed input: every slot a valid token) the mask is neither read nor
 //  copied: 16 bytes in per token instead of 17.
 //  Each block writes its partial (fp32 sums in a fixed order within the block, counts, the
@@ -60,6 +63,7 @@ constexpr int kPgSlowPerSm = 2;
 // Thresholds and band half-widths prepared on the host; ln of each ratio threshold as a
 // float-float pair (-inf for a threshold <= 0); the curve eps sorted ascending with perm
 // mapping sorted position -> caller's index.
+constexpr int kPkLut = 256;                    // buckets of |p_old - p_samp| over [0, 1]
 struct PgPrep {
     float lo_b, hi_b, cc, tis, ice_lo, ice_hi;
     float w_lo_b, w_hi_b, w_cc, w_tis, w_ice_lo, w_ice_hi;
@@ -68,6 +72,12 @@ struct PgPrep {
     float eps[RL_PG_MAX_CURVE];
     float weps[RL_PG_MAX_CURVE];
     int perm[RL_PG_MAX_CURVE];
+    // the packed pass's bucket table: entry b = (eps below bucket b) | (1 + the one eps
+    // inside it, sorted index; 0: none) << 8 | (1: take the exact path) << 16; eps_s / weps_s
+    // are eps / weps shifted up by one, entry 0 a sentinel no value is above or near
+    int lut[kPkLut];
+    float eps_s[RL_PG_MAX_CURVE + 1];
+    float weps_s[RL_PG_MAX_CURVE + 1];
 };
 
 struct PgArgs {
@@ -83,23 +93,23 @@ struct PgArgs {
     float* loss_dec;
     float* grad_ppo;
     float* grad_dec;
-    struct PgSlot* slots;         // [nb] one partial record per block
+    struct PgRecords* rec;        // the blocks' partials
     unsigned int* arrive;         // blocks of this launch that have written their record (0 between calls)
     int nb;                       // blocks of the pass
     uint64_t wait_ns;             // limit of the streaming loop's waits (RL_OPT_WAIT_LIMIT_US)
     rl_pg_metrics* metrics;       // or nullptr
 };
 
-// A block's partial: fp32 sums in the block's fixed order, counts (the curve in the
-// caller's order), the RL_STATUS_* bits its waits raised.  128 bytes.
-struct alignas(16) PgSlot {
-    float sum[kPgSums];
-    int cnt[6];
-    int curve[RL_PG_MAX_CURVE];
-    int status;
-    int pad[3];
+// The blocks' partials, field-major (field f of block b at [f][b], so the last block reads
+// each field's column with coalesced loads): fp32 sums in each block's fixed order, counts
+// (the curve in the caller's order), the RL_STATUS_* bits the block's waits raised.
+constexpr int kPgRecFields = kPgSums + 6 + RL_PG_MAX_CURVE + 1;   // + status
+constexpr int kPgMaxBlocks = 512;
+struct PgRecords {
+    float sum[kPgSums][kPgMaxBlocks];
+    int cnt[6 + RL_PG_MAX_CURVE][kPgMaxBlocks];
+    int status[kPgMaxBlocks];
 };
-static_assert(sizeof(PgSlot) == 128, "one record per 128 bytes");
 
 struct PgAcc {
     float sum[kPgSums];
@@ -289,66 +299,54 @@ RL_DEVINL void pg_write_metric(int k, double s, rl_pg_metrics* out) {
 // ----------------------------------------------------------------------------------
 // Batch totals
 // ----------------------------------------------------------------------------------
-// The last block: every record summed in block order (each thread its blocks t, t + nt,
-// ..., then a fixed butterfly within warps and the warps in order), into the metrics.  The
-// sums are carried as float-float pairs (about 44 significant bits; fp64 is a slow pipe on
-// this part), the counts as integers.
+// The last block: thread (f, g) of the first 29 x 9 sums field f over the blocks g, g + 9,
+// g + 18, ... (all its loads in flight at once; fp64 for the six sums, few enough not to
+// matter on this part's slow fp64 pipe, integers for the counts, OR for the status bits),
+// then thread f adds its field's nine group totals in order.  Fixed order throughout.
 RL_DEVINL void pg_final(const PgArgs& a) {
-    constexpr int kC = 6 + RL_PG_MAX_CURVE;
-    FF v[kPgSums];
-    int c[kC];
-    int st = 0;
+    constexpr int kG = 9;
+    constexpr int kPer = (kPgMaxBlocks + kG - 1) / kG;
+    __shared__ double part_s[kPgSums][kG];
+    __shared__ int part_c[kPgRecFields - kPgSums][kG];
+    const int tid = threadIdx.x;
+    for (int idx = tid; idx < kPgRecFields * kG; idx += blockDim.x) {   // one round for 288 threads
+        const int f = idx / kG, g = idx - (idx / kG) * kG;
+        if (f < kPgSums) {
+            const float* col = a.rec->sum[f];
+            float x[kPer];
 #pragma unroll
-    for (int f = 0; f < kPgSums; ++f) v[f] = {0.f, 0.f};
+            for (int i = 0; i < kPer; ++i) x[i] = g + kG * i < a.nb ? __ldcg(col + g + kG * i) : 0.f;
+            double v = 0.0;
 #pragma unroll
-    for (int f = 0; f < kC; ++f) c[f] = 0;
-    for (int b = threadIdx.x; b < a.nb; b += blockDim.x) {
-        const PgSlot* r = a.slots + b;
+            for (int i = 0; i < kPer; ++i) v += static_cast<double>(x[i]);
+            part_s[f][g] = v;
+        } else {
+            const bool is_status = f == kPgRecFields - 1;
+            const int* col = is_status ? a.rec->status : a.rec->cnt[f - kPgSums];
+            int x[kPer];
 #pragma unroll
-        for (int f = 0; f < kPgSums; ++f) v[f] = ff_add(v[f], {__ldcg(r->sum + f), 0.f});
+            for (int i = 0; i < kPer; ++i) x[i] = g + kG * i < a.nb ? __ldcg(col + g + kG * i) : 0;
+            int v = 0;
 #pragma unroll
-        for (int f = 0; f < 6; ++f) c[f] += __ldcg(r->cnt + f);
-#pragma unroll
-        for (int f = 0; f < RL_PG_MAX_CURVE; ++f) c[6 + f] += __ldcg(r->curve + f);
-        st |= __ldcg(&r->status);
-    }
-    __shared__ FF red_s[kPgSums][(kPgThreads + 32) / 32];
-    __shared__ int red_c[kC][(kPgThreads + 32) / 32];
-    __shared__ int red_st[(kPgThreads + 32) / 32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-#pragma unroll
-    for (int f = 0; f < kPgSums; ++f) {
-        FF x = v[f];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const FF y = {__shfl_xor_sync(0xffffffffu, x.hi, o), __shfl_xor_sync(0xffffffffu, x.lo, o)};
-            x = (lane & o) ? ff_add(y, x) : ff_add(x, y);   // the same operands in the same order on both lanes
+            for (int i = 0; i < kPer; ++i) v = is_status ? (v | x[i]) : v + x[i];
+            part_c[f - kPgSums][g] = v;
         }
-        if (lane == 0) red_s[f][warp] = x;
     }
-#pragma unroll
-    for (int f = 0; f < kC; ++f) {
-        const int x = __reduce_add_sync(0xffffffffu, c[f]);
-        if (lane == 0) red_c[f][warp] = x;
-    }
-    st = __reduce_or_sync(0xffffffffu, st);
-    if (lane == 0) red_st[warp] = st;
     __syncthreads();
-    if (threadIdx.x == 0) *a.arrive = 0u;   // every block has arrived: ready for the next call
-    if (!a.metrics) return;
-    const int f = threadIdx.x;
-    if (f < kPgSums) {
-        FF x = red_s[f][0];
-        for (int w = 1; w < nw; ++w) x = ff_add(x, red_s[f][w]);
-        pg_write_metric(f, static_cast<double>(x.hi) + static_cast<double>(x.lo), a.metrics);
-    } else if (f < kPgSums + kC) {
-        int x = 0;
-        for (int w = 0; w < nw; ++w) x += red_c[f - kPgSums][w];
-        pg_write_metric(f, static_cast<double>(x), a.metrics);
-    } else if (f == kPgSums + kC) {
-        int s2 = 0;
-        for (int w = 0; w < nw; ++w) s2 |= red_st[w];
-        a.metrics->status = s2;
+    if (tid == 0) *a.arrive = 0u;   // every block has arrived: ready for the next call
+    if (!a.metrics || tid >= kPgRecFields) return;
+    if (tid < kPgSums) {
+        double v = 0.0;
+        for (int g = 0; g < kG; ++g) v += part_s[tid][g];
+        pg_write_metric(tid, v, a.metrics);
+    } else if (tid < kPgRecFields - 1) {
+        int v = 0;
+        for (int g = 0; g < kG; ++g) v += part_c[tid - kPgSums][g];
+        pg_write_metric(tid, static_cast<double>(v), a.metrics);   // counts are exact integers
+    } else {
+        int v = 0;
+        for (int g = 0; g < kG; ++g) v |= part_c[tid - kPgSums][g];
+        a.metrics->status = v;
     }
 }
 
@@ -376,16 +374,13 @@ __global__ void __launch_bounds__(kPgThreads, kPgSlowPerSm) policy_slow_kernel(P
     __shared__ float sums[kPgSums];
     __shared__ int cnts[kPgCounts];
     pg_block_reduce(acc, sums, cnts);
-    PgSlot* rec = a.slots + blockIdx.x;
     const int k = threadIdx.x;
     if (k < kPgSums)
-        rec->sum[k] = sums[k];
-    else if (k < kPgSums + 6)
-        rec->cnt[k - kPgSums] = cnts[k - kPgSums];
+        a.rec->sum[k][blockIdx.x] = sums[k];
     else if (k < kPgFields)
-        rec->curve[k - kPgSums - 6] = cnts[k - kPgSums];
+        a.rec->cnt[k - kPgSums][blockIdx.x] = cnts[k - kPgSums];
     else if (k == kPgFields)
-        rec->status = 0;
+        a.rec->status[blockIdx.x] = 0;
     pg_finish(a);
 }
 
@@ -542,33 +537,30 @@ RL_DEVINL void pg_block_record(const PgArgs& a, const PgFastAcc& acc, const int*
             if (lane == 0) bins[b] = v;
         }
     __syncthreads();
-    PgSlot* rec = a.slots + blockIdx.x;
     const int f = threadIdx.x;
+    const int b = blockIdx.x;
     if (f < kPgSums) {
         float v = 0.f;
         for (int w = 0; w < kPgThreads / 32; ++w) v += shs[w][f];
-        rec->sum[f] = v;
+        a.rec->sum[f][b] = v;
     } else if (f < kPgSums + 6) {
         int v = 0;
         for (int w = 0; w < kPgThreads / 32; ++w) v += shc[w][f - kPgSums];
-        rec->cnt[f - kPgSums] = v;
+        a.rec->cnt[f - kPgSums][b] = v;
     } else if (f < kPgFields) {
         const int c = f - kPgSums - 6;        // caller's curve index
         int v = 0;
         if (c < a.q.n) {
             int js = 0;                        // its sorted position
             while (a.q.perm[js] != c) ++js;
-            for (int b = js + 1; b <= a.q.n; ++b) v += bins[b];
+            for (int k = js + 1; k <= a.q.n; ++k) v += bins[k];
         }
-        rec->curve[c] = v;
+        a.rec->cnt[6 + c][b] = v;
     } else if (f == kPgFields) {
-        rec->status = *blk_status;
+        a.rec->status[b] = *blk_status;
     }
 }
 
-// Packed-input variant of pg_fast: the curve bin from the bucket table (pk_curve).
-RL_DEVINL PgTok pg_fast_packed(float lt, float lo, float ls, float A, const PgPrep& q, const int* lut, const float* eps,
-                               const float* weps);
 
 // Stages of kPgStageSlots slots are dealt round-robin to the blocks (block b takes stages
 // b, b + nb, b + 2 nb, ... with nb odd, so a block's stages walk through every phase of a
@@ -727,34 +719,25 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
 // (two eps inside, or an eps whose band reaches into the bucket).
 constexpr int kPkStage = 1024;                 // tokens per stage
 constexpr int kPkDepth = 5;                    // stages in the ring
-constexpr int kPkLut = 1024;                   // buckets of |p_old - p_samp| over [0, 1]
 struct alignas(16) PkStage {
     float lt[kPkStage], lo[kPkStage], ls[kPkStage], A[kPkStage];
 };
 constexpr int kPkSmem = kPkDepth * static_cast<int>(sizeof(PkStage));
 
-// Curve bin and band of one |p_old - p_samp| value from the bucket table.
-RL_DEVINL void pk_curve(float adiff, const int* lut, const float* eps, const float* weps, int n, int& j, bool& band) {
+// Curve bin of one |p_old - p_samp| value from the bucket table (in shared memory), and
+// whether it lies in the band of a curve eps (or its bucket needs the exact path: two eps
+// inside it, or an eps whose band reaches into it).  Branch-free.
+RL_DEVINL void pk_curve(float adiff, const int* lut, const float* eps_s, const float* weps_s, int& j, bool& band) {
     int b = static_cast<int>(adiff * static_cast<float>(kPkLut));   // exact scaling: bucket edges are exact
     b = b < 0 ? 0 : (b > kPkLut - 1 ? kPkLut - 1 : b);
     const int e = lut[b];
-    j = e & 31;
     const int kin = (e >> 8) & 31;
-    if (kin) {
-        j += adiff > eps[kin - 1] ? 1 : 0;
-        band = band | (fabsf(adiff - eps[kin - 1]) <= weps[kin - 1]);
-    }
-    if (e >> 16) {   // the full search
-        j = 0;
-        for (int k = 0; k < n; ++k) {
-            j += adiff > eps[k] ? 1 : 0;
-            band = band | (fabsf(adiff - eps[k]) <= weps[k]);
-        }
-    }
+    j = (e & 31) + (adiff > eps_s[kin] ? 1 : 0);
+    band = band | (fabsf(adiff - eps_s[kin]) <= weps_s[kin]) | ((e >> 16) != 0);
 }
 
-RL_DEVINL PgTok pg_fast_packed(float lt, float lo, float ls, float A, const PgPrep& q, const int* lut, const float* eps,
-                               const float* weps) {
+RL_DEVINL PgTok pg_fast_packed(float lt, float lo, float ls, float A, const PgPrep& q, const int* lut,
+                               const float* eps_s, const float* weps_s) {
     PgTok o;
     const float r = exp_fast(lt - lo);
     const float l1 = -A * r;
@@ -768,7 +751,7 @@ RL_DEVINL PgTok pg_fast_packed(float lt, float lo, float ls, float A, const PgPr
                 ((A > 0.f) & (fabsf(r - q.hi_b) <= q.w_hi_b)) | (fabsf(rho_raw - q.tis) <= q.w_tis) |
                 (fabsf(rho_raw - q.ice_lo) <= q.w_ice_lo) | (fabsf(rho_raw - q.ice_hi) <= q.w_ice_hi);
     int j;
-    pk_curve(adiff, lut, eps, weps, q.n, j, band);
+    pk_curve(adiff, lut, eps_s, weps_s, j, band);
     const bool dual = (A < 0.f) & (r > q.cc);   // on the ratio, as in pg_token
     const bool clip = ((A > 0.f) & (r > q.hi_b)) | ((A < 0.f) & (r < q.lo_b));
     const float loss_ppo = dual ? l3 : lc;
@@ -801,7 +784,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
     __shared__ __align__(8) uint64_t empty[kPkDepth];
     __shared__ int hist_s[kPgBins * kPgThreads];   // bin-major: thread t's bin b at b * 256 + t
     __shared__ int lut[kPkLut];
-    __shared__ float s_eps[RL_PG_MAX_CURVE], s_weps[RL_PG_MAX_CURVE];
+    __shared__ float s_eps[RL_PG_MAX_CURVE + 1], s_weps[RL_PG_MAX_CURVE + 1];
     __shared__ int abort_flag;
     __shared__ int32_t blk_status;
 
@@ -826,29 +809,11 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
     }
     if (consumer) {
         for (int b = 0; b <= q.n; ++b) hist_s[b * kPgThreads + threadIdx.x] = 0;
-        if (threadIdx.x < q.n) {
-            s_eps[threadIdx.x] = q.eps[threadIdx.x];
-            s_weps[threadIdx.x] = q.weps[threadIdx.x];
+        if (threadIdx.x <= RL_PG_MAX_CURVE) {
+            s_eps[threadIdx.x] = q.eps_s[threadIdx.x];
+            s_weps[threadIdx.x] = q.weps_s[threadIdx.x];
         }
-        for (int i = threadIdx.x; i < kPkLut; i += kPgThreads) {   // the bucket table
-            const float blo = static_cast<float>(i) / static_cast<float>(kPkLut);
-            const float bhi = static_cast<float>(i + 1) / static_cast<float>(kPkLut);
-            int below = 0, inside = 0, kin = 0, slow = 0;
-            for (int k = 0; k < q.n; ++k) {
-                const float e = q.eps[k];
-                if (e < blo) {
-                    ++below;
-                    slow |= (blo - e <= q.weps[k]);
-                } else if (e < bhi || i == kPkLut - 1) {
-                    ++inside;
-                    kin = k + 1;
-                } else {
-                    slow |= (e - bhi <= q.weps[k]);
-                }
-            }
-            slow |= inside > 1;
-            lut[i] = below | (kin << 8) | (slow << 16);
-        }
+        for (int i = threadIdx.x; i < kPkLut; i += kPgThreads) lut[i] = q.lut[i];
     }
     __syncthreads();
 
@@ -909,21 +874,28 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
                 const float vs[4] = {ls4.x, ls4.y, ls4.z, ls4.w}, vA[4] = {A4.x, A4.y, A4.z, A4.w};
                 float lp[4], ld[4], gp[4], gd[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    PgTok t = pg_fast_packed(vt[u], vo[u], vs[u], vA[u], q, lut, s_eps, s_weps);
-                    if (t.band) pg_resolve(t, vt[u], vo[u], vs[u], vA[u], q);
-                    lp[u] = t.lp;
-                    ld[u] = t.ld;
-                    gp[u] = t.gp;
-                    gd[u] = t.gd;
+                for (int u = 0; u < 4; u += 2) {   // two tokens at a time: two independent chains, no branch
+                    PgTok t[2] = {pg_fast_packed(vt[u], vo[u], vs[u], vA[u], q, lut, s_eps, s_weps),
+                                  pg_fast_packed(vt[u + 1], vo[u + 1], vs[u + 1], vA[u + 1], q, lut, s_eps, s_weps)};
+                    if (t[0].band | t[1].band) {   // rare: re-decide exactly
+                        if (t[0].band) pg_resolve(t[0], vt[u], vo[u], vs[u], vA[u], q);
+                        if (t[1].band) pg_resolve(t[1], vt[u + 1], vo[u + 1], vs[u + 1], vA[u + 1], q);
+                    }
 #pragma unroll
-                    for (int k = 0; k < kPgSums; ++k) acc.sum[k] += t.s[k];
-                    acc.cnt[1] += t.clip;
-                    acc.cnt[2] += t.dual;
-                    acc.cnt[3] += t.ice_lo;
-                    acc.cnt[4] += t.ice_hi;
-                    acc.cnt[5] += t.tis;
-                    hist[t.j * kPgThreads] += 1;
+                    for (int h = 0; h < 2; ++h) {
+                        lp[u + h] = t[h].lp;
+                        ld[u + h] = t[h].ld;
+                        gp[u + h] = t[h].gp;
+                        gd[u + h] = t[h].gd;
+#pragma unroll
+                        for (int k = 0; k < kPgSums; ++k) acc.sum[k] += t[h].s[k];
+                        acc.cnt[1] += t[h].clip;
+                        acc.cnt[2] += t[h].dual;
+                        acc.cnt[3] += t[h].ice_lo;
+                        acc.cnt[4] += t[h].ice_hi;
+                        acc.cnt[5] += t[h].tis;
+                        hist[t[h].j * kPgThreads] += 1;
+                    }
                 }
                 acc.cnt[0] += 4;
                 if (a.loss_ppo) __stcs(reinterpret_cast<float4*>(a.loss_ppo + g + j4), make_float4(lp[0], lp[1], lp[2], lp[3]));
@@ -958,12 +930,11 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
 // Host side
 // ----------------------------------------------------------------------------------
 // Workspace: a 256-byte header (the arrival counter at byte 0: zero before the first call,
-// and the last block of every call leaves it zero), then one 128-byte partial record per
-// block.  At most kPgMaxBlocks blocks run (fewer than two per SM on a part with
+// and the last block of every call leaves it zero), then the blocks' partial records
+// (PgRecords, 29 words per block, field-major).  At most kPgMaxBlocks blocks run (fewer than two per SM on a part with
 // more than 256 SMs), so the workspace size does not depend on the device.
-constexpr int kPgMaxBlocks = 512;
 constexpr size_t kPgHeader = 256;
-static_assert(kPgHeader + kPgMaxBlocks * sizeof(PgSlot) == kPolicyWorkspaceBytes, "workspace layout");
+static_assert(kPgHeader + sizeof(PgRecords) <= kPolicyWorkspaceBytes, "workspace layout");
 
 static int fast_blocks(int sms) {   // odd: see policy_fast_kernel
     const int n = sms * kPgFastPerSm - 1;
@@ -1014,6 +985,33 @@ static PgPrep prepare(const rl_pg_params& p) {
         q.eps[k] = p.curve_eps[q.perm[k]];
         q.weps[k] = band(q.eps[k]);
     }
+    // the packed pass's bucket table over |p_old - p_samp| in [0, 1]: bucket b holds
+    // [b / kPkLut, (b + 1) / kPkLut) (the last one up to 1 inclusive)
+    q.eps_s[0] = INFINITY;
+    q.weps_s[0] = -1.f;
+    for (int k = 0; k < q.n; ++k) {
+        q.eps_s[k + 1] = q.eps[k];
+        q.weps_s[k + 1] = q.weps[k];
+    }
+    for (int b = 0; b < kPkLut; ++b) {
+        const float blo = static_cast<float>(b) / static_cast<float>(kPkLut);
+        const float bhi = static_cast<float>(b + 1) / static_cast<float>(kPkLut);
+        int below = 0, inside = 0, kin = 0, slow = 0;
+        for (int k = 0; k < q.n; ++k) {
+            const float e = q.eps[k];
+            if (e < blo) {
+                ++below;
+                slow |= blo - e <= q.weps[k];
+            } else if (e < bhi || b == kPkLut - 1) {
+                ++inside;
+                kin = k + 1;
+            } else {
+                slow |= e - bhi <= q.weps[k];
+            }
+        }
+        slow |= inside > 1;
+        q.lut[b] = below | (kin << 8) | (slow << 16);
+    }
     return q;
 }
 
@@ -1040,7 +1038,7 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
     a.grad_ppo = grad_ppo;
     a.grad_dec = grad_dec;
     a.arrive = static_cast<unsigned int*>(ws);
-    a.slots = reinterpret_cast<PgSlot*>(static_cast<uint8_t*>(ws) + kPgHeader);
+    a.rec = reinterpret_cast<PgRecords*>(static_cast<uint8_t*>(ws) + kPgHeader);
     a.metrics = metrics;
     a.wait_ns = wait_limit_ns();
     // per device: the fast pass's shared-memory opt-in (set once; concurrent first calls

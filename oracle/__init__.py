@@ -24,7 +24,7 @@ differences, except the items listed in ``PARITY_UNPINNED``.
 """
 from .rl_head import (HeadParams, LOSS_IPO, LOSS_ICEPOP, LOSS_REINFORCE, KL_EXACT, KL_K1,
                       STALE_NONE, STALE_INV_SQRT, head_forward, head_backward, head_loss_total,
-                      head_token_logits, token_forward, validate_support)
+                      head_token_logits, token_forward, validate_support, vocab_shard_stats)
 from .policy import PolicyParams, policy_loss_elementwise, IPO_CURVE_EPS
 from .rollout import RolloutParams, rollout_correction, rollout_metrics_named
 
@@ -37,6 +37,6 @@ PARITY_UNPINNED = (
 __all__ = [
     "HeadParams", "LOSS_IPO", "LOSS_ICEPOP", "LOSS_REINFORCE", "KL_EXACT", "KL_K1", "STALE_NONE",
     "STALE_INV_SQRT", "head_forward", "head_backward", "head_loss_total", "head_token_logits",
-    "token_forward", "validate_support", "PolicyParams", "policy_loss_elementwise", "IPO_CURVE_EPS", "PARITY_UNPINNED",
+    "token_forward", "validate_support", "vocab_shard_stats", "PolicyParams", "policy_loss_elementwise", "IPO_CURVE_EPS", "PARITY_UNPINNED",
     "RolloutParams", "rollout_correction", "rollout_metrics_named",
 ]

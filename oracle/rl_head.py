@@ -359,13 +359,15 @@ def head_forward(inputs: dict, p: HeadParams, rows=None, chunk: int = 64) -> dic
 
 def head_backward(inputs: dict, p: HeadParams, dloss: np.ndarray, chunk: int = 64,
                   rows=None, want_dW: bool = True, want_bounds: bool = False, want_dX: bool = True,
-                  vrows=None):
+                  vrows=None, vcols=None):
     """dX [N,H] and dW [V,H] of sum_t dloss_t * loss_t, fp64, by the chain rule:
     G_tj = dloss_t / T * d loss_t / d z_tj;  dX = G W;  dW = G^T X.
 
     ``rows`` restricts dX to those tokens (dW then sums over those tokens only).
     ``vrows`` keeps only those vocabulary rows of dW (in that order); ``want_dX=False``
-    skips dX (and its bounds), returning None for it.
+    skips dX (and its bounds), returning None for it; ``vcols`` restricts dX to the part
+    that flows through those vocabulary ids, G[:, vcols] W[vcols] (one rank's share when W
+    is split by vocabulary).
     ``want_bounds`` also returns the magnitudes a finite-precision evaluation is measured
     against, as a dict: ``X`` = |G| |W| and ``W`` = |G|^T |X| with |G| the sum of the
     magnitudes of the terms forming each G entry, and ``zX`` / ``zW`` the same products
@@ -413,7 +415,11 @@ def head_backward(inputs: dict, p: HeadParams, dloss: np.ndarray, chunk: int = 6
             else:
                 G[j] = scale * res
         if want_dX:
-            dX[c0:c0 + rr.shape[0]] = G @ W
+            if vcols is None:
+                dX[c0:c0 + rr.shape[0]] = G @ W
+            else:
+                vc = np.asarray(vcols, dtype=np.int64)
+                dX[c0:c0 + rr.shape[0]] = G[:, vc] @ W[vc]
         if want_dW:
             dW += G[:, vsel].T @ Xall[rr]
         if want_bounds:
@@ -446,3 +452,29 @@ def head_loss_total(inputs: dict, p: HeadParams, dloss: np.ndarray, frozen=None)
                            w_frozen=None if frozen is None else frozen[t])
         tot += float(dloss[t]) * fw["loss"]
     return tot
+
+
+def vocab_shard_stats(inputs: dict, p: HeadParams, v0: int, v1: int) -> dict:
+    """Per-token statistics of the logits over the vocabulary columns [v0, v1) alone (one
+    rank's rows of W when the head is split by vocabulary), fp64, from their definitions:
+    m = max_j z_j, s = sum_j e^(z_j - m), u = sum_j e^(z_j - m) (z_j - m) over the range;
+    and the label / support logits whose id lies in the range (0 for the others).
+    Combined over the ranges (logsumexp = M + log sum_r s_r e^(m_r - M)) they give the
+    full-vocabulary logsumexp and entropy of head_forward."""
+    off = _rows(inputs)
+    N = off.shape[0] - 1
+    W = np.asarray(inputs["W"], dtype=np.float64)[v0:v1]
+    X = np.asarray(inputs["hidden"], dtype=np.float64)
+    Z = (X @ W.T) / p.temperature
+    m = Z.max(axis=1)
+    e = np.exp(Z - m[:, None])
+    s = e.sum(axis=1)
+    u = (e * (Z - m[:, None])).sum(axis=1)
+    labels = np.asarray(inputs["labels"], dtype=np.int64)
+    ids = np.asarray(inputs["ids"], dtype=np.int64)
+    rows = np.repeat(np.arange(N), np.diff(off))
+    own_l = (labels >= v0) & (labels < v1)
+    own_s = (ids >= v0) & (ids < v1)
+    zlab = np.where(own_l, Z[np.arange(N), np.clip(labels - v0, 0, v1 - v0 - 1)], 0.0)
+    zsup = np.where(own_s, Z[rows, np.clip(ids - v0, 0, v1 - v0 - 1)], 0.0)
+    return dict(m=m, s=s, u=u, zlab=zlab, zsup=zsup)

@@ -572,3 +572,27 @@ def test_validation_accepts_a_clean_batch_and_names_each_fault():
              logq=np.concatenate([inp["logq"][:8], inp["logq"][14:]]))
     assert check(e) == S.STATUS_EMPTY_ROW
     assert check(dict(e, loss_mask=np.array([1, 0, 1, 1], np.uint8))) == 0
+
+
+def test_vocab_shard_statistics_combine_to_the_full_vocabulary():
+    """Split by vocabulary into three ranges, the shard statistics combine (max shift, sum)
+    to the full logsumexp and entropy of the plain forward, and every label / support
+    logit is owned by exactly one shard."""
+    rng = np.random.default_rng(24)
+    V = 40
+    z = rng.normal(0, 2.0, size=(5, V))
+    sup = [(sorted(rng.choice(V, 6, replace=False).tolist()), list(np.log(np.full(6, 1 / 6)))) for _ in range(5)]
+    inp = identity_case(z, [3, 11, 25, 39, 0], [math.log(0.1)] * 5, sup, [0] * 5)
+    p = HeadParams()
+    full = oracle.head_forward(inp, p)
+    parts = [oracle.vocab_shard_stats(inp, p, a, b) for a, b in ((0, 16), (16, 32), (32, 40))]
+    M = np.max([q["m"] for q in parts], axis=0)
+    S = sum(q["s"] * np.exp(q["m"] - M) for q in parts)
+    U = sum((q["u"] + q["s"] * (q["m"] - M)) * np.exp(q["m"] - M) for q in parts)
+    lse = M + np.log(S)
+    np.testing.assert_allclose(lse, full["lse"], rtol=1e-13)
+    np.testing.assert_allclose(np.log(S) - U / S, full["entropy"], rtol=1e-12, atol=1e-12)
+    zlab = sum(q["zlab"] for q in parts)
+    np.testing.assert_allclose(zlab - lse, full["logp_label"], rtol=1e-12, atol=1e-12)
+    zsup = sum(q["zsup"] for q in parts)
+    np.testing.assert_allclose(zsup, z[np.repeat(np.arange(5), 6), inp["ids"]], rtol=0, atol=0)
