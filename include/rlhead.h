@@ -283,7 +283,7 @@ typedef struct rl_pg_metrics {
 } rl_pg_metrics;
 
 /* Workspace bytes for T tokens: 65,792 (an arrival counter and one 128-byte partial record
- * per block of the pass), for any T and device.  The argument stays so that callers need
+ * per block of the pass; the workspace 16-byte aligned), for any T and device.  The argument stays so that callers need
  * not change if a later layout depends on T.  Zero the workspace once before its first
  * use (a cudaMemset when it is allocated): every call is one kernel launch whose last
  * block leaves the arrival counter at zero again, so later calls need no clearing.  Calls

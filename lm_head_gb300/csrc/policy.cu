@@ -100,15 +100,20 @@ struct PgArgs {
     rl_pg_metrics* metrics;       // or nullptr
 };
 
-// The blocks' partials, field-major (field f of block b at [f][b], so the last block reads
-// each field's column with coalesced loads): fp32 sums in each block's fixed order, counts
-// (the curve in the caller's order), the RL_STATUS_* bits the block's waits raised.
+// A block's partial, one 128-byte record per block (the last block loads them 16 bytes at
+// a time): fp32 sums in the block's fixed order, counts (the curve in the caller's order),
+// the RL_STATUS_* bits the block's waits raised.
 constexpr int kPgRecFields = kPgSums + 6 + RL_PG_MAX_CURVE + 1;   // + status
 constexpr int kPgMaxBlocks = 512;
+struct alignas(16) PgRecord {
+    float sum[kPgSums];
+    int cnt[6 + RL_PG_MAX_CURVE];
+    int status;
+    int pad[3];
+};
+static_assert(sizeof(PgRecord) == 128, "one record per 128 bytes");
 struct PgRecords {
-    float sum[kPgSums][kPgMaxBlocks];
-    int cnt[6 + RL_PG_MAX_CURVE][kPgMaxBlocks];
-    int status[kPgMaxBlocks];
+    PgRecord r[kPgMaxBlocks];
 };
 
 struct PgAcc {
@@ -299,46 +304,77 @@ RL_DEVINL void pg_write_metric(int k, double s, rl_pg_metrics* out) {
 // ----------------------------------------------------------------------------------
 // Batch totals
 // ----------------------------------------------------------------------------------
-// The last block: thread (f, g) of the first 29 x 9 sums field f over the blocks g, g + 9,
-// g + 18, ... (all its loads in flight at once; fp64 for the six sums, few enough not to
-// matter on this part's slow fp64 pipe, integers for the counts, OR for the status bits),
-// then thread f adds its field's nine group totals in order.  Fixed order throughout.
-RL_DEVINL void pg_final(const PgArgs& a) {
-    constexpr int kG = 9;
-    constexpr int kPer = (kPgMaxBlocks + kG - 1) / kG;
-    __shared__ double part_s[kPgSums][kG];
-    __shared__ int part_c[kPgRecFields - kPgSums][kG];
+// The last block.  The records come into shared memory (`scratch`, the block's stage ring,
+// idle by now; cap_bytes of it) 16 bytes per load, all loads of a chunk in flight at once;
+// then thread (f, g), f < 29, g < 9 (8 in a 256-thread block), adds field f of the staged
+// records g, g + 9, g + 18, ... (the sums as float-float pairs, about 44 significant bits, the counts as integers,
+// the status bits OR-ed), and thread f adds its field's nine group totals in order.  With
+// no scratch (the slow pass) the records are read from global memory directly.  Fixed
+// order throughout, whatever order the blocks arrived in.
+RL_DEVINL void pg_final(const PgArgs& a, uint8_t* scratch, int cap_bytes) {
+    constexpr int kGMax = 9;
+    __shared__ FF part_s[kPgSums][kGMax];
+    __shared__ int part_c[kPgRecFields - kPgSums][kGMax];
+    // groups per field: 9 with 288 threads (the streaming passes), 8 with 256 (the slow pass)
+    const int kG = static_cast<int>(blockDim.x) / kPgRecFields < kGMax ? static_cast<int>(blockDim.x) / kPgRecFields
+                                                                       : kGMax;
     const int tid = threadIdx.x;
-    for (int idx = tid; idx < kPgRecFields * kG; idx += blockDim.x) {   // one round for 288 threads
-        const int f = idx / kG, g = idx - (idx / kG) * kG;
-        if (f < kPgSums) {
-            const float* col = a.rec->sum[f];
-            float x[kPer];
+    FF vs = {0.f, 0.f};
+    int vc = 0;
+    const int chunk = scratch ? cap_bytes / static_cast<int>(sizeof(PgRecord)) : a.nb;
+    for (int c0 = 0; c0 < a.nb; c0 += chunk) {
+        const int n = a.nb - c0 < chunk ? a.nb - c0 : chunk;
+        const PgRecord* src = a.rec->r + c0;
+        if (scratch) {
+            // nine loads of each thread in flight before its first store: one L2 round trip
+            // per 9 x blockDim 16-byte pieces (303 records of 128 bytes: one round), not one
+            // per load
+            const uint4* g4 = reinterpret_cast<const uint4*>(src);
+            uint4* s4 = reinterpret_cast<uint4*>(scratch);
+            constexpr int kPer = 9;
+            const int step = kPer * static_cast<int>(blockDim.x);
+            for (int base = 0; base < n * 8; base += step) {
+                uint4 v[kPer];
 #pragma unroll
-            for (int i = 0; i < kPer; ++i) x[i] = g + kG * i < a.nb ? __ldcg(col + g + kG * i) : 0.f;
-            double v = 0.0;
+                for (int k = 0; k < kPer; ++k) {
+                    const int i = base + tid + k * static_cast<int>(blockDim.x);
+                    if (i < n * 8) v[k] = __ldcg(g4 + i);
+                }
 #pragma unroll
-            for (int i = 0; i < kPer; ++i) v += static_cast<double>(x[i]);
-            part_s[f][g] = v;
-        } else {
-            const bool is_status = f == kPgRecFields - 1;
-            const int* col = is_status ? a.rec->status : a.rec->cnt[f - kPgSums];
-            int x[kPer];
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) x[i] = g + kG * i < a.nb ? __ldcg(col + g + kG * i) : 0;
-            int v = 0;
-#pragma unroll
-            for (int i = 0; i < kPer; ++i) v = is_status ? (v | x[i]) : v + x[i];
-            part_c[f - kPgSums][g] = v;
+                for (int k = 0; k < kPer; ++k) {
+                    const int i = base + tid + k * static_cast<int>(blockDim.x);
+                    if (i < n * 8) s4[i] = v[k];
+                }
+            }
+            __syncthreads();
+            src = reinterpret_cast<const PgRecord*>(scratch);
         }
+        if (tid < kPgRecFields * kG) {
+            const int f = tid / kG, g = tid - (tid / kG) * kG;
+            if (f < kPgSums) {
+                for (int b = g; b < n; b += kG) vs = ff_add(vs, {scratch ? src[b].sum[f] : __ldcg(&src[b].sum[f]), 0.f});
+            } else if (f < kPgRecFields - 1) {
+                for (int b = g; b < n; b += kG) vc += scratch ? src[b].cnt[f - kPgSums] : __ldcg(&src[b].cnt[f - kPgSums]);
+            } else {
+                for (int b = g; b < n; b += kG) vc |= scratch ? src[b].status : __ldcg(&src[b].status);
+            }
+        }
+        __syncthreads();   // the chunk is read before the next one overwrites it
+    }
+    if (tid < kPgRecFields * kG) {
+        const int f = tid / kG, g = tid - (tid / kG) * kG;
+        if (f < kPgSums)
+            part_s[f][g] = vs;
+        else
+            part_c[f - kPgSums][g] = vc;
     }
     __syncthreads();
     if (tid == 0) *a.arrive = 0u;   // every block has arrived: ready for the next call
     if (!a.metrics || tid >= kPgRecFields) return;
     if (tid < kPgSums) {
-        double v = 0.0;
-        for (int g = 0; g < kG; ++g) v += part_s[tid][g];
-        pg_write_metric(tid, v, a.metrics);
+        FF v = part_s[tid][0];
+        for (int g = 1; g < kG; ++g) v = ff_add(v, part_s[tid][g]);
+        pg_write_metric(tid, static_cast<double>(v.hi) + static_cast<double>(v.lo), a.metrics);
     } else if (tid < kPgRecFields - 1) {
         int v = 0;
         for (int g = 0; g < kG; ++g) v += part_c[tid - kPgSums][g];
@@ -352,7 +388,7 @@ RL_DEVINL void pg_final(const PgArgs& a) {
 
 // Every thread of every block calls this after the block's record is written; the last
 // block to arrive finishes.
-RL_DEVINL void pg_finish(const PgArgs& a) {
+RL_DEVINL void pg_finish(const PgArgs& a, uint8_t* scratch, int cap_bytes) {
     __shared__ int last;
     __threadfence();   // this block's record (and outputs) before its arrival
     __syncthreads();
@@ -360,7 +396,7 @@ RL_DEVINL void pg_finish(const PgArgs& a) {
     __syncthreads();
     if (!last) return;
     __threadfence();
-    pg_final(a);
+    pg_final(a, scratch, cap_bytes);
 }
 
 // ----------------------------------------------------------------------------------
@@ -375,13 +411,14 @@ __global__ void __launch_bounds__(kPgThreads, kPgSlowPerSm) policy_slow_kernel(P
     __shared__ int cnts[kPgCounts];
     pg_block_reduce(acc, sums, cnts);
     const int k = threadIdx.x;
+    PgRecord& rec = a.rec->r[blockIdx.x];
     if (k < kPgSums)
-        a.rec->sum[k][blockIdx.x] = sums[k];
+        rec.sum[k] = sums[k];
     else if (k < kPgFields)
-        a.rec->cnt[k - kPgSums][blockIdx.x] = cnts[k - kPgSums];
+        rec.cnt[k - kPgSums] = cnts[k - kPgSums];
     else if (k == kPgFields)
-        a.rec->status[blockIdx.x] = 0;
-    pg_finish(a);
+        rec.status = 0;
+    pg_finish(a, nullptr, 0);
 }
 
 // ----------------------------------------------------------------------------------
@@ -538,15 +575,15 @@ RL_DEVINL void pg_block_record(const PgArgs& a, const PgFastAcc& acc, const int*
         }
     __syncthreads();
     const int f = threadIdx.x;
-    const int b = blockIdx.x;
+    PgRecord& rec = a.rec->r[blockIdx.x];
     if (f < kPgSums) {
         float v = 0.f;
         for (int w = 0; w < kPgThreads / 32; ++w) v += shs[w][f];
-        a.rec->sum[f][b] = v;
+        rec.sum[f] = v;
     } else if (f < kPgSums + 6) {
         int v = 0;
         for (int w = 0; w < kPgThreads / 32; ++w) v += shc[w][f - kPgSums];
-        a.rec->cnt[f - kPgSums][b] = v;
+        rec.cnt[f - kPgSums] = v;
     } else if (f < kPgFields) {
         const int c = f - kPgSums - 6;        // caller's curve index
         int v = 0;
@@ -555,9 +592,9 @@ RL_DEVINL void pg_block_record(const PgArgs& a, const PgFastAcc& acc, const int*
             while (a.q.perm[js] != c) ++js;
             for (int k = js + 1; k <= a.q.n; ++k) v += bins[k];
         }
-        a.rec->cnt[6 + c][b] = v;
+        rec.cnt[6 + c] = v;
     } else if (f == kPgFields) {
-        a.rec->status[b] = *blk_status;
+        rec.status = *blk_status;
     }
 }
 
@@ -702,7 +739,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
         }
     }
     pg_block_record(a, acc, hist_s, &blk_status);
-    pg_finish(a);
+    pg_finish(a, pg_smem, kPgStreamSmem);   // the ring is idle now: scratch for the last block
 }
 
 // ----------------------------------------------------------------------------------
@@ -923,7 +960,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
         }
     }
     pg_block_record(a, acc, hist_s, &blk_status);
-    pg_finish(a);
+    pg_finish(a, pk_smem, kPkSmem);   // the ring is idle now: scratch for the last block
 }
 
 // ----------------------------------------------------------------------------------
@@ -931,7 +968,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
 // ----------------------------------------------------------------------------------
 // Workspace: a 256-byte header (the arrival counter at byte 0: zero before the first call,
 // and the last block of every call leaves it zero), then the blocks' partial records
-// (PgRecords, 29 words per block, field-major).  At most kPgMaxBlocks blocks run (fewer than two per SM on a part with
+// (PgRecords, one 128-byte record per block).  At most kPgMaxBlocks blocks run (fewer than two per SM on a part with
 // more than 256 SMs), so the workspace size does not depend on the device.
 constexpr size_t kPgHeader = 256;
 static_assert(kPgHeader + sizeof(PgRecords) <= kPolicyWorkspaceBytes, "workspace layout");
@@ -1021,6 +1058,10 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
                 void* ws, size_t ws_bytes, cudaStream_t stream) {
     const int sms = num_sms();
     if (ws_bytes < policy_ws_bytes(T)) return RL_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 15u) != 0) {
+        set_last_error("workspace not 16-byte aligned");
+        return RL_ERR_ARG;
+    }
     auto al = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
     const bool fast = T < (int64_t(1) << 31) && al(lt) && al(lo) && al(ls) && al(adv) && al(mask) &&
                       al(loss_ppo) && al(loss_dec) && al(grad_ppo) && al(grad_dec);
@@ -1038,7 +1079,7 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
     a.grad_ppo = grad_ppo;
     a.grad_dec = grad_dec;
     a.arrive = static_cast<unsigned int*>(ws);
-    a.rec = reinterpret_cast<PgRecords*>(static_cast<uint8_t*>(ws) + kPgHeader);
+    a.rec = reinterpret_cast<PgRecords*>(static_cast<uint8_t*>(ws) + kPgHeader);   // 16-byte aligned
     a.metrics = metrics;
     a.wait_ns = wait_limit_ns();
     // per device: the fast pass's shared-memory opt-in (set once; concurrent first calls
