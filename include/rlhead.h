@@ -282,12 +282,13 @@ typedef struct rl_pg_metrics {
                                     out (the outputs and metrics are then incomplete) */
 } rl_pg_metrics;
 
-/* Workspace bytes for T tokens: 65,792 (an arrival counter and one 128-byte partial record
- * per block of the pass; the workspace 16-byte aligned), for any T and device.  The argument stays so that callers need
- * not change if a later layout depends on T.  Zero the workspace once before its first
- * use (a cudaMemset when it is allocated): every call is one kernel launch whose last
- * block leaves the arrival counter at zero again, so later calls need no clearing.  Calls
- * that overlap on the GPU must not share a workspace. */
+/* Workspace bytes for T tokens: 4096 (an arrival counter, a status word, a range flag, a
+ * stage-claim counter and the batch's metric accumulators, one 128-byte line each; the
+ * workspace 8-byte aligned), for any T and device.  The argument stays so that callers
+ * need not change if a later layout depends on T.  Zero the workspace once before its
+ * first use (a cudaMemset when it is allocated): every call is one kernel launch whose
+ * last block sets all of it back to zero, so later calls need no clearing.  Calls that
+ * overlap on the GPU must not share a workspace. */
 size_t rl_policy_workspace_bytes(int64_t T);
 /* All arrays device [T] fp32 (mask uint8, 1 = valid response token; any nonzero byte
  * counts as valid).  A masked slot's inputs are never used, whatever they hold (NaN and
@@ -307,14 +308,14 @@ int rl_policy_loss_elementwise(const float* lp_theta, const float* lp_old, const
  * trainer or inference engine whose device memory is reserved up front by its own pool,
  * where an extra cudaMalloc would fail or compete with that pool, or plain C code with
  * no device allocator at hand.  This variant takes no workspace and allocates nothing:
- * its scratch (the arrival counter and the blocks' partial records) is a file-scope
- * device array of 65,792 bytes, the size rl_policy_workspace_bytes returns.
+ * its scratch (the counters, flags and metric accumulators) is a file-scope device
+ * array of 4096 bytes, the size rl_policy_workspace_bytes returns.
  *   - Every GPU that loads the library holds that array until the process exits.
  *   - The first call on a device looks the array's device address up (once per
  *     device); make that first call before any stream capture.
  *   - All calls share the one array and it keeps the last call's contents.  The array
- *     starts at zero when the library is loaded; every block of a call writes its own
- *     record before the last block reads it, and that last block sets the arrival counter
+ *     starts at zero when the library is loaded; every block of a call adds its partial
+ *     before the last block reads the totals, and that last block sets the whole array
  *     back to zero, so each call leaves the array ready for the next.  Calls one after
  *     another on one stream are therefore safe; calls that overlap on the GPU (other
  *     streams, other threads) race on the array: serialise them.

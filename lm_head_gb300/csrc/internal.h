@@ -141,8 +141,9 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
                 float* loss_dec, float* grad_ppo, float* grad_dec, rl_pg_metrics* metrics,
                 void* ws, size_t ws_bytes, cudaStream_t stream);
 size_t policy_ws_bytes(int64_t T);
-// The elementwise pass's workspace: a 256-byte header and 512 per-block records of 128 bytes.
-constexpr size_t kPolicyWorkspaceBytes = 256 + 512 * 128;
+// The elementwise pass's workspace: counters, flags and the metric accumulators (one
+// 128-byte line each).
+constexpr size_t kPolicyWorkspaceBytes = 4096;
 int rollout_impl(const float* lt, const float* lr, const uint8_t* mask, const int64_t* off, int64_t B, int64_t T,
                  const rl_rc_params* p, float* w, uint8_t* keep, rl_rc_metrics* metrics, void* ws,
                  size_t ws_bytes, cudaStream_t stream);

@@ -23,23 +23,31 @@
 //                          over the sorted eps (binary search; only the two neighbouring
 //                          eps are band-checked).  A token inside a band is re-decided
 //                          exactly by the thread that met it.
-//  1'. policy_packed_kernel the same pass for packed input (no mask): an equal contiguous
-//                          range per block, four tokens per thread, no selects, the curve
-//                          bin from a bucket table.
+//  1'. policy_packed_kernel the same pass for packed input (no mask): 1024-token stages,
+//                          the first few dealt round-robin and the rest claimed by the
+//                          blocks as they free a ring slot (so blocks on faster SMs take
+//                          more), four tokens per thread, no selects, the curve bin from
+//                          a bucket table.
 //  2. policy_slow_kernel   the whole pass with exact decisions in the bands, for inputs the
 //                          fast passes do not take (unaligned, T >= 2^31).
 //  With no mask (packed input: every slot a valid token) the mask is neither read nor
 //  copied: 16 bytes in per token instead of 17.
-//  Each block writes its partial (fp32 sums in a fixed order within the block, counts, the
-//  status bits of its waits) to its own record in the workspace; the last block to arrive
-//  (an arrival counter) sums the records in block order (fp64 sums, int64 counts), writes
-//  the metrics and sets the counter back to zero.  So a workspace zeroed once before its
-//  first use needs no clearing before later calls, and a call is one kernel launch.
+//  Each block adds its partial (fp32 sums in a fixed order within the block, then in 2^-24
+//  fixed point; counts) to the batch accumulators with integer atomics, whose total does
+//  not depend on the order of arrival.  In the packed pass a thread's fp32 sum over its
+//  four tokens of a stage goes into 2^-24 fixed point at once, so the totals do not depend
+//  on which block took the stage either.  The last block to arrive (an arrival counter)
+//  writes the metrics and sets every accumulator and the counter back to zero, so a
+//  workspace zeroed once before its first use needs no clearing before later calls and a
+//  call is one kernel launch.  The last block's code is kept short: it runs once, on one
+//  SM, with every instruction fetched cold.  If a block's sum was too large for the fixed
+//  point, that block redoes the whole batch's metrics with exact decisions (slow, correct).
 //
 // Results are bitwise reproducible for a given device and T.
 #include <atomic>
 #include <cmath>
 #include <climits>
+#include <cstddef>
 
 #include "common.cuh"
 #include "ff.cuh"
@@ -72,6 +80,7 @@ struct PgPrep {
     float eps[RL_PG_MAX_CURVE];
     float weps[RL_PG_MAX_CURVE];
     int perm[RL_PG_MAX_CURVE];
+    int pos[RL_PG_MAX_CURVE];   // inverse of perm: caller's index -> sorted position
     // the packed pass's bucket table: entry b = (eps below bucket b) | (1 + the one eps
     // inside it, sorted index; 0: none) << 8 | (1: take the exact path) << 16; eps_s / weps_s
     // are eps / weps shifted up by one, entry 0 a sentinel no value is above or near
@@ -93,28 +102,27 @@ struct PgArgs {
     float* loss_dec;
     float* grad_ppo;
     float* grad_dec;
-    struct PgRecords* rec;        // the blocks' partials
-    unsigned int* arrive;         // blocks of this launch that have written their record (0 between calls)
+    long long* acc;               // the batch's sums (2^-24 fixed point) and counts, kPgAccStride apart
+    int* range;                   // set when a sum term is too large for the fixed point
+    float range_lim;              // |term| bound that keeps every accumulator inside int64
+    int32_t* status;              // RL_STATUS_* bits of this call's waits
+    unsigned int* arrive;         // blocks of this launch that have added their partial (0 between calls)
+    unsigned int* claim;          // stages claimed past the round-robin ones (packed pass; 0 between calls)
     int nb;                       // blocks of the pass
+    int curve_bins;               // curve accumulators hold sorted-eps bins 1..n (streaming passes),
+                                  // else the curve counts in the caller's order
     uint64_t wait_ns;             // limit of the streaming loop's waits (RL_OPT_WAIT_LIMIT_US)
     rl_pg_metrics* metrics;       // or nullptr
 };
 
-// A block's partial, one 128-byte record per block (the last block loads them 16 bytes at
-// a time): fp32 sums in the block's fixed order, counts (the curve in the caller's order),
-// the RL_STATUS_* bits the block's waits raised.
-constexpr int kPgRecFields = kPgSums + 6 + RL_PG_MAX_CURVE + 1;   // + status
+constexpr float kPgFix = 16777216.f;   // 2^24: fixed-point scale of the metric sums
 constexpr int kPgMaxBlocks = 512;
-struct alignas(16) PgRecord {
-    float sum[kPgSums];
-    int cnt[6 + RL_PG_MAX_CURVE];
-    int status;
-    int pad[3];
-};
-static_assert(sizeof(PgRecord) == 128, "one record per 128 bytes");
-struct PgRecords {
-    PgRecord r[kPgMaxBlocks];
-};
+constexpr int kPgAccStride = 16;       // one 128-byte line per accumulator: the blocks' atomics spread over L2
+
+// The metrics struct read as 8-byte words: the sums (fp64) in field order, then the counts.
+static_assert(offsetof(rl_pg_metrics, n_valid) == 8 * kPgSums && offsetof(rl_pg_metrics, ipo_curve) == 8 * 12 &&
+                  offsetof(rl_pg_metrics, status) == 8 * kPgFields,
+              "rl_pg_metrics layout");
 
 struct PgAcc {
     float sum[kPgSums];
@@ -304,99 +312,89 @@ RL_DEVINL void pg_write_metric(int k, double s, rl_pg_metrics* out) {
 // ----------------------------------------------------------------------------------
 // Batch totals
 // ----------------------------------------------------------------------------------
-// The last block.  The records come into shared memory (`scratch`, the block's stage ring,
-// idle by now; cap_bytes of it) 16 bytes per load, all loads of a chunk in flight at once;
-// then thread (f, g), f < 29, g < 9 (8 in a 256-thread block), adds field f of the staged
-// records g, g + 9, g + 18, ... (the sums as float-float pairs, about 44 significant bits, the counts as integers,
-// the status bits OR-ed), and thread f adds its field's nine group totals in order.  With
-// no scratch (the slow pass) the records are read from global memory directly.  Fixed
-// order throughout, whatever order the blocks arrived in.
-RL_DEVINL void pg_final(const PgArgs& a, uint8_t* scratch, int cap_bytes) {
-    constexpr int kGMax = 9;
-    __shared__ FF part_s[kPgSums][kGMax];
-    __shared__ int part_c[kPgRecFields - kPgSums][kGMax];
-    // groups per field: 9 with 288 threads (the streaming passes), 8 with 256 (the slow pass)
-    const int kG = static_cast<int>(blockDim.x) / kPgRecFields < kGMax ? static_cast<int>(blockDim.x) / kPgRecFields
-                                                                       : kGMax;
-    const int tid = threadIdx.x;
-    FF vs = {0.f, 0.f};
-    int vc = 0;
-    const int chunk = scratch ? cap_bytes / static_cast<int>(sizeof(PgRecord)) : a.nb;
-    for (int c0 = 0; c0 < a.nb; c0 += chunk) {
-        const int n = a.nb - c0 < chunk ? a.nb - c0 : chunk;
-        const PgRecord* src = a.rec->r + c0;
-        if (scratch) {
-            // nine loads of each thread in flight before its first store: one L2 round trip
-            // per 9 x blockDim 16-byte pieces (303 records of 128 bytes: one round), not one
-            // per load
-            const uint4* g4 = reinterpret_cast<const uint4*>(src);
-            uint4* s4 = reinterpret_cast<uint4*>(scratch);
-            constexpr int kPer = 9;
-            const int step = kPer * static_cast<int>(blockDim.x);
-            for (int base = 0; base < n * 8; base += step) {
-                uint4 v[kPer];
-#pragma unroll
-                for (int k = 0; k < kPer; ++k) {
-                    const int i = base + tid + k * static_cast<int>(blockDim.x);
-                    if (i < n * 8) v[k] = __ldcg(g4 + i);
-                }
-#pragma unroll
-                for (int k = 0; k < kPer; ++k) {
-                    const int i = base + tid + k * static_cast<int>(blockDim.x);
-                    if (i < n * 8) s4[i] = v[k];
-                }
-            }
-            __syncthreads();
-            src = reinterpret_cast<const PgRecord*>(scratch);
-        }
-        if (tid < kPgRecFields * kG) {
-            const int f = tid / kG, g = tid - (tid / kG) * kG;
-            if (f < kPgSums) {
-                for (int b = g; b < n; b += kG) vs = ff_add(vs, {scratch ? src[b].sum[f] : __ldcg(&src[b].sum[f]), 0.f});
-            } else if (f < kPgRecFields - 1) {
-                for (int b = g; b < n; b += kG) vc += scratch ? src[b].cnt[f - kPgSums] : __ldcg(&src[b].cnt[f - kPgSums]);
-            } else {
-                for (int b = g; b < n; b += kG) vc |= scratch ? src[b].status : __ldcg(&src[b].status);
-            }
-        }
-        __syncthreads();   // the chunk is read before the next one overwrites it
-    }
-    if (tid < kPgRecFields * kG) {
-        const int f = tid / kG, g = tid - (tid / kG) * kG;
-        if (f < kPgSums)
-            part_s[f][g] = vs;
-        else
-            part_c[f - kPgSums][g] = vc;
-    }
-    __syncthreads();
-    if (tid == 0) *a.arrive = 0u;   // every block has arrived: ready for the next call
-    if (!a.metrics || tid >= kPgRecFields) return;
-    if (tid < kPgSums) {
-        FF v = part_s[tid][0];
-        for (int g = 1; g < kG; ++g) v = ff_add(v, part_s[tid][g]);
-        pg_write_metric(tid, static_cast<double>(v.hi) + static_cast<double>(v.lo), a.metrics);
-    } else if (tid < kPgRecFields - 1) {
-        int v = 0;
-        for (int g = 0; g < kG; ++g) v += part_c[tid - kPgSums][g];
-        pg_write_metric(tid, static_cast<double>(v), a.metrics);   // counts are exact integers
+// A sum term in 2^-24 fixed point, or 0 with the range flag raised when |v| is at or past
+// the bound that keeps the batch's accumulators inside int64 (or v is not finite).
+RL_DEVINL long long pg_fix(const PgArgs& a, float v) {
+    if (fabsf(v) < a.range_lim) return __float2ll_rn(v * kPgFix);
+    atomicOr(a.range, 1);
+    return 0;
+}
+
+// A block's partial goes into the batch accumulators with integer atomics (sums in 2^-24
+// fixed point, counts as they are): integer addition does not depend on the order the
+// blocks arrive in, so the totals are reproducible.
+RL_DEVINL void pg_add_partial(const PgArgs& a, int k, float sum, long long count) {
+    const long long x = k < kPgSums ? pg_fix(a, sum) + count : count;
+    if (x != 0)
+        atomicAdd(reinterpret_cast<unsigned long long*>(a.acc + k * kPgAccStride), static_cast<unsigned long long>(x));
+}
+
+// The last block of the pass to finish: the accumulators into the metrics (a streaming
+// pass's curve bins turned into the curve counts, cnt_c = the tokens in the bins above
+// eps_c's sorted position), then every accumulator, the flags and the counters back to
+// zero.  If a sum term was too large for the fixed point, the whole batch again with exact
+// decisions and fp32 sums instead (one block: slow, correct).  Called by every thread of
+// the block.
+RL_DEVINL void pg_final(const PgArgs& a) {
+    const int k = threadIdx.x;
+    __shared__ long long tot[kPgFields];
+    // the accumulators, the range flag and the status together (one round trip)
+    const long long mine =
+        k < kPgFields ? static_cast<long long>(__ldcg(reinterpret_cast<const unsigned long long*>(a.acc + k * kPgAccStride)))
+                      : 0;
+    const bool range = __ldcg(a.range) != 0;
+    const int32_t st = __ldcg(a.status);
+    long long* out = reinterpret_cast<long long*>(a.metrics);   // see the layout assertion
+    if (range) {
+        PgAcc acc;
+        pg_zero(acc);
+        pg_exact_pass(a, threadIdx.x, blockDim.x, acc);
+        __shared__ float sums[kPgSums];
+        __shared__ int cnts[kPgCounts];
+        pg_block_reduce(acc, sums, cnts);
+        if (out && k < kPgFields)
+            out[k] = k < kPgSums ? __double_as_longlong(static_cast<double>(sums[k])) : cnts[k - kPgSums];
     } else {
-        int v = 0;
-        for (int g = 0; g < kG; ++g) v |= part_c[tid - kPgSums][g];
-        a.metrics->status = v;
+        if (k < kPgFields) tot[k] = mine;
+        __syncthreads();
+        long long v = k < kPgFields ? tot[k] : 0;
+        if (k < kPgSums) {
+            v = __double_as_longlong(static_cast<double>(v) * (1.0 / kPgFix));
+        } else if (k >= kPgSums + 6 && k < kPgFields && a.curve_bins) {
+            const int c = k - kPgSums - 6;   // caller's curve index
+            v = 0;
+            if (c < a.q.n)
+                for (int b = a.q.pos[c] + 1; b <= a.q.n; ++b) v += tot[kPgSums + 5 + b];
+        }
+        if (out && k < kPgFields) out[k] = v;
+    }
+    if (k == 0 && out) out[kPgFields] = st;
+    __syncthreads();   // every read of the accumulators is done
+    if (k < kPgFields) a.acc[k * kPgAccStride] = 0;
+    if (k == 0) {
+        *a.range = 0;
+        *a.status = 0;
+        *a.claim = 0u;
+        *a.arrive = 0u;
     }
 }
 
-// Every thread of every block calls this after the block's record is written; the last
-// block to arrive finishes.
-RL_DEVINL void pg_finish(const PgArgs& a, uint8_t* scratch, int cap_bytes) {
+// Every block calls this after adding its partial; the last one to arrive finishes.  One
+// thread counts the block in with an acquire-release atomic after the block's barrier:
+// the release makes the block's atomics (ordered before it by the barrier) visible
+// before the count, and the acquire, passed on by the second barrier, makes every other
+// block's visible to the last block's reads.
+RL_DEVINL void pg_finish(const PgArgs& a) {
     __shared__ int last;
-    __threadfence();   // this block's record (and outputs) before its arrival
     __syncthreads();
-    if (threadIdx.x == 0) last = atomicAdd(a.arrive, 1u) == static_cast<unsigned int>(a.nb - 1);
+    if (threadIdx.x == 0) {
+        unsigned int old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.arrive) : "memory");
+        last = old == static_cast<unsigned int>(a.nb - 1);
+    }
     __syncthreads();
     if (!last) return;
-    __threadfence();
-    pg_final(a, scratch, cap_bytes);
+    pg_final(a);
 }
 
 // ----------------------------------------------------------------------------------
@@ -411,14 +409,11 @@ __global__ void __launch_bounds__(kPgThreads, kPgSlowPerSm) policy_slow_kernel(P
     __shared__ int cnts[kPgCounts];
     pg_block_reduce(acc, sums, cnts);
     const int k = threadIdx.x;
-    PgRecord& rec = a.rec->r[blockIdx.x];
     if (k < kPgSums)
-        rec.sum[k] = sums[k];
+        pg_add_partial(a, k, sums[k], 0);
     else if (k < kPgFields)
-        rec.cnt[k - kPgSums] = cnts[k - kPgSums];
-    else if (k == kPgFields)
-        rec.status = 0;
-    pg_finish(a, nullptr, 0);
+        pg_add_partial(a, k, 0.f, cnts[k - kPgSums]);
+    pg_finish(a);
 }
 
 // ----------------------------------------------------------------------------------
@@ -545,10 +540,11 @@ RL_DEVINL void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* b
         : "memory");
 }
 
-// The block's partial into its record: warp trees (fp32 sums, exact int32 counts), then the
-// eight consumer warps in order; the curve counts from the histogram, cnt_k = #(j > k),
-// back in the caller's order.  Called by every thread of a streaming block (288).
-RL_DEVINL void pg_block_record(const PgArgs& a, const PgFastAcc& acc, const int* hist_s, const int32_t* blk_status) {
+// The block's partial into the batch accumulators: warp trees (fp32 sums, exact int32
+// counts), then the eight consumer warps in order; the curve bins 1..n from the histogram
+// (the last block turns them into the curve counts).  Called by every thread of a
+// streaming block (288).
+RL_DEVINL void pg_block_partial(const PgArgs& a, const PgFastAcc& acc, const int* hist_s, const int32_t* blk_status) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const bool consumer = threadIdx.x < kPgThreads;
     __shared__ float shs[kPgThreads / 32][kPgSums];
@@ -575,26 +571,19 @@ RL_DEVINL void pg_block_record(const PgArgs& a, const PgFastAcc& acc, const int*
         }
     __syncthreads();
     const int f = threadIdx.x;
-    PgRecord& rec = a.rec->r[blockIdx.x];
     if (f < kPgSums) {
         float v = 0.f;
         for (int w = 0; w < kPgThreads / 32; ++w) v += shs[w][f];
-        rec.sum[f] = v;
+        pg_add_partial(a, f, v, 0);
     } else if (f < kPgSums + 6) {
         int v = 0;
         for (int w = 0; w < kPgThreads / 32; ++w) v += shc[w][f - kPgSums];
-        rec.cnt[f - kPgSums] = v;
+        pg_add_partial(a, f, 0.f, v);
     } else if (f < kPgFields) {
-        const int c = f - kPgSums - 6;        // caller's curve index
-        int v = 0;
-        if (c < a.q.n) {
-            int js = 0;                        // its sorted position
-            while (a.q.perm[js] != c) ++js;
-            for (int k = js + 1; k <= a.q.n; ++k) v += bins[k];
-        }
-        rec.cnt[6 + c] = v;
-    } else if (f == kPgFields) {
-        rec.status = *blk_status;
+        const int b = f - kPgSums - 5;        // sorted bin 1..16
+        pg_add_partial(a, f, 0.f, b <= a.q.n ? bins[b] : 0);
+    } else if (f == kPgFields && *blk_status != 0) {
+        atomicOr(a.status, *blk_status);
     }
 }
 
@@ -628,7 +617,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
     const int64_t mine = blockIdx.x < nstages ? (nstages - blockIdx.x + a.nb - 1) / a.nb : 0;
     const int nst = static_cast<int>(mine);
     const bool consumer = threadIdx.x < kPgThreads;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     if (threadIdx.x == kPgThreads) {
         for (int s = 0; s < kPgDepth; ++s) {
             mbar_init(full + s, 1);
@@ -738,28 +727,33 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_fast_ker
             }
         }
     }
-    pg_block_record(a, acc, hist_s, &blk_status);
-    pg_finish(a, pg_smem, kPgStreamSmem);   // the ring is idle now: scratch for the last block
+    pg_block_partial(a, acc, hist_s, &blk_status);
+    pg_finish(a);
 }
 
 // ----------------------------------------------------------------------------------
 // Packed pass (no mask: every slot a valid token)
 // ----------------------------------------------------------------------------------
-// Each block takes one contiguous range of the tokens (an equal share, in groups of four),
-// streamed through a ring of 1024-token stages by a producer warp (four bulk copies per
-// stage); each consumer thread takes four consecutive tokens of a stage (16-byte shared
-// loads, 16-byte streaming stores).  Every token's values enter the sums and counts
-// without a select (there is no padding to keep out); a token inside a band is re-decided
-// exactly first.  The IPO-curve bin comes from a 1024-bucket table of |p_old - p_samp|
+// The tokens (the whole groups of four) are cut into 1024-token stages.  Block b's producer
+// warp fills a ring of kPkDepth shared-memory stages with bulk copies (four per stage):
+// first stages b, b + nb, ..., then, each time a slot frees, the next stage from a claim
+// counter, until none is left (it then marks the slot "end").  Blocks that get more of the
+// memory system's bandwidth so take more stages, and all of them finish together.  Each
+// consumer thread takes four consecutive tokens of a stage (16-byte shared loads, 16-byte
+// streaming stores), and its fp32 sums over those four go into its 2^-24 fixed-point
+// accumulators at once: a stage's contribution is the same whichever block took it.
+// Every token's values enter the sums and counts without a select (there is no padding
+// to keep out); a token inside a band is re-decided exactly first.  The IPO-curve bin comes from a 1024-bucket table of |p_old - p_samp|
 // built in shared memory at block start: a bucket records how many curve eps lie below
 // it, the one eps inside it (compared exactly), or that the token needs the full search
 // (two eps inside, or an eps whose band reaches into the bucket).
 constexpr int kPkStage = 1024;                 // tokens per stage
-constexpr int kPkDepth = 5;                    // stages in the ring
+constexpr int kPkDepth = 3;                    // stages in the ring (more measured no faster)
 struct alignas(16) PkStage {
     float lt[kPkStage], lo[kPkStage], ls[kPkStage], A[kPkStage];
 };
 constexpr int kPkSmem = kPkDepth * static_cast<int>(sizeof(PkStage));
+static_assert(kPkSmem >= (kPgSums * 8 + 6 * 4) * kPgThreads, "the ring holds the block's values at the end");
 
 // Curve bin of one |p_old - p_samp| value from the bucket table (in shared memory), and
 // whether it lies in the band of a curve eps (or its bucket needs the exact path: two eps
@@ -814,11 +808,69 @@ RL_DEVINL PgTok pg_fast_packed(float lt, float lo, float ls, float A, const PgPr
     return o;
 }
 
+// The packed pass's per-thread accumulators: sums in 2^-24 fixed point, counts.
+struct PkAcc {
+    long long fx[kPgSums];
+    int cnt[6];
+};
+
+// The packed block's partial into the batch accumulators.  The ring is idle once every
+// consumer is past its last stage, so it holds the threads' values field-major; then warp
+// w < 6 sums fixed-point field w (eight values a lane, then a shuffle tree), warps 6 and 7
+// the counts, and every warp some of the curve bins 1..n from the histogram, each adding
+// its total with one atomic (integers: any order gives the same total).  Called by every
+// thread of the block (288).
+RL_DEVINL void pk_block_partial(const PgArgs& a, const PkAcc& acc, const int* hist_s, const int32_t* blk_status,
+                                uint8_t* scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    long long* vx = reinterpret_cast<long long*>(scratch);                  // [kPgSums][256]
+    int* vc = reinterpret_cast<int*>(scratch + kPgSums * kPgThreads * 8);    // [6][256]
+    __syncthreads();   // the ring is free
+    if (threadIdx.x < kPgThreads) {
+#pragma unroll
+        for (int f = 0; f < kPgSums; ++f) vx[f * kPgThreads + threadIdx.x] = acc.fx[f];
+#pragma unroll
+        for (int f = 0; f < 6; ++f) vc[f * kPgThreads + threadIdx.x] = acc.cnt[f];
+    }
+    __syncthreads();
+    auto add = [&](int k, long long x) {
+        if (x != 0)
+            atomicAdd(reinterpret_cast<unsigned long long*>(a.acc + k * kPgAccStride), static_cast<unsigned long long>(x));
+    };
+    if (warp < kPgSums) {
+        long long v = 0;
+#pragma unroll
+        for (int i = 0; i < kPgThreads / 32; ++i) v += vx[warp * kPgThreads + lane + 32 * i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) add(warp, v);
+    } else if (warp < kPgThreads / 32) {
+        for (int f = (warp - kPgSums) * 3; f < (warp - kPgSums) * 3 + 3; ++f) {
+            int v = 0;
+#pragma unroll
+            for (int i = 0; i < kPgThreads / 32; ++i) v += vc[f * kPgThreads + lane + 32 * i];
+            v = __reduce_add_sync(0xffffffffu, v);
+            if (lane == 0) add(kPgSums + f, v);
+        }
+    } else if (lane == 0 && *blk_status != 0) {
+        atomicOr(a.status, *blk_status);
+    }
+    if (warp < kPgThreads / 32)
+        for (int b = 1 + warp; b <= a.q.n; b += kPgThreads / 32) {
+            int v = 0;
+#pragma unroll
+            for (int i = 0; i < kPgThreads / 32; ++i) v += hist_s[b * kPgThreads + lane + 32 * i];
+            v = __reduce_add_sync(0xffffffffu, v);
+            if (lane == 0) add(kPgSums + 5 + b, v);
+        }
+}
+
 __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_kernel(PgArgs a) {
     extern __shared__ __align__(128) uint8_t pk_smem[];
     PkStage* ring = reinterpret_cast<PkStage*>(pk_smem);
     __shared__ __align__(8) uint64_t full[kPkDepth];
     __shared__ __align__(8) uint64_t empty[kPkDepth];
+    __shared__ int stage_of[kPkDepth];             // the stage in each ring slot, -1: no more
     __shared__ int hist_s[kPgBins * kPgThreads];   // bin-major: thread t's bin b at b * 256 + t
     __shared__ int lut[kPkLut];
     __shared__ float s_eps[RL_PG_MAX_CURVE + 1], s_weps[RL_PG_MAX_CURVE + 1];
@@ -827,12 +879,10 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
 
     const PgPrep& q = a.q;
     const int64_t n4 = a.T >> 2;                   // groups of four tokens
-    const int64_t g0 = static_cast<int64_t>(blockIdx.x) * n4 / a.nb;
-    const int64_t g1 = static_cast<int64_t>(blockIdx.x + 1) * n4 / a.nb;
-    const int64_t t0 = 4 * g0, ntok = 4 * (g1 - g0);
+    const int64_t ntok = 4 * n4;                   // tokens the stages cover
     const int nst = static_cast<int>((ntok + kPkStage - 1) / kPkStage);
     const bool consumer = threadIdx.x < kPgThreads;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     if (threadIdx.x == kPgThreads) {
         for (int s = 0; s < kPkDepth; ++s) {
             mbar_init(full + s, 1);
@@ -854,35 +904,50 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
     }
     __syncthreads();
 
-    PgFastAcc acc;
+    PkAcc acc;
 #pragma unroll
-    for (int k = 0; k < kPgSums; ++k) acc.sum[k] = 0.f;
+    for (int k = 0; k < kPgSums; ++k) acc.fx[k] = 0;
 #pragma unroll
     for (int k = 0; k < 6; ++k) acc.cnt[k] = 0;
     volatile int* vflag = &abort_flag;
 
+    // The producer lane fills the ring: entry i goes to slot i mod kPkDepth, stage
+    // blockIdx + i nb for the first kPkDepth entries, then claimed ones (the claim's round
+    // trip overlaps the wait for the slot).  Returns false once it has placed the end mark
+    // (no stage left) or the block aborts.
+    int issued = 0;
+    auto fill = [&](int i) -> bool {
+        const int slot = i % kPkDepth;
+        const int s = i < kPkDepth ? static_cast<int>(blockIdx.x) + i * a.nb
+                                   : kPkDepth * a.nb + static_cast<int>(atomicAdd(a.claim, 1u));
+        if (i >= kPkDepth &&
+            !mbar_wait(empty + slot, static_cast<uint32_t>((i / kPkDepth - 1) & 1), &blk_status, a.wait_ns)) {
+            atomicExch(&abort_flag, 1);
+            return false;
+        }
+        if (*vflag) return false;
+        if (s >= nst) {   // none left: the consumers stop at this slot
+            stage_of[slot] = -1;
+            mbar_arrive(full + slot);
+            return false;
+        }
+        stage_of[slot] = s;
+        const int64_t g = static_cast<int64_t>(s) * kPkStage;
+        const int64_t left = ntok - g;
+        const uint32_t L = static_cast<uint32_t>(left < kPkStage ? left : kPkStage);
+        PkStage& st = ring[slot];
+        mbar_arrive_expect_tx(full + slot, 16u * L);
+        bulk_load(st.lt, a.lt + g, 4u * L, full + slot);
+        bulk_load(st.lo, a.lo + g, 4u * L, full + slot);
+        bulk_load(st.ls, a.ls + g, 4u * L, full + slot);
+        bulk_load(st.A, a.adv + g, 4u * L, full + slot);
+        issued = i + 1;
+        return true;
+    };
     if (!consumer) {
         if (lane == 0) {
-            int issued = 0;
-            for (int i = 0; i < nst; ++i) {
-                const int slot = i % kPkDepth;
-                if (i >= kPkDepth &&
-                    !mbar_wait(empty + slot, static_cast<uint32_t>((i / kPkDepth - 1) & 1), &blk_status, a.wait_ns)) {
-                    atomicExch(&abort_flag, 1);
-                    break;
-                }
-                if (*vflag) break;
-                const int64_t g = t0 + static_cast<int64_t>(i) * kPkStage;
-                const int64_t left = t0 + ntok - g;
-                const uint32_t L = static_cast<uint32_t>(left < kPkStage ? left : kPkStage);
-                PkStage& st = ring[slot];
-                mbar_arrive_expect_tx(full + slot, 16u * L);
-                bulk_load(st.lt, a.lt + g, 4u * L, full + slot);
-                bulk_load(st.lo, a.lo + g, 4u * L, full + slot);
-                bulk_load(st.ls, a.ls + g, 4u * L, full + slot);
-                bulk_load(st.A, a.adv + g, 4u * L, full + slot);
-                issued = i + 1;
-            }
+            int pi = 0;
+            while (fill(pi)) ++pi;
             if (*vflag) {
                 // the last stages issued may still be in flight: wait for them (bounded by
                 // the fixed kWaitLimitNs) before the block's shared memory goes away
@@ -893,15 +958,17 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
     } else {
         int* hist = hist_s + threadIdx.x;
         const int j4 = 4 * threadIdx.x;
-        for (int i = 0; i < nst; ++i) {
+        for (int i = 0;; ++i) {
             const int slot = i % kPkDepth;
             if (!mbar_wait(full + slot, static_cast<uint32_t>((i / kPkDepth) & 1), &blk_status, a.wait_ns)) {
                 atomicExch(&abort_flag, 1);
                 break;
             }
             if (*vflag) break;
-            const int64_t g = t0 + static_cast<int64_t>(i) * kPkStage;
-            if (g + j4 < t0 + ntok) {
+            const int s = stage_of[slot];
+            if (s < 0) break;
+            const int64_t g = static_cast<int64_t>(s) * kPkStage;
+            if (g + j4 < ntok) {
                 const PkStage& st = ring[slot];
                 const float4 lt4 = *reinterpret_cast<const float4*>(st.lt + j4);
                 const float4 lo4 = *reinterpret_cast<const float4*>(st.lo + j4);
@@ -910,6 +977,9 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
                 const float vt[4] = {lt4.x, lt4.y, lt4.z, lt4.w}, vo[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
                 const float vs[4] = {ls4.x, ls4.y, ls4.z, ls4.w}, vA[4] = {A4.x, A4.y, A4.z, A4.w};
                 float lp[4], ld[4], gp[4], gd[4];
+                float sum4[kPgSums];
+#pragma unroll
+                for (int k = 0; k < kPgSums; ++k) sum4[k] = 0.f;
 #pragma unroll
                 for (int u = 0; u < 4; u += 2) {   // two tokens at a time: two independent chains, no branch
                     PgTok t[2] = {pg_fast_packed(vt[u], vo[u], vs[u], vA[u], q, lut, s_eps, s_weps),
@@ -925,7 +995,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
                         gp[u + h] = t[h].gp;
                         gd[u + h] = t[h].gd;
 #pragma unroll
-                        for (int k = 0; k < kPgSums; ++k) acc.sum[k] += t[h].s[k];
+                        for (int k = 0; k < kPgSums; ++k) sum4[k] += t[h].s[k];
                         acc.cnt[1] += t[h].clip;
                         acc.cnt[2] += t[h].dual;
                         acc.cnt[3] += t[h].ice_lo;
@@ -934,6 +1004,8 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
                         hist[t[h].j * kPgThreads] += 1;
                     }
                 }
+#pragma unroll
+                for (int k = 0; k < kPgSums; ++k) acc.fx[k] += pg_fix(a, sum4[k]);
                 acc.cnt[0] += 4;
                 if (a.loss_ppo) __stcs(reinterpret_cast<float4*>(a.loss_ppo + g + j4), make_float4(lp[0], lp[1], lp[2], lp[3]));
                 if (a.loss_dec) __stcs(reinterpret_cast<float4*>(a.loss_dec + g + j4), make_float4(ld[0], ld[1], ld[2], ld[3]));
@@ -945,13 +1017,22 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
         }
         // the last T mod 4 tokens, scalar loads
         if (blockIdx.x == a.nb - 1) {
-            const int64_t t = 4 * n4 + threadIdx.x;
+            const int64_t t = ntok + threadIdx.x;
             if (t < a.T) {
                 float lp, ld, gp, gd;
                 const float xt = a.lt[t], xo = a.lo[t], xs = a.ls[t], xa = a.adv[t];
                 PgTok tk = pg_fast_packed(xt, xo, xs, xa, q, lut, s_eps, s_weps);
                 if (tk.band) pg_resolve(tk, xt, xo, xs, xa, q);
-                pg_take(tk, true, hist, acc, lp, ld, gp, gd);
+                PgFastAcc one;
+#pragma unroll
+                for (int k = 0; k < kPgSums; ++k) one.sum[k] = 0.f;
+#pragma unroll
+                for (int k = 0; k < 6; ++k) one.cnt[k] = 0;
+                pg_take(tk, true, hist, one, lp, ld, gp, gd);
+#pragma unroll
+                for (int k = 0; k < kPgSums; ++k) acc.fx[k] += pg_fix(a, one.sum[k]);
+#pragma unroll
+                for (int k = 0; k < 6; ++k) acc.cnt[k] += one.cnt[k];
                 if (a.loss_ppo) a.loss_ppo[t] = lp;
                 if (a.loss_dec) a.loss_dec[t] = ld;
                 if (a.grad_ppo) a.grad_ppo[t] = gp;
@@ -959,19 +1040,20 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
             }
         }
     }
-    pg_block_record(a, acc, hist_s, &blk_status);
-    pg_finish(a, pk_smem, kPkSmem);   // the ring is idle now: scratch for the last block
+    pk_block_partial(a, acc, hist_s, &blk_status, pk_smem);
+    pg_finish(a);
 }
 
 // ----------------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------------
-// Workspace: a 256-byte header (the arrival counter at byte 0: zero before the first call,
-// and the last block of every call leaves it zero), then the blocks' partial records
-// (PgRecords, one 128-byte record per block).  At most kPgMaxBlocks blocks run (fewer than two per SM on a part with
-// more than 256 SMs), so the workspace size does not depend on the device.
-constexpr size_t kPgHeader = 256;
-static_assert(kPgHeader + sizeof(PgRecords) <= kPolicyWorkspaceBytes, "workspace layout");
+// Workspace (kPolicyWorkspaceBytes): the first 128-byte line holds the arrival counter
+// (byte 0), the status word (4), the range flag (8) and the claim counter (12); the
+// kPgFields accumulators follow, one 128-byte line each.  All of it is zero before the
+// first call, and the last block of every call leaves it zero again.  At most
+// kPgMaxBlocks blocks run, so the workspace size does not depend on the device.
+constexpr size_t kPgAccBase = 128;
+static_assert(kPgAccBase + kPgFields * kPgAccStride * 8 <= kPolicyWorkspaceBytes, "workspace layout");
 
 static int fast_blocks(int sms) {   // odd: see policy_fast_kernel
     const int n = sms * kPgFastPerSm - 1;
@@ -1018,6 +1100,7 @@ static PgPrep prepare(const rl_pg_params& p) {
             q.perm[y] = q.perm[y - 1];
             q.perm[y - 1] = t;
         }
+    for (int k = 0; k < q.n; ++k) q.pos[q.perm[k]] = k;
     for (int k = 0; k < q.n; ++k) {
         q.eps[k] = p.curve_eps[q.perm[k]];
         q.weps[k] = band(q.eps[k]);
@@ -1058,8 +1141,8 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
                 void* ws, size_t ws_bytes, cudaStream_t stream) {
     const int sms = num_sms();
     if (ws_bytes < policy_ws_bytes(T)) return RL_ERR_WORKSPACE;
-    if ((reinterpret_cast<uintptr_t>(ws) & 15u) != 0) {
-        set_last_error("workspace not 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(ws) & 7u) != 0) {   // int64 accumulators
+        set_last_error("workspace not 8-byte aligned");
         return RL_ERR_ARG;
     }
     auto al = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
@@ -1078,8 +1161,12 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
     a.loss_dec = loss_dec;
     a.grad_ppo = grad_ppo;
     a.grad_dec = grad_dec;
-    a.arrive = static_cast<unsigned int*>(ws);
-    a.rec = reinterpret_cast<PgRecords*>(static_cast<uint8_t*>(ws) + kPgHeader);   // 16-byte aligned
+    uint8_t* hb = static_cast<uint8_t*>(ws);
+    a.arrive = reinterpret_cast<unsigned int*>(hb);
+    a.status = reinterpret_cast<int32_t*>(hb + 4);
+    a.range = reinterpret_cast<int*>(hb + 8);
+    a.claim = reinterpret_cast<unsigned int*>(hb + 12);
+    a.acc = reinterpret_cast<long long*>(hb + kPgAccBase);
     a.metrics = metrics;
     a.wait_ns = wait_limit_ns();
     // per device: the fast pass's shared-memory opt-in (set once; concurrent first calls
@@ -1097,6 +1184,12 @@ int policy_impl(const float* lt, const float* lo, const float* ls, const float* 
     }
     ProfScope ps(RL_PROF_POLICY, stream);   // the kernel launch
     a.nb = fast ? fast_blocks(sms) : slow_blocks(sms);
+    a.curve_bins = fast;
+    // a term below 2^38 / (terms per accumulator) keeps each accumulator's total below 2^62
+    // in 2^-24 units: one term per block, or in the packed pass one per thread and stage
+    // (a group of four tokens) and one per tail token
+    const double terms = fast && mask == nullptr ? static_cast<double>(T / 4 + 3) : static_cast<double>(a.nb);
+    a.range_lim = static_cast<float>(ldexp(1.0, 38) / terms);
     if (fast && mask == nullptr) {
         policy_packed_kernel<<<a.nb, kPgThreads + 32, kPkSmem, stream>>>(a);
     } else if (fast) {

@@ -1,6 +1,6 @@
 // rl_policy_loss_elementwise_noalloc: the elementwise PPO / TIS / mismatch path for callers
-// that cannot allocate device memory.  Its scratch (the arrival counter and the blocks'
-// partial records) lives in a file-scope device array instead of a caller workspace.
+// that cannot allocate device memory.  Its scratch (the counters, flags and metric
+// accumulators) lives in a file-scope device array instead of a caller workspace.
 #include <mutex>
 
 #include "common.cuh"
@@ -8,8 +8,7 @@
 
 namespace rl {
 
-// 65,792 bytes: the elementwise pass's workspace (a 256-byte header and 512 per-block
-// partial records of 128 bytes).
+// 4096 bytes: the elementwise pass's workspace.
 constexpr size_t kNoAllocScratchBytes = kPolicyWorkspaceBytes;
 static __device__ __align__(256) double g_policy_scratch[kNoAllocScratchBytes / sizeof(double)];
 

@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kRcThreads, 8) rc_seq_kernel(RcArgs a) {
 }
 
 // Warp f sums field f of the records over the sequences in order (lane l takes
-// b = l, l + 32, ..., eight loads in flight ahead of their adds, then a butterfly) into
+// b = l, l + 32, ..., sixteen loads in flight ahead of their adds, then a butterfly) into
 // tot[f].  With only_factor, just the two fields the batch-normalisation factor needs.
 // Every block that calls it computes the same bits.
 constexpr int kRcReduceThreads = 32 * kRcFields;
@@ -401,12 +401,12 @@ RL_DEVINL void rc_reduce_fields(const RcArgs& a, double* tot, bool only_factor) 
     if (f < kRcD) {
         const double* src = a.pd + f * B;
         double v = 0.0;
-        for (int64_t b0 = lane; b0 < B; b0 += 32 * 8) {
-            double x[8];
+        for (int64_t b0 = lane; b0 < B; b0 += 32 * 16) {
+            double x[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : 0.0;
+            for (int i = 0; i < 16; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : 0.0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v += x[i];
+            for (int i = 0; i < 16; ++i) v += x[i];
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -414,12 +414,12 @@ RL_DEVINL void rc_reduce_fields(const RcArgs& a, double* tot, bool only_factor) 
     } else if (f < kRcD + kRcC) {
         const long long* src = a.pc + (f - kRcD) * B;
         long long v = 0;
-        for (int64_t b0 = lane; b0 < B; b0 += 32 * 8) {
-            long long x[8];
+        for (int64_t b0 = lane; b0 < B; b0 += 32 * 16) {
+            long long x[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : 0;
+            for (int i = 0; i < 16; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v += x[i];
+            for (int i = 0; i < 16; ++i) v += x[i];
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -428,12 +428,12 @@ RL_DEVINL void rc_reduce_fields(const RcArgs& a, double* tot, bool only_factor) 
         const bool is_min = f == kRcD + kRcC;
         const float* src = is_min ? a.pmin : a.pmax;
         float v = is_min ? INFINITY : -INFINITY;
-        for (int64_t b0 = lane; b0 < B; b0 += 32 * 8) {
-            float x[8];
+        for (int64_t b0 = lane; b0 < B; b0 += 32 * 16) {
+            float x[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : v;
+            for (int i = 0; i < 16; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : v;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v = is_min ? fminf(v, x[i]) : fmaxf(v, x[i]);
+            for (int i = 0; i < 16; ++i) v = is_min ? fminf(v, x[i]) : fmaxf(v, x[i]);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
