@@ -200,6 +200,24 @@ def _time_back_to_back(torch, calls, passes):
     return e0.elapsed_time(e1) / (rounds * len(calls))
 
 
+def _copy_floor(torch, dev, nbytes: int, n_sets: int, passes: int) -> float:
+    """Average time per call (ms) of a plain device-to-device copy that moves nbytes (half
+    read, half written), timed as the pass it stands beside: back to back in a CUDA graph
+    over n_sets rotating sources.  At a few tens of MB a kernel's start and drain are a
+    large part of its time, so this is the floor a pass of that size meets, next to the
+    peak measured on GB-sized copies."""
+    half = (nbytes // 2 + 15) // 16 * 4
+    srcs = [torch.ones(half, dtype=torch.float32, device=dev) for _ in range(n_sets)]
+    dst = torch.empty(half, dtype=torch.float32, device=dev)
+    calls = [(lambda a=a: dst.copy_(a)) for a in srcs]
+    for c in calls:
+        c()
+    torch.cuda.synchronize()
+    ms = _time_back_to_back(torch, calls, passes)
+    del srcs, dst
+    return ms
+
+
 def elementwise_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb: int = 4096, packed: bool = True):
     """The elementwise PPO / dual-clip / decoupled-TIS / mismatch path on its own workload,
     1.8M valid tokens in sequences of 64..4096, against the HBM roofline.
@@ -250,6 +268,7 @@ def elementwise_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush
     n_valid = int(c.mask.sum())
     nbytes = T * (16 + (0 if packed else 1)) + T * 16
     gbs = nbytes / (ms / 1e3) / 1e9
+    copy_ms = _copy_floor(torch, dev, nbytes, len(sets), passes)
     peak = float(peaks["hbm_gbs"])
     layout = (f"packed: {n_valid} valid tokens end to end, no mask" if packed else
               f"padded: {len(c.seq_lens)} sequences of 64..4096 padded to {c.max_len} (T={T} slots) with a mask")
@@ -257,6 +276,8 @@ def elementwise_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush
                         "IcePop band, mismatch KL",
             "us_per_call_back_to_back": ms * 1e3, "kernel_us_single_launch": kms * 1e3,
             "tokens_per_s": n_valid / (ms / 1e3), "passes": passes, "input_sets": len(sets),
+            "device_copy_same_bytes": {"us_per_call_back_to_back": copy_ms * 1e3, "pass_over_copy": ms / copy_ms,
+                                       "frac_of_hbm_peak": nbytes / (copy_ms / 1e3) / 1e9 / float(peaks["hbm_gbs"])},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "traffic": None, "algorithmic_bytes_per_pass": nbytes,
                          "duration": "average per call, back to back in a CUDA graph (one kernel launch per call)",
@@ -271,9 +292,11 @@ def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb:
     lp_samp the rollout engine's; packed (the default): the 879 sequences end to end
     (cumulative lengths, every mask byte 1), else the padded rows.  Knobs: sequence-level
     TIS clipped to [0.1, 10] with batch normalisation, geometric RS in [0.9, 1.1], veto
-    1e-4.  Timed as elementwise_side.  Algorithmic bytes per slot: two fp32 inputs and the
-    mask read, the fp32 weight and the keep byte written (14 B), plus the weight read and
-    written again by the normalisation (8 B): the factor needs every token first."""
+    1e-4.  Timed as elementwise_side (per call: the sequence kernel, whose last block writes
+    the metrics and the factor, then the scaling kernel).  Algorithmic bytes per slot: two
+    fp32 inputs and the mask read, the fp32 weight and the keep byte written (14 B), plus
+    the weight read and written again by the normalisation (8 B): the factor needs every
+    token first."""
     import numpy as np
     import workloads
     c = workloads.make_policy_case()
@@ -293,7 +316,7 @@ def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb:
     sets = _rotating_sets(torch, dev, arrays, 2 * 129 * 2 ** 20 + 1)
     outs = (torch.empty(T, dtype=torch.float32, device=dev), torch.empty(T, dtype=torch.uint8, device=dev))
     met = torch.zeros(rh.ctypes.sizeof(rh.RlRcMetrics), dtype=torch.uint8, device=dev)
-    ws = torch.empty(rh.rl_rollout_correction_workspace_bytes(B), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(rh.rl_rollout_correction_workspace_bytes(B), dtype=torch.uint8, device=dev)   # zeroed once
     calls = [(lambda ins=ins: rh.rl_rollout_correction(*ins, off, rp, outputs=outs, ws=ws, metrics_dev=met))
              for ins in sets]
     for i in range(max(warmup, 3)):
@@ -324,7 +347,7 @@ def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb:
             "tokens_per_s": n_valid / (ms / 1e3), "passes": passes, "input_sets": len(sets),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "traffic": None, "algorithmic_bytes_per_pass": nbytes,
-                         "duration": "average per call, back to back in a CUDA graph (workspace memset + kernels)",
+                         "duration": "average per call, back to back in a CUDA graph (the sequence kernel, then the scaling kernel)",
                          "peak_kind": f"hbm_gbs ({peaks['source']})"},
             "l2": f"{len(sets)} rotating input sets (more than 2x L2 per round)"}
 
@@ -508,12 +531,16 @@ def run_ours(args):
     peaks = load_peaks()
 
     t_gen = time.perf_counter()
+    # the replayed top-p configurations with the pages' kept counts, as in the side figures
     case = workloads.make_head_case(args.config, device=dev, seed=workloads.BASE_SEED + 4 + 1000 * rank,
-                                    n_tokens=args.tokens)
+                                    n_tokens=args.tokens,
+                                    variant="pages" if args.config in ("c2", "c3") else "literal")
     torch.cuda.synchronize()
     t_gen = time.perf_counter() - t_gen
     N, H, V, nnz = case.N, case.H, case.V, case.nnz
     hp = head_params(rh, args.grad_precision)
+    if args.sparse:
+        hp = rh.HeadParams(loss_type=rh.RL_LOSS_IPO, eps=0.3, max_importance_ratio=10.0, all_replayed=1)
     batch = rh.HeadBatch.from_case(case)
     torch.cuda.reset_peak_memory_stats(dev)
     base_mem = torch.cuda.memory_allocated(dev)
@@ -628,6 +655,8 @@ def run_ours(args):
     if recomputed and "gemm_bwd_grad" in prof:
         n_chunks = prof["gemm_fwd_stats"][1] / args.steps
         flops_per_launch["gemm_bwd_grad"] = 2.0 * N * H * V / n_chunks * recomputed / (prof["gemm_bwd_grad"][1] / args.steps)
+    # the captured per-launch traffic holds for the dense path at the default 8192-token chunk
+    traffic_ok = not args.sparse and not hp.token_chunk and N >= 8192 and args.grad_precision == "bf16"
     dom = max(prof.items(), key=lambda kv: kv[1][0])
     dom_name, (dom_ms, dom_n) = dom
     peak_sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
@@ -636,8 +665,8 @@ def run_ours(args):
     if dom_name in flops_per_launch:
         ach = flops_per_launch[dom_name] / ((dom_ms / dom_n) / 1e3) / 1e12
         roof = {"kernel": dom_name, "bound": "tensor", "achieved": ach, "peak": peak_sus, "unit": "TFLOP/s",
-                "frac": ach / peak_sus, "traffic": TRAFFIC.get(dom_name),
-                "traffic_source": TRAFFIC_SOURCE if dom_name in TRAFFIC else None,
+                "frac": ach / peak_sus, "traffic": TRAFFIC.get(dom_name) if traffic_ok else None,
+                "traffic_source": TRAFFIC_SOURCE if traffic_ok and dom_name in TRAFFIC else None,
                 "peak_kind": f"bf16_tflops_sustained ({peaks['source']})",
                 "frac_of_burst": ach / peak_burst,
                 "algorithmic_flops_per_launch": flops_per_launch[dom_name]}
@@ -652,7 +681,9 @@ def run_ours(args):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "N": N, "H": H, "V": V, "nnz": nnz,
+            "config": {"workload": WORKLOAD if args.config == "c4" and not args.sparse else
+                       f"{args.config} shapes ({'sparse CSR backward, ipo 0.3 cap 10' if args.sparse else 'the c4 loss'}; "
+                       "a profiling run)", "N": N, "H": H, "V": V, "nnz": nnz,
                        "grad_precision": args.grad_precision, "parallelism": f"replicas x{world}",
                        "gemm": "sm-pair (cta_group::2, 256x256)" if rh.rl_get_option(rh.RL_OPT_GEMM_PAIR) else
                                "single-sm (128x256)",
@@ -686,10 +717,11 @@ def run_ours(args):
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of each kernel, from the ncu
-# capture of the kernel as it stands, summarised under profiles/ (one launch at the
-# library's default 8192-token chunk); empty until that capture exists.
-TRAFFIC = {}
-TRAFFIC_SOURCE = None
+# capture of the kernel as it stands (one launch at the library's default 8192-token chunk),
+# summarised in profiles/gemm_pair_dram_traffic_8k_chunk.md.
+TRAFFIC = {"gemm_fwd_stats": 1131648000 + 4935729152, "gemm_bwd_dx": 5748131840 + 30051072,
+           "gemm_bwd_dw": 4488490240 + 1219097088}
+TRAFFIC_SOURCE = "ncu capture at the 8192-token chunk, profiles/gemm_pair_dram_traffic_8k_chunk.md (not measured in this run)"
 
 
 def ctypes_metrics_size(rh):
@@ -721,6 +753,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="c4")
     ap.add_argument("--grad-precision", choices=["bf16", "split"], default="bf16")
+    ap.add_argument("--sparse", action="store_true",
+                    help="the sparse-backward configuration's loss (ipo 0.3, cap 10, replayed supports) with the "
+                         "sparse CSR backward; for --config c3 (profiling runs)")
     ap.add_argument("--cpu-tokens", type=int, default=128, help="oracle sample for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=32, help="oracle sample per step, --impl reference")
     ap.add_argument("--tokens", type=int, default=None, help="fewer tokens, same shapes (profiling runs)")

@@ -387,16 +387,20 @@ typedef struct rl_rc_metrics {
                                    [0, T) (bad sequences then count as empty) */
 } rl_rc_metrics;
 
-/* Workspace bytes for B sequences (per-sequence partial sums and a small header). */
+/* Workspace bytes for B sequences: a small header (counters, status, factor), per-sequence
+ * and per-group partial sums, per-group counters.  Zero the workspace once before its first
+ * use (8-byte aligned): every call leaves its counters and status word at zero again, so
+ * later calls need no clearing.  Calls that overlap on the GPU must not share a workspace. */
 size_t rl_rollout_correction_workspace_bytes(int64_t B);
 /* lp_train, lp_rollout: device [T] fp32; mask: device [T] uint8 (1 = response token);
  * seq_offsets: device [B + 1] int64, sequence s = tokens [seq_offsets[s], seq_offsets[s+1])
  * (padded rows: s * row_length; packed: cumulative lengths).  A token whose mask byte is 0
  * is not a response token and its log-probs are never used (NaN and inf included).
  * Outputs, device: weights [T] fp32 and keep [T] uint8 (either may be NULL), metrics
- * (overwritten, may be NULL).  Batch normalisation: each sequence's kept weights are summed
- * in fp32 and the sequences' sums added exactly in 2^-24 fixed point (a sequence sum at or
- * past 2^38 / B instead sends the factor through an fp64 sum in sequence order).
+ * (overwritten, may be NULL).  Sums: per sequence in fp32 (fp64 for the sequence-level
+ * terms), then over the sequences in fp64 in a fixed order (groups of 32 in sequence order,
+ * then the groups in order), so results are reproducible; the batch-normalisation factor
+ * n_kept / (sum of kept weights) comes from those totals.
  * Errors: RL_ERR_ARG (NULL input, B < 0, T < 0, B == 0 with T > 0, bad enum, L > U or
  * negative bound), RL_ERR_WORKSPACE; bad offsets are reported in metrics->status, not
  * trapped. */

@@ -635,8 +635,8 @@ def rl_rollout_correction(lp_train, lp_rollout, mask, seq_offsets, params: RcPar
         outputs = (torch.empty(T, dtype=torch.float32, device=dev), torch.empty(T, dtype=torch.uint8, device=dev))
     if metrics_dev is None:
         metrics_dev = torch.zeros(ctypes.sizeof(RlRcMetrics), dtype=torch.uint8, device=dev)
-    if ws is None:
-        ws = _u8(rl_rollout_correction_workspace_bytes(B), dev)
+    if ws is None:   # zeroed once: the library leaves its counters at zero after each call
+        ws = torch.zeros(max(rl_rollout_correction_workspace_bytes(B), 1), dtype=torch.uint8, device=dev)
     p = params.c()
     _check(lib.rl_rollout_correction(_ptr(lp_train), _ptr(lp_rollout), _ptr(mask), _ptr(seq_offsets), B, T,
                                      ctypes.byref(p), _ptr(outputs[0]), _ptr(outputs[1]), _ptr(metrics_dev),

@@ -86,6 +86,16 @@ RL_DEVINL bool mbar_try_wait(uint32_t addr, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// One bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16),
+// completion counted on an mbarrier of this CTA.
+RL_DEVINL void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // Bounded wait for the phase with the given parity.  Returns false (and sets the
 // timeout status bit) if the limit ran out.
 RL_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, int32_t* status, uint64_t limit_ns = kWaitLimitNs) {

@@ -661,11 +661,11 @@ __global__ void bucket_kernel(const int32_t* keys, int64_t n, int32_t V, int64_t
 
 __global__ void __launch_bounds__(256) sparse_dw_kernel(SparseArgs a, const int32_t* vals,
                                                         const int32_t* item_tok, const int64_t* bucket,
-                                                        float* dW) {
+                                                        float* dW, int overwrite) {
     if (gate_closed(a.gate)) return;
     const int64_t v = blockIdx.x;
     const int64_t b = bucket[v], e = bucket[v + 1];
-    if (e <= b) return;
+    if (e <= b && !overwrite) return;   // overwrite: a row no item touches is written as zeros
     for (int64_t h0 = static_cast<int64_t>(threadIdx.x) * 8; h0 < a.H; h0 += 256 * 8) {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int64_t i = b; i < e; ++i) {
@@ -677,6 +677,11 @@ __global__ void __launch_bounds__(256) sparse_dw_kernel(SparseArgs a, const int3
             if (c != 0.f) fma_row8(acc, a.X + static_cast<int64_t>(t) * a.H + h0, c);
         }
         float4* d = reinterpret_cast<float4*>(dW + v * a.H + h0);
+        if (overwrite) {
+            d[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            d[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            continue;
+        }
         float4 o0 = d[0], o1 = d[1];
         o0.x += acc[0];
         o0.y += acc[1];
@@ -691,7 +696,9 @@ __global__ void __launch_bounds__(256) sparse_dw_kernel(SparseArgs a, const int3
     }
 }
 
-static int sparse_dw(const SparseArgs& a, const BwdWs& w, float* dW, cudaStream_t s) {
+// overwrite: dW = the sparse part (every row written, no memset and no read of dW first);
+// else dW += the sparse part.
+static int sparse_dw(const SparseArgs& a, const BwdWs& w, float* dW, cudaStream_t s, int overwrite = 0) {
     const int64_t n = a.nnz + a.N;
     if (n >= (int64_t(1) << 31)) {
         set_last_error("sparse gradient items exceed 2^31");
@@ -724,7 +731,7 @@ static int sparse_dw(const SparseArgs& a, const BwdWs& w, float* dW, cudaStream_
     }
     bucket_kernel<<<static_cast<unsigned>((n + 1 + 255) / 256), 256, 0, s>>>(kin, n, static_cast<int32_t>(a.V), w.bucket,
                                                                              a.gate);
-    sparse_dw_kernel<<<static_cast<unsigned>(a.V), 256, 0, s>>>(a, vin, w.item_tok, w.bucket, dW);
+    sparse_dw_kernel<<<static_cast<unsigned>(a.V), 256, 0, s>>>(a, vin, w.item_tok, w.bucket, dW, overwrite);
     count_launch(2);
     return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }
@@ -755,12 +762,7 @@ int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* save
             sparse_dx_kernel<true><<<static_cast<unsigned>(N), 256, 0, stream>>>(sa, 0, nullptr, static_cast<uint16_t*>(dhidden));
         }
         count_launch();
-        if (!accumulate) {
-            ProfScope ps(RL_PROF_MEMSET, stream);
-            if (cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * sizeof(float), stream) != cudaSuccess)
-                return RL_ERR_CUDA;
-        }
-        return sparse_dw(sa, w, dW, stream);
+        return sparse_dw(sa, w, dW, stream, accumulate ? 0 : 1);
     }
 
     ResidArgs ra{0, N, V, nnz, b->labels, b->support.offsets, b->support.ids, dloss, sv.dcoef, sv.lse,

@@ -530,16 +530,6 @@ struct alignas(16) PgStage {
 constexpr int kPgStageBytes = static_cast<int>(sizeof(PgStage));
 constexpr int kPgStreamSmem = kPgDepth * kPgStageBytes;
 
-// One bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16),
-// completion counted on an mbarrier of this CTA.
-RL_DEVINL void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
 // The block's partial into the batch accumulators: warp trees (fp32 sums, exact int32
 // counts), then the eight consumer warps in order; the curve bins 1..n from the histogram
 // (the last block turns them into the curve counts).  Called by every thread of a

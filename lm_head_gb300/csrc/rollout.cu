@@ -11,16 +11,18 @@
 // against a threshold's logarithm (or n times it) prepared on the host as a float-float
 // pair.  Weight values are fp32.
 //
-//  1. rc_seq_kernel     one block per sequence: a pass over its tokens for the sequence
-//                       sums, the sequence's decisions by one thread, a second pass (the
-//                       tokens are now in L2) writing weights and keep flags; one record
-//                       of partial sums per sequence.
-//  2. rc_reduce_kernel  one block, one warp per field: the records summed in sequence
-//                       order (fixed tree), so results are reproducible; then the
-//                       metrics.  Without batch normalisation only.
-//  2'. rc_scale_kernel  with batch normalisation, instead: every block forms the factor
-//                       from the records in the same order (block 0 also all fields and
-//                       the metrics), then weights *= factor.
+//  1. rc_seq_kernel     one block per sequence: the sequence staged in shared memory (whole,
+//                       by bulk copies, up to 4096 tokens; longer ones chunk by chunk), a
+//                       pass over its tokens for the sequence sums, the sequence's
+//                       decisions by one thread, a second pass writing weights and keep
+//                       flags; one record of partial sums per sequence.  The last block of
+//                       each group of 32 sequences to finish sums the group's records in
+//                       sequence order, and the last group to finish sums the group records
+//                       in group order: a fixed order, so the totals are reproducible.  That
+//                       block writes the metrics and the batch-normalisation factor.
+//  2. rc_scale_kernel   with batch normalisation: weights *= factor.
+//  The counters the blocks meet at are set back to zero by the blocks that finish with
+//  them, so a workspace zeroed once before its first use needs no clearing between calls.
 #include <cmath>
 #include <climits>
 
@@ -58,17 +60,19 @@ struct RcArgs {
     long long* pc;       // [kRcC][B]
     float* pmin;         // [B]
     float* pmax;         // [B]
-    int32_t* status;
+    double* gd;          // [kRcD][G] the group records
+    long long* gc;       // [kRcC][G]
+    float* gmin;         // [G]
+    float* gmax;         // [G]
+    int64_t G;           // groups of kRcGroup sequences
+    unsigned int* gcnt;  // [G] sequences of the group done (0 between calls)
+    unsigned int* tcnt;  // groups done (0 between calls)
+    int32_t* status;     // RL_STATUS_* bits of this call (0 between calls)
     float* factor;       // the batch-normalisation factor applied
-    // batch normalisation: kept tokens and their weight sum over all sequences, exact
-    // integer totals (the weight in 2^-24 fixed point); kept_range set if a sequence's sum
-    // was too large for that (the factor then comes from the ordered record reduction)
-    long long* kept_n;
-    long long* kept_wfix;
-    int* kept_range;
-    float kept_lim;
+    uint64_t wait_ns;    // limit of the staging wait
     rl_rc_metrics* metrics;
 };
+constexpr int kRcGroup = 32;   // sequences per first-level group of the reduction
 
 // Fixed-order reductions: a butterfly within each warp (every lane ends with the same
 // value, the same operands in the same order on both lanes of an exchange), then the
@@ -109,25 +113,142 @@ struct RcSeq {   // one sequence's decisions (thread 0 -> block)
     float wseq;
 };
 
-// A sequence is staged in shared memory kRcChunk tokens at a time (coalesced loads, 16
-// bytes wide where the chunk is aligned, scalar otherwise); a sequence of at most kRcChunk tokens is read from memory once
-// for both passes, a longer one chunk by chunk in each pass (pass 2 starts from the chunk
-// still staged; the earlier ones come back from L2).  128 threads and 2048-token chunks
-// keep eight blocks on an SM, so a batch of up to 8 x SMs sequences is resident at once
-// (256 threads with 4096-token chunks, four per SM: 4 % slower on 879 sequences of 4096
-// slots).  Loops stay rolled: the code is fetched cold by every block, so its size is
-// part of the latency.
-constexpr int kRcChunk = 2048;
+// The factor and the metrics from the reduced fields (one thread).
+RL_DEVINL void rc_write_metrics(const RcArgs& a, const double* t) {
+    const double kept_w = t[RD_KEPT_W], n_kept = t[kRcD + RC_KEPT];
+    const double factor = a.q.use_tis && a.q.norm && n_kept > 0 && kept_w > 0 ? n_kept / kept_w : 1.0;
+    *a.factor = static_cast<float>(factor);
+    rl_rc_metrics* m = a.metrics;
+    if (!m) return;
+    m->w_before_sum = t[RD_W_BEFORE];
+    m->w_after_sum = t[RD_W_AFTER];
+    m->kept_w_sum = kept_w;
+    m->batch_norm_factor = factor;
+    m->final_sum = kept_w * factor;
+    m->final_min = n_kept > 0 ? t[kRcD + kRcC] * factor : 0.0;
+    m->final_max = n_kept > 0 ? t[kRcD + kRcC + 1] * factor : 0.0;
+    m->mis_kl_sum = t[RD_MIS_KL];
+    m->k3_sum = t[RD_K3];
+    m->abs_diff_sum = t[RD_ABS];
+    m->chi2_token_sum = t[RD_CHI2T];
+    m->train_lppl_sum = t[RD_TRAIN_LPPL];
+    m->rollout_lppl_sum = t[RD_ROLL_LPPL];
+    m->lppl_diff_sum = t[RD_LPPL_DIFF];
+    m->lppl_abs_diff_sum = t[RD_LPPL_ABS];
+    m->ppl_ratio_sum = t[RD_PPL_RATIO];
+    m->chi2_seq_sum = t[RD_CHI2S];
+    m->n_valid = static_cast<int64_t>(t[kRcD + RC_VALID]);
+    m->n_seq = static_cast<int64_t>(t[kRcD + RC_SEQ]);
+    m->n_kept = static_cast<int64_t>(n_kept);
+    m->n_tis_low = static_cast<int64_t>(t[kRcD + RC_TIS_LO]);
+    m->n_tis_high = static_cast<int64_t>(t[kRcD + RC_TIS_HI]);
+    m->n_rs_low = static_cast<int64_t>(t[kRcD + RC_RS_LO]);
+    m->n_rs_high = static_cast<int64_t>(t[kRcD + RC_RS_HI]);
+    m->n_cat_tokens = static_cast<int64_t>(t[kRcD + RC_CAT_TOK]);
+    m->n_cat_seqs = static_cast<int64_t>(t[kRcD + RC_CAT_SEQ]);
+    m->status = *a.status;
+}
+
+// A sequence of up to kRcChunk tokens is staged in shared memory whole, by bulk copies
+// when the arrays are 16-byte aligned (the aligned body; the few tokens past its last
+// 16-byte boundary by plain loads), and read from there by both passes.  A longer one is
+// staged kRcChunk tokens at a time with plain coalesced loads, chunk by chunk in each pass
+// (pass 2 starts from the chunk still staged).  A bulk copy must start on a 16-byte
+// boundary: it starts at the boundary at or before the sequence's first token and the
+// sequence sits at a small offset in the buffer (0..3 floats, 0..15 mask bytes).  128
+// threads and 37 KB of shared memory keep six blocks on an SM.  Loops stay rolled: the
+// code is fetched cold by every block, so its size is part of the latency.
+constexpr int kRcChunk = 4096;
 constexpr int kRcW = kRcThreads / 32;
 
-__global__ void __launch_bounds__(kRcThreads, 8) rc_seq_kernel(RcArgs a) {
-    __shared__ __align__(16) float s_lt[kRcChunk];
-    __shared__ __align__(16) float s_lr[kRcChunk];
-    __shared__ __align__(16) uint8_t s_m[kRcChunk];
+// The sums of up to 32 records (a group of sequence records, or the group records), as a
+// fixed-shape warp tree: lane l takes record r0 + l (a lane past r1 contributes the
+// identity), then a butterfly of five levels in which both lanes of an exchange add the
+// same operands in the same order, so the result does not depend on scheduling.  A warp
+// takes fields f = warp, warp + 4, ... (fp64 sums, int64 counts, min, max): five dependent
+// fp64 additions per field rather than one per record (fp64 is a slow pipe on this part).
+// Lane 0's results go to dsum / csum / mn / mx (shared, indexed by field).
+// Record fields that need the fp64 range (a sequence-level weight e^S n, chi^2 e^(2 S));
+// the others are sums of fp32 values and are carried as float-float pairs in their 8 bytes.
+RL_DEVINL constexpr bool rc_wide(int f) { return f == RD_W_BEFORE || f == RD_CHI2S; }
+
+struct RcRecs {
+    const double* d;
+    const long long* c;
+    const float* mn;
+    const float* mx;
+    int64_t ld;
+};
+RL_DEVINL void rc_sum_records(const RcRecs& r, int64_t r0, int64_t r1, double* dsum, long long* csum, float* mnmx) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t i = r0 + lane;
+    const bool in = i < r1;
+    constexpr int kPer = (kRcFields + kRcW - 1) / kRcW;
+    // every load of the warp's fields first (one round trip to L2 rather than one per field)
+    unsigned long long raw[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int f = warp + kRcW * k;
+        raw[k] = 0ull;
+        if (in && f < kRcFields) {
+            if (f < kRcD)
+                raw[k] = __ldcg(reinterpret_cast<const unsigned long long*>(r.d) + f * r.ld + i);
+            else if (f < kRcD + kRcC)
+                raw[k] = __ldcg(reinterpret_cast<const unsigned long long*>(r.c) + (f - kRcD) * r.ld + i);
+            else
+                raw[k] = __float_as_uint(__ldcg((f == kRcD + kRcC ? r.mn : r.mx) + i));
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+        const int f = warp + kRcW * k;
+        if (f >= kRcFields) continue;
+        if (f < kRcD && rc_wide(f)) {
+            double v = __longlong_as_double(static_cast<long long>(raw[k]));
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double u = __shfl_xor_sync(0xffffffffu, v, o);
+                v = (lane & o) ? u + v : v + u;
+            }
+            if (lane == 0) dsum[f] = v;
+        } else if (f < kRcD) {
+            FF v = {__uint_as_float(static_cast<unsigned>(raw[k])), __uint_as_float(static_cast<unsigned>(raw[k] >> 32))};
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const FF u = {__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+                v = (lane & o) ? ff_add(u, v) : ff_add(v, u);
+            }
+            if (lane == 0)
+                dsum[f] = __longlong_as_double(static_cast<long long>(__float_as_uint(v.hi)) |
+                                               (static_cast<long long>(__float_as_uint(v.lo)) << 32));
+        } else if (f < kRcD + kRcC) {
+            long long v = static_cast<long long>(raw[k]);
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) csum[f - kRcD] = v;
+        } else {
+            const bool is_min = f == kRcD + kRcC;
+            float v = in ? __uint_as_float(static_cast<unsigned>(raw[k])) : (is_min ? INFINITY : -INFINITY);
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_xor_sync(0xffffffffu, v, o);
+                v = is_min ? fminf(v, u) : fmaxf(v, u);
+            }
+            if (lane == 0) mnmx[f - kRcD - kRcC] = v;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kRcThreads, 6) rc_seq_kernel(RcArgs a) {
+    __shared__ __align__(16) float s_lt[kRcChunk + 4];
+    __shared__ __align__(16) float s_lr[kRcChunk + 4];
+    __shared__ __align__(16) uint8_t s_m[kRcChunk + 16];
+    __shared__ __align__(8) uint64_t bar;
     __shared__ FF shff[kRcW][4];
     __shared__ float shf[kRcW][5];
     __shared__ int shi[kRcW][6];
     __shared__ RcSeq sq;
+    __shared__ int role;
     const RcPrep& q = a.q;
     const int64_t b = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -141,7 +262,43 @@ __global__ void __launch_bounds__(kRcThreads, 8) rc_seq_kernel(RcArgs a) {
     const bool rs_seq = q.use_rs && q.rs_level == RL_LEVEL_SEQUENCE;
     const int64_t len = o1 - o0;
     const int nchunks = static_cast<int>((len + kRcChunk - 1) / kRcChunk);
-    auto stage = [&](int c) {   // chunk c into shared memory; returns its length
+    // token i of the staged chunk is s_lt[fo + i], s_lr[fo + i], s_m[mo + i]
+    int fo = 0, mo = 0;
+    const bool whole = nchunks == 1 &&
+                       ((reinterpret_cast<uintptr_t>(a.lt) | reinterpret_cast<uintptr_t>(a.lr) |
+                         reinterpret_cast<uintptr_t>(a.mask)) & 15) == 0;
+    if (whole) {
+        // the bodies from the 16-byte boundary at or before o0 to the last one at or before
+        // o1 by bulk copies, the rest of the sequence by plain loads
+        const int64_t f0 = o0 & ~int64_t(3), f1 = o1 & ~int64_t(3);
+        const int64_t m0 = o0 & ~int64_t(15), m1 = o1 & ~int64_t(15);
+        fo = static_cast<int>(o0 - f0);
+        mo = static_cast<int>(o0 - m0);
+        const uint32_t fb = static_cast<uint32_t>(4 * (f1 - f0)), mb = static_cast<uint32_t>(m1 - m0);
+        if (threadIdx.x == 0) {
+            mbar_init(&bar, 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(&bar, 2 * fb + mb);
+            if (fb > 0) {
+                bulk_load(s_lt, a.lt + f0, fb, &bar);
+                bulk_load(s_lr, a.lr + f0, fb, &bar);
+            }
+            if (mb > 0) bulk_load(s_m, a.mask + m0, mb, &bar);
+        }
+        for (int64_t t = (f1 > o0 ? f1 : o0) + threadIdx.x; t < o1; t += kRcThreads) {
+            s_lt[fo + (t - o0)] = a.lt[t];
+            s_lr[fo + (t - o0)] = a.lr[t];
+        }
+        for (int64_t t = (m1 > o0 ? m1 : o0) + threadIdx.x; t < o1; t += kRcThreads) s_m[mo + (t - o0)] = a.mask[t];
+        __syncthreads();   // the barrier's initialisation is visible
+        if (!mbar_wait(&bar, 0, a.status, a.wait_ns)) {
+            // a copy that never completed: the block's results are incomplete (the status
+            // says so); wait once more, bounded, for the copies before leaving
+            if (threadIdx.x == 0) mbar_wait(&bar, 0, a.status);
+        }
+        __syncthreads();
+    }
+    auto stage = [&](int c) {   // chunk c into shared memory (plain loads); returns its length
         const int64_t c0 = o0 + static_cast<int64_t>(c) * kRcChunk;
         const int n = static_cast<int>(o1 - c0 < kRcChunk ? o1 - c0 : kRcChunk);
         const float* lt = a.lt + c0;
@@ -150,7 +307,7 @@ __global__ void __launch_bounds__(kRcThreads, 8) rc_seq_kernel(RcArgs a) {
         int i0 = 0;
         if ((((reinterpret_cast<uintptr_t>(lt) | reinterpret_cast<uintptr_t>(lr)) & 15) |
              (reinterpret_cast<uintptr_t>(mk) & 3)) == 0) {
-            // 16-byte loads (4-byte for the mask), all of a thread's loads in flight at once
+            // 16-byte loads (4-byte for the mask)
             const int n4 = n >> 2;
 #pragma unroll 4
             for (int i = threadIdx.x; i < n4; i += kRcThreads) {
@@ -178,15 +335,20 @@ __global__ void __launch_bounds__(kRcThreads, 8) rc_seq_kernel(RcArgs a) {
     FF S = {0.f, 0.f}, E = {0.f, 0.f};   // the decisions' sums, float-float
     float st = 0.f, sr = 0.f;            // metric sums: fp32 per thread
     float mis = 0.f, k3 = 0.f, ad = 0.f, c2 = 0.f;
-    int staged = -1;
+    int staged = whole ? 0 : -1;
     for (int c = 0; c < nchunks; ++c) {
-        if (c > 0) __syncthreads();   // the previous chunk's readers are done
-        const int cn = stage(c);
-        staged = c;
+        int cn;
+        if (c == staged) {
+            cn = static_cast<int>(len);
+        } else {
+            if (c > 0) __syncthreads();   // the previous chunk's readers are done
+            cn = stage(c);
+            staged = c;
+        }
 #pragma unroll 1
         for (int i = threadIdx.x; i < cn; i += kRcThreads) {
-            if (s_m[i] == 0) continue;
-            const float x = s_lt[i], y = s_lr[i];
+            if (s_m[mo + i] == 0) continue;
+            const float x = s_lt[fo + i], y = s_lr[fo + i];
             const FF d = two_sum(x, -y);
             ++n;
             S = ff_add(S, d);
@@ -214,7 +376,8 @@ __global__ void __launch_bounds__(kRcThreads, 8) rc_seq_kernel(RcArgs a) {
         }
     }
     __syncthreads();
-    double seqd[7] = {0, 0, 0, 0, 0, 0, 0};   // w_before (sequence levels), lppl terms, chi2_seq
+    double seqd[2] = {0, 0};                   // w_before (sequence levels), chi2_seq: fp64 range
+    float seqf[5] = {0.f, 0.f, 0.f, 0.f, 0.f};   // the log-perplexity terms
     float tok1[4] = {0.f, 0.f, 0.f, 0.f};      // mis, k3, |d|, e^2d
     int nt = 0, catt = 0;
     if (threadIdx.x == 0) {
@@ -258,13 +421,13 @@ __global__ void __launch_bounds__(kRcThreads, 8) rc_seq_kernel(RcArgs a) {
             const float tr = -(Stb.hi + Stb.lo) * rn;
             const float ro = -(Srb.hi + Srb.lo) * rn;
             const float df = -(Sb.hi + Sb.lo) * rn;   // tr - ro = -S / n, from the exact sum of d
-            seqd[1] = tr;
-            seqd[2] = ro;
-            seqd[3] = df;
-            seqd[4] = fabsf(df);
-            seqd[5] = expf(df);
+            seqf[0] = tr;
+            seqf[1] = ro;
+            seqf[2] = df;
+            seqf[3] = fabsf(df);
+            seqf[4] = expf(df);
             // e^(2 S): fp32 while it fits, fp64 (one call) past the fp32 range
-            seqd[6] = Sb.hi < 44.f ? static_cast<double>(expf(2.f * Sb.hi) * (1.f + 2.f * Sb.lo))
+            seqd[1] = Sb.hi < 44.f ? static_cast<double>(expf(2.f * Sb.hi) * (1.f + 2.f * Sb.lo))
                                    : exp(2.0 * (static_cast<double>(Sb.hi) + static_cast<double>(Sb.lo)));
         }
         sq = s;
@@ -291,9 +454,9 @@ __global__ void __launch_bounds__(kRcThreads, 8) rc_seq_kernel(RcArgs a) {
         for (int i = threadIdx.x; i < cn; i += kRcThreads) {
             float wout = 0.f;
             uint8_t kp8 = 0;
-            if (s_m[i] != 0) {
+            if (s_m[mo + i] != 0) {
                 const bool tok = q.level == RL_LEVEL_TOKEN || (q.use_rs && q.rs_level == RL_LEVEL_TOKEN);
-                const FF d = tok ? two_sum(s_lt[i], -s_lr[i]) : FF{0.f, 0.f};
+                const FF d = tok ? two_sum(s_lt[fo + i], -s_lr[fo + i]) : FF{0.f, 0.f};
                 float w;
                 bool lo, hi;
                 if (q.level == RL_LEVEL_TOKEN) {
@@ -368,171 +531,106 @@ __global__ void __launch_bounds__(kRcThreads, 8) rc_seq_kernel(RcArgs a) {
             for (int f = 0; f < 5; ++f) I[f] += shi[w][f];
         }
         const int64_t B = a.B;
-        const double d[kRcD] = {q.level == RL_LEVEL_TOKEN ? static_cast<double>(F[2]) : seqd[0],
-                                F[0], F[1], tok1[0], tok1[1], tok1[2], tok1[3],
-                                seqd[1], seqd[2], seqd[3], seqd[4], seqd[5], seqd[6]};
-        for (int f = 0; f < kRcD; ++f) a.pd[f * B + b] = d[f];
+        // the two fp64-range fields as doubles, the others as float-float pairs (lo = 0)
+        a.pd[RD_W_BEFORE * B + b] = q.level == RL_LEVEL_TOKEN ? static_cast<double>(F[2]) : seqd[0];
+        a.pd[RD_CHI2S * B + b] = seqd[1];
+        const float nf[kRcD] = {0.f, F[0], F[1], tok1[0], tok1[1], tok1[2], tok1[3],
+                                seqf[0], seqf[1], seqf[2], seqf[3], seqf[4], 0.f};
+        for (int f = 0; f < kRcD; ++f)
+            if (!rc_wide(f)) reinterpret_cast<float2*>(a.pd)[f * B + b] = make_float2(nf[f], 0.f);
         const long long c[kRcC] = {nt, nt > 0 ? 1 : 0, I[0], I[1], I[2], I[3], I[4], catt, catt > 0 ? 1 : 0};
         for (int f = 0; f < kRcC; ++f) a.pc[f * B + b] = c[f];
         a.pmin[b] = F[3];
         a.pmax[b] = F[4];
-        if (q.use_tis && q.norm) {   // the factor's two totals, in any order of arrival
-            if (I[0] != 0) atomicAdd(reinterpret_cast<unsigned long long*>(a.kept_n), static_cast<unsigned long long>(I[0]));
-            if (fabsf(F[1]) < a.kept_lim) {
-                const long long x = __float2ll_rn(F[1] * 16777216.f);
-                if (x != 0) atomicAdd(reinterpret_cast<unsigned long long*>(a.kept_wfix), static_cast<unsigned long long>(x));
-            } else {
-                atomicExch(a.kept_range, 1);
+        // count the sequence in with its group: release (the record) and acquire (if this is
+        // the group's last, the other blocks' records)
+        const int64_t g = b / kRcGroup;
+        const int64_t gsize = a.B - g * kRcGroup < kRcGroup ? a.B - g * kRcGroup : kRcGroup;
+        unsigned int old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.gcnt + g) : "memory");
+        role = old == static_cast<unsigned int>(gsize - 1);
+    }
+    __syncthreads();
+    if (!role) return;
+    // the group's last block: its records into group record g
+    __shared__ double dsum[kRcD];
+    __shared__ long long csum[kRcC];
+    __shared__ float mnmx[2];
+    {
+        const int64_t g = b / kRcGroup;
+        const int64_t r0 = g * kRcGroup, r1 = r0 + kRcGroup < a.B ? r0 + kRcGroup : a.B;
+        rc_sum_records(RcRecs{a.pd, a.pc, a.pmin, a.pmax, a.B}, r0, r1, dsum, csum, mnmx);
+        __syncthreads();
+        const int f = threadIdx.x;
+        if (f < kRcD) a.gd[f * a.G + g] = dsum[f];
+        else if (f < kRcD + kRcC) a.gc[(f - kRcD) * a.G + g] = csum[f - kRcD];
+        else if (f == kRcD + kRcC) a.gmin[g] = mnmx[0];
+        else if (f == kRcD + kRcC + 1) a.gmax[g] = mnmx[1];
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            a.gcnt[g] = 0u;   // for the next call
+            unsigned int old;
+            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.tcnt) : "memory");
+            role = old == static_cast<unsigned int>(a.G - 1);
+        }
+        __syncthreads();
+        if (!role) return;
+    }
+    // the last group: the group records (32 at a time, the partial totals added in group
+    // order), then the factor and the metrics
+    {
+        __shared__ double tot[kRcFields];
+        for (int64_t g0 = 0; g0 < a.G; g0 += 32) {
+            rc_sum_records(RcRecs{a.gd, a.gc, a.gmin, a.gmax, a.G}, g0, g0 + 32 < a.G ? g0 + 32 : a.G, dsum, csum, mnmx);
+            __syncthreads();
+            const int f = threadIdx.x;
+            if (f < kRcFields) {
+                double x;
+                if (f < kRcD && !rc_wide(f)) {   // a float-float pair in the slot's bits
+                    const long long bits = __double_as_longlong(dsum[f]);
+                    x = static_cast<double>(__uint_as_float(static_cast<unsigned>(bits))) +
+                        static_cast<double>(__uint_as_float(static_cast<unsigned>(bits >> 32)));
+                } else {
+                    x = f < kRcD ? dsum[f] : (f < kRcD + kRcC ? static_cast<double>(csum[f - kRcD]) : mnmx[f - kRcD - kRcC]);
+                }
+                if (g0 == 0) tot[f] = x;
+                else if (f < kRcD + kRcC) tot[f] += x;
+                else if (f == kRcD + kRcC) tot[f] = fmin(tot[f], x);
+                else tot[f] = fmax(tot[f], x);
             }
+            __syncthreads();
+        }
+        if (threadIdx.x == 0) {
+            rc_write_metrics(a, tot);
+            *a.status = 0;     // for the next call
+            *a.tcnt = 0u;
         }
     }
 }
 
-// Warp f sums field f of the records over the sequences in order (lane l takes
-// b = l, l + 32, ..., sixteen loads in flight ahead of their adds, then a butterfly) into
-// tot[f].  With only_factor, just the two fields the batch-normalisation factor needs.
-// Every block that calls it computes the same bits.
-constexpr int kRcReduceThreads = 32 * kRcFields;
-RL_DEVINL void rc_reduce_fields(const RcArgs& a, double* tot, bool only_factor) {
-    const int f = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t B = a.B;
-    if (f >= kRcFields) return;
-    if (only_factor && f != RD_KEPT_W && f != kRcD + RC_KEPT) return;
-    if (f < kRcD) {
-        const double* src = a.pd + f * B;
-        double v = 0.0;
-        for (int64_t b0 = lane; b0 < B; b0 += 32 * 16) {
-            double x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : 0.0;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v += x[i];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) tot[f] = v;
-    } else if (f < kRcD + kRcC) {
-        const long long* src = a.pc + (f - kRcD) * B;
-        long long v = 0;
-        for (int64_t b0 = lane; b0 < B; b0 += 32 * 16) {
-            long long x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : 0;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v += x[i];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) tot[f] = static_cast<double>(v);
-    } else {
-        const bool is_min = f == kRcD + kRcC;
-        const float* src = is_min ? a.pmin : a.pmax;
-        float v = is_min ? INFINITY : -INFINITY;
-        for (int64_t b0 = lane; b0 < B; b0 += 32 * 16) {
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = b0 + 32 * i < B ? src[b0 + 32 * i] : v;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v = is_min ? fminf(v, x[i]) : fmaxf(v, x[i]);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float u = __shfl_xor_sync(0xffffffffu, v, o);
-            v = is_min ? fminf(v, u) : fmaxf(v, u);
-        }
-        if (lane == 0) tot[f] = v;
-    }
+
+
+// No sequence: zero sums, factor 1 (one thread).
+__global__ void rc_empty_kernel(RcArgs a) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    double t[kRcFields];
+    for (int f = 0; f < kRcFields; ++f) t[f] = 0.0;
+    rc_write_metrics(a, t);
+    *a.status = 0;
 }
 
-// The batch-normalisation factor n_kept / sum of kept weights: from the integer totals the
-// sequence blocks accumulated (t may then be null), else from the reduced fields t.
-RL_DEVINL bool rc_factor_fixed(const RcArgs& a) { return a.q.use_tis && a.q.norm && *a.kept_range == 0; }
-RL_DEVINL double rc_factor(const RcArgs& a, const double* t) {
-    if (!(a.q.use_tis && a.q.norm)) return 1.0;
-    double kept_w, n_kept;
-    if (rc_factor_fixed(a)) {
-        n_kept = static_cast<double>(*a.kept_n);
-        kept_w = static_cast<double>(*a.kept_wfix) * (1.0 / 16777216.0);
-    } else {
-        kept_w = t[RD_KEPT_W];
-        n_kept = t[kRcD + RC_KEPT];
-    }
-    return (n_kept > 0 && kept_w > 0) ? n_kept / kept_w : 1.0;
-}
-
-// The factor and the metrics from the reduced fields (one thread).
-RL_DEVINL void rc_write_metrics(const RcArgs& a, const double* t) {
-    const double kept_w = t[RD_KEPT_W], n_kept = t[kRcD + RC_KEPT];
-    const double factor = rc_factor(a, t);
-    *a.factor = static_cast<float>(factor);
-    rl_rc_metrics* m = a.metrics;
-    if (!m) return;
-    m->w_before_sum = t[RD_W_BEFORE];
-    m->w_after_sum = t[RD_W_AFTER];
-    m->kept_w_sum = kept_w;
-    m->batch_norm_factor = factor;
-    m->final_sum = kept_w * factor;
-    m->final_min = n_kept > 0 ? t[kRcD + kRcC] * factor : 0.0;
-    m->final_max = n_kept > 0 ? t[kRcD + kRcC + 1] * factor : 0.0;
-    m->mis_kl_sum = t[RD_MIS_KL];
-    m->k3_sum = t[RD_K3];
-    m->abs_diff_sum = t[RD_ABS];
-    m->chi2_token_sum = t[RD_CHI2T];
-    m->train_lppl_sum = t[RD_TRAIN_LPPL];
-    m->rollout_lppl_sum = t[RD_ROLL_LPPL];
-    m->lppl_diff_sum = t[RD_LPPL_DIFF];
-    m->lppl_abs_diff_sum = t[RD_LPPL_ABS];
-    m->ppl_ratio_sum = t[RD_PPL_RATIO];
-    m->chi2_seq_sum = t[RD_CHI2S];
-    m->n_valid = static_cast<int64_t>(t[kRcD + RC_VALID]);
-    m->n_seq = static_cast<int64_t>(t[kRcD + RC_SEQ]);
-    m->n_kept = static_cast<int64_t>(n_kept);
-    m->n_tis_low = static_cast<int64_t>(t[kRcD + RC_TIS_LO]);
-    m->n_tis_high = static_cast<int64_t>(t[kRcD + RC_TIS_HI]);
-    m->n_rs_low = static_cast<int64_t>(t[kRcD + RC_RS_LO]);
-    m->n_rs_high = static_cast<int64_t>(t[kRcD + RC_RS_HI]);
-    m->n_cat_tokens = static_cast<int64_t>(t[kRcD + RC_CAT_TOK]);
-    m->n_cat_seqs = static_cast<int64_t>(t[kRcD + RC_CAT_SEQ]);
-    m->status = *a.status;
-}
-
-
-// One block of kRcFields warps: the fields in sequence order, then the factor and the
-// metrics (used when no batch normalisation follows).
-__global__ void __launch_bounds__(kRcReduceThreads) rc_reduce_kernel(RcArgs a) {
-    __shared__ double tot[kRcFields];
-    rc_reduce_fields(a, tot, false);
-    __syncthreads();
-    if (threadIdx.x == 0) rc_write_metrics(a, tot);
-}
-
-// Batch normalisation: every block forms the factor (from the integer totals, or, when a
-// sequence's sum was out of their range, from the two fields it needs in the order
-// rc_reduce_kernel uses, so every block has the same bits), block 0 also reduces all the
-// fields and writes the metrics while the other blocks scale: w *= factor, float4 over the
-// 16-byte-aligned body (four loads in flight per thread) and scalars at the two ends.  One
-// launch where a reduce and a scale kernel would take two.
-__global__ void __launch_bounds__(kRcReduceThreads) rc_scale_kernel(RcArgs a) {
-    __shared__ double tot[kRcFields];
-    __shared__ float fac;
-    if (blockIdx.x == 0 || !rc_factor_fixed(a)) rc_reduce_fields(a, tot, blockIdx.x != 0);
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        fac = static_cast<float>(rc_factor(a, tot));
-        if (blockIdx.x == 0) rc_write_metrics(a, tot);
-    }
-    __syncthreads();
-    // block 0 (the metrics) takes no share of the scaling when there are other blocks
-    if (gridDim.x > 1 && blockIdx.x == 0) return;
-    const int64_t sb = gridDim.x > 1 ? blockIdx.x - 1 : 0, nsb = gridDim.x > 1 ? gridDim.x - 1 : 1;
-    const float f = fac;
+// Batch normalisation: w *= factor, float4 over the 16-byte-aligned body (four loads in
+// flight per thread) and scalars at the two ends.
+constexpr int kRcScaleThreads = 256;
+__global__ void __launch_bounds__(kRcScaleThreads) rc_scale_kernel(RcArgs a) {
+    const float f = *a.factor;
     float* w = a.w;
     const int64_t T = a.T;
     const int64_t head = ((16 - (reinterpret_cast<uintptr_t>(w) & 15)) & 15) / 4;
     const int64_t h = head < T ? head : T;
     const int64_t n4 = (T - h) / 4;
-    const int64_t tid = sb * blockDim.x + threadIdx.x;
-    const int64_t nth = nsb * blockDim.x;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
     float4* w4 = reinterpret_cast<float4*>(w + h);
 #pragma unroll 4
     for (int64_t i = tid; i < n4; i += nth) {
@@ -614,20 +712,29 @@ int rollout_named_impl(const rl_rc_metrics* m, const rl_rc_params* p, rl_rc_name
 // ----------------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------------
-// Workspace: a 256-byte header (status, factor, the factor's range flag and integer
-// totals), then the per-sequence records.
+// Workspace: a 256-byte header (the group counter at byte 0, the status word at 4, the
+// factor at 8), the per-sequence records, the group records and the per-group counters.
+// Zero before the first call; every call leaves the counters and the status word at zero.
 constexpr size_t kRcHeader = 256;
 
-static size_t rc_record_bytes(int64_t B) {
-    return align_up(static_cast<size_t>(B) * (kRcD * 8 + kRcC * 8 + 2 * 4) + 64, 256);
+static size_t rc_record_bytes(int64_t n) {   // n records of kRcD fp64, kRcC int64, min, max
+    return align_up(static_cast<size_t>(n) * (kRcD * 8 + kRcC * 8 + 2 * 4) + 64, 256);
 }
+static int64_t rc_groups(int64_t B) { return (B + kRcGroup - 1) / kRcGroup; }
 
-size_t rollout_ws_bytes(int64_t B) { return kRcHeader + rc_record_bytes(B < 1 ? 1 : B); }
+size_t rollout_ws_bytes(int64_t B) {
+    const int64_t b = B < 1 ? 1 : B, G = rc_groups(b);
+    return kRcHeader + rc_record_bytes(b) + rc_record_bytes(G) + align_up(static_cast<size_t>(G) * 4, 256);
+}
 
 int rollout_impl(const float* lt, const float* lr, const uint8_t* mask, const int64_t* off, int64_t B, int64_t T,
                  const rl_rc_params* p, float* w, uint8_t* keep, rl_rc_metrics* metrics, void* ws,
                  size_t ws_bytes, cudaStream_t stream) {
     if (ws_bytes < rollout_ws_bytes(B)) return RL_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 7u) != 0) {
+        set_last_error("rollout-correction workspace not 8-byte aligned");
+        return RL_ERR_ARG;
+    }
     RcArgs a{};
     a.lt = lt;
     a.lr = lr;
@@ -655,38 +762,36 @@ int rollout_impl(const float* lt, const float* lr, const uint8_t* mask, const in
     a.w = w;
     a.keep = keep;
     uint8_t* base = static_cast<uint8_t*>(ws);
+    a.tcnt = reinterpret_cast<unsigned int*>(base);
     a.status = reinterpret_cast<int32_t*>(base + 4);
     a.factor = reinterpret_cast<float*>(base + 8);
-    a.kept_range = reinterpret_cast<int*>(base + 12);
-    a.kept_n = reinterpret_cast<long long*>(base + 16);
-    a.kept_wfix = reinterpret_cast<long long*>(base + 24);
-    // a sequence's kept-weight sum below 2^38 / B keeps the total below 2^62 in 2^-24 units
-    a.kept_lim = static_cast<float>(ldexp(1.0, 38) / static_cast<double>(B > 0 ? B : 1));
+    const int64_t b1 = B < 1 ? 1 : B;
+    a.G = rc_groups(b1);
     uint8_t* rec = base + kRcHeader;
     a.pd = reinterpret_cast<double*>(rec);
-    a.pc = reinterpret_cast<long long*>(a.pd + kRcD * B);
-    a.pmin = reinterpret_cast<float*>(a.pc + kRcC * B);
-    a.pmax = a.pmin + B;
+    a.pc = reinterpret_cast<long long*>(a.pd + kRcD * b1);
+    a.pmin = reinterpret_cast<float*>(a.pc + kRcC * b1);
+    a.pmax = a.pmin + b1;
+    uint8_t* grec = rec + rc_record_bytes(b1);
+    a.gd = reinterpret_cast<double*>(grec);
+    a.gc = reinterpret_cast<long long*>(a.gd + kRcD * a.G);
+    a.gmin = reinterpret_cast<float*>(a.gc + kRcC * a.G);
+    a.gmax = a.gmin + a.G;
+    a.gcnt = reinterpret_cast<unsigned int*>(grec + rc_record_bytes(a.G));
+    a.wait_ns = wait_limit_ns();
     a.metrics = metrics;
-    {
-        ProfScope pm(RL_PROF_MEMSET, stream);
-        if (cudaMemsetAsync(ws, 0, 32, stream) != cudaSuccess) return RL_ERR_CUDA;   // status .. kept_wfix
-    }
-    ProfScope ps(RL_PROF_ROLLOUT, stream);   // the kernel launches alone
-    int launches = 0;
-    if (B > 0) {
+    ProfScope ps(RL_PROF_ROLLOUT, stream);   // the kernel launches
+    int launches = 1;
+    if (B > 0)
         rc_seq_kernel<<<static_cast<unsigned>(B), kRcThreads, 0, stream>>>(a);
+    else
+        rc_empty_kernel<<<1, 32, 0, stream>>>(a);
+    if (q.use_tis && q.norm && w != nullptr && T > 0) {
+        const int64_t blocks = (T / 4 + kRcScaleThreads - 1) / kRcScaleThreads + 1;
+        const int64_t cap = 4L * num_sms();
+        rc_scale_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), kRcScaleThreads, 0, stream>>>(a);
         ++launches;
     }
-    if (q.use_tis && q.norm && w != nullptr && T > 0) {
-        // the reduction rides along with the scaling (every block forms the factor)
-        const int64_t blocks = (T / 4 + kRcReduceThreads - 1) / kRcReduceThreads + 1;
-        const int64_t cap = 2L * num_sms();
-        rc_scale_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), kRcReduceThreads, 0, stream>>>(a);
-    } else {
-        rc_reduce_kernel<<<1, kRcReduceThreads, 0, stream>>>(a);
-    }
-    ++launches;
     count_launch(launches);
     return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }
