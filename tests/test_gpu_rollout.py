@@ -238,3 +238,20 @@ def test_named_metrics_ragged_against_the_oracle():
     for p in SETTINGS + [rh.RcParams(use_tis=False, rs_veto_threshold=1e-3),
                          rh.RcParams(tis_mode="mask", tis_lower_bound=0.8, tis_upper_bound=1.25)]:
         _named_compare(lt, lr, m, off, p)
+
+
+def test_repeated_calls_are_bitwise_identical():
+    """Sums in a fixed order (records by groups of 32 in sequence order, then the groups in
+    order, whichever block finishes last): three calls on one workspace, zeroed once, give
+    the same bits: weights, keep flags and the metrics struct."""
+    lt, lr, m, off = _c5()
+    d = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (lt, lr, m, np.asarray(off, np.int64))]
+    B = len(off) - 1
+    ws = torch.zeros(rh.rl_rollout_correction_workspace_bytes(B), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(3):
+        w, k, met = rh.rl_rollout_correction(*d, SETTINGS[1], ws=ws)
+        torch.cuda.synchronize()
+        outs.append((w.cpu().numpy().tobytes(), k.cpu().numpy().tobytes(), met.cpu().numpy().tobytes()))
+    assert outs[0] == outs[1] == outs[2]
+    assert rh.rc_metrics(met)["status"] == 0
