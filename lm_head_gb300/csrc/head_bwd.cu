@@ -589,62 +589,114 @@ __global__ void __launch_bounds__(256) radix_hist_kernel(const int32_t* keys, in
     for (int i = threadIdx.x; i < kDigits; i += blockDim.x) hist[static_cast<int64_t>(i) * tiles + blockIdx.x] = cnt[i];
 }
 
-// Exclusive scan over hist in digit-major order (single block).
+// Exclusive scan over hist in digit-major order (single block).  Each thread takes a
+// contiguous run of entries (16-byte loads, four in flight), the runs' sums are scanned
+// across the block with warp shuffles, then each thread writes its run's prefixes.
 __global__ void __launch_bounds__(1024) radix_scan_kernel(int32_t* hist, int64_t len, const int* gate) {
     if (gate_closed(gate)) return;
-    __shared__ int64_t part[1024];
-    const int64_t per = (len + blockDim.x - 1) / blockDim.x;
-    const int64_t b = threadIdx.x * per;
+    __shared__ int64_t wtot[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // len is a multiple of kDigits, so every run starts and ends on a 16-byte boundary
+    const int64_t per = ((len + blockDim.x - 1) / blockDim.x + 3) & ~int64_t(3);
+    const int64_t b = static_cast<int64_t>(threadIdx.x) * per;
     const int64_t e = b + per < len ? b + per : len;
     int64_t s = 0;
-    for (int64_t i = b; i < e; ++i) s += hist[i];
-    part[threadIdx.x] = s;
+#pragma unroll 4
+    for (int64_t i = b; i < e; i += 4) {
+        const int4 v = *reinterpret_cast<const int4*>(hist + i);
+        s += static_cast<int64_t>(v.x) + v.y + v.z + v.w;
+    }
+    // exclusive scan of the runs' sums over the block
+    int64_t x = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wtot[warp] = x;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int64_t run = 0;
-        for (int i = 0; i < static_cast<int>(blockDim.x); ++i) {
-            const int64_t v = part[i];
-            part[i] = run;
-            run += v;
+    if (warp == 0) {
+        int64_t t = lane < static_cast<int>(blockDim.x >> 5) ? wtot[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
         }
+        wtot[lane] = t;   // inclusive over warps
     }
     __syncthreads();
-    int64_t run = part[threadIdx.x];
-    for (int64_t i = b; i < e; ++i) {
-        const int32_t v = hist[i];
-        hist[i] = static_cast<int32_t>(run);
-        run += v;
+    int64_t run = x - s + (warp > 0 ? wtot[warp - 1] : 0);
+#pragma unroll 4
+    for (int64_t i = b; i < e; i += 4) {
+        int4 v = *reinterpret_cast<const int4*>(hist + i);
+        int4 o;
+        o.x = static_cast<int32_t>(run);
+        run += v.x;
+        o.y = static_cast<int32_t>(run);
+        run += v.y;
+        o.z = static_cast<int32_t>(run);
+        run += v.z;
+        o.w = static_cast<int32_t>(run);
+        run += v.w;
+        *reinterpret_cast<int4*>(hist + i) = o;
     }
 }
 
-// One warp per tile scatters its items in order: rank among equal digits inside each
-// group of 32 via match.any, plus running per-digit counters -> stable.
-__global__ void __launch_bounds__(32) radix_scatter_kernel(const int32_t* keys_in, const int32_t* vals_in,
-                                                           int64_t n, int shift, const int32_t* hist,
-                                                           int64_t tiles, int32_t* keys_out,
-                                                           int32_t* vals_out, const int* gate) {
+// One block of eight warps per tile; warp w takes the tile's items [256 w, 256 w + 256) in
+// order.  The warps' digit counts, scanned over the warps in order on top of the tile's
+// base from hist, give each warp its own running base per digit; within a warp the rank
+// among equal digits of each group of 32 comes from match.any.  Items keep their order
+// within a digit: stable.
+constexpr int kScatterWarps = kSortTile / 256;
+static_assert(kScatterWarps * 256 == kSortTile && kScatterWarps <= 32, "tiles of whole 256-item warp shares");
+__global__ void __launch_bounds__(256) radix_scatter_kernel(const int32_t* keys_in, const int32_t* vals_in,
+                                                            int64_t n, int shift, const int32_t* hist,
+                                                            int64_t tiles, int32_t* keys_out,
+                                                            int32_t* vals_out, const int* gate) {
     if (gate_closed(gate)) return;
-    __shared__ int base[kDigits];
-    const int lane = threadIdx.x;
-    for (int i = lane; i < kDigits; i += 32) base[i] = hist[static_cast<int64_t>(i) * tiles + blockIdx.x];
-    __syncwarp();
-    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kSortTile;
-    for (int i = 0; i < kSortTile; i += 32) {
-        const int64_t j = t0 + i + lane;
+    __shared__ int cnt[kScatterWarps][kDigits];   // counts, then running bases
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < kScatterWarps * kDigits; i += blockDim.x) (&cnt[0][0])[i] = 0;
+    // the warp's 256 items, eight per lane, all loads in flight
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kSortTile + warp * 256;
+    int32_t k[8], v[8];
+    int dg[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int64_t j = t0 + r * 32 + lane;
         const bool act = j < n;
-        const int32_t k = act ? keys_in[j] : 0;
-        const int digit = act ? ((k >> shift) & (kDigits - 1)) : kDigits;  // inactive lanes: own group
-        const unsigned peers = __match_any_sync(0xffffffffu, digit);
+        k[r] = act ? keys_in[j] : 0;
+        v[r] = act ? vals_in[j] : 0;
+        dg[r] = act ? ((k[r] >> shift) & (kDigits - 1)) : kDigits;   // inactive lanes: their own group
+    }
+    __syncthreads();   // counters zeroed
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+        if (dg[r] < kDigits) atomicAdd(&cnt[warp][dg[r]], 1);
+    __syncthreads();
+    for (int d = threadIdx.x; d < kDigits; d += blockDim.x) {
+        int run = hist[static_cast<int64_t>(d) * tiles + blockIdx.x];
+        for (int w = 0; w < kScatterWarps; ++w) {
+            const int c = cnt[w][d];
+            cnt[w][d] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const bool act = dg[r] < kDigits;
+        const unsigned peers = __match_any_sync(0xffffffffu, dg[r]);
         const int rank = __popc(peers & ((1u << lane) - 1u));
         int pos = 0;
-        if (act) pos = base[digit] + rank;
+        if (act) pos = cnt[warp][dg[r]] + rank;
         __syncwarp();
-        const int leader_hi = 31 - __clz(peers);  // highest lane of the group updates the counter
-        if (act && lane == leader_hi) base[digit] += __popc(peers);
+        const int leader_hi = 31 - __clz(peers);   // highest lane of the group updates the base
+        if (act && lane == leader_hi) cnt[warp][dg[r]] += __popc(peers);
         __syncwarp();
         if (act) {
-            keys_out[pos] = k;
-            vals_out[pos] = vals_in[j];
+            keys_out[pos] = k[r];
+            vals_out[pos] = v[r];
         }
     }
 }
@@ -659,14 +711,21 @@ __global__ void bucket_kernel(const int32_t* keys, int64_t n, int32_t V, int64_t
     for (int64_t v = prev + 1; v <= cur && v <= V + 1; ++v) bucket[v] = i;
 }
 
+// Four vocabulary rows per 256-thread block, 64 threads per row (8 columns per thread per
+// pass over the row's items, H / 512 passes): four times the rows in flight per SM of a
+// block per row, whose short life (two bucket loads, a few items, one 8 KB store) left
+// the SMs waiting on latency.
+constexpr int kDwRowsPerBlock = 4;
 __global__ void __launch_bounds__(256) sparse_dw_kernel(SparseArgs a, const int32_t* vals,
                                                         const int32_t* item_tok, const int64_t* bucket,
                                                         float* dW, int overwrite) {
     if (gate_closed(a.gate)) return;
-    const int64_t v = blockIdx.x;
+    constexpr int kRowThreads = 256 / kDwRowsPerBlock;
+    const int64_t v = static_cast<int64_t>(blockIdx.x) * kDwRowsPerBlock + threadIdx.x / kRowThreads;
+    if (v >= a.V) return;
     const int64_t b = bucket[v], e = bucket[v + 1];
     if (e <= b && !overwrite) return;   // overwrite: a row no item touches is written as zeros
-    for (int64_t h0 = static_cast<int64_t>(threadIdx.x) * 8; h0 < a.H; h0 += 256 * 8) {
+    for (int64_t h0 = static_cast<int64_t>(threadIdx.x % kRowThreads) * 8; h0 < a.H; h0 += kRowThreads * 8) {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int64_t i = b; i < e; ++i) {
             const int32_t item = vals[i];
@@ -719,7 +778,7 @@ static int sparse_dw(const SparseArgs& a, const BwdWs& w, float* dW, cudaStream_
         const int shift = p * kDigitBits;
         radix_hist_kernel<<<static_cast<unsigned>(tiles), 256, 0, s>>>(kin, n, shift, w.hist, tiles, a.gate);
         radix_scan_kernel<<<1, 1024, 0, s>>>(w.hist, tiles * kDigits, a.gate);
-        radix_scatter_kernel<<<static_cast<unsigned>(tiles), 32, 0, s>>>(kin, vin, n, shift, w.hist, tiles, kout,
+        radix_scatter_kernel<<<static_cast<unsigned>(tiles), 256, 0, s>>>(kin, vin, n, shift, w.hist, tiles, kout,
                                                                          vout, a.gate);
         count_launch(3);
         int32_t* tk = kin;
@@ -731,7 +790,8 @@ static int sparse_dw(const SparseArgs& a, const BwdWs& w, float* dW, cudaStream_
     }
     bucket_kernel<<<static_cast<unsigned>((n + 1 + 255) / 256), 256, 0, s>>>(kin, n, static_cast<int32_t>(a.V), w.bucket,
                                                                              a.gate);
-    sparse_dw_kernel<<<static_cast<unsigned>(a.V), 256, 0, s>>>(a, vin, w.item_tok, w.bucket, dW, overwrite);
+    sparse_dw_kernel<<<static_cast<unsigned>((a.V + kDwRowsPerBlock - 1) / kDwRowsPerBlock), 256, 0, s>>>(
+        a, vin, w.item_tok, w.bucket, dW, overwrite);
     count_launch(2);
     return cudaPeekAtLastError() == cudaSuccess ? RL_OK : RL_ERR_CUDA;
 }
