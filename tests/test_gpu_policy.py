@@ -189,10 +189,12 @@ def test_unaligned_inputs_take_the_exact_pass(offset):
     _compare(lt, lo, ls, A, m, rh.PgParams(), offset=offset)
 
 
-def test_huge_sum_terms():
+@pytest.mark.parametrize("packed", [False, True], ids=["padded", "packed"])
+def test_huge_sum_terms(packed):
     """A few tokens with log pi_old - log pi_rollout = 30 (k3 terms near e^30, beside terms
-    of order 1): block partials in fp32, the batch in fp64; outputs and metrics still match
-    the oracle."""
+    of order 1): past the range of the 2^-24 fixed-point accumulators, so the last block
+    redoes the batch's metrics with exact decisions; outputs and metrics still match the
+    oracle, on the padded pass and on the packed one."""
     rng = np.random.default_rng(21)
     T = 100_000
     ls = np.log(rng.random(T) * 0.9 + 0.05).astype(np.float32)
@@ -201,7 +203,7 @@ def test_huge_sum_terms():
     ls[::9999] = (lo[::9999] - 30.0).astype(np.float32)
     lt = (lo + rng.normal(0, 0.1, T)).astype(np.float32)
     A = rng.normal(0, 1, T).astype(np.float32)
-    m = np.ones(T, np.uint8)
+    m = None if packed else np.ones(T, np.uint8)
     gm, rm = _compare(lt, lo, ls, A, m, rh.PgParams())
     assert rm["k3"] > 1e13
 
@@ -263,11 +265,19 @@ def test_all_padding():
     assert gm["ipo_curve"] == [0] * len(pp.curve_eps)
 
 
-def test_bitwise_reproducible():
-    """Three c5 passes give identical bytes: metrics (the blocks' records summed in block
-    order, whatever the order in which blocks arrive) and outputs."""
+@pytest.mark.parametrize("packed", [False, True], ids=["padded", "packed"])
+def test_bitwise_reproducible(packed):
+    """Three c5 passes give identical bytes: metrics and outputs.  The blocks add integer
+    partials (order-free); in the packed pass the stages go to whichever block claims them
+    first, and each thread's four-token stage sum enters the fixed point on its own, so the
+    assignment does not show in the bits."""
     c = workloads.make_policy_case()
-    d = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in (c.lp_theta, c.lp_old, c.lp_samp, c.adv, c.mask)]
+    if packed:
+        p = c.packed()
+        arrays = (p["lp_theta"], p["lp_old"], p["lp_samp"], p["adv"])
+    else:
+        arrays = (c.lp_theta, c.lp_old, c.lp_samp, c.adv, c.mask)
+    d = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in arrays] + ([None] if packed else [])
     runs = []
     for _ in range(3):
         out = rh.rl_policy_loss_elementwise(*d, rh.PgParams())

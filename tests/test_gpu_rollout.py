@@ -255,3 +255,34 @@ def test_repeated_calls_are_bitwise_identical():
         outs.append((w.cpu().numpy().tobytes(), k.cpu().numpy().tobytes(), met.cpu().numpy().tobytes()))
     assert outs[0] == outs[1] == outs[2]
     assert rh.rc_metrics(met)["status"] == 0
+
+
+def test_unaligned_arrays_take_the_chunked_staging():
+    """The arrays one element past a 16-byte boundary: sequences of up to 4096 tokens are then
+    staged with plain loads instead of bulk copies; the results still equal the oracle's."""
+    rng = np.random.default_rng(17)
+    lens = rng.integers(1, 3000, size=40)
+    T = int(lens.sum())
+    off = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    lr = np.log(rng.random(T) * 0.98 + 0.01).astype(np.float32)
+    lt = np.minimum(lr + rng.normal(0, 0.2, T), 0).astype(np.float32)
+    m = (rng.random(T) < 0.9).astype(np.uint8)
+    d = []
+    for x in (lt, lr, m):
+        buf = torch.zeros(T + 1, dtype=torch.from_numpy(x).dtype, device="cuda")
+        buf[1:] = torch.from_numpy(x).cuda()
+        d.append(buf[1:])
+    assert d[0].data_ptr() % 16 != 0
+    offs = torch.from_numpy(off).cuda()
+    for p in SETTINGS:
+        w, k, met = rh.rl_rollout_correction(*d, offs, p)
+        torch.cuda.synchronize()
+        ref = rollout_correction(lt, lr, m, off, _oracle_params(p))
+        np.testing.assert_array_equal(k.cpu().numpy(), ref["keep"])
+        rw = ref["weights"]
+        wg = w.cpu().double().numpy()
+        assert np.all(np.abs(wg - rw) <= 4e-6 * np.abs(rw) + 1e-30)
+        gm = rh.rc_metrics(met)
+        assert gm["status"] == 0
+        for key in ("n_valid", "n_kept", "n_rs_low", "n_rs_high", "n_cat_tokens"):
+            assert gm[key] == ref["metrics"][key], key
