@@ -613,7 +613,7 @@ def run_ours(args):
     work_gib = (torch.cuda.max_memory_allocated(dev) - base_mem) / 2 ** 30
 
     # ---- side figure: the two-call path (forward, then backward with logit recompute) ----
-    unfused_ms = None
+    unfused_ms = kept_ms = kept_gib = None
     if not args.no_unfused:
         del ws_fb
         torch.cuda.empty_cache()
@@ -631,6 +631,29 @@ def run_ours(args):
         torch.cuda.synchronize()
         unfused_ms = e0.elapsed_time(e1) / min(args.steps, 3)
         del ws_f, ws_b
+        torch.cuda.empty_cache()
+        # the same two calls with the numerators kept by the forward (keep_e: 2 N V bf16 in
+        # the saved state, no logit recompute in the backward)
+        import dataclasses
+        hk = dataclasses.replace(hp, keep_e=1)
+        saved_k = torch.empty(rh.rl_head_saved_bytes_ex(N, nnz, V, hk), dtype=torch.uint8, device=dev)
+        ws_f = torch.empty(rh.rl_head_fwd_workspace_bytes(N, H, V, nnz, hk), dtype=torch.uint8, device=dev)
+        ws_b = torch.empty(rh.rl_head_bwd_workspace_bytes(N, H, V, nnz, hk), dtype=torch.uint8, device=dev)
+        for i in range(2 + min(args.steps, 3)):
+            if i == 2:
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+            rh.rl_head_loss_fwd(batch, hk, ws=ws_f, saved=saved_k, status=status)
+            rh.rl_head_loss_bwd(batch, hk, saved_k, dloss, dhidden=dX, dW=dW, ws=ws_b, status=status)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e1.record()
+        torch.cuda.synchronize()
+        kept_ms = e0.elapsed_time(e1) / min(args.steps, 3)
+        kept_gib = (saved_k.numel() + ws_f.numel() + ws_b.numel()) / 2 ** 30
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {rh.status_names(int(status.item()))}")
+        del ws_f, ws_b, saved_k
         torch.cuda.empty_cache()
         ws_fb = torch.empty(rh.rl_head_fwd_bwd_workspace_bytes(N, H, V, nnz, hp), dtype=torch.uint8, device=dev)
 
@@ -714,6 +737,9 @@ def run_ours(args):
             "step_tflops_6NHV": step_tflops,
             "peak_gib": peak_gib, "workspace_peak_gib": work_gib,
             "two_call_ms_per_step": unfused_ms,
+            "two_call_keep_e": None if kept_ms is None else
+                {"ms_per_step": kept_ms, "held_gib": kept_gib,
+                 "note": "rl_head_loss_fwd then rl_head_loss_bwd with keep_e=1: the forward keeps e / e^T of every token"},
             "roofline": roof, "kernels": kernels,
             "e2e": {"value": e_value, "unit": "tokens/s", "ms_per_step": e_ms, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

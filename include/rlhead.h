@@ -106,6 +106,16 @@ typedef struct rl_params {
                                      over the vocabulary, so a nonzero value rules out the sparse
                                      backward (RL_BWD_SPARSE then returns RL_ERR_ARG) and makes
                                      the fused BF16 backward recompute the logits (8 N H V) */
+    int32_t keep_e;               /* 1: rl_head_loss_fwd keeps the bf16 softmax numerators
+                                     e = exp(z - z_label) of every token, in both layouts (2 N V
+                                     bf16 values), in the saved state, and rl_head_loss_bwd runs
+                                     the fused call's backward on them: 6 N H V of tensor work for
+                                     the two calls instead of 8 (no logit recompute), the same
+                                     bits as rl_head_loss_fwd_bwd.  The saved state is then
+                                     rl_head_saved_bytes_ex bytes, and one backward consumes it
+                                     (it folds the gradient's spikes into the kept values).
+                                     Takes effect with a dense backward, BF16 gradients and no
+                                     entropy term; ignored otherwise.  Default 0. */
 } rl_params;
 
 /* Ragged per-token sampler support, CSR over tokens ("TokenSupport", pull request #4233,
@@ -168,6 +178,10 @@ typedef struct rl_head_outputs {
 
 /* Bytes of the caller-owned state the forward saves for the backward. */
 size_t rl_head_saved_bytes(int64_t N, int64_t nnz);
+/* Saved-state bytes for these params: rl_head_saved_bytes, plus with keep_e in effect the
+ * kept numerators (e [N, V] and e^T [V, N rounded up to 128] bf16), a reference logit per
+ * token and a flag per token chunk. */
+size_t rl_head_saved_bytes_ex(int64_t N, int64_t nnz, int64_t V, const rl_params* params);
 /* Workspace bytes of rl_head_loss_fwd / rl_head_loss_bwd for these sizes and knobs. */
 size_t rl_head_fwd_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz,
                                    const rl_params* params);
@@ -180,14 +194,17 @@ size_t rl_head_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz,
 int rl_validate_support(const rl_head_batch* batch, int32_t* dev_status, void* stream);
 
 /* Forward: per-token loss, label / support log-probs, entropy, masks, metrics, and the
- * saved state (`saved`, device, rl_head_saved_bytes) for the backward. */
+ * saved state (`saved`, device, rl_head_saved_bytes_ex: rl_head_saved_bytes unless keep_e) for
+ * the backward. */
 int rl_head_loss_fwd(const rl_head_batch* batch, const rl_params* params,
                      const rl_head_outputs* out, void* saved, void* ws, size_t ws_bytes,
                      int32_t* dev_status, void* stream);
 
 /* Backward of sum_t dloss[t] * loss_t.  dloss: device [N] fp32 (the caller's aggregation,
  * e.g. 1 / #RL tokens for a token mean).  dhidden: device [N, H] bf16, overwritten.
- * dW: device [V, H] fp32; accumulate_dW != 0 adds into it, else it is overwritten. */
+ * dW: device [V, H] fp32; accumulate_dW != 0 adds into it, else it is overwritten.
+ * params must be the forward's.  With keep_e in effect it runs on the numerators the
+ * forward kept (no logit recompute) and leaves them changed: call it once per forward. */
 int rl_head_loss_bwd(const rl_head_batch* batch, const rl_params* params, const void* saved,
                      const float* dloss, void* dhidden, float* dW, int accumulate_dW,
                      void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);

@@ -58,7 +58,7 @@ class RlParams(ctypes.Structure):
                 ("icepop_low", ctypes.c_float), ("icepop_high", ctypes.c_float),
                 ("adv_tau", ctypes.c_float), ("temperature", ctypes.c_float),
                 ("kl_coeff", ctypes.c_float), ("token_chunk", ctypes.c_int32),
-                ("entropy_coeff", ctypes.c_float)]
+                ("entropy_coeff", ctypes.c_float), ("keep_e", ctypes.c_int32)]
 
 
 class RlSupport(ctypes.Structure):
@@ -135,6 +135,8 @@ _lib = None
 
 _SIGS = {
     "rl_head_saved_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
+    "rl_head_saved_bytes_ex": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                                 ctypes.POINTER(RlParams)]),
     "rl_head_fwd_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 4 + [ctypes.c_void_p]),
     "rl_head_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 4 + [ctypes.c_void_p]),
     "rl_validate_support": (ctypes.c_int, [ctypes.c_void_p] * 3),
@@ -238,12 +240,13 @@ class HeadParams:
     all_replayed: int = 0
     token_chunk: int = 0
     entropy_coeff: float = 0.0
+    keep_e: int = 0
 
     def c(self) -> RlParams:
         return RlParams(self.loss_type, self.kl_estimator, self.kl_staleness, self.bwd_mode,
                         self.grad_precision, self.all_replayed, self.eps, self.max_importance_ratio,
                         self.icepop_low, self.icepop_high, self.adv_tau, self.temperature,
-                        self.kl_coeff, self.token_chunk, self.entropy_coeff)
+                        self.kl_coeff, self.token_chunk, self.entropy_coeff, self.keep_e)
 
 
 @dataclasses.dataclass
@@ -332,6 +335,11 @@ def rl_head_saved_bytes(N: int, nnz: int) -> int:
     return int(load().rl_head_saved_bytes(N, nnz))
 
 
+def rl_head_saved_bytes_ex(N: int, nnz: int, V: int, params: HeadParams) -> int:
+    p = params.c()
+    return int(load().rl_head_saved_bytes_ex(N, nnz, V, ctypes.byref(p)))
+
+
 def rl_head_fwd_workspace_bytes(N, H, V, nnz, params: HeadParams) -> int:
     p = params.c()
     return int(load().rl_head_fwd_workspace_bytes(N, H, V, nnz, ctypes.byref(p)))
@@ -364,7 +372,7 @@ def rl_head_loss_fwd(batch: HeadBatch, params: HeadParams, *, ws: Optional[torch
         lse=torch.empty(N, **f32), mask_label=torch.empty(N, dtype=torch.uint8, device=dev),
         mask_support=torch.empty(max(nnz, 1), dtype=torch.uint8, device=dev)[:nnz],
         metrics_dev=torch.zeros(ctypes.sizeof(RlHeadMetrics), dtype=torch.uint8, device=dev),
-        saved=saved if saved is not None else _u8(rl_head_saved_bytes(N, nnz), dev),
+        saved=saved if saved is not None else _u8(rl_head_saved_bytes_ex(N, nnz, batch.V, params), dev),
         status=torch.zeros(1, dtype=torch.int32, device=dev) if status is None else status)
     wsb = rl_head_fwd_workspace_bytes(N, batch.H, batch.V, nnz, params)
     if ws is None:

@@ -80,6 +80,16 @@ size_t rl_head_saved_bytes(int64_t N, int64_t nnz) {
     return bytes;
 }
 
+size_t rl_head_saved_bytes_ex(int64_t N, int64_t nnz, int64_t V, const rl_params* params) {
+    if (N < 0 || nnz < 0 || V <= 0 || !params) return 0;
+    size_t bytes = 0;
+    if (keep_e_active(params))
+        kept_view(nullptr, N, nnz, V, params, &bytes);
+    else
+        saved_view(nullptr, N, nnz, &bytes);
+    return bytes;
+}
+
 size_t rl_head_fwd_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* params) {
     (void)params;
     if (N < 0 || H <= 0 || V <= 0 || nnz < 0) return 0;
@@ -90,6 +100,7 @@ size_t rl_head_fwd_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz,
 
 size_t rl_head_bwd_workspace_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* params) {
     if (N < 0 || H <= 0 || V <= 0 || nnz < 0 || !params) return 0;
+    if (keep_e_active(params)) return kept_bwd_ws_bytes(N, H, V, nnz, params);
     size_t bytes = 0;
     bwd_ws_view(nullptr, N, H, V, nnz, params, &bytes);
     return bytes;

@@ -799,9 +799,13 @@ static int sparse_dw(const SparseArgs& a, const BwdWs& w, float* dW, cudaStream_
 // ----------------------------------------------------------------------------------
 // Entry
 // ----------------------------------------------------------------------------------
+static int head_bwd_kept(const rl_head_batch* b, const rl_params* prm, const void* saved, const float* dloss,
+                         void* dhidden, float* dW, int accumulate, void* ws, int32_t* status, cudaStream_t stream);
+
 int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* saved,
                   const float* dloss, void* dhidden, float* dW, int accumulate, void* ws,
                   int32_t* status, cudaStream_t stream) {
+    if (keep_e_active(prm)) return head_bwd_kept(b, prm, saved, dloss, dhidden, dW, accumulate, ws, status, stream);
     const int64_t N = b->N, H = b->H, V = b->V, nnz = b->support.nnz;
     if (N == 0) {
         if (!accumulate && V > 0)
@@ -1131,13 +1135,15 @@ struct FusedWs {
     BwdWs bw;   // Wt, Xt, dxs [chunk, H], resid, sort buffers; G, Gt, G_lo, Gt_lo with hi/lo
 };
 
+// kept: the backward of the kept-numerator two-call path, whose e / e^T and reference
+// logits live in the saved state: no forward workspace and no chunk copies of them here.
 static FusedWs fused_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* prm,
-                             size_t* bytes) {
+                             size_t* bytes, bool kept = false) {
     FusedWs f{};
     f.chunk = bwd_chunk(N, prm);
     f.nchunks = (N + f.chunk - 1) / f.chunk;
     size_t fb = 0;
-    f.fw = fwd_ws_view(base, f.chunk, H, V, nnz, &fb);
+    if (!kept) f.fw = fwd_ws_view(base, f.chunk, H, V, nnz, &fb);
     Carve c(base ? static_cast<uint8_t*>(base) + fb : nullptr);
     c.off = 0;
     f.ldm = (V + 31) / 32;
@@ -1153,9 +1159,11 @@ static FusedWs fused_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_
         w.G_lo = c.take<uint16_t>(static_cast<size_t>(f.chunk) * V);
         w.Gt_lo = c.take<uint16_t>(static_cast<size_t>(V) * f.chunk);
     } else {
-        f.Eb = c.take<uint16_t>(static_cast<size_t>(f.chunk) * V);
-        f.Ebt = c.take<uint16_t>(static_cast<size_t>(V) * f.chunk);
-        f.cref = c.take<float>(f.chunk);
+        if (!kept) {
+            f.Eb = c.take<uint16_t>(static_cast<size_t>(f.chunk) * V);
+            f.Ebt = c.take<uint16_t>(static_cast<size_t>(V) * f.chunk);
+            f.cref = c.take<float>(f.chunk);
+        }
         f.rs = c.take<float>(f.chunk);
         f.dls = c.take<float>(N);
         f.gates = c.take<int>(f.nchunks + 1);
@@ -1188,6 +1196,203 @@ size_t fused_ws_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_par
     size_t bytes = 0;
     fused_ws_view(nullptr, N, H, V, nnz, prm, &bytes);
     return bytes;
+}
+
+// The BF16 backward of one token chunk from its softmax numerators e / e^T (the fused
+// call's chunk buffers, or the ones the forward kept for every token), once the row scales
+// rs are formed: the gated logit recompute for a chunk whose range flag is up, the spikes
+// folded into e, X^T scaled by rs, the sparse part of the rows that cannot fold, dX and dW.
+struct ChunkE {
+    uint16_t* Eb;        // [n, V] from the chunk's first token
+    uint16_t* Ebt;       // [V, ldt] from the chunk's first token's column
+    int64_t ldt;
+    const float* cref;   // [n]
+    float* rs;           // [n]
+    int* flag;           // the chunk's range flag
+};
+static int bf16_chunk_bwd(const rl_head_batch* b, const rl_params* prm, const SavedView& sv, const float* dloss,
+                          int64_t c0, int64_t n, int64_t ci, const FusedWs& f, const ChunkE& ce, const SparseArgs& sa,
+                          const CUtensorMap& tmW, const CUtensorMap& tmWt, void* dhidden, float* dW, int accumulate,
+                          int32_t* status, cudaStream_t stream) {
+    const int64_t H = b->H, V = b->V, nnz = b->support.nnz;
+    const BwdWs& w = f.bw;
+    const float inv_T = 1.0f / prm->temperature;
+    const uint16_t* Xc = static_cast<const uint16_t*>(b->hidden) + c0 * H;
+    int rc;
+    // out-of-range chunk only: G recomputed from the logits into Eb / Ebt (rs := 1)
+    CUtensorMap tmX;
+    if ((rc = make_tmap_bf16(&tmX, Xc, n, H, H, kBM)) != RL_OK) return rc;
+    EpiGrad::Params gp{n, static_cast<int32_t>(V), inv_T, sv.lse + c0, dloss + c0, sv.dcoef + c0,
+                       ce.Eb, ce.Ebt, nullptr, nullptr, ce.ldt, ce.flag, sv.mterm + c0 * 8, prm->entropy_coeff};
+    const GemmPlan pg = make_plan_auto(n, V, H, 1, 1 << 30, 1, status);
+    {
+        ProfScope ps(RL_PROF_GEMM_GRAD, stream);
+        if ((rc = launch_gemm_auto<EpiGrad>(tmX, tmX, tmW, pg, gp, stream)) != RL_OK) return rc;
+    }
+    count_launch();
+    {
+        FoldArgs fa{c0, n, V, nnz, ce.ldt, b->labels, b->support.offsets, b->support.ids, dloss,
+                    sv.labcoef, sv.entcoef, sv.zlab, sv.zsup, sv.dcoef, sv.lse, inv_T, ce.cref, ce.rs, ce.flag,
+                    ce.Eb, ce.Ebt, f.dls, f.gates + ci, f.gates + f.nchunks, sv.mterm, prm->entropy_coeff};
+        ProfScope ps(RL_PROF_RESID, stream);
+        fold_kernel<<<static_cast<unsigned>((n + 7) / 8), 256, 0, stream>>>(fa);
+        count_launch();
+    }
+    if ((rc = transpose_bf16(Xc, n, H, H, w.Xt, f.chunk, stream, ce.rs, ce.flag)) != RL_OK) return rc;
+    CUtensorMap tmA, tmAt, tmXt;
+    if ((rc = make_tmap_bf16(&tmA, ce.Eb, n, V, V, kBM)) != RL_OK) return rc;
+    if ((rc = make_tmap_bf16(&tmAt, ce.Ebt, V, n, ce.ldt, kBM)) != RL_OK) return rc;
+    {
+        SparseArgs sc = sa;
+        sc.gate = f.gates + ci;
+        ProfScope ps(RL_PROF_SPARSE_DX, stream);
+        sparse_dx_kernel<false><<<static_cast<unsigned>(n), 256, 0, stream>>>(sc, c0, w.dxs, nullptr);
+        count_launch();
+    }
+    if ((rc = make_tmap_b(&tmXt, w.Xt, H, n, f.chunk)) != RL_OK) return rc;
+    EpiDx::Params dp{n, static_cast<int32_t>(H), w.dxs, static_cast<uint16_t*>(dhidden) + c0 * H, ce.rs, ce.flag,
+                     f.gates + ci};
+    const GemmPlan p2 = make_plan_auto(n, H, V, 1, 1 << 30, 0, status);
+    {
+        ProfScope ps(RL_PROF_GEMM_DX, stream);
+        if ((rc = launch_gemm_auto<EpiDx>(tmA, tmA, tmWt, p2, dp, stream)) != RL_OK) return rc;
+    }
+    EpiDw::Params wp{V, static_cast<int32_t>(H), (c0 > 0 || accumulate) ? 1 : 0, dW};
+    const GemmPlan p3 = make_plan_auto(V, H, n, 1, 1 << 30, 0, status);
+    {
+        ProfScope ps(RL_PROF_GEMM_DW, stream);
+        if ((rc = launch_gemm_auto<EpiDw>(tmAt, tmAt, tmXt, p3, wp, stream)) != RL_OK) return rc;
+    }
+    count_launch(2);
+    return RL_OK;
+}
+
+// ----------------------------------------------------------------------------------
+// Kept numerators (rl_params.keep_e): the two-call path without the logit recompute
+// ----------------------------------------------------------------------------------
+bool keep_e_active(const rl_params* prm) {
+    return prm != nullptr && prm->keep_e != 0 && bwd_is_dense(prm) && prm->grad_precision == RL_GRAD_BF16 &&
+           prm->entropy_coeff == 0.f;
+}
+
+KeptView kept_view(void* saved, int64_t N, int64_t nnz, int64_t V, const rl_params* prm, size_t* bytes) {
+    size_t sb = 0;
+    saved_view(nullptr, N, nnz, &sb);
+    Carve c(saved ? static_cast<uint8_t*>(saved) + sb : nullptr);
+    KeptView k{};
+    k.chunk = bwd_chunk(N, prm);
+    k.nchunks = (N + k.chunk - 1) / k.chunk;
+    k.ldt = (N + kBM - 1) / kBM * kBM;
+    k.Eb = c.take<uint16_t>(static_cast<size_t>(N) * V);
+    k.Ebt = c.take<uint16_t>(static_cast<size_t>(V) * k.ldt);
+    k.cref = c.take<float>(N);
+    k.flags = c.take<int>(k.nchunks > 0 ? k.nchunks : 1);
+    if (bytes) *bytes = align_up(sb + c.off, 256);
+    return k;
+}
+
+size_t kept_bwd_ws_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* prm) {
+    size_t bytes = 0;
+    fused_ws_view(nullptr, N, H, V, nnz, prm, &bytes, true);
+    return bytes;
+}
+
+// Forward with keep_e: per token chunk, the reference logits, then the forward GEMM that
+// also stores e (row-major, from the chunk's first row) and e^T (columns from the chunk's
+// first token, leading dimension N rounded up to 128) into the saved state and raises the chunk's flag when
+// a row's logits leave the bf16 range around its reference.  Everything else as the plain
+// forward.
+int head_fwd_kept(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out, void* saved,
+                  void* ws, int32_t* status, cudaStream_t stream) {
+    const int64_t N = b->N, H = b->H, V = b->V, nnz = b->support.nnz;
+    int rc = validate_impl(b, status, stream);
+    if (rc != RL_OK) return rc;
+    if (N == 0) return RL_OK;
+    const SavedView sv = saved_view(saved, N, nnz, nullptr);
+    const KeptView k = kept_view(saved, N, nnz, V, prm, nullptr);
+    const FwdWs w = fwd_ws_view(ws, N, H, V, nnz, nullptr);
+    const float inv_T = 1.0f / prm->temperature;
+    if (cudaMemsetAsync(k.flags, 0, sizeof(int) * k.nchunks, stream) != cudaSuccess) return RL_ERR_CUDA;
+    for (int64_t c0 = 0, ci = 0; c0 < N; c0 += k.chunk, ++ci) {
+        const int64_t n = N - c0 < k.chunk ? N - c0 : k.chunk;
+        const uint16_t* Xc = static_cast<const uint16_t*>(b->hidden) + c0 * H;
+        {
+            ProfScope ps(RL_PROF_REF_LOGIT, stream);
+            ref_logit_kernel<<<static_cast<unsigned>((n + 7) / 8), 256, 0, stream>>>(
+                Xc, static_cast<const uint16_t*>(b->weight), b->labels + c0, n, H, V, kLog2e * inv_T, k.cref + c0,
+                k.flags + ci);
+            count_launch();
+        }
+        EStore es;
+        es.Eb = k.Eb + c0 * V;
+        es.Ebt = k.Ebt + c0;
+        es.ldt = k.ldt;
+        es.cref = k.cref + c0;
+        es.flag = k.flags + ci;
+        es.rs = nullptr;      // the row scales need dloss: the backward forms them
+        es.dloss = nullptr;
+        if ((rc = fwd_rows(b, prm, out, sv, w, c0, n, &es, 0, status, stream)) != RL_OK) return rc;
+    }
+    if (out->metrics) return metrics_impl(b, saved, out->metrics, ws, stream);
+    return RL_OK;
+}
+
+// rs_t = alpha 2^(cref_t - lse_t log2 e) with alpha = dloss_t dcoef_t / T, formed as the
+// fused call's token pass forms it (the same bits); a gap outside the bf16 range, or a
+// non-finite factor, raises the chunk's recompute flag.  Chunk-relative arrays.
+__global__ void __launch_bounds__(256) rs_kernel(const float* dloss, const float* dcoef, const float* lse,
+                                                 const float* cref, float inv_T, int64_t n, float* rs, int* flag) {
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (r >= n) return;
+    const float alpha = __fmul_rn(__fmul_rn(dloss[r], dcoef[r]), inv_T);
+    float v = 0.f;
+    if (alpha != 0.f) {
+        const float gap = __fsub_rn(cref[r], __fmul_rn(lse[r], kLog2e));
+        v = __fmul_rn(alpha, exp2_approx(gap));
+        if (!(gap >= -kRefRangeLog2 && gap <= kRefRangeLog2) || !isfinite(v)) *flag = 1;
+    }
+    rs[r] = v;
+}
+
+// Backward with keep_e: the fused call's backward, chunk by chunk, on the kept numerators.
+static int head_bwd_kept(const rl_head_batch* b, const rl_params* prm, const void* saved, const float* dloss,
+                         void* dhidden, float* dW, int accumulate, void* ws, int32_t* status, cudaStream_t stream) {
+    const int64_t N = b->N, H = b->H, V = b->V, nnz = b->support.nnz;
+    if (N == 0) {
+        if (!accumulate && V > 0 &&
+            cudaMemsetAsync(dW, 0, static_cast<size_t>(V) * H * sizeof(float), stream) != cudaSuccess)
+            return RL_ERR_CUDA;
+        return RL_OK;
+    }
+    void* sp = const_cast<void*>(saved);
+    const SavedView sv = saved_view(sp, N, nnz, nullptr);
+    const KeptView k = kept_view(sp, N, nnz, V, prm, nullptr);
+    const FusedWs f = fused_ws_view(ws, N, H, V, nnz, prm, nullptr, true);
+    const float inv_T = 1.0f / prm->temperature;
+    SparseArgs sa{N, H, V, nnz,
+                  static_cast<const uint16_t*>(b->weight), static_cast<const uint16_t*>(b->hidden),
+                  b->labels, b->support.offsets, b->support.ids, f.dls, sv.labcoef, sv.entcoef,
+                  inv_T, nullptr, f.gates + f.nchunks};
+    if (cudaMemsetAsync(f.gates, 0, sizeof(int) * (f.nchunks + 1), stream) != cudaSuccess) return RL_ERR_CUDA;
+    int rc = transpose_bf16(b->weight, V, H, H, f.bw.Wt, V, stream);
+    if (rc != RL_OK) return rc;
+    CUtensorMap tmW, tmWt;
+    if ((rc = make_tmap_b(&tmW, b->weight, V, H, H)) != RL_OK) return rc;
+    if ((rc = make_tmap_b(&tmWt, f.bw.Wt, H, V, V)) != RL_OK) return rc;
+    for (int64_t c0 = 0, ci = 0; c0 < N; c0 += f.chunk, ++ci) {
+        const int64_t n = N - c0 < f.chunk ? N - c0 : f.chunk;
+        {
+            ProfScope ps(RL_PROF_TOKEN_LOSS, stream);
+            rs_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+                dloss + c0, sv.dcoef + c0, sv.lse + c0, k.cref + c0, inv_T, n, f.rs, k.flags + ci);
+            count_launch();
+        }
+        const ChunkE ce{k.Eb + c0 * V, k.Ebt + c0, k.ldt, k.cref + c0, f.rs, k.flags + ci};
+        if ((rc = bf16_chunk_bwd(b, prm, sv, dloss, c0, n, ci, f, ce, sa, tmW, tmWt, dhidden, dW, accumulate,
+                                 status, stream)) != RL_OK)
+            return rc;
+    }
+    return sparse_dw(sa, f.bw, dW, stream);
 }
 
 int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out,
@@ -1254,31 +1459,11 @@ int head_fused_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_
         if (!w.split && prm->entropy_coeff != 0.f && cudaMemsetAsync(flag, 1, 1, stream) != cudaSuccess)
             return RL_ERR_CUDA;
         if (!w.split) {
-            // out-of-range chunk only: G recomputed from the logits into Eb / Ebt (rs := 1)
-            CUtensorMap tmX;
-            if ((rc = make_tmap_bf16(&tmX, Xc, n, H, H, kBM)) != RL_OK) return rc;
-            EpiGrad::Params gp{n, static_cast<int32_t>(V), inv_T, sv.lse + c0, dloss + c0, sv.dcoef + c0,
-                               f.Eb, f.Ebt, nullptr, nullptr, f.chunk, flag, sv.mterm + c0 * 8,
-                               prm->entropy_coeff};
-            const GemmPlan pg = make_plan_auto(n, V, H, 1, 1 << 30, 1, status);
-            {
-                ProfScope ps(RL_PROF_GEMM_GRAD, stream);
-                if ((rc = launch_gemm_auto<EpiGrad>(tmX, tmX, tmW, pg, gp, stream)) != RL_OK) return rc;
-            }
-            count_launch();
-            {
-                FoldArgs fa{c0, n, V, nnz, f.chunk, b->labels, b->support.offsets, b->support.ids, dloss,
-                            sv.labcoef, sv.entcoef, sv.zlab, sv.zsup, sv.dcoef, sv.lse, inv_T, f.cref, f.rs, flag,
-                            f.Eb, f.Ebt, f.dls, f.gates + ci, f.gates + f.nchunks, sv.mterm, prm->entropy_coeff};
-                ProfScope ps(RL_PROF_RESID, stream);
-                fold_kernel<<<static_cast<unsigned>((n + 7) / 8), 256, 0, stream>>>(fa);
-                count_launch();
-            }
-            if ((rc = transpose_bf16(Xc, n, H, H, w.Xt, f.chunk, stream, f.rs, flag)) != RL_OK) return rc;
-            if ((rc = make_tmap_bf16(&tmA, f.Eb, n, V, V, kBM)) != RL_OK) return rc;
-            if ((rc = make_tmap_bf16(&tmAt, f.Ebt, V, n, f.chunk, kBM)) != RL_OK) return rc;
-            tmAlo = tmA;
-            tmAtlo = tmAt;
+            const ChunkE ce{f.Eb, f.Ebt, f.chunk, f.cref, f.rs, flag};
+            if ((rc = bf16_chunk_bwd(b, prm, sv, dloss, c0, n, ci, f, ce, sa, tmW, tmWt, dhidden, dW, accumulate,
+                                     status, stream)) != RL_OK)
+                return rc;
+            continue;
         } else {
             // spike residuals of the chunk's tokens, then G / G^T (hi/lo) from e
             ResidArgs ra{c0, n, V, nnz, b->labels, b->support.offsets, b->support.ids, dloss, sv.dcoef, sv.lse,

@@ -1023,6 +1023,7 @@ int loss_from_shards_impl(const rl_head_batch* b, const rl_params* prm, int32_t 
 
 int head_fwd_impl(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out,
                   void* saved, void* ws, int32_t* status, cudaStream_t stream) {
+    if (keep_e_active(prm)) return head_fwd_kept(b, prm, out, saved, ws, status, stream);
     const int64_t N = b->N, H = b->H, V = b->V, nnz = b->support.nnz;
     int rc = validate_impl(b, status, stream);
     if (rc != RL_OK) return rc;

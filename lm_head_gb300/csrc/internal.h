@@ -133,6 +133,25 @@ int loss_from_shards_impl(const rl_head_batch* b, const rl_params* prm, int32_t 
                           const float* zlab, const float* zsup, const rl_head_outputs* out, void* saved, void* ws,
                           int32_t* status, cudaStream_t stream);
 int64_t bwd_chunk(int64_t N, const rl_params* prm);
+// rl_params.keep_e in effect: a dense backward with BF16 gradients and no entropy term.
+bool keep_e_active(const rl_params* prm);
+// The kept numerators in the saved state, after the standard saved data: e [N, V] and
+// e^T [V, N] bf16, the reference logit per token, the range flag per token chunk.
+struct KeptView {
+    uint16_t* Eb;
+    uint16_t* Ebt;        // [V, ldt]: ldt = N rounded up to 128 (TMA strides are multiples of 16 bytes)
+    int64_t ldt;
+    float* cref;
+    int* flags;
+    int64_t chunk, nchunks;
+};
+KeptView kept_view(void* saved, int64_t N, int64_t nnz, int64_t V, const rl_params* prm, size_t* bytes);
+// The forward with keep_e: per token chunk the reference logits, then the forward GEMM that
+// also stores e / e^T into the saved state.
+int head_fwd_kept(const rl_head_batch* b, const rl_params* prm, const rl_head_outputs* out, void* saved,
+                  void* ws, int32_t* status, cudaStream_t stream);
+// Workspace of the backward on kept numerators.
+size_t kept_bwd_ws_bytes(int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* prm);
 int head_bwd_impl(const rl_head_batch* b, const rl_params* prm, const void* saved,
                   const float* dloss, void* dhidden, float* dW, int accumulate, void* ws,
                   int32_t* status, cudaStream_t stream);

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_struct_sizes_match_the_header_layout():
-    assert ctypes.sizeof(rh.RlParams) == 15 * 4
+    assert ctypes.sizeof(rh.RlParams) == 16 * 4
     assert ctypes.sizeof(rh.RlHeadMetrics) == 8 * 8 + 6 * 8
     assert ctypes.sizeof(rh.RlPgMetrics) == 6 * 8 + 6 * 8 + 16 * 8 + 8   # ..., ipo_curve[16], status
 
@@ -142,3 +142,18 @@ def test_options_and_new_entry_points_check_their_arguments(lib):
     assert lib.rl_rollout_metrics_named(ctypes.c_void_p(1 << 20), ctypes.byref(bad), ctypes.c_void_p(1 << 20),
                                         None) == rh.RL_ERR_ARG
     assert ctypes.sizeof(rh.RlRcNamed) == 28 * 8
+
+
+def test_saved_bytes_ex_grows_only_where_keep_e_applies():
+    """The saved state holds the kept numerators (2 N V bf16 and a little more) exactly when
+    keep_e can take effect: a dense backward, BF16 gradients, no entropy term."""
+    N, nnz, V = 1000, 5000, 4096
+    base = rh.rl_head_saved_bytes(N, nnz)
+    on = rh.HeadParams(bwd_mode=rh.RL_BWD_DENSE, keep_e=1)
+    assert rh.rl_head_saved_bytes_ex(N, nnz, V, on) >= base + 2 * 2 * N * V
+    for p in (rh.HeadParams(bwd_mode=rh.RL_BWD_DENSE),
+              rh.HeadParams(bwd_mode=rh.RL_BWD_DENSE, keep_e=1, grad_precision=rh.RL_GRAD_SPLIT),
+              rh.HeadParams(bwd_mode=rh.RL_BWD_SPARSE, keep_e=1),
+              rh.HeadParams(bwd_mode=rh.RL_BWD_DENSE, keep_e=1, entropy_coeff=0.1)):
+        assert rh.rl_head_saved_bytes_ex(N, nnz, V, p) == base
+    assert rh.rl_head_bwd_workspace_bytes(N, 2048, V, nnz, on) < rh.rl_head_fwd_bwd_workspace_bytes(N, 2048, V, nnz, on)

@@ -257,3 +257,42 @@ def test_entropy_regulariser_fused_and_two_call(prec):
     ref = oracle.head_forward(case.numpy(), oracle_params(hp))
     check_forward(case, hp, fwd, ref)
     check_backward(case, hp, batch, fwd, both=False)
+
+
+@pytest.mark.parametrize("far", [False, True], ids=["in-range", "recompute-chunk"])
+def test_keep_e_two_call_equals_fused(far):
+    """keep_e: rl_head_loss_fwd keeps the bf16 numerators e / e^T of every token in the
+    saved state and rl_head_loss_bwd runs the fused call's backward on them.  Over three
+    token chunks the forward outputs, dX and dW equal the fused call's bit for bit; with
+    far=True three rows of the second chunk put their label ~86 nats below the row's max,
+    so that chunk takes the gated logit recompute in both."""
+    if far:
+        case = workloads.make_head_case("c1", n_tokens=300, hidden_scale=60.0, noise=0.1, seed=121)
+        inp = case.numpy()
+        z = inp["hidden"] @ inp["W"].T
+        for t in (140, 141, 200):
+            v = int(np.argmin(z[t]))
+            lse = float(np.max(z[t]) + np.log(np.sum(np.exp(z[t] - np.max(z[t])))))
+            case.labels[t] = v
+            case.label_logq[t] = float(z[t, v] - lse)
+    else:
+        case = workloads.make_head_case("c1", n_tokens=300, hidden_scale=8.0, noise=0.7, loss_mask_frac=0.1,
+                                        age_max=4, seed=141)
+    hp = rh.HeadParams(loss_type=rh.RL_LOSS_IPO, eps=0.2, max_importance_ratio=3.0, kl_coeff=0.03,
+                       kl_estimator=rh.RL_KL_EXACT, kl_staleness=rh.RL_STALE_INV_SQRT, bwd_mode=rh.RL_BWD_DENSE,
+                       token_chunk=128)
+    hk = dataclasses.replace(hp, keep_e=1)
+    dev = case.to("cuda")
+    batch = rh.HeadBatch.from_case(dev)
+    mask = dev.loss_mask.float()
+    dl = (mask / mask.sum()).contiguous()
+    fwd, dX, dW = rh.rl_head_loss_fwd_bwd(batch, hp, dl)
+    f2 = rh.rl_head_loss_fwd(batch, hk)
+    assert f2.saved.numel() == rh.rl_head_saved_bytes_ex(case.N, case.nnz, case.V, hk)
+    assert f2.saved.numel() > rh.rl_head_saved_bytes(case.N, case.nnz) + 2 * 2 * case.N * case.V
+    dX2, dW2, st = rh.rl_head_loss_bwd(batch, hk, f2.saved, dl)
+    torch.cuda.synchronize()
+    assert f2.status_bits() == 0 and int(st.item()) == 0
+    for a, b in ((fwd.loss, f2.loss), (fwd.logp_label, f2.logp_label), (fwd.logp_support, f2.logp_support),
+                 (fwd.lse, f2.lse), (fwd.entropy, f2.entropy), (dX, dX2), (dW, dW2)):
+        assert torch.equal(a, b)
