@@ -240,6 +240,8 @@ int rl_head_loss_fwd_bwd(const rl_head_batch* batch, const rl_params* params,
  *                forward combines its vocabulary splits (the same bits on every rank).
  *   backward  rl_head_loss_bwd on the rank's rows with the local ids and the saved state of
  *             step 4: dW of its rows, and its part of dX (bf16), which the ranks all-reduce.
+ * keep_e does not apply: rl_head_shard_stats and rl_head_loss_from_shard_stats return
+ * RL_ERR_ARG when it would take effect (their saved state holds no numerators).
  * Unmeasured on hardware with more than one GPU: one process here emulates the ranks. */
 
 /* ids_local[i] = ids[i] - vocab_begin for an id inside [vocab_begin, vocab_end), -1 below

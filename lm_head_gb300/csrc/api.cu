@@ -34,6 +34,7 @@ int check_params(const rl_params* p) {
     if (!(p->entropy_coeff >= 0.f) || !std::isfinite(p->entropy_coeff)) return fail(RL_ERR_ARG, "bad entropy_coeff");
     if (p->entropy_coeff != 0.f && p->bwd_mode == RL_BWD_SPARSE)
         return fail(RL_ERR_ARG, "the entropy term's gradient is dense: no sparse backward with entropy_coeff > 0");
+    if (p->keep_e != 0 && p->keep_e != 1) return fail(RL_ERR_ARG, "keep_e must be 0 or 1");
     return RL_OK;
 }
 
@@ -182,6 +183,7 @@ int rl_head_shard_stats(const rl_head_batch* shard, const rl_params* params, flo
     int rc = check_batch(shard);
     if (rc != RL_OK) return rc;
     if ((rc = check_params(params)) != RL_OK) return rc;
+    if (keep_e_active(params)) return fail(RL_ERR_ARG, "keep_e is for the single-GPU forward, not a vocabulary shard");
     if (shard->N > 0 && (!stats || !zlab || (shard->support.nnz > 0 && !zsup))) return fail(RL_ERR_ARG, "output NULL");
     if (!dev_status) return fail(RL_ERR_ARG, "dev_status NULL");
     if (ws_bytes < rl_head_fwd_workspace_bytes(shard->N, shard->H, shard->V, shard->support.nnz, params) || !ws)
@@ -198,6 +200,8 @@ int rl_head_loss_from_shard_stats(const rl_head_batch* batch, const rl_params* p
     int rc = check_shape(batch->N, batch->H, batch->V, batch->support.nnz);
     if (rc != RL_OK) return rc;
     if ((rc = check_params(params)) != RL_OK) return rc;
+    if (keep_e_active(params))
+        return fail(RL_ERR_ARG, "keep_e is for the single-GPU forward: the shard path's saved state holds no numerators");
     if (n_shards < 1 || n_shards > 4096) return fail(RL_ERR_ARG, "n_shards out of [1, 4096]");
     const bool any = batch->N > 0;
     if (any && (!batch->labels || !batch->label_logq || !batch->adv || !batch->support.offsets ||

@@ -157,3 +157,20 @@ def test_saved_bytes_ex_grows_only_where_keep_e_applies():
               rh.HeadParams(bwd_mode=rh.RL_BWD_DENSE, keep_e=1, entropy_coeff=0.1)):
         assert rh.rl_head_saved_bytes_ex(N, nnz, V, p) == base
     assert rh.rl_head_bwd_workspace_bytes(N, 2048, V, nnz, on) < rh.rl_head_fwd_bwd_workspace_bytes(N, 2048, V, nnz, on)
+
+
+def test_shard_entry_points_refuse_keep_e():
+    """The vocabulary-split forward writes no kept numerators, so a backward told to use them
+    would read past the saved state: both shard entry points refuse keep_e on the host,
+    before touching the device."""
+    lib = rh.load()
+    fake = 1 << 20   # 16-byte aligned, never dereferenced: the call fails before any device work
+    sup = rh.RlSupport(fake, fake, fake, fake, 8)
+    b = rh.RlHeadBatch(fake, fake, 4, 128, 1024, fake, fake, fake, None, None, sup)
+    p = rh.HeadParams(bwd_mode=rh.RL_BWD_DENSE, keep_e=1).c()
+    st = ctypes.c_void_p(fake)
+    assert lib.rl_head_shard_stats(ctypes.byref(b), ctypes.byref(p), fake, fake, fake, fake, 1 << 40, st,
+                                   None) == rh.RL_ERR_ARG
+    assert lib.rl_head_loss_from_shard_stats(ctypes.byref(b), ctypes.byref(p), 2, fake, fake, fake, None, fake,
+                                             fake, 1 << 40, st, None) == rh.RL_ERR_ARG
+    assert b"keep_e" in lib.rl_last_error()
