@@ -417,7 +417,7 @@ def time_head_config(rh, torch, dev, case, hp, steps: int, warmup: int, peaks: d
     burst = float(peaks["bf16_tflops"])
     hbm = float(peaks["hbm_gbs"])
     out = {"workload": what, "N": N, "nnz": nnz, "ms_per_step": ms, "tokens_per_s": N / (ms / 1e3),
-           "token_chunk": hp.token_chunk or min(8192, (N + 127) // 128 * 128),
+           "token_chunk": rh.rl_head_token_chunk(N, case.H, hp),
            "grad_precision": "split" if hp.grad_precision == rh.RL_GRAD_SPLIT else "bf16",
            "held_gib": held, "recomputed_chunks": int(m["recomputed_chunks"]),
            "kernels_ms_per_step": {k: t / steps for k, (t, n) in sorted(prof.items(), key=lambda kv: -kv[1][0])}}
@@ -458,7 +458,7 @@ def side_configs(rh, torch, dev, case4, steps: int, warmup: int, peaks: dict) ->
     out = {"c4_split": time_head_config(rh, torch, dev, case4, dataclasses.replace(base, grad_precision=rh.RL_GRAD_SPLIT),
                                         steps, warmup, peaks, "c4, grad_precision SPLIT (bf16 hi + lo operand)")}
     out["c4_chunks"] = [time_head_config(rh, torch, dev, case4, dataclasses.replace(base, token_chunk=c), steps, warmup,
-                                         peaks, f"c4, token_chunk {c}") for c in (4096, 8192, 16384, 32768)]
+                                         peaks, f"c4, token_chunk {c}") for c in (4096, 8192, 9728, 16384, 32768)]
     c2 = workloads.make_head_case("c2", device=dev, variant="pages")
     hp2 = rh.HeadParams(loss_type=rh.RL_LOSS_ICEPOP, icepop_low=0.5, icepop_high=2.0, bwd_mode=rh.RL_BWD_DENSE)
     out["c2"] = time_head_config(rh, torch, dev, c2, hp2, steps, warmup, peaks,
@@ -701,7 +701,8 @@ def run_ours(args):
         n_chunks = prof["gemm_fwd_stats"][1] / args.steps
         flops_per_launch["gemm_bwd_grad"] = 2.0 * N * H * V / n_chunks * recomputed / (prof["gemm_bwd_grad"][1] / args.steps)
     # the captured per-launch traffic holds for the dense path at the default 8192-token chunk
-    traffic_ok = not args.sparse and not hp.token_chunk and N >= 8192 and args.grad_precision == "bf16"
+    chunk = rh.rl_head_token_chunk(N, H, hp)
+    traffic_ok = (not args.sparse and chunk == TRAFFIC_CHUNK and N >= chunk and args.grad_precision == "bf16")
     dom = max(prof.items(), key=lambda kv: kv[1][0])
     dom_name, (dom_ms, dom_n) = dom
     peak_sus = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]))
@@ -765,11 +766,13 @@ def run_ours(args):
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of each kernel, from the ncu
-# capture of the kernel as it stands (one launch at the library's default 8192-token chunk),
-# summarised in profiles/gemm_pair_dram_traffic_8k_chunk.md.
-TRAFFIC = {"gemm_fwd_stats": 1131648000 + 4935729152, "gemm_bwd_dx": 5748131840 + 30051072,
-           "gemm_bwd_dw": 4488490240 + 1219097088}
-TRAFFIC_SOURCE = "ncu capture at the 8192-token chunk, profiles/gemm_pair_dram_traffic_8k_chunk.md (not measured in this run)"
+# capture of the kernel as it stands (one launch at the library's default chunk on this
+# part, 9728 tokens), summarised in profiles/gemm_pair_dram_traffic_9728_chunk.md.
+TRAFFIC_CHUNK = 9728
+TRAFFIC = {"gemm_fwd_stats": 1061985536 + 5871818752,
+           "gemm_bwd_dx": 11018044928 + 34386176,
+           "gemm_bwd_dw": 7238419712 + 1228881152}
+TRAFFIC_SOURCE = "ncu capture at the 9728-token chunk, profiles/gemm_pair_dram_traffic_9728_chunk.md (not measured in this run)"
 
 
 def ctypes_metrics_size(rh):

@@ -98,8 +98,11 @@ typedef struct rl_params {
     float temperature;            /* T > 0; logits are (W h) / T */
     float kl_coeff;               /* >= 0; default 0 */
     int32_t token_chunk;          /* backward token chunk (multiple of 128); 0 = library default
-                                     (8192): memory held grows with it (about chunk x V x 4 bytes
-                                     for the bf16 softmax numerators of the fused call) */
+                                     (rl_head_token_chunk: the first multiple of the GEMM row tile
+                                     at or above 8192 at which the dX GEMM fills whole waves of
+                                     the device, 9728 with H = 2048 on 152 SMs): memory held grows
+                                     with it (about chunk x V x 4 bytes for the bf16 softmax
+                                     numerators of the fused call) */
     float entropy_coeff;          /* >= 0; default 0.  "10-KL-clip-entropy", section 3: the
                                      exploration regulariser, loss_t -= entropy_coeff * H_t with
                                      H_t the full-vocabulary token entropy; its gradient is dense
@@ -178,6 +181,9 @@ typedef struct rl_head_outputs {
 
 /* Bytes of the caller-owned state the forward saves for the backward. */
 size_t rl_head_saved_bytes(int64_t N, int64_t nnz);
+/* The token chunk the backward and the fused call use for these sizes and params on the
+ * current device (params->token_chunk if set; see rl_params.token_chunk). */
+int64_t rl_head_token_chunk(int64_t N, int64_t H, const rl_params* params);
 /* Saved-state bytes for these params: rl_head_saved_bytes, plus with keep_e in effect the
  * kept numerators (e [N, V] and e^T [V, N rounded up to 128] bf16), a reference logit per
  * token and a flag per token chunk. */

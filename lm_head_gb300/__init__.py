@@ -137,6 +137,7 @@ _SIGS = {
     "rl_head_saved_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
     "rl_head_saved_bytes_ex": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                                  ctypes.POINTER(RlParams)]),
+    "rl_head_token_chunk": (ctypes.c_int64, [ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(RlParams)]),
     "rl_head_fwd_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 4 + [ctypes.c_void_p]),
     "rl_head_bwd_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int64] * 4 + [ctypes.c_void_p]),
     "rl_validate_support": (ctypes.c_int, [ctypes.c_void_p] * 3),
@@ -333,6 +334,11 @@ def _u8(n, device):
 
 def rl_head_saved_bytes(N: int, nnz: int) -> int:
     return int(load().rl_head_saved_bytes(N, nnz))
+
+
+def rl_head_token_chunk(N: int, H: int, params: HeadParams) -> int:
+    p = params.c()
+    return int(load().rl_head_token_chunk(N, H, ctypes.byref(p)))
 
 
 def rl_head_saved_bytes_ex(N: int, nnz: int, V: int, params: HeadParams) -> int:

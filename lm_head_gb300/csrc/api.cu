@@ -81,6 +81,11 @@ size_t rl_head_saved_bytes(int64_t N, int64_t nnz) {
     return bytes;
 }
 
+int64_t rl_head_token_chunk(int64_t N, int64_t H, const rl_params* params) {
+    if (N < 0 || H <= 0 || !params) return 0;
+    return bwd_chunk(N, H, params);
+}
+
 size_t rl_head_saved_bytes_ex(int64_t N, int64_t nnz, int64_t V, const rl_params* params) {
     if (N < 0 || nnz < 0 || V <= 0 || !params) return 0;
     size_t bytes = 0;

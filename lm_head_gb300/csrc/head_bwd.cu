@@ -30,12 +30,34 @@ bool bwd_is_dense(const rl_params* prm) {
     return !(knobs_sparse || prm->all_replayed != 0);
 }
 
-// Default token chunk of the backward (and of the fused forward + backward): 8192.  At the
-// 64k-token batch a step took the same time with 8192 as with 16384 (85.7 ms each, one
-// box) and holds 4.7 GiB less (the bf16 softmax numerators, both layouts, are chunk x V
-// x 4 bytes); 4096 took 4 % longer.
-int64_t bwd_chunk(int64_t N, const rl_params* prm) {
-    int64_t c = prm->token_chunk > 0 ? prm->token_chunk : 8192;
+// Default token chunk of the backward (and of the fused forward + backward): the first
+// multiple of the GEMM's row tile at or above 8192 tokens at which the dX GEMM's tiles
+// (row blocks x H / 256 column tiles) fill whole waves of the GEMM's units (SM pairs, or
+// SMs): 9728 with H = 2048 on 152 SMs (38 row blocks x 8 = 4 waves of 76 pairs), where 8192
+// left a last wave 37 % full.  At the 64k-token batch 9728 took 83.4 / 84.2 ms against
+// 84.1 / 85.8 at 8192 in alternating runs (dX 24.8 / 25.0 ms against 27.5 / 28.1); 16384
+// held 4.7 GiB more for the same time as 8192, 4096 took 4 % longer.  Falls back to 8192
+// if no such multiple lies below 16384.
+static int64_t gcd64(int64_t a, int64_t b) {
+    while (b != 0) {
+        const int64_t t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+int64_t bwd_chunk(int64_t N, int64_t H, const rl_params* prm) {
+    int64_t c = prm->token_chunk;
+    if (c <= 0) {
+        const bool pair = gemm_pair_mode() != 0;
+        const int64_t units = pair ? num_sms() / 2 : num_sms();
+        const int64_t rows = pair ? 2 * kBM : kBM;
+        const int64_t cols = (H + kBN - 1) / kBN;
+        const int64_t step = units / gcd64(units, cols > 0 ? cols : 1);   // row blocks per whole-wave set
+        const int64_t rb = (8192 / rows + step - 1) / step * step;
+        c = rb * rows;
+        if (c < 8192 || c >= 16384) c = 8192;
+    }
     c = (c + kBM - 1) / kBM * kBM;
     const int64_t n128 = (N + kBM - 1) / kBM * kBM;
     if (c > n128) c = n128;
@@ -52,7 +74,7 @@ BwdWs bwd_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz, cons
     BwdWs w{};
     w.dense = bwd_is_dense(prm);
     w.split = prm->grad_precision == RL_GRAD_SPLIT;
-    w.chunk = bwd_chunk(N, prm);
+    w.chunk = bwd_chunk(N, H, prm);
     const int64_t items = nnz + N;
     if (w.dense) {
         w.Wt = c.take<uint16_t>(static_cast<size_t>(V) * H);
@@ -1140,7 +1162,7 @@ struct FusedWs {
 static FusedWs fused_ws_view(void* base, int64_t N, int64_t H, int64_t V, int64_t nnz, const rl_params* prm,
                              size_t* bytes, bool kept = false) {
     FusedWs f{};
-    f.chunk = bwd_chunk(N, prm);
+    f.chunk = bwd_chunk(N, H, prm);
     f.nchunks = (N + f.chunk - 1) / f.chunk;
     size_t fb = 0;
     if (!kept) f.fw = fwd_ws_view(base, f.chunk, H, V, nnz, &fb);
@@ -1280,13 +1302,12 @@ KeptView kept_view(void* saved, int64_t N, int64_t nnz, int64_t V, const rl_para
     saved_view(nullptr, N, nnz, &sb);
     Carve c(saved ? static_cast<uint8_t*>(saved) + sb : nullptr);
     KeptView k{};
-    k.chunk = bwd_chunk(N, prm);
-    k.nchunks = (N + k.chunk - 1) / k.chunk;
+    k.chunks_max = (N + kBM - 1) / kBM;   // the smallest chunk is one row tile
     k.ldt = (N + kBM - 1) / kBM * kBM;
     k.Eb = c.take<uint16_t>(static_cast<size_t>(N) * V);
     k.Ebt = c.take<uint16_t>(static_cast<size_t>(V) * k.ldt);
     k.cref = c.take<float>(N);
-    k.flags = c.take<int>(k.nchunks > 0 ? k.nchunks : 1);
+    k.flags = c.take<int>(k.chunks_max > 0 ? k.chunks_max : 1);
     if (bytes) *bytes = align_up(sb + c.off, 256);
     return k;
 }
@@ -1312,9 +1333,11 @@ int head_fwd_kept(const rl_head_batch* b, const rl_params* prm, const rl_head_ou
     const KeptView k = kept_view(saved, N, nnz, V, prm, nullptr);
     const FwdWs w = fwd_ws_view(ws, N, H, V, nnz, nullptr);
     const float inv_T = 1.0f / prm->temperature;
-    if (cudaMemsetAsync(k.flags, 0, sizeof(int) * k.nchunks, stream) != cudaSuccess) return RL_ERR_CUDA;
-    for (int64_t c0 = 0, ci = 0; c0 < N; c0 += k.chunk, ++ci) {
-        const int64_t n = N - c0 < k.chunk ? N - c0 : k.chunk;
+    const int64_t chunk = bwd_chunk(N, H, prm);   // the backward's chunk
+    const int64_t nchunks = (N + chunk - 1) / chunk;
+    if (cudaMemsetAsync(k.flags, 0, sizeof(int) * nchunks, stream) != cudaSuccess) return RL_ERR_CUDA;
+    for (int64_t c0 = 0, ci = 0; c0 < N; c0 += chunk, ++ci) {
+        const int64_t n = N - c0 < chunk ? N - c0 : chunk;
         const uint16_t* Xc = static_cast<const uint16_t*>(b->hidden) + c0 * H;
         {
             ProfScope ps(RL_PROF_REF_LOGIT, stream);

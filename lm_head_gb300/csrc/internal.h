@@ -132,7 +132,7 @@ int shard_stats_impl(const rl_head_batch* b, const rl_params* prm, float* stats,
 int loss_from_shards_impl(const rl_head_batch* b, const rl_params* prm, int32_t R, const float* stats_all,
                           const float* zlab, const float* zsup, const rl_head_outputs* out, void* saved, void* ws,
                           int32_t* status, cudaStream_t stream);
-int64_t bwd_chunk(int64_t N, const rl_params* prm);
+int64_t bwd_chunk(int64_t N, int64_t H, const rl_params* prm);
 // rl_params.keep_e in effect: a dense backward with BF16 gradients and no entropy term.
 bool keep_e_active(const rl_params* prm);
 // The kept numerators in the saved state, after the standard saved data: e [N, V] and
@@ -142,8 +142,8 @@ struct KeptView {
     uint16_t* Ebt;        // [V, ldt]: ldt = N rounded up to 128 (TMA strides are multiples of 16 bytes)
     int64_t ldt;
     float* cref;
-    int* flags;
-    int64_t chunk, nchunks;
+    int* flags;          // one per token chunk: room for the smallest chunk (one row tile)
+    int64_t chunks_max;
 };
 KeptView kept_view(void* saved, int64_t N, int64_t nnz, int64_t V, const rl_params* prm, size_t* bytes);
 // The forward with keep_e: per token chunk the reference logits, then the forward GEMM that
