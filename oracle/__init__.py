@@ -20,7 +20,9 @@ Readings where the pages are silent (R1..R20) are marked ``READING`` in the code
 
 Pinning status: every public function here is pinned by ``tests/test_oracle_*.py``
 against closed forms, worked examples from the pages, brute force or finite
-differences, except the items listed in ``PARITY_UNPINNED``.
+differences, except the items listed in ``PARITY_UNPINNED`` (parity unpinned: the value of
+the decoupled-TIS bound, reading R11, and the rollout-correction default bounds; the pages
+give neither number, and the functions themselves are pinned with explicit values).
 """
 from .rl_head import (HeadParams, LOSS_IPO, LOSS_ICEPOP, LOSS_REINFORCE, KL_EXACT, KL_K1,
                       STALE_NONE, STALE_INV_SQRT, head_forward, head_backward, head_loss_total,
