@@ -130,15 +130,6 @@ RL_DEVINL float dense_grad2(float alpha, float kappa, float ent, float z, float 
     const float pv = exp2_approx(__fmul_rn(x, kLog2e));
     return __fmul_rn(pv, fmaf(kappa, __fadd_rn(x, ent), alpha));
 }
-// What the bf16 operand(s) of the dense GEMMs drop from g: g - bf16(g), or with the hi/lo
-// split g - hi - lo.  Both differences are exact in fp32.
-RL_DEVINL float dense_residual(float g, bool split) {
-    const float hi = __bfloat162float(__float2bfloat16_rn(g));
-    float r = __fsub_rn(g, hi);
-    if (split) r = __fsub_rn(r, __bfloat162float(__float2bfloat16_rn(r)));
-    return r;
-}
-
 // G = alpha_t * exp(z - lse_t) for the tile, written as G [n, V] (row-major, ld V) and
 // G^T [V, ldt]; with `split`, also the bf16 remainder G - bf16(G) into G_lo / Gt_lo.
 struct EpiGrad {

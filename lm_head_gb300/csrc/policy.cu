@@ -291,23 +291,6 @@ RL_DEVINL void pg_block_reduce(const PgAcc& acc, float* sums, int* cnts) {
     __syncthreads();
 }
 
-RL_DEVINL void pg_write_metric(int k, double s, rl_pg_metrics* out) {
-    switch (k) {
-        case 0: out->loss_ppo = s; break;
-        case 1: out->loss_dec = s; break;
-        case 2: out->ppo_kl = s; break;
-        case 3: out->mis_kl = s; break;
-        case 4: out->k3 = s; break;
-        case 5: out->tis_sum = s; break;
-        case 6: out->n_valid = static_cast<int64_t>(s); break;
-        case 7: out->n_clip = static_cast<int64_t>(s); break;
-        case 8: out->n_clip_lower = static_cast<int64_t>(s); break;
-        case 9: out->icepop_low = static_cast<int64_t>(s); break;
-        case 10: out->icepop_high = static_cast<int64_t>(s); break;
-        case 11: out->n_tis_trunc = static_cast<int64_t>(s); break;
-        default: out->ipo_curve[k - 12] = static_cast<int64_t>(s); break;
-    }
-}
 
 // ----------------------------------------------------------------------------------
 // Batch totals

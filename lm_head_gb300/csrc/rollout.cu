@@ -92,19 +92,6 @@ RL_DEVINL FF warp_sum_ff(FF v) {
     }
     return v;
 }
-template <typename T, typename Op>
-RL_DEVINL T rc_block_reduce(T v, T* sh, Op op) {   // sh: one slot per warp
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
-    __syncthreads();
-    if (lane == 0) sh[warp] = v;
-    __syncthreads();
-    T r = sh[0];
-    for (int i = 1; i < nw; ++i) r = op(r, sh[i]);
-    return r;
-}
-
 // e^(hi + lo) for a float-float exponent: e^hi (float-float) times 1 + lo (|lo| tiny).
 RL_DEVINL FF exp_ff2(FF d) { return ff_mul(exp_ff(d.hi), two_sum(1.f, d.lo)); }
 
