@@ -317,11 +317,31 @@ __global__ void __launch_bounds__(kRcThreads, 6) rc_seq_kernel(RcArgs a) {
         return n;
     };
 
-    // pass 1: the sequence's sums
+    // pass 1: the sequence's sums.  Two accumulator sets per thread (tokens i and
+    // i + 128 of each step), added in that order at the end: two independent float-float
+    // chains in flight instead of one.
     int n = 0, cat = 0;
     FF S = {0.f, 0.f}, E = {0.f, 0.f};   // the decisions' sums, float-float
+    FF S2 = {0.f, 0.f}, E2 = {0.f, 0.f};
     float st = 0.f, sr = 0.f;            // metric sums: fp32 per thread
     float mis = 0.f, k3 = 0.f, ad = 0.f, c2 = 0.f;
+    auto take = [&](int i, FF& Sx, FF& Ex) {
+        if (s_m[mo + i] == 0) return;
+        const float x = s_lt[fo + i], y = s_lr[fo + i];
+        const FF d = two_sum(x, -y);
+        ++n;
+        Sx = ff_add(Sx, d);
+        st += x;
+        sr += y;
+        if (rs_seq) Ex = ff_add(Ex, exp_ff2(d));
+        if (q.veto) cat += ff_lt(d, q.lnVeto) ? 1 : 0;
+        const float df = d.hi;
+        const float ed = expf(df);
+        mis -= df;
+        k3 += ed - df - 1.f;
+        ad += fabsf(df);
+        c2 += ed * ed;
+    };
     int staged = whole ? 0 : -1;
     for (int c = 0; c < nchunks; ++c) {
         int cn;
@@ -333,24 +353,13 @@ __global__ void __launch_bounds__(kRcThreads, 6) rc_seq_kernel(RcArgs a) {
             staged = c;
         }
 #pragma unroll 1
-        for (int i = threadIdx.x; i < cn; i += kRcThreads) {
-            if (s_m[mo + i] == 0) continue;
-            const float x = s_lt[fo + i], y = s_lr[fo + i];
-            const FF d = two_sum(x, -y);
-            ++n;
-            S = ff_add(S, d);
-            st += x;
-            sr += y;
-            if (rs_seq) E = ff_add(E, exp_ff2(d));
-            if (q.veto) cat += ff_lt(d, q.lnVeto) ? 1 : 0;
-            const float df = d.hi;
-            const float ed = expf(df);
-            mis -= df;
-            k3 += ed - df - 1.f;
-            ad += fabsf(df);
-            c2 += ed * ed;
+        for (int i = threadIdx.x; i < cn; i += 2 * kRcThreads) {
+            take(i, S, E);
+            if (i + kRcThreads < cn) take(i + kRcThreads, S2, E2);
         }
     }
+    S = ff_add(S, S2);
+    E = ff_add(E, E2);
     {
         const FF w4[4] = {warp_sum_ff(S), rs_seq ? warp_sum_ff(E) : FF{0.f, 0.f}, {warp_sum_f(st), 0.f},
                           {warp_sum_f(sr), 0.f}};
@@ -538,6 +547,8 @@ __global__ void __launch_bounds__(kRcThreads, 6) rc_seq_kernel(RcArgs a) {
         role = old == static_cast<unsigned int>(gsize - 1);
     }
     __syncthreads();
+    // the scaling kernel may be scheduled from here on (it waits for this grid to end)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (!role) return;
     // the group's last block: its records into group record g
     __shared__ double dsum[kRcD];
@@ -610,6 +621,9 @@ __global__ void rc_empty_kernel(RcArgs a) {
 // flight per thread) and scalars at the two ends.
 constexpr int kRcScaleThreads = 256;
 __global__ void __launch_bounds__(kRcScaleThreads) rc_scale_kernel(RcArgs a) {
+    // launched as a programmatic dependent of the sequence kernel: it may be resident
+    // before that kernel ends, and waits here (in hardware) until it has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float f = *a.factor;
     float* w = a.w;
     const int64_t T = a.T;
@@ -776,7 +790,16 @@ int rollout_impl(const float* lt, const float* lr, const uint8_t* mask, const in
     if (q.use_tis && q.norm && w != nullptr && T > 0) {
         const int64_t blocks = (T / 4 + kRcScaleThreads - 1) / kRcScaleThreads + 1;
         const int64_t cap = 4L * num_sms();
-        rc_scale_kernel<<<static_cast<unsigned>(blocks < cap ? blocks : cap), kRcScaleThreads, 0, stream>>>(a);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(blocks < cap ? blocks : cap), 1, 1);
+        cfg.blockDim = dim3(kRcScaleThreads, 1, 1);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = B > 0 ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, rc_scale_kernel, a) != cudaSuccess) return RL_ERR_CUDA;
         ++launches;
     }
     count_launch(launches);
