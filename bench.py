@@ -318,7 +318,8 @@ def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb:
     the metrics and the factor, then the scaling kernel).  Algorithmic bytes per slot: two
     fp32 inputs and the mask read, the fp32 weight and the keep byte written (14 B), plus
     the weight read and written again by the normalisation (8 B): the factor needs every
-    token first."""
+    token first.  Beside it: a device copy of the same bytes timed the same way, and the
+    same call on the batch tiled eight times (7032 sequences, 14.4M tokens)."""
     import numpy as np
     import workloads
     c = workloads.make_policy_case()
@@ -361,12 +362,39 @@ def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb:
     gbs = nbytes / (ms / 1e3) / 1e9
     peak = float(peaks["hbm_gbs"])
     n_valid = int(c.mask.sum())
+    copy_ms = _copy_floor(torch, dev, nbytes, len(sets), passes)
+    # the same call on the batch tiled eight times (8 x 879 sequences, 14.4M tokens): more
+    # sequences than resident blocks, so the block scheduler balances the SMs as it goes
+    big_arrays = [np.tile(x, 8) for x in arrays]
+    Tb = int(big_arrays[0].shape[0])
+    off_b = np.concatenate([off_h[:-1] + k * T for k in range(8)] + [np.array([8 * T], np.int64)]).astype(np.int64)
+    offb = torch.from_numpy(off_b).to(dev)
+    bsets = _rotating_sets(torch, dev, big_arrays, 2 * 129 * 2 ** 20 + 1)
+    bouts = (torch.empty(Tb, dtype=torch.float32, device=dev), torch.empty(Tb, dtype=torch.uint8, device=dev))
+    bws = torch.zeros(rh.rl_rollout_correction_workspace_bytes(8 * B), dtype=torch.uint8, device=dev)
+    bcalls = [(lambda ins=ins: rh.rl_rollout_correction(*ins, offb, rp, outputs=bouts, ws=bws, metrics_dev=met))
+              for ins in bsets]
+    for c_ in bcalls:
+        c_()
+    torch.cuda.synchronize()
+    bpasses = 10 * len(bcalls)
+    bms = _time_back_to_back(torch, bcalls, bpasses)
+    bbytes = 8 * nbytes
+    bcopy_ms = _copy_floor(torch, dev, bbytes, len(bsets), bpasses)
+    del bsets, bouts, bcalls, bws
+    torch.cuda.empty_cache()
     layout = (f"{B} sequences packed end to end (T={T} tokens, mask all 1)" if packed else
               f"{B} padded rows of {c.max_len} (T={T} slots, {n_valid} response tokens)")
     return {"workload": f"c5 as {layout}; sequence-level TIS clip [0.1, 10] + batch normalisation, geometric RS "
                         "[0.9, 1.1], veto 1e-4, mismatch metrics",
             "us_per_call_back_to_back": ms * 1e3, "kernel_us_single_launch": kms * 1e3,
             "tokens_per_s": n_valid / (ms / 1e3), "passes": passes, "input_sets": len(sets),
+            "device_copy_same_bytes": {"us_per_call_back_to_back": copy_ms * 1e3, "call_over_copy": ms / copy_ms,
+                                       "frac_of_hbm_peak": nbytes / (copy_ms / 1e3) / 1e9 / peak},
+            "tiled_x8": {"sequences": 8 * B, "tokens": Tb, "bytes_per_call": bbytes, "us_per_call_back_to_back": bms * 1e3,
+                         "frac_of_hbm_peak": bbytes / (bms / 1e3) / 1e9 / peak,
+                         "device_copy_same_bytes_us": bcopy_ms * 1e3,
+                         "copy_frac_of_hbm_peak": bbytes / (bcopy_ms / 1e3) / 1e9 / peak},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                          "traffic": None, "algorithmic_bytes_per_pass": nbytes,
                          "duration": "average per call, back to back in a CUDA graph (the sequence kernel, then the scaling kernel)",
