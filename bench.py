@@ -201,20 +201,23 @@ def _time_back_to_back(torch, calls, passes):
 
 
 def _copy_floor(torch, dev, nbytes: int, n_sets: int, passes: int) -> float:
-    """Average time per call (ms) of a plain device-to-device copy that moves nbytes (half
-    read, half written), timed as the pass it stands beside: back to back in a CUDA graph
-    over n_sets rotating sources.  At a few tens of MB a kernel's start and drain are a
-    large part of its time, so this is the floor a pass of that size meets, next to the
-    peak measured on GB-sized copies."""
+    """Average time per call (ms) of a plain streaming kernel that moves nbytes (half read,
+    half written: dst = src * 1 in fp32, torch's vectorised elementwise kernel on the SMs,
+    not the driver's memcpy, whose path changes with the size), timed as the pass it
+    stands beside: back to back in a CUDA graph over n_sets rotating sources and as many
+    destinations (a destination written again on the next pass would take its writes in
+    L2).  At a few tens of MB a kernel's start and drain are a large part of its time, so
+    this is the floor a pass of that size meets, next to the peak measured on GB-sized
+    copies."""
     half = (nbytes // 2 + 15) // 16 * 4
     srcs = [torch.ones(half, dtype=torch.float32, device=dev) for _ in range(n_sets)]
-    dst = torch.empty(half, dtype=torch.float32, device=dev)
-    calls = [(lambda a=a: dst.copy_(a)) for a in srcs]
+    dsts = [torch.empty(half, dtype=torch.float32, device=dev) for _ in range(n_sets)]
+    calls = [(lambda a=a, d=d: torch.mul(a, 1.0, out=d)) for a, d in zip(srcs, dsts)]
     for c in calls:
         c()
     torch.cuda.synchronize()
     ms = _time_back_to_back(torch, calls, passes)
-    del srcs, dst
+    del srcs, dsts
     return ms
 
 
@@ -243,11 +246,12 @@ def elementwise_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush
     T = int(arrays[0].shape[0])
     pp = rh.PgParams()
     sets = _rotating_sets(torch, dev, arrays, 2 * 129 * 2 ** 20 + 1)
-    outs = tuple(torch.empty(T, dtype=torch.float32, device=dev) for _ in range(4))
+    # outputs rotate with the inputs: a pass never writes lines the previous passes left in L2
+    out_sets = [tuple(torch.empty(T, dtype=torch.float32, device=dev) for _ in range(4)) for _ in sets]
     met = torch.zeros(rh.ctypes.sizeof(rh.RlPgMetrics), dtype=torch.uint8, device=dev)
     ws = torch.zeros(rh.rl_policy_workspace_bytes(T), dtype=torch.uint8, device=dev)   # zeroed once
-    calls = [(lambda ins=ins: rh.rl_policy_loss_elementwise(*ins, pp, outputs=outs, ws=ws, metrics_dev=met))
-             for ins in sets]
+    calls = [(lambda ins=ins, outs=outs: rh.rl_policy_loss_elementwise(*ins, pp, outputs=outs, ws=ws, metrics_dev=met))
+             for ins, outs in zip(sets, out_sets)]
     for i in range(max(warmup, 3)):
         calls[i % len(calls)]()
     torch.cuda.synchronize()
@@ -274,9 +278,9 @@ def elementwise_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush
     big_arrays = [None if x is None else np.tile(x, 8) for x in arrays]
     Tb = int(big_arrays[0].shape[0])
     bsets = _rotating_sets(torch, dev, big_arrays, 2 * 129 * 2 ** 20 + 1)
-    bouts = tuple(torch.empty(Tb, dtype=torch.float32, device=dev) for _ in range(4))
-    bcalls = [(lambda ins=ins: rh.rl_policy_loss_elementwise(*ins, pp, outputs=bouts, ws=ws, metrics_dev=met))
-              for ins in bsets]
+    bout_sets = [tuple(torch.empty(Tb, dtype=torch.float32, device=dev) for _ in range(4)) for _ in bsets]
+    bcalls = [(lambda ins=ins, outs=outs: rh.rl_policy_loss_elementwise(*ins, pp, outputs=outs, ws=ws, metrics_dev=met))
+              for ins, outs in zip(bsets, bout_sets)]
     for c_ in bcalls:
         c_()
     torch.cuda.synchronize()
@@ -284,7 +288,7 @@ def elementwise_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush
     bms = _time_back_to_back(torch, bcalls, bpasses)
     bbytes = 8 * nbytes
     bcopy_ms = _copy_floor(torch, dev, bbytes, len(bsets), bpasses)
-    del bsets, bouts, bcalls
+    del bsets, bout_sets, bcalls
     torch.cuda.empty_cache()
     peak = float(peaks["hbm_gbs"])
     layout = (f"packed: {n_valid} valid tokens end to end, no mask" if packed else
@@ -305,7 +309,7 @@ def elementwise_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush
                          "duration": "average per call, back to back in a CUDA graph (one kernel launch per call)",
                          "peak_kind": f"hbm_gbs ({peaks['source']})"},
             "l2": f"{len(sets)} rotating input sets of {sum(a.nbytes for a in arrays if a is not None) >> 20} MB "
-                  "(more than 2x L2 per round)"}
+                  "(more than 2x L2 per round), each with its own output buffers"}
 
 
 def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb: int = 4096, packed: bool = True):
@@ -337,11 +341,12 @@ def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb:
                      tis_batch_normalize=True, use_rs=True, rs_level="geometric", rs_lower_bound=0.9,
                      rs_upper_bound=1.1, rs_veto_threshold=1e-4)
     sets = _rotating_sets(torch, dev, arrays, 2 * 129 * 2 ** 20 + 1)
-    outs = (torch.empty(T, dtype=torch.float32, device=dev), torch.empty(T, dtype=torch.uint8, device=dev))
+    out_sets = [(torch.empty(T, dtype=torch.float32, device=dev), torch.empty(T, dtype=torch.uint8, device=dev))
+                for _ in sets]   # rotating with the inputs
     met = torch.zeros(rh.ctypes.sizeof(rh.RlRcMetrics), dtype=torch.uint8, device=dev)
     ws = torch.zeros(rh.rl_rollout_correction_workspace_bytes(B), dtype=torch.uint8, device=dev)   # zeroed once
-    calls = [(lambda ins=ins: rh.rl_rollout_correction(*ins, off, rp, outputs=outs, ws=ws, metrics_dev=met))
-             for ins in sets]
+    calls = [(lambda ins=ins, outs=outs: rh.rl_rollout_correction(*ins, off, rp, outputs=outs, ws=ws, metrics_dev=met))
+             for ins, outs in zip(sets, out_sets)]
     for i in range(max(warmup, 3)):
         calls[i % len(calls)]()
     torch.cuda.synchronize()
@@ -370,10 +375,11 @@ def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb:
     off_b = np.concatenate([off_h[:-1] + k * T for k in range(8)] + [np.array([8 * T], np.int64)]).astype(np.int64)
     offb = torch.from_numpy(off_b).to(dev)
     bsets = _rotating_sets(torch, dev, big_arrays, 2 * 129 * 2 ** 20 + 1)
-    bouts = (torch.empty(Tb, dtype=torch.float32, device=dev), torch.empty(Tb, dtype=torch.uint8, device=dev))
+    bout_sets = [(torch.empty(Tb, dtype=torch.float32, device=dev), torch.empty(Tb, dtype=torch.uint8, device=dev))
+                 for _ in bsets]
     bws = torch.zeros(rh.rl_rollout_correction_workspace_bytes(8 * B), dtype=torch.uint8, device=dev)
-    bcalls = [(lambda ins=ins: rh.rl_rollout_correction(*ins, offb, rp, outputs=bouts, ws=bws, metrics_dev=met))
-              for ins in bsets]
+    bcalls = [(lambda ins=ins, outs=outs: rh.rl_rollout_correction(*ins, offb, rp, outputs=outs, ws=bws, metrics_dev=met))
+              for ins, outs in zip(bsets, bout_sets)]
     for c_ in bcalls:
         c_()
     torch.cuda.synchronize()
@@ -381,7 +387,7 @@ def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb:
     bms = _time_back_to_back(torch, bcalls, bpasses)
     bbytes = 8 * nbytes
     bcopy_ms = _copy_floor(torch, dev, bbytes, len(bsets), bpasses)
-    del bsets, bouts, bcalls, bws
+    del bsets, bout_sets, bcalls, bws
     torch.cuda.empty_cache()
     layout = (f"{B} sequences packed end to end (T={T} tokens, mask all 1)" if packed else
               f"{B} padded rows of {c.max_len} (T={T} slots, {n_valid} response tokens)")
@@ -399,7 +405,7 @@ def rollout_side(rh, torch, dev, steps: int, warmup: int, peaks: dict, flush_mb:
                          "traffic": None, "algorithmic_bytes_per_pass": nbytes,
                          "duration": "average per call, back to back in a CUDA graph (the sequence kernel, then the scaling kernel)",
                          "peak_kind": f"hbm_gbs ({peaks['source']})"},
-            "l2": f"{len(sets)} rotating input sets (more than 2x L2 per round)"}
+            "l2": f"{len(sets)} rotating input sets (more than 2x L2 per round), each with its own output buffers"}
 
 
 def time_head_config(rh, torch, dev, case, hp, steps: int, warmup: int, peaks: dict, what: str) -> dict:
