@@ -303,6 +303,15 @@ RL_DEVINL long long pg_fix(const PgArgs& a, float v) {
     return 0;
 }
 
+// The same value as pg_fix, through a 32-bit conversion whenever v 2^24 fits in an int32
+// (then |v| < 128, inside the range bound for any T < 2^31, and both conversions round to
+// nearest even): the 64-bit conversion is a slow instruction and most terms never need it.
+RL_DEVINL long long pg_fix_fast(const PgArgs& a, float v) {
+    const float x = v * kPgFix;
+    if (fabsf(x) < 2147483648.f) return static_cast<long long>(__float2int_rn(x));
+    return pg_fix(a, v);
+}
+
 // A block's partial goes into the batch accumulators with integer atomics (sums in 2^-24
 // fixed point, counts as they are): integer addition does not depend on the order the
 // blocks arrive in, so the totals are reproducible.
@@ -856,34 +865,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
     const int nst = static_cast<int>((ntok + kPkStage - 1) / kPkStage);
     const bool consumer = threadIdx.x < kPgThreads;
     const int lane = threadIdx.x & 31;
-    if (threadIdx.x == kPgThreads) {
-        for (int s = 0; s < kPkDepth; ++s) {
-            mbar_init(full + s, 1);
-            mbar_init(empty + s, kPgThreads / 32);
-        }
-        fence_mbar_init();
-    }
-    if (threadIdx.x == 0) {
-        abort_flag = 0;
-        blk_status = 0;
-    }
-    if (consumer) {
-        for (int b = 0; b <= q.n; ++b) hist_s[b * kPgThreads + threadIdx.x] = 0;
-        if (threadIdx.x <= RL_PG_MAX_CURVE) {
-            s_eps[threadIdx.x] = q.eps_s[threadIdx.x];
-            s_weps[threadIdx.x] = q.weps_s[threadIdx.x];
-        }
-        for (int i = threadIdx.x; i < kPkLut; i += kPgThreads) lut[i] = q.lut[i];
-    }
-    __syncthreads();
-
-    PkAcc acc;
-#pragma unroll
-    for (int k = 0; k < kPgSums; ++k) acc.fx[k] = 0;
-#pragma unroll
-    for (int k = 0; k < 6; ++k) acc.cnt[k] = 0;
     volatile int* vflag = &abort_flag;
-
     // The producer lane fills the ring: entry i goes to slot i mod kPkDepth, stage
     // blockIdx + i nb for the first kPkDepth entries, then claimed ones (the claim's round
     // trip overlaps the wait for the slot).  Returns false once it has placed the end mark
@@ -917,10 +899,39 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
         issued = i + 1;
         return true;
     };
+    int pi = 0;
+    if (threadIdx.x == kPgThreads) {
+        for (int s = 0; s < kPkDepth; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, kPgThreads / 32);
+        }
+        fence_mbar_init();
+        abort_flag = 0;
+        blk_status = 0;
+        // the first ring entries at once: their copies overlap the block's table setup
+        while (pi < kPkDepth && fill(pi)) ++pi;
+    }
+    if (consumer) {
+        for (int b = 0; b <= q.n; ++b) hist_s[b * kPgThreads + threadIdx.x] = 0;
+        if (threadIdx.x <= RL_PG_MAX_CURVE) {
+            s_eps[threadIdx.x] = q.eps_s[threadIdx.x];
+            s_weps[threadIdx.x] = q.weps_s[threadIdx.x];
+        }
+        for (int i = threadIdx.x; i < kPkLut; i += kPgThreads) lut[i] = q.lut[i];
+    }
+    __syncthreads();
+
+    PkAcc acc;
+#pragma unroll
+    for (int k = 0; k < kPgSums; ++k) acc.fx[k] = 0;
+#pragma unroll
+    for (int k = 0; k < 6; ++k) acc.cnt[k] = 0;
+
     if (!consumer) {
         if (lane == 0) {
-            int pi = 0;
-            while (fill(pi)) ++pi;
+            // after the first entries (pi < kPkDepth here only if the stages ran out)
+            if (pi == kPkDepth)
+                while (fill(pi)) ++pi;
             if (*vflag) {
                 // the last stages issued may still be in flight: wait for them (bounded by
                 // the fixed kWaitLimitNs) before the block's shared memory goes away
@@ -978,7 +989,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
                     }
                 }
 #pragma unroll
-                for (int k = 0; k < kPgSums; ++k) acc.fx[k] += pg_fix(a, sum4[k]);
+                for (int k = 0; k < kPgSums; ++k) acc.fx[k] += pg_fix_fast(a, sum4[k]);
                 acc.cnt[0] += 4;
                 if (a.loss_ppo) __stcs(reinterpret_cast<float4*>(a.loss_ppo + g + j4), make_float4(lp[0], lp[1], lp[2], lp[3]));
                 if (a.loss_dec) __stcs(reinterpret_cast<float4*>(a.loss_dec + g + j4), make_float4(ld[0], ld[1], ld[2], ld[3]));
