@@ -737,20 +737,27 @@ struct alignas(16) PkStage {
 constexpr int kPkSmem = kPkDepth * static_cast<int>(sizeof(PkStage));
 static_assert(kPkSmem >= (kPgSums * 8 + 6 * 4) * kPgThreads, "the ring holds the block's values at the end");
 
-// Curve bin of one |p_old - p_samp| value from the bucket table (in shared memory), and
-// whether it lies in the band of a curve eps (or its bucket needs the exact path: two eps
-// inside it, or an eps whose band reaches into it).  Branch-free.
-RL_DEVINL void pk_curve(float adiff, const int* lut, const float* eps_s, const float* weps_s, int& j, bool& band) {
+// One bucket of |p_old - p_samp| in shared memory: its code (eps below it | the eps inside
+// it << 8 | needs the exact path << 16) with that eps and its band half-width beside it,
+// so a token reads its bucket with one 16-byte load.
+struct __align__(16) PkBucket {
+    int code;
+    float eps, weps;
+    int pad;
+};
+
+// Curve bin of one |p_old - p_samp| value from the bucket table, and whether it lies in
+// the band of a curve eps (or its bucket needs the exact path: two eps inside it, or an
+// eps whose band reaches into it).  Branch-free.
+RL_DEVINL void pk_curve(float adiff, const PkBucket* lut, int& j, bool& band) {
     int b = static_cast<int>(adiff * static_cast<float>(kPkLut));   // exact scaling: bucket edges are exact
     b = b < 0 ? 0 : (b > kPkLut - 1 ? kPkLut - 1 : b);
-    const int e = lut[b];
-    const int kin = (e >> 8) & 31;
-    j = (e & 31) + (adiff > eps_s[kin] ? 1 : 0);
-    band = band | (fabsf(adiff - eps_s[kin]) <= weps_s[kin]) | ((e >> 16) != 0);
+    const PkBucket e = lut[b];
+    j = (e.code & 31) + (adiff > e.eps ? 1 : 0);
+    band = band | (fabsf(adiff - e.eps) <= e.weps) | ((e.code >> 16) != 0);
 }
 
-RL_DEVINL PgTok pg_fast_packed(float lt, float lo, float ls, float A, const PgPrep& q, const int* lut,
-                               const float* eps_s, const float* weps_s) {
+RL_DEVINL PgTok pg_fast_packed(float lt, float lo, float ls, float A, const PgPrep& q, const PkBucket* lut) {
     PgTok o;
     const float r = exp_fast(lt - lo);
     const float l1 = -A * r;
@@ -764,7 +771,7 @@ RL_DEVINL PgTok pg_fast_packed(float lt, float lo, float ls, float A, const PgPr
                 ((A > 0.f) & (fabsf(r - q.hi_b) <= q.w_hi_b)) | (fabsf(rho_raw - q.tis) <= q.w_tis) |
                 (fabsf(rho_raw - q.ice_lo) <= q.w_ice_lo) | (fabsf(rho_raw - q.ice_hi) <= q.w_ice_hi);
     int j;
-    pk_curve(adiff, lut, eps_s, weps_s, j, band);
+    pk_curve(adiff, lut, j, band);
     const bool dual = (A < 0.f) & (r > q.cc);   // on the ratio, as in pg_token
     const bool clip = ((A > 0.f) & (r > q.hi_b)) | ((A < 0.f) & (r < q.lo_b));
     const float loss_ppo = dual ? l3 : lc;
@@ -854,8 +861,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
     __shared__ __align__(8) uint64_t empty[kPkDepth];
     __shared__ int stage_of[kPkDepth];             // the stage in each ring slot, -1: no more
     __shared__ int hist_s[kPgBins * kPgThreads];   // bin-major: thread t's bin b at b * 256 + t
-    __shared__ int lut[kPkLut];
-    __shared__ float s_eps[RL_PG_MAX_CURVE + 1], s_weps[RL_PG_MAX_CURVE + 1];
+    __shared__ PkBucket lut[kPkLut];
     __shared__ int abort_flag;
     __shared__ int32_t blk_status;
 
@@ -913,11 +919,11 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
     }
     if (consumer) {
         for (int b = 0; b <= q.n; ++b) hist_s[b * kPgThreads + threadIdx.x] = 0;
-        if (threadIdx.x <= RL_PG_MAX_CURVE) {
-            s_eps[threadIdx.x] = q.eps_s[threadIdx.x];
-            s_weps[threadIdx.x] = q.weps_s[threadIdx.x];
+        for (int i = threadIdx.x; i < kPkLut; i += kPgThreads) {
+            const int e = q.lut[i];
+            const int kin = (e >> 8) & 31;
+            lut[i] = PkBucket{e, q.eps_s[kin], q.weps_s[kin], 0};
         }
-        for (int i = threadIdx.x; i < kPkLut; i += kPgThreads) lut[i] = q.lut[i];
     }
     __syncthreads();
 
@@ -966,8 +972,8 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
                 for (int k = 0; k < kPgSums; ++k) sum4[k] = 0.f;
 #pragma unroll
                 for (int u = 0; u < 4; u += 2) {   // two tokens at a time: two independent chains, no branch
-                    PgTok t[2] = {pg_fast_packed(vt[u], vo[u], vs[u], vA[u], q, lut, s_eps, s_weps),
-                                  pg_fast_packed(vt[u + 1], vo[u + 1], vs[u + 1], vA[u + 1], q, lut, s_eps, s_weps)};
+                    PgTok t[2] = {pg_fast_packed(vt[u], vo[u], vs[u], vA[u], q, lut),
+                                  pg_fast_packed(vt[u + 1], vo[u + 1], vs[u + 1], vA[u + 1], q, lut)};
                     if (t[0].band | t[1].band) {   // rare: re-decide exactly
                         if (t[0].band) pg_resolve(t[0], vt[u], vo[u], vs[u], vA[u], q);
                         if (t[1].band) pg_resolve(t[1], vt[u + 1], vo[u + 1], vs[u + 1], vA[u + 1], q);
@@ -985,7 +991,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
                         acc.cnt[3] += t[h].ice_lo;
                         acc.cnt[4] += t[h].ice_hi;
                         acc.cnt[5] += t[h].tis;
-                        hist[t[h].j * kPgThreads] += 1;
+                        atomicAdd(hist + t[h].j * kPgThreads, 1);   // the thread's own column: no contention
                     }
                 }
 #pragma unroll
@@ -1005,7 +1011,7 @@ __global__ void __launch_bounds__(kPgThreads + 32, kPgFastPerSm) policy_packed_k
             if (t < a.T) {
                 float lp, ld, gp, gd;
                 const float xt = a.lt[t], xo = a.lo[t], xs = a.ls[t], xa = a.adv[t];
-                PgTok tk = pg_fast_packed(xt, xo, xs, xa, q, lut, s_eps, s_weps);
+                PgTok tk = pg_fast_packed(xt, xo, xs, xa, q, lut);
                 if (tk.band) pg_resolve(tk, xt, xo, xs, xa, q);
                 PgFastAcc one;
 #pragma unroll
